@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Benchmark of the CQ hot path on GB300.
+
+One JSON line on rank 0. The headline step is the Needle-shaped decode step
+(batch 1): 27 layers x {Q 512x512, K 256x512, V 256x512, gate 512x512,
+O 512x512} in CQ2 plus the 8192x512 CQ4 head -- 136 matrices, 9,682,944
+packed bytes -- run as ONE grouped GEMV launch over int8 per-token
+activations. ``value`` is the effective GEMV bandwidth on packed bytes
+(GB/s). The same run also times, each under its own events:
+  * the grouped GEMM (prefill) over the same matrix set at M=2048 (TFLOP/s),
+  * the encoder on 16 fp32 matrices of 8192x8192 with 1% outliers (GB/s).
+
+L2: every config's weights fit in the 126 MB L2, so the decode step cycles
+through R copies of the weight set whose footprint is >= 4x L2; each step
+reads a copy that was evicted long ago.
+
+``--impl reference`` times the oracle (plain C, fp64, single thread) on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CQ2 GEMV effective GB/s and % HBM roofline; CQ GEMM TOPS at M=2048"
+WORKLOAD = ("Needle-shaped decode step, batch 1: 27 x {Q 512x512, K 256x512, V 256x512, gate 512x512, "
+            "O 512x512} CQ2 + head 8192x512 CQ4, int8 per-token activations")
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the grouped GEMV
+# from an ncu capture, keyed by the sha256 of the kernel source it was taken
+# on; reported only while the source is unchanged.
+NCU_TRAFFIC = {}
+
+
+def _src_hash(name: str) -> str:
+    p = os.path.join(ROOT, "hadamard_rotated_codebook_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.cmd = ["nvidia-smi", f"--id={gpu_id}", "--query-gpu=" + ",".join(self.FIELDS),
+                    "--format=csv,noheader,nounits", f"-lms={period_ms}"]
+        self.rows, self.proc, self.th = [], None, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+        time.sleep(0.3)  # let the first sample land before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.th:
+            self.th.join(timeout=5)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                smax.append(float(r[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads
+
+def decode_workload(C, S, device, copies_min_bytes):
+    import torch
+    mats = S.decode_step_mats()
+    cbs = {b: C.cq_codebook_init(b) for b in (2, 4)}
+    sizes = [C.cq_packed_bytes(m.out, m.n_in, 128, m.bits) for m in mats]
+    offs, tot = [], 0
+    for sz in sizes:
+        offs.append(tot)
+        tot += (sz + 255) // 256 * 256
+    base = torch.empty(tot, dtype=torch.uint8, device=device)
+    for m, o, sz in zip(mats, offs, sizes):
+        W = S.decode_weights(m, device=device)
+        C.cq_encode(W, m.bits, cbs[m.bits], blob=base[o:o + sz])
+    packed = sum(sizes)
+    R = max(2, math.ceil(copies_min_bytes / packed))
+    copies = [base] + [base.clone() for _ in range(R - 1)]
+    nact = S.n_activations(mats)
+    X = torch.cat([S.decode_activation(a, device=device) for a in range(nact)])  # [55, 512]
+    Xq, xs = C.cq_act_quant_int8(X)
+    out_total = sum(m.out for m in mats)
+    ybuf = torch.empty(out_total, dtype=torch.float32, device=device)
+    yoffs, t = [], 0
+    for m in mats:
+        yoffs.append(t)
+        t += m.out
+    plans = []
+    for cp in copies:
+        items = []
+        for m, o, sz, yo in zip(mats, offs, sizes, yoffs):
+            items.append(dict(blob=cp[o:o + sz], out=m.out, **{"in": m.n_in}, bits=m.bits, codebook=cbs[m.bits],
+                              x=Xq[m.act:m.act + 1], x_scale=xs[m.act:m.act + 1],
+                              y=ybuf[yo:yo + m.out].view(1, m.out)))
+        plans.append(C.GemvPlan(items))
+    algo = packed + Xq.numel() + 4 * xs.numel() + 4 * out_total
+    return dict(mats=mats, plans=plans, R=R, packed=packed, algo_bytes=algo, Xq=Xq, xs=xs, ybuf=ybuf,
+                copies=copies, offs=offs, sizes=sizes, cbs=cbs, out_total=out_total)
+
+
+def time_graph(torch, steps_fn, K, chunk, stream):
+    """Captures `chunk` steps in a CUDA graph; returns (graph, replays)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        steps_fn(chunk)
+    return g
+
+
+def run_cq(args):
+    import torch
+    import torch.distributed as dist
+
+    import hadamard_rotated_codebook_gb300 as C
+    import synthetic as S
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    peaks, peak_kind = measured_peaks()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    wl = decode_workload(C, S, device, 4 * l2)
+    plans, R = wl["plans"], wl["R"]
+    K, Wm = args.steps, args.warmup
+    stream = torch.cuda.Stream(device)
+
+    # ---- warm-up: W untimed steps ----
+    with torch.cuda.stream(stream):
+        for i in range(Wm):
+            plans[i % R].run(stream)
+    stream.synchronize()
+
+    # ---- graph of `chunk` steps cycling through the copies ----
+    chunk = min(K, 4 * R * max(1, 1000 // (4 * R)))
+    while K % chunk:
+        chunk -= 1
+
+    def steps(n):
+        for i in range(n):
+            plans[i % R].run(stream)
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        steps(chunk)
+    g.replay()  # upload the graph (untimed)
+    stream.synchronize()
+
+    gpu_id = f"GPU-{props.uuid}" if hasattr(props, "uuid") else str(local)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(K // chunk):
+        g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks.stop()
+    C.cq_device_status(device)
+    ms = max_over_ranks(ev0.elapsed_time(ev1))
+    ms_step = ms / K
+    gbs = world * wl["packed"] * K / (ms * 1e-3) / 1e9
+    launches = K  # one grouped GEMV launch per step
+    achieved = wl["algo_bytes"] / (ms_step * 1e-3) / 1e9
+    roofline = {
+        "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
+        "traffic": NCU_TRAFFIC.get(_src_hash("cq_gemv.cu")),
+        "kernel": "gemv (grouped decode step)",
+        "algorithmic_bytes_per_launch": wl["algo_bytes"],
+    }
+
+    result = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": round(ms_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "matrices": len(wl["mats"]), "packed_bytes": wl["packed"],
+                   "batch": 1, "weight_copies": R, "l2": f"inputs larger than L2: {R} rotating weight copies "
+                   f"({R * wl['packed'] / 1e6:.0f} MB >= 4x L2 {l2 / 1e6:.0f} MB)",
+                   "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "pct_of_8tbs": round(100 * (wl["packed"] * K / (ms * 1e-3) / 1e9) / 8000.0, 2),
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+    }
+
+    # ---- end to end: host activations in, host outputs back, every step ----
+    xq_h = wl["Xq"].cpu().pin_memory()
+    xs_h = wl["xs"].cpu().pin_memory()
+    y_h = torch.empty(wl["out_total"], dtype=torch.float32).pin_memory()
+    Ke = min(K, 20000)
+    ce = min(chunk, Ke)
+    while Ke % ce:
+        ce -= 1
+
+    def e2e_steps(n):
+        for i in range(n):
+            wl["Xq"].copy_(xq_h, non_blocking=True)
+            wl["xs"].copy_(xs_h, non_blocking=True)
+            plans[i % R].run(stream)
+            y_h.copy_(wl["ybuf"], non_blocking=True)
+
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ge, stream=stream):
+        e2e_steps(ce)
+    ge.replay()
+    stream.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke // ce):
+        ge.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    mse = max_over_ranks(e0.elapsed_time(e1))
+    result["e2e"] = {"value": round(world * wl["packed"] * Ke / (mse * 1e-3) / 1e9, 1), "unit": "GB/s",
+                     "h2d_bytes_per_step": wl["Xq"].numel() + 4 * wl["xs"].numel(),
+                     "d2h_bytes_per_step": 4 * wl["out_total"], "steps": Ke,
+                     "ms_per_step": round(mse / Ke, 6)}
+
+    if not args.skip_extra:
+        result["gemm"] = bench_gemm(C, S, torch, wl, device, stream, peaks, peak_kind, barrier, max_over_ranks, world)
+        result["encode"] = bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        result["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def bench_gemm(C, S, torch, wl, device, stream, peaks, peak_kind, barrier, max_over_ranks, world, M=2048):
+    mats = wl["mats"]
+    nact = S.n_activations(mats)
+    acts = []
+    for a in range(nact):
+        X = S.decode_activation(a, tokens=M, device=device)
+        acts.append(C.cq_act_quant_int8(X))
+    items = []
+    for m, o, sz in zip(mats, wl["offs"], wl["sizes"]):
+        items.append(dict(blob=wl["copies"][0][o:o + sz], out=m.out, **{"in": m.n_in}, bits=m.bits,
+                          codebook=wl["cbs"][m.bits], Xq=acts[m.act][0], x_scale=acts[m.act][1],
+                          Y=torch.empty((M, m.out), dtype=torch.float32, device=device)))
+    flops = 2.0 * M * sum(m.out * m.n_in for m in mats)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            C.cq_gemm_grouped(items)
+    stream.synchronize()
+    Kg = 10
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(Kg):
+            C.cq_gemm_grouped(items)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1)) / Kg
+    C.cq_device_status(device)
+    tflops = flops / (ms * 1e-3) / 1e12
+    out_bytes = 4.0 * M * sum(m.out for m in mats)
+    return {"metric": "CQ GEMM TFLOP/s at M=2048 (Needle-shaped matrix set, int8 per-token activations)",
+            "value": round(world * tflops, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4), "steps": Kg,
+            "warmup": 3, "M": M, "flops_per_step": flops, "output_bytes_per_step": out_bytes,
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(tflops / peaks["bf16_tflops"], 4),
+                         "peak_source": peak_kind + " (bf16 dense; fp16 operands run at the same rate)",
+                         "traffic": None}}
+
+
+def bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world):
+    n = S.ENCODE_COUNT
+    Ws = [S.encode_matrix(i, device=device) for i in range(n)]
+    cb = C.cq_codebook_init(2)
+    nb = C.cq_packed_bytes(*S.ENCODE_SHAPE, 128, 2)
+    blobs = [torch.empty(nb, dtype=torch.uint8, device=device) for _ in range(n)]
+
+    def one_pass():
+        for W, b in zip(Ws, blobs):
+            C.cq_encode(W, 2, cb, blob=b)
+
+    with torch.cuda.stream(stream):
+        one_pass()
+    stream.synchronize()
+    Ke = 3
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(Ke):
+            one_pass()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1)) / Ke
+    elems = n * S.ENCODE_SHAPE[0] * S.ENCODE_SHAPE[1]
+    algo = elems * 4 + n * nb
+    gbs = algo / (ms * 1e-3) / 1e9
+    return {"metric": "CQ2 encode GB/s (16 fp32 8192x8192 with 1% outliers -> codes + fp16 norms)",
+            "value": round(world * gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 3), "steps": Ke,
+            "warmup": 1, "launches_per_step": n,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                         "algorithmic_bytes_per_launch": algo // n}}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def _oracle_step_sample(budget_s: float):
+    """Times the oracle's product (dequantise with the explicit Hadamard,
+    fp64 matmul) over decode-step matrices in order until `budget_s` is
+    spent; returns (packed bytes processed, seconds, matrices)."""
+    import numpy as np
+
+    import oracle as O
+    import synthetic as S
+    mats = S.decode_step_mats()
+    cbs = {b: O.analytic_codebook(b) for b in (2, 4)}
+    done_bytes, t_used, n = 0, 0.0, 0
+    for i, m in enumerate(mats):
+        ip = O.in_padded(m.n_in)
+        blob = S.random_blob(m.out * ip * O.width(m.bits) // 8, m.out * ip // 128, 9000 + i)
+        x = S.decode_activation(m.act).numpy()
+        q, s = O.act_quant_int8(x)
+        xt = q.astype(np.float64) * s.astype(np.float64)[:, None]
+        t0 = time.perf_counter()
+        What = O.dequant(blob, m.out, m.n_in, m.bits, cbs[m.bits])
+        O.matmul(What, xt)
+        t_used += time.perf_counter() - t0
+        done_bytes += blob.size
+        n += 1
+        if t_used >= budget_s:
+            break
+    return done_bytes, t_used, n
+
+
+def cpu_baseline(budget_s: float = 10.0):
+    b, t, n = _oracle_step_sample(budget_s)
+    return {"value": round(b / t / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"oracle dequantise + fp64 matmul over the first {n} decode-step matrices "
+                      f"({b} packed bytes) in {t:.1f} s, single thread"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    K, Wm = args.steps, args.warmup
+    per_step = max(0.05, min(2.0, 120.0 / max(1, min(K, 200) + Wm)))
+    K_run = min(K, 200)
+    for _ in range(min(Wm, 3)):
+        _oracle_step_sample(per_step / 4)
+    tot_b, tot_t = 0, 0.0
+    for _ in range(K_run):
+        b, t, _ = _oracle_step_sample(per_step)
+        tot_b += b
+        tot_t += t
+    v = tot_b / tot_t / 1e9
+    res = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s", "n_gpus": world,
+           "steps": K_run, "warmup": Wm, "ms_per_step": round(1e3 * tot_t / K_run, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "sample": f"about {per_step:.2f} s of oracle work per step"},
+           "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                            "sample": "decode-step matrices in order, oracle dequantise + fp64 matmul"},
+           "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=1000)
+    ap.add_argument("--impl", default="cq", choices=["cq", "reference"])
+    ap.add_argument("--skip-extra", action="store_true", help="decode step only")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cq(args)
+
+
+if __name__ == "__main__":
+    main()

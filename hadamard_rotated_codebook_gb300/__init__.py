@@ -1,0 +1,336 @@
+"""Cactus Quants (CQ) on GB300: Hadamard-rotated codebook encode, GEMV and
+GEMM over CQ-packed weights, and a .cact-shaped container.
+
+Thin binding over libcq's C ABI (include/cq.h): every function here only
+checks and marshals arguments (torch tensors for device memory and the
+current CUDA stream) and calls the entry point of the same name. All
+arithmetic of the hot path runs in the CUDA kernels of libcq.so; if the
+library is missing the import fails rather than falling back.
+
+Page citations use the page title and section:
+  "The .cact format" (cactuscompute.com blog), "The .cact archive and Cactus
+  Quants" (needle.js tutorial), OpenNeedle docs/reference.md.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Iterable, Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _capi
+from ._capi import (CQ_DTYPE_CQ, CQ_DTYPE_FP16, CQ_DTYPE_FP32, CQ_DTYPE_RAW, CQ_X_F32,
+                    CQ_X_I8, CQError, GemmDesc, GemvDesc, TensorDesc, check)
+
+GROUP = 128
+
+__all__ = [
+    "cq_levels", "cq_code_width", "cq_codebook_init", "cq_packed_bytes", "cq_encode",
+    "cq_act_quant_int8", "cq_gemv", "cq_gemv_grouped", "cq_gemm", "cq_gemm_grouped",
+    "cq_device_status", "cq_cact_write", "cq_cact_open", "cq_cact_open_memory", "CactReader",
+    "CQError", "library_path", "GROUP",
+]
+
+
+def _lib():
+    return _capi.load()
+
+
+def library_path() -> str:
+    return _capi.LIB_PATH
+
+
+def _stream(device: Optional[torch.device] = None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dev_ptr(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _codebook_arg(codebook, bits: int):
+    cb = np.ascontiguousarray(np.asarray(
+        codebook.detach().cpu() if isinstance(codebook, torch.Tensor) else codebook,
+        dtype=np.float32))
+    if cb.size != cq_levels(bits):
+        raise ValueError(f"codebook for bits={bits} needs {cq_levels(bits)} levels, got {cb.size}")
+    return cb, cb.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+# ------------------------------------------------------------------- host
+
+def cq_levels(bits: int) -> int:
+    return _lib().cq_levels(bits)
+
+
+def cq_code_width(bits: int) -> int:
+    return _lib().cq_code_width(bits)
+
+
+def cq_codebook_init(bits: int, group: int = GROUP) -> np.ndarray:
+    """Analytic Lloyd-Max codebook of N(0,1) divided by sqrt(group) (fp32);
+    ternary (bits=5) levels +-1.2240064/sqrt(group) and 0."""
+    n = ctypes.c_size_t(0)
+    check(_lib().cq_codebook_init(bits, group, None, 0, ctypes.byref(n)))
+    out = np.zeros(n.value, dtype=np.float32)
+    check(_lib().cq_codebook_init(bits, group, out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                  out.size, None))
+    return out
+
+
+def cq_packed_bytes(out: int, n_in: int, group: int, bits: int) -> int:
+    return int(_lib().cq_packed_bytes(out, n_in, group, bits))
+
+
+# ----------------------------------------------------------------- device
+
+def cq_encode(W: torch.Tensor, bits: int, codebook, group: int = GROUP,
+              blob: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Encodes fp32 W[out, in] (CUDA) into a CQ blob (uint8, CUDA)."""
+    if W.dim() != 2:
+        raise ValueError("W must be 2-D [out, in]")
+    out, n_in = W.shape
+    nbytes = cq_packed_bytes(out, n_in, group, bits)
+    if blob is None:
+        blob = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    elif blob.numel() != nbytes:
+        raise ValueError(f"blob must hold {nbytes} bytes")
+    _, cbp = _codebook_arg(codebook, bits)
+    check(_lib().cq_encode(_dev_ptr(W, torch.float32, "W"), out, n_in, group, bits, cbp,
+                           _dev_ptr(blob, torch.uint8, "blob"), _stream(W.device)))
+    return blob
+
+
+def cq_act_quant_int8(X: torch.Tensor, Xq: Optional[torch.Tensor] = None,
+                      s: Optional[torch.Tensor] = None):
+    """Per-token int8 quantisation of fp32 X[M, in]; returns (Xq int8, s fp32)."""
+    X2 = X if X.dim() == 2 else X.reshape(1, -1)
+    M, n_in = X2.shape
+    if Xq is None:
+        Xq = torch.empty((M, n_in), dtype=torch.int8, device=X.device)
+    if s is None:
+        s = torch.empty(M, dtype=torch.float32, device=X.device)
+    check(_lib().cq_act_quant_int8(_dev_ptr(X2, torch.float32, "X"), M, n_in,
+                                   _dev_ptr(Xq, torch.int8, "Xq"), _dev_ptr(s, torch.float32, "s"),
+                                   _stream(X.device)))
+    return Xq, s
+
+
+def _gemv_desc(blob, out, n_in, bits, codebook, x, x_scale, y, group, keep):
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    B = x2.shape[0]
+    if x2.shape[1] != n_in:
+        raise ValueError(f"x has {x2.shape[1]} columns, matrix has in={n_in}")
+    if x2.dtype == torch.float32:
+        xdt, xs = CQ_X_F32, None
+    elif x2.dtype == torch.int8:
+        xdt = CQ_X_I8
+        if x_scale is None:
+            raise ValueError("int8 activations need x_scale")
+        xs = _dev_ptr(x_scale, torch.float32, "x_scale")
+    else:
+        raise TypeError("x must be float32 or int8")
+    if y is None:
+        y = torch.empty((B, out), dtype=torch.float32, device=x.device)
+    cb, cbp = _codebook_arg(codebook, bits)
+    keep.append(cb)
+    d = GemvDesc(blob=_dev_ptr(blob, torch.uint8, "blob"), x=x2.data_ptr() if x2.is_cuda else None,
+                 x_scale=xs, y=_dev_ptr(y, torch.float32, "y"), codebook=cbp, out=out, in_=n_in,
+                 group=group, bits=bits, x_dtype=xdt, B=B)
+    if not x2.is_cuda or not x2.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    return d, y
+
+
+def cq_gemv(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook, x: torch.Tensor,
+            x_scale: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
+            group: int = GROUP) -> torch.Tensor:
+    """y[B, out] = W_hat x over one CQ blob; x fp32 [B, in] or int8 with
+    per-token scales x_scale[B]."""
+    keep = []
+    d, y = _gemv_desc(blob, out, n_in, bits, codebook, x, x_scale, y, group, keep)
+    check(_lib().cq_gemv_grouped(ctypes.byref(d), 1, _stream(x.device)))
+    return y
+
+
+def cq_gemv_grouped(items: Sequence[dict]) -> list:
+    """Runs many GEMVs in one launch. Each item is a dict with keys blob,
+    out, in, bits, codebook, x and optionally x_scale, y. Returns the ys."""
+    if not items:
+        return []
+    keep, ds, ys = [], [], []
+    for it in items:
+        d, y = _gemv_desc(it["blob"], it["out"], it["in"], it["bits"], it["codebook"], it["x"],
+                          it.get("x_scale"), it.get("y"), it.get("group", GROUP), keep)
+        ds.append(d)
+        ys.append(y)
+    arr = (GemvDesc * len(ds))(*ds)
+    check(_lib().cq_gemv_grouped(arr, len(ds), _stream(items[0]["x"].device)))
+    return ys
+
+
+class GemvPlan:
+    """Prebuilt descriptor array for repeated grouped GEMV calls on the same
+    buffers (the decode step): only the ctypes call remains per step."""
+
+    def __init__(self, items: Sequence[dict]):
+        self._keep, ds, self.ys = [], [], []
+        for it in items:
+            d, y = _gemv_desc(it["blob"], it["out"], it["in"], it["bits"], it["codebook"], it["x"],
+                              it.get("x_scale"), it.get("y"), it.get("group", GROUP), self._keep)
+            ds.append(d)
+            self.ys.append(y)
+        self._items = list(items)  # keep tensors alive
+        self._arr = (GemvDesc * len(ds))(*ds)
+        self._n = len(ds)
+        self._device = items[0]["x"].device
+
+    def run(self, stream: Optional[torch.cuda.Stream] = None):
+        st = ctypes.c_void_p((stream or torch.cuda.current_stream(self._device)).cuda_stream)
+        check(_lib().cq_gemv_grouped(self._arr, self._n, st))
+        return self.ys
+
+
+def _gemm_desc(blob, out, n_in, bits, codebook, Xq, x_scale, Y, group, keep):
+    if Xq.dim() != 2 or Xq.shape[1] != n_in:
+        raise ValueError("Xq must be [M, in]")
+    M = Xq.shape[0]
+    if Y is None:
+        Y = torch.empty((M, out), dtype=torch.float32, device=Xq.device)
+    cb, cbp = _codebook_arg(codebook, bits)
+    keep.append(cb)
+    d = GemmDesc(blob=_dev_ptr(blob, torch.uint8, "blob"), Xq=_dev_ptr(Xq, torch.int8, "Xq"),
+                 x_scale=_dev_ptr(x_scale, torch.float32, "x_scale"), Y=_dev_ptr(Y, torch.float32, "Y"),
+                 codebook=cbp, out=out, in_=n_in, group=group, bits=bits, M=M)
+    return d, Y
+
+
+def cq_gemm(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook, Xq: torch.Tensor,
+            x_scale: torch.Tensor, Y: Optional[torch.Tensor] = None, group: int = GROUP) -> torch.Tensor:
+    """Y[M, out] = s[m] * W_hat Xq[m] on the tensor cores (int8 per-token activations)."""
+    keep = []
+    d, Y = _gemm_desc(blob, out, n_in, bits, codebook, Xq, x_scale, Y, group, keep)
+    check(_lib().cq_gemm_grouped(ctypes.byref(d), 1, _stream(Xq.device)))
+    return Y
+
+
+def cq_gemm_grouped(items: Sequence[dict]) -> list:
+    """Items: dicts with blob, out, in, bits, codebook, Xq, x_scale and optionally Y."""
+    if not items:
+        return []
+    keep, ds, Ys = [], [], []
+    for it in items:
+        d, Y = _gemm_desc(it["blob"], it["out"], it["in"], it["bits"], it["codebook"], it["Xq"],
+                          it["x_scale"], it.get("Y"), it.get("group", GROUP), keep)
+        ds.append(d)
+        Ys.append(Y)
+    arr = (GemmDesc * len(ds))(*ds)
+    check(_lib().cq_gemm_grouped(arr, len(ds), _stream(items[0]["Xq"].device)))
+    return Ys
+
+
+def cq_device_status(device: Optional[torch.device] = None) -> int:
+    """Reads and clears the device status word of bounded waits (raises
+    CQError(CQ_ERR_TIMEOUT) if one gave up)."""
+    return check(_lib().cq_device_status(_stream(device)))
+
+
+# -------------------------------------------------------------- container
+
+@dataclass
+class CactTensor:
+    dtype: int
+    shape: tuple
+    nbytes: int
+    group: int
+    bits: int
+    data: bytes
+
+
+def _tensor_desc(t) -> tuple:
+    """Accepts a CactTensor or a dict(dtype, shape, data, group=0, bits=0)."""
+    if isinstance(t, dict):
+        t = CactTensor(dtype=t["dtype"], shape=tuple(t["shape"]), nbytes=len(t["data"]),
+                       group=t.get("group", 0), bits=t.get("bits", 0), data=bytes(t["data"]))
+    buf = ctypes.create_string_buffer(t.data, len(t.data))
+    shp = (ctypes.c_uint32 * 4)(*(list(t.shape) + [0] * (4 - len(t.shape))))
+    d = TensorDesc(dtype=t.dtype, ndim=len(t.shape), shape=shp, nbytes=len(t.data),
+                   group=t.group, bits=t.bits, data=ctypes.cast(buf, ctypes.c_void_p))
+    return d, buf
+
+
+def cq_cact_write(path: str, tensors: Iterable, codebook28, default_group: int = GROUP) -> None:
+    ds, bufs = [], []
+    for t in tensors:
+        d, b = _tensor_desc(t)
+        ds.append(d)
+        bufs.append(b)
+    arr = (TensorDesc * max(1, len(ds)))(*ds)
+    cb = np.ascontiguousarray(np.asarray(codebook28, dtype=np.float32))
+    if cb.size != 28:
+        raise ValueError("the container codebook has 28 floats (CQ2|CQ3|CQ4)")
+    check(_lib().cq_cact_write(path.encode(), arr, len(ds),
+                               cb.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), default_group))
+
+
+class CactReader:
+    """Validated view of a container; tensors are copied out as bytes."""
+
+    def __init__(self, handle: ctypes.c_void_p):
+        self._h = handle
+
+    def __len__(self):
+        return _lib().cq_cact_count(self._h)
+
+    def codebook(self) -> np.ndarray:
+        out = np.zeros(28, dtype=np.float32)
+        check(_lib().cq_cact_codebook(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_float))))
+        return out
+
+    def default_group(self) -> int:
+        return int(_lib().cq_cact_default_group(self._h))
+
+    def tensor(self, i: int) -> CactTensor:
+        d = TensorDesc()
+        check(_lib().cq_cact_tensor(self._h, i, ctypes.byref(d)))
+        data = ctypes.string_at(d.data, d.nbytes) if d.nbytes else b""
+        return CactTensor(dtype=d.dtype, shape=tuple(d.shape[: d.ndim]), nbytes=d.nbytes,
+                          group=d.group, bits=d.bits, data=data)
+
+    def close(self):
+        if self._h:
+            _lib().cq_cact_close(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def cq_cact_open(path: str) -> CactReader:
+    h = ctypes.c_void_p()
+    check(_lib().cq_cact_open(path.encode(), ctypes.byref(h)))
+    return CactReader(h)
+
+
+def cq_cact_open_memory(data: bytes) -> CactReader:
+    h = ctypes.c_void_p()
+    buf = ctypes.create_string_buffer(bytes(data), len(data))
+    check(_lib().cq_cact_open_memory(ctypes.cast(buf, ctypes.c_void_p), len(data), ctypes.byref(h)))
+    return CactReader(h)

@@ -1,0 +1,368 @@
+// cq_encode.cu -- CQ encoder and per-token int8 activation quantiser.
+//
+// Encoder ("The .cact format", "Cactus Quants"; OpenNeedle docs/reference.md,
+// CQ quantisation): per group of 128 weights along the input axis,
+//   r = w . H (normalised Sylvester Hadamard), n = fp32 |r|,
+//   u = r / max(n, 1e-12), q_k = nearest level (ties -> smaller index),
+//   store fp16(n) and the codes as an LSB-first bitstream per row.
+//
+// GB300 mapping. The encoder streams 4 bytes in per weight and writes
+// ~0.27 bytes out, so it is bound by HBM; the arithmetic per weight (7
+// butterfly adds, a scale, the level search, packing) must stay inside the
+// issue budget that leaves. A CTA of 256 threads stages 128 groups (64 KB)
+// in shared memory with coalesced 16-byte loads; two threads own one group,
+// 64 values each, split on bit 2 of the coordinate. Each thread reads its
+// 16 chunks of 16 bytes with an XOR swizzle (chunk 2*(j^f)+h, f = pair&3)
+// that keeps every quarter-warp on 8 distinct bank groups. The swizzle
+// permutes the inputs of the transform by XOR, which only flips the signs
+// of outputs (H(x o xor_f) = diag((-1)^<f,m>) H x); the sign is folded into
+// the per-coordinate scale. Six butterfly stages run in registers and one
+// across the thread pair with a shuffle.
+//
+// Exactness. Codes: the nearest-level search in fp32 with ties to the
+// smaller index is a step function of u whose steps sit at fixed fp32
+// thresholds T_j (the first u with fl(c_{j+1}-u) < fl(u-c_j)); each CTA finds
+// them once by bisection over the ordered fp32 values, then the code is the
+// number of thresholds <= u. Norms: the fp16 norm must equal
+// fp16(fp32(sqrt(sum w^2))) exactly (the sum of squares is the same on both
+// sides of the rotation). A pairwise fp32 sum has relative error below
+// 8 * 2^-24; when every value within 5e-7 of the fp32 estimate rounds to the
+// same fp16 the result is certain, otherwise (about 0.2% of groups) the
+// group recomputes the sum in fp64 from exact products.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "cq_internal.h"
+
+namespace cq {
+namespace {
+
+constexpr int kEncThreads = 256;
+constexpr int kEncGroupsPerTile = kEncThreads / 2;             // 128 groups
+constexpr int kEncTileFloats = kEncGroupsPerTile * kGroup;     // 16384 floats = 64 KB
+constexpr float kInvSqrt128 = 0.08838834764831845f;            // 1/sqrt(128)
+
+struct EncodeParams {
+    const float *W;
+    uint8_t *codes;
+    __half *norms;
+    long long n_groups;  // out * ng
+    int in, ng;
+    float cb[kMaxLevels];
+};
+
+// Order-preserving map from fp32 (non-NaN) to uint32 and back.
+__device__ __forceinline__ uint32_t ord_key(float f) {
+    uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+    uint32_t b = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+    return __uint_as_float(b);
+}
+
+// First fp32 u in (a, b] at which level b is strictly nearer than level a
+// under fp32 subtraction; below it the tie rule keeps the smaller index.
+__device__ float decision_threshold(float a, float b) {
+    uint32_t lo = ord_key(a), hi = ord_key(b);
+    while (hi - lo > 1u) {
+        uint32_t mid = lo + (hi - lo) / 2u;
+        float u = key_float(mid);
+        if (__fsub_rn(b, u) < __fsub_rn(u, a))
+            hi = mid;
+        else
+            lo = mid;
+    }
+    return key_float(hi);
+}
+
+template <int L>
+__device__ __forceinline__ int level_index(float u, const float (&T)[16]) {
+    if (L == 4) {
+        // two-step search over 3 thresholds
+        return u >= T[1] ? (u >= T[2] ? 3 : 2) : (u >= T[0] ? 1 : 0);
+    } else {
+        int q = 0;
+#pragma unroll
+        for (int j = 0; j < L - 1; ++j) q += (u >= T[j]) ? 1 : 0;
+        return q;
+    }
+}
+
+// BITS: 2, 3, 4 or 5 (ternary). ALIGNED: in % 128 == 0 and W 16-byte aligned,
+// so the groups of the matrix form one contiguous fp32 array.
+template <int BITS, bool ALIGNED>
+__global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_constant__ EncodeParams p) {
+    constexpr int L = BITS == 5 ? 3 : (1 << BITS);
+    constexpr int W = BITS == 5 ? 2 : BITS;  // code width
+    extern __shared__ float4 smem4[];
+    float *tile = reinterpret_cast<float *>(smem4);
+    __shared__ float s_thr[16];
+
+    const int tid = threadIdx.x;
+    if (tid < L - 1) s_thr[tid] = decision_threshold(p.cb[tid], p.cb[tid + 1]);
+    __syncthreads();
+    float T[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) T[j] = j < L - 1 ? s_thr[j] : 0.0f;
+
+    const int pair = tid >> 1, h = tid & 1, f = pair & 3;
+    const long long n_tiles = (p.n_groups + kEncGroupsPerTile - 1) / kEncGroupsPerTile;
+
+    for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const long long g0 = t * kEncGroupsPerTile;
+        // ---- stage 128 groups into shared memory (coalesced) ----
+        if (ALIGNED) {
+            const float4 *src = reinterpret_cast<const float4 *>(p.W) + g0 * (kGroup / 4);
+            const long long avail4 = (p.n_groups - g0) * (kGroup / 4);
+#pragma unroll 4
+            for (int i = tid; i < kEncTileFloats / 4; i += kEncThreads)
+                smem4[i] = i < avail4 ? __ldcs(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            for (int i = tid; i < kEncTileFloats; i += kEncThreads) {
+                const long long G = g0 + i / kGroup;
+                float v = 0.0f;
+                if (G < p.n_groups) {
+                    const long long o = G / p.ng;
+                    const int col = (int)(G - o * p.ng) * kGroup + (i % kGroup);
+                    if (col < p.in) v = __ldcs(p.W + o * p.in + col);
+                }
+                tile[i] = v;
+            }
+        }
+        __syncthreads();
+
+        const long long G = g0 + pair;
+        // ---- load my 64 values: register 4j+e = coordinate 8(j^f)+4h+e ----
+        float x[64];
+        const float4 *grp = smem4 + pair * (kGroup / 4);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            float4 v = grp[2 * (j ^ f) + h];
+            x[4 * j + 0] = v.x;
+            x[4 * j + 1] = v.y;
+            x[4 * j + 2] = v.z;
+            x[4 * j + 3] = v.w;
+        }
+        __syncthreads();  // the tile may be overwritten from here on
+
+        // ---- sum of squares, pairwise in fp32 ----
+        float sq[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sq[i] = __fadd_rn(__fmul_rn(x[2 * i], x[2 * i]), __fmul_rn(x[2 * i + 1], x[2 * i + 1]));
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) sq[i] = __fadd_rn(sq[i], sq[i + w]);
+        const float s32 = __fadd_rn(sq[0], __shfl_xor_sync(0xffffffffu, sq[0], 1));
+
+        // ---- fast Walsh-Hadamard transform: 6 stages in registers ----
+#pragma unroll
+        for (int bit = 1; bit < 64; bit <<= 1)
+#pragma unroll
+            for (int r = 0; r < 64; ++r)
+                if (!(r & bit)) {
+                    float a = x[r], b = x[r | bit];
+                    x[r] = __fadd_rn(a, b);
+                    x[r | bit] = __fsub_rn(a, b);
+                }
+        // ... and one across the thread pair (coordinate bit 2)
+#pragma unroll
+        for (int r = 0; r < 64; ++r) {
+            float o = __shfl_xor_sync(0xffffffffu, x[r], 1);
+            x[r] = h ? __fsub_rn(o, x[r]) : __fadd_rn(x[r], o);
+        }
+
+        // ---- fp32 group norm, exact fp16 storage ----
+        float n32 = __fsqrt_rn(s32);
+        bool sure = s32 >= 1e-30f && s32 <= 1e30f;
+        if (sure) {
+            __half lo = __float2half_rn(__fmul_rn(n32, 1.0f - 5e-7f));
+            __half hi = __float2half_rn(__fmul_rn(n32, 1.0f + 5e-7f));
+            sure = __half_as_ushort(lo) == __half_as_ushort(hi);
+        }
+        // Both threads of a pair hold the same s32, hence the same verdict.
+        const bool need64 = !sure;
+        if (__any_sync(0xffffffffu, need64)) {
+            // Rare path: exact products and an fp64 sum over the group's
+            // original values, reread from global memory.
+            double d = 0.0;
+            if (need64 && G < p.n_groups) {
+                const long long o = G / p.ng;
+                const int gcol = (int)(G - o * p.ng) * kGroup;
+#pragma unroll 4
+                for (int j = 0; j < 16; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = gcol + 8 * (j ^ f) + 4 * h + e;
+                        const double w = col < p.in ? (double)p.W[o * p.in + col] : 0.0;
+                        d = __fma_rn(w, w, d);
+                    }
+            }
+            d += __shfl_xor_sync(0xffffffffu, d, 1);
+            if (need64) n32 = __double2float_rn(__dsqrt_rn(d));
+        }
+
+        // ---- directions and codes ----
+        const float den = fmaxf(n32, 1e-12f);
+        const float sc = __fdiv_rn(kInvSqrt128, den);
+        float scale4[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) scale4[b] = (__popc(f & b) & 1) ? -sc : sc;
+
+        uint32_t chunk[16];  // 4 codes (4W bits) per j
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            uint32_t c = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float u = __fmul_rn(x[4 * j + e], scale4[j & 3]);
+                int q = level_index<L>(u, T);
+                if (BITS == 5) q = (q - 1) & 3;  // ternary crumb
+                c |= (uint32_t)q << (W * e);
+            }
+            chunk[j] = c;
+        }
+
+        // ---- exchange: thread h writes coordinates [64h, 64h+64) = j in [8h, 8h+8) ----
+        // (register-indexed selects keep the chunk array out of local memory)
+        uint32_t send[4], recv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = h ? chunk[2 * i] : chunk[8 + 2 * i];
+            const uint32_t hi = h ? chunk[2 * i + 1] : chunk[8 + 2 * i + 1];
+            send[i] = lo | (hi << 16);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) recv[i] = __shfl_xor_sync(0xffffffffu, send[i], 1);
+
+        // block i (8 coordinates, 8W bits) = [thread-0 chunk | thread-1 chunk]
+        uint32_t outw[2 * W];
+#pragma unroll
+        for (int k = 0; k < 2 * W; ++k) outw[k] = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t mine = h ? chunk[8 + i] : chunk[i];
+            const uint32_t theirs = (recv[i >> 1] >> (16 * (i & 1))) & 0xffffu;
+            const uint32_t lo = h ? theirs : mine;  // coordinates 8j'+0..3 come from thread 0
+            const uint32_t hi = h ? mine : theirs;
+            const uint64_t blk = (uint64_t)lo | ((uint64_t)hi << (4 * W));
+            const int bitpos = 8 * W * i;
+            outw[bitpos / 32] |= (uint32_t)(blk << (bitpos % 32));
+            if ((bitpos % 32) + 8 * W > 32) outw[bitpos / 32 + 1] |= (uint32_t)(blk >> (32 - bitpos % 32));
+        }
+
+        if (G < p.n_groups) {
+            uint8_t *dst = p.codes + G * (16 * W) + h * (8 * W);
+            if (W == 3) {
+                uint2 *d2 = reinterpret_cast<uint2 *>(dst);
+#pragma unroll
+                for (int k = 0; k < 3; ++k) __stcs(d2 + k, make_uint2(outw[2 * k], outw[2 * k + 1]));
+            } else {
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                for (int k = 0; k < W / 2; ++k)
+                    __stcs(d4 + k, make_uint4(outw[4 * k], outw[4 * k + 1], outw[4 * k + 2], outw[4 * k + 3]));
+            }
+            if (h == 0) p.norms[G] = __float2half_rn(n32);
+        }
+    }
+}
+
+// ----------------------------------------------------- activation quant --
+// One CTA per token: s = absmax/127 (IEEE division), q = rint(x/s) clamped.
+__global__ void act_quant_kernel(const float *__restrict__ X, int M, int in, int8_t *__restrict__ Q,
+                                 float *__restrict__ S) {
+    __shared__ float red[32];
+    for (int t = blockIdx.x; t < M; t += gridDim.x) {
+        const float *x = X + (size_t)t * in;
+        float amax = 0.0f;
+        for (int k = threadIdx.x; k < in; k += blockDim.x) amax = fmaxf(amax, fabsf(x[k]));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (threadIdx.x == 0) red[0] = v;
+        }
+        __syncthreads();
+        amax = red[0];
+        const float s = amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 1.0f;
+        for (int k = threadIdx.x; k < in; k += blockDim.x) {
+            float v = rintf(__fdiv_rn(x[k], s));
+            v = fminf(fmaxf(v, -128.0f), 127.0f);
+            Q[(size_t)t * in + k] = (int8_t)(int)v;
+        }
+        if (threadIdx.x == 0) S[t] = s;
+        __syncthreads();
+    }
+}
+
+template <int BITS, bool ALIGNED>
+int launch_encode_t(const EncodeParams &p, cudaStream_t st) {
+    const size_t smem = kEncTileFloats * sizeof(float);
+    auto k = encode_kernel<BITS, ALIGNED>;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attr = true;
+    }
+    const long long tiles = (p.n_groups + kEncGroupsPerTile - 1) / kEncGroupsPerTile;
+    const long long grid = std::min<long long>(tiles, (long long)sm_count() * 2);
+    k<<<(unsigned)grid, kEncThreads, smem, st>>>(p);
+    return CQ_OK;
+}
+
+}  // namespace
+
+int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+    }
+    return n;
+}
+
+int launch_encode(const float *W, int out, int in, int bits, const float *cb, uint8_t *blob,
+                  void *stream) {
+    EncodeParams p;
+    p.W = W;
+    p.in = in;
+    p.ng = in_padded(in) / kGroup;
+    p.n_groups = (long long)out * p.ng;
+    const size_t rowBytes = (size_t)in_padded(in) * width_of(bits) / 8;
+    p.codes = blob;
+    uint8_t *nb = blob + (size_t)out * rowBytes;
+    if ((reinterpret_cast<uintptr_t>(blob) & 15) || (reinterpret_cast<uintptr_t>(nb) & 1))
+        return set_error(CQ_ERR_ARG, "blob must be 16-byte aligned");
+    p.norms = reinterpret_cast<__half *>(nb);
+    const int L = levels_of(bits);
+    for (int j = 0; j < kMaxLevels; ++j) p.cb[j] = j < L ? cb[j] : 0.0f;
+    const bool aligned = (in % kGroup == 0) && !(reinterpret_cast<uintptr_t>(W) & 15);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    switch (bits) {
+    case 2: aligned ? launch_encode_t<2, true>(p, st) : launch_encode_t<2, false>(p, st); break;
+    case 3: aligned ? launch_encode_t<3, true>(p, st) : launch_encode_t<3, false>(p, st); break;
+    case 4: aligned ? launch_encode_t<4, true>(p, st) : launch_encode_t<4, false>(p, st); break;
+    case 5: aligned ? launch_encode_t<5, true>(p, st) : launch_encode_t<5, false>(p, st); break;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "encode launch: %s", cudaGetErrorString(e));
+    return CQ_OK;
+}
+
+int launch_act_quant(const float *X, int M, int in, int8_t *Xq, float *s, void *stream) {
+    const int grid = std::min(M, sm_count() * 8);
+    act_quant_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(X, M, in, Xq, s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "act_quant launch: %s", cudaGetErrorString(e));
+    return CQ_OK;
+}
+
+}  // namespace cq

@@ -1,0 +1,269 @@
+// cq_gemv.cu -- matrix-vector products over CQ-packed weights (batch 1..16),
+// single and grouped.
+//
+// The rotated-domain identity (OpenNeedle docs/reference.md; "The .cact
+// archive and Cactus Quants", "Reconstructing one group"): with H symmetric
+// and orthogonal, <w_hat_g, x_g> = n_g * <c[q_g], H x_g>. Each activation
+// group is rotated once by a fast Walsh-Hadamard transform in registers and
+// reused for every output row; the codes are looked up, never expanded to a
+// dense matrix ("The .cact format", "How the kernel reads it").
+//
+// Work decomposition: a work item is (matrix, tile of 32 rows, chunk of
+// groups). A CTA rotates the activation chunk of its item into shared memory
+// (fp32, one warp per group: four coordinates per lane, two butterfly stages
+// in registers and five with shuffles), then its threads take (row, group)
+// pairs: each loads the group's 16*width code bytes with 16-byte loads,
+// accumulates level*z in fp32 for every batch column, scales by the group
+// norm and adds into a per-row shared accumulator. Rows split over several
+// chunks (long inputs with a large batch) accumulate into y atomically.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "cq_internal.h"
+
+namespace cq {
+namespace {
+
+constexpr int kGemvThreads = 256;
+constexpr int kRowsPerItem = 32;
+constexpr int kZPad = kGroup + 1;            // padded group stride in shared memory
+constexpr int kZBudgetFloats = 12288;        // 48 KB of rotated activations
+constexpr float kInvSqrt128 = 0.08838834764831845f;
+
+struct GemvMat {
+    const uint8_t *codes;
+    const __half *norms;
+    const void *x;
+    const float *xs;
+    float *y;
+    int out, in, ng, bits, xdt, B, lut, kcg, nchunks, row_tiles, items_before;
+};
+
+struct GemvParams {
+    int n, total_items, zfloats;
+    float lut[kMaxLuts][16];
+    GemvMat m[CQ_MAX_GROUPED];
+};
+
+// Rotates activation groups [gbeg, gend) of every batch row into zs:
+// zs[(b*kcg + (g-gbeg))*kZPad + k] = (H x_{b,g})[k].
+__device__ void rotate_chunk(const GemvMat &M, int gbeg, int gend, int kcg, float *zs) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ngc = gend - gbeg;
+    for (int task = warp; task < M.B * ngc; task += kGemvThreads / 32) {
+        const int b = task / ngc, gl = task % ngc, g = gbeg + gl;
+        float v[4];
+        float scale = kInvSqrt128;
+        if (M.xdt == CQ_X_I8) {
+            const int8_t *xq = static_cast<const int8_t *>(M.x) + (size_t)b * M.in;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int col = g * kGroup + 4 * lane + i;
+                v[i] = col < M.in ? (float)xq[col] : 0.0f;
+            }
+            scale = __fmul_rn(M.xs[b], kInvSqrt128);
+        } else {
+            const float *xf = static_cast<const float *>(M.x) + (size_t)b * M.in;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int col = g * kGroup + 4 * lane + i;
+                v[i] = col < M.in ? xf[col] : 0.0f;
+            }
+        }
+        // coordinate bits 0,1 in registers
+        float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+        v[0] = a0 + a2;
+        v[1] = a1 + a3;
+        v[2] = a0 - a2;
+        v[3] = a1 - a3;
+        // coordinate bits 2..6 across lanes
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+                v[i] = (lane & m) ? o - v[i] : v[i] + o;
+            }
+        float *dst = zs + (size_t)(b * kcg + gl) * kZPad + 4 * lane;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = v[i] * scale;
+    }
+}
+
+template <int W>
+__device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[4 * W], int k) {
+    const int bit = k * W, word = bit >> 5, off = bit & 31;
+    uint32_t v = w[word] >> off;
+    if (off + W > 32) v |= w[word + 1] << (32 - off);
+    return v & ((1u << W) - 1u);
+}
+
+template <int W, int BMAX>
+__global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constant__ GemvParams p) {
+    extern __shared__ float smem[];
+    float *zs = smem;
+    float *ys = smem + p.zfloats;  // [kRowsPerItem][16]
+    __shared__ float lut_s[16];
+
+    for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
+        // locate the matrix of this item
+        int lo = 0, hi = p.n - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) / 2;
+            if (p.m[mid].items_before <= item) lo = mid;
+            else hi = mid - 1;
+        }
+        const GemvMat &M = p.m[lo];
+        const int local = item - M.items_before;
+        const int rt = local / M.nchunks, kc = local % M.nchunks;
+        const int gbeg = kc * M.kcg, gend = min(M.ng, gbeg + M.kcg);
+        const int row0 = rt * kRowsPerItem;
+        const int B = M.B;
+
+        if (threadIdx.x < 16) lut_s[threadIdx.x] = p.lut[M.lut][threadIdx.x];
+        for (int i = threadIdx.x; i < kRowsPerItem * 16; i += kGemvThreads) ys[i] = 0.0f;
+        rotate_chunk(M, gbeg, gend, M.kcg, zs);
+        __syncthreads();
+
+        const int ngc = gend - gbeg;
+        const size_t rowBytes = (size_t)M.ng * 16 * W;
+        for (int pr = threadIdx.x; pr < kRowsPerItem * ngc; pr += kGemvThreads) {
+            const int r = pr / ngc, gl = pr % ngc, o = row0 + r;
+            if (o >= M.out) continue;
+            const int g = gbeg + gl;
+            uint32_t w[4 * W];
+            const uint4 *src = reinterpret_cast<const uint4 *>(M.codes + (size_t)o * rowBytes + (size_t)g * 16 * W);
+#pragma unroll
+            for (int i = 0; i < W; ++i) {
+                const uint4 t = __ldg(src + i);
+                w[4 * i] = t.x;
+                w[4 * i + 1] = t.y;
+                w[4 * i + 2] = t.z;
+                w[4 * i + 3] = t.w;
+            }
+            float acc[BMAX];
+#pragma unroll
+            for (int b = 0; b < BMAX; ++b) acc[b] = 0.0f;
+            const float *z = zs + (size_t)gl * kZPad;
+#pragma unroll 8
+            for (int k = 0; k < kGroup; ++k) {
+                const float lv = lut_s[code_at<W>(w, k)];
+#pragma unroll
+                for (int b = 0; b < BMAX; ++b)
+                    if (b < B) acc[b] = fmaf(lv, z[(size_t)b * M.kcg * kZPad + k], acc[b]);
+            }
+            const float nrm = __half2float(M.norms[(size_t)o * M.ng + g]);
+#pragma unroll
+            for (int b = 0; b < BMAX; ++b)
+                if (b < B) atomicAdd(&ys[r * 16 + b], acc[b] * nrm);
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < kRowsPerItem * B; i += kGemvThreads) {
+            const int r = i / B, b = i % B, o = row0 + r;
+            if (o >= M.out) continue;
+            float *dst = M.y + (size_t)b * M.out + o;
+            if (M.nchunks == 1) *dst = ys[r * 16 + b];
+            else atomicAdd(dst, ys[r * 16 + b]);
+        }
+        __syncthreads();
+    }
+}
+
+template <int W, int BMAX>
+void launch_w(const GemvParams &p, size_t smem, int grid, cudaStream_t st) {
+    auto k = gemv_kernel<W, BMAX>;
+    static int attr_set = 0;  // raise the dynamic shared memory cap once
+    if (!attr_set) {
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024 + 4096);
+        attr_set = 1;
+    }
+    k<<<grid, kGemvThreads, smem, st>>>(p);
+}
+
+template <int W>
+void launch_b(int bmax, const GemvParams &p, size_t smem, int grid, cudaStream_t st) {
+    if (bmax <= 1) launch_w<W, 1>(p, smem, grid, st);
+    else if (bmax <= 4) launch_w<W, 4>(p, smem, grid, st);
+    else if (bmax <= 8) launch_w<W, 8>(p, smem, grid, st);
+    else launch_w<W, 16>(p, smem, grid, st);
+}
+
+}  // namespace
+
+int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // One launch per code width present; each launch walks all descriptors of
+    // its width (matrices of other widths contribute no items).
+    for (int W = 2; W <= 4; ++W) {
+        static GemvParams p;  // large: keep off the stack
+        p.n = 0;
+        int bmax = 0, nlut = 0, items = 0, zfloats = 0;
+        for (int i = 0; i < n; ++i) {
+            if (width_of(d[i].bits) != W || d[i].out == 0) continue;
+            if (d[i].in == 0) {  // empty reduction: the product is zero
+                cudaMemsetAsync(d[i].y, 0, sizeof(float) * d[i].B * d[i].out, st);
+                continue;
+            }
+            GemvMat &M = p.m[p.n];
+            const int ip = in_padded(d[i].in);
+            M.codes = d[i].blob;
+            M.norms = reinterpret_cast<const __half *>(d[i].blob + (size_t)d[i].out * ip * W / 8);
+            M.x = d[i].x;
+            M.xs = d[i].x_scale;
+            M.y = d[i].y;
+            M.out = d[i].out;
+            M.in = d[i].in;
+            M.ng = ip / kGroup;
+            M.bits = d[i].bits;
+            M.xdt = d[i].x_dtype;
+            M.B = d[i].B;
+            // level table for the stored codes (ternary crumbs sign-extend)
+            float lut[16] = {0};
+            if (d[i].bits == 5) {
+                const float c = d[i].codebook[2];
+                lut[0] = 0.0f;
+                lut[1] = c;
+                lut[2] = -2.0f * c;
+                lut[3] = -c;
+            } else {
+                for (int j = 0; j < levels_of(d[i].bits); ++j) lut[j] = d[i].codebook[j];
+            }
+            int li = -1;
+            for (int j = 0; j < nlut; ++j)
+                if (std::equal(lut, lut + 16, p.lut[j])) li = j;
+            if (li < 0) {
+                if (nlut == kMaxLuts) return set_error(CQ_ERR_ARG, "more than %d distinct codebooks in one call", kMaxLuts);
+                std::copy(lut, lut + 16, p.lut[nlut]);
+                li = nlut++;
+            }
+            M.lut = li;
+            const int bclass = M.B <= 1 ? 1 : M.B <= 4 ? 4 : M.B <= 8 ? 8 : 16;
+            bmax = std::max(bmax, bclass);
+            M.kcg = std::max(1, std::min(M.ng, kZBudgetFloats / (M.B * kZPad)));
+            M.nchunks = (M.ng + M.kcg - 1) / M.kcg;
+            M.row_tiles = (M.out + kRowsPerItem - 1) / kRowsPerItem;
+            M.items_before = items;
+            items += M.row_tiles * M.nchunks;
+            zfloats = std::max(zfloats, M.B * M.kcg * kZPad);
+            if (M.nchunks > 1) cudaMemsetAsync(M.y, 0, sizeof(float) * M.B * M.out, st);
+            ++p.n;
+        }
+        if (p.n == 0) continue;
+        p.total_items = items;
+        p.zfloats = zfloats;
+        const size_t smem = sizeof(float) * (zfloats + kRowsPerItem * 16);
+        const int grid = std::min(items, sm_count() * 8);
+        switch (W) {
+        case 2: launch_b<2>(bmax, p, smem, grid, st); break;
+        case 3: launch_b<3>(bmax, p, smem, grid, st); break;
+        case 4: launch_b<4>(bmax, p, smem, grid, st); break;
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemv launch: %s", cudaGetErrorString(e));
+    }
+    return CQ_OK;
+}
+
+}  // namespace cq

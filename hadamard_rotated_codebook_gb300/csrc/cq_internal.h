@@ -1,0 +1,62 @@
+// cq_internal.h -- declarations shared by the translation units of libcq.
+// Host code (cq_host.cpp) validates arguments and calls the launchers below;
+// each launcher lives in the .cu file of its kernel.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/cq.h"
+
+namespace cq {
+
+// Record an error for cq_last_error() and return `code`.
+int set_error(int code, const char *fmt, ...);
+void clear_error();
+
+constexpr int kGroup = 128;          // the group size the kernels support
+constexpr int kMaxLevels = 16;
+constexpr int kMaxLuts = 8;          // distinct codebooks per grouped launch
+
+inline int levels_of(int bits) {
+    switch (bits) {
+    case 2: return 4;
+    case 3: return 8;
+    case 4: return 16;
+    case 5: return 3;
+    default: return -1;
+    }
+}
+inline int width_of(int bits) {
+    switch (bits) {
+    case 2: return 2;
+    case 3: return 3;
+    case 4: return 4;
+    case 5: return 2;
+    default: return -1;
+    }
+}
+inline int in_padded(int in) { return (in + kGroup - 1) / kGroup * kGroup; }
+
+// Checks a host codebook: non-null, finite, strictly increasing.
+int check_codebook(const float *cb, int bits);
+
+// ------------------------------------------------------------- encode --
+int launch_encode(const float *W, int out, int in, int bits, const float *cb,
+                  uint8_t *blob, void *stream);
+int launch_act_quant(const float *X, int M, int in, int8_t *Xq, float *s,
+                     void *stream);
+
+// --------------------------------------------------------------- gemv --
+int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream);
+
+// --------------------------------------------------------------- gemm --
+int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream);
+
+// Number of SMs of the current device (cached).
+int sm_count();
+
+// Device status word shared by kernels with bounded waits.
+int read_and_clear_device_status(void *stream);
+
+}  // namespace cq

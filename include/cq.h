@@ -1,0 +1,276 @@
+/*
+ * cq.h -- C ABI of libcq: Cactus Quants (CQ) encode, GEMV and GEMM over
+ * CQ-packed weights on one GB300 (sm_103a), plus a minimal .cact-shaped
+ * container.
+ *
+ * Page citations give the page title and the section:
+ *   [CF]  "The .cact format" (cactuscompute.com blog): "Five regions",
+ *         "Cactus Quants", "How the kernel reads it", "Versions".
+ *   [NJ]  "The .cact archive and Cactus Quants" (needle.js tutorial):
+ *         "Shared codebooks", "Tensor directory", "Anatomy of a CQ matrix",
+ *         "2-bit", "4-bit", "3-bit", "Reconstructing one group",
+ *         "Keep the quantized views".
+ *   [ON]  OpenNeedle docs/reference.md: CQ quantisation, file format,
+ *         rotated-domain identity, fake_quant_act, SDOT kernels.
+ *   [PN]  "Porting Needle 3" (cactuscompute.com blog): "2. The tensor order
+ *         is the contract".
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Return value: CQ_OK (0) or a negative CQ_ERR_* code. On error the
+ *    reason is available from cq_last_error() (thread-local, valid until the
+ *    next call on the same thread). No entry point aborts the process.
+ *  - Device entry points take caller-owned DEVICE pointers for tensors and
+ *    are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ *    the legacy default stream). They validate arguments on the host before
+ *    launching and report launch failures as CQ_ERR_CUDA. Codebooks are
+ *    HOST pointers: their values are copied into the launch parameters, so
+ *    the caller may free them as soon as the call returns.
+ *  - A CQ blob passed to a device entry point must start on a 16-byte
+ *    boundary (the kernels read codes with 16-byte loads); CQ_ERR_ARG
+ *    otherwise. cudaMalloc and torch allocations satisfy this.
+ *  - Matrices are row-major [out][in], stored pre-transposed as in [CF]
+ *    "Five regions": an output row is contiguous along the reduction axis.
+ *  - The kernels support group = 128 (the only group size the pages ship);
+ *    other powers of two are valid in the format and container and are
+ *    rejected by the device entry points with CQ_ERR_SHAPE.
+ *  - bits: 2, 3, 4 (CQ2/CQ3/CQ4, 4/8/16 levels) or 5, the ternary marker of
+ *    [NJ] "Shared codebooks" (3 levels {-c, 0, +c}, stored as 2-bit crumbs).
+ *  - A codebook is cq_levels(bits) floats, strictly increasing, already
+ *    divided by sqrt(group) ([NJ] "Shared codebooks"). For bits = 5 it is
+ *    {-c, 0, +c}.
+ */
+#ifndef CQ_H
+#define CQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CQ_OK 0
+#define CQ_ERR_ARG (-1)     /* null pointer, bad enum, bad codebook */
+#define CQ_ERR_SHAPE (-2)   /* unsupported or inconsistent sizes */
+#define CQ_ERR_FORMAT (-3)  /* malformed container */
+#define CQ_ERR_IO (-4)      /* file system error */
+#define CQ_ERR_CUDA (-5)    /* CUDA runtime or launch failure */
+#define CQ_ERR_TIMEOUT (-6) /* a bounded device wait gave up (see cq_device_status) */
+#define CQ_ERR_NOMEM (-7)   /* host or device allocation failed */
+
+/* Activation element types for cq_gemv. */
+#define CQ_X_F32 0 /* fp32 activations x[B][in] */
+#define CQ_X_I8 1  /* int8 activations q[B][in] with fp32 per-token scales s[B]: x = s*q */
+
+/* Largest batch accepted by cq_gemv / cq_gemv_grouped. */
+#define CQ_GEMV_MAX_BATCH 16
+/* Largest number of matrices in one grouped call. */
+#define CQ_MAX_GROUPED 256
+
+/* Thread-local description of the last error on this thread ("" if none). */
+const char *cq_last_error(void);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int cq_version(void);
+
+/* ------------------------------------------------------------- host -- */
+
+/* Number of codebook levels for `bits` (4, 8, 16; 3 for the ternary
+ * marker 5), or -1. */
+int cq_levels(int bits);
+
+/* Packed code width in bits per weight (2, 3, 4; 2 for ternary), or -1. */
+int cq_code_width(int bits);
+
+/* Analytic codebook for `bits` and `group`.
+ * [NJ] "Shared codebooks" and [CF] "Cactus Quants": Lloyd-Max levels of the
+ * Gaussian, divided by sqrt(group). This computes them on the host by
+ * iterating the Lloyd-Max centroid / midpoint conditions on the exact
+ * standard normal density to a fixed point (the pages' own files carry an
+ * empirical codebook instead; any strictly increasing codebook, such as one
+ * read from a container, may be passed to the other entry points).
+ * For bits = 5 the levels are {-1.2240064, 0, +1.2240064}/sqrt(group), the
+ * constant printed in [NJ] "Shared codebooks".
+ * levels: host buffer of `cap` floats, or NULL to query the count only
+ *         (the convention of needle_embed in [PN]).
+ * n_levels: receives cq_levels(bits); may be NULL.
+ * Errors: CQ_ERR_ARG for bad bits/group or cap too small. */
+int cq_codebook_init(int bits, int group, float *levels, size_t cap,
+                     size_t *n_levels);
+
+/* Bytes of one CQ blob ([NJ] "Anatomy of a CQ matrix"):
+ * out*in_pad*width/8 + out*(in_pad/group)*2, in_pad = ceil(in/group)*group.
+ * Returns 0 on invalid arguments (out or in < 0, group not a power of two
+ * >= 8, unknown bits). */
+uint64_t cq_packed_bytes(int out, int in, int group, int bits);
+
+/* ----------------------------------------------------------- device -- */
+
+/* Encode W[out][in] (fp32, device) into one CQ blob (device, exactly
+ * cq_packed_bytes(out,in,group,bits) bytes): codes of all rows as an
+ * LSB-first bitstream per row, then fp16 norms [out][in_pad/group].
+ * Per group of 128 along the input axis ([CF] "Cactus Quants", [ON] CQ
+ * quantisation): zero-pad, rotate by the normalised Walsh-Hadamard matrix
+ * (natural Sylvester order), fp32 norm n, direction u = r / max(n, 1e-12),
+ * nearest level per coordinate with ties to the smaller index (decided in
+ * fp32), fp16(n) stored. Ternary crumbs: 0 -> 00, +c -> 01, -c -> 11.
+ * W and blob must not overlap. Errors: CQ_ERR_ARG, CQ_ERR_SHAPE,
+ * CQ_ERR_CUDA. */
+int cq_encode(const float *W, int out, int in, int group, int bits,
+              const float *codebook, uint8_t *blob, void *stream);
+
+/* Per-token int8 quantisation of activations ([ON] fake_quant_act):
+ * s[t] = absmax(X[t,:])/127 in fp32 (1 for an all-zero row),
+ * Xq[t,k] = clamp(rint(X[t,k]/s[t]), -128, 127). X fp32 [M][in], Xq int8
+ * [M][in], s fp32 [M], all device. Errors: CQ_ERR_ARG, CQ_ERR_CUDA. */
+int cq_act_quant_int8(const float *X, int M, int in, int8_t *Xq, float *s,
+                      void *stream);
+
+/* Matrix-vector product over one CQ blob, batch 1..16:
+ *   y[b][o] = sum_g n[o][g] * < c[q[o,g,:]], H x_b,g >        ([ON], [NJ])
+ * which equals W_hat x_b exactly in real arithmetic: the activation is
+ * rotated once per group (in-register fast Walsh-Hadamard transform) and the
+ * weights are never expanded to a dense matrix ([CF] "How the kernel reads
+ * it"). Arithmetic is fp32 apart from tensor-core products of exactly
+ * represented code planes.
+ * x: device, fp32 [B][in] (x_dtype = CQ_X_F32, x_scale ignored, may be
+ *    NULL) or int8 [B][in] with x_scale fp32 [B] on the device
+ *    (x_dtype = CQ_X_I8).
+ * y: device fp32 [B][out], fully overwritten.
+ * Errors: CQ_ERR_ARG, CQ_ERR_SHAPE (group != 128, B out of range),
+ * CQ_ERR_CUDA. */
+int cq_gemv(const uint8_t *blob, int out, int in, int group, int bits,
+            const float *codebook, const void *x, int x_dtype,
+            const float *x_scale, int B, float *y, void *stream);
+
+/* One matrix of a grouped GEMV. All pointers are device pointers; the
+ * codebook is the host array `codebook` (cq_levels(bits) floats). */
+typedef struct cq_gemv_desc {
+    const uint8_t *blob;
+    const void *x;        /* [B][in], fp32 or int8 per x_dtype */
+    const float *x_scale; /* [B] for CQ_X_I8, else NULL */
+    float *y;             /* [B][out] */
+    const float *codebook;/* host pointer */
+    int out, in, group, bits, x_dtype, B;
+} cq_gemv_desc;
+
+/* Runs n (1..CQ_MAX_GROUPED) independent GEMVs in one kernel launch: the
+ * decode step of a Needle-shaped model, where many small matrices would
+ * otherwise each pay a launch. Descriptors that share the same x pointer
+ * share one activation rotation ([ON]: Q/K/V/gate reuse one rotated input).
+ * Results are identical to n separate cq_gemv calls up to fp32 summation
+ * order. Output buffers must not overlap. Errors as cq_gemv. */
+int cq_gemv_grouped(const cq_gemv_desc *descs, int n, void *stream);
+
+/* Prefill product over one CQ blob with int8 per-token activations:
+ *   Y[m][o] = s[m] * sum_k W_hat[o][k] Xq[m][k]
+ * computed as a dense contraction on the tensor cores: the activations are
+ * rotated exactly in integers per group (H0 Xq, |v| <= 16384) and stored in
+ * fp16; code tiles are expanded to fp16 W'[o][k] = c[q] n[o][g] in shared
+ * memory only, and tcgen05 accumulates in fp32 in tensor memory.
+ * Xq int8 [M][in], x_scale fp32 [M], Y fp32 [M][out]: device.
+ * The library keeps one internal device workspace for the rotated
+ * activations (M*in_pad fp16), grown on demand by the first call that
+ * needs more; make one untimed call before capturing a CUDA graph.
+ * Errors: CQ_ERR_ARG, CQ_ERR_SHAPE, CQ_ERR_NOMEM, CQ_ERR_CUDA,
+ * CQ_ERR_TIMEOUT (a pipeline wait exceeded its bound; results invalid). */
+int cq_gemm(const uint8_t *blob, int out, int in, int group, int bits,
+            const float *codebook, const int8_t *Xq, const float *x_scale,
+            int M, float *Y, void *stream);
+
+/* One matrix of a grouped GEMM (device pointers; host codebook). */
+typedef struct cq_gemm_desc {
+    const uint8_t *blob;
+    const int8_t *Xq;     /* [M][in] */
+    const float *x_scale; /* [M] */
+    float *Y;             /* [M][out] */
+    const float *codebook;/* host pointer */
+    int out, in, group, bits, M;
+} cq_gemm_desc;
+
+/* n independent GEMMs in as few launches as possible (one rotation launch
+ * per distinct activation, one persistent GEMM launch). Errors as cq_gemm. */
+int cq_gemm_grouped(const cq_gemm_desc *descs, int n, void *stream);
+
+/* Reads and clears the device-side status word that bounded waits set when
+ * they give up (synchronises `stream`). CQ_OK or CQ_ERR_TIMEOUT. */
+int cq_device_status(void *stream);
+
+/* -------------------------------------------------------- container -- */
+/*
+ * Own .cact-shaped container (the pages disagree on the header: 196 bytes
+ * and tag 0x05E12A84 in [CF] "Five regions" / "Versions", 120 bytes and tag
+ * 0x05E12A83 in [NJ] "Header"; and on dtype codes: 1..4 in [CF], [NJ], [ON]
+ * against 0..3 elsewhere). Layout, all little-endian:
+ *   header 64 B: u32 tag 0x42475143 ("CQGB"), u32 version = 1,
+ *                u32 header_bytes = 64, u32 n_tensors, u32 cb_len = 28,
+ *                u32 default group, 10 x u32 reserved (0)
+ *   codebook 28 x f32: CQ2[0..3], CQ3[4..11], CQ4[12..27] ([NJ] "Shared
+ *                codebooks")
+ *   directory n x 44 B ([NJ] "Tensor directory", [CF] "Five regions"):
+ *                u8 dtype (1 FP16, 2 FP32, 3 CQ, 4 RAW), u8 ndim (<= 4),
+ *                u16 pad, u32 shape[4], u64 offset, u64 nbytes, u32 group,
+ *                u32 bits
+ *   blobs at absolute offsets, each 64-byte aligned; tensors are nameless
+ *                and positional ([PN]).
+ * The reader refuses foreign tags with a message ([CF] "Versions") and
+ * checks every record before exposing any byte: offset + nbytes within the
+ * file (64-bit overflow-checked), 64-byte alignment, ndim <= 4, known
+ * dtype, FP16/FP32 byte counts equal to the element count, and for CQ a
+ * power-of-two group and nbytes equal to cq_packed_bytes(shape[0],
+ * shape[1], group, bits) ([NJ] "Header", "Anatomy of a CQ matrix").
+ */
+
+#define CQ_CACT_TAG 0x42475143u
+#define CQ_CACT_VERSION 1u
+#define CQ_CACT_HEADER_BYTES 64u
+#define CQ_CACT_CODEBOOK_LEN 28u
+#define CQ_CACT_RECORD_BYTES 44u
+#define CQ_CACT_ALIGN 64u
+
+#define CQ_DTYPE_FP16 1
+#define CQ_DTYPE_FP32 2
+#define CQ_DTYPE_CQ 3
+#define CQ_DTYPE_RAW 4
+
+typedef struct cq_tensor_desc {
+    uint8_t dtype;     /* CQ_DTYPE_* */
+    uint8_t ndim;      /* 0..4; a CQ tensor is 2-D [out][in] */
+    uint32_t shape[4]; /* unused dimensions are 0 */
+    uint64_t nbytes;   /* blob length */
+    uint32_t group;    /* CQ group, else 0 */
+    uint32_t bits;     /* CQ bits (2,3,4,5), else 0 */
+    const void *data;  /* host bytes: input to the writer; for the reader a
+                          pointer into the handle's copy of the file */
+} cq_tensor_desc;
+
+typedef struct cq_cact cq_cact; /* opaque reader handle */
+
+/* Writes n tensors (host data) and the 28-float codebook to `path`,
+ * atomically (temporary file, then rename). default_group goes into the
+ * header. Errors: CQ_ERR_ARG (bad descriptor, CQ nbytes inconsistent),
+ * CQ_ERR_IO. */
+int cq_cact_write(const char *path, const cq_tensor_desc *tensors, int n,
+                  const float codebook[28], uint32_t default_group);
+
+/* Opens and validates a container; on success *h owns one host copy of the
+ * file. Errors: CQ_ERR_IO, CQ_ERR_FORMAT (with a message naming the first
+ * failed check), CQ_ERR_NOMEM. */
+int cq_cact_open(const char *path, cq_cact **h);
+
+/* Same checks on an in-memory image (copied; `bytes` may be freed after). */
+int cq_cact_open_memory(const void *bytes, uint64_t size, cq_cact **h);
+
+int cq_cact_count(const cq_cact *h);            /* number of tensors, or -1 */
+int cq_cact_codebook(const cq_cact *h, float out[28]);
+uint32_t cq_cact_default_group(const cq_cact *h);
+/* Descriptor of tensor i; d->data points into the handle (valid until
+ * cq_cact_close). Errors: CQ_ERR_ARG for a bad index. */
+int cq_cact_tensor(const cq_cact *h, int i, cq_tensor_desc *d);
+void cq_cact_close(cq_cact *h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CQ_H */

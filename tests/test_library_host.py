@@ -1,0 +1,117 @@
+"""Host-side checks of libcq (no GPU needed): the library loads, exports
+every entry point include/cq.h declares, and its host logic (codebooks,
+byte accounting, argument validation) agrees with the oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def C():
+    from hadamard_rotated_codebook_gb300 import build
+    build.build()
+    import hadamard_rotated_codebook_gb300 as pkg
+    return pkg
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "cq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(cq_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(C):
+    from hadamard_rotated_codebook_gb300 import _capi
+    lib = ctypes.CDLL(C.library_path())
+    declared = _declared_functions()
+    assert len(declared) >= 20
+    for name in declared:
+        assert hasattr(lib, name), f"libcq.so does not export {name}"
+    # and the binding types every one of them
+    assert set(declared) == set(_capi.SIGNATURES)
+
+
+def test_library_is_built_for_sm103a(C):
+    # the build recipe is the one the package ships; check its arch flags
+    from hadamard_rotated_codebook_gb300 import build
+    assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5])
+def test_codebook_init_matches_oracle(C, bits):
+    np.testing.assert_array_equal(C.cq_codebook_init(bits, 128), O.analytic_codebook(bits, 128))
+    np.testing.assert_array_equal(C.cq_codebook_init(bits, 64), O.analytic_codebook(bits, 64))
+
+
+def test_codebook_init_query_and_errors(C):
+    from hadamard_rotated_codebook_gb300 import _capi
+    lib = _capi.load()
+    n = ctypes.c_size_t(0)
+    assert lib.cq_codebook_init(4, 128, None, 0, ctypes.byref(n)) == 0 and n.value == 16
+    assert lib.cq_codebook_init(6, 128, None, 0, None) == _capi.CQ_ERR_ARG
+    assert lib.cq_codebook_init(2, 100, None, 0, None) == _capi.CQ_ERR_ARG
+    buf = (ctypes.c_float * 2)()
+    assert lib.cq_codebook_init(2, 128, buf, 2, None) == _capi.CQ_ERR_ARG
+    assert b"need 4" in lib.cq_last_error()
+
+
+def test_levels_and_widths(C):
+    for bits in (2, 3, 4, 5):
+        assert C.cq_levels(bits) == O.levels(bits)
+        assert C.cq_code_width(bits) == O.width(bits)
+    assert C.cq_levels(1) == -1 and C.cq_code_width(7) == -1
+
+
+def test_packed_bytes_matches_oracle(C):
+    rng = np.random.RandomState(0)
+    for _ in range(200):
+        out, n_in = int(rng.randint(0, 5000)), int(rng.randint(0, 9000))
+        group = int(2 ** rng.randint(3, 9))
+        bits = int(rng.choice([2, 3, 4, 5]))
+        assert C.cq_packed_bytes(out, n_in, group, bits) == O.packed_bytes(out, n_in, group, bits)
+    assert C.cq_packed_bytes(4, 4, 96, 2) == 0
+    assert C.cq_packed_bytes(-1, 4, 128, 2) == 0
+
+
+def test_device_entry_points_reject_bad_arguments_before_launch(C):
+    """Argument errors come back as status codes with a message, before any
+    CUDA call (this host has no GPU)."""
+    from hadamard_rotated_codebook_gb300 import _capi
+    lib = _capi.load()
+    cb = (ctypes.c_float * 4)(-0.1, -0.03, 0.03, 0.1)
+    bad = (ctypes.c_float * 4)(-0.1, 0.03, -0.03, 0.1)
+    assert lib.cq_encode(None, 4, 128, 64, 2, cb, None, None) == _capi.CQ_ERR_SHAPE
+    assert b"group = 128" in lib.cq_last_error()
+    assert lib.cq_encode(None, 4, 128, 128, 2, bad, None, None) == _capi.CQ_ERR_ARG
+    assert b"increasing" in lib.cq_last_error()
+    assert lib.cq_encode(None, 4, 128, 128, 7, cb, None, None) == _capi.CQ_ERR_ARG
+    assert lib.cq_encode(None, 4, 128, 128, 2, cb, None, None) == _capi.CQ_ERR_ARG  # null W
+    assert lib.cq_encode(None, 0, 128, 128, 2, cb, None, None) == _capi.CQ_OK  # empty: no work
+    d = _capi.GemvDesc(blob=1, x=1, x_scale=None, y=1, codebook=cb, out=4, in_=128, group=128,
+                       bits=2, x_dtype=_capi.CQ_X_F32, B=17)
+    assert lib.cq_gemv_grouped(ctypes.byref(d), 1, None) == _capi.CQ_ERR_SHAPE
+    assert b"descriptor 0" in lib.cq_last_error()
+    d.B, d.x_dtype = 1, _capi.CQ_X_I8
+    assert lib.cq_gemv_grouped(ctypes.byref(d), 1, None) == _capi.CQ_ERR_ARG  # no scales
+    assert lib.cq_gemv_grouped(ctypes.byref(d), 0, None) == _capi.CQ_ERR_ARG
+    g = _capi.GemmDesc(blob=1, Xq=1, x_scale=None, Y=1, codebook=cb, out=4, in_=128, group=128,
+                       bits=2, M=8)
+    assert lib.cq_gemm_grouped(ctypes.byref(g), 1, None) == _capi.CQ_ERR_ARG
+    assert lib.cq_act_quant_int8(None, 2, 8, None, None, None) == _capi.CQ_ERR_ARG
+
+
+def test_binding_requires_the_library(tmp_path, monkeypatch):
+    """No silent fallback: a missing libcq.so is an ImportError."""
+    from hadamard_rotated_codebook_gb300 import _capi
+    monkeypatch.setattr(_capi, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_capi, "_lib", None)
+    with pytest.raises(ImportError):
+        _capi.load()
