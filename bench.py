@@ -153,14 +153,6 @@ def decode_workload(C, S, device, copies_min_bytes):
                 copies=copies, offs=offs, sizes=sizes, cbs=cbs, out_total=out_total)
 
 
-def time_graph(torch, steps_fn, K, chunk, stream):
-    """Captures `chunk` steps in a CUDA graph; returns (graph, replays)."""
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        steps_fn(chunk)
-    return g
-
-
 def run_cq(args):
     import torch
     import torch.distributed as dist
@@ -213,7 +205,8 @@ def run_cq(args):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         steps(chunk)
-    g.replay()  # upload the graph (untimed)
+    with torch.cuda.stream(stream):
+        g.replay()  # upload the graph (untimed)
     stream.synchronize()
 
     gpu_id = f"GPU-{props.uuid}" if hasattr(props, "uuid") else str(local)
@@ -222,10 +215,11 @@ def run_cq(args):
     barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(K // chunk):
-        g.replay()
-    ev1.record(stream)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        ev0.record(stream)
+        for _ in range(K // chunk):
+            g.replay()
+        ev1.record(stream)
     torch.cuda.synchronize()
     barrier()
     clocks.stop()
@@ -276,14 +270,16 @@ def run_cq(args):
     ge = torch.cuda.CUDAGraph()
     with torch.cuda.graph(ge, stream=stream):
         e2e_steps(ce)
-    ge.replay()
+    with torch.cuda.stream(stream):
+        ge.replay()
     stream.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(Ke // ce):
-        ge.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(Ke // ce):
+            ge.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
     mse = max_over_ranks(e0.elapsed_time(e1))
     result["e2e"] = {"value": round(world * wl["packed"] * Ke / (mse * 1e-3) / 1e9, 1), "unit": "GB/s",

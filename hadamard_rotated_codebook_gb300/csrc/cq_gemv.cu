@@ -194,6 +194,18 @@ void launch_b(int bmax, const GemvParams &p, size_t smem, int grid, cudaStream_t
 
 int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // Small batches go to the tensor-core kernel (one launch for all of
+    // them); the rest run here.
+    int fast_idx[CQ_MAX_GROUPED], nfast = 0;
+    bool is_fast[CQ_MAX_GROUPED];
+    for (int i = 0; i < n; ++i) {
+        is_fast[i] = gemv_fast_eligible(d[i]);
+        if (is_fast[i]) fast_idx[nfast++] = i;
+    }
+    if (nfast) {
+        int st2 = launch_gemv_fast(d, fast_idx, nfast, stream);
+        if (st2) return st2;
+    }
     // One launch per code width present; each launch walks all descriptors of
     // its width (matrices of other widths contribute no items).
     for (int W = 2; W <= 4; ++W) {
@@ -201,7 +213,7 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
         p.n = 0;
         int bmax = 0, nlut = 0, items = 0, zfloats = 0;
         for (int i = 0; i < n; ++i) {
-            if (width_of(d[i].bits) != W || d[i].out == 0) continue;
+            if (is_fast[i] || width_of(d[i].bits) != W || d[i].out == 0) continue;
             if (d[i].in == 0) {  // empty reduction: the product is zero
                 cudaMemsetAsync(d[i].y, 0, sizeof(float) * d[i].B * d[i].out, st);
                 continue;

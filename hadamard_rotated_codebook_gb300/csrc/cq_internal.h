@@ -49,6 +49,10 @@ int launch_act_quant(const float *X, int M, int in, int8_t *Xq, float *s,
 
 // --------------------------------------------------------------- gemv --
 int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream);
+// Tensor-core GEMV for small batches (cq_gemv_fast.cu): which descriptors it
+// takes, and one launch over the descriptors d[idx[0..n)].
+bool gemv_fast_eligible(const cq_gemv_desc &d);
+int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream);
 
 // --------------------------------------------------------------- gemm --
 int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream);
