@@ -23,8 +23,9 @@
 
 namespace cq {
 
-// Status word written by bounded device waits (see cq_device_status).
-__device__ unsigned int g_cq_device_status = 0;
+// Status word written by this file's bounded device waits (see
+// cq_device_status).
+static __device__ unsigned int g_cq_device_status = 0;
 
 int read_and_clear_device_status(void *stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

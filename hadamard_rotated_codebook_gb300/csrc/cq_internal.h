@@ -54,13 +54,15 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream);
 bool gemv_fast_eligible(const cq_gemv_desc &d);
 int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream);
 
+
 // --------------------------------------------------------------- gemm --
 int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream);
 
 // Number of SMs of the current device (cached).
 int sm_count();
 
-// Device status word shared by kernels with bounded waits.
+// Device status word shared by kernels with bounded waits (defined in
+// cq_gemm.cu; kernels OR a nonzero code into it when a wait gives up).
 int read_and_clear_device_status(void *stream);
 
 }  // namespace cq
