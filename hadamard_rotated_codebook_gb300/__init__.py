@@ -28,7 +28,7 @@ GROUP = 128
 
 __all__ = [
     "cq_levels", "cq_code_width", "cq_codebook_init", "cq_packed_bytes", "cq_encode",
-    "cq_act_quant_int8", "cq_gemv", "cq_gemv_grouped", "cq_gemm", "cq_gemm_grouped",
+    "cq_act_quant_int8", "cq_gemv", "cq_gemv_grouped", "cq_gemm", "cq_gemm_grouped", "cq_gemm_noalloc",
     "cq_device_status", "cq_cact_write", "cq_cact_open", "cq_cact_open_memory", "CactReader",
     "CQError", "library_path", "GROUP",
 ]
@@ -219,6 +219,21 @@ def cq_gemm(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook, Xq: to
     keep = []
     d, Y = _gemm_desc(blob, out, n_in, bits, codebook, Xq, x_scale, Y, group, keep)
     check(_lib().cq_gemm_grouped(ctypes.byref(d), 1, _stream(Xq.device)))
+    return Y
+
+
+def cq_gemm_noalloc(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook, Xq: torch.Tensor,
+                    x_scale: torch.Tensor, Y: torch.Tensor, group: int = GROUP) -> torch.Tensor:
+    """cq_gemm for callers that cannot allocate device memory while they run:
+    the rotated activations live in a fixed array inside the library (at most
+    CQ_GEMM_NOALLOC_MAX_ELEMS = M * in_pad fp16 values). Y must be given.
+    Calls share that array, so calls that overlap on the GPU race."""
+    cb, cbp = _codebook_arg(codebook, bits)
+    if Xq.dim() != 2 or Xq.shape[1] != n_in or Y.shape != (Xq.shape[0], out):
+        raise ValueError("Xq must be [M, in] and Y [M, out]")
+    check(_lib().cq_gemm_noalloc(_dev_ptr(blob, torch.uint8, "blob"), out, n_in, group, bits, cbp,
+                                 _dev_ptr(Xq, torch.int8, "Xq"), _dev_ptr(x_scale, torch.float32, "x_scale"),
+                                 Xq.shape[0], _dev_ptr(Y, torch.float32, "Y"), _stream(Xq.device)))
     return Y
 
 

@@ -22,6 +22,7 @@ CQ_ERR_CUDA, CQ_ERR_TIMEOUT, CQ_ERR_NOMEM = -5, -6, -7
 CQ_X_F32, CQ_X_I8 = 0, 1
 CQ_GEMV_MAX_BATCH = 16
 CQ_MAX_GROUPED = 256
+CQ_GEMM_NOALLOC_MAX_ELEMS = 2 * 1024 * 1024
 CQ_DTYPE_FP16, CQ_DTYPE_FP32, CQ_DTYPE_CQ, CQ_DTYPE_RAW = 1, 2, 3, 4
 
 ERROR_NAMES = {
@@ -71,6 +72,8 @@ SIGNATURES = {
     "cq_gemm": (c_int, [c_void_p, c_int, c_int, c_int, c_int, P(c_float), c_void_p, c_void_p,
                         c_int, c_void_p, c_void_p]),
     "cq_gemm_grouped": (c_int, [P(GemmDesc), c_int, c_void_p]),
+    "cq_gemm_noalloc": (c_int, [c_void_p, c_int, c_int, c_int, c_int, P(c_float), c_void_p, c_void_p,
+                                c_int, c_void_p, c_void_p]),
     "cq_device_status": (c_int, [c_void_p]),
     "cq_cact_write": (c_int, [c_char_p, P(TensorDesc), c_int, P(c_float), c_uint32]),
     "cq_cact_open": (c_int, [c_char_p, P(c_void_p)]),

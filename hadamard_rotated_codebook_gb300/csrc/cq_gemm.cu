@@ -217,14 +217,18 @@ void *workspace(size_t bytes, int *err) {
 
 }  // namespace
 
-int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream) {
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // Distinct activations are rotated once each into the workspace.
-    std::vector<const int8_t *> xs_ptr;
-    std::vector<size_t> xs_off;
-    std::vector<int> xs_M, xs_in;
+// Distinct activations of a call and where their rotations go in a
+// workspace (each rotated once: M * in_pad fp16, 256-byte aligned).
+struct ActPlan {
+    std::vector<const int8_t *> ptr;
+    std::vector<size_t> off;
+    std::vector<int> M, in;
+    std::vector<int> act_of;  // per descriptor, -1 when it needs no product
     size_t total = 0;
-    std::vector<int> act_of(n, -1);
+};
+
+static void plan_activations(const cq_gemm_desc *d, int n, cudaStream_t st, ActPlan &pl) {
+    pl.act_of.assign(n, -1);
     for (int i = 0; i < n; ++i) {
         if (d[i].M == 0 || d[i].out == 0) continue;
         if (d[i].in == 0) {  // empty reduction: the product is zero
@@ -232,28 +236,41 @@ int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream) {
             continue;
         }
         int a = -1;
-        for (size_t j = 0; j < xs_ptr.size(); ++j)
-            if (xs_ptr[j] == d[i].Xq && xs_in[j] == d[i].in && xs_M[j] == d[i].M) a = (int)j;
+        for (size_t j = 0; j < pl.ptr.size(); ++j)
+            if (pl.ptr[j] == d[i].Xq && pl.in[j] == d[i].in && pl.M[j] == d[i].M) a = (int)j;
         if (a < 0) {
-            a = (int)xs_ptr.size();
-            xs_ptr.push_back(d[i].Xq);
-            xs_M.push_back(d[i].M);
-            xs_in.push_back(d[i].in);
-            xs_off.push_back(total);
-            total += ((size_t)d[i].M * in_padded(d[i].in) * sizeof(__half) + 255) / 256 * 256;
+            a = (int)pl.ptr.size();
+            pl.ptr.push_back(d[i].Xq);
+            pl.M.push_back(d[i].M);
+            pl.in.push_back(d[i].in);
+            pl.off.push_back(pl.total);
+            pl.total += ((size_t)d[i].M * in_padded(d[i].in) * sizeof(__half) + 255) / 256 * 256;
         }
-        act_of[i] = a;
+        pl.act_of[i] = a;
     }
-    if (xs_ptr.empty()) return CQ_OK;
+}
+
+// Rotations into `ws` (at least pl.total bytes), then the products.
+static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, cudaStream_t st);
+
+int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    ActPlan pl;
+    plan_activations(d, n, st, pl);
+    if (pl.ptr.empty()) return CQ_OK;
     int err = CQ_OK;
-    uint8_t *ws = static_cast<uint8_t *>(workspace(total, &err));
+    uint8_t *ws = static_cast<uint8_t *>(workspace(pl.total, &err));
     if (!ws) return err;
-    for (size_t j = 0; j < xs_ptr.size(); ++j) {
-        const int ng = in_padded(xs_in[j]) / kGroup;
-        const long long tasks = (long long)xs_M[j] * ng;
+    return run_gemm(d, n, pl, ws, st);
+}
+
+static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, cudaStream_t st) {
+    for (size_t j = 0; j < pl.ptr.size(); ++j) {
+        const int ng = in_padded(pl.in[j]) / kGroup;
+        const long long tasks = (long long)pl.M[j] * ng;
         const int grid = (int)std::min<long long>((tasks + 7) / 8, (long long)sm_count() * 16);
-        act_rotate_kernel<<<grid, 256, 0, st>>>(xs_ptr[j], xs_M[j], xs_in[j], ng,
-                                                reinterpret_cast<__half *>(ws + xs_off[j]));
+        act_rotate_kernel<<<grid, 256, 0, st>>>(pl.ptr[j], pl.M[j], pl.in[j], ng,
+                                                reinterpret_cast<__half *>(ws + pl.off[j]));
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "act_rotate launch: %s", cudaGetErrorString(e));
@@ -263,12 +280,12 @@ int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream) {
         p.n = 0;
         int nlut = 0, tiles = 0;
         for (int i = 0; i < n; ++i) {
-            if (act_of[i] < 0 || width_of(d[i].bits) != W) continue;
+            if (pl.act_of[i] < 0 || width_of(d[i].bits) != W) continue;
             GemmMat &G = p.m[p.n];
             const int ip = in_padded(d[i].in);
             G.codes = d[i].blob;
             G.norms = reinterpret_cast<const __half *>(d[i].blob + (size_t)d[i].out * ip * W / 8);
-            G.Z = reinterpret_cast<const __half *>(ws + xs_off[act_of[i]]);
+            G.Z = reinterpret_cast<const __half *>(ws + pl.off[pl.act_of[i]]);
             G.xs = d[i].x_scale;
             G.Y = d[i].Y;
             G.out = d[i].out;
@@ -313,4 +330,63 @@ int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream) {
     return CQ_OK;
 }
 
+// ------------------------------------------------- allocation-free GEMM --
+// Some callers cannot allocate device memory while they run: an inference
+// engine that reserves all device memory up front and hands the library only
+// its inputs and outputs, or a host thread that must not touch the CUDA
+// allocator (cudaMalloc synchronises the device and can fail under memory
+// pressure). cq_gemm_noalloc serves them: the rotated activations that
+// cq_gemm keeps in its grown-on-demand workspace live instead in the fixed
+// array below, which every GPU that loads this library holds until the
+// process exits.
+static __device__ __align__(256) __half g_noalloc_scratch[CQ_GEMM_NOALLOC_MAX_ELEMS];
+
+// Device address of the array, looked up once per device (host code cannot
+// use the array's name as a device pointer).
+static void *g_noalloc_ptr[64];
+
 }  // namespace cq
+
+extern "C" int cq_gemm_noalloc(const uint8_t *blob, int out, int in, int group, int bits, const float *codebook,
+                               const int8_t *Xq, const float *x_scale, int M, float *Y, void *stream) {
+    using namespace cq;
+    clear_error();
+    cq_gemm_desc d;
+    d.blob = blob;
+    d.Xq = Xq;
+    d.x_scale = x_scale;
+    d.Y = Y;
+    d.codebook = codebook;
+    d.out = out;
+    d.in = in;
+    d.group = group;
+    d.bits = bits;
+    d.M = M;
+    int st = check_gemm_args(d);
+    if (st) return st;
+    if (M > 0 && in > 0 && (size_t)M * in_padded(in) > (size_t)CQ_GEMM_NOALLOC_MAX_ELEMS)
+        return set_error(CQ_ERR_SHAPE,
+                         "cq_gemm_noalloc: M*in_pad = %lld exceeds the fixed scratch of %d fp16 elements; "
+                         "use cq_gemm or split M",
+                         (long long)M * in_padded(in), (int)CQ_GEMM_NOALLOC_MAX_ELEMS);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return set_error(CQ_ERR_CUDA, "cq_gemm_noalloc: no current CUDA device");
+    }
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return set_error(CQ_ERR_CUDA, "cq_gemm_noalloc: cannot resolve the scratch array: %s",
+                             cudaGetErrorString(e));
+        }
+        g_noalloc_ptr[dev] = ptr;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    ActPlan pl;
+    plan_activations(&d, 1, s, pl);
+    if (pl.ptr.empty()) return CQ_OK;
+    return run_gemm(&d, 1, pl, static_cast<uint8_t *>(g_noalloc_ptr[dev]), s);
+}

@@ -214,6 +214,14 @@ static int check_gemm_desc(const cq_gemm_desc &d, int i) {
     return CQ_OK;
 }
 
+}  // extern "C"
+
+namespace cq {
+int check_gemm_args(const cq_gemm_desc &d) { return check_gemm_desc(d, 0); }
+}  // namespace cq
+
+extern "C" {
+
 int cq_gemm(const uint8_t *blob, int out, int in, int group, int bits, const float *codebook,
             const int8_t *Xq, const float *x_scale, int M, float *Y, void *stream) {
     cq_gemm_desc d;

@@ -57,6 +57,8 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
 
 // --------------------------------------------------------------- gemm --
 int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream);
+// Argument checks of one GEMM descriptor (as cq_gemm does them).
+int check_gemm_args(const cq_gemm_desc &d);
 
 // Number of SMs of the current device (cached).
 int sm_count();

@@ -193,6 +193,38 @@ typedef struct cq_gemm_desc {
  * per distinct activation, one persistent GEMM launch). Errors as cq_gemm. */
 int cq_gemm_grouped(const cq_gemm_desc *descs, int n, void *stream);
 
+/* Largest M * in_pad accepted by cq_gemm_noalloc (fp16 elements of its
+ * fixed scratch array: 4 MiB of device memory per GPU). */
+#define CQ_GEMM_NOALLOC_MAX_ELEMS (2 * 1024 * 1024)
+
+/* cq_gemm without any device allocation.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory while they run -- an engine that reserves
+ * all device memory up front and passes the library only its inputs and
+ * outputs, or a thread that must not enter the CUDA allocator (cudaMalloc
+ * synchronises the device and may fail under memory pressure). cq_gemm keeps
+ * the rotated activations in a workspace it grows with cudaMalloc; this
+ * variant keeps them in a fixed array of CQ_GEMM_NOALLOC_MAX_ELEMS fp16
+ * values compiled into the library, which every GPU that loads the library
+ * holds until the process exits. Arguments, layouts and results are those of
+ * cq_gemm.
+ *  - Sizes: M * in_pad must not exceed CQ_GEMM_NOALLOC_MAX_ELEMS
+ *    (in_pad = in rounded up to 128); larger calls fail with CQ_ERR_SHAPE
+ *    before anything is launched.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - The function allocates nothing: no cudaMalloc, no cudaFree, no
+ *    allocating library call.
+ *  - All calls share the one array. Each call overwrites every element it
+ *    uses before reading it, so nothing needs clearing, but calls whose
+ *    kernels overlap on the GPU (different streams, or several host threads)
+ *    race on the array: serialise them, e.g. on one stream.
+ * Errors: those of cq_gemm, and CQ_ERR_SHAPE for the size limit. */
+int cq_gemm_noalloc(const uint8_t *blob, int out, int in, int group, int bits,
+                    const float *codebook, const int8_t *Xq,
+                    const float *x_scale, int M, float *Y, void *stream);
+
 /* Reads and clears the device-side status word that bounded waits set when
  * they give up (synchronises `stream`). CQ_OK or CQ_ERR_TIMEOUT. */
 int cq_device_status(void *stream);
