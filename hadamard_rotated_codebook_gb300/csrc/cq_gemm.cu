@@ -101,9 +101,6 @@ struct GemmParams {
     GemmMat m[CQ_MAX_GROUPED];
 };
 
-constexpr int kTM = 64, kTN = 64;  // tokens x output rows per CTA tile
-constexpr int kSimtThreads = 256;
-
 template <int W>
 __device__ __forceinline__ uint32_t code_at(const uint32_t *w, int k) {
     const int bit = k * W, word = bit >> 5, off = bit & 31;
@@ -112,16 +109,127 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t *w, int k) {
     return v & ((1u << W) - 1u);
 }
 
-// Reference-quality tile kernel on the CUDA cores with the same operand
-// precision as the tensor-core path (fp16 x fp16 products, fp32 sums).
+// ------------------------------------------------- GEMM on tcgen05/TMEM --
+// One CTA (4 warps) computes a 128 (weight rows) x 128 (tokens) tile of
+// Y^T = W' Z^T per step of a persistent loop: for each group of 128 inputs
+// the threads expand the codes of their row into W' = c[q] * n in fp16 and
+// copy the rotated activations of their token, both into shared memory in the
+// canonical K-major layout with 128-byte swizzle; one thread then issues
+// eight tcgen05.mma.kind::f16 (M=128, N=128, K=16) accumulating in fp32 in
+// tensor memory and commits them to an mbarrier. The epilogue reads the
+// accumulator with tcgen05.ld (warp w owns TMEM lanes 32w..32w+31, i.e. 32
+// weight rows) and stores Y[m][o] * s[m] / sqrt(128), coalesced along o.
+namespace tc {
+
+constexpr int kThreads = 128;
+constexpr int kTileRows = 128;   // MMA M: weight rows
+constexpr int kTileTok = 128;    // MMA N: tokens
+constexpr int kSegBytes = 128 * 128;  // one 64-wide K segment of a 128-row operand
+constexpr int kOpBytes = 2 * kSegBytes;  // a 128-wide K group
+constexpr unsigned kWaitIters = 1u << 24;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Byte offset of 16-byte chunk `j` (0..15, 8 fp16 each) of row `r` in a
+// K-major operand with 128-byte swizzle: two 64-wide K segments of 8-row
+// atoms (1024 B), chunk index XORed with the row inside its atom.
+__device__ __forceinline__ uint32_t sw128_off(int r, int j) {
+    return (uint32_t)((j >> 3) * kSegBytes + (r >> 3) * 1024 + (r & 7) * 128 + (((j & 7) ^ (r & 7)) << 4));
+}
+
+// UMMA shared-memory descriptor: K-major, SWIZZLE_128B, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (both K-major), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; false (and the status word set) if the phase never completed.
+__device__ bool mbar_wait(uint64_t *bar, uint32_t phase, unsigned int *status, unsigned code) {
+    for (unsigned i = 0; i < kWaitIters; ++i)
+        if (mbar_try_wait(bar, phase)) return true;
+    atomicOr(status, code);
+    return false;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%"
+        "19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+
+}  // namespace tc
+
 template <int W>
-__global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const __grid_constant__ GemmParams p) {
-    __shared__ __half Ws[kTN][kGroup + 2];
-    __shared__ __half Zs[kTM][kGroup + 2];
+__global__ void __launch_bounds__(tc::kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = smem;             // W' tile: 128 rows x 128 k fp16, swizzled
+    uint8_t *sB = smem + kOpBytes;  // Z tile: 128 tokens x 128 k fp16, swizzled
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t s_tmem;
     __shared__ float lut_s[16];
-    const int tid = threadIdx.x;
-    const int tx = tid % 16, ty = tid / 16;  // 4x4 outputs per thread
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+    __shared__ int s_abort;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (warp == 0) {  // 128 fp32 accumulator columns for a 128-token tile
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&s_tmem)),
+                     "r"(kTileTok));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
+    }
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        s_abort = 0;
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t idesc = idesc_f16(kTileRows, kTileTok);
+    uint32_t phase = 0;
+
+    for (int tile = blockIdx.x; tile < p.total_tiles && !s_abort; tile += gridDim.x) {
         int lo = 0, hi = p.n - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) / 2;
@@ -130,61 +238,107 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const __grid_co
         }
         const GemmMat &G = p.m[lo];
         const int local = tile - G.tiles_before;
-        const int mt = local % G.m_tiles, nt = local / G.m_tiles;
-        const int m0 = mt * kTM, o0 = nt * kTN;
+        const int m0 = (local % G.m_tiles) * kTileTok, o0 = (local / G.m_tiles) * kTileRows;
         if (tid < 16) lut_s[tid] = p.lut[G.lut][tid];
-        float acc[4][4] = {};
+        __syncthreads();
+        const int o = o0 + tid, m = m0 + tid;  // this thread's weight row and token
         const size_t rowBytes = (size_t)G.ng * 16 * W;
+
         for (int g = 0; g < G.ng; ++g) {
-            __syncthreads();
-            // expand 64 rows x 128 codes: thread -> (row, 32-code quarter)
+            // ---- expand W' for row o ----
             {
-                const int r = tid / 4, qtr = tid % 4, o = o0 + r;
-                uint32_t w[4 * W + 1];
+                uint32_t w[4 * W];
                 float nrm = 0.0f;
                 if (o < G.out) {
-                    const uint32_t *src = reinterpret_cast<const uint32_t *>(G.codes + (size_t)o * rowBytes + (size_t)g * 16 * W);
+                    const uint4 *src = reinterpret_cast<const uint4 *>(G.codes + (size_t)o * rowBytes + (size_t)g * 16 * W);
 #pragma unroll
-                    for (int i = 0; i < 4 * W; ++i) w[i] = src[i];
+                    for (int i = 0; i < W; ++i) {
+                        const uint4 v = __ldg(src + i);
+                        w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
+                    }
                     nrm = __half2float(G.norms[(size_t)o * G.ng + g]);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 4 * W; ++i) w[i] = 0;
                 }
-                w[4 * W] = 0;
-                for (int k = qtr * 32; k < qtr * 32 + 32; ++k)
-                    Ws[r][k] = __float2half_rn(lut_s[code_at<W>(w, k)] * nrm);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    uint32_t h[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half lo16 = __float2half_rn(lut_s[code_at<W>(w, 8 * j + 2 * e)] * nrm);
+                        const __half hi16 = __float2half_rn(lut_s[code_at<W>(w, 8 * j + 2 * e + 1)] * nrm);
+                        h[e] = (uint32_t)__half_as_ushort(lo16) | ((uint32_t)__half_as_ushort(hi16) << 16);
+                    }
+                    *reinterpret_cast<uint4 *>(sA + sw128_off(tid, j)) = make_uint4(h[0], h[1], h[2], h[3]);
+                }
             }
-            for (int i = tid; i < kTM * kGroup; i += kSimtThreads) {
-                const int r = i / kGroup, k = i % kGroup, m = m0 + r;
-                Zs[r][k] = m < G.M ? G.Z[(size_t)m * G.ng * kGroup + (size_t)g * kGroup + k] : __float2half_rn(0.0f);
+            // ---- copy Z for token m ----
+            {
+                const uint4 *zrow = reinterpret_cast<const uint4 *>(G.Z + (size_t)m * G.ng * kGroup + (size_t)g * kGroup);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint4 v = m < G.M ? __ldg(zrow + j) : make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(sB + sw128_off(tid, j)) = v;
+                }
             }
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            fence_before();
             __syncthreads();
-#pragma unroll 4
-            for (int k = 0; k < kGroup; ++k) {
-                float a[4], b[4];
+            if (tid == 0) {
+                fence_after();
+                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) a[i] = __half2float(Zs[ty * 4 + i][k]);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kSegBytes + (kk & 3) * 32;
+                    mma_f16(tmem, sw128_desc(a0 + off), sw128_desc(b0 + off), idesc, (g | kk) != 0);
+                }
+                mma_commit(&bar);
+            }
+            const bool ok = mbar_wait(&bar, phase, &g_cq_device_status, 0x47470001u);
+            phase ^= 1;
+            if (!ok) s_abort = 1;
+            fence_after();
+            __syncthreads();
+            if (s_abort) break;
+        }
+        if (s_abort) break;
+        // ---- epilogue: warp w holds rows o0 + 32w + lane ----
+        {
+            const int orow = o0 + 32 * warp + lane;
+#pragma unroll 1
+            for (int c = 0; c < kTileTok / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * c, v);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) b[j] = __half2float(Ws[tx * 4 + j][k]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int i = 0; i < 32; ++i) {
+                    const int mm = m0 + 32 * c + i;
+                    if (mm < G.M && orow < G.out)
+                        G.Y[(size_t)mm * G.out + orow] = __uint_as_float(v[i]) * __fmul_rn(G.xs[mm], kInvSqrt128);
+                }
             }
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int m = m0 + ty * 4 + i;
-            if (m >= G.M) continue;
-            const float sc = __fmul_rn(G.xs[m], kInvSqrt128);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int o = o0 + tx * 4 + j;
-                if (o < G.out) G.Y[(size_t)m * G.out + o] = acc[i][j] * sc;
-            }
-        }
+        fence_before();
+        __syncthreads();
     }
+    // a timed-out MMA may still be writing: give it one more bounded wait
+    if (s_abort && tid == 0) mbar_wait(&bar, phase ^ 1, &g_cq_device_status, 0x47470002u);
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTileTok));
+    }
+}
+
+template <int W>
+void launch_tc(const GemmParams &p, int grid, size_t smem, cudaStream_t st) {
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(gemm_tc_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attr = true;
+    }
+    gemm_tc_kernel<W><<<grid, tc::kThreads, smem, st>>>(p);
 }
 
 // ------------------------------------------------------------ workspace --
@@ -310,19 +464,20 @@ static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws
                 li = nlut++;
             }
             G.lut = li;
-            G.m_tiles = (G.M + kTM - 1) / kTM;
-            G.n_tiles = (G.out + kTN - 1) / kTN;
+            G.m_tiles = (G.M + tc::kTileTok - 1) / tc::kTileTok;
+            G.n_tiles = (G.out + tc::kTileRows - 1) / tc::kTileRows;
             G.tiles_before = tiles;
             tiles += G.m_tiles * G.n_tiles;
             ++p.n;
         }
         if (!p.n) continue;
         p.total_tiles = tiles;
-        const int grid = std::min(tiles, sm_count() * 4);
+        const size_t smem = 2 * tc::kOpBytes + 1024;
+        const int grid = std::min(tiles, sm_count() * 2);
         switch (W) {
-        case 2: gemm_simt_kernel<2><<<grid, kSimtThreads, 0, st>>>(p); break;
-        case 3: gemm_simt_kernel<3><<<grid, kSimtThreads, 0, st>>>(p); break;
-        case 4: gemm_simt_kernel<4><<<grid, kSimtThreads, 0, st>>>(p); break;
+        case 2: launch_tc<2>(p, grid, smem, st); break;
+        case 3: launch_tc<3>(p, grid, smem, st); break;
+        case 4: launch_tc<4>(p, grid, smem, st); break;
         }
         e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
