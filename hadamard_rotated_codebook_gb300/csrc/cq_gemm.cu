@@ -13,6 +13,7 @@
 // "How the kernel reads it"; "The .cact archive and Cactus Quants", "Keep
 // the quantized views"). Products of two fp16 values are exact in fp32 and
 // accumulate in fp32.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -46,42 +47,103 @@ namespace {
 constexpr float kInvSqrt128 = 0.08838834764831845f;
 
 // ---------------------------------------------------------- act rotate --
-// One warp per (token, group): Z[m][g*128 + k] = fp16((H0 q)[k]).
-__global__ void act_rotate_kernel(const int8_t *__restrict__ Xq, int M, int in, int ng,
-                                  __half *__restrict__ Z) {
+// Z[m][g*128 + k] = fp16((H0 q)[k]): the exact integer transform of each
+// 128-group of the int8 row, rounded once to fp16.
+// One warp task is (token, four consecutive groups): lane l holds the 16
+// consecutive elements of group 4*quad + l/8 at positions 16*(l%8) .. +15.
+// The 128-point Sylvester butterfly runs over index bits 0-3 in registers and
+// over bits 4-6 across lanes l^1, l^2, l^4 (all inside one 8-lane segment).
+// All distinct activations of a call go in one launch: task t belongs to the
+// activation whose task range holds it. Each warp keeps two tasks' loads in
+// flight.
+constexpr int kMaxRot = 256;
+struct RotTable {
+    int n;
+    long long task_before[kMaxRot + 1];
+    const int8_t *x[kMaxRot];
+    __half *z[kMaxRot];
+    int M[kMaxRot], in[kMaxRot];
+};
+
+struct RotSlot {
+    uint4 raw;     // 16 int8 values
+    __half *dst;   // where this lane's 16 outputs go, or null
+};
+
+__device__ __forceinline__ RotSlot rot_load(const RotTable &r, long long task, long long total, int lane) {
+    RotSlot sl;
+    sl.raw = make_uint4(0, 0, 0, 0);
+    sl.dst = nullptr;
+    if (task >= total) return sl;
+    int lo = 0, hi = r.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (r.task_before[mid] <= task) lo = mid;
+        else hi = mid - 1;
+    }
+    const int in = r.in[lo], ng = (in + kGroup - 1) / kGroup, nq = (ng + 3) / 4;
+    const long long local = task - r.task_before[lo];
+    const long long m = local / nq;
+    const int g = 4 * (int)(local - m * nq) + (lane >> 3);
+    if (g >= ng) return sl;
+    const int col0 = g * kGroup + 16 * (lane & 7);
+    const int8_t *src = r.x[lo] + m * in + col0;
+    if (col0 + 16 <= in && !(reinterpret_cast<uintptr_t>(src) & 15)) {
+        sl.raw = __ldg(reinterpret_cast<const uint4 *>(src));
+    } else {
+        uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (col0 + i < in) w[i >> 2] |= (uint32_t)(uint8_t)src[i] << (8 * (i & 3));
+        sl.raw = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    sl.dst = r.z[lo] + m * (long long)ng * kGroup + col0;
+    return sl;
+}
+
+__device__ __forceinline__ void rot_finish(const RotSlot &sl, int lane) {
+    const uint32_t w[4] = {sl.raw.x, sl.raw.y, sl.raw.z, sl.raw.w};
+    int v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = (int)(int8_t)(uint8_t)(w[k >> 2] >> (8 * (k & 3)));
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            if (!(k & h)) {
+                const int a = v[k], b = v[k + h];
+                v[k] = a + b;
+                v[k + h] = a - b;
+            }
+#pragma unroll
+    for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int o = __shfl_xor_sync(0xffffffffu, v[k], s);
+            v[k] = (lane & s) ? o - v[k] : v[k] + o;
+        }
+    if (!sl.dst) return;
+    uint32_t h2[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const __half2 t = __halves2half2(__int2half_rn(v[2 * k]), __int2half_rn(v[2 * k + 1]));
+        h2[k] = *reinterpret_cast<const uint32_t *>(&t);
+    }
+    uint4 *d = reinterpret_cast<uint4 *>(sl.dst);
+    d[0] = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+    d[1] = make_uint4(h2[4], h2[5], h2[6], h2[7]);
+}
+
+__global__ void __launch_bounds__(256, 4) act_rotate_many_kernel(const __grid_constant__ RotTable r) {
     const int lane = threadIdx.x & 31;
     const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-    for (long long task = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-         task < (long long)M * ng; task += warps) {
-        const long long m = task / ng;
-        const int g = (int)(task - m * ng);
-        int v[4];
-        const int col0 = g * kGroup + 4 * lane;
-        if (col0 + 3 < in && !(((uintptr_t)(Xq + m * in + col0)) & 3)) {
-            const char4 c = *reinterpret_cast<const char4 *>(Xq + m * in + col0);
-            v[0] = c.x;
-            v[1] = c.y;
-            v[2] = c.z;
-            v[3] = c.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = col0 + i < in ? (int)Xq[m * in + col0 + i] : 0;
-        }
-        int a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
-        v[0] = a0 + a2;
-        v[1] = a1 + a3;
-        v[2] = a0 - a2;
-        v[3] = a1 - a3;
-#pragma unroll
-        for (int s = 1; s < 32; s <<= 1)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int o = __shfl_xor_sync(0xffffffffu, v[i], s);
-                v[i] = (lane & s) ? o - v[i] : v[i] + o;
-            }
-        __half2 *dst = reinterpret_cast<__half2 *>(Z + m * (long long)ng * kGroup + col0);
-        dst[0] = __halves2half2(__int2half_rn(v[0]), __int2half_rn(v[1]));
-        dst[1] = __halves2half2(__int2half_rn(v[2]), __int2half_rn(v[3]));
+    const long long total = r.task_before[r.n];
+    for (long long task = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < total;
+         task += 2 * warps) {
+        const RotSlot a = rot_load(r, task, total, lane);
+        const RotSlot b = rot_load(r, task + warps, total, lane);
+        rot_finish(a, lane);
+        rot_finish(b, lane);
     }
 }
 
@@ -126,7 +188,7 @@ constexpr int kTileRows = 128;   // MMA M: weight rows
 constexpr int kTileTok = 128;    // MMA N: tokens
 constexpr int kSegBytes = 128 * 128;  // one 64-wide K segment of a 128-row operand
 constexpr int kOpBytes = 2 * kSegBytes;  // a 128-wide K group
-constexpr unsigned kWaitIters = 1u << 24;
+constexpr unsigned kWaitIters = 1u << 22;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -153,12 +215,16 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
 
+// Test for completion of the phase with parity `phase`; a thread whose phase
+// is not complete is suspended in hardware for up to ~1 us (suspend-time
+// hint) instead of spinning, so waiting warps leave the issue slots to the
+// warps that work.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(phase)
+        : "r"(smem_u32(bar)), "r"(phase), "r"(1000u)
         : "memory");
     return ok != 0;
 }
@@ -341,6 +407,364 @@ void launch_tc(const GemmParams &p, int grid, size_t smem, cudaStream_t st) {
     gemm_tc_kernel<W><<<grid, tc::kThreads, smem, st>>>(p);
 }
 
+// ------------------------------- pipelined GEMM for inputs up to 512 wide --
+// Persistent, one CTA per SM, warp-specialised:
+//   warp 0      TMA producer: rotated activations, one 128-token x 128-input
+//               stage (two 2-D TMA boxes of 64 inputs, 128-byte swizzle, rows
+//               past M zero-filled) per (token tile, group), 2-stage ring
+//   warp 1      MMA issuer: 8 x tcgen05.mma (M=128, N=128, K=16) per stage
+//               into one of two TMEM accumulators
+//   warps 2-5   epilogue: tcgen05.ld of an accumulator while the MMAs fill
+//               the other; Y[m][o] = D * s[m]/sqrt(128)
+//   warps 6-9   expand the 128 weight rows of a work item (all groups, up to
+//               4 x 32 KB) into W' = c[q]*n once; the item then streams up to
+//               8 token tiles against them
+// Hand-offs are mbarriers: a_full/a_empty (weights), b_full/b_empty (stages),
+// acc_full/acc_empty (accumulators). Every wait is bounded; on expiry the
+// status word records where, all roles drain, and TMEM is released.
+namespace tc2 {
+
+constexpr int kThreads = 320;
+constexpr int kTPI = 8;          // token tiles per work item
+constexpr int kMaxActs = 64;     // distinct activations (tensor maps) per launch
+constexpr int kMaxNg = 4;        // groups of the inputs kept resident
+constexpr int kStageBytes = 2 * tc::kSegBytes;  // 128 tokens x 128 inputs fp16
+constexpr unsigned kSpin = 1u << 22;  // polls of one barrier (each may suspend ~1 us)
+
+struct Mat {
+    const uint8_t *codes;
+    const __half *norms;
+    const float *xs;
+    float *Y;
+    int out, ng, M, lut, act, n_tiles, m_tiles, chunks, items_before;
+};
+
+struct Params {
+    CUtensorMap tmap[kMaxActs];  // one per distinct rotated activation
+    float lut[kMaxLuts][16];
+    int n, total_items, ng_max;
+    Mat m[CQ_MAX_GROUPED];
+};
+
+struct Item {
+    int mat, o0, t0, t1;
+};
+
+__device__ __forceinline__ Item decode_item(const Params &p, int item) {
+    int lo = 0, hi = p.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (p.m[mid].items_before <= item) lo = mid;
+        else hi = mid - 1;
+    }
+    const Mat &G = p.m[lo];
+    const int local = item - G.items_before;
+    Item it;
+    it.mat = lo;
+    it.o0 = (local / G.chunks) * tc::kTileRows;
+    it.t0 = (local % G.chunks) * kTPI;
+    it.t1 = min(G.m_tiles, it.t0 + kTPI);
+    return it;
+}
+
+// Copies matrix `mi` of the parameter block into `dst` with the lanes of the
+// calling warp (all 32 must call) and returns it.
+__device__ __forceinline__ const Mat &warp_mat(const Params &p, int mi, Mat *dst) {
+    static_assert(sizeof(Mat) % 4 == 0 && sizeof(Mat) / 4 <= 32, "descriptor copy");
+    const int lane = threadIdx.x & 31;
+    __syncwarp();
+    if (lane < (int)(sizeof(Mat) / 4))
+        reinterpret_cast<uint32_t *>(dst)[lane] = reinterpret_cast<const uint32_t *>(&p.m[mi])[lane];
+    __syncwarp();
+    return *dst;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(tc::smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+            tc::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
+        : "memory");
+}
+
+// Bounded wait for the phase of `bar` with parity `parity`; gives up when
+// another role aborted or after kSpin polls (then records `code`).
+__device__ bool wait(uint64_t *bar, uint32_t parity, volatile int *abort, unsigned code) {
+    for (unsigned i = 0;; ++i) {
+        if (tc::mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && *abort) return false;
+        if (i >= kSpin) {
+            atomicOr(&g_cq_device_status, code);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+}  // namespace tc2
+
+template <int W>
+__global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid_constant__ tc2::Params p) {
+    using namespace tc;
+    using tc2::Item;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *sA = smem;                                // ng_max x 32 KB of W'
+    uint8_t *sB = smem + (size_t)p.ng_max * kOpBytes;  // 2 stages x 32 KB of Z
+    __shared__ __align__(8) uint64_t a_full, a_empty, b_full[2], b_empty[2], acc_full[2], acc_empty[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+    __shared__ float s_lut[4][16];
+    __shared__ tc2::Mat s_mat[10];  // per warp: the current item's matrix (parameter reads
+                                    // with a runtime index stay out of the loops)
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (warp == 0) {  // two 128-column fp32 accumulators
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&s_tmem)),
+                     "r"(256));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
+    }
+    if (tid == 0) {
+        mbar_init(&a_full, 4);
+        mbar_init(&a_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        s_abort = 0;
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            uint32_t s = 0, pe = 3u;  // empty-phase parity of stage s in bit s
+            for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
+                const Item it = tc2::decode_item(p, item);
+                const int ng = p.m[it.mat].ng;
+                const CUtensorMap *map = &p.tmap[p.m[it.mat].act];
+                for (int t = it.t0; t < it.t1; ++t)
+                    for (int g = 0; g < ng; ++g) {
+                        if (!tc2::wait(&b_empty[s], (pe >> s) & 1u, &s_abort, 0x47480001u)) goto done_prod;
+                        pe ^= 1u << s;
+                        tc2::mbar_expect_tx(&b_full[s], tc2::kStageBytes);
+                        tc2::tma_load_2d(sB + s * tc2::kStageBytes, map, g * kGroup, t * kTileTok, &b_full[s]);
+                        tc2::tma_load_2d(sB + s * tc2::kStageBytes + kSegBytes, map, g * kGroup + 64, t * kTileTok,
+                                         &b_full[s]);
+                        s ^= 1;
+                    }
+            }
+        done_prod:;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(kTileRows, kTileTok);
+            // parities in bit i: stage full (pf), accumulator empty (pae)
+            uint32_t s = 0, pf = 0u, pae = 3u, paf = 0;
+            int acc = 0;
+            for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
+                const Item it = tc2::decode_item(p, item);
+                const int ng = p.m[it.mat].ng;
+                if (!tc2::wait(&a_full, paf, &s_abort, 0x47480002u)) break;
+                paf ^= 1;
+                for (int t = it.t0; t < it.t1; ++t, ++acc) {
+                    const int a = acc & 1;
+                    if (!tc2::wait(&acc_empty[a], (pae >> a) & 1u, &s_abort, 0x47480003u)) goto done_mma;
+                    pae ^= 1u << a;
+                    fence_after();
+                    for (int g = 0; g < ng; ++g) {
+                        if (!tc2::wait(&b_full[s], (pf >> s) & 1u, &s_abort, 0x47480004u)) goto done_mma;
+                        pf ^= 1u << s;
+                        fence_after();
+                        const uint32_t a0 = smem_u32(sA + g * kOpBytes), b0 = smem_u32(sB + s * tc2::kStageBytes);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t off = (kk >> 2) * kSegBytes + (kk & 3) * 32;
+                            mma_f16(tmem + a * kTileTok, sw128_desc(a0 + off), sw128_desc(b0 + off), idesc,
+                                    (g | kk) != 0);
+                        }
+                        mma_commit(&b_empty[s]);
+                        s ^= 1;
+                    }
+                    mma_commit(&acc_full[a]);
+                }
+                mma_commit(&a_empty);
+            }
+        done_mma:;
+        }
+    } else if (warp < 6) {
+        // --------------------------------------------------- epilogue --
+        const int q = warp & 3;  // TMEM lane quarter of this warp
+        uint32_t pfa = 0u;  // accumulator-full parity of buffer a in bit a
+        int acc = 0;
+        for (int item = blockIdx.x; item < p.total_items && !s_abort; item += gridDim.x) {
+            const Item it = tc2::decode_item(p, item);
+            const tc2::Mat &G = tc2::warp_mat(p, it.mat, &s_mat[warp]);
+            const int out = G.out, Mtok = G.M;
+            const float *xs = G.xs;
+            float *Y = G.Y;
+            const int o = it.o0 + 32 * q + lane;
+            for (int t = it.t0; t < it.t1; ++t, ++acc) {
+                const int a = acc & 1;
+                if (!tc2::wait(&acc_full[a], (pfa >> a) & 1u, &s_abort, 0x47480005u)) break;
+                pfa ^= 1u << a;
+                fence_after();
+                const bool ocol = o < out;
+#pragma unroll 1
+                for (int c = 0; c < kTileTok / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + a * kTileTok + 32 * c + ((uint32_t)(32 * q) << 16), v);
+                    const int mbase = t * kTileTok + 32 * c;
+                    float *yb = Y + (size_t)mbase * out + o;
+                    if (mbase + 32 <= Mtok) {
+                        // the chunk's 32 token scales, the same for every lane
+                        const float4 *s4 = reinterpret_cast<const float4 *>(xs + mbase);
+                        float sc[32];
+                        if ((reinterpret_cast<uintptr_t>(xs + mbase) & 15) == 0) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float4 f = __ldg(s4 + i);
+                                sc[4 * i] = f.x, sc[4 * i + 1] = f.y, sc[4 * i + 2] = f.z, sc[4 * i + 3] = f.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) sc[i] = __ldg(xs + mbase + i);
+                        }
+                        if (ocol) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                yb[(size_t)i * out] = __uint_as_float(v[i]) * __fmul_rn(sc[i], kInvSqrt128);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (ocol && mbase + i < Mtok)
+                                yb[(size_t)i * out] = __uint_as_float(v[i]) * __fmul_rn(__ldg(xs + mbase + i), kInvSqrt128);
+                    }
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) tc2::mbar_arrive(&acc_empty[a]);
+            }
+        }
+    } else {
+        // ------------------------------------------ weight expansion --
+        const int et = tid - 192;  // 0..127: weight row of the item
+        uint32_t pe = 1;
+        for (int item = blockIdx.x; item < p.total_items && !s_abort; item += gridDim.x) {
+            const Item it = tc2::decode_item(p, item);
+            const tc2::Mat &G = tc2::warp_mat(p, it.mat, &s_mat[warp]);
+            if (!tc2::wait(&a_empty, pe, &s_abort, 0x47480006u)) break;
+            pe ^= 1;
+            // level table in warp-private shared memory (indexed by code)
+            if (lane < 16) s_lut[warp - 6][lane] = p.lut[G.lut][lane];
+            __syncwarp();
+            const float *lut = s_lut[warp - 6];
+            const int o = it.o0 + et;
+            const size_t rowBytes = (size_t)G.ng * 16 * W;
+            for (int g = 0; g < G.ng; ++g) {
+                uint32_t w[4 * W];
+                float nrm = 0.0f;
+                if (o < G.out) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(G.codes + (size_t)o * rowBytes + (size_t)g * 16 * W);
+#pragma unroll
+                    for (int i = 0; i < W; ++i) {
+                        const uint4 v = __ldg(src + i);
+                        w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
+                    }
+                    nrm = __half2float(G.norms[(size_t)o * G.ng + g]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4 * W; ++i) w[i] = 0;
+                }
+                uint8_t *dst = sA + g * kOpBytes;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    uint32_t h[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half lo16 = __float2half_rn(lut[code_at<W>(w, 8 * j + 2 * e)] * nrm);
+                        const __half hi16 = __float2half_rn(lut[code_at<W>(w, 8 * j + 2 * e + 1)] * nrm);
+                        h[e] = (uint32_t)__half_as_ushort(lo16) | ((uint32_t)__half_as_ushort(hi16) << 16);
+                    }
+                    *reinterpret_cast<uint4 *>(dst + sw128_off(et, j)) = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            __syncwarp();
+            if (lane == 0) tc2::mbar_arrive(&a_full);
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(256));
+    }
+}
+
+// Dynamic shared memory of the pipelined kernel: 4 x 32 KB of W', 2 x 32 KB
+// of activation stages, 1 KB of alignment slack.
+constexpr int kTc2MaxSmem = tc2::kMaxNg * tc::kOpBytes + 2 * tc2::kStageBytes + 1024;
+
+template <int W>
+int launch_tc2(const tc2::Params &p, size_t smem, cudaStream_t st) {
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   kTc2MaxSmem);
+        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm smem attribute: %s", cudaGetErrorString(e));
+        attr = true;
+    }
+    const int grid = std::min(p.total_items, sm_count());
+    gemm_tc2_kernel<W><<<grid, tc2::kThreads, smem, st>>>(p);
+    return CQ_OK;
+}
+
+// 2-D tensor map over one rotated activation Z[M][in_pad] (fp16): boxes of
+// 64 inputs x 128 tokens, 128-byte swizzle, zero fill past M.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static int make_z_map(CUtensorMap *map, const void *Z, int M, int in_pad) {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !f) {
+            cudaGetLastError();
+            return set_error(CQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+        }
+        fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)in_pad, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)in_pad * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)tc::kTileTok};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(Z), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(CQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return CQ_OK;
+}
+
 // ------------------------------------------------------------ workspace --
 struct Workspace {
     void *ptr = nullptr;
@@ -418,23 +842,122 @@ int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream) {
     return run_gemm(d, n, pl, ws, st);
 }
 
+// Level table of one descriptor (ternary crumbs sign-extend).
+static void level_table(const cq_gemm_desc &d, float lut[16]) {
+    for (int j = 0; j < 16; ++j) lut[j] = 0.0f;
+    if (d.bits == 5) {
+        const float c = d.codebook[2];
+        lut[1] = c;
+        lut[2] = -2.0f * c;
+        lut[3] = -c;
+    } else {
+        for (int j = 0; j < levels_of(d.bits); ++j) lut[j] = d.codebook[j];
+    }
+}
+
+// The pipelined kernel over every descriptor of code width W whose input is
+// at most 512 wide; launches as often as its parameter block fills.
+static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, int W, cudaStream_t st) {
+    static tc2::Params p;
+    std::vector<int> map_of(pl.ptr.size(), -1);
+    int nmaps = 0, nlut = 0, items = 0, ngmax = 0;
+    p.n = 0;
+    auto flush = [&]() -> int {
+        if (!p.n) return CQ_OK;
+        p.total_items = items;
+        p.ng_max = ngmax;
+        const size_t smem = (size_t)ngmax * tc::kOpBytes + 2 * tc2::kStageBytes + 1024;
+        int rc = CQ_OK;
+        switch (W) {
+        case 2: rc = launch_tc2<2>(p, smem, st); break;
+        case 3: rc = launch_tc2<3>(p, smem, st); break;
+        case 4: rc = launch_tc2<4>(p, smem, st); break;
+        }
+        if (rc) return rc;
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
+        p.n = 0;
+        nmaps = nlut = items = ngmax = 0;
+        std::fill(map_of.begin(), map_of.end(), -1);
+        return CQ_OK;
+    };
+    for (int i = 0; i < n; ++i) {
+        if (pl.act_of[i] < 0 || width_of(d[i].bits) != W) continue;
+        const int ip = in_padded(d[i].in), ng = ip / kGroup;
+        if (ng > tc2::kMaxNg) continue;
+        const int a = pl.act_of[i];
+        float lut[16];
+        level_table(d[i], lut);
+        int li = -1;
+        for (int j = 0; j < nlut; ++j)
+            if (std::equal(lut, lut + 16, p.lut[j])) li = j;
+        const bool need_map = map_of[a] < 0;
+        if (p.n == CQ_MAX_GROUPED || (need_map && nmaps == tc2::kMaxActs) || (li < 0 && nlut == kMaxLuts)) {
+            const int e = flush();
+            if (e) return e;
+            li = -1;
+        }
+        if (map_of[a] < 0) {
+            const int e = make_z_map(&p.tmap[nmaps], ws + pl.off[a], pl.M[a], ip);
+            if (e) return e;
+            map_of[a] = nmaps++;
+        }
+        if (li < 0) {
+            std::copy(lut, lut + 16, p.lut[nlut]);
+            li = nlut++;
+        }
+        tc2::Mat &G = p.m[p.n];
+        G.codes = d[i].blob;
+        G.norms = reinterpret_cast<const __half *>(d[i].blob + (size_t)d[i].out * ip * W / 8);
+        G.xs = d[i].x_scale;
+        G.Y = d[i].Y;
+        G.out = d[i].out;
+        G.ng = ng;
+        G.M = d[i].M;
+        G.lut = li;
+        G.act = map_of[a];
+        G.n_tiles = (G.out + tc::kTileRows - 1) / tc::kTileRows;
+        G.m_tiles = (G.M + tc::kTileTok - 1) / tc::kTileTok;
+        G.chunks = (G.m_tiles + tc2::kTPI - 1) / tc2::kTPI;
+        G.items_before = items;
+        items += G.n_tiles * G.chunks;
+        ngmax = std::max(ngmax, ng);
+        ++p.n;
+    }
+    return flush();
+}
+
 static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, cudaStream_t st) {
-    for (size_t j = 0; j < pl.ptr.size(); ++j) {
-        const int ng = in_padded(pl.in[j]) / kGroup;
-        const long long tasks = (long long)pl.M[j] * ng;
-        const int grid = (int)std::min<long long>((tasks + 7) / 8, (long long)sm_count() * 16);
-        act_rotate_kernel<<<grid, 256, 0, st>>>(pl.ptr[j], pl.M[j], pl.in[j], ng,
-                                                reinterpret_cast<__half *>(ws + pl.off[j]));
+    // every distinct activation rotated in one launch
+    {
+        static RotTable rt;
+        rt.n = 0;
+        rt.task_before[0] = 0;
+        for (size_t j = 0; j < pl.ptr.size(); ++j) {
+            const int k = rt.n++;
+            rt.x[k] = pl.ptr[j];
+            rt.z[k] = reinterpret_cast<__half *>(ws + pl.off[j]);
+            rt.M[k] = pl.M[j];
+            rt.in[k] = pl.in[j];
+            const int ng = in_padded(pl.in[j]) / kGroup;
+            rt.task_before[k + 1] = rt.task_before[k] + (long long)pl.M[j] * ((ng + 3) / 4);
+        }
+        const long long tasks = rt.task_before[rt.n];
+        const int grid = (int)std::min<long long>((tasks + 15) / 16, (long long)sm_count() * 4);
+        act_rotate_many_kernel<<<grid, 256, 0, st>>>(rt);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "act_rotate launch: %s", cudaGetErrorString(e));
 
     for (int W = 2; W <= 4; ++W) {
+        const int e2 = run_gemm_pipelined(d, n, pl, ws, W, st);
+        if (e2) return e2;
         static GemmParams p;
         p.n = 0;
         int nlut = 0, tiles = 0;
         for (int i = 0; i < n; ++i) {
             if (pl.act_of[i] < 0 || width_of(d[i].bits) != W) continue;
+            if (in_padded(d[i].in) / kGroup <= tc2::kMaxNg) continue;  // taken by the pipelined kernel
             GemmMat &G = p.m[p.n];
             const int ip = in_padded(d[i].in);
             G.codes = d[i].blob;
