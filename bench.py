@@ -182,6 +182,20 @@ def run_cq(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
+    if args.only in ("gemm", "encode"):
+        # one part alone, for profiling: only that part's buffers are held
+        stream = torch.cuda.Stream(device)
+        if args.only == "gemm":
+            wl = decode_workload(C, S, device, 0)
+            res = bench_gemm(C, S, torch, wl, device, stream, peaks, peak_kind, barrier, max_over_ranks, world)
+        else:
+            res = bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
     wl = decode_workload(C, S, device, 4 * l2)
     plans, R = wl["plans"], wl["R"]
     K, Wm = args.steps, args.warmup
@@ -452,6 +466,8 @@ def main():
     ap.add_argument("--impl", default="cq", choices=["cq", "reference"])
     ap.add_argument("--skip-extra", action="store_true", help="decode step only")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--only", default="all", choices=["all", "gemm", "encode"],
+                    help="time one secondary part alone and print its JSON object (profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:

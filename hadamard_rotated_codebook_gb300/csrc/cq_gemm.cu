@@ -205,6 +205,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            (2ull << 61);
 }
 
+// The same for a K-major operand with 64-byte swizzle (32-wide K rows of
+// 64 B, 8-row groups 512 B apart).
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(512 >> 4) << 32) | (1ull << 46) |
+           (4ull << 61);
+}
+
 // Instruction descriptor, kind::f16: fp16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -225,6 +232,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(phase), "r"(1000u)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking test for completion of the phase with parity `phase`.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(phase)
         : "memory");
     return ok != 0;
 }
@@ -425,47 +443,132 @@ void launch_tc(const GemmParams &p, int grid, size_t smem, cudaStream_t st) {
 namespace tc2 {
 
 constexpr int kThreads = 320;
-constexpr int kTPI = 8;          // token tiles per work item
 constexpr int kMaxActs = 64;     // distinct activations (tensor maps) per launch
 constexpr int kMaxNg = 4;        // groups of the inputs kept resident
-constexpr int kStageBytes = 2 * tc::kSegBytes;  // 128 tokens x 128 inputs fp16
+constexpr int kTok = 256;        // MMA N: tokens of a tile
+constexpr int kStages = 5;       // activation stages
+constexpr int kStageK = 32;      // inputs per stage (two K=16 MMAs)
+constexpr int kStageBytes = kTok * kStageK * 2;  // 256 tokens x 32 inputs fp16, 64-byte swizzle
 constexpr unsigned kSpin = 1u << 22;  // polls of one barrier (each may suspend ~1 us)
+constexpr unsigned kDrainSpin = 1u << 20;
 
 struct Mat {
     const uint8_t *codes;
     const __half *norms;
     const float *xs;
     float *Y;
-    int out, ng, M, lut, act, n_tiles, m_tiles, chunks, items_before;
+    int out, ng, M, lut, act, n_tiles, m_tiles, tiles_before, runs_before;
 };
 
 struct Params {
     CUtensorMap tmap[kMaxActs];  // one per distinct rotated activation
     float lut[kMaxLuts][16];
-    int n, total_items, ng_max;
+    int n, total_tiles, ng_max;
+    int full_rounds, tail_T0;    // schedule (see Cursor)
     Mat m[CQ_MAX_GROUPED];
 };
 
-struct Item {
-    int mat, o0, t0, t1;
+// Output tiles are 128 rows x 256 tokens. Tiles are numbered matrix by
+// matrix (matrices that share an activation are adjacent), weight-row tile by
+// weight-row tile, token tile fastest; the tiles of one (matrix, row tile)
+// form a run. The schedule works in rounds: in round k, CTA b takes the whole
+// run k*G + b (G CTAs), so a CTA reuses the expanded weights W' in shared
+// memory across the run, and the CTAs of a round move through the token tiles
+// of the same activations together, which keeps each activation tile in L2
+// while the row tiles that need it read it. The runs left after the full
+// rounds are split into G equal contiguous ranges of tiles.
+//
+// The per-matrix numbers the schedule needs live in a shared-memory table
+// (parameter reads with a runtime index miss the constant cache).
+struct SchedTab {
+    int4 m[CQ_MAX_GROUPED];          // tiles_before, runs_before, m_tiles, n_tiles
+    uint16_t ngact[CQ_MAX_GROUPED];  // ng | act << 8
 };
 
-__device__ __forceinline__ Item decode_item(const Params &p, int item) {
-    int lo = 0, hi = p.n - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) / 2;
-        if (p.m[mid].items_before <= item) lo = mid;
-        else hi = mid - 1;
+__device__ void load_sched(const Params &p, SchedTab *tab) {
+    for (int i = threadIdx.x; i < p.n; i += blockDim.x) {
+        tab->m[i] = make_int4(p.m[i].tiles_before, p.m[i].runs_before, p.m[i].m_tiles, p.m[i].n_tiles);
+        tab->ngact[i] = (uint16_t)(p.m[i].ng | (p.m[i].act << 8));
     }
-    const Mat &G = p.m[lo];
-    const int local = item - G.items_before;
-    Item it;
-    it.mat = lo;
-    it.o0 = (local / G.chunks) * tc::kTileRows;
-    it.t0 = (local % G.chunks) * kTPI;
-    it.t1 = min(G.m_tiles, it.t0 + kTPI);
-    return it;
 }
+
+// Position in this CTA's sequence of tiles: segment k = [A, B), tile T =
+// token tile t of row tile n of matrix mat. Advancing inside a segment is
+// plain arithmetic; only a new segment searches the table.
+struct Cursor {
+    int k, A, B, T, mat, n, t, mt, nt;
+    const SchedTab *tab;
+    int nmat, full_rounds, total_tiles, tail_T0;
+
+    __device__ int ng() const { return tab->ngact[mat] & 0xFF; }
+    __device__ int act() const { return tab->ngact[mat] >> 8; }
+    __device__ int o0() const { return n * tc::kTileRows; }
+    __device__ bool first() const { return T == A || t == 0; }  // run starts here
+    __device__ bool last() const { return T + 1 == B || t + 1 == mt; }  // run ends here
+    __device__ void set_mat(int m) {
+        mat = m;
+        mt = tab->m[m].z;
+        nt = tab->m[m].w;
+    }
+    // the matrix whose range of field f (0 tiles, 1 runs) holds v
+    __device__ int find(int v, int f) const {
+        int lo = 0, hi = nmat - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) / 2;
+            const int4 e = tab->m[mid];
+            if ((f ? e.y : e.x) <= v) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    }
+    __device__ bool segment(int kk) {
+        for (k = kk; k <= full_rounds; ++k) {
+            if (k < full_rounds) {
+                const int r = k * (int)gridDim.x + (int)blockIdx.x;
+                set_mat(find(r, 1));
+                n = r - tab->m[mat].y;
+                t = 0;
+                A = T = tab->m[mat].x + n * mt;
+                B = A + mt;
+                return true;
+            }
+            const long long len = total_tiles - tail_T0;
+            A = tail_T0 + (int)(blockIdx.x * len / gridDim.x);
+            B = tail_T0 + (int)((blockIdx.x + 1) * len / gridDim.x);
+            if (A < B) {
+                T = A;
+                set_mat(find(T, 0));
+                const int local = T - tab->m[mat].x;
+                n = local / mt;
+                t = local - n * mt;
+                return true;
+            }
+        }
+        return false;
+    }
+    __device__ bool begin(const Params &p, const SchedTab *s) {
+        tab = s;
+        nmat = p.n;
+        full_rounds = p.full_rounds;
+        total_tiles = p.total_tiles;
+        tail_T0 = p.tail_T0;
+        return segment(0);
+    }
+    __device__ bool advance() {
+        if (T + 1 < B) {
+            ++T;
+            if (++t == mt) {
+                t = 0;
+                if (++n == nt) {
+                    n = 0;
+                    set_mat(mat + 1);
+                }
+            }
+            return true;
+        }
+        return segment(k + 1);
+    }
+};
 
 // Copies matrix `mi` of the parameter block into `dst` with the lanes of the
 // calling warp (all 32 must call) and returns it.
@@ -493,10 +596,20 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
         : "memory");
 }
+// 4-byte asynchronous copy global -> shared; `valid` false zero-fills.
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(tc::smem_u32(dst)), "l"(src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
 // Bounded wait for the phase of `bar` with parity `parity`; gives up when
 // another role aborted or after kSpin polls (then records `code`).
 __device__ bool wait(uint64_t *bar, uint32_t parity, volatile int *abort, unsigned code) {
+    if (tc::mbar_test(bar, parity)) return true;  // fast path, cheaper than a suspending poll
     for (unsigned i = 0;; ++i) {
         if (tc::mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 255u && *abort) return false;
@@ -508,38 +621,66 @@ __device__ bool wait(uint64_t *bar, uint32_t parity, volatile int *abort, unsign
     }
 }
 
+// After an abort: waits (bounded, without regard to the abort flag) for a
+// phase that asynchronous work already in flight will complete.
+__device__ void drain_wait(uint64_t *bar, uint32_t parity) {
+    for (unsigned i = 0; i < kDrainSpin; ++i)
+        if (tc::mbar_try_wait(bar, parity)) return;
+}
+
 }  // namespace tc2
 
+// Pipelined, warp-specialised GEMM for inputs of at most 512 (ng <= 4
+// groups): the 128 x (128 ng) slice of W' stays in shared memory for the
+// whole run of token tiles that use it.
+//   warp 0     TMA producer: Z tiles (256 tokens x 32 inputs) into five stages
+//   warp 1     MMA issuer: tcgen05.mma (M=128, N=256) into two 256-column
+//              TMEM accumulators
+//   warps 2-5  epilogue: TMEM -> registers, token scale, fp32 stores of Y
+//   warps 6-9  expansion of the next run's codes and norms into fp16 W',
+//              one group at a time, as soon as the MMAs of the previous run
+//              are done with that group
+// Every wait is bounded; a role that gives up sets the abort flag, the others
+// leave their loops, and work already issued (TMA loads, MMAs) is waited for
+// before TMEM is freed.
 template <int W>
 __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid_constant__ tc2::Params p) {
     using namespace tc;
-    using tc2::Item;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;                                // ng_max x 32 KB of W'
-    uint8_t *sB = smem + (size_t)p.ng_max * kOpBytes;  // 2 stages x 32 KB of Z
-    __shared__ __align__(8) uint64_t a_full, a_empty, b_full[2], b_empty[2], acc_full[2], acc_empty[2];
+    uint8_t *sB = smem + (size_t)p.ng_max * kOpBytes;  // kStages x 16 KB of Z
+    __shared__ __align__(8) uint64_t a_full[tc2::kMaxNg], a_empty[tc2::kMaxNg], b_full[tc2::kStages],
+        b_empty[tc2::kStages], acc_full[2], acc_empty[2], drain;
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     __shared__ float s_lut[4][16];
-    __shared__ tc2::Mat s_mat[10];  // per warp: the current item's matrix (parameter reads
+    __shared__ __align__(16) float s_scale[4][2][tc2::kTok];  // per epilogue warp: token scales of two tiles
+    __shared__ tc2::Mat s_mat[10];  // per warp: the current matrix (parameter reads
                                     // with a runtime index stay out of the loops)
+    __shared__ tc2::SchedTab s_tab;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    tc2::load_sched(p, &s_tab);
 
-    if (warp == 0) {  // two 128-column fp32 accumulators
+    if (warp == 0) {  // two 256-column fp32 accumulators
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&s_tmem)),
-                     "r"(256));
+                     "r"(512));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
     }
     if (tid == 0) {
-        mbar_init(&a_full, 4);
-        mbar_init(&a_empty, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int g = 0; g < tc2::kMaxNg; ++g) {
+            mbar_init(&a_full[g], 4);
+            mbar_init(&a_empty[g], 1);
+        }
+        for (int i = 0; i < tc2::kStages; ++i) {
             mbar_init(&b_full[i], 1);
             mbar_init(&b_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], 4);
         }
+        mbar_init(&drain, 1);
         s_abort = 0;
     }
     fence_before();
@@ -550,146 +691,193 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            uint32_t s = 0, pe = 3u;  // empty-phase parity of stage s in bit s
-            for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
-                const Item it = tc2::decode_item(p, item);
-                const int ng = p.m[it.mat].ng;
-                const CUtensorMap *map = &p.tmap[p.m[it.mat].act];
-                for (int t = it.t0; t < it.t1; ++t)
-                    for (int g = 0; g < ng; ++g) {
-                        if (!tc2::wait(&b_empty[s], (pe >> s) & 1u, &s_abort, 0x47480001u)) goto done_prod;
-                        pe ^= 1u << s;
-                        tc2::mbar_expect_tx(&b_full[s], tc2::kStageBytes);
-                        tc2::tma_load_2d(sB + s * tc2::kStageBytes, map, g * kGroup, t * kTileTok, &b_full[s]);
-                        tc2::tma_load_2d(sB + s * tc2::kStageBytes + kSegBytes, map, g * kGroup + 64, t * kTileTok,
-                                         &b_full[s]);
-                        s ^= 1;
-                    }
+            uint32_t s = 0, pe = (1u << tc2::kStages) - 1u;  // empty-phase parity of stage s in bit s
+            uint32_t loaded = 0, pfull = 0;  // stages ever loaded; parity their last load completes
+            tc2::Cursor c;
+            for (bool more = c.begin(p, &s_tab); more; more = c.advance()) {
+                const int ng = c.ng();
+                const CUtensorMap *map = &p.tmap[c.act()];
+                for (int h = 0; h < 4 * ng; ++h) {  // 32-input quarters of the groups
+                    if (!tc2::wait(&b_empty[s], (pe >> s) & 1u, &s_abort, 0x47480001u)) goto done_prod;
+                    pe ^= 1u << s;
+                    tc2::mbar_expect_tx(&b_full[s], tc2::kStageBytes);
+                    tc2::tma_load_2d(sB + s * tc2::kStageBytes, map, h * tc2::kStageK, c.t * tc2::kTok, &b_full[s]);
+                    // the k-th load into stage s completes b_full phase k, whose
+                    // parity equals bit s of pe after the flip above
+                    pfull = (pfull & ~(1u << s)) | (pe & (1u << s));
+                    loaded |= 1u << s;
+                    s = s + 1 == tc2::kStages ? 0 : s + 1;
+                }
             }
-        done_prod:;
+        done_prod:
+            if (s_abort)  // copies still in flight land before the CTA exits
+                for (int i = 0; i < tc2::kStages; ++i)
+                    if (loaded >> i & 1u) tc2::drain_wait(&b_full[i], (pfull >> i) & 1u);
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16(kTileRows, kTileTok);
-            // parities in bit i: stage full (pf), accumulator empty (pae)
-            uint32_t s = 0, pf = 0u, pae = 3u, paf = 0;
+            const uint32_t idesc = idesc_f16(kTileRows, tc2::kTok);
+            // parities in bit i: stage full (pf), accumulator empty (pae), W' group full (paf)
+            uint32_t s = 0, pf = 0u, pae = 3u, paf = 0u;
             int acc = 0;
-            for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
-                const Item it = tc2::decode_item(p, item);
-                const int ng = p.m[it.mat].ng;
-                if (!tc2::wait(&a_full, paf, &s_abort, 0x47480002u)) break;
-                paf ^= 1;
-                for (int t = it.t0; t < it.t1; ++t, ++acc) {
-                    const int a = acc & 1;
-                    if (!tc2::wait(&acc_empty[a], (pae >> a) & 1u, &s_abort, 0x47480003u)) goto done_mma;
-                    pae ^= 1u << a;
-                    fence_after();
-                    for (int g = 0; g < ng; ++g) {
-                        if (!tc2::wait(&b_full[s], (pf >> s) & 1u, &s_abort, 0x47480004u)) goto done_mma;
-                        pf ^= 1u << s;
-                        fence_after();
-                        const uint32_t a0 = smem_u32(sA + g * kOpBytes), b0 = smem_u32(sB + s * tc2::kStageBytes);
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t off = (kk >> 2) * kSegBytes + (kk & 3) * 32;
-                            mma_f16(tmem + a * kTileTok, sw128_desc(a0 + off), sw128_desc(b0 + off), idesc,
-                                    (g | kk) != 0);
-                        }
-                        mma_commit(&b_empty[s]);
-                        s ^= 1;
+            bool issued = false;
+            tc2::Cursor c;
+            for (bool more = c.begin(p, &s_tab); more; more = c.advance(), ++acc) {
+                const int ng = c.ng();
+                const bool first = c.first(), last = c.last();
+                const int a = acc & 1;
+                if (!tc2::wait(&acc_empty[a], (pae >> a) & 1u, &s_abort, 0x47480003u)) goto done_mma;
+                pae ^= 1u << a;
+                fence_after();
+                for (int h = 0; h < 4 * ng; ++h) {
+                    const int g = h >> 2;
+                    if (first && !(h & 3)) {
+                        if (!tc2::wait(&a_full[g], (paf >> g) & 1u, &s_abort, 0x47480002u)) goto done_mma;
+                        paf ^= 1u << g;
                     }
-                    mma_commit(&acc_full[a]);
+                    if (!tc2::wait(&b_full[s], (pf >> s) & 1u, &s_abort, 0x47480004u)) goto done_mma;
+                    pf ^= 1u << s;
+                    fence_after();
+                    // W' rows: 128-byte swizzle, inputs 32h .. 32h+31 of the group are bytes
+                    // 64 (h & 1) .. +63 of segment (h >> 1) & 1; Z: 64-byte swizzle
+                    const uint64_t da = sw128_desc(smem_u32(sA + g * kOpBytes + ((h >> 1) & 1) * kSegBytes + (h & 1) * 64)),
+                                   db = sw64_desc(smem_u32(sB + s * tc2::kStageBytes));
+                    mma_f16(tmem + a * tc2::kTok, da, db, idesc, h != 0);
+                    mma_f16(tmem + a * tc2::kTok, da + 2, db + 2, idesc, 1u);
+                    issued = true;
+                    mma_commit(&b_empty[s]);
+                    s = s + 1 == tc2::kStages ? 0 : s + 1;
+                    if (last && (h & 3) == 3) mma_commit(&a_empty[g]);
                 }
-                mma_commit(&a_empty);
+                mma_commit(&acc_full[a]);
             }
-        done_mma:;
+        done_mma:
+            if (s_abort && issued) {  // MMAs in flight finish before TMEM is freed
+                mma_commit(&drain);
+                tc2::drain_wait(&drain, 0);
+            }
         }
     } else if (warp < 6) {
         // --------------------------------------------------- epilogue --
         const int q = warp & 3;  // TMEM lane quarter of this warp
+        float(*scl)[tc2::kTok] = s_scale[warp - 2];
+        int cur = -1;  // matrix held in s_mat[warp]
+        // token scales of the tile at `nx` (none if !valid) into buffer b (zero
+        // past M), one cp.async group
+        auto prefetch = [&](const tc2::Cursor &nx, bool valid, int b) {
+            if (valid) {
+                const bool same = nx.mat == cur;
+                const float *xs = same ? s_mat[warp].xs : p.m[nx.mat].xs;
+                const int Mtok = same ? s_mat[warp].M : p.m[nx.mat].M;
+#pragma unroll
+                for (int j = 0; j < tc2::kTok / 32; ++j) {
+                    const int m = nx.t * tc2::kTok + 32 * j + lane;
+                    tc2::cp_async4(&scl[b][32 * j + lane], m < Mtok ? xs + m : xs, m < Mtok);
+                }
+            }
+            tc2::cp_async_commit();
+        };
         uint32_t pfa = 0u;  // accumulator-full parity of buffer a in bit a
         int acc = 0;
-        for (int item = blockIdx.x; item < p.total_items && !s_abort; item += gridDim.x) {
-            const Item it = tc2::decode_item(p, item);
-            const tc2::Mat &G = tc2::warp_mat(p, it.mat, &s_mat[warp]);
+        tc2::Cursor c;
+        bool more = c.begin(p, &s_tab);
+        prefetch(c, more, 0);
+        for (; more && !s_abort; more = c.advance(), ++acc) {
+            if (c.mat != cur) {
+                tc2::warp_mat(p, c.mat, &s_mat[warp]);
+                cur = c.mat;
+            }
+            const tc2::Mat &G = s_mat[warp];
             const int out = G.out, Mtok = G.M;
-            const float *xs = G.xs;
             float *Y = G.Y;
-            const int o = it.o0 + 32 * q + lane;
-            for (int t = it.t0; t < it.t1; ++t, ++acc) {
-                const int a = acc & 1;
-                if (!tc2::wait(&acc_full[a], (pfa >> a) & 1u, &s_abort, 0x47480005u)) break;
-                pfa ^= 1u << a;
-                fence_after();
-                const bool ocol = o < out;
+            const int o = c.o0() + 32 * q + lane;
+            const int a = acc & 1;  // accumulator and scale buffer of this tile
+            {
+                tc2::Cursor nx = c;
+                const bool nv = nx.advance();
+                prefetch(nx, nv, a ^ 1);
+            }
+            if (!tc2::wait(&acc_full[a], (pfa >> a) & 1u, &s_abort, 0x47480005u)) break;
+            pfa ^= 1u << a;
+            fence_after();
+            tc2::cp_async_wait1();  // this tile's scales (the next tile's may be in flight)
+            __syncwarp();
+            const bool ocol = o < out;
 #pragma unroll 1
-                for (int c = 0; c < kTileTok / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + a * kTileTok + 32 * c + ((uint32_t)(32 * q) << 16), v);
-                    const int mbase = t * kTileTok + 32 * c;
-                    float *yb = Y + (size_t)mbase * out + o;
-                    if (mbase + 32 <= Mtok) {
-                        // the chunk's 32 token scales, the same for every lane
-                        const float4 *s4 = reinterpret_cast<const float4 *>(xs + mbase);
-                        float sc[32];
-                        if ((reinterpret_cast<uintptr_t>(xs + mbase) & 15) == 0) {
+            for (int ch = 0; ch < tc2::kTok / 32; ++ch) {
+                uint32_t v[32];
+                tmem_ld32(tmem + a * tc2::kTok + 32 * ch + ((uint32_t)(32 * q) << 16), v);
+                const int mbase = c.t * tc2::kTok + 32 * ch;
+                float *yb = Y + (size_t)mbase * out + o;
+                const float4 *s4 = reinterpret_cast<const float4 *>(&scl[a][32 * ch]);
+                float sc[32];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const float4 f = __ldg(s4 + i);
-                                sc[4 * i] = f.x, sc[4 * i + 1] = f.y, sc[4 * i + 2] = f.z, sc[4 * i + 3] = f.w;
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) sc[i] = __ldg(xs + mbase + i);
-                        }
-                        if (ocol) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                yb[(size_t)i * out] = __uint_as_float(v[i]) * __fmul_rn(sc[i], kInvSqrt128);
-                        }
-                    } else {
+                for (int i = 0; i < 8; ++i) {
+                    const float4 f = s4[i];
+                    sc[4 * i] = f.x, sc[4 * i + 1] = f.y, sc[4 * i + 2] = f.z, sc[4 * i + 3] = f.w;
+                }
+                if (mbase + 32 <= Mtok) {
+                    if (ocol) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (ocol && mbase + i < Mtok)
-                                yb[(size_t)i * out] = __uint_as_float(v[i]) * __fmul_rn(__ldg(xs + mbase + i), kInvSqrt128);
+                            yb[(size_t)i * out] = __uint_as_float(v[i]) * __fmul_rn(sc[i], kInvSqrt128);
                     }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (ocol && mbase + i < Mtok)
+                            yb[(size_t)i * out] = __uint_as_float(v[i]) * __fmul_rn(sc[i], kInvSqrt128);
                 }
-                fence_before();
-                __syncwarp();
-                if (lane == 0) tc2::mbar_arrive(&acc_empty[a]);
             }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) tc2::mbar_arrive(&acc_empty[a]);
         }
+        tc2::cp_async_wait0();
     } else {
         // ------------------------------------------ weight expansion --
-        const int et = tid - 192;  // 0..127: weight row of the item
-        uint32_t pe = 1;
-        for (int item = blockIdx.x; item < p.total_items && !s_abort; item += gridDim.x) {
-            const Item it = tc2::decode_item(p, item);
-            const tc2::Mat &G = tc2::warp_mat(p, it.mat, &s_mat[warp]);
-            if (!tc2::wait(&a_empty, pe, &s_abort, 0x47480006u)) break;
-            pe ^= 1;
+        const int et = tid - 192;  // 0..127: weight row of the tile
+        uint32_t pe = (1u << tc2::kMaxNg) - 1u;  // a_empty parity of group g in bit g
+        tc2::Cursor c;
+        for (bool more = c.begin(p, &s_tab); more && !s_abort; more = c.advance()) {
+            if (!c.first()) continue;
+            const tc2::Mat &G = tc2::warp_mat(p, c.mat, &s_mat[warp]);
             // level table in warp-private shared memory (indexed by code)
             if (lane < 16) s_lut[warp - 6][lane] = p.lut[G.lut][lane];
             __syncwarp();
             const float *lut = s_lut[warp - 6];
-            const int o = it.o0 + et;
-            const size_t rowBytes = (size_t)G.ng * 16 * W;
-            for (int g = 0; g < G.ng; ++g) {
-                uint32_t w[4 * W];
-                float nrm = 0.0f;
-                if (o < G.out) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(G.codes + (size_t)o * rowBytes + (size_t)g * 16 * W);
+            const int o = c.o0() + et;
+            const bool orow = o < G.out;
+            const int ng = G.ng;
+            const size_t rowBytes = (size_t)ng * 16 * W;
+            const uint4 *src = reinterpret_cast<const uint4 *>(G.codes + (size_t)o * rowBytes);
+            const __half *nsrc = G.norms + (size_t)o * ng;
+            // codes and norm of group g+1 are fetched while group g expands
+            uint32_t w[4 * W];
+            float nrm = 0.0f;
 #pragma unroll
-                    for (int i = 0; i < W; ++i) {
-                        const uint4 v = __ldg(src + i);
-                        w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
-                    }
-                    nrm = __half2float(G.norms[(size_t)o * G.ng + g]);
-                } else {
+            for (int i = 0; i < W; ++i) {
+                const uint4 v = orow ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+                w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
+            }
+            if (orow) nrm = __half2float(nsrc[0]);
+            bool ok = true;
+            for (int g = 0; g < ng; ++g) {
+                uint32_t wn[4 * W];
+                float nn = 0.0f;
+                const bool more = orow && g + 1 < ng;
 #pragma unroll
-                    for (int i = 0; i < 4 * W; ++i) w[i] = 0;
+                for (int i = 0; i < W; ++i) {
+                    const uint4 v = more ? __ldg(src + (g + 1) * W + i) : make_uint4(0, 0, 0, 0);
+                    wn[4 * i] = v.x, wn[4 * i + 1] = v.y, wn[4 * i + 2] = v.z, wn[4 * i + 3] = v.w;
                 }
+                if (more) nn = __half2float(nsrc[g + 1]);
+                if (!tc2::wait(&a_empty[g], (pe >> g) & 1u, &s_abort, 0x47480006u)) {
+                    ok = false;
+                    break;
+                }
+                pe ^= 1u << g;
                 uint8_t *dst = sA + g * kOpBytes;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -702,10 +890,14 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
                     }
                     *reinterpret_cast<uint4 *>(dst + sw128_off(et, j)) = make_uint4(h[0], h[1], h[2], h[3]);
                 }
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                __syncwarp();
+                if (lane == 0) tc2::mbar_arrive(&a_full[g]);
+#pragma unroll
+                for (int i = 0; i < 4 * W; ++i) w[i] = wn[i];
+                nrm = nn;
             }
-            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-            __syncwarp();
-            if (lane == 0) tc2::mbar_arrive(&a_full);
+            if (!ok) break;
         }
     }
 
@@ -713,16 +905,16 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
     __syncthreads();
     if (warp == 0) {
         fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(256));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(512));
     }
 }
 
-// Dynamic shared memory of the pipelined kernel: 4 x 32 KB of W', 2 x 32 KB
+// Dynamic shared memory of the pipelined kernel: 4 x 32 KB of W', 5 x 16 KB
 // of activation stages, 1 KB of alignment slack.
-constexpr int kTc2MaxSmem = tc2::kMaxNg * tc::kOpBytes + 2 * tc2::kStageBytes + 1024;
+constexpr int kTc2MaxSmem = tc2::kMaxNg * tc::kOpBytes + tc2::kStages * tc2::kStageBytes + 1024;
 
 template <int W>
-int launch_tc2(const tc2::Params &p, size_t smem, cudaStream_t st) {
+int launch_tc2(const tc2::Params &p, int grid, size_t smem, cudaStream_t st) {
     static bool attr = false;
     if (!attr) {
         const cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -730,13 +922,12 @@ int launch_tc2(const tc2::Params &p, size_t smem, cudaStream_t st) {
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm smem attribute: %s", cudaGetErrorString(e));
         attr = true;
     }
-    const int grid = std::min(p.total_items, sm_count());
     gemm_tc2_kernel<W><<<grid, tc2::kThreads, smem, st>>>(p);
     return CQ_OK;
 }
 
 // 2-D tensor map over one rotated activation Z[M][in_pad] (fp16): boxes of
-// 64 inputs x 128 tokens, 128-byte swizzle, zero fill past M.
+// 32 inputs x 256 tokens, 64-byte swizzle, zero fill past M.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -756,10 +947,10 @@ static int make_z_map(CUtensorMap *map, const void *Z, int M, int in_pad) {
     }
     const cuuint64_t dims[2] = {(cuuint64_t)in_pad, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)in_pad * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)tc::kTileTok};
+    const cuuint32_t box[2] = {(cuuint32_t)tc2::kStageK, (cuuint32_t)tc2::kTok};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(Z), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(CQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return CQ_OK;
@@ -860,28 +1051,42 @@ static void level_table(const cq_gemm_desc &d, float lut[16]) {
 static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, int W, cudaStream_t st) {
     static tc2::Params p;
     std::vector<int> map_of(pl.ptr.size(), -1);
-    int nmaps = 0, nlut = 0, items = 0, ngmax = 0;
+    int nmaps = 0, nlut = 0, tiles = 0, runs = 0, ngmax = 0;
     p.n = 0;
     auto flush = [&]() -> int {
         if (!p.n) return CQ_OK;
-        p.total_items = items;
+        p.total_tiles = tiles;
         p.ng_max = ngmax;
-        const size_t smem = (size_t)ngmax * tc::kOpBytes + 2 * tc2::kStageBytes + 1024;
+        // rounds of whole runs, then the rest split by tiles
+        const int grid = std::min(tiles, sm_count());
+        p.full_rounds = runs / grid;
+        const int r0 = p.full_rounds * grid;  // first run of the tail
+        p.tail_T0 = tiles;
+        for (int j = 0; j < p.n; ++j)
+            if (r0 < p.m[j].runs_before + p.m[j].n_tiles) {
+                p.tail_T0 = p.m[j].tiles_before + (r0 - p.m[j].runs_before) * p.m[j].m_tiles;
+                break;
+            }
+        const size_t smem = (size_t)ngmax * tc::kOpBytes + tc2::kStages * tc2::kStageBytes + 1024;
         int rc = CQ_OK;
         switch (W) {
-        case 2: rc = launch_tc2<2>(p, smem, st); break;
-        case 3: rc = launch_tc2<3>(p, smem, st); break;
-        case 4: rc = launch_tc2<4>(p, smem, st); break;
+        case 2: rc = launch_tc2<2>(p, grid, smem, st); break;
+        case 3: rc = launch_tc2<3>(p, grid, smem, st); break;
+        case 4: rc = launch_tc2<4>(p, grid, smem, st); break;
         }
         if (rc) return rc;
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
         p.n = 0;
-        nmaps = nlut = items = ngmax = 0;
+        nmaps = nlut = tiles = runs = ngmax = 0;
         std::fill(map_of.begin(), map_of.end(), -1);
         return CQ_OK;
     };
-    for (int i = 0; i < n; ++i) {
+    // matrices that share an activation next to each other (see the schedule)
+    std::vector<int> order(n);
+    for (int i = 0; i < n; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return pl.act_of[x] < pl.act_of[y]; });
+    for (int i : order) {
         if (pl.act_of[i] < 0 || width_of(d[i].bits) != W) continue;
         const int ip = in_padded(d[i].in), ng = ip / kGroup;
         if (ng > tc2::kMaxNg) continue;
@@ -917,10 +1122,11 @@ static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, u
         G.lut = li;
         G.act = map_of[a];
         G.n_tiles = (G.out + tc::kTileRows - 1) / tc::kTileRows;
-        G.m_tiles = (G.M + tc::kTileTok - 1) / tc::kTileTok;
-        G.chunks = (G.m_tiles + tc2::kTPI - 1) / tc2::kTPI;
-        G.items_before = items;
-        items += G.n_tiles * G.chunks;
+        G.m_tiles = (G.M + tc2::kTok - 1) / tc2::kTok;
+        G.tiles_before = tiles;
+        G.runs_before = runs;
+        tiles += G.n_tiles * G.m_tiles;
+        runs += G.n_tiles;
         ngmax = std::max(ngmax, ng);
         ++p.n;
     }
