@@ -40,12 +40,34 @@ WORKLOAD = ("Needle-shaped decode step, batch 1: 27 x {Q 512x512, K 256x512, V 2
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the grouped GEMV
 # from an ncu capture, keyed by the sha256 of the kernel source it was taken
 # on; reported only while the source is unchanged.
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) per launch of a kernel, from one ncu capture
+# of the bench workload, keyed by kernel and by a hash of the sources it was built from:
+# once a source changes the entry no longer matches and traffic reads null.
+NCU_TRAFFIC = {
+    "gemv_fast": ("e1bb55a7a7b04b5f", 9770496),
+    "gemm_tc2_cq2": ("1625e149c981408d", 530369024),
+    "encode_cq2": ("496c94bb6c2c9db6", 278230272),
+}
+KERNEL_SOURCES = {
+    "gemv_fast": ("cq_gemv_fast.cu", "cq_internal.h"),
+    "gemm_tc2_cq2": ("cq_gemm.cu", "cq_internal.h"),
+    "encode_cq2": ("cq_encode.cu", "cq_internal.h"),
+}
 
 
-def _src_hash(name: str) -> str:
-    p = os.path.join(ROOT, "hadamard_rotated_codebook_gb300", "csrc", name)
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+def _src_hash(*names: str) -> str:
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "hadamard_rotated_codebook_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    rec = NCU_TRAFFIC.get(kernel)
+    if rec and rec[0] == _src_hash(*KERNEL_SOURCES[kernel]):
+        return rec[1]
+    return None
 
 
 def measured_peaks():
@@ -189,7 +211,7 @@ def run_cq(args):
             wl = decode_workload(C, S, device, 0)
             res = bench_gemm(C, S, torch, wl, device, stream, peaks, peak_kind, barrier, max_over_ranks, world)
         else:
-            res = bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
+            res = bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world, args.encode_count)
         if rank == 0:
             print(json.dumps(res), flush=True)
         if world > 1:
@@ -246,7 +268,7 @@ def run_cq(args):
     roofline = {
         "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
         "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
-        "traffic": NCU_TRAFFIC.get(_src_hash("cq_gemv.cu")),
+        "traffic": ncu_traffic("gemv_fast"),
         "kernel": "gemv (grouped decode step)",
         "algorithmic_bytes_per_launch": wl["algo_bytes"],
     }
@@ -303,7 +325,8 @@ def run_cq(args):
 
     if not args.skip_extra:
         result["gemm"] = bench_gemm(C, S, torch, wl, device, stream, peaks, peak_kind, barrier, max_over_ranks, world)
-        result["encode"] = bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
+        result["encode"] = bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world,
+                                        args.encode_count)
     if rank == 0 and world == 1 and not args.skip_cpu:
         result["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     if rank == 0:
@@ -357,11 +380,11 @@ def bench_gemm(C, S, torch, wl, device, stream, peaks, peak_kind, barrier, max_o
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(tflops / peaks["bf16_tflops"], 4),
                          "peak_source": peak_kind + " (bf16 dense; fp16 operands run at the same rate)",
-                         "traffic": None}}
+                         "traffic": None, "traffic_cq2_kernel": ncu_traffic("gemm_tc2_cq2")}}
 
 
-def bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world):
-    n = S.ENCODE_COUNT
+def bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world, count=0):
+    n = count or S.ENCODE_COUNT
     Ws = [S.encode_matrix(i, device=device) for i in range(n)]
     cb = C.cq_codebook_init(2)
     nb = C.cq_packed_bytes(*S.ENCODE_SHAPE, 128, 2)
@@ -374,24 +397,31 @@ def bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, wo
     with torch.cuda.stream(stream):
         one_pass()
     stream.synchronize()
+    # the pass as a graph: host-side argument checks stay out of the timed region
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        one_pass()
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
     Ke = 3
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(Ke):
-            one_pass()
+            g.replay()
         e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1)) / Ke
     elems = n * S.ENCODE_SHAPE[0] * S.ENCODE_SHAPE[1]
     algo = elems * 4 + n * nb
     gbs = algo / (ms * 1e-3) / 1e9
-    return {"metric": "CQ2 encode GB/s (16 fp32 8192x8192 with 1% outliers -> codes + fp16 norms)",
+    return {"metric": f"CQ2 encode GB/s ({n} fp32 8192x8192 with 1% outliers -> codes + fp16 norms)",
             "value": round(world * gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 3), "steps": Ke,
             "warmup": 1, "launches_per_step": n,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": ncu_traffic("encode_cq2"),
                          "algorithmic_bytes_per_launch": algo // n}}
 
 
@@ -466,6 +496,7 @@ def main():
     ap.add_argument("--impl", default="cq", choices=["cq", "reference"])
     ap.add_argument("--skip-extra", action="store_true", help="decode step only")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--encode-count", type=int, default=0, help="matrices in the encode part (default 16)")
     ap.add_argument("--only", default="all", choices=["all", "gemm", "encode"],
                     help="time one secondary part alone and print its JSON object (profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
