@@ -37,12 +37,10 @@ METRIC = "CQ2 GEMV effective GB/s and % HBM roofline; CQ GEMM TOPS at M=2048"
 WORKLOAD = ("Needle-shaped decode step, batch 1: 27 x {Q 512x512, K 256x512, V 256x512, gate 512x512, "
             "O 512x512} CQ2 + head 8192x512 CQ4, int8 per-token activations")
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the grouped GEMV
-# from an ncu capture, keyed by the sha256 of the kernel source it was taken
-# on; reported only while the source is unchanged.
-# DRAM bytes (read + write) per launch of a kernel, from one ncu capture
-# of the bench workload, keyed by kernel and by a hash of the sources it was built from:
-# once a source changes the entry no longer matches and traffic reads null.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a
+# kernel, from one ncu capture of the bench workload, keyed by kernel and by a
+# hash of the sources it was built from: once a source changes the entry no
+# longer matches and traffic reads null.
 NCU_TRAFFIC = {
     "gemv_fast": ("e1bb55a7a7b04b5f", 9770496),
     "gemm_tc2_cq2": ("1625e149c981408d", 530369024),
