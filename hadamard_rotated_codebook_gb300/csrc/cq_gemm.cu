@@ -18,6 +18,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
 #include <vector>
 
 #include "cq_internal.h"
@@ -956,35 +958,54 @@ static int make_z_map(CUtensorMap *map, const void *Z, int M, int in_pad) {
     return CQ_OK;
 }
 
+
+}  // namespace
+
 // ------------------------------------------------------------ workspace --
-struct Workspace {
+// Device scratch per (device, stream, kind), grown on demand. Grow-only: an
+// outgrown buffer stays allocated until the process exits, because a CUDA
+// graph captured earlier may still point at it (freeing it would leave the
+// graph reading freed memory). Calls on one stream are ordered, so they may
+// share its buffer; calls on different streams get different buffers.
+namespace {
+struct WsKey {
+    int dev;
+    cudaStream_t st;
+    int kind;
+    bool operator<(const WsKey &o) const {
+        if (dev != o.dev) return dev < o.dev;
+        if (st != o.st) return st < o.st;
+        return kind < o.kind;
+    }
+};
+struct WsBuf {
     void *ptr = nullptr;
     size_t bytes = 0;
 };
-std::vector<Workspace> g_ws;
+std::mutex g_ws_mutex;
+std::map<WsKey, WsBuf> g_ws;
+std::vector<void *> g_ws_retired;
+}  // namespace
 
-// Device workspace of at least `bytes`, grown on demand (cudaFree of the old
-// buffer synchronises the device, so no kernel still reads it).
-void *workspace(size_t bytes, int *err) {
+void *stream_workspace(void *stream, int kind, size_t bytes, int *err) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int dev = 0;
     cudaGetDevice(&dev);
-    if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1);
-    Workspace &w = g_ws[dev];
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    WsBuf &w = g_ws[WsKey{dev, st, kind}];
     if (w.bytes >= bytes) return w.ptr;
-    if (w.ptr) cudaFree(w.ptr);
-    w.ptr = nullptr;
-    w.bytes = 0;
     size_t want = std::max(bytes, (size_t)1 << 20);
-    if (cudaMalloc(&w.ptr, want) != cudaSuccess) {
+    void *p = nullptr;
+    if (cudaMalloc(&p, want) != cudaSuccess) {
         cudaGetLastError();
-        *err = set_error(CQ_ERR_NOMEM, "cannot allocate %zu bytes of GEMM workspace", want);
+        *err = set_error(CQ_ERR_NOMEM, "cannot allocate %zu bytes of workspace", want);
         return nullptr;
     }
+    if (w.ptr) g_ws_retired.push_back(w.ptr);
+    w.ptr = p;
     w.bytes = want;
     return w.ptr;
 }
-
-}  // namespace
 
 // Distinct activations of a call and where their rotations go in a
 // workspace (each rotated once: M * in_pad fp16, 256-byte aligned).
@@ -1028,7 +1049,7 @@ int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream) {
     plan_activations(d, n, st, pl);
     if (pl.ptr.empty()) return CQ_OK;
     int err = CQ_OK;
-    uint8_t *ws = static_cast<uint8_t *>(workspace(pl.total, &err));
+    uint8_t *ws = static_cast<uint8_t *>(stream_workspace(st, 0, pl.total, &err));
     if (!ws) return err;
     return run_gemm(d, n, pl, ws, st);
 }
