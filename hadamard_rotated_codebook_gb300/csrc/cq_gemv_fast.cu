@@ -266,9 +266,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     // one copy of this CTA's matrix descriptor in shared memory (parameter
     // reads with a runtime index would otherwise repeat inside the loops)
     __shared__ FastMat sM;
+    __shared__ __half s_lv[16];  // the codebook's levels (parameter reads with a
+                                 // per-lane index would serialise)
     const int mi = p.item_mat[blockIdx.x];
     if (threadIdx.x < (int)(sizeof(FastMat) / 4))
         reinterpret_cast<uint32_t *>(&sM)[threadIdx.x] = reinterpret_cast<const uint32_t *>(&p.m[mi])[threadIdx.x];
+    else if (threadIdx.x >= 128 && threadIdx.x < 144)
+        s_lv[threadIdx.x - 128] = p.lut[p.m[mi].lut][threadIdx.x - 128];
     __syncthreads();
     const FastMat &M = sM;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -284,7 +288,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     uint32_t *frag = reinterpret_cast<uint32_t *>(smem + p.smem_frag);
     float *red = reinterpret_cast<float *>(smem + p.smem_red);
     __shared__ float ginv[kMaxFastB * kMaxFastNg];  // 1/sigma [B][ng]
-    __shared__ float s_alpha[kMaxFastB];
 
     // ---- 1. code rows and norms -> shared memory (16-byte cp.async; rows
     // past the matrix zero-filled) ----
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
 
     // ---- 2. while they land: the level table and the output scales ----
     {
-        const __half *lv = p.lut[M.lut];
+        const __half *lv = s_lv;
         if (kind == 0) {
             // byte -> four fp16 levels (codes LSB first), 16 copies so that a
             // half-warp's 8-byte lookups hit distinct banks
@@ -339,12 +342,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
                 tab[e] = (uint32_t)__half_as_ushort(lv[v & 15]) | ((uint32_t)__half_as_ushort(lv[v >> 4]) << 16);
             }
         }
-    }
-    if (threadIdx.x < kMaxFastB) {
-        const int b = threadIdx.x;
-        float a = kInvSqrt128;
-        if (b < B && M.xdt == CQ_X_I8) a = __fmul_rn(M.xs[b], kInvSqrt128);
-        s_alpha[b] = a;
     }
 
     // ---- 3. the activation's B fragments and 1/sigma, written by the
@@ -368,6 +365,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     const bool wide = tiles >= kWarps;
     const int step = wide ? kWarps : tiles + 1;
     const int kc = wide ? 0 : warp % KC;
+    const bool live = gq < 2 * B;  // this lane's B column belongs to a batch row
+    // output scale of this lane's batch row t
+    const float alpha = t < B && M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[t], kInvSqrt128) : kInvSqrt128;
     const uint2 *tab2 = reinterpret_cast<const uint2 *>(smem + p.smem_tab) + (lane & 15);
     const uint32_t *tab4 = reinterpret_cast<const uint32_t *>(smem + p.smem_tab) + lane;
 
@@ -379,11 +379,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
         const int ra = 16 * ta + gq, rb = 16 * (has_b ? tb : ta) + gq;  // local rows (and +8)
 #pragma unroll 1
         for (int g = kc; g < ng; g += KC) {
+            // B columns 2B .. 7 are zero: only the lanes of the live columns load
             uint32_t fr[kFragWords];
             const uint4 *fl = reinterpret_cast<const uint4 *>(frag + (size_t)g * 32 * kFragWords) + lane;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint4 v = fl[32 * i];
+                const uint4 v = live ? fl[32 * i] : make_uint4(0, 0, 0, 0);
                 fr[4 * i] = v.x, fr[4 * i + 1] = v.y, fr[4 * i + 2] = v.z, fr[4 * i + 3] = v.w;
             }
             const float inv = t < B ? ginv[t * ng + g] : 0.0f;
@@ -418,9 +419,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
             const float yr = acc[h][0] + acc[h][1], ys = acc[h][2] + acc[h][3];
             if (t < B) {
                 if (KC == 1) {
-                    const float a = s_alpha[t];
-                    if (row_r < M.out) M.y[(size_t)t * M.out + row_r] = yr * a;
-                    if (row_s < M.out) M.y[(size_t)t * M.out + row_s] = ys * a;
+                    if (row_r < M.out) M.y[(size_t)t * M.out + row_r] = yr * alpha;
+                    if (row_s < M.out) M.y[(size_t)t * M.out + row_s] = ys * alpha;
                 } else {
                     float *rt = red + ((size_t)(tl * KC + kc) * 16) * kMaxFastB;
                     rt[gq * kMaxFastB + t] = yr;
@@ -437,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
             if (row >= M.out) continue;
             float sum = 0.0f;
             for (int c = 0; c < KC; ++c) sum += red[((size_t)(tl * KC + c) * 16 + rr) * kMaxFastB + b];
-            M.y[(size_t)b * M.out + row] = sum * s_alpha[b];
+            const float ab = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[b], kInvSqrt128) : kInvSqrt128;
+            M.y[(size_t)b * M.out + row] = sum * ab;
         }
     }
 }
