@@ -109,15 +109,31 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
     const int pair = tid >> 1, h = tid & 1, f = pair & 3;
     const long long n_tiles = (p.n_groups + kEncGroupsPerTile - 1) / kEncGroupsPerTile;
 
+    // Aligned rows: the tile is staged with 16-byte cp.async (every copy of a
+    // tile in flight at once, no registers held), and the next tile's copies
+    // are issued as soon as the current tile has moved to registers, so
+    // they stream while it is encoded.
+    auto stage = [&](long long tt) {
+        const long long gs = tt * kEncGroupsPerTile;
+        const float4 *src = reinterpret_cast<const float4 *>(p.W) + gs * (kGroup / 4);
+        const long long avail4 = (p.n_groups - gs) * (kGroup / 4);
+        const uint32_t dst0 = (uint32_t)__cvta_generic_to_shared(smem4);
+#pragma unroll
+        for (int i = tid; i < kEncTileFloats / 4; i += kEncThreads) {
+            const bool ok = i < avail4;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst0 + 16u * i),
+                         "l"(ok ? src + i : src), "r"(ok ? 16 : 0)
+                         : "memory");
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+    };
+    if (ALIGNED && blockIdx.x < n_tiles) stage(blockIdx.x);
+
     for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x) {
         const long long g0 = t * kEncGroupsPerTile;
         // ---- stage 128 groups into shared memory (coalesced) ----
         if (ALIGNED) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.W) + g0 * (kGroup / 4);
-            const long long avail4 = (p.n_groups - g0) * (kGroup / 4);
-#pragma unroll 4
-            for (int i = tid; i < kEncTileFloats / 4; i += kEncThreads)
-                smem4[i] = i < avail4 ? __ldcs(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            asm volatile("cp.async.wait_all;\n" ::: "memory");
         } else {
             for (int i = tid; i < kEncTileFloats; i += kEncThreads) {
                 const long long G = g0 + i / kGroup;
@@ -145,6 +161,7 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
             x[4 * j + 3] = v.w;
         }
         __syncthreads();  // the tile may be overwritten from here on
+        if (ALIGNED && t + gridDim.x < n_tiles) stage(t + gridDim.x);
 
         // ---- sum of squares, pairwise in fp32 ----
         float sq[32];
