@@ -56,6 +56,19 @@ def _dev_ptr(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
     return t.data_ptr()
 
 
+def _io_ptr(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
+    """Pointer to a GEMV activation, scale or output: a CUDA tensor, or a
+    pinned (page-locked) host tensor, which the kernels read or write in
+    place over the host link (unified addressing)."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
+        raise TypeError(f"{name} must be a CUDA tensor or a pinned host tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
 def _codebook_arg(codebook, bits: int):
     cb = np.ascontiguousarray(np.asarray(
         codebook.detach().cpu() if isinstance(codebook, torch.Tensor) else codebook,
@@ -135,18 +148,16 @@ def _gemv_desc(blob, out, n_in, bits, codebook, x, x_scale, y, group, keep):
         xdt = CQ_X_I8
         if x_scale is None:
             raise ValueError("int8 activations need x_scale")
-        xs = _dev_ptr(x_scale, torch.float32, "x_scale")
+        xs = _io_ptr(x_scale, torch.float32, "x_scale")
     else:
         raise TypeError("x must be float32 or int8")
     if y is None:
-        y = torch.empty((B, out), dtype=torch.float32, device=x.device)
+        y = torch.empty((B, out), dtype=torch.float32, device=blob.device)
     cb, cbp = _codebook_arg(codebook, bits)
     keep.append(cb)
-    d = GemvDesc(blob=_dev_ptr(blob, torch.uint8, "blob"), x=x2.data_ptr() if x2.is_cuda else None,
-                 x_scale=xs, y=_dev_ptr(y, torch.float32, "y"), codebook=cbp, out=out, in_=n_in,
+    d = GemvDesc(blob=_dev_ptr(blob, torch.uint8, "blob"), x=_io_ptr(x2, x2.dtype, "x"),
+                 x_scale=xs, y=_io_ptr(y, torch.float32, "y"), codebook=cbp, out=out, in_=n_in,
                  group=group, bits=bits, x_dtype=xdt, B=B)
-    if not x2.is_cuda or not x2.is_contiguous():
-        raise ValueError("x must be a contiguous CUDA tensor")
     return d, y
 
 
@@ -157,7 +168,7 @@ def cq_gemv(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook, x: tor
     per-token scales x_scale[B]."""
     keep = []
     d, y = _gemv_desc(blob, out, n_in, bits, codebook, x, x_scale, y, group, keep)
-    check(_lib().cq_gemv_grouped(ctypes.byref(d), 1, _stream(x.device)))
+    check(_lib().cq_gemv_grouped(ctypes.byref(d), 1, _stream(blob.device)))
     return y
 
 
@@ -173,7 +184,7 @@ def cq_gemv_grouped(items: Sequence[dict]) -> list:
         ds.append(d)
         ys.append(y)
     arr = (GemvDesc * len(ds))(*ds)
-    check(_lib().cq_gemv_grouped(arr, len(ds), _stream(items[0]["x"].device)))
+    check(_lib().cq_gemv_grouped(arr, len(ds), _stream(items[0]["blob"].device)))
     return ys
 
 
@@ -191,7 +202,7 @@ class GemvPlan:
         self._items = list(items)  # keep tensors alive
         self._arr = (GemvDesc * len(ds))(*ds)
         self._n = len(ds)
-        self._device = items[0]["x"].device
+        self._device = items[0]["blob"].device
 
     def run(self, stream: Optional[torch.cuda.Stream] = None):
         st = ctypes.c_void_p((stream or torch.cuda.current_stream(self._device)).cuda_stream)

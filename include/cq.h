@@ -132,20 +132,27 @@ int cq_act_quant_int8(const float *X, int M, int in, int8_t *Xq, float *s,
  * which equals W_hat x_b exactly in real arithmetic: the activation is
  * rotated once per group (in-register fast Walsh-Hadamard transform) and the
  * weights are never expanded to a dense matrix ([CF] "How the kernel reads
- * it"). Arithmetic is fp32 apart from tensor-core products of exactly
- * represented code planes.
- * x: device, fp32 [B][in] (x_dtype = CQ_X_F32, x_scale ignored, may be
- *    NULL) or int8 [B][in] with x_scale fp32 [B] on the device
- *    (x_dtype = CQ_X_I8).
- * y: device fp32 [B][out], fully overwritten.
+ * it"). On the tensor-core path (2- and 4-bit codes, B <= 4, in <= 4096) the
+ * codebook levels are rounded to fp16 and multiplied with z split into fp16
+ * hi + lo terms, accumulating in fp32; other shapes use fp32 arithmetic.
+ * x: fp32 [B][in] (x_dtype = CQ_X_F32, x_scale ignored, may be NULL) or
+ *    int8 [B][in] with x_scale fp32 [B] (x_dtype = CQ_X_I8).
+ * y: fp32 [B][out], fully overwritten.
+ * x, x_scale and y are device memory or page-locked host memory that the
+ * device can address (cudaHostAlloc / cudaHostRegister with unified
+ * addressing): the kernels then read the activation and write the result
+ * across the host link themselves, with no separate copy (on Grace-Blackwell
+ * over NVLink-C2C). blob is device memory.
  * Errors: CQ_ERR_ARG, CQ_ERR_SHAPE (group != 128, B out of range),
  * CQ_ERR_CUDA. */
 int cq_gemv(const uint8_t *blob, int out, int in, int group, int bits,
             const float *codebook, const void *x, int x_dtype,
             const float *x_scale, int B, float *y, void *stream);
 
-/* One matrix of a grouped GEMV. All pointers are device pointers; the
- * codebook is the host array `codebook` (cq_levels(bits) floats). */
+/* One matrix of a grouped GEMV. blob is a device pointer; x, x_scale and y
+ * are device pointers or device-addressable page-locked host memory (as for
+ * cq_gemv); the codebook is the host array `codebook` (cq_levels(bits)
+ * floats). */
 typedef struct cq_gemv_desc {
     const uint8_t *blob;
     const void *x;        /* [B][in], fp32 or int8 per x_dtype */

@@ -177,3 +177,20 @@ def test_gemv_sweep_full_size_sampled(C, shape, bits, B):
     rows = np.array([0, 1, out // 3, out // 2, out - 129, out - 2, out - 1, 17])
     y_ref, bound = _oracle_y(sub_blob(blob, out, n_in, bits, rows), len(rows), n_in, bits, cb, x.numpy())
     check_matmul(y[:, rows], y_ref, bound, f"sweep {shape} cq{bits} B={B}")
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_gemv_host_resident_activations_and_outputs(C, B):
+    """x, x_scale and y in pinned host memory: the kernels read and write them
+    in place, and the result is bit-identical to the device-resident call."""
+    out, n_in, bits = 272, 640, 2
+    blob = torch.from_numpy(_rand_blob(out, n_in, bits, 61)).cuda()
+    cb = O.analytic_codebook(bits)
+    q, s = O.act_quant_int8(S.normal((B, n_in), 62).numpy())
+    xq_d, xs_d = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+    y_d = C.cq_gemv(blob, out, n_in, bits, cb, xq_d, xs_d)
+    xq_h, xs_h = torch.from_numpy(q).pin_memory(), torch.from_numpy(s).pin_memory()
+    y_h = torch.full((B, out), float("nan")).pin_memory()
+    C.cq_gemv(blob, out, n_in, bits, cb, xq_h, xs_h, y=y_h)
+    torch.cuda.synchronize()
+    assert torch.equal(y_h, y_d.cpu())
