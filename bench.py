@@ -189,23 +189,22 @@ def make_plans(C, wl, Xq, xs, ybuf):
     return plans
 
 
-def run_cq(args):
+# ------------------------------------------------------------ ranks
+# One process per GPU; every rank runs the whole workload on its own GPU (the
+# units are independent: weak scaling, no data-path collective). Only the
+# barriers around the timed region and the max of the ranks' times cross.
+
+def rank_context():
+    """(world size, rank, local rank) from the launcher's environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_ops(world, device):
+    """barrier() and max_over_ranks(v) for an initialised process group
+    (tensors on `device`: a GPU for NCCL, the CPU for gloo)."""
     import torch
     import torch.distributed as dist
-
-    import hadamard_rotated_codebook_gb300 as C
-    import synthetic as S
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    props = torch.cuda.get_device_properties(device)
-    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
-    peaks, peak_kind = measured_peaks()
 
     def barrier():
         if world > 1:
@@ -217,6 +216,32 @@ def run_cq(args):
         t = torch.tensor([v], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
+
+    return barrier, max_over_ranks
+
+
+def aggregate_gbs(bytes_per_rank_step, steps, world, max_ms):
+    """Whole-job throughput: the bytes every rank processed over the slowest
+    rank's time."""
+    return world * bytes_per_rank_step * steps / (max_ms * 1e-3) / 1e9
+
+
+def run_cq(args):
+    import torch
+    import torch.distributed as dist
+
+    import hadamard_rotated_codebook_gb300 as C
+    import synthetic as S
+
+    world, rank, local = rank_context()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    peaks, peak_kind = measured_peaks()
+    barrier, max_over_ranks = rank_ops(world, device)
 
     if args.only in ("gemm", "encode"):
         # one part alone, for profiling: only that part's buffers are held
@@ -276,7 +301,7 @@ def run_cq(args):
     C.cq_device_status(device)
     ms = max_over_ranks(ev0.elapsed_time(ev1))
     ms_step = ms / K
-    gbs = world * wl["packed"] * K / (ms * 1e-3) / 1e9
+    gbs = aggregate_gbs(wl["packed"], K, world, ms)
     launches = K  # one grouped GEMV launch per step
     achieved = wl["algo_bytes"] / (ms_step * 1e-3) / 1e9
     roofline = {
@@ -338,7 +363,7 @@ def run_cq(args):
     # the host-side result is the device-side one
     if not torch.equal(y_h, wl["ybuf"].cpu()):
         raise RuntimeError("end-to-end outputs differ from the device-resident run")
-    result["e2e"] = {"value": round(world * wl["packed"] * Ke / (mse * 1e-3) / 1e9, 1), "unit": "GB/s",
+    result["e2e"] = {"value": round(aggregate_gbs(wl["packed"], Ke, world, mse), 1), "unit": "GB/s",
                      "h2d_bytes_per_step": wl["inbuf"].numel(),
                      "d2h_bytes_per_step": 4 * wl["out_total"], "steps": Ke,
                      "ms_per_step": round(mse / Ke, 6)}
@@ -483,9 +508,8 @@ def cpu_baseline(budget_s: float = 10.0):
 
 
 def run_reference(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    world, rank, _ = rank_context()
+    if rank != 0:  # the oracle runs on rank 0 alone; the other ranks exit without work
         return
     K, Wm = args.steps, args.warmup
     per_step = max(0.05, min(2.0, 120.0 / max(1, min(K, 200) + Wm)))

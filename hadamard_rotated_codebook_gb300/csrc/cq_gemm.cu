@@ -1252,6 +1252,30 @@ static void *g_noalloc_ptr[64];
 
 }  // namespace cq
 
+// ------------------------------------------------------------ self-test --
+namespace cq {
+// One warp polls (bounded) an mbarrier phase that nothing completes, then
+// takes the same give-up path as the GEMM's waits: record a code in the
+// status word and return.
+__global__ void wait_timeout_probe_kernel(unsigned polls) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) tc::mbar_init(&bar, 1);
+    __syncwarp();
+    if (threadIdx.x == 0) {
+        bool done = false;
+        for (unsigned i = 0; i < polls && !done; ++i) done = tc::mbar_test(&bar, 0);
+        if (!done) atomicOr(&g_cq_device_status, 0x4748FFFFu);
+    }
+}
+}  // namespace cq
+
+extern "C" int cq_selftest_wait_timeout(void *stream) {
+    cq::wait_timeout_probe_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(1u << 16);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cq::set_error(CQ_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
+    return CQ_OK;
+}
+
 extern "C" int cq_gemm_noalloc(const uint8_t *blob, int out, int in, int group, int bits, const float *codebook,
                                const int8_t *Xq, const float *x_scale, int M, float *Y, void *stream) {
     using namespace cq;

@@ -236,6 +236,15 @@ int cq_gemm_noalloc(const uint8_t *blob, int out, int in, int group, int bits,
  * they give up (synchronises `stream`). CQ_OK or CQ_ERR_TIMEOUT. */
 int cq_device_status(void *stream);
 
+/* Diagnostic without a counterpart on the pages: exercises the give-up path
+ * of a bounded device wait without faulting the GPU. Launches one warp on
+ * `stream` that polls, a bounded number of times, an mbarrier phase that
+ * nothing completes; the wait gives up, records code 0x4748FFFF in the
+ * device status word and the kernel returns. A following cq_device_status
+ * then reports CQ_ERR_TIMEOUT (and clears the word); the context stays
+ * usable. Errors: CQ_ERR_CUDA if the launch fails. */
+int cq_selftest_wait_timeout(void *stream);
+
 /* -------------------------------------------------------- container -- */
 /*
  * Own .cact-shaped container (the pages disagree on the header: 196 bytes
