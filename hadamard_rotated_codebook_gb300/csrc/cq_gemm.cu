@@ -207,13 +207,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            (2ull << 61);
 }
 
-// The same for a K-major operand with 64-byte swizzle (32-wide K rows of
-// 64 B, 8-row groups 512 B apart).
-__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(512 >> 4) << 32) | (1ull << 46) |
-           (4ull << 61);
-}
-
 // Instruction descriptor, kind::f16: fp16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -262,6 +255,27 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
             d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// The same with A read from tensor memory (a_tmem: lane = row, column c
+// holding K elements 2c, 2c+1 as fp16 low | high).
+__device__ __forceinline__ void mma_f16_tA(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                           uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+        "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -447,10 +461,11 @@ namespace tc2 {
 constexpr int kThreads = 320;
 constexpr int kMaxActs = 64;     // distinct activations (tensor maps) per launch
 constexpr int kMaxNg = 4;        // groups of the inputs kept resident
-constexpr int kTok = 256;        // MMA N: tokens of a tile
-constexpr int kStages = 5;       // activation stages
-constexpr int kStageK = 32;      // inputs per stage (two K=16 MMAs)
-constexpr int kStageBytes = kTok * kStageK * 2;  // 256 tokens x 32 inputs fp16, 64-byte swizzle
+constexpr int kTok = 128;        // MMA N: tokens of a tile
+constexpr int kStages = 6;       // activation stages, one 128-input group each (eight K=16 MMAs)
+constexpr int kStageBytes = kTok * kGroup * 2;  // 128 tokens x 128 inputs fp16: two 64-wide 128-byte-swizzled segments
+constexpr int kAcc = 0;          // TMEM columns: accumulators at 0 and kTok
+constexpr int kWcol = 256;       // TMEM columns: W' group g at kWcol + 64 g (two fp16 per column)
 constexpr unsigned kSpin = 1u << 22;  // polls of one barrier (each may suspend ~1 us)
 constexpr unsigned kDrainSpin = 1u << 20;
 
@@ -470,7 +485,7 @@ struct Params {
     Mat m[CQ_MAX_GROUPED];
 };
 
-// Output tiles are 128 rows x 256 tokens. Tiles are numbered matrix by
+// Output tiles are 128 rows x 128 tokens. Tiles are numbered matrix by
 // matrix (matrices that share an activation are adjacent), weight-row tile by
 // weight-row tile, token tile fastest; the tiles of one (matrix, row tile)
 // form a run. The schedule works in rounds: in round k, CTA b takes the whole
@@ -633,15 +648,17 @@ __device__ void drain_wait(uint64_t *bar, uint32_t parity) {
 }  // namespace tc2
 
 // Pipelined, warp-specialised GEMM for inputs of at most 512 (ng <= 4
-// groups): the 128 x (128 ng) slice of W' stays in shared memory for the
-// whole run of token tiles that use it.
-//   warp 0     TMA producer: Z tiles (256 tokens x 32 inputs) into five stages
-//   warp 1     MMA issuer: tcgen05.mma (M=128, N=256) into two 256-column
-//              TMEM accumulators
+// groups): the 128 x (128 ng) slice of W' stays in tensor memory, where the
+// MMAs read it as their A operand, for the whole run of token tiles that use
+// it; shared memory holds only activation stages.
+//   warp 0     TMA producer: Z tiles (128 tokens x 128 inputs) into six stages
+//   warp 1     MMA issuer: tcgen05.mma (M=128, N=128, A from TMEM) into two
+//              128-column TMEM accumulators, eight MMAs per stage
 //   warps 2-5  epilogue: TMEM -> registers, token scale, fp32 stores of Y
-//   warps 6-9  expansion of the next run's codes and norms into fp16 W',
-//              one group at a time, as soon as the MMAs of the previous run
-//              are done with that group
+//   warps 6-9  expansion of the next run's codes and norms into fp16 W'
+//              rows of TMEM (tcgen05.st; each warp its lane quarter), one
+//              group at a time, as soon as the MMAs of the previous run are
+//              done with that group
 // Every wait is bounded; a role that gives up sets the abort flag, the others
 // leave their loops, and work already issued (TMA loads, MMAs) is waited for
 // before TMEM is freed.
@@ -650,8 +667,7 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *sA = smem;                                // ng_max x 32 KB of W'
-    uint8_t *sB = smem + (size_t)p.ng_max * kOpBytes;  // kStages x 16 KB of Z
+    uint8_t *sB = smem;  // kStages x 32 KB of Z
     __shared__ __align__(8) uint64_t a_full[tc2::kMaxNg], a_empty[tc2::kMaxNg], b_full[tc2::kStages],
         b_empty[tc2::kStages], acc_full[2], acc_empty[2], drain;
     __shared__ uint32_t s_tmem;
@@ -664,7 +680,7 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     tc2::load_sched(p, &s_tab);
 
-    if (warp == 0) {  // two 256-column fp32 accumulators
+    if (warp == 0) {  // two 128-column fp32 accumulators and 256 columns of W'
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&s_tmem)),
                      "r"(512));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
@@ -699,11 +715,13 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
             for (bool more = c.begin(p, &s_tab); more; more = c.advance()) {
                 const int ng = c.ng();
                 const CUtensorMap *map = &p.tmap[c.act()];
-                for (int h = 0; h < 4 * ng; ++h) {  // 32-input quarters of the groups
+                for (int g = 0; g < ng; ++g) {  // one group per stage
                     if (!tc2::wait(&b_empty[s], (pe >> s) & 1u, &s_abort, 0x47480001u)) goto done_prod;
                     pe ^= 1u << s;
                     tc2::mbar_expect_tx(&b_full[s], tc2::kStageBytes);
-                    tc2::tma_load_2d(sB + s * tc2::kStageBytes, map, h * tc2::kStageK, c.t * tc2::kTok, &b_full[s]);
+                    tc2::tma_load_2d(sB + s * tc2::kStageBytes, map, g * kGroup, c.t * tc2::kTok, &b_full[s]);
+                    tc2::tma_load_2d(sB + s * tc2::kStageBytes + kSegBytes, map, g * kGroup + 64, c.t * tc2::kTok,
+                                     &b_full[s]);
                     // the k-th load into stage s completes b_full phase k, whose
                     // parity equals bit s of pe after the flip above
                     pfull = (pfull & ~(1u << s)) | (pe & (1u << s));
@@ -732,25 +750,27 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
                 if (!tc2::wait(&acc_empty[a], (pae >> a) & 1u, &s_abort, 0x47480003u)) goto done_mma;
                 pae ^= 1u << a;
                 fence_after();
-                for (int h = 0; h < 4 * ng; ++h) {
-                    const int g = h >> 2;
-                    if (first && !(h & 3)) {
+                for (int g = 0; g < ng; ++g) {
+                    if (first) {
                         if (!tc2::wait(&a_full[g], (paf >> g) & 1u, &s_abort, 0x47480002u)) goto done_mma;
                         paf ^= 1u << g;
+                        fence_after();  // W' written with tcgen05.st by the expansion warps
                     }
+                    // the stage was filled by TMA: its mbarrier orders the MMA's reads
                     if (!tc2::wait(&b_full[s], (pf >> s) & 1u, &s_abort, 0x47480004u)) goto done_mma;
                     pf ^= 1u << s;
-                    fence_after();
-                    // W' rows: 128-byte swizzle, inputs 32h .. 32h+31 of the group are bytes
-                    // 64 (h & 1) .. +63 of segment (h >> 1) & 1; Z: 64-byte swizzle
-                    const uint64_t da = sw128_desc(smem_u32(sA + g * kOpBytes + ((h >> 1) & 1) * kSegBytes + (h & 1) * 64)),
-                                   db = sw64_desc(smem_u32(sB + s * tc2::kStageBytes));
-                    mma_f16(tmem + a * tc2::kTok, da, db, idesc, h != 0);
-                    mma_f16(tmem + a * tc2::kTok, da + 2, db + 2, idesc, 1u);
+                    // K step kk: inputs 16kk .. 16kk+15 of the group; Z: 32 bytes into
+                    // the rows of segment kk/4; W': 8 TMEM columns
+                    const uint64_t db = sw128_desc(smem_u32(sB + s * tc2::kStageBytes));
+                    const uint32_t wa = tmem + tc2::kWcol + 64 * g, da = tmem + tc2::kAcc + a * tc2::kTok;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_f16_tA(da, wa + 8 * kk, db + (uint64_t)((kk >> 2) * (kSegBytes >> 4) + (kk & 3) * 2), idesc,
+                                   (g | kk) != 0);
                     issued = true;
                     mma_commit(&b_empty[s]);
                     s = s + 1 == tc2::kStages ? 0 : s + 1;
-                    if (last && (h & 3) == 3) mma_commit(&a_empty[g]);
+                    if (last) mma_commit(&a_empty[g]);
                 }
                 mma_commit(&acc_full[a]);
             }
@@ -809,7 +829,7 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
 #pragma unroll 1
             for (int ch = 0; ch < tc2::kTok / 32; ++ch) {
                 uint32_t v[32];
-                tmem_ld32(tmem + a * tc2::kTok + 32 * ch + ((uint32_t)(32 * q) << 16), v);
+                tmem_ld32(tmem + tc2::kAcc + a * tc2::kTok + 32 * ch + ((uint32_t)(32 * q) << 16), v);
                 const int mbase = c.t * tc2::kTok + 32 * ch;
                 float *yb = Y + (size_t)mbase * out + o;
                 const float4 *s4 = reinterpret_cast<const float4 *>(&scl[a][32 * ch]);
@@ -839,7 +859,7 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
         tc2::cp_async_wait0();
     } else {
         // ------------------------------------------ weight expansion --
-        const int et = tid - 192;  // 0..127: weight row of the tile
+        const int et = 32 * (warp & 3) + lane;  // weight row of the tile = this warp's TMEM lane
         uint32_t pe = (1u << tc2::kMaxNg) - 1u;  // a_empty parity of group g in bit g
         tc2::Cursor c;
         for (bool more = c.begin(p, &s_tab); more && !s_abort; more = c.advance()) {
@@ -880,19 +900,23 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
                     break;
                 }
                 pe ^= 1u << g;
-                uint8_t *dst = sA + g * kOpBytes;
+                fence_after();
+                // row et of W' group g: column c of the group holds inputs 2c, 2c+1
+                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + tc2::kWcol + 64 * g;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    uint32_t h[4];
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t hv[32];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __half lo16 = __float2half_rn(lut[code_at<W>(w, 8 * j + 2 * e)] * nrm);
-                        const __half hi16 = __float2half_rn(lut[code_at<W>(w, 8 * j + 2 * e + 1)] * nrm);
-                        h[e] = (uint32_t)__half_as_ushort(lo16) | ((uint32_t)__half_as_ushort(hi16) << 16);
+                    for (int c2 = 0; c2 < 32; ++c2) {
+                        const int k = 2 * (32 * hf + c2);
+                        const __half lo16 = __float2half_rn(lut[code_at<W>(w, k)] * nrm);
+                        const __half hi16 = __float2half_rn(lut[code_at<W>(w, k + 1)] * nrm);
+                        hv[c2] = (uint32_t)__half_as_ushort(lo16) | ((uint32_t)__half_as_ushort(hi16) << 16);
                     }
-                    *reinterpret_cast<uint4 *>(dst + sw128_off(et, j)) = make_uint4(h[0], h[1], h[2], h[3]);
+                    tmem_st32(taddr + 32 * hf, hv);
                 }
-                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+                fence_before();
                 __syncwarp();
                 if (lane == 0) tc2::mbar_arrive(&a_full[g]);
 #pragma unroll
@@ -911,9 +935,9 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
     }
 }
 
-// Dynamic shared memory of the pipelined kernel: 4 x 32 KB of W', 5 x 16 KB
-// of activation stages, 1 KB of alignment slack.
-constexpr int kTc2MaxSmem = tc2::kMaxNg * tc::kOpBytes + tc2::kStages * tc2::kStageBytes + 1024;
+// Dynamic shared memory of the pipelined kernel: 6 x 32 KB of activation
+// stages, 1 KB of alignment slack.
+constexpr int kTc2MaxSmem = tc2::kStages * tc2::kStageBytes + 1024;
 
 template <int W>
 int launch_tc2(const tc2::Params &p, int grid, size_t smem, cudaStream_t st) {
@@ -929,7 +953,7 @@ int launch_tc2(const tc2::Params &p, int grid, size_t smem, cudaStream_t st) {
 }
 
 // 2-D tensor map over one rotated activation Z[M][in_pad] (fp16): boxes of
-// 32 inputs x 256 tokens, 64-byte swizzle, zero fill past M.
+// 64 inputs x 128 tokens, 128-byte swizzle, zero fill past M.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -949,10 +973,10 @@ static int make_z_map(CUtensorMap *map, const void *Z, int M, int in_pad) {
     }
     const cuuint64_t dims[2] = {(cuuint64_t)in_pad, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)in_pad * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)tc2::kStageK, (cuuint32_t)tc2::kTok};
+    const cuuint32_t box[2] = {64, (cuuint32_t)tc2::kTok};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(Z), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(CQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return CQ_OK;
@@ -1088,7 +1112,7 @@ static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, u
                 p.tail_T0 = p.m[j].tiles_before + (r0 - p.m[j].runs_before) * p.m[j].m_tiles;
                 break;
             }
-        const size_t smem = (size_t)ngmax * tc::kOpBytes + tc2::kStages * tc2::kStageBytes + 1024;
+        const size_t smem = (size_t)tc2::kStages * tc2::kStageBytes + 1024;
         int rc = CQ_OK;
         switch (W) {
         case 2: rc = launch_tc2<2>(p, grid, smem, st); break;
