@@ -137,6 +137,9 @@ __device__ __forceinline__ void rot_finish(const RotSlot &sl, int lane) {
 }
 
 __global__ void __launch_bounds__(256, 4) act_rotate_many_kernel(const __grid_constant__ RotTable r) {
+    // the GEMM that follows may launch now; it waits for this grid before it
+    // reads Z (griddepcontrol.wait in its TMA producer)
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int lane = threadIdx.x & 31;
     const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
     const long long total = r.task_before[r.n];
@@ -259,6 +262,8 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
 
 // The same with A read from tensor memory (a_tmem: lane = row, column c
 // holding K elements 2c, 2c+1 as fp16 low | high).
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 __device__ __forceinline__ void mma_f16_tA(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                            uint32_t acc) {
     asm volatile(
@@ -442,28 +447,23 @@ void launch_tc(const GemmParams &p, int grid, size_t smem, cudaStream_t st) {
 }
 
 // ------------------------------- pipelined GEMM for inputs up to 512 wide --
-// Persistent, one CTA per SM, warp-specialised:
-//   warp 0      TMA producer: rotated activations, one 128-token x 128-input
-//               stage (two 2-D TMA boxes of 64 inputs, 128-byte swizzle, rows
-//               past M zero-filled) per (token tile, group), 2-stage ring
-//   warp 1      MMA issuer: 8 x tcgen05.mma (M=128, N=128, K=16) per stage
-//               into one of two TMEM accumulators
-//   warps 2-5   epilogue: tcgen05.ld of an accumulator while the MMAs fill
-//               the other; Y[m][o] = D * s[m]/sqrt(128)
-//   warps 6-9   expand the 128 weight rows of a work item (all groups, up to
-//               4 x 32 KB) into W' = c[q]*n once; the item then streams up to
-//               8 token tiles against them
-// Hand-offs are mbarriers: a_full/a_empty (weights), b_full/b_empty (stages),
-// acc_full/acc_empty (accumulators). Every wait is bounded; on expiry the
-// status word records where, all roles drain, and TMEM is released.
+// Persistent, one CTA per SM, warp-specialised (roles at gemm_tc2_kernel).
+// Hand-offs are mbarriers: a_full/a_empty (W' groups in tensor memory),
+// b_full/b_empty (activation stages), acc_full/acc_empty (accumulators).
+// Every wait is bounded; on expiry the status word records where, all roles
+// drain, and TMEM is released.
 namespace tc2 {
 
 constexpr int kThreads = 320;
 constexpr int kMaxActs = 64;     // distinct activations (tensor maps) per launch
 constexpr int kMaxNg = 4;        // groups of the inputs kept resident
 constexpr int kTok = 128;        // MMA N: tokens of a tile
-constexpr int kStages = 6;       // activation stages, one 128-input group each (eight K=16 MMAs)
-constexpr int kStageBytes = kTok * kGroup * 2;  // 128 tokens x 128 inputs fp16: two 64-wide 128-byte-swizzled segments
+// Activation stages hold two 128-input groups (sixteen K=16 MMAs per commit):
+// on this GPU a stream of M=128, N=128 MMAs loses ~30 % of the tensor pipe
+// when a commit follows every eight of them, ~6 % at sixteen.
+constexpr int kStages = 3;
+constexpr int kGroupBytes = kTok * kGroup * 2;  // 128 tokens x 128 inputs fp16: two 64-wide 128-byte-swizzled segments
+constexpr int kStageBytes = 2 * kGroupBytes;
 constexpr int kAcc = 0;          // TMEM columns: accumulators at 0 and kTok
 constexpr int kWcol = 256;       // TMEM columns: W' group g at kWcol + 64 g (two fp16 per column)
 constexpr unsigned kSpin = 1u << 22;  // polls of one barrier (each may suspend ~1 us)
@@ -475,6 +475,7 @@ struct Mat {
     const float *xs;
     float *Y;
     int out, ng, M, lut, act, n_tiles, m_tiles, tiles_before, runs_before;
+    int w;  // code width in bits (2: CQ2 and ternary, 3, 4)
 };
 
 struct Params {
@@ -645,15 +646,92 @@ __device__ void drain_wait(uint64_t *bar, uint32_t parity) {
         if (tc::mbar_try_wait(bar, parity)) return;
 }
 
+
+// Expands the W' rows of one run into tensor memory. The calling thread
+// holds weight row o (its TMEM lane); group g goes to columns lane_tmem + 64 g,
+// column c holding inputs 2c (low half) and 2c+1 (high half), each
+// fp16(level) * norm rounded once to fp16. Group g is written once the MMAs of
+// the previous run are done with it (a_empty[g]) and handed to the MMA issuer
+// through a_full[g]; the codes and norm of group g+1 are fetched while group g
+// expands. All 32 lanes of the warp call this; `hlv` is the warp's private
+// 16-word table. Returns false if a wait gave up.
+template <int W>
+__device__ __forceinline__ bool expand_run(const Mat &G, const float *lv, int o, uint32_t *hlv, uint32_t lane_tmem,
+                                           uint64_t *a_empty, uint64_t *a_full, uint32_t &pe, volatile int *abort) {
+    using namespace tc;
+    const int lane = threadIdx.x & 31;
+    // CQ2 / ternary: entry v (a nibble: the codes of inputs 2c and 2c+1) holds
+    // the half2 of their two levels; CQ3 / CQ4: entry q holds level q. Sixteen
+    // words, so every lookup is free of bank conflicts.
+    if (lane < 16)
+        hlv[lane] = W == 2 ? h2_bits(__floats2half2_rn(lv[lane & 3], lv[lane >> 2]))
+                           : (uint32_t)__half_as_ushort(__float2half_rn(lv[lane]));
+    __syncwarp();
+    const bool orow = o < G.out;
+    const int ng = G.ng;
+    const uint4 *src = reinterpret_cast<const uint4 *>(G.codes + (size_t)o * ng * 16 * W);
+    const __half *nsrc = G.norms + (size_t)o * ng;
+    uint32_t w[4 * W];
+    __half nrm = __ushort_as_half(0);
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        const uint4 v = orow ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+        w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
+    }
+    if (orow) nrm = nsrc[0];
+    for (int g = 0; g < ng; ++g) {
+        uint32_t wn[4 * W];
+        __half nn = __ushort_as_half(0);
+        const bool more = orow && g + 1 < ng;
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            const uint4 v = more ? __ldg(src + (g + 1) * W + i) : make_uint4(0, 0, 0, 0);
+            wn[4 * i] = v.x, wn[4 * i + 1] = v.y, wn[4 * i + 2] = v.z, wn[4 * i + 3] = v.w;
+        }
+        if (more) nn = nsrc[g + 1];
+        if (!wait(&a_empty[g], (pe >> g) & 1u, abort, 0x47480006u)) return false;
+        pe ^= 1u << g;
+        fence_after();
+        const __half2 n2 = __half2half2(nrm);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            uint32_t hv[32];
+#pragma unroll
+            for (int c2 = 0; c2 < 32; ++c2) {
+                const int col = 32 * hf + c2;
+                uint32_t pair;
+                if (W == 2) {
+                    pair = hlv[(w[col >> 3] >> (4 * (col & 7))) & 15u];
+                } else if (W == 4) {
+                    const uint32_t b = (w[col >> 2] >> (8 * (col & 3))) & 255u;
+                    pair = __byte_perm(hlv[b & 15u], hlv[b >> 4], 0x5410);
+                } else {
+                    pair = __byte_perm(hlv[code_at<W>(w, 2 * col)], hlv[code_at<W>(w, 2 * col + 1)], 0x5410);
+                }
+                hv[c2] = h2_bits(__hmul2(bits_h2(pair), n2));
+            }
+            tmem_st32(lane_tmem + 64 * g + 32 * hf, hv);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[g]);
+#pragma unroll
+        for (int i = 0; i < 4 * W; ++i) w[i] = wn[i];
+        nrm = nn;
+    }
+    return true;
+}
+
 }  // namespace tc2
 
 // Pipelined, warp-specialised GEMM for inputs of at most 512 (ng <= 4
 // groups): the 128 x (128 ng) slice of W' stays in tensor memory, where the
 // MMAs read it as their A operand, for the whole run of token tiles that use
 // it; shared memory holds only activation stages.
-//   warp 0     TMA producer: Z tiles (128 tokens x 128 inputs) into six stages
+//   warp 0     TMA producer: Z tiles (128 tokens x 256 inputs) into three stages
 //   warp 1     MMA issuer: tcgen05.mma (M=128, N=128, A from TMEM) into two
-//              128-column TMEM accumulators, eight MMAs per stage
+//              128-column TMEM accumulators, sixteen MMAs per stage
 //   warps 2-5  epilogue: TMEM -> registers, token scale, fp32 stores of Y
 //   warps 6-9  expansion of the next run's codes and norms into fp16 W'
 //              rows of TMEM (tcgen05.st; each warp its lane quarter), one
@@ -662,17 +740,16 @@ __device__ void drain_wait(uint64_t *bar, uint32_t parity) {
 // Every wait is bounded; a role that gives up sets the abort flag, the others
 // leave their loops, and work already issued (TMA loads, MMAs) is waited for
 // before TMEM is freed.
-template <int W>
 __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid_constant__ tc2::Params p) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *sB = smem;  // kStages x 32 KB of Z
+    uint8_t *sB = smem;  // kStages x 64 KB of Z
     __shared__ __align__(8) uint64_t a_full[tc2::kMaxNg], a_empty[tc2::kMaxNg], b_full[tc2::kStages],
         b_empty[tc2::kStages], acc_full[2], acc_empty[2], drain;
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
-    __shared__ float s_lut[4][16];
+    __shared__ uint32_t s_hlv[4][16];  // per expansion warp: fp16 level table (see the expansion role)
     __shared__ __align__(16) float s_scale[4][2][tc2::kTok];  // per epilogue warp: token scales of two tiles
     __shared__ tc2::Mat s_mat[10];  // per warp: the current matrix (parameter reads
                                     // with a runtime index stay out of the loops)
@@ -709,19 +786,24 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
+            // Z is written by the rotation kernel this grid may overlap
+            asm volatile("griddepcontrol.wait;\n" ::: "memory");
             uint32_t s = 0, pe = (1u << tc2::kStages) - 1u;  // empty-phase parity of stage s in bit s
             uint32_t loaded = 0, pfull = 0;  // stages ever loaded; parity their last load completes
             tc2::Cursor c;
             for (bool more = c.begin(p, &s_tab); more; more = c.advance()) {
                 const int ng = c.ng();
                 const CUtensorMap *map = &p.tmap[c.act()];
-                for (int g = 0; g < ng; ++g) {  // one group per stage
+                for (int g = 0; g < ng; g += 2) {  // two groups per stage (one if ng is odd and g = ng-1)
+                    const int n2 = ng - g >= 2 ? 2 : 1;
                     if (!tc2::wait(&b_empty[s], (pe >> s) & 1u, &s_abort, 0x47480001u)) goto done_prod;
                     pe ^= 1u << s;
-                    tc2::mbar_expect_tx(&b_full[s], tc2::kStageBytes);
-                    tc2::tma_load_2d(sB + s * tc2::kStageBytes, map, g * kGroup, c.t * tc2::kTok, &b_full[s]);
-                    tc2::tma_load_2d(sB + s * tc2::kStageBytes + kSegBytes, map, g * kGroup + 64, c.t * tc2::kTok,
-                                     &b_full[s]);
+                    tc2::mbar_expect_tx(&b_full[s], n2 * tc2::kGroupBytes);
+                    for (int h = 0; h < n2; ++h) {
+                        uint8_t *dst = sB + s * tc2::kStageBytes + h * tc2::kGroupBytes;
+                        tc2::tma_load_2d(dst, map, (g + h) * kGroup, c.t * tc2::kTok, &b_full[s]);
+                        tc2::tma_load_2d(dst + kSegBytes, map, (g + h) * kGroup + 64, c.t * tc2::kTok, &b_full[s]);
+                    }
                     // the k-th load into stage s completes b_full phase k, whose
                     // parity equals bit s of pe after the flip above
                     pfull = (pfull & ~(1u << s)) | (pe & (1u << s));
@@ -750,27 +832,33 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
                 if (!tc2::wait(&acc_empty[a], (pae >> a) & 1u, &s_abort, 0x47480003u)) goto done_mma;
                 pae ^= 1u << a;
                 fence_after();
-                for (int g = 0; g < ng; ++g) {
-                    if (first) {
-                        if (!tc2::wait(&a_full[g], (paf >> g) & 1u, &s_abort, 0x47480002u)) goto done_mma;
-                        paf ^= 1u << g;
-                        fence_after();  // W' written with tcgen05.st by the expansion warps
-                    }
+                for (int g = 0; g < ng; g += 2) {  // stage s holds groups g and g+1 (if g+1 < ng)
+                    const int n2 = ng - g >= 2 ? 2 : 1;
                     // the stage was filled by TMA: its mbarrier orders the MMA's reads
                     if (!tc2::wait(&b_full[s], (pf >> s) & 1u, &s_abort, 0x47480004u)) goto done_mma;
                     pf ^= 1u << s;
-                    // K step kk: inputs 16kk .. 16kk+15 of the group; Z: 32 bytes into
-                    // the rows of segment kk/4; W': 8 TMEM columns
-                    const uint64_t db = sw128_desc(smem_u32(sB + s * tc2::kStageBytes));
-                    const uint32_t wa = tmem + tc2::kWcol + 64 * g, da = tmem + tc2::kAcc + a * tc2::kTok;
+                    const uint32_t da = tmem + tc2::kAcc + a * tc2::kTok;
+                    for (int h = 0; h < n2; ++h) {
+                        if (first) {  // a new run: group g+h of W' is being expanded
+                            if (!tc2::wait(&a_full[g + h], (paf >> (g + h)) & 1u, &s_abort, 0x47480002u))
+                                goto done_mma;
+                            paf ^= 1u << (g + h);
+                            fence_after();  // W' written with tcgen05.st by the expansion warps
+                        }
+                        // K step kk of group g+h: inputs 16kk .. 16kk+15; Z: 32 bytes into
+                        // the rows of segment kk/4; W': 8 TMEM columns
+                        const uint64_t db = sw128_desc(smem_u32(sB + s * tc2::kStageBytes + h * tc2::kGroupBytes));
+                        const uint32_t wa = tmem + tc2::kWcol + 64 * (g + h);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_f16_tA(da, wa + 8 * kk, db + (uint64_t)((kk >> 2) * (kSegBytes >> 4) + (kk & 3) * 2), idesc,
-                                   (g | kk) != 0);
-                    issued = true;
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_f16_tA(da, wa + 8 * kk, db + (uint64_t)((kk >> 2) * (kSegBytes >> 4) + (kk & 3) * 2),
+                                       idesc, ((g + h) | kk) != 0);
+                        issued = true;
+                    }
                     mma_commit(&b_empty[s]);
                     s = s + 1 == tc2::kStages ? 0 : s + 1;
-                    if (last) mma_commit(&a_empty[g]);
+                    if (last)
+                        for (int h = 0; h < n2; ++h) mma_commit(&a_empty[g + h]);
                 }
                 mma_commit(&acc_full[a]);
             }
@@ -860,69 +948,19 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
     } else {
         // ------------------------------------------ weight expansion --
         const int et = 32 * (warp & 3) + lane;  // weight row of the tile = this warp's TMEM lane
+        const uint32_t lane_tmem = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + tc2::kWcol;
         uint32_t pe = (1u << tc2::kMaxNg) - 1u;  // a_empty parity of group g in bit g
         tc2::Cursor c;
         for (bool more = c.begin(p, &s_tab); more && !s_abort; more = c.advance()) {
             if (!c.first()) continue;
             const tc2::Mat &G = tc2::warp_mat(p, c.mat, &s_mat[warp]);
-            // level table in warp-private shared memory (indexed by code)
-            if (lane < 16) s_lut[warp - 6][lane] = p.lut[G.lut][lane];
-            __syncwarp();
-            const float *lut = s_lut[warp - 6];
+            const float *lv = p.lut[G.lut];
             const int o = c.o0() + et;
-            const bool orow = o < G.out;
-            const int ng = G.ng;
-            const size_t rowBytes = (size_t)ng * 16 * W;
-            const uint4 *src = reinterpret_cast<const uint4 *>(G.codes + (size_t)o * rowBytes);
-            const __half *nsrc = G.norms + (size_t)o * ng;
-            // codes and norm of group g+1 are fetched while group g expands
-            uint32_t w[4 * W];
-            float nrm = 0.0f;
-#pragma unroll
-            for (int i = 0; i < W; ++i) {
-                const uint4 v = orow ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
-                w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
-            }
-            if (orow) nrm = __half2float(nsrc[0]);
-            bool ok = true;
-            for (int g = 0; g < ng; ++g) {
-                uint32_t wn[4 * W];
-                float nn = 0.0f;
-                const bool more = orow && g + 1 < ng;
-#pragma unroll
-                for (int i = 0; i < W; ++i) {
-                    const uint4 v = more ? __ldg(src + (g + 1) * W + i) : make_uint4(0, 0, 0, 0);
-                    wn[4 * i] = v.x, wn[4 * i + 1] = v.y, wn[4 * i + 2] = v.z, wn[4 * i + 3] = v.w;
-                }
-                if (more) nn = __half2float(nsrc[g + 1]);
-                if (!tc2::wait(&a_empty[g], (pe >> g) & 1u, &s_abort, 0x47480006u)) {
-                    ok = false;
-                    break;
-                }
-                pe ^= 1u << g;
-                fence_after();
-                // row et of W' group g: column c of the group holds inputs 2c, 2c+1
-                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + tc2::kWcol + 64 * g;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t hv[32];
-#pragma unroll
-                    for (int c2 = 0; c2 < 32; ++c2) {
-                        const int k = 2 * (32 * hf + c2);
-                        const __half lo16 = __float2half_rn(lut[code_at<W>(w, k)] * nrm);
-                        const __half hi16 = __float2half_rn(lut[code_at<W>(w, k + 1)] * nrm);
-                        hv[c2] = (uint32_t)__half_as_ushort(lo16) | ((uint32_t)__half_as_ushort(hi16) << 16);
-                    }
-                    tmem_st32(taddr + 32 * hf, hv);
-                }
-                asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-                fence_before();
-                __syncwarp();
-                if (lane == 0) tc2::mbar_arrive(&a_full[g]);
-#pragma unroll
-                for (int i = 0; i < 4 * W; ++i) w[i] = wn[i];
-                nrm = nn;
-            }
+            uint32_t *hlv = s_hlv[warp - 6];
+            const bool ok =
+                G.w == 2   ? tc2::expand_run<2>(G, lv, o, hlv, lane_tmem, a_empty, a_full, pe, &s_abort)
+                : G.w == 3 ? tc2::expand_run<3>(G, lv, o, hlv, lane_tmem, a_empty, a_full, pe, &s_abort)
+                           : tc2::expand_run<4>(G, lv, o, hlv, lane_tmem, a_empty, a_full, pe, &s_abort);
             if (!ok) break;
         }
     }
@@ -935,20 +973,34 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
     }
 }
 
-// Dynamic shared memory of the pipelined kernel: 6 x 32 KB of activation
+// Dynamic shared memory of the pipelined kernel: 3 x 64 KB of activation
 // stages, 1 KB of alignment slack.
 constexpr int kTc2MaxSmem = tc2::kStages * tc2::kStageBytes + 1024;
 
-template <int W>
+// Launched as a programmatic dependent of the activation rotation, which
+// lets it start as that kernel's blocks retire: the prologue and the first
+// weight expansions overlap the rotation's tail, and only the TMA producer
+// waits (griddepcontrol.wait) for the rotated activations.
 int launch_tc2(const tc2::Params &p, int grid, size_t smem, cudaStream_t st) {
     static bool attr = false;
     if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        const cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    kTc2MaxSmem);
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm smem attribute: %s", cudaGetErrorString(e));
         attr = true;
     }
-    gemm_tc2_kernel<W><<<grid, tc2::kThreads, smem, st>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(tc2::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, p);
+    if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
     return CQ_OK;
 }
 
@@ -1093,7 +1145,9 @@ static void level_table(const cq_gemm_desc &d, float lut[16]) {
 
 // The pipelined kernel over every descriptor of code width W whose input is
 // at most 512 wide; launches as often as its parameter block fills.
-static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, int W, cudaStream_t st) {
+// All matrices with in <= 512, whatever their code width, in one launch (more
+// only when a parameter block fills up).
+static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, cudaStream_t st) {
     static tc2::Params p;
     std::vector<int> map_of(pl.ptr.size(), -1);
     int nmaps = 0, nlut = 0, tiles = 0, runs = 0, ngmax = 0;
@@ -1113,12 +1167,7 @@ static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, u
                 break;
             }
         const size_t smem = (size_t)tc2::kStages * tc2::kStageBytes + 1024;
-        int rc = CQ_OK;
-        switch (W) {
-        case 2: rc = launch_tc2<2>(p, grid, smem, st); break;
-        case 3: rc = launch_tc2<3>(p, grid, smem, st); break;
-        case 4: rc = launch_tc2<4>(p, grid, smem, st); break;
-        }
+        const int rc = launch_tc2(p, grid, smem, st);
         if (rc) return rc;
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
@@ -1132,8 +1181,8 @@ static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, u
     for (int i = 0; i < n; ++i) order[i] = i;
     std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return pl.act_of[x] < pl.act_of[y]; });
     for (int i : order) {
-        if (pl.act_of[i] < 0 || width_of(d[i].bits) != W) continue;
-        const int ip = in_padded(d[i].in), ng = ip / kGroup;
+        if (pl.act_of[i] < 0) continue;
+        const int ip = in_padded(d[i].in), ng = ip / kGroup, W = width_of(d[i].bits);
         if (ng > tc2::kMaxNg) continue;
         const int a = pl.act_of[i];
         float lut[16];
@@ -1166,6 +1215,7 @@ static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, u
         G.M = d[i].M;
         G.lut = li;
         G.act = map_of[a];
+        G.w = W;
         G.n_tiles = (G.out + tc::kTileRows - 1) / tc::kTileRows;
         G.m_tiles = (G.M + tc2::kTok - 1) / tc2::kTok;
         G.tiles_before = tiles;
@@ -1200,9 +1250,11 @@ static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "act_rotate launch: %s", cudaGetErrorString(e));
 
-    for (int W = 2; W <= 4; ++W) {
-        const int e2 = run_gemm_pipelined(d, n, pl, ws, W, st);
+    {
+        const int e2 = run_gemm_pipelined(d, n, pl, ws, st);
         if (e2) return e2;
+    }
+    for (int W = 2; W <= 4; ++W) {
         static GemmParams p;
         p.n = 0;
         int nlut = 0, tiles = 0;
