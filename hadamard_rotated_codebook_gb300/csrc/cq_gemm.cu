@@ -447,25 +447,15 @@ void launch_tc(const GemmParams &p, int grid, size_t smem, cudaStream_t st) {
 }
 
 // ------------------------------- pipelined GEMM for inputs up to 512 wide --
-// Persistent, one CTA per SM, warp-specialised (roles at gemm_tc2_kernel).
-// Hand-offs are mbarriers: a_full/a_empty (W' groups in tensor memory),
-// b_full/b_empty (activation stages), acc_full/acc_empty (accumulators).
-// Every wait is bounded; on expiry the status word records where, all roles
-// drain, and TMEM is released.
+// Pieces of the persistent, warp-specialised GEMM below (gemm_x8_kernel):
+// its parameter block, tile schedule and bounded mbarrier waits. Every wait
+// is bounded; on expiry the status word records where, all roles drain, and
+// TMEM is released.
 namespace tc2 {
 
-constexpr int kThreads = 320;
 constexpr int kMaxActs = 64;     // distinct activations (tensor maps) per launch
 constexpr int kMaxNg = 4;        // groups of the inputs kept resident
-constexpr int kTok = 128;        // MMA N: tokens of a tile
-// Activation stages hold two 128-input groups (sixteen K=16 MMAs per commit):
-// on this GPU a stream of M=128, N=128 MMAs loses ~30 % of the tensor pipe
-// when a commit follows every eight of them, ~6 % at sixteen.
-constexpr int kStages = 3;
-constexpr int kGroupBytes = kTok * kGroup * 2;  // 128 tokens x 128 inputs fp16: two 64-wide 128-byte-swizzled segments
-constexpr int kStageBytes = 2 * kGroupBytes;
-constexpr int kAcc = 0;          // TMEM columns: accumulators at 0 and kTok
-constexpr int kWcol = 256;       // TMEM columns: W' group g at kWcol + 64 g (two fp16 per column)
+constexpr int kTok = 128;        // tokens of a tile
 constexpr unsigned kSpin = 1u << 22;  // polls of one barrier (each may suspend ~1 us)
 constexpr unsigned kDrainSpin = 1u << 20;
 
@@ -614,16 +604,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
         : "memory");
 }
-// 4-byte asynchronous copy global -> shared; `valid` false zero-fills.
-__device__ __forceinline__ void cp_async4(void *dst, const void *src, bool valid) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(tc::smem_u32(dst)), "l"(src),
-                 "r"(valid ? 4 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
-
 // Bounded wait for the phase of `bar` with parity `parity`; gives up when
 // another role aborted or after kSpin polls (then records `code`).
 __device__ bool wait(uint64_t *bar, uint32_t parity, volatile int *abort, unsigned code) {
@@ -646,76 +626,163 @@ __device__ void drain_wait(uint64_t *bar, uint32_t parity) {
         if (tc::mbar_try_wait(bar, parity)) return;
 }
 
+}  // namespace tc2
 
-// Expands the W' rows of one run into tensor memory. The calling thread
-// holds weight row o (its TMEM lane); group g goes to columns lane_tmem + 64 g,
-// column c holding inputs 2c (low half) and 2c+1 (high half), each
-// fp16(level) * norm rounded once to fp16. Group g is written once the MMAs of
-// the previous run are done with it (a_empty[g]) and handed to the MMA issuer
-// through a_full[g]; the codes and norm of group g+1 are fetched while group g
-// expands. All 32 lanes of the warp call this; `hlv` is the warp's private
-// 16-word table. Returns false if a wait gave up.
+// ------------------------ pipelined GEMM on int8 activations (in <= 512) --
+// The rotated-domain product, with the rotation moved onto the weights:
+// H is symmetric and orthonormal, so per group
+//     n * <c[q], H x> = <n * H c[q], x>,
+// and the weight tile W''[o][k] = n[o] * (H c[q[o]])[k] (fp16) meets the
+// int8 activations q directly: Y[m][o] = s[m] * sum_k W''[o][k] q[m][k].
+// The FWHT runs once per run of token tiles on 128 weight rows, instead of
+// once per token on every activation, and the activations stay int8 until
+// they reach tensor memory (exactly as fp16: |q| <= 128).
+//   warp 0      TMA producer: int8 X groups (128 tokens x 128 inputs, 16 KB,
+//               128-byte swizzle) into four stages
+//   warp 1      MMA issuer: tcgen05.mma (M = 128 tokens, N = 128 weight
+//               rows, K = 16; A = X from TMEM, B = W'' from shared memory),
+//               sixteen MMAs (two groups) per commit, into two 128-column
+//               TMEM accumulators D[token][row]
+//   warps 2-5   conversion: each lane its token row of a stage, int8 -> fp16
+//               pairs, tcgen05.st into one of two 128-column X slots
+//   warps 6-9   epilogue: D -> registers, Y[m][o0..o0+127] = D * s[m];
+//               32 x 32 blocks pass through shared memory so that eight
+//               lanes store one 128-byte row segment of Y
+//   warps 10-13 expansion: W'' rows of the next run into shared memory
+//               (one thread per row), one group at a time, as soon as the
+//               MMAs of the previous run are done with that group
+namespace tc3 {
+
+constexpr int kThreads = 448;
+constexpr int kStages = 4;                            // X stages, one group each
+constexpr int kStageBytes = tc2::kTok * kGroup;       // 128 tokens x 128 inputs int8
+constexpr int kWGroupBytes = tc::kTileRows * kGroup * 2;  // W'' group: two 64-wide segments
+constexpr int kAcc = 0;                               // TMEM columns of the accumulators (0, 128)
+constexpr int kXcol = 256;                            // TMEM columns of the X slots (256, 384)
+constexpr int kStageY = 32 * 128;                     // per epilogue warp: 32 rows x 32 fp32, transposed
+constexpr int kSmem = tc2::kMaxNg * kWGroupBytes + kStages * kStageBytes + 4 * kStageY + 1024;
+
+// 16-byte shared-memory accesses by 32-bit shared address. The dynamic
+// shared memory is re-aligned through an integer, after which the compiler
+// no longer knows that the pointers are shared (it would emit generic
+// accesses, ordered against the global stores of the epilogue).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Sylvester-ordered FWHT of 64 values in registers (no normalisation).
+__device__ __forceinline__ void fwht64(float (&a)[64]) {
+#pragma unroll
+    for (int h = 1; h < 64; h <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+            if (!(k & h)) {
+                const float x = a[k], y = a[k + h];
+                a[k] = x + y;
+                a[k + h] = x - y;
+            }
+        }
+    }
+}
+
+// One W'' row of one run (this thread's weight row o), group by group into
+// shared memory, K-major with 128-byte swizzle (row e of the tile, segment
+// s holds inputs 64 s .. 64 s + 63). H_128 = [[H_64, H_64], [H_64, -H_64]],
+// so the first 64 outputs are H_64 (v_lo + v_hi) and the last 64 are
+// H_64 (v_lo - v_hi), v = c[q] the group's levels; both are scaled by
+// n / sqrt(128) and rounded once to fp16. Group g is written once the MMAs of
+// the previous run are done with it (w_empty[g]) and handed over through
+// w_full[g]. All 32 lanes of the warp call this. False if a wait gave up.
+//
+// Level tables (`tab`: this warp's 32 floats). CQ2 / ternary: the pairs of
+// inputs k and k+64 that the first step of H_128 combines are read at once,
+// tab[v] = c[v & 3] + c[v >> 2] and tab[16 + v] = c[v & 3] - c[v >> 2] for
+// the nibble v = q[k] | q[k+64] << 2; other widths: tab[q] = c[q].
 template <int W>
-__device__ __forceinline__ bool expand_run(const Mat &G, const float *lv, int o, uint32_t *hlv, uint32_t lane_tmem,
-                                           uint64_t *a_empty, uint64_t *a_full, uint32_t &pe, volatile int *abort) {
-    using namespace tc;
+__device__ __forceinline__ bool expand_row(const tc2::Mat &G, const float *levels, float *tab, int o, int e,
+                                           uint8_t *sW, uint64_t *w_empty, uint64_t *w_full, uint32_t &pe,
+                                           volatile int *abort) {
     const int lane = threadIdx.x & 31;
-    // CQ2 / ternary: entry v (a nibble: the codes of inputs 2c and 2c+1) holds
-    // the half2 of their two levels; CQ3 / CQ4: entry q holds level q. Sixteen
-    // words, so every lookup is free of bank conflicts.
-    if (lane < 16)
-        hlv[lane] = W == 2 ? h2_bits(__floats2half2_rn(lv[lane & 3], lv[lane >> 2]))
-                           : (uint32_t)__half_as_ushort(__float2half_rn(lv[lane]));
+    __syncwarp();  // the previous run's reads of the table are done
+    if (W == 2) {
+        const int v = lane & 15;
+        tab[lane] = lane < 16 ? levels[v & 3] + levels[v >> 2] : levels[v & 3] - levels[v >> 2];
+    } else if (lane < 16) {
+        tab[lane] = levels[lane];
+    }
     __syncwarp();
     const bool orow = o < G.out;
     const int ng = G.ng;
     const uint4 *src = reinterpret_cast<const uint4 *>(G.codes + (size_t)o * ng * 16 * W);
     const __half *nsrc = G.norms + (size_t)o * ng;
     uint32_t w[4 * W];
-    __half nrm = __ushort_as_half(0);
+    float nrm = 0.0f;
 #pragma unroll
     for (int i = 0; i < W; ++i) {
         const uint4 v = orow ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
         w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
     }
-    if (orow) nrm = nsrc[0];
+    if (orow) nrm = __half2float(nsrc[0]);
     for (int g = 0; g < ng; ++g) {
         uint32_t wn[4 * W];
-        __half nn = __ushort_as_half(0);
+        float nn = 0.0f;
         const bool more = orow && g + 1 < ng;
 #pragma unroll
         for (int i = 0; i < W; ++i) {
             const uint4 v = more ? __ldg(src + (g + 1) * W + i) : make_uint4(0, 0, 0, 0);
             wn[4 * i] = v.x, wn[4 * i + 1] = v.y, wn[4 * i + 2] = v.z, wn[4 * i + 3] = v.w;
         }
-        if (more) nn = nsrc[g + 1];
-        if (!wait(&a_empty[g], (pe >> g) & 1u, abort, 0x47480006u)) return false;
+        if (more) nn = __half2float(nsrc[g + 1]);
+        if (!tc2::wait(&w_empty[g], (pe >> g) & 1u, abort, 0x47480016u)) return false;
         pe ^= 1u << g;
-        fence_after();
-        const __half2 n2 = __half2half2(nrm);
+        const float sc = nrm * kInvSqrt128;
+        const uint32_t row = tc::smem_u32(sW) + g * kWGroupBytes + (e >> 3) * 1024 + (e & 7) * 128;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            // the codes are re-read by each pass (keeps the table addresses
+            // from being computed once and held across the passes)
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            uint32_t hv[32];
+            for (int i = 0; i < 4 * W; ++i) asm volatile("" : "+r"(w[i]));
+            // a = v_lo + v_hi (pass 0) or v_lo - v_hi (pass 1)
+            float a[64];
+            if (W == 2) {
+                const float *t = tab + 16 * pass;
 #pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2) {
-                const int col = 32 * hf + c2;
-                uint32_t pair;
-                if (W == 2) {
-                    pair = hlv[(w[col >> 3] >> (4 * (col & 7))) & 15u];
-                } else if (W == 4) {
-                    const uint32_t b = (w[col >> 2] >> (8 * (col & 3))) & 255u;
-                    pair = __byte_perm(hlv[b & 15u], hlv[b >> 4], 0x5410);
-                } else {
-                    pair = __byte_perm(hlv[code_at<W>(w, 2 * col)], hlv[code_at<W>(w, 2 * col + 1)], 0x5410);
+                for (int m = 0; m < 4; ++m) {  // word m: codes 16m .. 16m+15; word m+4: the same + 64
+                    const uint32_t ev = (w[m] & 0x33333333u) | ((w[m + 4] & 0x33333333u) << 2);
+                    const uint32_t od = ((w[m] >> 2) & 0x33333333u) | (w[m + 4] & 0xCCCCCCCCu);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        a[16 * m + 2 * j] = t[(ev >> (4 * j)) & 15u];
+                        a[16 * m + 2 * j + 1] = t[(od >> (4 * j)) & 15u];
+                    }
                 }
-                hv[c2] = h2_bits(__hmul2(bits_h2(pair), n2));
+            } else {
+                const float sgn = pass ? -1.0f : 1.0f;
+#pragma unroll
+                for (int k = 0; k < 64; ++k) a[k] = fmaf(sgn, tab[code_at<W>(w, k + 64)], tab[code_at<W>(w, k)]);
             }
-            tmem_st32(lane_tmem + 64 * g + 32 * hf, hv);
+            fwht64(a);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint4 c;
+                c.x = tc::h2_bits(__floats2half2_rn(a[8 * j] * sc, a[8 * j + 1] * sc));
+                c.y = tc::h2_bits(__floats2half2_rn(a[8 * j + 2] * sc, a[8 * j + 3] * sc));
+                c.z = tc::h2_bits(__floats2half2_rn(a[8 * j + 4] * sc, a[8 * j + 5] * sc));
+                c.w = tc::h2_bits(__floats2half2_rn(a[8 * j + 6] * sc, a[8 * j + 7] * sc));
+                sts128(row + pass * tc::kSegBytes + ((j ^ (e & 7)) << 4), c);
+            }
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-        fence_before();
+        // generic-proxy stores, read next by the tensor cores (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[g]);
+        if (lane == 0) tc2::mbar_arrive(&w_full[g]);
 #pragma unroll
         for (int i = 0; i < 4 * W; ++i) w[i] = wn[i];
         nrm = nn;
@@ -723,55 +790,51 @@ __device__ __forceinline__ bool expand_run(const Mat &G, const float *lv, int o,
     return true;
 }
 
-}  // namespace tc2
+// int8 x 4 (one word) -> two fp16 pairs, exactly: bias to unsigned, place
+// each byte under the exponent of 1024 (0x64xx = 1024 + byte), subtract 1152.
+__device__ __forceinline__ void i8x4_to_h2(uint32_t v, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = v ^ 0x80808080u;
+    const __half2 off = __floats2half2_rn(1152.0f, 1152.0f);
+    lo = tc::h2_bits(__hsub2(tc::bits_h2(__byte_perm(u, 0x64646464u, 0x5140)), off));
+    hi = tc::h2_bits(__hsub2(tc::bits_h2(__byte_perm(u, 0x64646464u, 0x5342)), off));
+}
 
-// Pipelined, warp-specialised GEMM for inputs of at most 512 (ng <= 4
-// groups): the 128 x (128 ng) slice of W' stays in tensor memory, where the
-// MMAs read it as their A operand, for the whole run of token tiles that use
-// it; shared memory holds only activation stages.
-//   warp 0     TMA producer: Z tiles (128 tokens x 256 inputs) into three stages
-//   warp 1     MMA issuer: tcgen05.mma (M=128, N=128, A from TMEM) into two
-//              128-column TMEM accumulators, sixteen MMAs per stage
-//   warps 2-5  epilogue: TMEM -> registers, token scale, fp32 stores of Y
-//   warps 6-9  expansion of the next run's codes and norms into fp16 W'
-//              rows of TMEM (tcgen05.st; each warp its lane quarter), one
-//              group at a time, as soon as the MMAs of the previous run are
-//              done with that group
-// Every wait is bounded; a role that gives up sets the abort flag, the others
-// leave their loops, and work already issued (TMA loads, MMAs) is waited for
-// before TMEM is freed.
-__global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid_constant__ tc2::Params p) {
+}  // namespace tc3
+
+__global__ void __launch_bounds__(tc3::kThreads, 1) gemm_x8_kernel(const __grid_constant__ tc2::Params p) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *sB = smem;  // kStages x 64 KB of Z
-    __shared__ __align__(8) uint64_t a_full[tc2::kMaxNg], a_empty[tc2::kMaxNg], b_full[tc2::kStages],
-        b_empty[tc2::kStages], acc_full[2], acc_empty[2], drain;
+    uint8_t *sW = smem;                                         // kMaxNg x 32 KB: W'' groups
+    uint8_t *sX = smem + tc2::kMaxNg * tc3::kWGroupBytes;       // kStages x 16 KB: int8 X
+    uint8_t *sY = sX + tc3::kStages * tc3::kStageBytes;         // 4 x 4 KB: epilogue transposes
+    __shared__ __align__(8) uint64_t w_full[tc2::kMaxNg], w_empty[tc2::kMaxNg], x_full[tc3::kStages],
+        x_empty[tc3::kStages], t_full[2], t_empty[2], acc_full[2], acc_empty[2], drain;
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
-    __shared__ uint32_t s_hlv[4][16];  // per expansion warp: fp16 level table (see the expansion role)
-    __shared__ __align__(16) float s_scale[4][2][tc2::kTok];  // per epilogue warp: token scales of two tiles
-    __shared__ tc2::Mat s_mat[10];  // per warp: the current matrix (parameter reads
-                                    // with a runtime index stay out of the loops)
+    __shared__ float s_lv[4][32];    // per expansion warp: level tables (see expand_row)
+    __shared__ tc2::Mat s_mat[14];   // per warp: the current matrix
     __shared__ tc2::SchedTab s_tab;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     tc2::load_sched(p, &s_tab);
 
-    if (warp == 0) {  // two 128-column fp32 accumulators and 256 columns of W'
+    if (warp == 0) {  // two 128-column fp32 accumulators and two 128-column X slots
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&s_tmem)),
                      "r"(512));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
     }
     if (tid == 0) {
         for (int g = 0; g < tc2::kMaxNg; ++g) {
-            mbar_init(&a_full[g], 4);
-            mbar_init(&a_empty[g], 1);
+            mbar_init(&w_full[g], 4);
+            mbar_init(&w_empty[g], 1);
         }
-        for (int i = 0; i < tc2::kStages; ++i) {
-            mbar_init(&b_full[i], 1);
-            mbar_init(&b_empty[i], 1);
+        for (int i = 0; i < tc3::kStages; ++i) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], 4);
         }
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&t_full[i], 4);
+            mbar_init(&t_empty[i], 1);
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], 4);
         }
@@ -786,42 +849,35 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            // Z is written by the rotation kernel this grid may overlap
+            // X may be written by the kernel this grid overlaps (padded copies)
             asm volatile("griddepcontrol.wait;\n" ::: "memory");
-            uint32_t s = 0, pe = (1u << tc2::kStages) - 1u;  // empty-phase parity of stage s in bit s
+            uint32_t s = 0, pe = (1u << tc3::kStages) - 1u;  // empty-phase parity of stage s in bit s
             uint32_t loaded = 0, pfull = 0;  // stages ever loaded; parity their last load completes
             tc2::Cursor c;
             for (bool more = c.begin(p, &s_tab); more; more = c.advance()) {
                 const int ng = c.ng();
                 const CUtensorMap *map = &p.tmap[c.act()];
-                for (int g = 0; g < ng; g += 2) {  // two groups per stage (one if ng is odd and g = ng-1)
-                    const int n2 = ng - g >= 2 ? 2 : 1;
-                    if (!tc2::wait(&b_empty[s], (pe >> s) & 1u, &s_abort, 0x47480001u)) goto done_prod;
+                for (int g = 0; g < ng; ++g) {
+                    if (!tc2::wait(&x_empty[s], (pe >> s) & 1u, &s_abort, 0x47480011u)) goto done_prod;
                     pe ^= 1u << s;
-                    tc2::mbar_expect_tx(&b_full[s], n2 * tc2::kGroupBytes);
-                    for (int h = 0; h < n2; ++h) {
-                        uint8_t *dst = sB + s * tc2::kStageBytes + h * tc2::kGroupBytes;
-                        tc2::tma_load_2d(dst, map, (g + h) * kGroup, c.t * tc2::kTok, &b_full[s]);
-                        tc2::tma_load_2d(dst + kSegBytes, map, (g + h) * kGroup + 64, c.t * tc2::kTok, &b_full[s]);
-                    }
-                    // the k-th load into stage s completes b_full phase k, whose
-                    // parity equals bit s of pe after the flip above
+                    tc2::mbar_expect_tx(&x_full[s], tc3::kStageBytes);
+                    tc2::tma_load_2d(sX + s * tc3::kStageBytes, map, g * kGroup, c.t * tc2::kTok, &x_full[s]);
                     pfull = (pfull & ~(1u << s)) | (pe & (1u << s));
                     loaded |= 1u << s;
-                    s = s + 1 == tc2::kStages ? 0 : s + 1;
+                    s = s + 1 == tc3::kStages ? 0 : s + 1;
                 }
             }
         done_prod:
             if (s_abort)  // copies still in flight land before the CTA exits
-                for (int i = 0; i < tc2::kStages; ++i)
-                    if (loaded >> i & 1u) tc2::drain_wait(&b_full[i], (pfull >> i) & 1u);
+                for (int i = 0; i < tc3::kStages; ++i)
+                    if (loaded >> i & 1u) tc2::drain_wait(&x_full[i], (pfull >> i) & 1u);
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16(kTileRows, tc2::kTok);
-            // parities in bit i: stage full (pf), accumulator empty (pae), W' group full (paf)
-            uint32_t s = 0, pf = 0u, pae = 3u, paf = 0u;
+            const uint32_t idesc = idesc_f16(tc2::kTok, kTileRows);
+            // parities in bit i: X slot full (ptf), accumulator empty (pae), W'' group full (pwf)
+            uint32_t sl = 0, ptf = 0u, pae = 3u, pwf = 0u;
             int acc = 0;
             bool issued = false;
             tc2::Cursor c;
@@ -829,36 +885,36 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
                 const int ng = c.ng();
                 const bool first = c.first(), last = c.last();
                 const int a = acc & 1;
-                if (!tc2::wait(&acc_empty[a], (pae >> a) & 1u, &s_abort, 0x47480003u)) goto done_mma;
+                if (!tc2::wait(&acc_empty[a], (pae >> a) & 1u, &s_abort, 0x47480013u)) goto done_mma;
                 pae ^= 1u << a;
                 fence_after();
-                for (int g = 0; g < ng; g += 2) {  // stage s holds groups g and g+1 (if g+1 < ng)
-                    const int n2 = ng - g >= 2 ? 2 : 1;
-                    // the stage was filled by TMA: its mbarrier orders the MMA's reads
-                    if (!tc2::wait(&b_full[s], (pf >> s) & 1u, &s_abort, 0x47480004u)) goto done_mma;
-                    pf ^= 1u << s;
-                    const uint32_t da = tmem + tc2::kAcc + a * tc2::kTok;
+                const uint32_t da = tmem + tc3::kAcc + a * kTileRows;
+                for (int g0 = 0; g0 < ng; g0 += 2) {  // X slot sl holds groups g0 and g0+1 (if g0+1 < ng)
+                    const int n2 = ng - g0 >= 2 ? 2 : 1;
+                    if (!tc2::wait(&t_full[sl], (ptf >> sl) & 1u, &s_abort, 0x47480014u)) goto done_mma;
+                    ptf ^= 1u << sl;
+                    fence_after();  // X written with tcgen05.st by the conversion warps
                     for (int h = 0; h < n2; ++h) {
-                        if (first) {  // a new run: group g+h of W' is being expanded
-                            if (!tc2::wait(&a_full[g + h], (paf >> (g + h)) & 1u, &s_abort, 0x47480002u))
-                                goto done_mma;
-                            paf ^= 1u << (g + h);
-                            fence_after();  // W' written with tcgen05.st by the expansion warps
+                        const int g = g0 + h;
+                        if (first) {  // a new run: W'' group g is being expanded
+                            if (!tc2::wait(&w_full[g], (pwf >> g) & 1u, &s_abort, 0x47480012u)) goto done_mma;
+                            pwf ^= 1u << g;
+                            fence_after();
                         }
-                        // K step kk of group g+h: inputs 16kk .. 16kk+15; Z: 32 bytes into
-                        // the rows of segment kk/4; W': 8 TMEM columns
-                        const uint64_t db = sw128_desc(smem_u32(sB + s * tc2::kStageBytes + h * tc2::kGroupBytes));
-                        const uint32_t wa = tmem + tc2::kWcol + 64 * (g + h);
+                        // K step kk: inputs 16kk .. 16kk+15 of group g; X: 8 TMEM columns;
+                        // W'': 32 bytes into the rows of segment kk/4
+                        const uint64_t db = sw128_desc(smem_u32(sW + g * tc3::kWGroupBytes));
+                        const uint32_t xa = tmem + tc3::kXcol + 128 * sl + 64 * h;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            mma_f16_tA(da, wa + 8 * kk, db + (uint64_t)((kk >> 2) * (kSegBytes >> 4) + (kk & 3) * 2),
-                                       idesc, ((g + h) | kk) != 0);
+                            mma_f16_tA(da, xa + 8 * kk, db + (uint64_t)((kk >> 2) * (kSegBytes >> 4) + (kk & 3) * 2),
+                                       idesc, (g | kk) != 0);
                         issued = true;
                     }
-                    mma_commit(&b_empty[s]);
-                    s = s + 1 == tc2::kStages ? 0 : s + 1;
+                    mma_commit(&t_empty[sl]);
+                    sl ^= 1u;
                     if (last)
-                        for (int h = 0; h < n2; ++h) mma_commit(&a_empty[g + h]);
+                        for (int h = 0; h < n2; ++h) mma_commit(&w_empty[g0 + h]);
                 }
                 mma_commit(&acc_full[a]);
             }
@@ -869,98 +925,141 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
             }
         }
     } else if (warp < 6) {
+        // ------------------------------------------------- conversion --
+        const int q = warp & 3;          // TMEM lane quarter of this warp
+        const int r = 32 * q + lane;     // token row of the tile
+        const uint32_t lane_x = tmem + tc3::kXcol + ((uint32_t)(32 * q) << 16);
+        uint32_t s = 0, pf = 0u, pte = 3u, sl = 0;
+        tc2::Cursor c;
+        for (bool more = c.begin(p, &s_tab); more && !s_abort; more = c.advance()) {
+            const int ng = c.ng();
+            bool ok = true;
+            for (int g0 = 0; g0 < ng && ok; g0 += 2) {
+                const int n2 = ng - g0 >= 2 ? 2 : 1;
+                if (!tc2::wait(&t_empty[sl], (pte >> sl) & 1u, &s_abort, 0x47480015u)) {
+                    ok = false;
+                    break;
+                }
+                pte ^= 1u << sl;
+                fence_after();  // the MMAs that read this slot are complete
+                for (int h = 0; h < n2; ++h) {
+                    if (!tc2::wait(&x_full[s], (pf >> s) & 1u, &s_abort, 0x47480017u)) {
+                        ok = false;
+                        break;
+                    }
+                    pf ^= 1u << s;
+                    // row r of the stage: eight 16-byte chunks, chunk j at j ^ (r & 7)
+                    const uint32_t row = smem_u32(sX) + s * tc3::kStageBytes + r * 128;
+                    uint4 v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] = tc3::lds128(row + ((j ^ (r & 7)) << 4));
+                    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // before TMA refills it
+                    __syncwarp();
+                    if (lane == 0) tc2::mbar_arrive(&x_empty[s]);
+                    s = s + 1 == tc3::kStages ? 0 : s + 1;
+                    // column c of the group holds inputs 2c (low half) and 2c+1
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t hv[32];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 x = v[4 * hf + j];
+                            tc3::i8x4_to_h2(x.x, hv[8 * j], hv[8 * j + 1]);
+                            tc3::i8x4_to_h2(x.y, hv[8 * j + 2], hv[8 * j + 3]);
+                            tc3::i8x4_to_h2(x.z, hv[8 * j + 4], hv[8 * j + 5]);
+                            tc3::i8x4_to_h2(x.w, hv[8 * j + 6], hv[8 * j + 7]);
+                        }
+                        tmem_st32(lane_x + 128 * sl + 64 * h + 32 * hf, hv);
+                    }
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+                if (!ok) break;
+                fence_before();
+                __syncwarp();
+                if (lane == 0) tc2::mbar_arrive(&t_full[sl]);
+                sl ^= 1u;
+            }
+            if (!ok) break;
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+    } else if (warp < 10) {
         // --------------------------------------------------- epilogue --
         const int q = warp & 3;  // TMEM lane quarter of this warp
-        float(*scl)[tc2::kTok] = s_scale[warp - 2];
-        int cur = -1;  // matrix held in s_mat[warp]
-        // token scales of the tile at `nx` (none if !valid) into buffer b (zero
-        // past M), one cp.async group
-        auto prefetch = [&](const tc2::Cursor &nx, bool valid, int b) {
-            if (valid) {
-                const bool same = nx.mat == cur;
-                const float *xs = same ? s_mat[warp].xs : p.m[nx.mat].xs;
-                const int Mtok = same ? s_mat[warp].M : p.m[nx.mat].M;
-#pragma unroll
-                for (int j = 0; j < tc2::kTok / 32; ++j) {
-                    const int m = nx.t * tc2::kTok + 32 * j + lane;
-                    tc2::cp_async4(&scl[b][32 * j + lane], m < Mtok ? xs + m : xs, m < Mtok);
-                }
-            }
-            tc2::cp_async_commit();
-        };
+        const int r = 32 * q + lane;
+        int cur = -1;
         uint32_t pfa = 0u;  // accumulator-full parity of buffer a in bit a
         int acc = 0;
         tc2::Cursor c;
-        bool more = c.begin(p, &s_tab);
-        prefetch(c, more, 0);
-        for (; more && !s_abort; more = c.advance(), ++acc) {
+        for (bool more = c.begin(p, &s_tab); more && !s_abort; more = c.advance(), ++acc) {
             if (c.mat != cur) {
                 tc2::warp_mat(p, c.mat, &s_mat[warp]);
                 cur = c.mat;
             }
             const tc2::Mat &G = s_mat[warp];
-            const int out = G.out, Mtok = G.M;
-            float *Y = G.Y;
-            const int o = c.o0() + 32 * q + lane;
-            const int a = acc & 1;  // accumulator and scale buffer of this tile
-            {
-                tc2::Cursor nx = c;
-                const bool nv = nx.advance();
-                prefetch(nx, nv, a ^ 1);
-            }
-            if (!tc2::wait(&acc_full[a], (pfa >> a) & 1u, &s_abort, 0x47480005u)) break;
+            const int out = G.out, m = c.t * tc2::kTok + r, o0 = c.o0();
+            const bool mrow = m < G.M;
+            const float sc = mrow ? G.xs[m] : 0.0f;
+            const bool vec = ((out & 3) == 0) && ((reinterpret_cast<uintptr_t>(G.Y) & 15) == 0);
+            const int a = acc & 1;
+            if (!tc2::wait(&acc_full[a], (pfa >> a) & 1u, &s_abort, 0x47480018u)) break;
             pfa ^= 1u << a;
             fence_after();
-            tc2::cp_async_wait1();  // this tile's scales (the next tile's may be in flight)
-            __syncwarp();
-            const bool ocol = o < out;
+            const uint32_t ty = smem_u32(sY) + (warp - 6) * tc3::kStageY;  // this warp's 32 x 128-byte block
+            const int grp = lane >> 3, p = lane & 7;        // store phase: row group, 16-byte unit
 #pragma unroll 1
-            for (int ch = 0; ch < tc2::kTok / 32; ++ch) {
+            for (int ch = 0; ch < kTileRows / 32; ++ch) {
                 uint32_t v[32];
-                tmem_ld32(tmem + tc2::kAcc + a * tc2::kTok + 32 * ch + ((uint32_t)(32 * q) << 16), v);
-                const int mbase = c.t * tc2::kTok + 32 * ch;
-                float *yb = Y + (size_t)mbase * out + o;
-                const float4 *s4 = reinterpret_cast<const float4 *>(&scl[a][32 * ch]);
-                float sc[32];
+                tmem_ld32(tmem + tc3::kAcc + a * kTileRows + 32 * ch + ((uint32_t)(32 * q) << 16), v);
+                const int o = o0 + 32 * ch;
+                if (o >= out) continue;  // uniform across the warp
+                if (vec) {
+                    // row `lane` of the block, unit u at u ^ (lane & 7)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 f = s4[i];
-                    sc[4 * i] = f.x, sc[4 * i + 1] = f.y, sc[4 * i + 2] = f.z, sc[4 * i + 3] = f.w;
-                }
-                if (mbase + 32 <= Mtok) {
-                    if (ocol) {
+                    for (int u = 0; u < 8; ++u)
+                        tc3::sts128(ty + lane * 128 + ((u ^ (lane & 7)) << 4),
+                                    make_uint4(__float_as_uint(__uint_as_float(v[4 * u]) * sc),
+                                               __float_as_uint(__uint_as_float(v[4 * u + 1]) * sc),
+                                               __float_as_uint(__uint_as_float(v[4 * u + 2]) * sc),
+                                               __float_as_uint(__uint_as_float(v[4 * u + 3]) * sc)));
+                    __syncwarp();
+                    // store k: lanes 8 grp .. 8 grp + 7 write row 8 grp + k, floats 4p .. 4p + 3
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            yb[(size_t)i * out] = __uint_as_float(v[i]) * __fmul_rn(sc[i], kInvSqrt128);
+                    for (int k = 0; k < 8; ++k) {
+                        const int rr = 8 * grp + k;
+                        const int mm = c.t * tc2::kTok + 32 * q + rr;
+                        const uint4 f = tc3::lds128(ty + rr * 128 + ((p ^ (rr & 7)) << 4));
+                        // streaming (evict-first): Y is written once and would otherwise push
+                        // the activations that other row tiles still read out of L2
+                        if (mm < G.M && o + 4 * p < out)
+                            __stcs(reinterpret_cast<int4 *>(G.Y + (size_t)mm * out + o + 4 * p),
+                                   make_int4((int)f.x, (int)f.y, (int)f.z, (int)f.w));
                     }
-                } else {
+                    __syncwarp();
+                } else if (mrow) {
+                    float *yr = G.Y + (size_t)m * out;
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (ocol && mbase + i < Mtok)
-                            yb[(size_t)i * out] = __uint_as_float(v[i]) * __fmul_rn(sc[i], kInvSqrt128);
+                        if (o + i < out) __stcs(yr + o + i, __uint_as_float(v[i]) * sc);
                 }
             }
             fence_before();
             __syncwarp();
             if (lane == 0) tc2::mbar_arrive(&acc_empty[a]);
         }
-        tc2::cp_async_wait0();
     } else {
         // ------------------------------------------ weight expansion --
-        const int et = 32 * (warp & 3) + lane;  // weight row of the tile = this warp's TMEM lane
-        const uint32_t lane_tmem = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + tc2::kWcol;
-        uint32_t pe = (1u << tc2::kMaxNg) - 1u;  // a_empty parity of group g in bit g
+        const int e = 32 * (warp - 10) + lane;  // weight row of the tile
+        float *lv = s_lv[warp - 10];
+        uint32_t pe = (1u << tc2::kMaxNg) - 1u;  // w_empty parity of group g in bit g
         tc2::Cursor c;
         for (bool more = c.begin(p, &s_tab); more && !s_abort; more = c.advance()) {
             if (!c.first()) continue;
             const tc2::Mat &G = tc2::warp_mat(p, c.mat, &s_mat[warp]);
-            const float *lv = p.lut[G.lut];
-            const int o = c.o0() + et;
-            uint32_t *hlv = s_hlv[warp - 6];
-            const bool ok =
-                G.w == 2   ? tc2::expand_run<2>(G, lv, o, hlv, lane_tmem, a_empty, a_full, pe, &s_abort)
-                : G.w == 3 ? tc2::expand_run<3>(G, lv, o, hlv, lane_tmem, a_empty, a_full, pe, &s_abort)
-                           : tc2::expand_run<4>(G, lv, o, hlv, lane_tmem, a_empty, a_full, pe, &s_abort);
+            const float *levels = p.lut[G.lut];
+            const int o = c.o0() + e;
+            const bool ok = G.w == 2   ? tc3::expand_row<2>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort)
+                            : G.w == 3 ? tc3::expand_row<3>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort)
+                                       : tc3::expand_row<4>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort);
             if (!ok) break;
         }
     }
@@ -973,44 +1072,40 @@ __global__ void __launch_bounds__(tc2::kThreads, 1) gemm_tc2_kernel(const __grid
     }
 }
 
-// Dynamic shared memory of the pipelined kernel: 3 x 64 KB of activation
-// stages, 1 KB of alignment slack.
-constexpr int kTc2MaxSmem = tc2::kStages * tc2::kStageBytes + 1024;
-
-// Launched as a programmatic dependent of the activation rotation, which
-// lets it start as that kernel's blocks retire: the prologue and the first
-// weight expansions overlap the rotation's tail, and only the TMA producer
-// waits (griddepcontrol.wait) for the rotated activations.
-int launch_tc2(const tc2::Params &p, int grid, size_t smem, cudaStream_t st) {
+// `pdl`: launched as a programmatic dependent of the kernel before it (one of
+// this library's that triggers early; only the TMA producer then waits for
+// it, so every other input must be complete when that kernel started).
+int launch_x8(const tc2::Params &p, int grid, bool pdl, cudaStream_t st) {
     static bool attr = false;
     if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   kTc2MaxSmem);
+        const cudaError_t e =
+            cudaFuncSetAttribute(gemm_x8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc3::kSmem);
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm smem attribute: %s", cudaGetErrorString(e));
         attr = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(tc2::kThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.blockDim = dim3(tc3::kThreads);
+    cfg.dynamicSmemBytes = tc3::kSmem;
     cfg.stream = st;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, p);
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_x8_kernel, p);
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
     return CQ_OK;
 }
 
-// 2-D tensor map over one rotated activation Z[M][in_pad] (fp16): boxes of
-// 64 inputs x 128 tokens, 128-byte swizzle, zero fill past M.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-static int make_z_map(CUtensorMap *map, const void *Z, int M, int in_pad) {
+// 2-D tensor map over int8 activations X[M][in] with rows `ld` bytes apart
+// (ld a multiple of 16, X 16-byte aligned): boxes of 128 inputs x 128
+// tokens, 128-byte swizzle; inputs past `in` and tokens past M read as zero.
+static int make_x_map(CUtensorMap *map, const void *X, int M, int in, int ld) {
     static EncodeTiledFn fn = nullptr;
     if (!fn) {
         cudaDriverEntryPointQueryResult q;
@@ -1023,17 +1118,32 @@ static int make_z_map(CUtensorMap *map, const void *Z, int M, int in_pad) {
         }
         fn = reinterpret_cast<EncodeTiledFn>(f);
     }
-    const cuuint64_t dims[2] = {(cuuint64_t)in_pad, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)in_pad * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)tc2::kTok};
+    const cuuint64_t dims[2] = {(cuuint64_t)in, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld};
+    const cuuint32_t box[2] = {(cuuint32_t)kGroup, (cuuint32_t)tc2::kTok};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(Z), dims, strides, box, estr,
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(X), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(CQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return CQ_OK;
 }
 
+// Copy of int8 activations whose rows a tensor map cannot address (row
+// length not a multiple of 16 bytes, or a base that is not 16-byte aligned)
+// into rows of `ld` bytes (ld = in rounded up to 16; the tail is zero).
+__global__ void __launch_bounds__(256) pad_rows_kernel(const int8_t *__restrict__ X, int M, int in, int ld,
+                                                       int8_t *__restrict__ Y) {
+    // the GEMM that follows may launch now; it waits for this grid before it reads Y
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    const long long total = (long long)M * ld;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long m = i / ld;
+        const int k = (int)(i - m * ld);
+        Y[i] = k < in ? X[m * in + k] : (int8_t)0;
+    }
+}
 
 }  // namespace
 
@@ -1083,12 +1193,18 @@ void *stream_workspace(void *stream, int kind, size_t bytes, int *err) {
     return w.ptr;
 }
 
-// Distinct activations of a call and where their rotations go in a
-// workspace (each rotated once: M * in_pad fp16, 256-byte aligned).
+// Distinct activations of a call and their workspace (256-byte aligned
+// pieces). An activation read by matrices with in > 512 is rotated once
+// into Z (M * in_pad fp16, at `off`); one with in <= 512 is read as int8 by
+// a tensor map, in place when its rows allow it, else from a padded copy
+// (M * ld bytes, at `off`).
 struct ActPlan {
     std::vector<const int8_t *> ptr;
     std::vector<size_t> off;
     std::vector<int> M, in;
+    std::vector<int> wide;    // 1: rotated into Z
+    std::vector<int> ld;      // narrow: row pitch of the tensor map's rows
+    std::vector<int> padded;  // narrow: 1 when the map reads the padded copy
     std::vector<int> act_of;  // per descriptor, -1 when it needs no product
     size_t total = 0;
 };
@@ -1106,11 +1222,20 @@ static void plan_activations(const cq_gemm_desc *d, int n, cudaStream_t st, ActP
             if (pl.ptr[j] == d[i].Xq && pl.in[j] == d[i].in && pl.M[j] == d[i].M) a = (int)j;
         if (a < 0) {
             a = (int)pl.ptr.size();
+            const int wide = in_padded(d[i].in) / kGroup > tc2::kMaxNg;
+            const bool direct = !wide && d[i].in % 16 == 0 && (reinterpret_cast<uintptr_t>(d[i].Xq) & 15) == 0;
+            const int ld = (d[i].in + 15) / 16 * 16;
             pl.ptr.push_back(d[i].Xq);
             pl.M.push_back(d[i].M);
             pl.in.push_back(d[i].in);
+            pl.wide.push_back(wide);
+            pl.ld.push_back(wide ? 0 : ld);
+            pl.padded.push_back(!wide && !direct);
             pl.off.push_back(pl.total);
-            pl.total += ((size_t)d[i].M * in_padded(d[i].in) * sizeof(__half) + 255) / 256 * 256;
+            size_t bytes = 0;
+            if (wide) bytes = (size_t)d[i].M * in_padded(d[i].in) * sizeof(__half);
+            else if (!direct) bytes = (size_t)d[i].M * ld;
+            pl.total += (bytes + 255) / 256 * 256;
         }
         pl.act_of[i] = a;
     }
@@ -1125,8 +1250,11 @@ int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream) {
     plan_activations(d, n, st, pl);
     if (pl.ptr.empty()) return CQ_OK;
     int err = CQ_OK;
-    uint8_t *ws = static_cast<uint8_t *>(stream_workspace(st, 0, pl.total, &err));
-    if (!ws) return err;
+    uint8_t *ws = nullptr;
+    if (pl.total) {
+        ws = static_cast<uint8_t *>(stream_workspace(st, 0, pl.total, &err));
+        if (!ws) return err;
+    }
     return run_gemm(d, n, pl, ws, st);
 }
 
@@ -1143,11 +1271,10 @@ static void level_table(const cq_gemm_desc &d, float lut[16]) {
     }
 }
 
-// The pipelined kernel over every descriptor of code width W whose input is
-// at most 512 wide; launches as often as its parameter block fills.
-// All matrices with in <= 512, whatever their code width, in one launch (more
-// only when a parameter block fills up).
-static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, cudaStream_t st) {
+// All matrices with in <= 512, whatever their code width, in one launch of
+// gemm_x8_kernel (more only when a parameter block fills up). `pdl`: the
+// first launch may overlap the kernel launched just before it.
+static int run_gemm_x8(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, bool pdl, cudaStream_t st) {
     static tc2::Params p;
     std::vector<int> map_of(pl.ptr.size(), -1);
     int nmaps = 0, nlut = 0, tiles = 0, runs = 0, ngmax = 0;
@@ -1166,9 +1293,9 @@ static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, u
                 p.tail_T0 = p.m[j].tiles_before + (r0 - p.m[j].runs_before) * p.m[j].m_tiles;
                 break;
             }
-        const size_t smem = (size_t)tc2::kStages * tc2::kStageBytes + 1024;
-        const int rc = launch_tc2(p, grid, smem, st);
+        const int rc = launch_x8(p, grid, pdl, st);
         if (rc) return rc;
+        pdl = false;
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
         p.n = 0;
@@ -1197,7 +1324,8 @@ static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, u
             li = -1;
         }
         if (map_of[a] < 0) {
-            const int e = make_z_map(&p.tmap[nmaps], ws + pl.off[a], pl.M[a], ip);
+            const void *X = pl.padded[a] ? static_cast<const void *>(ws + pl.off[a]) : pl.ptr[a];
+            const int e = make_x_map(&p.tmap[nmaps], X, pl.M[a], pl.in[a], pl.ld[a]);
             if (e) return e;
             map_of[a] = nmaps++;
         }
@@ -1229,12 +1357,16 @@ static int run_gemm_pipelined(const cq_gemm_desc *d, int n, const ActPlan &pl, u
 }
 
 static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, cudaStream_t st) {
-    // every distinct activation rotated in one launch
-    {
+    bool any_wide = false, any_narrow = false;
+    for (size_t j = 0; j < pl.ptr.size(); ++j) (pl.wide[j] ? any_wide : any_narrow) = true;
+    bool pdl = false;  // the kernel launched last triggers its dependents early
+    // every distinct activation of the wide matrices rotated in one launch
+    if (any_wide) {
         static RotTable rt;
         rt.n = 0;
         rt.task_before[0] = 0;
         for (size_t j = 0; j < pl.ptr.size(); ++j) {
+            if (!pl.wide[j]) continue;
             const int k = rt.n++;
             rt.x[k] = pl.ptr[j];
             rt.z[k] = reinterpret_cast<__half *>(ws + pl.off[j]);
@@ -1246,14 +1378,27 @@ static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws
         const long long tasks = rt.task_before[rt.n];
         const int grid = (int)std::min<long long>((tasks + 15) / 16, (long long)sm_count() * 4);
         act_rotate_many_kernel<<<grid, 256, 0, st>>>(rt);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "act_rotate launch: %s", cudaGetErrorString(e));
+        pdl = true;
     }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "act_rotate launch: %s", cudaGetErrorString(e));
-
-    {
-        const int e2 = run_gemm_pipelined(d, n, pl, ws, st);
+    // narrow activations whose rows a tensor map cannot address: padded copies
+    for (size_t j = 0; j < pl.ptr.size(); ++j) {
+        if (pl.wide[j] || !pl.padded[j]) continue;
+        const long long bytes = (long long)pl.M[j] * pl.ld[j];
+        const int grid = (int)std::min<long long>((bytes + 255) / 256, (long long)sm_count() * 8);
+        pad_rows_kernel<<<grid, 256, 0, st>>>(pl.ptr[j], pl.M[j], pl.in[j], pl.ld[j],
+                                              reinterpret_cast<int8_t *>(ws + pl.off[j]));
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "pad launch: %s", cudaGetErrorString(e));
+        pdl = true;
+    }
+    if (any_narrow) {
+        const int e2 = run_gemm_x8(d, n, pl, ws, pdl, st);
         if (e2) return e2;
     }
+    if (!any_wide) return CQ_OK;
+    cudaError_t e;
     for (int W = 2; W <= 4; ++W) {
         static GemmParams p;
         p.n = 0;
@@ -1316,9 +1461,10 @@ static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws
 // engine that reserves all device memory up front and hands the library only
 // its inputs and outputs, or a host thread that must not touch the CUDA
 // allocator (cudaMalloc synchronises the device and can fail under memory
-// pressure). cq_gemm_noalloc serves them: the rotated activations that
-// cq_gemm keeps in its grown-on-demand workspace live instead in the fixed
-// array below, which every GPU that loads this library holds until the
+// pressure). cq_gemm_noalloc serves them: the scratch that cq_gemm keeps in
+// its grown-on-demand workspace (rotated activations of inputs wider than
+// 512, padded copies of activations a tensor map cannot address) lives
+// instead in the fixed array below, which every GPU that loads this library holds until the
 // process exits.
 static __device__ __align__(256) __half g_noalloc_scratch[CQ_GEMM_NOALLOC_MAX_ELEMS];
 

@@ -172,14 +172,21 @@ int cq_gemv_grouped(const cq_gemv_desc *descs, int n, void *stream);
 
 /* Prefill product over one CQ blob with int8 per-token activations:
  *   Y[m][o] = s[m] * sum_k W_hat[o][k] Xq[m][k]
- * computed as a dense contraction on the tensor cores: the activations are
- * rotated exactly in integers per group (H0 Xq, |v| <= 16384) and stored in
- * fp16; code tiles are expanded to fp16 W'[o][k] = c[q] n[o][g] in shared
- * memory only, and tcgen05 accumulates in fp32 in tensor memory.
+ * computed as a dense contraction on the tensor cores, the codes expanded
+ * only tile by tile on chip, tcgen05 accumulating in fp32 in tensor memory.
+ * The rotation of the rotated-domain identity is applied on whichever side
+ * is cheaper ("Reconstructing one group": n <c[q], H x> = <n H c[q], x>):
+ *  - in <= 512: per run of token tiles, the 128 weight rows of a tile are
+ *    expanded and rotated back once, W''[o][k] = fp16(n[o][g] (H c[q])[k]),
+ *    and meet the int8 activations directly (exact in fp16);
+ *  - in > 512: the activations are rotated exactly in integers per group
+ *    (H0 Xq, |v| <= 16384), stored in fp16, and meet W'[o][k] =
+ *    fp16(c[q] n[o][g]).
  * Xq int8 [M][in], x_scale fp32 [M], Y fp32 [M][out]: device.
- * The library keeps one internal device workspace for the rotated
- * activations (M*in_pad fp16), grown on demand by the first call that
- * needs more; make one untimed call before capturing a CUDA graph.
+ * The library keeps one internal device workspace, grown on demand by the
+ * first call that needs more (rotated activations for in > 512; padded
+ * copies of activations whose rows are not a multiple of 16 bytes or not
+ * 16-byte aligned); make one untimed call before capturing a CUDA graph.
  * Errors: CQ_ERR_ARG, CQ_ERR_SHAPE, CQ_ERR_NOMEM, CQ_ERR_CUDA,
  * CQ_ERR_TIMEOUT (a pipeline wait exceeded its bound; results invalid). */
 int cq_gemm(const uint8_t *blob, int out, int in, int group, int bits,
@@ -196,8 +203,10 @@ typedef struct cq_gemm_desc {
     int out, in, group, bits, M;
 } cq_gemm_desc;
 
-/* n independent GEMMs in as few launches as possible (one rotation launch
- * per distinct activation, one persistent GEMM launch). Errors as cq_gemm. */
+/* n independent GEMMs in as few launches as possible: one persistent GEMM
+ * launch for all matrices with in <= 512 (whatever their code width), and
+ * for wider inputs one rotation launch over their distinct activations plus
+ * one GEMM launch per code width. Errors as cq_gemm. */
 int cq_gemm_grouped(const cq_gemm_desc *descs, int n, void *stream);
 
 /* Largest M * in_pad accepted by cq_gemm_noalloc (fp16 elements of its
@@ -210,9 +219,9 @@ int cq_gemm_grouped(const cq_gemm_desc *descs, int n, void *stream);
  * all device memory up front and passes the library only its inputs and
  * outputs, or a thread that must not enter the CUDA allocator (cudaMalloc
  * synchronises the device and may fail under memory pressure). cq_gemm keeps
- * the rotated activations in a workspace it grows with cudaMalloc; this
- * variant keeps them in a fixed array of CQ_GEMM_NOALLOC_MAX_ELEMS fp16
- * values compiled into the library, which every GPU that loads the library
+ * its scratch (rotated or padded activations) in a workspace it grows with
+ * cudaMalloc; this variant keeps it in a fixed array of
+ * CQ_GEMM_NOALLOC_MAX_ELEMS fp16 values compiled into the library, which every GPU that loads the library
  * holds until the process exits. Arguments, layouts and results are those of
  * cq_gemm.
  *  - Sizes: M * in_pad must not exceed CQ_GEMM_NOALLOC_MAX_ELEMS

@@ -101,3 +101,45 @@ def test_gemm_empty(C):
                   torch.zeros((3, 0), dtype=torch.int8, device="cuda"), torch.ones(3, device="cuda"))
     torch.cuda.synchronize()
     assert torch.all(Y == 0)
+
+
+def test_gemm_grouped_mixed_inputs(C):
+    """One grouped call over inputs above 512 (rotated activations), at most
+    512 and aligned (activations read in place), and rows that are not a
+    multiple of 16 bytes (padded copies), across all code widths."""
+    M = 200
+    shapes = [(300, 640, 2), (256, 512, 4), (129, 300, 3), (64, 128, 5), (200, 384, 2)]
+    items, refs = [], []
+    for i, (out, n_in, bits) in enumerate(shapes):
+        cb = O.analytic_codebook(bits)
+        blob = _rand_blob(out, n_in, bits, 700 + i)
+        q, s = _tokens(M, n_in, 800 + i)
+        items.append(dict(blob=torch.from_numpy(blob).cuda(), out=out, **{"in": n_in}, bits=bits, codebook=cb,
+                          Xq=torch.from_numpy(q).cuda(), x_scale=torch.from_numpy(s).cuda()))
+        refs.append((blob, out, n_in, bits, cb, q, s))
+    Ys = C.cq_gemm_grouped(items)
+    torch.cuda.synchronize()
+    for Y, (blob, out, n_in, bits, cb, q, s) in zip(Ys, refs):
+        xt = q.astype(np.float64) * s.astype(np.float64)[:, None]
+        What = O.dequant(blob, out, n_in, bits, cb)
+        y_ref, bound = O.matmul(What, xt)
+        check_matmul(Y.cpu().numpy(), y_ref, bound, f"mixed out={out} in={n_in} bits={bits}")
+
+
+def test_gemm_misaligned_activation_rows(C):
+    """Activations whose base address is not 16-byte aligned take the padded
+    copy; the result is the same as for an aligned copy of the same values."""
+    out, n_in, M = 256, 256, 70
+    cb = O.analytic_codebook(2)
+    blob = torch.from_numpy(_rand_blob(out, n_in, 2, 901)).cuda()
+    q, s = _tokens(M, n_in, 902)
+    buf = torch.zeros(M * n_in + 16, dtype=torch.int8, device="cuda")
+    Xmis = buf[3:3 + M * n_in].view(M, n_in)
+    Xmis.copy_(torch.from_numpy(q).cuda())
+    assert Xmis.data_ptr() % 16 != 0
+    xs = torch.from_numpy(s).cuda()
+    Y1 = C.cq_gemm(blob, out, n_in, 2, cb, Xmis, xs)
+    Y2 = C.cq_gemm(blob, out, n_in, 2, cb, torch.from_numpy(q).cuda(), xs)
+    torch.cuda.synchronize()
+    assert torch.equal(Y1, Y2)
+    _check(C, blob.cpu().numpy(), out, n_in, 2, cb, q, s, what="misaligned")
