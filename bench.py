@@ -43,12 +43,12 @@ WORKLOAD = ("Needle-shaped decode step, batch 1: 27 x {Q 512x512, K 256x512, V 2
 # longer matches and traffic reads null.
 NCU_TRAFFIC = {
     "gemv_fast": ("308a05255cfbb0fb", 10163200),
-    "gemm_tc2_cq2": ("d0277638671d2628", 530353664),
+    "gemm_x8": ("4b79b037d5f9c7e5", 528337920),
     "encode_cq2": ("1a3db57f51cc2349", 281883904),
 }
 KERNEL_SOURCES = {
     "gemv_fast": ("cq_gemv_fast.cu", "cq_internal.h"),
-    "gemm_tc2_cq2": ("cq_gemm.cu", "cq_internal.h"),
+    "gemm_x8": ("cq_gemm.cu", "cq_internal.h"),
     "encode_cq2": ("cq_encode.cu", "cq_internal.h"),
 }
 
@@ -394,10 +394,10 @@ def bench_gemm(C, S, torch, wl, device, stream, peaks, peak_kind, barrier, max_o
                           Y=torch.empty((M, m.out), dtype=torch.float32, device=device)))
     flops = 2.0 * M * sum(m.out * m.n_in for m in mats)
     with torch.cuda.stream(stream):
-        for _ in range(3):  # warm-up; also grows the rotated-activation workspace
+        for _ in range(3):  # warm-up
             C.cq_gemm_grouped(items)
     stream.synchronize()
-    # one prefill step (activation rotation + every matrix's GEMM) as a graph, so
+    # one prefill step (every matrix's GEMM: one persistent launch) as a graph, so
     # the host's tensor-map encoding stays outside the timed region
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -419,13 +419,25 @@ def bench_gemm(C, S, torch, wl, device, stream, peaks, peak_kind, barrier, max_o
     C.cq_device_status(device)
     tflops = flops / (ms * 1e-3) / 1e12
     out_bytes = 4.0 * M * sum(m.out for m in mats)
+    # algorithmic bytes: fp32 Y written once, each int8 activation and every
+    # blob (codes + norms) read once
+    act_in = {m.act: m.n_in for m in mats}
+    in_bytes = float(sum(M * n for n in act_in.values()) + sum(wl["sizes"]))
+    alg_bytes = out_bytes + in_bytes
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    # At K = 512 with fp32 outputs the step needs more time at HBM speed
+    # (alg_bytes / hbm) than at tensor speed (flops / bf16 peak): it is bound
+    # by HBM; the tensor-core view is reported beside it.
     return {"metric": "CQ GEMM TFLOP/s at M=2048 (Needle-shaped matrix set, int8 per-token activations)",
             "value": round(world * tflops, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4), "steps": Kg,
-            "warmup": 3, "M": M, "l2": "outputs larger than L2 (fp32 Y, 520 MB per step)", "flops_per_step": flops, "output_bytes_per_step": out_bytes,
-            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": round(tflops / peaks["bf16_tflops"], 4),
-                         "peak_source": peak_kind + " (bf16 dense; fp16 operands run at the same rate)",
-                         "traffic": None, "traffic_cq2_kernel": ncu_traffic("gemm_tc2_cq2")}}
+            "warmup": 3, "M": M, "l2": "outputs larger than L2 (fp32 Y, 520 MB per step)", "flops_per_step": flops,
+            "output_bytes_per_step": out_bytes, "algorithmic_bytes_per_step": alg_bytes,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": peak_kind,
+                         "traffic": ncu_traffic("gemm_x8"), "kernel": "gemm_x8_kernel (one launch per step)"},
+            "tensor_view": {"achieved": round(tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": round(tflops / peaks["bf16_tflops"], 4),
+                            "peak_source": peak_kind + " (bf16 dense; fp16 operands run at the same rate)"}}
 
 
 def bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world, count=0):
