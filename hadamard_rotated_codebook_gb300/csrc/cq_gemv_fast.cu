@@ -6,9 +6,11 @@
 // (OpenNeedle docs/reference.md; "The .cact archive and Cactus Quants",
 // "Reconstructing one group"):
 //     y[o] += n[o][g] * sum_k c[q[o,g,k]] * z[g,k],   z = H x (per group).
-// The activation is rotated once per launch ("How the kernel reads it": the
-// FWHT is shared by all rows that read it), by a small prologue kernel that
-// also lays z out as MMA operand fragments.
+// Each CTA rotates the activation of its matrix itself (a few warp-tasks:
+// one per group and batch row) and lays z out as MMA operand fragments in
+// shared memory; the FWHT is shared by all the rows of the CTA ("How the
+// kernel reads it"). A separate prologue kernel would put a launch and a
+// round trip through global memory on the critical path of a decode step.
 //
 // GB300 mapping. The weights stay packed in HBM and in shared memory; a
 // code byte is expanded to fp16 levels in registers through a 256-entry
@@ -27,11 +29,10 @@
 // Work: a CTA owns one matrix's row range (16*T rows) and its whole input.
 // At entry it issues 16-byte cp.async copies of its contiguous code rows and
 // norms into shared memory (rows padded so the operand reads are free of
-// bank conflicts; rows past the matrix are zero-filled), builds the level
-// table while they land, then waits for the prologue kernel (programmatic
-// dependent launch) and copies the activation's fragments in. Its warps
-// split the row tiles and, when a CTA has fewer tiles than warps, the groups
-// of the input (partial sums meet in shared memory).
+// bank conflicts; rows past the matrix are zero-filled), then, while they
+// land, builds the level table and rotates the activation. Its warps split
+// the row tiles and, when a CTA has fewer tiles than warps, the groups of the
+// input (partial sums meet in shared memory).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -65,34 +66,19 @@ struct FastMat {
     int kchunks;   // warps sharing one tile (split of the groups)
     int item0;     // first CTA of this matrix
     int row_stride;  // shared-memory bytes per code row (padded against bank conflicts)
-    int frag_off;  // workspace words: the activation's B fragments [ng][4][32 lanes][4]
-    int gs_off;    // workspace words: 1/sigma [B][ng]
 };
 
 static_assert(sizeof(FastMat) % 4 == 0 && sizeof(FastMat) / 4 <= 256, "descriptor copy");
 
 struct FastParams {
     int n_items;
-    // byte offsets of the shared regions: code rows, norms, B fragments,
-    // partial sums, level table
-    int smem_codes, smem_norms, smem_frag, smem_red, smem_tab;
+    // byte offsets of the shared regions: code rows, norms, B fragments
+    // [ng][4][32 lanes][4] words, partial sums, level table, rotation scratch
+    int smem_codes, smem_norms, smem_frag, smem_red, smem_tab, smem_terms;
     __half lut[kMaxLuts][16];  // levels by code (2-bit: entries 0..3)
     FastMat m[kMaxFastMats];
     int n_mats;
-    const uint32_t *ws;               // written by gemv_prep_kernel
     uint8_t item_mat[kMaxFastItems];  // CTA -> matrix
-};
-
-// One distinct activation of a launch, as the prologue kernel sees it.
-struct PrepAct {
-    const void *x;
-    int in, ng, B, xdt, frag_off, gs_off, task0;
-};
-
-struct PrepParams {
-    int n_acts, n_tasks;
-    uint32_t *ws;
-    PrepAct a[kMaxFastMats];
 };
 
 constexpr float kInvSqrt128 = 0.08838834764831845f;
@@ -111,7 +97,7 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_b
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
 }
 
-// ------------------------------------------------------------ prologue --
+// ------------------------------------------------------------ rotation --
 // Largest power of two sigma with amax * sigma <= lim (1 for amax == 0).
 __device__ __forceinline__ float pow2_scale(float amax, float lim) {
     if (!(amax > 0.0f)) return 1.0f;
@@ -124,9 +110,19 @@ __device__ __forceinline__ float pow2_scale(float amax, float lim) {
 
 // Activation values of (batch row b, group g): lane holds
 // x[b][g*128 + 4 lane + i], zero past `in`.
-__device__ __forceinline__ void load_x_bg(const PrepAct &A, int b, int g, int lane, float (&v)[4]) {
+__device__ __forceinline__ void load_x_bg(const FastMat &A, int b, int g, int lane, float (&v)[4]) {
     const int col0 = g * kGroup + 4 * lane;
-    if (A.xdt == CQ_X_I8) {
+    if (A.xdt == CQ_X_I8 && (A.in & 3) == 0 && (reinterpret_cast<uintptr_t>(A.x) & 3) == 0) {
+        // one 4-byte load, kept in program order (issued before the copies
+        // and the table that follow it)
+        uint32_t w = 0;
+        if (col0 < A.in)
+            asm volatile("ld.global.b32 %0, [%1];\n"
+                         : "=r"(w)
+                         : "l"(static_cast<const int8_t *>(A.x) + (size_t)b * A.in + col0));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = (float)(int8_t)(w >> (8 * i));
+    } else if (A.xdt == CQ_X_I8) {
         const int8_t *xq = static_cast<const int8_t *>(A.x) + (size_t)b * A.in;
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[i] = col0 + i < A.in ? (float)xq[col0 + i] : 0.0f;
@@ -137,13 +133,11 @@ __device__ __forceinline__ void load_x_bg(const PrepAct &A, int b, int g, int la
     }
 }
 
-// Rotation of (b, g) by one warp: z = H0 x_{b,g} (without the 1/sqrt(128);
-// exact integers for int8 x). Position k is written to terms[k] as fp16
+// Rotation of (b, g) by one warp, from the values load_x_bg gave this lane:
+// z = H0 x_{b,g} (without the 1/sqrt(128); exact integers for int8 x). Position k is written to terms[k] as fp16
 // hi | lo of sigma * z[k], sigma a power of two per (b, g) (|sigma z| <=
 // 2^14, so hi + lo carries z to ~2^-22 relative); returns 1/sigma.
-__device__ float rotate_bg(const PrepAct &A, int b, int g, int lane, uint32_t *terms) {
-    float v[4];
-    load_x_bg(A, b, g, lane, v);
+__device__ float rotate_bg(float (&v)[4], int lane, uint32_t *terms) {
     float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
     v[0] = a0 + a2;
     v[1] = a1 + a3;
@@ -176,7 +170,7 @@ __device__ float rotate_bg(const PrepAct &A, int b, int g, int lane, uint32_t *t
 // (fp16 hi / lo). dst receives the group's words as [f/4][lane][f%4], so
 // that a warp's 16-byte load of words 4i..4i+3 is contiguous across lanes
 // (free of bank conflicts).
-__device__ void frag_words(const PrepAct &A, const uint32_t (*terms)[kGroup], int lane, uint32_t *dst) {
+__device__ void frag_words(const FastMat &A, const uint32_t (*terms)[kGroup], int lane, uint32_t *dst) {
     const int gq = lane >> 2, t = lane & 3;
     const int b = gq >> 1, tau = gq & 1;
     uint32_t w[kFragWords];
@@ -193,34 +187,6 @@ __device__ void frag_words(const PrepAct &A, const uint32_t (*terms)[kGroup], in
     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
     for (int i = 0; i < 4; ++i) d4[i * 32 + lane] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-}
-
-// Activation prologue of a launch: one warp per (activation, group) rotates
-// every batch row of the group once and writes the B fragments and 1/sigma
-// per (b, g) to the workspace. The GEMV kernel that follows is launched as
-// its programmatic dependent: it starts (and streams its code rows) while
-// this kernel runs, and waits for it only before reading these.
-constexpr int kPrepWarps = 8;
-__global__ void __launch_bounds__(kPrepWarps * 32) gemv_prep_kernel(const __grid_constant__ PrepParams p) {
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-    __shared__ __align__(16) uint32_t s_terms[kPrepWarps][kMaxFastB][kGroup];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int task = blockIdx.x * kPrepWarps + warp;
-    if (task >= p.n_tasks) return;
-    int lo = 0, hi = p.n_acts - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) / 2;
-        if (p.a[mid].task0 <= task) lo = mid;
-        else hi = mid - 1;
-    }
-    const PrepAct A = p.a[lo];
-    const int g = task - A.task0;
-    for (int b = 0; b < A.B; ++b) {
-        const float inv = rotate_bg(A, b, g, lane, s_terms[warp][b]);
-        if (lane == 0) reinterpret_cast<float *>(p.ws + A.gs_off)[b * A.ng + g] = inv;
-    }
-    __syncwarp();
-    frag_words(A, s_terms[warp], lane, p.ws + A.frag_off + (size_t)g * 32 * kFragWords);
 }
 
 // -------------------------------------------------------------- products --
@@ -283,6 +249,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     const int rowBytes = ng * (kind == 0 ? 32 : 64);
     const int rs = M.row_stride;  // padded shared-memory row stride (bytes)
 
+    // ---- 0. the activation values of this warp's first group (every batch
+    // row), requested first: their latency overlaps the copies and the table ----
+    float xv[kMaxFastB][4];
+    if (warp < ng)
+#pragma unroll
+        for (int b = 0; b < kMaxFastB; ++b)
+            if (b < B) load_x_bg(M, b, warp, lane, xv[b]);
+
     uint8_t *sc = smem + p.smem_codes;                             // [nrows][rs]
     __half *sn = reinterpret_cast<__half *>(smem + p.smem_norms);  // [nrows][ng]
     uint32_t *frag = reinterpret_cast<uint32_t *>(smem + p.smem_frag);
@@ -344,16 +318,22 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
         }
     }
 
-    // ---- 3. the activation's B fragments and 1/sigma, written by the
-    // prologue kernel this launch depends on ----
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // ---- 3. the activation: warp w rotates groups w, w+8, ... of every
+    // batch row into B fragments and 1/sigma ----
     {
-        const int fwords = ng * 32 * kFragWords;
-        const uint32_t *fsrc = p.ws + M.frag_off;
-        for (int c = threadIdx.x; 4 * c < fwords; c += kThreads) cp_async16(frag + 4 * c, fsrc + 4 * c, 16);
-        asm volatile("cp.async.commit_group;\n" ::);
-        const float *gsrc = reinterpret_cast<const float *>(p.ws + M.gs_off);
-        for (int c = threadIdx.x; c < B * ng; c += kThreads) ginv[c] = gsrc[c];
+        uint32_t(*terms)[kGroup] = reinterpret_cast<uint32_t(*)[kGroup]>(smem + p.smem_terms) + warp * kMaxFastB;
+        for (int g = warp; g < ng; g += kWarps) {
+#pragma unroll
+            for (int b = 0; b < kMaxFastB; ++b) {
+                if (b >= B) break;
+                if (g != warp) load_x_bg(M, b, g, lane, xv[b]);
+                const float inv = rotate_bg(xv[b], lane, terms[b]);
+                if (lane == 0) ginv[b * ng + g] = inv;
+            }
+            __syncwarp();
+            frag_words(M, terms, lane, frag + (size_t)g * 32 * kFragWords);
+            __syncwarp();
+        }
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
     __syncthreads();
@@ -457,9 +437,8 @@ struct Need {
     size_t codes = 0, norms = 0, frag = 0, red = 0;
 };
 
-// Launches the activation prologue and then the GEMV over the CTAs gathered
-// in p (its programmatic dependent); resets p and pp.
-static int flush(FastParams &p, PrepParams &pp, size_t ws_words, int &nm, int &nlut, Need &need, cudaStream_t st) {
+// Launches the GEMV over the CTAs gathered in p; resets p.
+static int flush(FastParams &p, int &nm, int &nlut, Need &need, cudaStream_t st) {
     if (!p.n_items) return CQ_OK;
     size_t off = 0;
     auto place = [&](int &field, size_t bytes) {
@@ -471,6 +450,7 @@ static int flush(FastParams &p, PrepParams &pp, size_t ws_words, int &nm, int &n
     place(p.smem_frag, need.frag);
     place(p.smem_red, need.red);
     place(p.smem_tab, 256 * 32 * sizeof(uint32_t));  // either table: 32 KB
+    place(p.smem_terms, (size_t)kWarps * kMaxFastB * kGroup * sizeof(uint32_t));  // rotation scratch: 16 KB
     const size_t smem = off;
     p.n_mats = nm;
     static bool attr = false;
@@ -479,48 +459,23 @@ static int flush(FastParams &p, PrepParams &pp, size_t ws_words, int &nm, int &n
         attr = true;
     }
     if (smem > 200 * 1024) return set_error(CQ_ERR_SHAPE, "fast GEMV needs %zu bytes of shared memory", smem);
-    int err = CQ_OK;
-    uint32_t *ws = static_cast<uint32_t *>(stream_workspace(st, 1, ws_words * 4, &err));
-    if (!ws) return err;
-    pp.ws = ws;
-    p.ws = ws;
-    gemv_prep_kernel<<<(pp.n_tasks + kPrepWarps - 1) / kPrepWarps, kPrepWarps * 32, 0, st>>>(pp);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemv prologue launch: %s", cudaGetErrorString(e));
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_items);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute la[1];
-    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    la[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = la;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemv_fast_kernel, p);
+    gemv_fast_kernel<<<p.n_items, kThreads, smem, st>>>(p);
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "fast gemv launch: %s", cudaGetErrorString(e));
     p.n_items = 0;
     nm = 0;
     nlut = 0;
     need = Need();
-    pp.n_acts = pp.n_tasks = 0;
     return CQ_OK;
 }
 
 int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream) {
     static FastParams p;
-    static PrepParams pp;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     p.n_items = 0;
-    pp.n_acts = pp.n_tasks = 0;
-    size_t ws_words = 0;  // workspace words used by this flush's activations
     int nlut = 0, nm = 0;
     Need need;
-    auto do_flush = [&]() -> int {
-        const int e = flush(p, pp, ws_words, nm, nlut, need, st);
-        ws_words = 0;
-        return e;
-    };
+    auto do_flush = [&]() -> int { return flush(p, nm, nlut, need, st); };
     for (int ii = 0; ii < n; ++ii) {
         const cq_gemv_desc &D = d[idx[ii]];
         const int ip = in_padded(D.in), W = width_of(D.bits), ng = ip / kGroup;
@@ -577,30 +532,6 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
         M.B = D.B;
         M.kind = kind;
         M.lut = li;
-        // the activation's slot in the prologue's output (shared by the
-        // matrices that read the same activation)
-        int ai = -1;
-        for (int j = 0; j < pp.n_acts; ++j) {
-            const PrepAct &A = pp.a[j];
-            if (A.x == D.x && A.in == D.in && A.B == D.B && A.xdt == D.x_dtype) ai = j;
-        }
-        if (ai < 0) {
-            PrepAct &A = pp.a[pp.n_acts];
-            A.x = D.x;
-            A.in = D.in;
-            A.ng = ng;
-            A.B = D.B;
-            A.xdt = D.x_dtype;
-            A.frag_off = (int)ws_words;
-            ws_words += (size_t)ng * 32 * kFragWords;
-            A.gs_off = (int)ws_words;
-            ws_words += ((size_t)D.B * ng + 3) / 4 * 4;  // keep the next block 16-byte aligned
-            A.task0 = pp.n_tasks;
-            pp.n_tasks += ng;
-            ai = pp.n_acts++;
-        }
-        M.frag_off = pp.a[ai].frag_off;
-        M.gs_off = pp.a[ai].gs_off;
         M.tiles = tp;
         M.kchunks = tp >= kWarps ? 1 : std::min(kWarps / tp, M.ng);
         // row stride in shared memory: the 2-bit path reads 8 bytes per lane

@@ -64,8 +64,8 @@ int check_gemm_args(const cq_gemm_desc &d);
 int sm_count();
 
 // Device scratch of at least `bytes` for work queued on `stream`; `kind`
-// selects an independent buffer (0: GEMM rotated activations, 1: GEMV
-// operand fragments). Grow-only; null with *err set if allocation fails.
+// selects an independent buffer (0: GEMM rotated or padded activations).
+// Grow-only; null with *err set if allocation fails.
 void *stream_workspace(void *stream, int kind, size_t bytes, int *err);
 
 // Device status word shared by kernels with bounded waits (defined in

@@ -164,9 +164,10 @@ typedef struct cq_gemv_desc {
 
 /* Runs n (1..CQ_MAX_GROUPED) independent GEMVs in one kernel launch: the
  * decode step of a Needle-shaped model, where many small matrices would
- * otherwise each pay a launch. Descriptors that share the same x pointer
- * share one activation rotation ([ON]: Q/K/V/gate reuse one rotated input).
- * Results are identical to n separate cq_gemv calls up to fp32 summation
+ * otherwise each pay a launch. On the tensor-core path each thread block
+ * rotates the activation of its slice of output rows itself (a few FWHTs
+ * per block; [ON]: Q/K/V/gate reuse one rotated input, here within a
+ * block), so the launch has no prologue and no scratch memory. Results are identical to n separate cq_gemv calls up to fp32 summation
  * order. Output buffers must not overlap. Errors as cq_gemv. */
 int cq_gemv_grouped(const cq_gemv_desc *descs, int n, void *stream);
 
