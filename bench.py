@@ -243,12 +243,14 @@ def run_cq(args):
     peaks, peak_kind = measured_peaks()
     barrier, max_over_ranks = rank_ops(world, device)
 
-    if args.only in ("gemm", "encode"):
+    if args.only in ("gemm", "encode", "gather"):
         # one part alone, for profiling: only that part's buffers are held
         stream = torch.cuda.Stream(device)
         if args.only == "gemm":
             wl = decode_workload(C, S, device, 0)
             res = bench_gemm(C, S, torch, wl, device, stream, peaks, peak_kind, barrier, max_over_ranks, world)
+        elif args.only == "gather":
+            res = bench_gather(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
         else:
             res = bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world, args.encode_count)
         if rank == 0:
@@ -372,6 +374,7 @@ def run_cq(args):
         result["gemm"] = bench_gemm(C, S, torch, wl, device, stream, peaks, peak_kind, barrier, max_over_ranks, world)
         result["encode"] = bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world,
                                         args.encode_count)
+        result["gather"] = bench_gather(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
     if rank == 0 and world == 1 and not args.skip_cpu:
         result["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     if rank == 0:
@@ -482,6 +485,52 @@ def bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, wo
                          "algorithmic_bytes_per_launch": algo // n}}
 
 
+def bench_gather(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world, n=65536):
+    """Row-gather dequantisation: n random token ids into the tied 8192 x 512
+    CQ4 embedding/logit table of the Needle-shaped set (fp32 rows out)."""
+    out, n_in = 8192, 512
+    cb = C.cq_codebook_init(4)
+    nb = C.cq_packed_bytes(out, n_in, 128, 4)
+    blob = torch.from_numpy(S.random_blob(out * n_in * 4 // 8, out * (n_in // 128), 74)).to(device)
+    assert blob.numel() == nb
+    g_ = torch.Generator(device="cpu").manual_seed(75)
+    idx = torch.randint(0, out, (n,), generator=g_, dtype=torch.int32).to(device)
+    dst = torch.empty((n, n_in), dtype=torch.float32, device=device)
+    with torch.cuda.stream(stream):
+        C.cq_gather_rows(blob, out, n_in, 4, cb, idx, dst=dst)
+    stream.synchronize()
+    C.cq_device_status(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        C.cq_gather_rows(blob, out, n_in, 4, cb, idx, dst=dst)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    stream.synchronize()
+    Kg = 20
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(Kg):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1)) / Kg
+    C.cq_device_status(device)
+    # algorithmic bytes: each indexed row's codes and norms read, its fp32 row
+    # written, the indices read
+    row_bytes = nb // out
+    algo = n * (row_bytes + 4 * n_in + 4)
+    gbs = algo / (ms * 1e-3) / 1e9
+    return {"metric": f"CQ4 row gather GB/s ({n} token ids into the 8192x512 embedding table -> fp32 rows)",
+            "value": round(world * gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4), "steps": Kg,
+            "warmup": 3, "l2": "outputs larger than L2 (128 MB per step)",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                         "algorithmic_bytes_per_launch": algo}}
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def _oracle_step_sample(budget_s: float):
@@ -553,7 +602,7 @@ def main():
     ap.add_argument("--skip-extra", action="store_true", help="decode step only")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--encode-count", type=int, default=0, help="matrices in the encode part (default 16)")
-    ap.add_argument("--only", default="all", choices=["all", "gemm", "encode"],
+    ap.add_argument("--only", default="all", choices=["all", "gemm", "encode", "gather"],
                     help="time one secondary part alone and print its JSON object (profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()

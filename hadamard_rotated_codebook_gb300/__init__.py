@@ -263,6 +263,25 @@ def cq_gemm_grouped(items: Sequence[dict]) -> list:
     return Ys
 
 
+def cq_gather_rows(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook, idx: torch.Tensor,
+                   dst: Optional[torch.Tensor] = None, group: int = GROUP) -> torch.Tensor:
+    """dst[i] = W_hat[idx[i]] (fp32 [n, in]): only the indexed rows of the CQ
+    table are decoded. An index outside [0, out) gives a zero row, reported by
+    a later cq_device_status as CQError(CQ_ERR_INDEX)."""
+    if idx.dim() != 1:
+        raise ValueError("idx must be one-dimensional")
+    n = idx.shape[0]
+    if dst is None:
+        dst = torch.empty((n, n_in), dtype=torch.float32, device=idx.device)
+    if dst.shape != (n, n_in):
+        raise ValueError("dst must be [n, in]")
+    cb, cbp = _codebook_arg(codebook, bits)
+    check(_lib().cq_gather_rows(_dev_ptr(blob, torch.uint8, "blob"), out, n_in, group, bits, cbp,
+                                _dev_ptr(idx, torch.int32, "idx"), n, _dev_ptr(dst, torch.float32, "dst"),
+                                _stream(idx.device)))
+    return dst
+
+
 def cq_device_status(device: Optional[torch.device] = None) -> int:
     """Reads and clears the device status word of bounded waits (raises
     CQError(CQ_ERR_TIMEOUT) if one gave up)."""

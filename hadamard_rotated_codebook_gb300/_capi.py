@@ -18,7 +18,7 @@ P = ctypes.POINTER
 
 CQ_OK = 0
 CQ_ERR_ARG, CQ_ERR_SHAPE, CQ_ERR_FORMAT, CQ_ERR_IO = -1, -2, -3, -4
-CQ_ERR_CUDA, CQ_ERR_TIMEOUT, CQ_ERR_NOMEM = -5, -6, -7
+CQ_ERR_CUDA, CQ_ERR_TIMEOUT, CQ_ERR_NOMEM, CQ_ERR_INDEX = -5, -6, -7, -8
 CQ_X_F32, CQ_X_I8 = 0, 1
 CQ_GEMV_MAX_BATCH = 16
 CQ_MAX_GROUPED = 256
@@ -28,7 +28,7 @@ CQ_DTYPE_FP16, CQ_DTYPE_FP32, CQ_DTYPE_CQ, CQ_DTYPE_RAW = 1, 2, 3, 4
 ERROR_NAMES = {
     CQ_ERR_ARG: "CQ_ERR_ARG", CQ_ERR_SHAPE: "CQ_ERR_SHAPE", CQ_ERR_FORMAT: "CQ_ERR_FORMAT",
     CQ_ERR_IO: "CQ_ERR_IO", CQ_ERR_CUDA: "CQ_ERR_CUDA", CQ_ERR_TIMEOUT: "CQ_ERR_TIMEOUT",
-    CQ_ERR_NOMEM: "CQ_ERR_NOMEM",
+    CQ_ERR_NOMEM: "CQ_ERR_NOMEM", CQ_ERR_INDEX: "CQ_ERR_INDEX",
 }
 
 
@@ -74,6 +74,8 @@ SIGNATURES = {
     "cq_gemm_grouped": (c_int, [P(GemmDesc), c_int, c_void_p]),
     "cq_gemm_noalloc": (c_int, [c_void_p, c_int, c_int, c_int, c_int, P(c_float), c_void_p, c_void_p,
                                 c_int, c_void_p, c_void_p]),
+    "cq_gather_rows": (c_int, [c_void_p, c_int, c_int, c_int, c_int, P(c_float), c_void_p, c_int,
+                               c_void_p, c_void_p]),
     "cq_device_status": (c_int, [c_void_p]),
     "cq_selftest_wait_timeout": (c_int, [c_void_p]),
     "cq_cact_write": (c_int, [c_char_p, P(TensorDesc), c_int, P(c_float), c_uint32]),

@@ -30,6 +30,24 @@ namespace cq {
 // cq_device_status).
 static __device__ unsigned int g_cq_device_status = 0;
 
+unsigned int *device_status_ptr() {
+    static unsigned int *ptr[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (!ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_cq_device_status) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    return ptr[dev];
+}
+
 int read_and_clear_device_status(void *stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     unsigned int v = 0;
@@ -40,7 +58,8 @@ int read_and_clear_device_status(void *stream) {
     const unsigned int zero = 0;
     e = cudaMemcpyToSymbol(g_cq_device_status, &zero, sizeof(zero));
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
-    if (v) return set_error(CQ_ERR_TIMEOUT, "a bounded device wait gave up (code 0x%08x)", v);
+    if (v & ~kStatusIndex) return set_error(CQ_ERR_TIMEOUT, "a bounded device wait gave up (code 0x%08x)", v);
+    if (v) return set_error(CQ_ERR_INDEX, "a gathered row index was out of range");
     return CQ_OK;
 }
 

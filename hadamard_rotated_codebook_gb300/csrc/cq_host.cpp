@@ -201,6 +201,30 @@ int cq_gemv_grouped(const cq_gemv_desc *descs, int n, void *stream) {
     return launch_gemv_grouped(descs, n, stream);
 }
 
+int cq_gather_rows(const uint8_t *blob, int out, int in, int group, int bits, const float *codebook,
+                   const int32_t *idx, int n, float *dst, void *stream) {
+    clear_error();
+    int st = check_matrix(out, in, group, bits);
+    if (st) return st;
+    if ((st = check_codebook(codebook, bits))) return st;
+    if (n < 0) return set_error(CQ_ERR_SHAPE, "negative row count %d", n);
+    if (n == 0 || in == 0) return CQ_OK;
+    if (!idx || !dst) return set_error(CQ_ERR_ARG, "null idx or dst");
+    if (out > 0 && !blob) return set_error(CQ_ERR_ARG, "null blob");
+    if (reinterpret_cast<uintptr_t>(blob) & 15) return set_error(CQ_ERR_ARG, "blob must be 16-byte aligned");
+    // level table by code; ternary crumbs sign-extend (10 -> -2c)
+    float lv[16] = {0};
+    if (bits == 5) {
+        const float c = codebook[2];
+        lv[1] = c;
+        lv[2] = -2.0f * c;
+        lv[3] = -c;
+    } else {
+        for (int j = 0; j < levels_of(bits); ++j) lv[j] = codebook[j];
+    }
+    return launch_gather_rows(blob, out, in, bits, lv, idx, n, dst, stream);
+}
+
 static int check_gemm_desc(const cq_gemm_desc &d, int i) {
     int st = check_matrix(d.out, d.in, d.group, d.bits);
     if (st) return prefix_error(st, i);

@@ -71,5 +71,15 @@ void *stream_workspace(void *stream, int kind, size_t bytes, int *err);
 // Device status word shared by kernels with bounded waits (defined in
 // cq_gemm.cu; kernels OR a nonzero code into it when a wait gives up).
 int read_and_clear_device_status(void *stream);
+// Device address of that word on the current device (null if unavailable),
+// for kernels of other translation units. Bit 31 marks an index out of
+// range; the other bits are the codes of waits that gave up.
+unsigned int *device_status_ptr();
+constexpr unsigned int kStatusIndex = 0x80000000u;
+
+// ------------------------------------------------------------- gather --
+// `levels`: the 16-entry level table by code (ternary crumbs sign-extend).
+int launch_gather_rows(const uint8_t *blob, int out, int in, int bits, const float *levels,
+                       const int32_t *idx, int n, float *dst, void *stream);
 
 }  // namespace cq

@@ -58,6 +58,7 @@ extern "C" {
 #define CQ_ERR_CUDA (-5)    /* CUDA runtime or launch failure */
 #define CQ_ERR_TIMEOUT (-6) /* a bounded device wait gave up (see cq_device_status) */
 #define CQ_ERR_NOMEM (-7)   /* host or device allocation failed */
+#define CQ_ERR_INDEX (-8)   /* a device-side index was out of range (see cq_device_status) */
 
 /* Activation element types for cq_gemv. */
 #define CQ_X_F32 0 /* fp32 activations x[B][in] */
@@ -242,8 +243,26 @@ int cq_gemm_noalloc(const uint8_t *blob, int out, int in, int group, int bits,
                     const float *codebook, const int8_t *Xq,
                     const float *x_scale, int M, float *Y, void *stream);
 
-/* Reads and clears the device-side status word that bounded waits set when
- * they give up (synchronises `stream`). CQ_OK or CQ_ERR_TIMEOUT. */
+/* Row-gather dequantisation of a CQ table: an embedding or engram table
+ * stored as one blob, of which a step needs a few rows.
+ *   dst[i][k] = W_hat[idx[i]][k],  k < in
+ * Each group of an indexed row is rebuilt as n * H c[q] ("The .cact archive
+ * and Cactus Quants", "Reconstructing one group"; [ON] "rotated-domain
+ * identity"), in fp32 (levels, transform and norm scaling; the fp16 norm is
+ * exact in fp32). Only the indexed rows are read.
+ * blob: device, 16-byte aligned; idx: int32 [n], device; dst: fp32 [n][in],
+ * device, fully overwritten. n may be 0.
+ * An index outside [0, out) yields a row of zeros and marks the device
+ * status word, which a following cq_device_status reports as CQ_ERR_INDEX.
+ * Errors: CQ_ERR_ARG, CQ_ERR_SHAPE (group != 128), CQ_ERR_CUDA. */
+int cq_gather_rows(const uint8_t *blob, int out, int in, int group, int bits,
+                   const float *codebook, const int32_t *idx, int n,
+                   float *dst, void *stream);
+
+/* Reads and clears the device-side status word (synchronises `stream`).
+ * CQ_OK; CQ_ERR_TIMEOUT if a bounded wait gave up (results of that call are
+ * invalid); CQ_ERR_INDEX if a gather met an index out of range (and no wait
+ * gave up). */
 int cq_device_status(void *stream);
 
 /* Diagnostic without a counterpart on the pages: exercises the give-up path

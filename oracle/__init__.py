@@ -184,6 +184,16 @@ def dequant(blob: np.ndarray, out: int, n_in: int, bits: int, codebook,
     return What
 
 
+def gather_rows(blob: np.ndarray, out: int, n_in: int, bits: int, codebook, idx,
+                group: int = 128) -> np.ndarray:
+    """Rows ``idx`` of the dequantised table, by definition: every row
+    rebuilt group by group as n * H c[q] ("The .cact archive and Cactus
+    Quants", "Reconstructing one group"), then the indexed rows selected.
+    Indices must lie in [0, out)."""
+    What = dequant(blob, out, n_in, bits, codebook, group)
+    return What[np.asarray(idx, dtype=np.int64)]
+
+
 def matmul(What: np.ndarray, X: np.ndarray):
     """Returns (Y[B, out], Bound[B, out]) in float64."""
     What = np.ascontiguousarray(What, dtype=np.float64)

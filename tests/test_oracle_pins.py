@@ -428,3 +428,21 @@ def test_act_quant_error_bound():
     assert np.all(np.abs(Q).max(axis=1) == 127)
     err = np.abs(Q * S[:, None].astype(np.float64) - X)
     assert np.all(err <= 0.5 * S[:, None] * (1 + 1e-6))
+
+
+def test_gather_rows_selects_in_order_with_repeats():
+    """Row gather ("Reconstructing one group" applied to indexed rows only):
+    row r of a 3-row table has every code equal to r and norm 2^r, so its
+    dequantised group is 2^r * c_r * sqrt(128) * e_0; gathering [2, 0, 2, 1]
+    must return those rows in that order."""
+    cb = _cq2()
+    out = 3
+    blob = np.zeros(O.packed_bytes(out, 128, 128, 2), dtype=np.uint8)
+    for r, byte in enumerate((0b00000000, 0b01010101, 0b10101010)):
+        blob[32 * r: 32 * (r + 1)] = byte
+    norms = np.array([0x3C00, 0x4000, 0x4400], dtype="<u2")  # 1, 2, 4
+    blob[96:102] = norms.view(np.uint8)
+    got = O.gather_rows(blob, out, 128, 2, cb, [2, 0, 2, 1])
+    for i, r in enumerate([2, 0, 2, 1]):
+        assert abs(got[i, 0] - (2.0 ** r) * float(cb[r]) * math.sqrt(128)) < 1e-12
+        assert np.allclose(got[i, 1:], 0.0, atol=1e-14)
