@@ -46,6 +46,7 @@ struct EncodeParams {
     const float *W;
     uint8_t *codes;
     __half *norms;
+    unsigned int *status;  // device status word (bounded waits)
     long long n_groups;  // out * ng
     int in, ng;
     float cb[kMaxLevels];
@@ -98,9 +99,14 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
     extern __shared__ float4 smem4[];
     float *tile = reinterpret_cast<float *>(smem4);
     __shared__ float s_thr[16];
+    __shared__ __align__(8) uint64_t s_bar;  // aligned rows: the tile's bulk copy
 
     const int tid = threadIdx.x;
     if (tid < L - 1) s_thr[tid] = decision_threshold(p.cb[tid], p.cb[tid + 1]);
+    if (ALIGNED && tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"((uint32_t)__cvta_generic_to_shared(&s_bar)));
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
     __syncthreads();
     float T[16];
 #pragma unroll
@@ -109,31 +115,43 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
     const int pair = tid >> 1, h = tid & 1, f = pair & 3;
     const long long n_tiles = (p.n_groups + kEncGroupsPerTile - 1) / kEncGroupsPerTile;
 
-    // Aligned rows: the tile is staged with 16-byte cp.async (every copy of a
-    // tile in flight at once, no registers held), and the next tile's copies
-    // are issued as soon as the current tile has moved to registers, so
-    // they stream while it is encoded.
+    // Aligned rows: the tile's groups are one contiguous block of W, staged by
+    // one bulk copy (TMA engine) that completes on s_bar; the next tile's
+    // copy is issued as soon as every thread has moved the current tile to
+    // registers, so it streams while that tile is encoded. Groups past the
+    // end of the matrix are not copied (their codes are never stored).
     auto stage = [&](long long tt) {
         const long long gs = tt * kEncGroupsPerTile;
-        const float4 *src = reinterpret_cast<const float4 *>(p.W) + gs * (kGroup / 4);
-        const long long avail4 = (p.n_groups - gs) * (kGroup / 4);
-        const uint32_t dst0 = (uint32_t)__cvta_generic_to_shared(smem4);
-#pragma unroll
-        for (int i = tid; i < kEncTileFloats / 4; i += kEncThreads) {
-            const bool ok = i < avail4;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst0 + 16u * i),
-                         "l"(ok ? src + i : src), "r"(ok ? 16 : 0)
-                         : "memory");
-        }
-        asm volatile("cp.async.commit_group;\n" ::: "memory");
+        const long long ngrp = p.n_groups - gs < kEncGroupsPerTile ? p.n_groups - gs : kEncGroupsPerTile;
+        const uint32_t bytes = (uint32_t)ngrp * kGroup * 4;
+        const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_bar);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(smem4)),
+                     "l"(p.W + gs * kGroup), "r"(bytes), "r"(bar)
+                     : "memory");
     };
-    if (ALIGNED && blockIdx.x < n_tiles) stage(blockIdx.x);
+    if (ALIGNED && tid == 0 && blockIdx.x < n_tiles) stage(blockIdx.x);
+    uint32_t phase = 0;  // parity of the bulk copy being waited for
 
     for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x) {
         const long long g0 = t * kEncGroupsPerTile;
         // ---- stage 128 groups into shared memory (coalesced) ----
         if (ALIGNED) {
-            asm volatile("cp.async.wait_all;\n" ::: "memory");
+            // bounded wait for the tile's bulk copy (on expiry the status word records it)
+            const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_bar);
+            bool done = false;
+            for (unsigned i = 0; i < (1u << 24) && !done; ++i) {
+                uint32_t ok;
+                asm volatile(
+                    "{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n selp.u32 %0, 1, 0, q;\n}\n"
+                    : "=r"(ok)
+                    : "r"(bar), "r"(phase)
+                    : "memory");
+                done = ok != 0;
+            }
+            if (!done && tid == 0 && p.status) atomicOr(p.status, 0x45430001u);
+            phase ^= 1u;
         } else {
             for (int i = tid; i < kEncTileFloats; i += kEncThreads) {
                 const long long G = g0 + i / kGroup;
@@ -145,8 +163,8 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
                 }
                 tile[i] = v;
             }
+            __syncthreads();
         }
-        __syncthreads();
 
         const long long G = g0 + pair;
         // ---- load my 64 values: register 4j+e = coordinate 8(j^f)+4h+e ----
@@ -161,7 +179,7 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
             x[4 * j + 3] = v.w;
         }
         __syncthreads();  // the tile may be overwritten from here on
-        if (ALIGNED && t + gridDim.x < n_tiles) stage(t + gridDim.x);
+        if (ALIGNED && tid == 0 && t + gridDim.x < n_tiles) stage(t + gridDim.x);
 
         // ---- sum of squares, pairwise in fp32 ----
         float sq[32];
@@ -359,6 +377,7 @@ int launch_encode(const float *W, int out, int in, int bits, const float *cb, ui
     if ((reinterpret_cast<uintptr_t>(blob) & 15) || (reinterpret_cast<uintptr_t>(nb) & 1))
         return set_error(CQ_ERR_ARG, "blob must be 16-byte aligned");
     p.norms = reinterpret_cast<__half *>(nb);
+    p.status = device_status_ptr();
     const int L = levels_of(bits);
     for (int j = 0; j < kMaxLevels; ++j) p.cb[j] = j < L ? cb[j] : 0.0f;
     const bool aligned = (in % kGroup == 0) && !(reinterpret_cast<uintptr_t>(W) & 15);
