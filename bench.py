@@ -42,14 +42,16 @@ WORKLOAD = ("Needle-shaped decode step, batch 1: 27 x {Q 512x512, K 256x512, V 2
 # hash of the sources it was built from: once a source changes the entry no
 # longer matches and traffic reads null.
 NCU_TRAFFIC = {
-    "gemv_fast": ("308a05255cfbb0fb", 10163200),
-    "gemm_x8": ("4b79b037d5f9c7e5", 528337920),
-    "encode_cq2": ("1a3db57f51cc2349", 281883904),
+    "gemv_fast": ("8e0c6f21b5462ac7", 9773824),
+    "gemm_x8": ("5723b56b3496d55d", 528133632),
+    "encode_cq2": ("862e5561fa0f8f3d", 282203392),
+    "gather_cq4": ("b90eb30ececdaf8e", 75766528),
 }
 KERNEL_SOURCES = {
     "gemv_fast": ("cq_gemv_fast.cu", "cq_internal.h"),
     "gemm_x8": ("cq_gemm.cu", "cq_internal.h"),
     "encode_cq2": ("cq_encode.cu", "cq_internal.h"),
+    "gather_cq4": ("cq_gather.cu", "cq_internal.h"),
 }
 
 
@@ -527,7 +529,7 @@ def bench_gather(C, S, torch, device, stream, peaks, barrier, max_over_ranks, wo
             "value": round(world * gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4), "steps": Kg,
             "warmup": 3, "l2": "outputs larger than L2 (128 MB per step)",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": ncu_traffic("gather_cq4"),
                          "algorithmic_bytes_per_launch": algo}}
 
 
