@@ -28,8 +28,8 @@ GROUP = 128
 
 __all__ = [
     "cq_levels", "cq_code_width", "cq_codebook_init", "cq_packed_bytes", "cq_encode",
-    "cq_act_quant_int8", "cq_gemv", "cq_gemv_grouped", "cq_gemm", "cq_gemm_grouped", "cq_gemm_noalloc",
-    "cq_device_status", "cq_cact_write", "cq_cact_open", "cq_cact_open_memory", "CactReader",
+    "cq_act_quant_int8", "cq_gemv", "cq_gemv_grouped", "cq_gemv_shared", "cq_gemm", "cq_gemm_grouped", "cq_gemm_noalloc",
+    "cq_gather_rows", "cq_device_status", "cq_cact_write", "cq_cact_open", "cq_cact_open_memory", "CactReader",
     "CQError", "library_path", "GROUP",
 ]
 
@@ -185,6 +185,26 @@ def cq_gemv_grouped(items: Sequence[dict]) -> list:
         ys.append(y)
     arr = (GemvDesc * len(ds))(*ds)
     check(_lib().cq_gemv_grouped(arr, len(ds), _stream(items[0]["blob"].device)))
+    return ys
+
+
+def cq_gemv_shared(blobs: Sequence[torch.Tensor], outs: Sequence[int], n_in: int, bits: int, codebook,
+                   x: torch.Tensor, x_scale: Optional[torch.Tensor] = None, group: int = GROUP) -> list:
+    """y_j = W_j x for matrices that share the activation x (Q/K/V/gate of a
+    layer), in one launch. Returns the list of y_j [B, outs[j]]."""
+    if len(blobs) != len(outs) or not blobs:
+        raise ValueError("blobs and outs must be non-empty and of equal length")
+    B = x.shape[0] if x.dim() == 2 else 1
+    ys = [torch.empty((B, o), dtype=torch.float32, device=blobs[0].device) for o in outs]
+    keep = []
+    d, _ = _gemv_desc(blobs[0], outs[0], n_in, bits, codebook, x, x_scale, ys[0], group, keep)
+    n = len(blobs)
+    bp = (ctypes.c_void_p * n)(*[_dev_ptr(b, torch.uint8, "blob") for b in blobs])
+    op = (ctypes.c_int * n)(*outs)
+    yp = (ctypes.c_void_p * n)(*[y.data_ptr() for y in ys])
+    cb, cbp = _codebook_arg(codebook, bits)
+    check(_lib().cq_gemv_shared(bp, op, n, n_in, group, bits, cbp, d.x, d.x_dtype, d.x_scale, d.B, yp,
+                                _stream(blobs[0].device)))
     return ys
 
 

@@ -69,6 +69,8 @@ SIGNATURES = {
     "cq_gemv": (c_int, [c_void_p, c_int, c_int, c_int, c_int, P(c_float), c_void_p, c_int,
                         c_void_p, c_int, c_void_p, c_void_p]),
     "cq_gemv_grouped": (c_int, [P(GemvDesc), c_int, c_void_p]),
+    "cq_gemv_shared": (c_int, [P(c_void_p), P(c_int), c_int, c_int, c_int, c_int, P(c_float), c_void_p, c_int,
+                               c_void_p, c_int, P(c_void_p), c_void_p]),
     "cq_gemm": (c_int, [c_void_p, c_int, c_int, c_int, c_int, P(c_float), c_void_p, c_void_p,
                         c_int, c_void_p, c_void_p]),
     "cq_gemm_grouped": (c_int, [P(GemmDesc), c_int, c_void_p]),

@@ -201,6 +201,30 @@ int cq_gemv_grouped(const cq_gemv_desc *descs, int n, void *stream) {
     return launch_gemv_grouped(descs, n, stream);
 }
 
+int cq_gemv_shared(const uint8_t *const *blobs, const int *outs, int n_mats, int in, int group, int bits,
+                   const float *codebook, const void *x, int x_dtype, const float *x_scale, int B, float *const *ys,
+                   void *stream) {
+    clear_error();
+    if (!blobs || !outs || !ys) return set_error(CQ_ERR_ARG, "null blobs, outs or ys array");
+    if (n_mats < 1 || n_mats > CQ_MAX_GROUPED)
+        return set_error(CQ_ERR_ARG, "need 1..%d matrices, got %d", CQ_MAX_GROUPED, n_mats);
+    cq_gemv_desc d[CQ_MAX_GROUPED];
+    for (int j = 0; j < n_mats; ++j) {
+        d[j].blob = blobs[j];
+        d[j].x = x;
+        d[j].x_scale = x_scale;
+        d[j].y = ys[j];
+        d[j].codebook = codebook;
+        d[j].out = outs[j];
+        d[j].in = in;
+        d[j].group = group;
+        d[j].bits = bits;
+        d[j].x_dtype = x_dtype;
+        d[j].B = B;
+    }
+    return cq_gemv_grouped(d, n_mats, stream);
+}
+
 int cq_gather_rows(const uint8_t *blob, int out, int in, int group, int bits, const float *codebook,
                    const int32_t *idx, int n, float *dst, void *stream) {
     clear_error();

@@ -168,9 +168,25 @@ typedef struct cq_gemv_desc {
  * otherwise each pay a launch. On the tensor-core path each thread block
  * rotates the activation of its slice of output rows itself (a few FWHTs
  * per block; [ON]: Q/K/V/gate reuse one rotated input, here within a
- * block), so the launch has no prologue and no scratch memory. Results are identical to n separate cq_gemv calls up to fp32 summation
- * order. Output buffers must not overlap. Errors as cq_gemv. */
+ * block), so the launch has no prologue and no scratch memory. Results
+ * are identical to n separate cq_gemv calls up to fp32 summation order.
+ * Output buffers must not overlap. Errors as cq_gemv. */
 int cq_gemv_grouped(const cq_gemv_desc *descs, int n, void *stream);
+
+/* Shared-input products: y_j = W_j x for n_mats (1..CQ_MAX_GROUPED)
+ * matrices that read the same activation, such as the Q, K, V and gate
+ * projections of a layer ([ON]: "Q/K/V/gate reuse one rotated input";
+ * out_proj reads a different one). One launch; on the tensor-core path every
+ * thread block rotates x once for all the rows it holds. blobs, outs and ys
+ * are host arrays of n_mats entries (device pointers in blobs and ys, as for
+ * cq_gemv); in, group, bits, codebook, x, x_dtype, x_scale and B are shared
+ * and mean what they mean for cq_gemv. Results are bit-identical to
+ * cq_gemv_grouped over the same matrices. Errors as cq_gemv, CQ_ERR_ARG for
+ * null arrays or n_mats out of range. */
+int cq_gemv_shared(const uint8_t *const *blobs, const int *outs, int n_mats,
+                   int in, int group, int bits, const float *codebook,
+                   const void *x, int x_dtype, const float *x_scale, int B,
+                   float *const *ys, void *stream);
 
 /* Prefill product over one CQ blob with int8 per-token activations:
  *   Y[m][o] = s[m] * sum_k W_hat[o][k] Xq[m][k]

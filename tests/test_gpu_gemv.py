@@ -163,6 +163,40 @@ def test_gemv_grouped_equals_single_calls(C):
         assert torch.allclose(y1, yg, rtol=1e-5, atol=1e-6)
 
 
+@pytest.mark.parametrize("B", [1, 4])
+def test_gemv_shared_input_qkvg(C, B):
+    """Shared-input entry point: Q, K, V and gate of one Needle layer read one
+    int8 activation; results are bit-identical to the grouped call over the
+    same matrices and match the oracle."""
+    outs, n_in, bits = [512, 256, 256, 512], 512, 2
+    cb = O.analytic_codebook(bits)
+    blobs_np = [_rand_blob(o, n_in, bits, 510 + j) for j, o in enumerate(outs)]
+    blobs = [torch.from_numpy(b).cuda() for b in blobs_np]
+    q, s = O.act_quant_int8(S.normal((B, n_in), 520 + B).numpy())
+    xq, xs = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+    ys = C.cq_gemv_shared(blobs, outs, n_in, bits, cb, xq, xs)
+    items = [dict(blob=b, out=o, **{"in": n_in}, bits=bits, codebook=cb, x=xq, x_scale=xs)
+             for b, o in zip(blobs, outs)]
+    yg = C.cq_gemv_grouped(items)
+    torch.cuda.synchronize()
+    xt = q.astype(np.float64) * s.astype(np.float64)[:, None]
+    for j in range(len(outs)):
+        assert ys[j].shape == (B, outs[j])
+        assert torch.equal(ys[j], yg[j])
+        y_ref, bound = _oracle_y(blobs_np[j], outs[j], n_in, bits, cb, xt)
+        check_matmul(ys[j].cpu().numpy(), y_ref, bound, f"shared mat {j}")
+
+
+def test_gemv_shared_rejects_bad_counts(C):
+    cb = O.analytic_codebook(2)
+    x = torch.zeros((1, 128), device="cuda")
+    with pytest.raises(ValueError):
+        C.cq_gemv_shared([], [], 128, 2, cb, x)
+    blobs = [torch.zeros(O.packed_bytes(8, 128, 128, 2), dtype=torch.uint8, device="cuda")] * 300
+    with pytest.raises(C.CQError):
+        C.cq_gemv_shared(blobs, [8] * 300, 128, 2, cb, x)
+
+
 @pytest.mark.parametrize("shape", S.SWEEP_SHAPES)
 @pytest.mark.parametrize("bits", [2, 3, 4, 5])
 @pytest.mark.parametrize("B", [1, 16])

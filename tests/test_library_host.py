@@ -106,6 +106,12 @@ def test_device_entry_points_reject_bad_arguments_before_launch(C):
                        bits=2, M=8)
     assert lib.cq_gemm_grouped(ctypes.byref(g), 1, None) == _capi.CQ_ERR_ARG
     assert lib.cq_act_quant_int8(None, 2, 8, None, None, None) == _capi.CQ_ERR_ARG
+    bl = (ctypes.c_void_p * 2)(1, 1)
+    outs = (ctypes.c_int * 2)(4, 4)
+    ys = (ctypes.c_void_p * 2)(1, 1)
+    assert lib.cq_gemv_shared(bl, outs, 0, 128, 128, 2, cb, 1, _capi.CQ_X_F32, None, 1, ys, None) == _capi.CQ_ERR_ARG
+    assert lib.cq_gemv_shared(None, outs, 2, 128, 128, 2, cb, 1, _capi.CQ_X_F32, None, 1, ys, None) == _capi.CQ_ERR_ARG
+    assert lib.cq_gemv_shared(bl, outs, 2, 128, 128, 2, cb, 1, _capi.CQ_X_F32, None, 17, ys, None) == _capi.CQ_ERR_SHAPE
 
 
 def test_binding_requires_the_library(tmp_path, monkeypatch):
