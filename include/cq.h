@@ -275,6 +275,74 @@ int cq_gather_rows(const uint8_t *blob, int out, int in, int group, int bits,
                    const float *codebook, const int32_t *idx, int n,
                    float *dst, void *stream);
 
+/* ------------------------------------------------------ CQ KV cache -- */
+/*
+ * A key or a value cache quantised with CQ: the header's kv_bits (2, 3 or 4;
+ * 8 means int8 and is not this path) names the code width, and "the same
+ * path" as the weights serves it ([CF] "Five regions": kv_bits field; "How
+ * the kernel reads it"; [ON]: below 8 bits the KV cache goes through the CQ
+ * quantiser). One cache holds `cap` token rows; row t is the concatenation
+ * of the n_kv_heads head vectors of token t (width in = n_kv_heads *
+ * head_dim), encoded exactly like a weight matrix with out = cap (groups of
+ * 128 along the row, zero-padded tail): codes [cap][in_pad*width/8], then
+ * fp16 norms [cap][in_pad/128], cq_packed_bytes(cap, in, 128, bits) bytes.
+ * A cache of one head per row (n_kv_heads = 1) is the per-head layout.
+ */
+
+/* Encodes rows[n][in] (fp32, device) into cache rows t0 .. t0+n-1 of a cache
+ * of `cap` rows (device, 16-byte aligned, cq_packed_bytes(cap, in, 128, bits)
+ * bytes), as cq_encode would encode those rows; other rows are untouched.
+ * 0 <= t0, t0 + n <= cap; n = 0 does nothing. A ring buffer over a sliding
+ * window wraps by calling twice. Errors: CQ_ERR_ARG, CQ_ERR_SHAPE,
+ * CQ_ERR_CUDA. */
+int cq_kv_write(uint8_t *cache, int cap, int in, int bits,
+                const float *codebook, const float *rows, int t0, int n,
+                void *stream);
+
+/* Geometry shared by the sequences of one cq_kv_attend call (one layer). */
+typedef struct cq_kv_geom {
+    int n_q_heads;        /* 1..16, a multiple of n_kv_heads */
+    int n_kv_heads;       /* >= 1 */
+    int head_dim_k;       /* query/key head width; n_kv_heads*head_dim_k <= 512 */
+    int head_dim_v;       /* value head width;     n_kv_heads*head_dim_v <= 512 */
+    int k_bits, v_bits;   /* 2, 3, 4 or 5 (ternary) */
+    const float *k_codebook, *v_codebook; /* host, cq_levels(bits) floats */
+    float scale;          /* logit scale, typically 1/sqrt(head_dim_k) */
+} cq_kv_geom;
+
+/* One sequence: its two caches (cq_kv_write layout, `cap` rows each; the key
+ * cache of width n_kv_heads*head_dim_k, the value cache of width
+ * n_kv_heads*head_dim_v), the query q[n_q_heads][head_dim_k] and the output
+ * o[n_q_heads][head_dim_v] (fp32). All device pointers. */
+typedef struct cq_kv_seq {
+    const uint8_t *k_cache;
+    const uint8_t *v_cache;
+    const float *q;
+    float *o;
+    int cap;
+    int n_tokens;         /* rows 0 .. n_tokens-1 are attended; 0..cap */
+} cq_kv_seq;
+
+/* Decode-step attention over CQ caches for n_seqs (>= 1) sequences:
+ *   o[b] = sum_t p[b][t] v_hat[t][h], p[b] = softmax_t(scale * <q[b], k_hat[t][h]>)
+ * with h = b / (n_q_heads / n_kv_heads) (consecutive query heads share a
+ * key/value head) and k_hat, v_hat the head slices of the dequantised cache
+ * rows. Neither cache is expanded: the logits use the rotated identity
+ * n <c[q], H x> with x the query placed at its head's columns of the row
+ * ([ON] rotated-domain identity), and the value sum is accumulated in the
+ * rotated domain, sum_t p n_t c[q_t], and rotated back once per group at the
+ * end (H is its own inverse). Rows outside 0 .. n_tokens-1 are never read
+ * (they may hold anything); a sequence with n_tokens = 0 gets o = 0.
+ * Arithmetic: levels and the rotated query (as fp16 hi + lo terms) meet on
+ * the tensor cores with fp32 accumulation; softmax in fp32; the value
+ * weights p*n enter the tensor cores in fp16.
+ * The library keeps an internal device workspace for the partial results of
+ * long sequences (grown on demand; make one untimed call before capturing a
+ * CUDA graph). The o buffers must not overlap.
+ * Errors: CQ_ERR_ARG, CQ_ERR_SHAPE, CQ_ERR_NOMEM, CQ_ERR_CUDA. */
+int cq_kv_attend(const cq_kv_geom *geom, const cq_kv_seq *seqs, int n_seqs,
+                 void *stream);
+
 /* Reads and clears the device-side status word (synchronises `stream`).
  * CQ_OK; CQ_ERR_TIMEOUT if a bounded wait gave up (results of that call are
  * invalid); CQ_ERR_INDEX if a gather met an index out of range (and no wait

@@ -227,3 +227,86 @@ def act_quant_int8(X: np.ndarray):
     lib().cqo_act_quant_int8(_ptr(X, ctypes.c_float), B, n_in,
                              _ptr(Q, ctypes.c_int8), _ptr(S, ctypes.c_float))
     return Q, S
+
+
+# ------------------------------------------------------------ KV cache --
+# A CQ key or value cache is a CQ matrix whose rows are tokens: row t holds
+# the n_kv_heads head vectors of token t side by side, encoded like weights
+# ("The .cact format", "Five regions": the kv_bits field, and "How the
+# kernel reads it": the same path serves the KV cache; OpenNeedle
+# docs/reference.md: below 8 bits the KV cache goes through the CQ
+# quantiser).
+
+def _cache_geometry(n_in: int, bits: int, group: int = 128):
+    ip = in_padded(n_in, group)
+    return ip * width(bits) // 8, ip // group  # code bytes per row, groups per row
+
+
+def kv_write(cache: np.ndarray, cap: int, n_in: int, bits: int, codebook, rows,
+             t0: int, group: int = 128):
+    """Encodes ``rows`` [n, n_in] as a CQ matrix and stores its code rows and
+    norms at rows t0 .. t0+n-1 of ``cache`` (uint8, packed_bytes(cap, ...)
+    bytes; modified in place). Returns (flags, n_flagged) of the encode."""
+    rows = np.ascontiguousarray(np.atleast_2d(rows), dtype=np.float32)
+    n = rows.shape[0]
+    if t0 < 0 or t0 + n > cap:
+        raise ValueError("rows outside the cache")
+    if n == 0:
+        return np.zeros((0, in_padded(n_in, group)), dtype=np.uint8), 0
+    rb, ng = _cache_geometry(n_in, bits, group)
+    blob, flags, nflag = encode(rows, bits, codebook, group)
+    cache[t0 * rb:(t0 + n) * rb] = blob[:n * rb]
+    nb = cap * rb + 2 * ng * t0
+    cache[nb:nb + 2 * ng * n] = blob[n * rb:]
+    return flags, nflag
+
+
+def kv_rows_blob(cache: np.ndarray, cap: int, n_in: int, bits: int, n: int,
+                 group: int = 128) -> np.ndarray:
+    """The CQ blob of the first n rows of a cache of cap rows."""
+    rb, ng = _cache_geometry(n_in, bits, group)
+    return np.concatenate([cache[:n * rb], cache[cap * rb:cap * rb + 2 * ng * n]])
+
+
+def attend(K: np.ndarray, V: np.ndarray, q: np.ndarray, n_kv_heads: int, scale: float):
+    """Decode-step attention by its definition, in float64:
+    o[b] = sum_t p[b, t] V[t, head h], p[b] = softmax_t(scale * <q[b], K[t, head h]>),
+    h = b // (n_q_heads / n_kv_heads): consecutive query heads share one
+    key/value head (grouped-query attention; OpenNeedle docs/reference.md:
+    two query heads per KV head). K [T, n_kv_heads*dk], V [T, n_kv_heads*dv],
+    q [n_q_heads, dk]. Returns (o [n_q_heads, dv], p [n_q_heads, T]); with
+    T = 0 both are empty sums (o = 0)."""
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    q = np.atleast_2d(np.asarray(q, dtype=np.float64))
+    Hq, dk = q.shape
+    T = K.shape[0]
+    dv = V.shape[1] // n_kv_heads
+    per = Hq // n_kv_heads
+    o = np.zeros((Hq, dv))
+    P = np.zeros((Hq, T))
+    for b in range(Hq):
+        h = b // per
+        if T == 0:
+            continue
+        s = scale * (K[:, h * dk:(h + 1) * dk] @ q[b])
+        e = np.exp(s - s.max())
+        p = e / e.sum()
+        o[b] = p @ V[:, h * dv:(h + 1) * dv]
+        P[b] = p
+    return o, P
+
+
+def kv_attend(k_cache, v_cache, cap: int, n_tokens: int, q, n_kv_heads: int,
+              head_dim_k: int, head_dim_v: int, k_bits: int, v_bits: int,
+              k_codebook, v_codebook, scale: float):
+    """Attention over the first n_tokens rows of two CQ caches: the rows are
+    dequantised (n * H c[q] per group) and ``attend`` applies. Returns
+    (o, p, K_hat, V_hat)."""
+    in_k, in_v = n_kv_heads * head_dim_k, n_kv_heads * head_dim_v
+    Kh = dequant(kv_rows_blob(k_cache, cap, in_k, k_bits, n_tokens), n_tokens, in_k,
+                 k_bits, k_codebook) if n_tokens else np.zeros((0, in_k))
+    Vh = dequant(kv_rows_blob(v_cache, cap, in_v, v_bits, n_tokens), n_tokens, in_v,
+                 v_bits, v_codebook) if n_tokens else np.zeros((0, in_v))
+    o, P = attend(Kh, Vh, q, n_kv_heads, scale)
+    return o, P, Kh, Vh

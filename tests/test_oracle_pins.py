@@ -446,3 +446,122 @@ def test_gather_rows_selects_in_order_with_repeats():
     for i, r in enumerate([2, 0, 2, 1]):
         assert abs(got[i, 0] - (2.0 ** r) * float(cb[r]) * math.sqrt(128)) < 1e-12
         assert np.allclose(got[i, 1:], 0.0, atol=1e-14)
+
+
+# ------------------------------------------------------------ KV cache --
+# Attention pins: closed forms of the softmax-weighted sum that a dropped
+# scale, a wrong head mapping, a transposed operand or an unstable softmax
+# would break.
+
+def test_attend_single_token_returns_its_value_slice():
+    """One token: the softmax weight is 1 whatever the logit, so each head
+    returns its key/value head's slice of the value row."""
+    rng = np.random.RandomState(1)
+    K, V, q = rng.randn(1, 2 * 3), rng.randn(1, 2 * 5), rng.randn(4, 3)
+    o, P = O.attend(K, V, q, 2, 0.7)
+    assert np.array_equal(P, np.ones((4, 1)))
+    for b in range(4):
+        h = b // 2
+        assert np.array_equal(o[b], V[0, 5 * h:5 * h + 5])
+
+
+def test_attend_zero_query_averages_values():
+    """q = 0 (or scale 0): every logit is 0, the weights are uniform and the
+    output is the mean of the value rows."""
+    rng = np.random.RandomState(2)
+    K, V = rng.randn(7, 8), rng.randn(7, 8)
+    o, P = O.attend(K, V, np.zeros((2, 8)), 1, 0.35)
+    assert np.allclose(P, 1.0 / 7.0, rtol=0, atol=1e-15)
+    assert np.allclose(o, np.tile(V.mean(axis=0), (2, 1)), rtol=0, atol=1e-14)
+    o2, _ = O.attend(K, V, rng.randn(2, 8), 1, 0.0)
+    assert np.allclose(o2, o, rtol=0, atol=1e-14)
+
+
+def test_attend_two_tokens_logistic_closed_form():
+    """Two tokens with logits a and b: the weight of the second is the
+    logistic function of scale * (b - a)."""
+    K = np.array([[1.0, 0.0], [0.0, 1.0]])
+    V = np.array([[2.0, -1.0], [5.0, 3.0]])
+    q = np.array([[0.25, 1.75]])
+    scale = 0.8
+    w1 = 1.0 / (1.0 + math.exp(-scale * (1.75 - 0.25)))
+    o, P = O.attend(K, V, q, 1, scale)
+    assert abs(P[0, 1] - w1) < 1e-15 and abs(P[0, 0] - (1 - w1)) < 1e-15
+    assert np.allclose(o[0], (1 - w1) * V[0] + w1 * V[1], rtol=0, atol=1e-14)
+
+
+def test_attend_grouped_query_heads_use_their_kv_head():
+    """Four query heads over two key/value heads: heads 0, 1 read key head 0
+    (columns 0..1) and heads 2, 3 read key head 1 (columns 2..3). Token 0's
+    key points along q in head 0 only, token 1's in head 1 only, so each
+    query head picks one token's value slice of its own head."""
+    K = np.array([[40.0, 0.0, 0.0, 0.0],
+                  [0.0, 0.0, 40.0, 0.0]])
+    V = np.array([[1.0, 2.0, 3.0, 4.0],
+                  [5.0, 6.0, 7.0, 8.0]])
+    q = np.tile(np.array([[1.0, 0.0]]), (4, 1))
+    o, _ = O.attend(K, V, q, 2, 1.0)
+    e = math.exp(-40.0)
+    for b in (0, 1):  # token 0 dominates, value head 0 = columns 0..1
+        assert np.allclose(o[b], ([1.0, 2.0] + e * np.array([5.0, 6.0])) / (1 + e), rtol=0, atol=1e-15)
+    for b in (2, 3):  # token 1 dominates, value head 1 = columns 2..3
+        assert np.allclose(o[b], ([7.0, 8.0] + e * np.array([3.0, 4.0])) / (1 + e), rtol=0, atol=1e-15)
+
+
+def test_attend_large_logits_do_not_overflow():
+    """Logits of order 1e4 would overflow exp without the max shift; the
+    result is the value row of the largest logit."""
+    K = np.array([[1.0], [2.0], [1.5]]) * 1e4
+    V = np.array([[1.0, 0.0], [0.0, 1.0], [9.0, 9.0]])
+    o, P = O.attend(K, V, np.array([[1.0]]), 1, 1.0)
+    assert np.all(np.isfinite(o)) and np.array_equal(o[0], [0.0, 1.0])
+
+
+def test_attend_no_tokens_gives_zero():
+    o, P = O.attend(np.zeros((0, 4)), np.zeros((0, 6)), np.ones((2, 4)), 1, 1.0)
+    assert o.shape == (2, 6) and not o.any() and P.shape == (2, 0)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 5])
+def test_kv_write_in_pieces_equals_one_encode(bits):
+    """Writing the rows of a cache in three pieces, out of order, gives the
+    blob that encoding the whole matrix at once gives ([CF] "How the kernel
+    reads it": the KV cache uses the weight path); rows never written stay
+    as they were."""
+    rng = np.random.RandomState(3 + bits)
+    n_in, T = 96, 11
+    rows = (rng.randn(T, n_in) * 0.5).astype(np.float32)
+    cb = O.analytic_codebook(bits)
+    whole, _, _ = O.encode(rows, bits, cb)
+    cache = np.zeros(O.packed_bytes(T, n_in, 128, bits), dtype=np.uint8)
+    for a, b in ((4, 9), (0, 4), (9, 11)):
+        O.kv_write(cache, T, n_in, bits, cb, rows[a:b], a)
+    assert np.array_equal(cache, whole)
+    big = np.full(O.packed_bytes(T + 5, n_in, 128, bits), 0xA5, dtype=np.uint8)
+    O.kv_write(big, T + 5, n_in, bits, cb, rows, 0)
+    assert np.array_equal(O.kv_rows_blob(big, T + 5, n_in, bits, T), whole)
+    rb = O.in_padded(n_in) * O.width(bits) // 8
+    assert np.all(big[T * rb:(T + 5) * rb] == 0xA5)  # rows past T untouched
+
+
+def test_kv_attend_ignores_rows_past_n_tokens_and_single_row_is_exact():
+    """Rows past n_tokens may hold anything (0xFF: NaN norms); with one row
+    the output is that row's dequantised value slice, n * H c[q] per group
+    ([NJ] "Reconstructing one group")."""
+    rng = np.random.RandomState(4)
+    Hkv, dk, dv, cap = 2, 48, 64, 9
+    cb = O.analytic_codebook(2)
+    kc = np.full(O.packed_bytes(cap, Hkv * dk, 128, 2), 0xFF, dtype=np.uint8)
+    vc = np.full(O.packed_bytes(cap, Hkv * dv, 128, 2), 0xFF, dtype=np.uint8)
+    O.kv_write(kc, cap, Hkv * dk, 2, cb, rng.randn(5, Hkv * dk), 0)
+    O.kv_write(vc, cap, Hkv * dv, 2, cb, rng.randn(5, Hkv * dv), 0)
+    q = rng.randn(4, dk)
+    o, P, Kh, Vh = O.kv_attend(kc, vc, cap, 5, q, Hkv, dk, dv, 2, 2, cb, cb, 0.2)
+    assert np.all(np.isfinite(o)) and Kh.shape == (5, Hkv * dk)
+    o1, _, _, Vh1 = O.kv_attend(kc, vc, cap, 1, q, Hkv, dk, dv, 2, 2, cb, cb, 0.2)
+    codes, norms = O.unpack(O.kv_rows_blob(vc, cap, Hkv * dv, 2, 1), 1, Hkv * dv, 2)
+    n = O.f16_bits_to_f32(norms)[0]
+    row = n * O.hadamard(128) @ cb[codes[0]].astype(np.float64)  # normalised H
+    for b in range(4):
+        h = b // 2
+        assert np.allclose(o1[b], row[h * dv:(h + 1) * dv], rtol=0, atol=1e-12)
