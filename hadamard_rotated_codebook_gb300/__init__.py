@@ -22,14 +22,14 @@ import torch
 
 from . import _capi
 from ._capi import (CQ_DTYPE_CQ, CQ_DTYPE_FP16, CQ_DTYPE_FP32, CQ_DTYPE_RAW, CQ_X_F32,
-                    CQ_X_I8, CQError, GemmDesc, GemvDesc, TensorDesc, check)
+                    CQ_X_I8, CQError, GemmDesc, GemvDesc, KvGeom, KvSeq, TensorDesc, check)
 
 GROUP = 128
 
 __all__ = [
     "cq_levels", "cq_code_width", "cq_codebook_init", "cq_packed_bytes", "cq_encode",
     "cq_act_quant_int8", "cq_gemv", "cq_gemv_grouped", "cq_gemv_shared", "cq_gemm", "cq_gemm_grouped", "cq_gemm_noalloc",
-    "cq_gather_rows", "cq_device_status", "cq_cact_write", "cq_cact_open", "cq_cact_open_memory", "CactReader",
+    "cq_gather_rows", "cq_kv_write", "cq_kv_attend", "cq_device_status", "cq_cact_write", "cq_cact_open", "cq_cact_open_memory", "CactReader",
     "CQError", "library_path", "GROUP",
 ]
 
@@ -300,6 +300,51 @@ def cq_gather_rows(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook,
                                 _dev_ptr(idx, torch.int32, "idx"), n, _dev_ptr(dst, torch.float32, "dst"),
                                 _stream(idx.device)))
     return dst
+
+
+def cq_kv_write(cache: torch.Tensor, cap: int, n_in: int, bits: int, codebook, rows: torch.Tensor,
+                t0: int) -> None:
+    """Encodes rows [n, n_in] (fp32, device) into rows t0 .. t0+n-1 of a CQ
+    cache of ``cap`` rows (uint8 device tensor of cq_packed_bytes(cap, n_in,
+    128, bits) bytes)."""
+    rows2 = rows if rows.dim() == 2 else rows.reshape(1, -1)
+    if rows2.shape[1] != n_in:
+        raise ValueError(f"rows have {rows2.shape[1]} columns, cache rows have {n_in}")
+    cb, cbp = _codebook_arg(codebook, bits)
+    check(_lib().cq_kv_write(_dev_ptr(cache, torch.uint8, "cache"), cap, n_in, bits, cbp,
+                             _dev_ptr(rows2, torch.float32, "rows"), t0, rows2.shape[0],
+                             _stream(cache.device)))
+
+
+def cq_kv_attend(seqs: Sequence[dict], n_q_heads: int, n_kv_heads: int, head_dim_k: int,
+                 head_dim_v: int, k_bits: int, v_bits: int, k_codebook, v_codebook,
+                 scale: float) -> list:
+    """Decode-step attention over CQ caches for several sequences (one
+    launch per 256). Each item has k_cache, v_cache (uint8 device tensors),
+    cap, n_tokens, q [n_q_heads, head_dim_k] fp32 and optionally o. Returns
+    the o tensors [n_q_heads, head_dim_v]."""
+    if not seqs:
+        return []
+    kcb, kp = _codebook_arg(k_codebook, k_bits)
+    vcb, vp = _codebook_arg(v_codebook, v_bits)
+    geom = KvGeom(n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim_k=head_dim_k,
+                  head_dim_v=head_dim_v, k_bits=k_bits, v_bits=v_bits, k_codebook=kp,
+                  v_codebook=vp, scale=scale)
+    outs, arr = [], (KvSeq * len(seqs))()
+    for i, it in enumerate(seqs):
+        q = it["q"]
+        if tuple(q.shape) != (n_q_heads, head_dim_k):
+            raise ValueError(f"q has shape {tuple(q.shape)}, expected {(n_q_heads, head_dim_k)}")
+        o = it.get("o")
+        if o is None:
+            o = torch.empty((n_q_heads, head_dim_v), dtype=torch.float32, device=q.device)
+        outs.append(o)
+        arr[i] = KvSeq(k_cache=_dev_ptr(it["k_cache"], torch.uint8, "k_cache"),
+                       v_cache=_dev_ptr(it["v_cache"], torch.uint8, "v_cache"),
+                       q=_dev_ptr(q, torch.float32, "q"), o=_dev_ptr(o, torch.float32, "o"),
+                       cap=it["cap"], n_tokens=it["n_tokens"])
+    check(_lib().cq_kv_attend(ctypes.byref(geom), arr, len(seqs), _stream(seqs[0]["q"].device)))
+    return outs
 
 
 def cq_device_status(device: Optional[torch.device] = None) -> int:

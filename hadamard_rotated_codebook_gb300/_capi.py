@@ -49,6 +49,21 @@ class GemmDesc(ctypes.Structure):
     ]
 
 
+class KvGeom(ctypes.Structure):
+    _fields_ = [
+        ("n_q_heads", c_int), ("n_kv_heads", c_int), ("head_dim_k", c_int), ("head_dim_v", c_int),
+        ("k_bits", c_int), ("v_bits", c_int), ("k_codebook", P(c_float)), ("v_codebook", P(c_float)),
+        ("scale", c_float),
+    ]
+
+
+class KvSeq(ctypes.Structure):
+    _fields_ = [
+        ("k_cache", c_void_p), ("v_cache", c_void_p), ("q", c_void_p), ("o", c_void_p),
+        ("cap", c_int), ("n_tokens", c_int),
+    ]
+
+
 class TensorDesc(ctypes.Structure):
     _fields_ = [
         ("dtype", ctypes.c_uint8), ("ndim", ctypes.c_uint8), ("shape", c_uint32 * 4),
@@ -78,6 +93,8 @@ SIGNATURES = {
                                 c_int, c_void_p, c_void_p]),
     "cq_gather_rows": (c_int, [c_void_p, c_int, c_int, c_int, c_int, P(c_float), c_void_p, c_int,
                                c_void_p, c_void_p]),
+    "cq_kv_write": (c_int, [c_void_p, c_int, c_int, c_int, P(c_float), c_void_p, c_int, c_int, c_void_p]),
+    "cq_kv_attend": (c_int, [P(KvGeom), P(KvSeq), c_int, c_void_p]),
     "cq_device_status": (c_int, [c_void_p]),
     "cq_selftest_wait_timeout": (c_int, [c_void_p]),
     "cq_cact_write": (c_int, [c_char_p, P(TensorDesc), c_int, P(c_float), c_uint32]),

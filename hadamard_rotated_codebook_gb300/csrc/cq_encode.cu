@@ -366,15 +366,19 @@ int sm_count() {
 
 int launch_encode(const float *W, int out, int in, int bits, const float *cb, uint8_t *blob,
                   void *stream) {
+    const size_t rowBytes = (size_t)in_padded(in) * width_of(bits) / 8;
+    return launch_encode_rows(W, out, in, bits, cb, blob, blob + (size_t)out * rowBytes, stream);
+}
+
+int launch_encode_rows(const float *W, int out, int in, int bits, const float *cb, uint8_t *codes,
+                       uint8_t *nb, void *stream) {
     EncodeParams p;
     p.W = W;
     p.in = in;
     p.ng = in_padded(in) / kGroup;
     p.n_groups = (long long)out * p.ng;
-    const size_t rowBytes = (size_t)in_padded(in) * width_of(bits) / 8;
-    p.codes = blob;
-    uint8_t *nb = blob + (size_t)out * rowBytes;
-    if ((reinterpret_cast<uintptr_t>(blob) & 15) || (reinterpret_cast<uintptr_t>(nb) & 1))
+    p.codes = codes;
+    if ((reinterpret_cast<uintptr_t>(codes) & 15) || (reinterpret_cast<uintptr_t>(nb) & 1))
         return set_error(CQ_ERR_ARG, "blob must be 16-byte aligned");
     p.norms = reinterpret_cast<__half *>(nb);
     p.status = device_status_ptr();

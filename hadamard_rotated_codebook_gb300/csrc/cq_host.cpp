@@ -76,6 +76,20 @@ static void lloyd_max_half(int L, double *c) {
     }
 }
 
+// Level by code (16 entries): the codebook, or for the ternary marker the
+// 2-bit crumbs read as signed (01 -> +c, 11 -> -c, 10 -> -2c, never written).
+void level_table(int bits, const float *codebook, float lv[16]) {
+    for (int j = 0; j < 16; ++j) lv[j] = 0.0f;
+    if (bits == 5) {
+        const float c = codebook[2];
+        lv[1] = c;
+        lv[2] = -2.0f * c;
+        lv[3] = -c;
+    } else {
+        for (int j = 0; j < levels_of(bits); ++j) lv[j] = codebook[j];
+    }
+}
+
 }  // namespace cq
 
 using namespace cq;
@@ -236,17 +250,58 @@ int cq_gather_rows(const uint8_t *blob, int out, int in, int group, int bits, co
     if (!idx || !dst) return set_error(CQ_ERR_ARG, "null idx or dst");
     if (out > 0 && !blob) return set_error(CQ_ERR_ARG, "null blob");
     if (reinterpret_cast<uintptr_t>(blob) & 15) return set_error(CQ_ERR_ARG, "blob must be 16-byte aligned");
-    // level table by code; ternary crumbs sign-extend (10 -> -2c)
-    float lv[16] = {0};
-    if (bits == 5) {
-        const float c = codebook[2];
-        lv[1] = c;
-        lv[2] = -2.0f * c;
-        lv[3] = -c;
-    } else {
-        for (int j = 0; j < levels_of(bits); ++j) lv[j] = codebook[j];
-    }
+    float lv[16];
+    level_table(bits, codebook, lv);
     return launch_gather_rows(blob, out, in, bits, lv, idx, n, dst, stream);
+}
+
+int cq_kv_write(uint8_t *cache, int cap, int in, int bits, const float *codebook, const float *rows, int t0, int n,
+                void *stream) {
+    clear_error();
+    int st = check_matrix(cap, in, kGroup, bits);
+    if (st) return st;
+    if ((st = check_codebook(codebook, bits))) return st;
+    if (n < 0 || t0 < 0 || (long long)t0 + n > cap)
+        return set_error(CQ_ERR_SHAPE, "rows %d..%lld outside a cache of %d rows", t0, (long long)t0 + n - 1, cap);
+    if (n == 0 || in == 0) return CQ_OK;
+    if (!cache || !rows) return set_error(CQ_ERR_ARG, "null cache or rows");
+    if (reinterpret_cast<uintptr_t>(cache) & 15) return set_error(CQ_ERR_ARG, "cache must be 16-byte aligned");
+    const size_t rb = (size_t)in_padded(in) * width_of(bits) / 8, ng = in_padded(in) / kGroup;
+    uint8_t *codes = cache + (size_t)t0 * rb;
+    uint8_t *norms = cache + (size_t)cap * rb + 2 * ng * (size_t)t0;
+    return launch_encode_rows(rows, n, in, bits, codebook, codes, norms, stream);
+}
+
+int cq_kv_attend(const cq_kv_geom *g, const cq_kv_seq *seqs, int n_seqs, void *stream) {
+    clear_error();
+    if (!g || !seqs) return set_error(CQ_ERR_ARG, "null geometry or sequence array");
+    if (n_seqs < 1) return set_error(CQ_ERR_ARG, "need at least one sequence, got %d", n_seqs);
+    if (g->n_q_heads < 1 || g->n_q_heads > 16 || g->n_kv_heads < 1 || g->n_q_heads % g->n_kv_heads)
+        return set_error(CQ_ERR_SHAPE, "need 1..16 query heads, a multiple of the %d key/value heads; got %d",
+                         g->n_kv_heads, g->n_q_heads);
+    if (g->head_dim_k < 1 || g->head_dim_v < 1 || (long long)g->n_kv_heads * g->head_dim_k > 512 ||
+        (long long)g->n_kv_heads * g->head_dim_v > 512)
+        return set_error(CQ_ERR_SHAPE, "cache rows of %d x %d (keys) and %d x %d (values) exceed 512 or are empty",
+                         g->n_kv_heads, g->head_dim_k, g->n_kv_heads, g->head_dim_v);
+    if (width_of(g->k_bits) < 0 || width_of(g->v_bits) < 0)
+        return set_error(CQ_ERR_ARG, "bits must be 2, 3, 4 or 5 (got %d, %d)", g->k_bits, g->v_bits);
+    int st = check_codebook(g->k_codebook, g->k_bits);
+    if (st) return st;
+    if ((st = check_codebook(g->v_codebook, g->v_bits))) return st;
+    if (!std::isfinite(g->scale)) return set_error(CQ_ERR_ARG, "scale must be finite");
+    for (int i = 0; i < n_seqs; ++i) {
+        const cq_kv_seq &s = seqs[i];
+        if (s.cap < 0 || s.n_tokens < 0 || s.n_tokens > s.cap)
+            return set_error(CQ_ERR_SHAPE, "sequence %d: n_tokens %d outside 0..cap (%d)", i, s.n_tokens, s.cap);
+        if (!s.o || (s.n_tokens > 0 && (!s.q || !s.k_cache || !s.v_cache)))
+            return set_error(CQ_ERR_ARG, "sequence %d: null cache, q or o", i);
+        if ((reinterpret_cast<uintptr_t>(s.k_cache) | reinterpret_cast<uintptr_t>(s.v_cache)) & 15)
+            return set_error(CQ_ERR_ARG, "sequence %d: caches must be 16-byte aligned", i);
+    }
+    float lk[16], lv[16];
+    level_table(g->k_bits, g->k_codebook, lk);
+    level_table(g->v_bits, g->v_codebook, lv);
+    return launch_kv_attend(*g, seqs, n_seqs, lk, lv, stream);
 }
 
 static int check_gemm_desc(const cq_gemm_desc &d, int i) {

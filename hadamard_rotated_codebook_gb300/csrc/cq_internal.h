@@ -44,6 +44,10 @@ int check_codebook(const float *cb, int bits);
 // ------------------------------------------------------------- encode --
 int launch_encode(const float *W, int out, int in, int bits, const float *cb,
                   uint8_t *blob, void *stream);
+// Encodes W[n][in] into explicit code and norm regions (rows of a larger
+// blob: codes at `codes`, fp16 norms at `norms`).
+int launch_encode_rows(const float *W, int n, int in, int bits, const float *cb, uint8_t *codes,
+                       uint8_t *norms, void *stream);
 int launch_act_quant(const float *X, int M, int in, int8_t *Xq, float *s,
                      void *stream);
 
@@ -81,5 +85,13 @@ constexpr unsigned int kStatusIndex = 0x80000000u;
 // `levels`: the 16-entry level table by code (ternary crumbs sign-extend).
 int launch_gather_rows(const uint8_t *blob, int out, int in, int bits, const float *levels,
                        const int32_t *idx, int n, float *dst, void *stream);
+
+// Level by code, 16 entries (ternary crumbs read as signed 2-bit values).
+void level_table(int bits, const float *codebook, float lv[16]);
+
+// ---------------------------------------------------------- KV cache --
+// lk, lv: level tables of the key and value codes (level_table).
+int launch_kv_attend(const cq_kv_geom &g, const cq_kv_seq *seqs, int n, const float *lk, const float *lv,
+                     void *stream);
 
 }  // namespace cq

@@ -1,0 +1,615 @@
+// cq_kv.cu -- decode-step attention over CQ key/value caches.
+//
+// A cache row is one token's head vectors side by side, stored as a CQ
+// matrix row ("The .cact format", "How the kernel reads it": the weight path
+// serves the KV cache at the header's kv_bits). For query head b, reading
+// key/value head h, and group g of a row:
+//   logit[b][t] = scale * sum_g n_k[t][g] * < c[q_k[t,g,:]], H x_{b,g} >
+// where x_b is q_b placed at head h's columns of the row (zero elsewhere) --
+// the rotated-domain identity of the weight GEMV (OpenNeedle
+// docs/reference.md). The value sum stays in the rotated domain,
+//   R[b][g] = sum_t p[b][t] n_v[t][g] c[q_v[t,g,:]],   o_b = slice_h(H R[b]) / l_b,
+// so neither cache is ever expanded and H (its own inverse) is applied once
+// per group and head at the end.
+//
+// GB300 mapping. A thread block owns a chunk of one sequence's tokens and
+// walks it in sub-tiles of 128 tokens with an online softmax:
+//  - key side: warp w takes tokens 16w..16w+15 of the sub-tile; their code
+//    bits come straight from global memory into registers, a pair table in
+//    shared memory (two codes -> two fp16 levels, one replica per bank)
+//    turns them into A fragments of mma.sync m16n8k16, and the rotated
+//    queries (fp16 hi + lo terms, two B columns per head) are the B operand;
+//  - softmax statistics per head in fp32 (running max, sum, rescale factor);
+//  - value side: the MMA contracts over tokens. Rows of A are value
+//    coordinates (two neighbours per code pair), columns of A are tokens
+//    (code pairs of two tokens interleaved with a byte permute), B holds the
+//    weights p * n_v in fp16; each warp owns a few 16-coordinate slices and
+//    keeps their accumulators in registers across the whole chunk.
+// Sequences longer than one chunk write their partial (max, sum, R) to a
+// workspace; the last block of the sequence to finish (an atomic ticket; no
+// block waits for another) merges them and writes o.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <vector>
+
+#include "cq_internal.h"
+
+namespace cq {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTile = 128;      // tokens per sub-tile
+constexpr int kMaxHeads = 16;   // query heads per call
+constexpr int kMaxNg = 4;       // groups per cache row
+constexpr int kMaxSeqs = 256;   // sequences per launch (the host splits larger calls)
+constexpr float kInvSqrt128 = 0.08838834764831845f;
+
+struct KvSeqDev {
+    const uint8_t *kc, *vc;  // caches
+    const float *q;
+    float *o;
+    int cap, n;              // rows allocated, rows attended
+    int cta0, n_chunks;      // first block and number of blocks of this sequence
+    int chunk_tok;           // tokens per block (a multiple of kTile)
+    int slot0;               // first workspace slot (n_chunks > 1)
+};
+
+struct KvParams {
+    int Hq, per, dk, dv;     // per = query heads per key/value head
+    int in_k, in_v, ngk, ngv;
+    int ntk, ntv;            // n-tiles of 8 columns: key side (hi, lo per head), value side
+    float logit_scale;       // scale / sqrt(128) (z is rotated without normalisation)
+    int n_seqs;
+    int vrow;                // staged value-code row stride (bytes)
+    // shared-memory byte offsets
+    int sm_tabk, sm_tabv, sm_zf, sm_isig, sm_vcodes, sm_vnorm, sm_p, sm_wf, sm_terms, sm_r;
+    uint16_t lvk[16], lvv[16];  // fp16 level bits by code
+    float *part;             // [slot][Hq][ngv*128] partial rotated value sums
+    float *ml;               // [slot][Hq][2] running max and sum
+    unsigned int *ticket;    // [seq] blocks finished
+    KvSeqDev s[kMaxSeqs];
+};
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+}
+
+// Largest power of two sigma with amax * sigma <= lim (1 for amax == 0).
+__device__ __forceinline__ float pow2_scale(float amax, float lim) {
+    if (!(amax > 0.0f)) return 1.0f;
+    const float q = __fdiv_rn(lim, amax);
+    const int E = min(max((__float_as_int(q) >> 23) & 0xff, 1), 254);
+    float s = __int_as_float(E << 23);
+    if (__fmul_rn(amax, s) > lim) s *= 0.5f;
+    return s;
+}
+
+// Unnormalised 128-point transform of the values a warp holds (lane: 4*lane + i).
+__device__ __forceinline__ void fwht128(float (&v)[4], int lane) {
+    const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+    v[0] = a0 + a2;
+    v[1] = a1 + a3;
+    v[2] = a0 - a2;
+    v[3] = a1 - a3;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+            v[i] = (lane & m) ? o - v[i] : v[i] + o;
+        }
+}
+
+// 2W code bits starting at bit `off` of a little-endian word array (W <= 4,
+// so at most 8 bits, possibly straddling two words).
+template <int W>
+__device__ __forceinline__ uint32_t bits2(const uint32_t *w, int off) {
+    const int i = off >> 5, sh = off & 31;
+    if (W != 3) return (w[i] >> sh) & ((1u << (2 * W)) - 1u);
+    return __funnelshift_r(w[i], w[i + 1], sh) & 63u;
+}
+
+// Code words of one key row's group for lane quarter c: 4W bytes holding the
+// thread's 32 coordinates 32c .. 32c+31 (zero for a token past the end).
+template <int W>
+__device__ __forceinline__ void load_key_words(const uint8_t *grp, int c, bool ok, uint32_t (&w)[5]) {
+    w[0] = w[1] = w[2] = w[3] = w[4] = 0u;
+    if (!ok) return;
+    if (W == 2) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(grp) + c);
+        w[0] = v.x;
+        w[1] = v.y;
+    } else if (W == 4) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(grp) + c);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+    } else {
+        const uint32_t *p = reinterpret_cast<const uint32_t *>(grp) + 3 * c;
+        w[0] = __ldg(p);
+        w[1] = __ldg(p + 1);
+        w[2] = __ldg(p + 2);
+    }
+}
+
+// Rotated-domain value sums R[b][k] in shared memory -> o[b] = slice of
+// (H0 R[b]) / (sqrt(128) l_b) for the groups that overlap head b's columns.
+__device__ void finish_heads(const KvParams &p, const float *sr, const float *sl, float *o, int warp, int lane) {
+    const int ipv = p.ngv * kGroup;
+    for (int task = warp; task < p.Hq * p.ngv; task += kWarps) {
+        const int b = task / p.ngv, g = task % p.ngv;
+        const int h = b / p.per, c0 = h * p.dv, c1 = c0 + p.dv;
+        if (c1 <= g * kGroup || c0 >= (g + 1) * kGroup) continue;  // group outside the head
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = sr[b * ipv + g * kGroup + 4 * lane + i];
+        fwht128(v, lane);
+        const float f = kInvSqrt128 / sl[b];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int col = g * kGroup + 4 * lane + i;
+            if (col >= c0 && col < c1) o[(size_t)b * p.dv + col - c0] = v[i] * f;
+        }
+    }
+}
+
+template <int WK, int WV>
+__global__ void __launch_bounds__(kThreads, 2) kv_attend_kernel(const __grid_constant__ KvParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float sM[kMaxHeads], sL[kMaxHeads], sF[kMaxHeads];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, c = lane & 3;
+
+    int lo = 0, hi = p.n_seqs - 1;  // this block's sequence
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.s[mid].cta0 <= (int)blockIdx.x) lo = mid;
+        else hi = mid - 1;
+    }
+    const int si = lo;
+    const KvSeqDev &S = p.s[si];
+    const int chunk = (int)blockIdx.x - S.cta0;
+    const int Hq = p.Hq, ngk = p.ngk, ngv = p.ngv, ntk = p.ntk, ntv = p.ntv;
+    if (S.n == 0) {  // empty softmax: o = 0
+        for (int i = tid; i < Hq * p.dv; i += kThreads) S.o[i] = 0.0f;
+        return;
+    }
+    const int t_begin = chunk * S.chunk_tok, t_end = min(S.n, t_begin + S.chunk_tok);
+
+    uint32_t *tabk = reinterpret_cast<uint32_t *>(smem + p.sm_tabk);  // [4^WK][32]
+    uint32_t *tabv = reinterpret_cast<uint32_t *>(smem + p.sm_tabv);  // [4^WV][32]
+    uint2 *zf = reinterpret_cast<uint2 *>(smem + p.sm_zf);             // [ngk][8][ntk][32]
+    float *isig = reinterpret_cast<float *>(smem + p.sm_isig);         // [Hq][ngk]
+    uint8_t *vcodes = smem + p.sm_vcodes;                              // [kTile][vrow]
+    float *vnorm = reinterpret_cast<float *>(smem + p.sm_vnorm);       // [kTile][ngv]
+    float *sp = reinterpret_cast<float *>(smem + p.sm_p);              // [kTile][16] logits, then weights
+    uint2 *wf = reinterpret_cast<uint2 *>(smem + p.sm_wf);             // [ngv][8][ntv][32]
+    uint32_t *terms = reinterpret_cast<uint32_t *>(smem + p.sm_terms); // [Hq][ngk][128] (setup only)
+    float *sr = reinterpret_cast<float *>(smem + p.sm_r);              // [Hq][ngv*128] (end only)
+
+    // ---- setup: pair tables, rotated queries as B fragments ----
+    for (int i = tid; i < (1 << (2 * WK)) * 32; i += kThreads) {
+        const int e = i >> 5;
+        tabk[i] = (uint32_t)p.lvk[e & ((1 << WK) - 1)] | ((uint32_t)p.lvk[e >> WK] << 16);
+    }
+    for (int i = tid; i < (1 << (2 * WV)) * 32; i += kThreads) {
+        const int e = i >> 5;
+        tabv[i] = (uint32_t)p.lvv[e & ((1 << WV) - 1)] | ((uint32_t)p.lvv[e >> WV] << 16);
+    }
+    if (tid < kMaxHeads) {
+        sM[tid] = -INFINITY;
+        sL[tid] = 0.0f;
+        sF[tid] = 1.0f;  // heads past Hq keep 1 (their accumulators stay 0)
+    }
+    for (int task = warp; task < Hq * ngk; task += kWarps) {
+        const int b = task / ngk, g = task % ngk;
+        const int h = b / p.per, c0 = h * p.dk;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int col = g * kGroup + 4 * lane + i;
+            v[i] = (col >= c0 && col < c0 + p.dk) ? S.q[(size_t)b * p.dk + col - c0] : 0.0f;
+        }
+        fwht128(v, lane);
+        float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+        for (int m = 16; m; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        const float sigma = pow2_scale(mx, 16384.0f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x = __fmul_rn(v[i], sigma);
+            const __half hh = __float2half_rn(x);
+            const __half ll = __float2half_rn(__fsub_rn(x, __half2float(hh)));
+            terms[(b * ngk + g) * kGroup + 4 * lane + i] =
+                (uint32_t)__half_as_ushort(hh) | ((uint32_t)__half_as_ushort(ll) << 16);
+        }
+        if (lane == 0) isig[b * ngk + g] = 1.0f / sigma;
+    }
+    __syncthreads();
+    for (int i = tid; i < ngk * 8 * ntk * 32; i += kThreads) {
+        const int ln = i & 31, nt = (i >> 5) % ntk, nu = (i >> 5) / ntk % 8, g = (i >> 5) / ntk / 8;
+        const int n = 8 * nt + (ln >> 2), b = n >> 1, tau = n & 1, k0 = 32 * (ln & 3) + 4 * nu;
+        uint2 f = make_uint2(0u, 0u);
+        if (b < Hq) {
+            const uint32_t *tw = terms + (b * ngk + g) * kGroup + k0;
+            f.x = ((tw[0] >> (16 * tau)) & 0xffffu) | (((tw[1] >> (16 * tau)) & 0xffffu) << 16);
+            f.y = ((tw[2] >> (16 * tau)) & 0xffffu) | (((tw[3] >> (16 * tau)) & 0xffffu) << 16);
+        }
+        zf[i] = f;
+    }
+    __syncthreads();  // terms (aliased by the value staging) are dead from here
+
+    const int rbk = ngk * 16 * WK, rbv = ngv * 16 * WV;
+    const __half *knorm = reinterpret_cast<const __half *>(S.kc + (size_t)S.cap * rbk);
+    const __half *vn_g = reinterpret_cast<const __half *>(S.vc + (size_t)S.cap * rbv);
+    float acc[kMaxNg][2][4];
+#pragma unroll
+    for (int j = 0; j < kMaxNg; ++j)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[j][nt][i] = 0.0f;
+
+    for (int t0 = t_begin; t0 < t_end; t0 += kTile) {
+        const int nv = min(kTile, t_end - t0);
+        // ---- A. value codes of the sub-tile -> shared memory (async); norms ----
+        for (int i = tid; i < nv * (rbv / 16); i += kThreads) {
+            const int r = i / (rbv / 16), j = i % (rbv / 16);
+            cp_async16(vcodes + r * p.vrow + 16 * j, S.vc + (size_t)(t0 + r) * rbv + 16 * j);
+        }
+        for (int i = tid; i < kTile * ngv; i += kThreads) {
+            const int r = i / ngv;
+            vnorm[i] = r < nv ? __half2float(vn_g[(size_t)(t0 + r) * ngv + i % ngv]) : 0.0f;
+        }
+        // ---- B. logits of 16 tokens per warp ----
+        {
+            const int ta = t0 + 16 * warp + gq, tb = ta + 8;
+            const bool va = ta < t_end, vb = tb < t_end;
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int g = 0; g < ngk; ++g) {
+                uint32_t wa[5], wb[5];
+                load_key_words<WK>(S.kc + (size_t)ta * rbk + g * 16 * WK, c, va, wa);
+                load_key_words<WK>(S.kc + (size_t)tb * rbk + g * 16 * WK, c, vb, wb);
+                const float na = va ? __half2float(knorm[(size_t)ta * ngk + g]) : 0.0f;
+                const float nb = vb ? __half2float(knorm[(size_t)tb * ngk + g]) : 0.0f;
+                float d[4][4];
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) d[nt][i] = 0.0f;
+#pragma unroll
+                for (int nu = 0; nu < 8; ++nu) {
+                    const uint32_t a0 = tabk[bits2<WK>(wa, WK * 4 * nu) * 32 + lane];
+                    const uint32_t a1 = tabk[bits2<WK>(wb, WK * 4 * nu) * 32 + lane];
+                    const uint32_t a2 = tabk[bits2<WK>(wa, WK * (4 * nu + 2)) * 32 + lane];
+                    const uint32_t a3 = tabk[bits2<WK>(wb, WK * (4 * nu + 2)) * 32 + lane];
+                    const uint2 *zb = zf + ((g * 8 + nu) * ntk) * 32 + lane;
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt)
+                        if (nt < ntk) {
+                            const uint2 bf = zb[nt * 32];
+                            mma_f16(d[nt], a0, a1, a2, a3, bf.x, bf.y);
+                        }
+                }
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int b = 4 * nt + c;
+                    if (nt < ntk && b < Hq) {
+                        const float is = isig[b * ngk + g];
+                        sa[nt] = fmaf(na * is, d[nt][0] + d[nt][1], sa[nt]);
+                        sb[nt] = fmaf(nb * is, d[nt][2] + d[nt][3], sb[nt]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int b = 4 * nt + c;
+                if (nt < ntk && b < Hq) {
+                    sp[(16 * warp + gq) * kMaxHeads + b] = va ? sa[nt] * p.logit_scale : -INFINITY;
+                    sp[(16 * warp + gq + 8) * kMaxHeads + b] = vb ? sb[nt] * p.logit_scale : -INFINITY;
+                }
+            }
+        }
+        __syncthreads();
+        // ---- C. online softmax per head ----
+        for (int b = warp; b < Hq; b += kWarps) {
+            float s[4], m = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                s[i] = sp[(lane + 32 * i) * kMaxHeads + b];
+                m = fmaxf(m, s[i]);
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const float m_old = sM[b], m_new = fmaxf(m_old, m);
+            float sum = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float e = expf(s[i] - m_new);  // exp(-inf) = 0 for tokens past the end
+                sp[(lane + 32 * i) * kMaxHeads + b] = e;
+                sum += e;
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (lane == 0) {
+                const float f = expf(m_old - m_new);  // 0 on the first sub-tile
+                sF[b] = f;
+                sM[b] = m_new;
+                sL[b] = fmaf(sL[b], f, sum);
+            }
+        }
+        __syncthreads();
+        // value-side B fragments: w[t][b] = p[t][b] * n_v[t][g] in fp16
+        for (int i = tid; i < ngv * 8 * ntv * 32; i += kThreads) {
+            const int ln = i & 31, nt = (i >> 5) % ntv, tau = (i >> 5) / ntv % 8, g = (i >> 5) / ntv / 8;
+            const int b = 8 * nt + (ln >> 2), t = 16 * tau + 2 * (ln & 3);
+            uint2 f = make_uint2(0u, 0u);
+            if (b < Hq) {
+                f.x = pack_h2(sp[t * kMaxHeads + b] * vnorm[t * ngv + g],
+                              sp[(t + 1) * kMaxHeads + b] * vnorm[(t + 1) * ngv + g]);
+                f.y = pack_h2(sp[(t + 8) * kMaxHeads + b] * vnorm[(t + 8) * ngv + g],
+                              sp[(t + 9) * kMaxHeads + b] * vnorm[(t + 9) * ngv + g]);
+            }
+            wf[i] = f;
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        // ---- D. rotated value sums: rows = coordinates, columns of A = tokens ----
+#pragma unroll
+        for (int j = 0; j < kMaxNg; ++j) {
+            const int mt = warp + kWarps * j;
+            if (mt >= ngv * 8) break;
+            const int g = mt >> 3, mu = mt & 7;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+                if (nt < ntv) {
+                    const float f0 = sF[min(8 * nt + 2 * c, kMaxHeads - 1)];
+                    const float f1 = sF[min(8 * nt + 2 * c + 1, kMaxHeads - 1)];
+                    acc[j][nt][0] *= f0;
+                    acc[j][nt][1] *= f1;
+                    acc[j][nt][2] *= f0;
+                    acc[j][nt][3] *= f1;
+                }
+            const int off = g * kGroup * WV + WV * (16 * mu + 2 * gq);  // bit offset of the code pair
+            for (int tau = 0; tau < 8; ++tau) {
+                const int t = 16 * tau + 2 * c;
+                const uint32_t *r0 = reinterpret_cast<const uint32_t *>(vcodes + t * p.vrow);
+                const uint32_t *r1 = reinterpret_cast<const uint32_t *>(vcodes + (t + 1) * p.vrow);
+                const uint32_t *r2 = reinterpret_cast<const uint32_t *>(vcodes + (t + 8) * p.vrow);
+                const uint32_t *r3 = reinterpret_cast<const uint32_t *>(vcodes + (t + 9) * p.vrow);
+                const uint32_t h0 = tabv[bits2<WV>(r0, off) * 32 + lane];
+                const uint32_t h1 = tabv[bits2<WV>(r1, off) * 32 + lane];
+                const uint32_t h2 = tabv[bits2<WV>(r2, off) * 32 + lane];
+                const uint32_t h3 = tabv[bits2<WV>(r3, off) * 32 + lane];
+                const uint32_t a0 = __byte_perm(h0, h1, 0x5410), a1 = __byte_perm(h0, h1, 0x7632);
+                const uint32_t a2 = __byte_perm(h2, h3, 0x5410), a3 = __byte_perm(h2, h3, 0x7632);
+                const uint2 *wb = wf + ((g * 8 + tau) * ntv) * 32 + lane;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+                    if (nt < ntv) {
+                        const uint2 bf = wb[nt * 32];
+                        mma_f16(acc[j][nt], a0, a1, a2, a3, bf.x, bf.y);
+                    }
+            }
+        }
+        __syncthreads();  // the next sub-tile reuses the staging, the logits and the fragments
+    }
+
+    // ---- E. results: accumulator element i of (slice j, n-tile nt) is
+    // coordinate g*128 + 16*mu + 2*gq + (i >> 1), head 8*nt + 2*c + (i & 1) ----
+    const int ipv = ngv * kGroup;
+    if (S.n_chunks == 1) {
+#pragma unroll
+        for (int j = 0; j < kMaxNg; ++j) {
+            const int mt = warp + kWarps * j;
+            if (mt >= ngv * 8) break;
+            const int k0 = (mt >> 3) * kGroup + 16 * (mt & 7) + 2 * gq;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+                if (nt < ntv)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int b = 8 * nt + 2 * c + (i & 1);
+                        if (b < Hq) sr[b * ipv + k0 + (i >> 1)] = acc[j][nt][i];
+                    }
+        }
+        __syncthreads();
+        finish_heads(p, sr, sL, S.o, warp, lane);
+        return;
+    }
+    const int slot = S.slot0 + chunk;
+    float *part = p.part + (size_t)slot * Hq * ipv;
+#pragma unroll
+    for (int j = 0; j < kMaxNg; ++j) {
+        const int mt = warp + kWarps * j;
+        if (mt >= ngv * 8) break;
+        const int k0 = (mt >> 3) * kGroup + 16 * (mt & 7) + 2 * gq;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+            if (nt < ntv)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int b = 8 * nt + 2 * c + (i & 1);
+                    if (b < Hq) __stcg(part + b * ipv + k0 + (i >> 1), acc[j][nt][i]);
+                }
+    }
+    if (tid < Hq) {
+        __stcg(p.ml + ((size_t)slot * Hq + tid) * 2, sM[tid]);
+        __stcg(p.ml + ((size_t)slot * Hq + tid) * 2 + 1, sL[tid]);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(p.ticket + si, 1u) == (unsigned)(S.n_chunks - 1);
+    __syncthreads();
+    if (!s_last) return;
+    // ---- F. the last block of the sequence merges the partials ----
+    __threadfence();
+    const float *ml0 = p.ml + (size_t)S.slot0 * Hq * 2;
+    if (tid < Hq) {
+        float mx = -INFINITY;
+        for (int ch = 0; ch < S.n_chunks; ++ch) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)ch * Hq + tid) * 2));
+        sM[tid] = mx;
+    }
+    __syncthreads();
+    // per (chunk, head) rescale factors (the logits' buffer holds kTile * 16 >= n_chunks * Hq floats)
+    for (int i = tid; i < S.n_chunks * Hq; i += kThreads) sp[i] = expf(__ldcg(ml0 + 2 * (size_t)i) - sM[i % Hq]);
+    __syncthreads();
+    if (tid < Hq) {
+        float l = 0.0f;
+        for (int ch = 0; ch < S.n_chunks; ++ch) l = fmaf(__ldcg(ml0 + ((size_t)ch * Hq + tid) * 2 + 1), sp[ch * Hq + tid], l);
+        sL[tid] = l;
+    }
+    const float *part0 = p.part + (size_t)S.slot0 * Hq * ipv;
+    for (int i = tid; i < Hq * ipv; i += kThreads) {
+        const int b = i / ipv;
+        float r = 0.0f;
+        for (int ch = 0; ch < S.n_chunks; ++ch) r = fmaf(__ldcg(part0 + (size_t)ch * Hq * ipv + i), sp[ch * Hq + b], r);
+        sr[i] = r;
+    }
+    if (tid == 0) p.ticket[si] = 0u;  // ready for the next launch
+    __syncthreads();
+    finish_heads(p, sr, sL, S.o, warp, lane);
+}
+
+template <int WK, int WV>
+int launch_t(const KvParams &p, int grid, int smem, cudaStream_t st) {
+    auto k = kv_attend_kernel<WK, WV>;
+    static int attr = 0;
+    if (smem > attr) {
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention attribute: %s", cudaGetErrorString(e));
+        attr = smem;
+    }
+    k<<<grid, kThreads, smem, st>>>(p);
+    return CQ_OK;
+}
+
+int align16(int x) { return (x + 15) & ~15; }
+
+}  // namespace
+
+int launch_kv_attend(const cq_kv_geom &g, const cq_kv_seq *seqs, int n, const float *lk, const float *lv,
+                     void *stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int Hq = g.n_q_heads, Hkv = g.n_kv_heads;
+    const int WK = width_of(g.k_bits), WV = width_of(g.v_bits);
+    KvParams p;  // large parameter block (about 15 KB): built here, copied into the launch
+    p.Hq = Hq;
+    p.per = Hq / Hkv;
+    p.dk = g.head_dim_k;
+    p.dv = g.head_dim_v;
+    p.in_k = Hkv * g.head_dim_k;
+    p.in_v = Hkv * g.head_dim_v;
+    p.ngk = in_padded(p.in_k) / kGroup;
+    p.ngv = in_padded(p.in_v) / kGroup;
+    p.ntk = (2 * Hq + 7) / 8;
+    p.ntv = (Hq + 7) / 8;
+    p.logit_scale = g.scale * kInvSqrt128;
+    for (int j = 0; j < 16; ++j) {
+        p.lvk[j] = __half_as_ushort(__float2half_rn(lk[j]));
+        p.lvv[j] = __half_as_ushort(__float2half_rn(lv[j]));
+    }
+    const int rbv = p.ngv * 16 * WV;
+    p.vrow = (rbv % 32 == 16) ? rbv : rbv + 16;  // stride = 16 mod 32 bytes: the four row pairs a warp reads hit distinct banks
+
+    // shared memory: tables, rotated-query fragments, 1/sigma, then one region
+    // used in turn by the query terms (setup), the value codes (sub-tiles) and
+    // the rotated sums (end), then norms, logits and value fragments
+    int off = 0;
+    p.sm_tabk = off;  off += align16((1 << (2 * WK)) * 32 * 4);
+    p.sm_tabv = off;  off += align16((1 << (2 * WV)) * 32 * 4);
+    p.sm_zf = off;    off += align16(p.ngk * 8 * p.ntk * 32 * 8);
+    p.sm_isig = off;  off += align16(Hq * p.ngk * 4);
+    const int uni = std::max({Hq * p.ngk * kGroup * 4, kTile * p.vrow + 16, Hq * p.ngv * kGroup * 4});
+    p.sm_terms = p.sm_vcodes = p.sm_r = off;
+    off += align16(uni);
+    p.sm_vnorm = off; off += align16(kTile * p.ngv * 4);
+    p.sm_p = off;     off += align16(kTile * kMaxHeads * 4);
+    p.sm_wf = off;    off += align16(p.ngv * 8 * p.ntv * 32 * 8);
+    const int smem = off;
+
+    const int sms = sm_count();
+    for (int base = 0; base < n; base += kMaxSeqs) {
+        const int cnt = std::min(kMaxSeqs, n - base);
+        long long total_sub = 0;
+        for (int i = 0; i < cnt; ++i) total_sub += (seqs[base + i].n_tokens + kTile - 1) / kTile;
+        // sub-tiles per block: enough blocks for about four per SM, at most 128 blocks per sequence
+        const long long per_blk = std::max(1LL, (total_sub + 4LL * sms - 1) / (4LL * sms));
+        int cta = 0, slots = 0;
+        for (int i = 0; i < cnt; ++i) {
+            const cq_kv_seq &s = seqs[base + i];
+            KvSeqDev &d = p.s[i];
+            d.kc = s.k_cache;
+            d.vc = s.v_cache;
+            d.q = s.q;
+            d.o = s.o;
+            d.cap = s.cap;
+            d.n = s.n_tokens;
+            const int sub = (s.n_tokens + kTile - 1) / kTile;
+            int chunk_sub = (int)std::min<long long>(per_blk, std::max(sub, 1));
+            if ((sub + chunk_sub - 1) / chunk_sub > 128) chunk_sub = (sub + 127) / 128;
+            d.chunk_tok = chunk_sub * kTile;
+            d.n_chunks = sub == 0 ? 1 : (sub + chunk_sub - 1) / chunk_sub;
+            d.cta0 = cta;
+            cta += d.n_chunks;
+            d.slot0 = slots;
+            if (d.n_chunks > 1) slots += d.n_chunks;
+        }
+        p.n_seqs = cnt;
+        p.part = nullptr;
+        p.ml = nullptr;
+        p.ticket = nullptr;
+        if (slots > 0) {
+            const size_t part_b = ((size_t)slots * Hq * p.ngv * kGroup * 4 + 255) & ~(size_t)255;
+            const size_t ml_b = ((size_t)slots * Hq * 2 * 4 + 255) & ~(size_t)255;
+            int err = CQ_OK;
+            uint8_t *ws = static_cast<uint8_t *>(stream_workspace(stream, 1, part_b + ml_b + (size_t)cnt * 4, &err));
+            if (!ws) return err;
+            p.part = reinterpret_cast<float *>(ws);
+            p.ml = reinterpret_cast<float *>(ws + part_b);
+            p.ticket = reinterpret_cast<unsigned int *>(ws + part_b + ml_b);
+            const cudaError_t e = cudaMemsetAsync(p.ticket, 0, (size_t)cnt * 4, st);
+            if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention tickets: %s", cudaGetErrorString(e));
+        }
+        int rc = CQ_OK;
+        switch (WK * 8 + WV) {
+        case 2 * 8 + 2: rc = launch_t<2, 2>(p, cta, smem, st); break;
+        case 2 * 8 + 3: rc = launch_t<2, 3>(p, cta, smem, st); break;
+        case 2 * 8 + 4: rc = launch_t<2, 4>(p, cta, smem, st); break;
+        case 3 * 8 + 2: rc = launch_t<3, 2>(p, cta, smem, st); break;
+        case 3 * 8 + 3: rc = launch_t<3, 3>(p, cta, smem, st); break;
+        case 3 * 8 + 4: rc = launch_t<3, 4>(p, cta, smem, st); break;
+        case 4 * 8 + 2: rc = launch_t<4, 2>(p, cta, smem, st); break;
+        case 4 * 8 + 3: rc = launch_t<4, 3>(p, cta, smem, st); break;
+        default: rc = launch_t<4, 4>(p, cta, smem, st); break;
+        }
+        if (rc) return rc;
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention launch: %s", cudaGetErrorString(e));
+    }
+    return CQ_OK;
+}
+
+}  // namespace cq

@@ -19,6 +19,13 @@ in OpenNeedle docs/reference.md -- width 512, 27 layers, 8 query heads and
   z / sqrt(chi2_4 / 4) from five seeded normals), x ~ N(0,1).
 * ``encode``:  16 matrices 8192x8192 ~ N(0, 0.02^2), each entry scaled by 20
   with independent probability 0.01 (outliers).
+* ``kv``:      decode-step attention over CQ key/value caches in the Needle 3
+  attention geometry ("Porting Needle 3", "The geometry, for the header": 12
+  query heads of 48 over 2 key/value heads, value heads of 64, context
+  8192): 256 sequences of 8192 cached tokens, CQ2 keys and values. Caches
+  are seeded random blobs (random codes, fp16 norms uniform in [1, 8)) so
+  that the logits spread over several units; queries N(0, 1); logit scale
+  1/sqrt(48).
 """
 from __future__ import annotations
 
@@ -122,3 +129,17 @@ def random_blob(code_bytes: int, n_norms: int, seed: int, ternary: bool = False,
         codes = rng.randint(0, 256, size=code_bytes).astype(np.uint8)
     norms = rng.uniform(norm_lo, norm_hi, size=n_norms).astype(np.float16)
     return np.concatenate([codes, norms.view(np.uint8)])
+
+
+# ------------------------------------------------------------------ kv --
+KV_GEOM = dict(n_q_heads=12, n_kv_heads=2, head_dim_k=48, head_dim_v=64)
+KV_SEQS, KV_TOKENS, KV_BITS = 256, 8192, 2
+
+
+def kv_cache_blob(cap: int, width: int, bits: int, seed: int, norm_lo: float = 1.0,
+                  norm_hi: float = 8.0) -> "np.ndarray":
+    """A seeded random CQ cache of `cap` rows of `width` columns."""
+    ip = (width + 127) // 128 * 128
+    w = 2 if bits == 5 else bits
+    return random_blob(cap * ip * w // 8, cap * ip // 128, seed, ternary=bits == 5,
+                       norm_lo=norm_lo, norm_hi=norm_hi)

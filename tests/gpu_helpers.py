@@ -45,3 +45,42 @@ def compare_encodings(blob_gpu, blob_ref, flags, out, n_in, bits):
     bad = diff & (flags == 0)
     assert not bad.any(), f"{int(bad.sum())} codes differ away from decision boundaries"
     return int(flags.sum()), int((diff & (flags != 0)).sum())
+
+
+def attention_bound(Kh, Vh, q, P, o_ref, n_kv_heads, scale):
+    """Per-element tolerance of decode attention over CQ caches, derived
+    from the product rule. Each logit is a product over CQ weights (the key
+    cache), so it may be off by d_t = scale * 2e-3 * sum_i |k_t,i||q_i|; with
+    d = max_t d_t every softmax weight moves by a factor within e^(+-2d), so
+    o moves by at most (e^(2d) - 1) * sum_t p_t |v_t - o|. The value sum is a
+    product over CQ weights taken in the rotated domain, which bounds its
+    error by 2e-3 * sum_t p_t ||v_t||_2 in every coordinate."""
+    Hq, dk = q.shape
+    per = Hq // n_kv_heads
+    dv = Vh.shape[1] // n_kv_heads
+    bound = np.zeros_like(o_ref)
+    for b in range(Hq):
+        h = b // per
+        if Kh.shape[0] == 0:
+            continue
+        kh, vh = Kh[:, h * dk:(h + 1) * dk], Vh[:, h * dv:(h + 1) * dv]
+        d = scale * MATMUL_TOL * float((np.abs(kh) @ np.abs(q[b])).max())
+        spread = P[b] @ np.abs(vh - o_ref[b])
+        vnorm = float(P[b] @ np.linalg.norm(Vh, axis=1))
+        bound[b] = np.expm1(2 * d) * spread + MATMUL_TOL * vnorm
+    return bound
+
+
+def check_attention(o, o_ref, bound, what=""):
+    o = np.asarray(o, dtype=np.float64)
+    err = np.abs(o - o_ref)
+    worst = float((err / np.maximum(bound, 1e-300)).max()) if err.size else 0.0
+    assert np.all(err <= bound + 1e-30), f"{what}: max |err|/bound = {worst:.3e}"
+    for b in range(o.shape[0]):
+        no, nr = np.linalg.norm(o[b]), np.linalg.norm(o_ref[b])
+        if nr == 0:
+            assert no == 0, f"{what}: head {b} should be exactly zero"
+            continue
+        cos = float(np.dot(o[b], o_ref[b]) / (no * nr))
+        assert cos >= COS_MIN, f"{what}: cosine {cos:.8f} in head {b}"
+    return worst

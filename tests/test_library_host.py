@@ -112,6 +112,21 @@ def test_device_entry_points_reject_bad_arguments_before_launch(C):
     assert lib.cq_gemv_shared(bl, outs, 0, 128, 128, 2, cb, 1, _capi.CQ_X_F32, None, 1, ys, None) == _capi.CQ_ERR_ARG
     assert lib.cq_gemv_shared(None, outs, 2, 128, 128, 2, cb, 1, _capi.CQ_X_F32, None, 1, ys, None) == _capi.CQ_ERR_ARG
     assert lib.cq_gemv_shared(bl, outs, 2, 128, 128, 2, cb, 1, _capi.CQ_X_F32, None, 17, ys, None) == _capi.CQ_ERR_SHAPE
+    geom = _capi.KvGeom(n_q_heads=12, n_kv_heads=5, head_dim_k=48, head_dim_v=64, k_bits=2, v_bits=2,
+                        k_codebook=cb, v_codebook=cb, scale=0.1)
+    seq = _capi.KvSeq(k_cache=16, v_cache=16, q=16, o=16, cap=4, n_tokens=5)
+    assert lib.cq_kv_attend(ctypes.byref(geom), ctypes.byref(seq), 1, None) == _capi.CQ_ERR_SHAPE  # 12 % 5
+    geom.n_kv_heads = 2
+    assert lib.cq_kv_attend(ctypes.byref(geom), ctypes.byref(seq), 1, None) == _capi.CQ_ERR_SHAPE  # n > cap
+    assert b"sequence 0" in lib.cq_last_error()
+    seq.n_tokens, seq.k_cache = 4, 8
+    assert lib.cq_kv_attend(ctypes.byref(geom), ctypes.byref(seq), 1, None) == _capi.CQ_ERR_ARG  # alignment
+    geom.head_dim_k = 300
+    assert lib.cq_kv_attend(ctypes.byref(geom), ctypes.byref(seq), 1, None) == _capi.CQ_ERR_SHAPE  # 600 > 512
+    assert lib.cq_kv_attend(ctypes.byref(geom), ctypes.byref(seq), 0, None) == _capi.CQ_ERR_ARG
+    assert lib.cq_kv_write(None, 4, 96, 2, cb, None, 2, 3, None) == _capi.CQ_ERR_SHAPE  # rows past cap
+    assert lib.cq_kv_write(None, 4, 96, 2, cb, None, 0, 2, None) == _capi.CQ_ERR_ARG   # null cache
+    assert lib.cq_kv_write(None, 4, 96, 2, cb, None, 1, 0, None) == _capi.CQ_OK        # nothing to write
 
 
 def test_binding_requires_the_library(tmp_path, monkeypatch):
