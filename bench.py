@@ -52,6 +52,7 @@ KERNEL_SOURCES = {
     "gemm_x8": ("cq_gemm.cu", "cq_internal.h"),
     "encode_cq2": ("cq_encode.cu", "cq_internal.h"),
     "gather_cq4": ("cq_gather.cu", "cq_internal.h"),
+    "kv_attend": ("cq_kv.cu", "cq_internal.h"),
 }
 
 
@@ -245,7 +246,7 @@ def run_cq(args):
     peaks, peak_kind = measured_peaks()
     barrier, max_over_ranks = rank_ops(world, device)
 
-    if args.only in ("gemm", "encode", "gather"):
+    if args.only in ("gemm", "encode", "gather", "kv"):
         # one part alone, for profiling: only that part's buffers are held
         stream = torch.cuda.Stream(device)
         if args.only == "gemm":
@@ -253,6 +254,8 @@ def run_cq(args):
             res = bench_gemm(C, S, torch, wl, device, stream, peaks, peak_kind, barrier, max_over_ranks, world)
         elif args.only == "gather":
             res = bench_gather(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
+        elif args.only == "kv":
+            res = bench_kv(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
         else:
             res = bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world, args.encode_count)
         if rank == 0:
@@ -377,6 +380,7 @@ def run_cq(args):
         result["encode"] = bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world,
                                         args.encode_count)
         result["gather"] = bench_gather(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
+        result["kv"] = bench_kv(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
     if rank == 0 and world == 1 and not args.skip_cpu:
         result["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     if rank == 0:
@@ -533,6 +537,65 @@ def bench_gather(C, S, torch, device, stream, peaks, barrier, max_over_ranks, wo
                          "algorithmic_bytes_per_launch": algo}}
 
 
+def bench_kv(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world):
+    """Decode-step attention over CQ KV caches: 256 sequences x 8192 cached
+    tokens in the Needle 3 attention geometry, CQ2 keys and values, one call
+    per step. Two copies of the caches (different seeds) alternate between
+    steps, so a step's 144 MB never sit in L2 from the step before."""
+    g = S.KV_GEOM
+    Hq, Hkv, dk, dv = g["n_q_heads"], g["n_kv_heads"], g["head_dim_k"], g["head_dim_v"]
+    T, nseq, bits = S.KV_TOKENS, S.KV_SEQS, S.KV_BITS
+    cb = C.cq_codebook_init(bits)
+    scale = 1.0 / math.sqrt(dk)
+    sets = []
+    for r in range(2):
+        items = []
+        for i in range(nseq):
+            kc = torch.from_numpy(S.kv_cache_blob(T, Hkv * dk, bits, 20000 * r + 5000 + i)).to(device)
+            vc = torch.from_numpy(S.kv_cache_blob(T, Hkv * dv, bits, 20000 * r + 6000 + i)).to(device)
+            q = S.normal((Hq, dk), 20000 * r + 7000 + i).to(device)
+            items.append(dict(k_cache=kc, v_cache=vc, cap=T, n_tokens=T, q=q,
+                              o=torch.empty((Hq, dv), dtype=torch.float32, device=device)))
+        sets.append(items)
+    with torch.cuda.stream(stream):  # grows the workspace before capture
+        for items in sets:
+            C.cq_kv_attend(items, Hq, Hkv, dk, dv, bits, bits, cb, cb, scale)
+    stream.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for items in sets:
+            C.cq_kv_attend(items, Hq, Hkv, dk, dv, bits, bits, cb, cb, scale)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            gr.replay()
+    stream.synchronize()
+    Kg = 20
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(Kg):
+            gr.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1)) / (2 * Kg)
+    # algorithmic bytes: every attended cache row's codes and norms, the
+    # queries read and the outputs written
+    kb = C.cq_packed_bytes(T, Hkv * dk, 128, bits)
+    vb = C.cq_packed_bytes(T, Hkv * dv, 128, bits)
+    algo = nseq * (kb + vb + 4 * Hq * dk + 4 * Hq * dv)
+    gbs = algo / (ms * 1e-3) / 1e9
+    tok = nseq * T / (ms * 1e-3)
+    return {"metric": f"CQ{bits} KV-cache decode attention GB/s ({nseq} sequences x {T} tokens, "
+                      f"{Hq} query heads of {dk} over {Hkv} KV heads, values of {dv})",
+            "value": round(world * gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "cached_tokens_per_s": round(world * tok, 1), "steps": 2 * Kg, "warmup": 6,
+            "l2": "two cache copies alternate (288 MB cycle, 2.2x L2)",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": ncu_traffic("kv_attend"),
+                         "algorithmic_bytes_per_launch": algo}}
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def _oracle_step_sample(budget_s: float):
@@ -604,7 +667,7 @@ def main():
     ap.add_argument("--skip-extra", action="store_true", help="decode step only")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--encode-count", type=int, default=0, help="matrices in the encode part (default 16)")
-    ap.add_argument("--only", default="all", choices=["all", "gemm", "encode", "gather"],
+    ap.add_argument("--only", default="all", choices=["all", "gemm", "encode", "gather", "kv"],
                     help="time one secondary part alone and print its JSON object (profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()

@@ -44,8 +44,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTile = 128;      // tokens per sub-tile
+constexpr int kMaxStages = 3;   // sub-tiles whose copies are in flight
+constexpr int kSpRow = kTile + 8;  // logits [head][token]: the stride spreads a warp's heads over banks
 constexpr int kMaxHeads = 16;   // query heads per call
-constexpr int kMaxNg = 4;       // groups per cache row
 constexpr int kMaxSeqs = 256;   // sequences per launch (the host splits larger calls)
 constexpr float kInvSqrt128 = 0.08838834764831845f;
 
@@ -63,11 +64,16 @@ struct KvParams {
     int Hq, per, dk, dv;     // per = query heads per key/value head
     int in_k, in_v, ngk, ngv;
     int ntk, ntv;            // n-tiles of 8 columns: key side (hi, lo per head), value side
-    float logit_scale;       // scale / sqrt(128) (z is rotated without normalisation)
+    float logit_scale;       // scale * log2(e) / sqrt(128): base-2 logits of the unnormalised rotation
     int n_seqs;
     int vrow;                // staged value-code row stride (bytes)
-    // shared-memory byte offsets
-    int sm_tabk, sm_tabv, sm_zf, sm_isig, sm_vcodes, sm_vnorm, sm_p, sm_wf, sm_terms, sm_r;
+    int krow;                // staged key-code row stride (bytes)
+    int cprk_magic, cprv_magic;  // ceil(65536 / (16-byte pieces per key / value row))
+    int n_stages;            // sub-tiles in flight (1..3)
+    // shared-memory byte offsets; a stage holds key codes at 0, value codes at
+    // off_v, key norms at off_kn and value norms at off_vn
+    int sm_tabk, sm_tabv, sm_zf, sm_isig, sm_p, sm_wf, sm_terms, sm_r, sm_stage;
+    int stage_bytes, off_v, off_kn, off_vn;
     uint16_t lvk[16], lvv[16];  // fp16 level bits by code
     float *part;             // [slot][Hq][ngv*128] partial rotated value sums
     float *ml;               // [slot][Hq][2] running max and sum
@@ -84,11 +90,14 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+// 16-byte asynchronous copy reading src_bytes (1..16) and zero-filling the rest.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
     const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
@@ -129,27 +138,22 @@ __device__ __forceinline__ uint32_t bits2(const uint32_t *w, int off) {
     return __funnelshift_r(w[i], w[i + 1], sh) & 63u;
 }
 
-// Code words of one key row's group for lane quarter c: 4W bytes holding the
-// thread's 32 coordinates 32c .. 32c+31 (zero for a token past the end).
+// Code words of one key row's group (staged in shared memory) for lane
+// quarter c: 4W bytes holding the thread's 32 coordinates 32c .. 32c+31.
 template <int W>
-__device__ __forceinline__ void load_key_words(const uint8_t *grp, int c, bool ok, uint32_t (&w)[5]) {
+__device__ __forceinline__ void load_key_words(const uint8_t *grp, int c, uint32_t (&w)[5]) {
     w[0] = w[1] = w[2] = w[3] = w[4] = 0u;
-    if (!ok) return;
-    if (W == 2) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(grp) + c);
-        w[0] = v.x;
-        w[1] = v.y;
-    } else if (W == 4) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(grp) + c);
+    if (W == 4) {
+        const uint4 v = reinterpret_cast<const uint4 *>(grp)[c];
         w[0] = v.x;
         w[1] = v.y;
         w[2] = v.z;
         w[3] = v.w;
     } else {
-        const uint32_t *p = reinterpret_cast<const uint32_t *>(grp) + 3 * c;
-        w[0] = __ldg(p);
-        w[1] = __ldg(p + 1);
-        w[2] = __ldg(p + 2);
+        const uint32_t *q = reinterpret_cast<const uint32_t *>(grp) + 3 * c;
+        w[0] = q[0];
+        w[1] = q[1];
+        w[2] = q[2];
     }
 }
 
@@ -174,13 +178,24 @@ __device__ void finish_heads(const KvParams &p, const float *sr, const float *sl
     }
 }
 
+// Accumulator slot ms of a warp's value-side work: coordinate of its row
+// gq (hi = 0) or gq + 8 (hi = 1). With 2-bit codes a unit is a pair of
+// 16-coordinate slices fed by one byte lookup per token: slice A holds
+// coordinates 4j, 4j+1 and slice B 4j+2, 4j+3 of bytes j = 8s + gq; with
+// wider codes a unit is one slice of 16 neighbouring coordinates.
+template <int WV>
+__device__ __forceinline__ int slot_coord(int unit, int ms_in_unit, int gq, int hi) {
+    if (WV == 2) return (unit >> 2) * kGroup + 4 * (8 * (unit & 3) + gq) + 2 * ms_in_unit + hi;
+    return (unit >> 3) * kGroup + 16 * (unit & 7) + 2 * gq + hi;
+}
+
 template <int WK, int WV>
 __global__ void __launch_bounds__(kThreads, 2) kv_attend_kernel(const __grid_constant__ KvParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float sM[kMaxHeads], sL[kMaxHeads], sF[kMaxHeads];
     __shared__ int s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gq = lane >> 2, c = lane & 3;
+    const int gq = lane >> 2, c = lane & 3, r16 = lane & 15;
 
     int lo = 0, hi = p.n_seqs - 1;  // this block's sequence
     while (lo < hi) {
@@ -189,34 +204,55 @@ __global__ void __launch_bounds__(kThreads, 2) kv_attend_kernel(const __grid_con
         else hi = mid - 1;
     }
     const int si = lo;
-    const KvSeqDev &S = p.s[si];
-    const int chunk = (int)blockIdx.x - S.cta0;
-    const int Hq = p.Hq, ngk = p.ngk, ngv = p.ngv, ntk = p.ntk, ntv = p.ntv;
-    if (S.n == 0) {  // empty softmax: o = 0
-        for (int i = tid; i < Hq * p.dv; i += kThreads) S.o[i] = 0.0f;
+    // the sequence's fields in registers (indexed parameter reads would repeat in the loops)
+    const uint8_t *const kc = p.s[si].kc;
+    const uint8_t *const vc = p.s[si].vc;
+    const float *const qv = p.s[si].q;
+    float *const ov = p.s[si].o;
+    const int cap = p.s[si].cap, n_tok = p.s[si].n, n_chunks = p.s[si].n_chunks, slot0 = p.s[si].slot0;
+    const int chunk = (int)blockIdx.x - p.s[si].cta0;
+    const int Hq = p.Hq, ngk = p.ngk, ngv = p.ngv, ntk = p.ntk, ntv = p.ntv, vrow = p.vrow;
+    if (n_tok == 0) {  // empty softmax: o = 0
+        for (int i = tid; i < Hq * p.dv; i += kThreads) ov[i] = 0.0f;
         return;
     }
-    const int t_begin = chunk * S.chunk_tok, t_end = min(S.n, t_begin + S.chunk_tok);
+    const int t_begin = chunk * p.s[si].chunk_tok, t_end = min(n_tok, t_begin + p.s[si].chunk_tok);
 
-    uint32_t *tabk = reinterpret_cast<uint32_t *>(smem + p.sm_tabk);  // [4^WK][32]
-    uint32_t *tabv = reinterpret_cast<uint32_t *>(smem + p.sm_tabv);  // [4^WV][32]
+    uint32_t *tabk = reinterpret_cast<uint32_t *>(smem + p.sm_tabk);  // pair table [4^W][32], or quad table [256][16] (W = 2)
+    uint32_t *tabv = reinterpret_cast<uint32_t *>(smem + p.sm_tabv);
     uint2 *zf = reinterpret_cast<uint2 *>(smem + p.sm_zf);             // [ngk][8][ntk][32]
     float *isig = reinterpret_cast<float *>(smem + p.sm_isig);         // [Hq][ngk]
-    uint8_t *vcodes = smem + p.sm_vcodes;                              // [kTile][vrow]
-    float *vnorm = reinterpret_cast<float *>(smem + p.sm_vnorm);       // [kTile][ngv]
-    float *sp = reinterpret_cast<float *>(smem + p.sm_p);              // [kTile][16] logits, then weights
+    float *sp = reinterpret_cast<float *>(smem + p.sm_p);              // [16][kSpRow] logits, then weights
     uint2 *wf = reinterpret_cast<uint2 *>(smem + p.sm_wf);             // [ngv][8][ntv][32]
     uint32_t *terms = reinterpret_cast<uint32_t *>(smem + p.sm_terms); // [Hq][ngk][128] (setup only)
     float *sr = reinterpret_cast<float *>(smem + p.sm_r);              // [Hq][ngv*128] (end only)
 
-    // ---- setup: pair tables, rotated queries as B fragments ----
-    for (int i = tid; i < (1 << (2 * WK)) * 32; i += kThreads) {
-        const int e = i >> 5;
-        tabk[i] = (uint32_t)p.lvk[e & ((1 << WK) - 1)] | ((uint32_t)p.lvk[e >> WK] << 16);
+    // ---- setup: level tables, rotated queries as B fragments ----
+    if (WK == 2) {  // quad table: a code byte -> four fp16 levels, 16 replicas
+        for (int i = tid; i < 256 * 16; i += kThreads) {
+            const int e = i >> 4;
+            tabk[2 * i] = (uint32_t)p.lvk[e & 3] | ((uint32_t)p.lvk[(e >> 2) & 3] << 16);
+            tabk[2 * i + 1] = (uint32_t)p.lvk[(e >> 4) & 3] | ((uint32_t)p.lvk[e >> 6] << 16);
+        }
+    } else {  // pair table: two codes -> two fp16 levels, 32 replicas
+        for (int i = tid; i < (1 << (2 * WK)) * 32; i += kThreads) {
+            const int e = i >> 5;
+            tabk[i] = (uint32_t)p.lvk[e & ((1 << WK) - 1)] | ((uint32_t)p.lvk[e >> WK] << 16);
+        }
     }
-    for (int i = tid; i < (1 << (2 * WV)) * 32; i += kThreads) {
-        const int e = i >> 5;
-        tabv[i] = (uint32_t)p.lvv[e & ((1 << WV) - 1)] | ((uint32_t)p.lvv[e >> WV] << 16);
+    if (p.sm_tabv != p.sm_tabk) {
+        if (WV == 2) {
+            for (int i = tid; i < 256 * 16; i += kThreads) {
+                const int e = i >> 4;
+                tabv[2 * i] = (uint32_t)p.lvv[e & 3] | ((uint32_t)p.lvv[(e >> 2) & 3] << 16);
+                tabv[2 * i + 1] = (uint32_t)p.lvv[(e >> 4) & 3] | ((uint32_t)p.lvv[e >> 6] << 16);
+            }
+        } else {
+            for (int i = tid; i < (1 << (2 * WV)) * 32; i += kThreads) {
+                const int e = i >> 5;
+                tabv[i] = (uint32_t)p.lvv[e & ((1 << WV) - 1)] | ((uint32_t)p.lvv[e >> WV] << 16);
+            }
+        }
     }
     if (tid < kMaxHeads) {
         sM[tid] = -INFINITY;
@@ -224,13 +260,13 @@ __global__ void __launch_bounds__(kThreads, 2) kv_attend_kernel(const __grid_con
         sF[tid] = 1.0f;  // heads past Hq keep 1 (their accumulators stay 0)
     }
     for (int task = warp; task < Hq * ngk; task += kWarps) {
-        const int b = task / ngk, g = task % ngk;
-        const int h = b / p.per, c0 = h * p.dk;
+        const int b = task / ngk, g = task - b * ngk;
+        const int c0 = (b / p.per) * p.dk;
         float v[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int col = g * kGroup + 4 * lane + i;
-            v[i] = (col >= c0 && col < c0 + p.dk) ? S.q[(size_t)b * p.dk + col - c0] : 0.0f;
+            v[i] = (col >= c0 && col < c0 + p.dk) ? qv[(size_t)b * p.dk + col - c0] : 0.0f;
         }
         fwht128(v, lane);
         float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
@@ -248,70 +284,131 @@ __global__ void __launch_bounds__(kThreads, 2) kv_attend_kernel(const __grid_con
         if (lane == 0) isig[b * ngk + g] = 1.0f / sigma;
     }
     __syncthreads();
-    for (int i = tid; i < ngk * 8 * ntk * 32; i += kThreads) {
-        const int ln = i & 31, nt = (i >> 5) % ntk, nu = (i >> 5) / ntk % 8, g = (i >> 5) / ntk / 8;
-        const int n = 8 * nt + (ln >> 2), b = n >> 1, tau = n & 1, k0 = 32 * (ln & 3) + 4 * nu;
-        uint2 f = make_uint2(0u, 0u);
-        if (b < Hq) {
-            const uint32_t *tw = terms + (b * ngk + g) * kGroup + k0;
-            f.x = ((tw[0] >> (16 * tau)) & 0xffffu) | (((tw[1] >> (16 * tau)) & 0xffffu) << 16);
-            f.y = ((tw[2] >> (16 * tau)) & 0xffffu) | (((tw[3] >> (16 * tau)) & 0xffffu) << 16);
-        }
-        zf[i] = f;
-    }
+    // B fragments: word (g, nu, nt, lane) of column n = 8 nt + lane/4 (head n/2,
+    // term n%2), positions 32 (lane%4) + 4 nu + {0,1} and {2,3}
+    for (int g = 0; g < ngk; ++g)
+        for (int nu = warp; nu < 8; nu += kWarps)
+            for (int nt = 0; nt < ntk; ++nt) {
+                const int n = 8 * nt + gq, b = n >> 1, tau = n & 1, k0 = 32 * c + 4 * nu;
+                uint2 f = make_uint2(0u, 0u);
+                if (b < Hq) {
+                    const uint32_t *tw = terms + (b * ngk + g) * kGroup + k0;
+                    f.x = ((tw[0] >> (16 * tau)) & 0xffffu) | (((tw[1] >> (16 * tau)) & 0xffffu) << 16);
+                    f.y = ((tw[2] >> (16 * tau)) & 0xffffu) | (((tw[3] >> (16 * tau)) & 0xffffu) << 16);
+                }
+                zf[((g * 8 + nu) * ntk + nt) * 32 + lane] = f;
+            }
     __syncthreads();  // terms (aliased by the value staging) are dead from here
 
-    const int rbk = ngk * 16 * WK, rbv = ngv * 16 * WV;
-    const __half *knorm = reinterpret_cast<const __half *>(S.kc + (size_t)S.cap * rbk);
-    const __half *vn_g = reinterpret_cast<const __half *>(S.vc + (size_t)S.cap * rbv);
-    float acc[kMaxNg][2][4];
+    const int rbk = ngk * 16 * WK, rbv = ngv * 16 * WV, cprk = rbk >> 4, cprv = rbv >> 4;
+    const int krow = p.krow;
+    const uint8_t *const knorm_b = kc + (size_t)cap * rbk;  // fp16 norms [cap][ngk]
+    const uint8_t *const vnorm_b = vc + (size_t)cap * rbv;
+    // value-side work of this warp: its units, and its token tiles when two
+    // warps share a unit (2-bit codes, one group: four units for eight warps)
+    const int units = (WV == 2 ? 4 : 8) * ngv;
+    const int split = units < kWarps ? kWarps / units : 1;
+    const int unit0 = split > 1 ? warp % units : warp;
+    const int tau0 = split > 1 ? (warp / units) * (8 / split) : 0;
+    const int tau1 = split > 1 ? tau0 + 8 / split : 8;
+    float acc[4][2][4];
 #pragma unroll
-    for (int j = 0; j < kMaxNg; ++j)
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[j][nt][i] = 0.0f;
 
-    for (int t0 = t_begin; t0 < t_end; t0 += kTile) {
-        const int nv = min(kTile, t_end - t0);
-        // ---- A. value codes of the sub-tile -> shared memory (async); norms ----
-        for (int i = tid; i < nv * (rbv / 16); i += kThreads) {
-            const int r = i / (rbv / 16), j = i % (rbv / 16);
-            cp_async16(vcodes + r * p.vrow + 16 * j, S.vc + (size_t)(t0 + r) * rbv + 16 * j);
+    // Copies of sub-tile i into stage i % kStages, one commit group: key and
+    // value code rows, then the two fp16 norm blocks (contiguous in the
+    // cache; the last 16-byte piece reads only the rows that exist and
+    // zero-fills the rest).
+    const int nsub = (t_end - t_begin + kTile - 1) / kTile, NB = p.n_stages;
+    auto issue = [&](int i) {
+        uint8_t *stg = smem + p.sm_stage + (i % NB) * p.stage_bytes;
+        const int t0 = t_begin + i * kTile, nv = min(kTile, t_end - t0);
+        for (int x = tid; x < nv * cprk; x += kThreads) {
+            const int r = (x * p.cprk_magic) >> 16, j = x - r * cprk;  // x / cprk, exact here
+            cp_async16(stg + r * krow + 16 * j, kc + (size_t)(t0 + r) * rbk + 16 * j, 16);
         }
-        for (int i = tid; i < kTile * ngv; i += kThreads) {
-            const int r = i / ngv;
-            vnorm[i] = r < nv ? __half2float(vn_g[(size_t)(t0 + r) * ngv + i % ngv]) : 0.0f;
+        for (int x = tid; x < nv * cprv; x += kThreads) {
+            const int r = (x * p.cprv_magic) >> 16, j = x - r * cprv;
+            cp_async16(stg + p.off_v + r * vrow + 16 * j, vc + (size_t)(t0 + r) * rbv + 16 * j, 16);
         }
-        // ---- B. logits of 16 tokens per warp ----
+        const int kb = nv * 2 * ngk, vb = nv * 2 * ngv, kp = (kb + 15) >> 4, vp = (vb + 15) >> 4;
+        for (int x = tid; x < kp + vp; x += kThreads) {
+            if (x < kp)
+                cp_async16(stg + p.off_kn + 16 * x, knorm_b + (size_t)t0 * 2 * ngk + 16 * x, min(16, kb - 16 * x));
+            else
+                cp_async16(stg + p.off_vn + 16 * (x - kp), vnorm_b + (size_t)t0 * 2 * ngv + 16 * (x - kp),
+                           min(16, vb - 16 * (x - kp)));
+        }
+        cp_async_commit();
+    };
+    for (int j = 0; j + 1 < NB; ++j) {
+        if (j < nsub) issue(j);
+        else cp_async_commit();  // empty groups keep the count of groups in flight uniform
+    }
+    for (int it = 0; it < nsub; ++it) {
+        if (it + NB - 1 < nsub) issue(it + NB - 1);
+        else cp_async_commit();
+        // this sub-tile's copies have landed (NB - 1 younger groups may still fly)
+        if (NB == 3) cp_async_wait<2>();
+        else if (NB == 2) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        __syncthreads();
+        const int t0 = t_begin + it * kTile, nv = min(kTile, t_end - t0);
+        const uint8_t *ks = smem + p.sm_stage + (it % NB) * p.stage_bytes;
+        const uint8_t *vcodes = ks + p.off_v;
+        const __half *kns = reinterpret_cast<const __half *>(ks + p.off_kn);
+        const __half *vns = reinterpret_cast<const __half *>(ks + p.off_vn);
+        // ---- B. logits of 16 tokens per warp (log2 units) ----
         {
-            const int ta = t0 + 16 * warp + gq, tb = ta + 8;
-            const bool va = ta < t_end, vb = tb < t_end;
+            const int ra = 16 * warp + gq, rb = ra + 8;  // rows of the sub-tile
+            const bool va = ra < nv, vb = rb < nv;
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
             for (int g = 0; g < ngk; ++g) {
-                uint32_t wa[5], wb[5];
-                load_key_words<WK>(S.kc + (size_t)ta * rbk + g * 16 * WK, c, va, wa);
-                load_key_words<WK>(S.kc + (size_t)tb * rbk + g * 16 * WK, c, vb, wb);
-                const float na = va ? __half2float(knorm[(size_t)ta * ngk + g]) : 0.0f;
-                const float nb = vb ? __half2float(knorm[(size_t)tb * ngk + g]) : 0.0f;
+                const float na = __half2float(kns[ra * ngk + g]), nb = __half2float(kns[rb * ngk + g]);
                 float d[4][4];
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) d[nt][i] = 0.0f;
+                if (WK == 2) {
+                    const uint2 ca = *reinterpret_cast<const uint2 *>(ks + ra * krow + g * 32 + 8 * c);
+                    const uint2 cb = *reinterpret_cast<const uint2 *>(ks + rb * krow + g * 32 + 8 * c);
+                    const uint2 *t4 = reinterpret_cast<const uint2 *>(tabk) + r16;
 #pragma unroll
-                for (int nu = 0; nu < 8; ++nu) {
-                    const uint32_t a0 = tabk[bits2<WK>(wa, WK * 4 * nu) * 32 + lane];
-                    const uint32_t a1 = tabk[bits2<WK>(wb, WK * 4 * nu) * 32 + lane];
-                    const uint32_t a2 = tabk[bits2<WK>(wa, WK * (4 * nu + 2)) * 32 + lane];
-                    const uint32_t a3 = tabk[bits2<WK>(wb, WK * (4 * nu + 2)) * 32 + lane];
-                    const uint2 *zb = zf + ((g * 8 + nu) * ntk) * 32 + lane;
+                    for (int nu = 0; nu < 8; ++nu) {
+                        const uint32_t wa = nu < 4 ? ca.x : ca.y, wb = nu < 4 ? cb.x : cb.y;
+                        const uint2 ea = t4[((wa >> (8 * (nu & 3))) & 0xffu) * 16];
+                        const uint2 eb = t4[((wb >> (8 * (nu & 3))) & 0xffu) * 16];
+                        const uint2 *zb = zf + ((g * 8 + nu) * ntk) * 32 + lane;
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt)
-                        if (nt < ntk) {
-                            const uint2 bf = zb[nt * 32];
-                            mma_f16(d[nt], a0, a1, a2, a3, bf.x, bf.y);
-                        }
+                        for (int nt = 0; nt < 4; ++nt)
+                            if (nt < ntk) {
+                                const uint2 bf = zb[nt * 32];
+                                mma_f16(d[nt], ea.x, eb.x, ea.y, eb.y, bf.x, bf.y);
+                            }
+                    }
+                } else {
+                    uint32_t wa[5], wb[5];
+                    load_key_words<WK>(ks + ra * krow + g * 16 * WK, c, wa);
+                    load_key_words<WK>(ks + rb * krow + g * 16 * WK, c, wb);
+#pragma unroll
+                    for (int nu = 0; nu < 8; ++nu) {
+                        const uint32_t a0 = tabk[bits2<WK>(wa, WK * 4 * nu) * 32 + lane];
+                        const uint32_t a1 = tabk[bits2<WK>(wb, WK * 4 * nu) * 32 + lane];
+                        const uint32_t a2 = tabk[bits2<WK>(wa, WK * (4 * nu + 2)) * 32 + lane];
+                        const uint32_t a3 = tabk[bits2<WK>(wb, WK * (4 * nu + 2)) * 32 + lane];
+                        const uint2 *zb = zf + ((g * 8 + nu) * ntk) * 32 + lane;
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt)
+                            if (nt < ntk) {
+                                const uint2 bf = zb[nt * 32];
+                                mma_f16(d[nt], a0, a1, a2, a3, bf.x, bf.y);
+                            }
+                    }
                 }
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
@@ -323,22 +420,23 @@ __global__ void __launch_bounds__(kThreads, 2) kv_attend_kernel(const __grid_con
                     }
                 }
             }
+            // rows past the end hold stale bytes: their logits are -inf
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 const int b = 4 * nt + c;
                 if (nt < ntk && b < Hq) {
-                    sp[(16 * warp + gq) * kMaxHeads + b] = va ? sa[nt] * p.logit_scale : -INFINITY;
-                    sp[(16 * warp + gq + 8) * kMaxHeads + b] = vb ? sb[nt] * p.logit_scale : -INFINITY;
+                    sp[b * kSpRow + ra] = va ? sa[nt] * p.logit_scale : -INFINITY;
+                    sp[b * kSpRow + rb] = vb ? sb[nt] * p.logit_scale : -INFINITY;
                 }
             }
         }
         __syncthreads();
-        // ---- C. online softmax per head ----
+        // ---- C. online softmax per head (base 2: the logits carry log2(e)) ----
         for (int b = warp; b < Hq; b += kWarps) {
             float s[4], m = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                s[i] = sp[(lane + 32 * i) * kMaxHeads + b];
+                s[i] = sp[b * kSpRow + lane + 32 * i];
                 m = fmaxf(m, s[i]);
             }
 #pragma unroll
@@ -347,150 +445,177 @@ __global__ void __launch_bounds__(kThreads, 2) kv_attend_kernel(const __grid_con
             float sum = 0.0f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float e = expf(s[i] - m_new);  // exp(-inf) = 0 for tokens past the end
-                sp[(lane + 32 * i) * kMaxHeads + b] = e;
+                const float e = exp2f(s[i] - m_new);  // 0 for tokens past the end
+                sp[b * kSpRow + lane + 32 * i] = e;
                 sum += e;
             }
 #pragma unroll
             for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
             if (lane == 0) {
-                const float f = expf(m_old - m_new);  // 0 on the first sub-tile
+                const float f = exp2f(m_old - m_new);  // 0 on the first sub-tile
                 sF[b] = f;
                 sM[b] = m_new;
                 sL[b] = fmaf(sL[b], f, sum);
             }
         }
         __syncthreads();
-        // value-side B fragments: w[t][b] = p[t][b] * n_v[t][g] in fp16
-        for (int i = tid; i < ngv * 8 * ntv * 32; i += kThreads) {
-            const int ln = i & 31, nt = (i >> 5) % ntv, tau = (i >> 5) / ntv % 8, g = (i >> 5) / ntv / 8;
-            const int b = 8 * nt + (ln >> 2), t = 16 * tau + 2 * (ln & 3);
-            uint2 f = make_uint2(0u, 0u);
-            if (b < Hq) {
-                f.x = pack_h2(sp[t * kMaxHeads + b] * vnorm[t * ngv + g],
-                              sp[(t + 1) * kMaxHeads + b] * vnorm[(t + 1) * ngv + g]);
-                f.y = pack_h2(sp[(t + 8) * kMaxHeads + b] * vnorm[(t + 8) * ngv + g],
-                              sp[(t + 9) * kMaxHeads + b] * vnorm[(t + 9) * ngv + g]);
+        // value-side B fragments of token tile `warp`: w[t][b] = p[t][b] * n_v[t][g] in fp16
+        {
+            const int t = 16 * warp + 2 * c;
+            for (int g = 0; g < ngv; ++g) {
+                const float n0 = t < nv ? __half2float(vns[t * ngv + g]) : 0.0f;
+                const float n1 = t + 1 < nv ? __half2float(vns[(t + 1) * ngv + g]) : 0.0f;
+                const float n8 = t + 8 < nv ? __half2float(vns[(t + 8) * ngv + g]) : 0.0f;
+                const float n9 = t + 9 < nv ? __half2float(vns[(t + 9) * ngv + g]) : 0.0f;
+                for (int nt = 0; nt < ntv; ++nt) {
+                    const int b = 8 * nt + gq;
+                    uint2 f = make_uint2(0u, 0u);
+                    if (b < Hq) {
+                        f.x = pack_h2(sp[b * kSpRow + t] * n0, sp[b * kSpRow + t + 1] * n1);
+                        f.y = pack_h2(sp[b * kSpRow + t + 8] * n8, sp[b * kSpRow + t + 9] * n9);
+                    }
+                    wf[((g * 8 + warp) * ntv + nt) * 32 + lane] = f;
+                }
             }
-            wf[i] = f;
         }
-        cp_async_wait_all();
         __syncthreads();
-        // ---- D. rotated value sums: rows = coordinates, columns of A = tokens ----
+        // ---- D. rotated value sums: rows of A = coordinates, columns = tokens ----
 #pragma unroll
-        for (int j = 0; j < kMaxNg; ++j) {
-            const int mt = warp + kWarps * j;
-            if (mt >= ngv * 8) break;
-            const int g = mt >> 3, mu = mt & 7;
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
                 if (nt < ntv) {
-                    const float f0 = sF[min(8 * nt + 2 * c, kMaxHeads - 1)];
-                    const float f1 = sF[min(8 * nt + 2 * c + 1, kMaxHeads - 1)];
+                    const float f0 = sF[8 * nt + 2 * c], f1 = sF[8 * nt + 2 * c + 1];
                     acc[j][nt][0] *= f0;
                     acc[j][nt][1] *= f1;
                     acc[j][nt][2] *= f0;
                     acc[j][nt][3] *= f1;
                 }
-            const int off = g * kGroup * WV + WV * (16 * mu + 2 * gq);  // bit offset of the code pair
-            for (int tau = 0; tau < 8; ++tau) {
-                const int t = 16 * tau + 2 * c;
-                const uint32_t *r0 = reinterpret_cast<const uint32_t *>(vcodes + t * p.vrow);
-                const uint32_t *r1 = reinterpret_cast<const uint32_t *>(vcodes + (t + 1) * p.vrow);
-                const uint32_t *r2 = reinterpret_cast<const uint32_t *>(vcodes + (t + 8) * p.vrow);
-                const uint32_t *r3 = reinterpret_cast<const uint32_t *>(vcodes + (t + 9) * p.vrow);
-                const uint32_t h0 = tabv[bits2<WV>(r0, off) * 32 + lane];
-                const uint32_t h1 = tabv[bits2<WV>(r1, off) * 32 + lane];
-                const uint32_t h2 = tabv[bits2<WV>(r2, off) * 32 + lane];
-                const uint32_t h3 = tabv[bits2<WV>(r3, off) * 32 + lane];
-                const uint32_t a0 = __byte_perm(h0, h1, 0x5410), a1 = __byte_perm(h0, h1, 0x7632);
-                const uint32_t a2 = __byte_perm(h2, h3, 0x5410), a3 = __byte_perm(h2, h3, 0x7632);
-                const uint2 *wb = wf + ((g * 8 + tau) * ntv) * 32 + lane;
+        if (WV == 2) {
+            const uint2 *t4 = reinterpret_cast<const uint2 *>(tabv) + r16;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-                    if (nt < ntv) {
-                        const uint2 bf = wb[nt * 32];
-                        mma_f16(acc[j][nt], a0, a1, a2, a3, bf.x, bf.y);
-                    }
+            for (int k = 0; k < 2; ++k) {
+                const int unit = unit0 + k * kWarps;
+                if (unit >= units || (split > 1 && k > 0)) break;
+                const int g = unit >> 2, boff = g * 32 + 8 * (unit & 3) + gq;
+                for (int tau = tau0; tau < tau1; ++tau) {
+                    const uint8_t *row = vcodes + (16 * tau + 2 * c) * vrow + boff;
+                    const uint2 h0 = t4[(uint32_t)row[0] * 16], h1 = t4[(uint32_t)row[vrow] * 16];
+                    const uint2 h2 = t4[(uint32_t)row[8 * vrow] * 16], h3 = t4[(uint32_t)row[9 * vrow] * 16];
+                    const uint32_t aA0 = __byte_perm(h0.x, h1.x, 0x5410), aA1 = __byte_perm(h0.x, h1.x, 0x7632);
+                    const uint32_t aA2 = __byte_perm(h2.x, h3.x, 0x5410), aA3 = __byte_perm(h2.x, h3.x, 0x7632);
+                    const uint32_t aB0 = __byte_perm(h0.y, h1.y, 0x5410), aB1 = __byte_perm(h0.y, h1.y, 0x7632);
+                    const uint32_t aB2 = __byte_perm(h2.y, h3.y, 0x5410), aB3 = __byte_perm(h2.y, h3.y, 0x7632);
+                    const uint2 *wb = wf + ((g * 8 + tau) * ntv) * 32 + lane;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+                        if (nt < ntv) {
+                            const uint2 bf = wb[nt * 32];
+                            mma_f16(acc[2 * k][nt], aA0, aA1, aA2, aA3, bf.x, bf.y);
+                            mma_f16(acc[2 * k + 1][nt], aB0, aB1, aB2, aB3, bf.x, bf.y);
+                        }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int unit = unit0 + k * kWarps;
+                if (unit >= units) break;
+                const int g = unit >> 3, mu = unit & 7;
+                const int off = g * kGroup * WV + WV * (16 * mu + 2 * gq);  // bit offset of the code pair
+                for (int tau = 0; tau < 8; ++tau) {
+                    const int t = 16 * tau + 2 * c;
+                    const uint32_t *r0 = reinterpret_cast<const uint32_t *>(vcodes + t * vrow);
+                    const uint32_t *r1 = reinterpret_cast<const uint32_t *>(vcodes + (t + 1) * vrow);
+                    const uint32_t *r2 = reinterpret_cast<const uint32_t *>(vcodes + (t + 8) * vrow);
+                    const uint32_t *r3 = reinterpret_cast<const uint32_t *>(vcodes + (t + 9) * vrow);
+                    const uint32_t h0 = tabv[bits2<WV>(r0, off) * 32 + lane];
+                    const uint32_t h1 = tabv[bits2<WV>(r1, off) * 32 + lane];
+                    const uint32_t h2 = tabv[bits2<WV>(r2, off) * 32 + lane];
+                    const uint32_t h3 = tabv[bits2<WV>(r3, off) * 32 + lane];
+                    const uint32_t a0 = __byte_perm(h0, h1, 0x5410), a1 = __byte_perm(h0, h1, 0x7632);
+                    const uint32_t a2 = __byte_perm(h2, h3, 0x5410), a3 = __byte_perm(h2, h3, 0x7632);
+                    const uint2 *wb = wf + ((g * 8 + tau) * ntv) * 32 + lane;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+                        if (nt < ntv) {
+                            const uint2 bf = wb[nt * 32];
+                            mma_f16(acc[k][nt], a0, a1, a2, a3, bf.x, bf.y);
+                        }
+                }
             }
         }
-        __syncthreads();  // the next sub-tile reuses the staging, the logits and the fragments
+        __syncthreads();  // the stage is refilled two sub-tiles later; logits and fragments next one
     }
+    cp_async_wait<0>();  // only empty groups remain; nothing may land after the block moves on
 
-    // ---- E. results: accumulator element i of (slice j, n-tile nt) is
-    // coordinate g*128 + 16*mu + 2*gq + (i >> 1), head 8*nt + 2*c + (i & 1) ----
+    // ---- E. rotated sums into shared memory: element i of slot (unit, m)
+    // is row gq + 8 (i >> 1), head 8 nt + 2c + (i & 1); warps that split a
+    // unit's tokens add into the same words ----
     const int ipv = ngv * kGroup;
-    if (S.n_chunks == 1) {
+    for (int i = tid; i < Hq * ipv; i += kThreads) sr[i] = 0.0f;
+    __syncthreads();
 #pragma unroll
-        for (int j = 0; j < kMaxNg; ++j) {
-            const int mt = warp + kWarps * j;
-            if (mt >= ngv * 8) break;
-            const int k0 = (mt >> 3) * kGroup + 16 * (mt & 7) + 2 * gq;
+    for (int k = 0; k < (WV == 2 ? 2 : 4); ++k) {
+        const int unit = unit0 + k * kWarps;
+        if (unit >= units || (split > 1 && k > 0)) break;
+#pragma unroll
+        for (int m = 0; m < (WV == 2 ? 2 : 1); ++m) {
+            const int ms = WV == 2 ? 2 * k + m : k;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
                 if (nt < ntv)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int b = 8 * nt + 2 * c + (i & 1);
-                        if (b < Hq) sr[b * ipv + k0 + (i >> 1)] = acc[j][nt][i];
+                        if (b < Hq) atomicAdd(sr + b * ipv + slot_coord<WV>(unit, m, gq, i >> 1), acc[ms][nt][i]);
                     }
         }
-        __syncthreads();
-        finish_heads(p, sr, sL, S.o, warp, lane);
+    }
+    __syncthreads();
+    if (n_chunks == 1) {
+        finish_heads(p, sr, sL, ov, warp, lane);
         return;
     }
-    const int slot = S.slot0 + chunk;
+    const int slot = slot0 + chunk;
     float *part = p.part + (size_t)slot * Hq * ipv;
-#pragma unroll
-    for (int j = 0; j < kMaxNg; ++j) {
-        const int mt = warp + kWarps * j;
-        if (mt >= ngv * 8) break;
-        const int k0 = (mt >> 3) * kGroup + 16 * (mt & 7) + 2 * gq;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-            if (nt < ntv)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int b = 8 * nt + 2 * c + (i & 1);
-                    if (b < Hq) __stcg(part + b * ipv + k0 + (i >> 1), acc[j][nt][i]);
-                }
-    }
+    for (int i = tid; i < Hq * ipv; i += kThreads) __stcg(part + i, sr[i]);
     if (tid < Hq) {
         __stcg(p.ml + ((size_t)slot * Hq + tid) * 2, sM[tid]);
         __stcg(p.ml + ((size_t)slot * Hq + tid) * 2 + 1, sL[tid]);
     }
     __threadfence();
     __syncthreads();
-    if (tid == 0) s_last = atomicAdd(p.ticket + si, 1u) == (unsigned)(S.n_chunks - 1);
+    if (tid == 0) s_last = atomicAdd(p.ticket + si, 1u) == (unsigned)(n_chunks - 1);
     __syncthreads();
     if (!s_last) return;
     // ---- F. the last block of the sequence merges the partials ----
     __threadfence();
-    const float *ml0 = p.ml + (size_t)S.slot0 * Hq * 2;
+    const float *ml0 = p.ml + (size_t)slot0 * Hq * 2;
     if (tid < Hq) {
         float mx = -INFINITY;
-        for (int ch = 0; ch < S.n_chunks; ++ch) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)ch * Hq + tid) * 2));
+        for (int ch = 0; ch < n_chunks; ++ch) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)ch * Hq + tid) * 2));
         sM[tid] = mx;
     }
     __syncthreads();
-    // per (chunk, head) rescale factors (the logits' buffer holds kTile * 16 >= n_chunks * Hq floats)
-    for (int i = tid; i < S.n_chunks * Hq; i += kThreads) sp[i] = expf(__ldcg(ml0 + 2 * (size_t)i) - sM[i % Hq]);
+    // per (chunk, head) rescale factors (the logits' buffer holds 16 * kSpRow >= n_chunks * Hq floats)
+    for (int i = tid; i < n_chunks * Hq; i += kThreads) sp[i] = exp2f(__ldcg(ml0 + 2 * (size_t)i) - sM[i % Hq]);
     __syncthreads();
     if (tid < Hq) {
         float l = 0.0f;
-        for (int ch = 0; ch < S.n_chunks; ++ch) l = fmaf(__ldcg(ml0 + ((size_t)ch * Hq + tid) * 2 + 1), sp[ch * Hq + tid], l);
+        for (int ch = 0; ch < n_chunks; ++ch) l = fmaf(__ldcg(ml0 + ((size_t)ch * Hq + tid) * 2 + 1), sp[ch * Hq + tid], l);
         sL[tid] = l;
     }
-    const float *part0 = p.part + (size_t)S.slot0 * Hq * ipv;
+    const float *part0 = p.part + (size_t)slot0 * Hq * ipv;
     for (int i = tid; i < Hq * ipv; i += kThreads) {
         const int b = i / ipv;
         float r = 0.0f;
-        for (int ch = 0; ch < S.n_chunks; ++ch) r = fmaf(__ldcg(part0 + (size_t)ch * Hq * ipv + i), sp[ch * Hq + b], r);
+        for (int ch = 0; ch < n_chunks; ++ch) r = fmaf(__ldcg(part0 + (size_t)ch * Hq * ipv + i), sp[ch * Hq + b], r);
         sr[i] = r;
     }
     if (tid == 0) p.ticket[si] = 0u;  // ready for the next launch
     __syncthreads();
-    finish_heads(p, sr, sL, S.o, warp, lane);
+    finish_heads(p, sr, sL, ov, warp, lane);
 }
 
 template <int WK, int WV>
@@ -526,28 +651,60 @@ int launch_kv_attend(const cq_kv_geom &g, const cq_kv_seq *seqs, int n, const fl
     p.ngv = in_padded(p.in_v) / kGroup;
     p.ntk = (2 * Hq + 7) / 8;
     p.ntv = (Hq + 7) / 8;
-    p.logit_scale = g.scale * kInvSqrt128;
+    p.logit_scale = (float)((double)g.scale * 1.4426950408889634 / std::sqrt(128.0));
     for (int j = 0; j < 16; ++j) {
         p.lvk[j] = __half_as_ushort(__float2half_rn(lk[j]));
         p.lvv[j] = __half_as_ushort(__float2half_rn(lv[j]));
     }
     const int rbv = p.ngv * 16 * WV;
     p.vrow = (rbv % 32 == 16) ? rbv : rbv + 16;  // stride = 16 mod 32 bytes: the four row pairs a warp reads hit distinct banks
+    const int rbk = p.ngk * 16 * WK;
+    // key rows: a half-warp's 8-byte (2-bit) or 16-byte (4-bit) reads of
+    // four or two rows fall in distinct banks
+    p.krow = rbk;
+    if (WK == 2 && rbk % 64 == 0) p.krow = rbk + 32;
+    if (WK == 4 && rbk % 128 == 0) p.krow = rbk + 64;
+    if (WK == 3 && rbk % 32 == 0) p.krow = rbk + 16;
+    p.cprk_magic = (65536 + rbk / 16 - 1) / (rbk / 16);
+    p.cprv_magic = (65536 + rbv / 16 - 1) / (rbv / 16);
+    bool same_levels = WK == WV;
+    for (int j = 0; j < 16; ++j) same_levels = same_levels && p.lvk[j] == p.lvv[j];
 
     // shared memory: tables, rotated-query fragments, 1/sigma, then one region
     // used in turn by the query terms (setup), the value codes (sub-tiles) and
     // the rotated sums (end), then norms, logits and value fragments
     int off = 0;
-    p.sm_tabk = off;  off += align16((1 << (2 * WK)) * 32 * 4);
-    p.sm_tabv = off;  off += align16((1 << (2 * WV)) * 32 * 4);
+    // level tables: 2-bit codes a byte -> four levels (256 x 16 replicas x 8 B),
+    // else a code pair -> two levels (4^W x 32 replicas x 4 B); one table when
+    // keys and values share their codes and levels
+    const int tabk_b = WK == 2 ? 256 * 16 * 8 : (1 << (2 * WK)) * 32 * 4;
+    const int tabv_b = WV == 2 ? 256 * 16 * 8 : (1 << (2 * WV)) * 32 * 4;
+    p.sm_tabk = off;  off += align16(tabk_b);
+    if (same_levels) {
+        p.sm_tabv = p.sm_tabk;
+    } else {
+        p.sm_tabv = off;  off += align16(tabv_b);
+    }
     p.sm_zf = off;    off += align16(p.ngk * 8 * p.ntk * 32 * 8);
     p.sm_isig = off;  off += align16(Hq * p.ngk * 4);
-    const int uni = std::max({Hq * p.ngk * kGroup * 4, kTile * p.vrow + 16, Hq * p.ngv * kGroup * 4});
-    p.sm_terms = p.sm_vcodes = p.sm_r = off;
-    off += align16(uni);
-    p.sm_vnorm = off; off += align16(kTile * p.ngv * 4);
-    p.sm_p = off;     off += align16(kTile * kMaxHeads * 4);
+    p.sm_p = off;     off += align16(kSpRow * kMaxHeads * 4);
     p.sm_wf = off;    off += align16(p.ngv * 8 * p.ntv * 32 * 8);
+    // one stage: key rows, value rows (+16 bytes: 3-bit pairs may read one word
+    // past a row), key norms, value norms
+    p.off_v = align16(kTile * p.krow);
+    p.off_kn = p.off_v + align16(kTile * p.vrow + 16);
+    p.off_vn = p.off_kn + align16(kTile * 2 * p.ngk);
+    p.stage_bytes = p.off_vn + align16(kTile * 2 * p.ngv);
+    const int fixed = off, limit = 227 * 1024;
+    p.n_stages = kMaxStages;
+    auto union_bytes = [&](int nb) {
+        return align16(std::max({Hq * p.ngk * kGroup * 4, nb * p.stage_bytes, Hq * p.ngv * kGroup * 4}));
+    };
+    while (p.n_stages > 1 && fixed + union_bytes(p.n_stages) > limit) --p.n_stages;
+    // the union region is used in turn by the query terms (setup), the stages
+    // (sub-tiles) and the rotated sums (end)
+    p.sm_terms = p.sm_stage = p.sm_r = off;
+    off += union_bytes(p.n_stages);
     const int smem = off;
 
     const int sms = sm_count();
@@ -555,7 +712,7 @@ int launch_kv_attend(const cq_kv_geom &g, const cq_kv_seq *seqs, int n, const fl
         const int cnt = std::min(kMaxSeqs, n - base);
         long long total_sub = 0;
         for (int i = 0; i < cnt; ++i) total_sub += (seqs[base + i].n_tokens + kTile - 1) / kTile;
-        // sub-tiles per block: enough blocks for about four per SM, at most 128 blocks per sequence
+        // sub-tiles per block: about two blocks per resident slot, at most 128 blocks per sequence
         const long long per_blk = std::max(1LL, (total_sub + 4LL * sms - 1) / (4LL * sms));
         int cta = 0, slots = 0;
         for (int i = 0; i < cnt; ++i) {
@@ -568,8 +725,9 @@ int launch_kv_attend(const cq_kv_geom &g, const cq_kv_seq *seqs, int n, const fl
             d.cap = s.cap;
             d.n = s.n_tokens;
             const int sub = (s.n_tokens + kTile - 1) / kTile;
-            int chunk_sub = (int)std::min<long long>(per_blk, std::max(sub, 1));
-            if ((sub + chunk_sub - 1) / chunk_sub > 128) chunk_sub = (sub + 127) / 128;
+            // as many blocks as per_blk asks for, with equal shares of the sub-tiles
+            const int nch = (int)std::min<long long>(128, std::max(1LL, (sub + per_blk - 1) / per_blk));
+            const int chunk_sub = std::max(1, (sub + nch - 1) / nch);
             d.chunk_tok = chunk_sub * kTile;
             d.n_chunks = sub == 0 ? 1 : (sub + chunk_sub - 1) / chunk_sub;
             d.cta0 = cta;
