@@ -45,6 +45,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTile = 128;      // tokens per sub-tile
 constexpr int kMaxStages = 3;   // sub-tiles whose copies are in flight
+constexpr int kMaxParts = 128;  // blocks sharing one sequence (the merge's factors fit the logits buffer)
 constexpr int kSpRow = kTile + 8;  // logits [head][token]: the stride spreads a warp's heads over banks
 constexpr int kMaxHeads = 16;   // query heads per call
 constexpr int kMaxSeqs = 256;   // sequences per launch (the host splits larger calls)
@@ -55,9 +56,9 @@ struct KvSeqDev {
     const float *q;
     float *o;
     int cap, n;              // rows allocated, rows attended
-    int cta0, n_chunks;      // first block and number of blocks of this sequence
-    int chunk_tok;           // tokens per block (a multiple of kTile)
-    int slot0;               // first workspace slot (n_chunks > 1)
+    int sub0;                // first sub-tile of the sequence in the launch's flat order
+    int part_b0, n_parts;    // first block that works on it, and how many do
+    int slot0;               // first workspace slot (n_parts > 1)
 };
 
 struct KvParams {
@@ -66,6 +67,7 @@ struct KvParams {
     int ntk, ntv;            // n-tiles of 8 columns: key side (hi, lo per head), value side
     float logit_scale;       // scale * log2(e) / sqrt(128): base-2 logits of the unnormalised rotation
     int n_seqs;
+    int total_sub;           // sub-tiles of all sequences; block b takes [b T / G, (b + 1) T / G)
     int vrow;                // staged value-code row stride (bytes)
     int krow;                // staged key-code row stride (bytes)
     int cprk_magic, cprv_magic;  // ceil(65536 / (16-byte pieces per key / value row))
@@ -190,33 +192,14 @@ __device__ __forceinline__ int slot_coord(int unit, int ms_in_unit, int gq, int 
 }
 
 template <int WK, int WV>
-__global__ void __launch_bounds__(kThreads, 2) kv_attend_kernel(const __grid_constant__ KvParams p) {
+__global__ void __launch_bounds__(kThreads, 3) kv_attend_kernel(const __grid_constant__ KvParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ float sM[kMaxHeads], sL[kMaxHeads], sF[kMaxHeads];
     __shared__ int s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, c = lane & 3, r16 = lane & 15;
 
-    int lo = 0, hi = p.n_seqs - 1;  // this block's sequence
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.s[mid].cta0 <= (int)blockIdx.x) lo = mid;
-        else hi = mid - 1;
-    }
-    const int si = lo;
-    // the sequence's fields in registers (indexed parameter reads would repeat in the loops)
-    const uint8_t *const kc = p.s[si].kc;
-    const uint8_t *const vc = p.s[si].vc;
-    const float *const qv = p.s[si].q;
-    float *const ov = p.s[si].o;
-    const int cap = p.s[si].cap, n_tok = p.s[si].n, n_chunks = p.s[si].n_chunks, slot0 = p.s[si].slot0;
-    const int chunk = (int)blockIdx.x - p.s[si].cta0;
     const int Hq = p.Hq, ngk = p.ngk, ngv = p.ngv, ntk = p.ntk, ntv = p.ntv, vrow = p.vrow;
-    if (n_tok == 0) {  // empty softmax: o = 0
-        for (int i = tid; i < Hq * p.dv; i += kThreads) ov[i] = 0.0f;
-        return;
-    }
-    const int t_begin = chunk * p.s[si].chunk_tok, t_end = min(n_tok, t_begin + p.s[si].chunk_tok);
 
     uint32_t *tabk = reinterpret_cast<uint32_t *>(smem + p.sm_tabk);  // pair table [4^W][32], or quad table [256][16] (W = 2)
     uint32_t *tabv = reinterpret_cast<uint32_t *>(smem + p.sm_tabv);
@@ -254,6 +237,33 @@ __global__ void __launch_bounds__(kThreads, 2) kv_attend_kernel(const __grid_con
             }
         }
     }
+    for (int q = blockIdx.x; q < p.n_seqs; q += gridDim.x)  // empty softmax: o = 0
+        if (p.s[q].n == 0)
+            for (int i = tid; i < Hq * p.dv; i += kThreads) p.s[q].o[i] = 0.0f;
+
+    // This block's share of the flat sub-tile order, walked as segments of
+    // consecutive sub-tiles of one sequence.
+    const int G = gridDim.x, T = p.total_sub, bid = blockIdx.x;
+    const int x_end = (int)(((long long)(bid + 1) * T) / G);
+    for (int x = (int)(((long long)bid * T) / G); x < x_end;) {
+    int lo = 0, hi = p.n_seqs - 1;  // the sequence holding sub-tile x
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.s[mid].sub0 <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    const int si = lo;
+    // the sequence's fields in registers (indexed parameter reads would repeat in the loops)
+    const uint8_t *const kc = p.s[si].kc;
+    const uint8_t *const vc = p.s[si].vc;
+    const float *const qv = p.s[si].q;
+    float *const ov = p.s[si].o;
+    const int cap = p.s[si].cap, n_tok = p.s[si].n, n_parts = p.s[si].n_parts, slot0 = p.s[si].slot0;
+    const int sub0 = p.s[si].sub0, sub_end = sub0 + (n_tok + kTile - 1) / kTile;
+    const int seg_end = min(x_end, sub_end), part = bid - p.s[si].part_b0;
+    const int t_begin = (x - sub0) * kTile, t_end = min(n_tok, (seg_end - sub0) * kTile);
+    x = seg_end;
+
     if (tid < kMaxHeads) {
         sM[tid] = -INFINITY;
         sL[tid] = 0.0f;
@@ -573,53 +583,58 @@ __global__ void __launch_bounds__(kThreads, 2) kv_attend_kernel(const __grid_con
         }
     }
     __syncthreads();
-    if (n_chunks == 1) {
+    if (n_parts == 1) {
         finish_heads(p, sr, sL, ov, warp, lane);
-        return;
+        __syncthreads();
+        continue;
     }
-    const int slot = slot0 + chunk;
-    float *part = p.part + (size_t)slot * Hq * ipv;
-    for (int i = tid; i < Hq * ipv; i += kThreads) __stcg(part + i, sr[i]);
+    const int slot = slot0 + part;
+    float *pdst = p.part + (size_t)slot * Hq * ipv;
+    for (int i = tid; i < Hq * ipv; i += kThreads) __stcg(pdst + i, sr[i]);
     if (tid < Hq) {
         __stcg(p.ml + ((size_t)slot * Hq + tid) * 2, sM[tid]);
         __stcg(p.ml + ((size_t)slot * Hq + tid) * 2 + 1, sL[tid]);
     }
     __threadfence();
     __syncthreads();
-    if (tid == 0) s_last = atomicAdd(p.ticket + si, 1u) == (unsigned)(n_chunks - 1);
+    if (tid == 0) s_last = atomicAdd(p.ticket + si, 1u) == (unsigned)(n_parts - 1);
     __syncthreads();
-    if (!s_last) return;
+    if (!s_last) continue;  // (s_last is uniform; the next segment starts after a barrier)
     // ---- F. the last block of the sequence merges the partials ----
     __threadfence();
     const float *ml0 = p.ml + (size_t)slot0 * Hq * 2;
     if (tid < Hq) {
         float mx = -INFINITY;
-        for (int ch = 0; ch < n_chunks; ++ch) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)ch * Hq + tid) * 2));
+        for (int ch = 0; ch < n_parts; ++ch) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)ch * Hq + tid) * 2));
         sM[tid] = mx;
     }
     __syncthreads();
     // per (chunk, head) rescale factors (the logits' buffer holds 16 * kSpRow >= n_chunks * Hq floats)
-    for (int i = tid; i < n_chunks * Hq; i += kThreads) sp[i] = exp2f(__ldcg(ml0 + 2 * (size_t)i) - sM[i % Hq]);
+    for (int i = tid; i < n_parts * Hq; i += kThreads) sp[i] = exp2f(__ldcg(ml0 + 2 * (size_t)i) - sM[i % Hq]);
     __syncthreads();
     if (tid < Hq) {
         float l = 0.0f;
-        for (int ch = 0; ch < n_chunks; ++ch) l = fmaf(__ldcg(ml0 + ((size_t)ch * Hq + tid) * 2 + 1), sp[ch * Hq + tid], l);
+        for (int ch = 0; ch < n_parts; ++ch) l = fmaf(__ldcg(ml0 + ((size_t)ch * Hq + tid) * 2 + 1), sp[ch * Hq + tid], l);
         sL[tid] = l;
     }
     const float *part0 = p.part + (size_t)slot0 * Hq * ipv;
     for (int i = tid; i < Hq * ipv; i += kThreads) {
         const int b = i / ipv;
         float r = 0.0f;
-        for (int ch = 0; ch < n_chunks; ++ch) r = fmaf(__ldcg(part0 + (size_t)ch * Hq * ipv + i), sp[ch * Hq + b], r);
+        for (int ch = 0; ch < n_parts; ++ch) r = fmaf(__ldcg(part0 + (size_t)ch * Hq * ipv + i), sp[ch * Hq + b], r);
         sr[i] = r;
     }
     if (tid == 0) p.ticket[si] = 0u;  // ready for the next launch
     __syncthreads();
     finish_heads(p, sr, sL, ov, warp, lane);
+    __syncthreads();
+    }  // segments
 }
 
+// Resident blocks per SM of one instance at `smem` bytes (sets the
+// shared-memory attribute first), or a negative CQ error.
 template <int WK, int WV>
-int launch_t(const KvParams &p, int grid, int smem, cudaStream_t st) {
+int occupancy_t(int smem) {
     auto k = kv_attend_kernel<WK, WV>;
     static int attr = 0;
     if (smem > attr) {
@@ -627,8 +642,37 @@ int launch_t(const KvParams &p, int grid, int smem, cudaStream_t st) {
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention attribute: %s", cudaGetErrorString(e));
         attr = smem;
     }
-    k<<<grid, kThreads, smem, st>>>(p);
+    int nb = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k, kThreads, smem);
+    if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention occupancy: %s", cudaGetErrorString(e));
+    return std::max(nb, 1);
+}
+
+template <int WK, int WV>
+void launch_t(const KvParams &p, int grid, int smem, cudaStream_t st) {
+    kv_attend_kernel<WK, WV><<<grid, kThreads, smem, st>>>(p);
+}
+
+template <int WK, int WV>
+int dispatch_t(bool occ, const KvParams &p, int grid, int smem, cudaStream_t st) {
+    if (occ) return occupancy_t<WK, WV>(smem);
+    launch_t<WK, WV>(p, grid, smem, st);
     return CQ_OK;
+}
+
+// occ: return the occupancy of the (WK, WV) instance; else launch it.
+int dispatch(int WK, int WV, bool occ, const KvParams &p, int grid, int smem, cudaStream_t st) {
+    switch (WK * 8 + WV) {
+    case 2 * 8 + 2: return dispatch_t<2, 2>(occ, p, grid, smem, st);
+    case 2 * 8 + 3: return dispatch_t<2, 3>(occ, p, grid, smem, st);
+    case 2 * 8 + 4: return dispatch_t<2, 4>(occ, p, grid, smem, st);
+    case 3 * 8 + 2: return dispatch_t<3, 2>(occ, p, grid, smem, st);
+    case 3 * 8 + 3: return dispatch_t<3, 3>(occ, p, grid, smem, st);
+    case 3 * 8 + 4: return dispatch_t<3, 4>(occ, p, grid, smem, st);
+    case 4 * 8 + 2: return dispatch_t<4, 2>(occ, p, grid, smem, st);
+    case 4 * 8 + 3: return dispatch_t<4, 3>(occ, p, grid, smem, st);
+    default: return dispatch_t<4, 4>(occ, p, grid, smem, st);
+    }
 }
 
 int align16(int x) { return (x + 15) & ~15; }
@@ -695,26 +739,48 @@ int launch_kv_attend(const cq_kv_geom &g, const cq_kv_seq *seqs, int n, const fl
     p.off_kn = p.off_v + align16(kTile * p.vrow + 16);
     p.off_vn = p.off_kn + align16(kTile * 2 * p.ngk);
     p.stage_bytes = p.off_vn + align16(kTile * 2 * p.ngv);
-    const int fixed = off, limit = 227 * 1024;
-    p.n_stages = kMaxStages;
+    const int fixed = off;
     auto union_bytes = [&](int nb) {
         return align16(std::max({Hq * p.ngk * kGroup * 4, nb * p.stage_bytes, Hq * p.ngv * kGroup * 4}));
     };
-    while (p.n_stages > 1 && fixed + union_bytes(p.n_stages) > limit) --p.n_stages;
+    // the most stages that keep three blocks on an SM (228 KB, 1 KB reserved
+    // per block); failing that, the most that fit one block
+    const int per3 = 228 * 1024 / 3 - 1024, limit = 227 * 1024;
+    p.n_stages = kMaxStages;
+    while (p.n_stages > 1 && fixed + union_bytes(p.n_stages) > per3) --p.n_stages;
+    if (fixed + union_bytes(p.n_stages) > per3) {
+        p.n_stages = kMaxStages;
+        while (p.n_stages > 1 && fixed + union_bytes(p.n_stages) > limit) --p.n_stages;
+    }
     // the union region is used in turn by the query terms (setup), the stages
     // (sub-tiles) and the rotated sums (end)
     p.sm_terms = p.sm_stage = p.sm_r = off;
     off += union_bytes(p.n_stages);
     const int smem = off;
 
-    const int sms = sm_count();
+    const int per_sm = dispatch(WK, WV, true, p, 0, smem, st);
+    if (per_sm < 0) return per_sm;
+    const long long slots_gpu = (long long)per_sm * sm_count();
     for (int base = 0; base < n; base += kMaxSeqs) {
         const int cnt = std::min(kMaxSeqs, n - base);
-        long long total_sub = 0;
-        for (int i = 0; i < cnt; ++i) total_sub += (seqs[base + i].n_tokens + kTile - 1) / kTile;
-        // sub-tiles per block: about two blocks per resident slot, at most 128 blocks per sequence
-        const long long per_blk = std::max(1LL, (total_sub + 4LL * sms - 1) / (4LL * sms));
-        int cta = 0, slots = 0;
+        long long total = 0;
+        for (int i = 0; i < cnt; ++i) total += (seqs[base + i].n_tokens + kTile - 1) / kTile;
+        if (total > (1LL << 30)) return set_error(CQ_ERR_SHAPE, "too many cached tokens in one call");
+        // one block per resident slot, each an equal run of the flat sub-tile order
+        const int T = (int)total;
+        int G = (int)std::max(1LL, std::min<long long>(slots_gpu, total));
+        auto block_of = [&](long long x) { return (int)(((x + 1) * G - 1) / T); };  // block holding sub-tile x
+        for (;;) {  // at most kMaxParts blocks per sequence (the merge keeps one factor per part and head)
+            int worst = 0, s0 = 0;
+            for (int i = 0; i < cnt; ++i) {
+                const int ns = (seqs[base + i].n_tokens + kTile - 1) / kTile;
+                if (ns) worst = std::max(worst, block_of(s0 + ns - 1) - block_of(s0) + 1);
+                s0 += ns;
+            }
+            if (worst <= kMaxParts || G == 1) break;
+            G = std::max(1, G * 3 / 4);
+        }
+        int slots = 0, sub = 0;
         for (int i = 0; i < cnt; ++i) {
             const cq_kv_seq &s = seqs[base + i];
             KvSeqDev &d = p.s[i];
@@ -724,18 +790,16 @@ int launch_kv_attend(const cq_kv_geom &g, const cq_kv_seq *seqs, int n, const fl
             d.o = s.o;
             d.cap = s.cap;
             d.n = s.n_tokens;
-            const int sub = (s.n_tokens + kTile - 1) / kTile;
-            // as many blocks as per_blk asks for, with equal shares of the sub-tiles
-            const int nch = (int)std::min<long long>(128, std::max(1LL, (sub + per_blk - 1) / per_blk));
-            const int chunk_sub = std::max(1, (sub + nch - 1) / nch);
-            d.chunk_tok = chunk_sub * kTile;
-            d.n_chunks = sub == 0 ? 1 : (sub + chunk_sub - 1) / chunk_sub;
-            d.cta0 = cta;
-            cta += d.n_chunks;
+            const int ns = (s.n_tokens + kTile - 1) / kTile;
+            d.sub0 = sub;
+            d.part_b0 = ns ? block_of(sub) : 0;
+            d.n_parts = ns ? block_of(sub + ns - 1) - d.part_b0 + 1 : 0;
             d.slot0 = slots;
-            if (d.n_chunks > 1) slots += d.n_chunks;
+            if (d.n_parts > 1) slots += d.n_parts;
+            sub += ns;
         }
         p.n_seqs = cnt;
+        p.total_sub = T;
         p.part = nullptr;
         p.ml = nullptr;
         p.ticket = nullptr;
@@ -751,19 +815,7 @@ int launch_kv_attend(const cq_kv_geom &g, const cq_kv_seq *seqs, int n, const fl
             const cudaError_t e = cudaMemsetAsync(p.ticket, 0, (size_t)cnt * 4, st);
             if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention tickets: %s", cudaGetErrorString(e));
         }
-        int rc = CQ_OK;
-        switch (WK * 8 + WV) {
-        case 2 * 8 + 2: rc = launch_t<2, 2>(p, cta, smem, st); break;
-        case 2 * 8 + 3: rc = launch_t<2, 3>(p, cta, smem, st); break;
-        case 2 * 8 + 4: rc = launch_t<2, 4>(p, cta, smem, st); break;
-        case 3 * 8 + 2: rc = launch_t<3, 2>(p, cta, smem, st); break;
-        case 3 * 8 + 3: rc = launch_t<3, 3>(p, cta, smem, st); break;
-        case 3 * 8 + 4: rc = launch_t<3, 4>(p, cta, smem, st); break;
-        case 4 * 8 + 2: rc = launch_t<4, 2>(p, cta, smem, st); break;
-        case 4 * 8 + 3: rc = launch_t<4, 3>(p, cta, smem, st); break;
-        default: rc = launch_t<4, 4>(p, cta, smem, st); break;
-        }
-        if (rc) return rc;
+        dispatch(WK, WV, false, p, G, smem, st);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention launch: %s", cudaGetErrorString(e));
     }
