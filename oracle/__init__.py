@@ -124,7 +124,9 @@ def lloyd_max_samples(x: np.ndarray, L: int, iters: int) -> np.ndarray:
 def analytic_codebook(bits: int, group: int = 128) -> np.ndarray:
     """Oracle-side codebook: Lloyd-Max on N(0,1) divided by sqrt(group), as
     fp32; ternary uses the constant 1.2240064 printed in the needle.js
-    tutorial ("Shared codebooks")."""
+    tutorial ("Shared codebooks"); binary (bits=1) is the two-level
+    Lloyd-Max quantiser, whose centroids are closed-form ("The .cact format",
+    "Cactus Quants": binary packs eight codes per byte)."""
     if bits == 5:
         c = 1.2240064 / np.sqrt(group)
         return np.array([-c, 0.0, c], dtype=np.float32)

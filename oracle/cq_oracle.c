@@ -207,6 +207,7 @@ float cqo_f16_to_f32(uint16_t h)
 int cqo_levels(int bits)
 {
     switch (bits) {
+    case 1: return 2; /* binary: eight codes per byte ([CF] "Cactus Quants") */
     case 2: return 4;
     case 3: return 8;
     case 4: return 16;
@@ -218,6 +219,7 @@ int cqo_levels(int bits)
 int cqo_width(int bits)
 {
     switch (bits) {
+    case 1: return 1;
     case 2: return 2;
     case 3: return 3;
     case 4: return 4;

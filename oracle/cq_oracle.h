@@ -60,7 +60,8 @@ uint16_t cqo_f32_to_f16(float f);
 float cqo_f16_to_f32(uint16_t h);
 
 /* Number of levels and packed code width for a record `bits` value
- * (2, 3, 4; 5 = ternary marker with 3 levels in 2-bit crumbs). */
+ * (1 = binary, two levels, one bit per code; 2, 3, 4; 5 = ternary marker
+ * with 3 levels in 2-bit crumbs). */
 int cqo_levels(int bits);
 int cqo_width(int bits);
 

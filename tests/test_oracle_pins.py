@@ -565,3 +565,108 @@ def test_kv_attend_ignores_rows_past_n_tokens_and_single_row_is_exact():
     for b in range(4):
         h = b // 2
         assert np.allclose(o1[b], row[h * dv:(h + 1) * dv], rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------ binary codes and group 64
+# [CF] "Cactus Quants": binary weights pack eight per byte and have
+# closed-form centroids; OpenNeedle docs/reference.md tests group 64 and 128.
+
+def test_binary_centroids_closed_form():
+    """The two-level Lloyd-Max quantiser of N(0,1) has centroids
+    +-E|X| = +-sqrt(2/pi) (the conditional mean of a half-normal)."""
+    c, _ = O.lloyd_max_normal(2)
+    assert np.allclose(c, [-math.sqrt(2 / math.pi), math.sqrt(2 / math.pi)], rtol=0, atol=1e-12)
+    for g in (64, 128):
+        cb = O.analytic_codebook(1, g)
+        assert np.allclose(cb, np.float32(np.array([-1, 1]) * math.sqrt(2 / math.pi) / math.sqrt(g)), rtol=0, atol=0)
+
+
+def _brute_encode(W, group, cb):
+    """Brute force with scipy's Hadamard matrix: codes of the nearest level to
+    u = H w / |w| per group (ties to the smaller index), and fp32 norms."""
+    from scipy.linalg import hadamard as sh
+    H = sh(group).astype(np.float64) / math.sqrt(group)
+    out, n_in = W.shape
+    ip = O.in_padded(n_in, group)
+    Wp = np.zeros((out, ip)); Wp[:, :n_in] = W
+    codes = np.zeros((out, ip), dtype=np.int64); norms = np.zeros((out, ip // group))
+    for o in range(out):
+        for g in range(ip // group):
+            w = Wp[o, g * group:(g + 1) * group]
+            n = np.float32(np.sqrt(np.sum(w * w)))
+            u = (H @ w) / max(float(n), 1e-12)
+            d = np.abs(u[:, None] - cb.astype(np.float64)[None, :])
+            codes[o, g * group:(g + 1) * group] = np.argmin(d, axis=1)
+            norms[o, g] = n
+    return codes, norms
+
+
+@pytest.mark.parametrize("bits,group", [(1, 128), (1, 64), (2, 64), (3, 64), (4, 64)])
+def test_encode_matches_brute_force(bits, group):
+    """Codes and norms for binary codes and 64-wide groups against a direct
+    computation with an independently built Hadamard matrix."""
+    rng = np.random.RandomState(40 + bits + group)
+    W = (rng.randn(3, 200) * 0.02).astype(np.float32)
+    cb = O.analytic_codebook(bits, group)
+    blob, flags, _ = O.encode(W, bits, cb, group)
+    codes, norms = O.unpack(blob, 3, 200, bits, group)
+    bc, bn = _brute_encode(W, group, cb)
+    assert np.array_equal(codes[flags == 0], bc[flags == 0])
+    assert np.array_equal(O.f16_bits_to_f32(norms).reshape(bn.shape), bn.astype(np.float16).astype(np.float32))
+
+
+def test_binary_packing_eight_codes_per_byte():
+    """One continuous LSB-first stream per row ([CF] "Cactus Quants"):
+    binary code k of a row is bit k % 8 of byte k // 8; a row of 256 codes
+    takes 32 bytes, then the fp16 norms follow."""
+    rng = np.random.RandomState(44)
+    W = (rng.randn(2, 256) * 0.02).astype(np.float32)
+    cb = O.analytic_codebook(1)
+    blob, _, _ = O.encode(W, 1, cb)
+    assert blob.size == O.packed_bytes(2, 256, 128, 1) == 2 * 32 + 2 * 2 * 2
+    codes, _ = O.unpack(blob, 2, 256, 1)
+    assert np.array_equal(blob[:64], np.packbits(codes.astype(np.uint8).reshape(-1), bitorder="little"))
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_binary_dequant_closed_form(group):
+    """All codes 1 with norm n give n * c * (1,...,1) H = n * c * sqrt(group) * e_0
+    in every group ([NJ] "Reconstructing one group")."""
+    cb = O.analytic_codebook(1, group)
+    nb = O.packed_bytes(1, 2 * group, group, 1)
+    blob = np.zeros(nb, dtype=np.uint8)
+    blob[:2 * group // 8] = 0xFF
+    blob[2 * group // 8:] = np.array([0x4000, 0x3C00], dtype="<u2").view(np.uint8)  # n = 2, 1
+    What = O.dequant(blob, 1, 2 * group, 1, cb, group)
+    for g, n in ((0, 2.0), (1, 1.0)):
+        seg = What[0, g * group:(g + 1) * group]
+        assert abs(seg[0] - n * float(cb[1]) * math.sqrt(group)) < 1e-12
+        assert np.allclose(seg[1:], 0.0, atol=1e-14)
+
+
+def test_binary_reconstruction_error_matches_distortion():
+    """The 1-bit Lloyd-Max quantiser of N(0,1) has distortion 1 - 2/pi; the
+    relative squared reconstruction error of Gaussian groups approaches it
+    (at group 64 and 128)."""
+    rng = np.random.RandomState(45)
+    W = (rng.randn(64, 512) * 0.02).astype(np.float32)
+    for group in (64, 128):
+        cb = O.analytic_codebook(1, group)
+        blob, _, _ = O.encode(W, 1, cb, group)
+        What = O.dequant(blob, 64, 512, 1, cb, group)
+        rel = np.sum((What - W) ** 2) / np.sum(W.astype(np.float64) ** 2)
+        assert abs(rel - (1 - 2 / math.pi)) < 0.06 * (1 - 2 / math.pi)
+
+
+@pytest.mark.parametrize("bits,group", [(1, 128), (1, 64), (2, 64), (4, 64), (5, 64)])
+def test_rotated_identity_other_geometries(bits, group):
+    """The rotated route n <c[q], H x_g> equals the dense product for binary
+    codes and 64-wide groups."""
+    rng = np.random.RandomState(46 + bits + group)
+    W = (rng.randn(5, 200) * 0.02).astype(np.float32)
+    X = rng.randn(2, 200)
+    cb = O.analytic_codebook(bits, group)
+    blob, _, _ = O.encode(W, bits, cb, group)
+    Y1, Bd = O.matmul(O.dequant(blob, 5, 200, bits, cb, group), X)
+    Y2 = O.matmul_rotated(blob, 5, 200, bits, cb, X, group)
+    assert np.max(np.abs(Y1 - Y2) / Bd) < 1e-12
