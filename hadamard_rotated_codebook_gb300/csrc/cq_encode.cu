@@ -304,6 +304,98 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
     }
 }
 
+// ------------------------------------------- group 64 and binary codes --
+// One warp per 128 positions: a group of 128, or two groups of 64 (lanes
+// 0-15 and 16-31, whose transforms stop before the stage that would mix
+// them). Lane l holds coordinates 4l..4l+3. Same steps as encode_kernel:
+// fp32 sum of squares in a tree (fp64 recount near an fp16 rounding
+// boundary), FWHT, u = r / n, threshold search, LSB-first packing.
+template <int G, int BITS>
+__global__ void __launch_bounds__(256) encode_warp_kernel(const __grid_constant__ EncodeParams p) {
+    constexpr int L = BITS == 5 ? 3 : (1 << BITS);
+    constexpr int W = BITS == 5 ? 2 : BITS;
+    constexpr int HALF = G == 128 ? 32 : 16;  // lanes per group
+    constexpr int PER = 128 / G;              // groups per warp task
+    constexpr int NW = G * W / 32;            // code words per group
+    __shared__ float s_thr[16];
+    __shared__ uint32_t s_words[8][PER][NW + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < L - 1) s_thr[tid] = decision_threshold(p.cb[tid], p.cb[tid + 1]);
+    __syncthreads();
+    float T[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) T[j] = j < L - 1 ? s_thr[j] : 0.0f;
+    const int sub = lane / HALF, pos = 4 * (lane % HALF);  // group of the task, first coordinate
+    const long long n_tasks = (p.n_groups + PER - 1) / PER;
+    for (long long task = (long long)blockIdx.x * 8 + warp; task < n_tasks; task += (long long)gridDim.x * 8) {
+        const long long Gi = task * PER + sub;
+        const bool live = Gi < p.n_groups;
+        const long long o = live ? Gi / p.ng : 0;
+        const int col0 = (int)(Gi - o * p.ng) * G + pos;
+        float x[4], w0[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            w0[e] = live && col0 + e < p.in ? __ldcs(p.W + o * p.in + col0 + e) : 0.0f;
+            x[e] = w0[e];
+        }
+        // sum of squares, a tree in fp32
+        float sq = __fadd_rn(__fadd_rn(__fmul_rn(x[0], x[0]), __fmul_rn(x[1], x[1])),
+                             __fadd_rn(__fmul_rn(x[2], x[2]), __fmul_rn(x[3], x[3])));
+#pragma unroll
+        for (int m = 1; m < HALF; m <<= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, m));
+        // transform: coordinate bits 0, 1 in registers, bits 2.. across lanes
+        const float a0 = __fadd_rn(x[0], x[1]), a1 = __fsub_rn(x[0], x[1]);
+        const float a2 = __fadd_rn(x[2], x[3]), a3 = __fsub_rn(x[2], x[3]);
+        x[0] = __fadd_rn(a0, a2);
+        x[1] = __fadd_rn(a1, a3);
+        x[2] = __fsub_rn(a0, a2);
+        x[3] = __fsub_rn(a1, a3);
+#pragma unroll
+        for (int m = 1; m < HALF; m <<= 1)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float v = __shfl_xor_sync(0xffffffffu, x[e], m);
+                x[e] = (lane & m) ? __fsub_rn(v, x[e]) : __fadd_rn(x[e], v);
+            }
+        // fp32 norm; exact fp64 recount when its fp16 rounding is in doubt
+        float n32 = __fsqrt_rn(sq);
+        bool sure = sq >= 1e-30f && sq <= 1e30f;
+        if (sure) {
+            const __half lo = __float2half_rn(__fmul_rn(n32, 1.0f - 5e-7f));
+            const __half hi = __float2half_rn(__fmul_rn(n32, 1.0f + 5e-7f));
+            sure = __half_as_ushort(lo) == __half_as_ushort(hi);
+        }
+        if (__any_sync(0xffffffffu, !sure)) {
+            double d = 0.0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d = __fma_rn((double)w0[e], (double)w0[e], d);
+#pragma unroll
+            for (int m = 1; m < HALF; m <<= 1) d += __shfl_xor_sync(0xffffffffu, d, m);
+            if (!sure) n32 = __double2float_rn(__dsqrt_rn(d));
+        }
+        const float sc = __fdiv_rn(G == 128 ? 0.08838834764831845f : 0.125f, fmaxf(n32, 1e-12f));
+        uint32_t bits = 0;  // my four codes, 4W bits
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            int q = level_index<L>(__fmul_rn(x[e], sc), T);
+            if (BITS == 5) q = (q - 1) & 3;  // ternary crumb
+            bits |= (uint32_t)q << (W * e);
+        }
+        // pack the group's LSB-first stream in shared memory, then store it
+        uint32_t *sw = s_words[warp][sub];
+        if (lane % HALF < NW) sw[lane % HALF] = 0u;
+        __syncwarp();
+        const int b0 = W * pos, wi = b0 >> 5, sh = b0 & 31;
+        atomicOr(sw + wi, bits << sh);
+        if (sh + 4 * W > 32) atomicOr(sw + wi + 1, bits >> (32 - sh));
+        __syncwarp();
+        if (live && lane % HALF < NW)
+            reinterpret_cast<uint32_t *>(p.codes + Gi * (G * W / 8))[lane % HALF] = sw[lane % HALF];
+        if (live && lane % HALF == 0) p.norms[Gi] = __float2half_rn(n32);
+        __syncwarp();
+    }
+}
+
 // ----------------------------------------------------- activation quant --
 // One CTA per token: s = absmax/127 (IEEE division), q = rint(x/s) clamped.
 __global__ void act_quant_kernel(const float *__restrict__ X, int M, int in, int8_t *__restrict__ Q,
@@ -364,18 +456,25 @@ int sm_count() {
     return n;
 }
 
-int launch_encode(const float *W, int out, int in, int bits, const float *cb, uint8_t *blob,
+int launch_encode(const float *W, int out, int in, int group, int bits, const float *cb, uint8_t *blob,
                   void *stream) {
-    const size_t rowBytes = (size_t)in_padded(in) * width_of(bits) / 8;
-    return launch_encode_rows(W, out, in, bits, cb, blob, blob + (size_t)out * rowBytes, stream);
+    const size_t rowBytes = (size_t)in_padded(in, group) * width_of(bits) / 8;
+    return launch_encode_rows(W, out, in, group, bits, cb, blob, blob + (size_t)out * rowBytes, stream);
 }
 
-int launch_encode_rows(const float *W, int out, int in, int bits, const float *cb, uint8_t *codes,
+template <int G, int BITS>
+void launch_encode_warp(const EncodeParams &p, cudaStream_t st) {
+    const long long tasks = (p.n_groups + 128 / G - 1) / (128 / G);
+    const long long grid = std::min<long long>((tasks + 7) / 8, (long long)sm_count() * 8);
+    encode_warp_kernel<G, BITS><<<(unsigned)grid, 256, 0, st>>>(p);
+}
+
+int launch_encode_rows(const float *W, int out, int in, int group, int bits, const float *cb, uint8_t *codes,
                        uint8_t *nb, void *stream) {
     EncodeParams p;
     p.W = W;
     p.in = in;
-    p.ng = in_padded(in) / kGroup;
+    p.ng = in_padded(in, group) / group;
     p.n_groups = (long long)out * p.ng;
     p.codes = codes;
     if ((reinterpret_cast<uintptr_t>(codes) & 15) || (reinterpret_cast<uintptr_t>(nb) & 1))
@@ -384,13 +483,25 @@ int launch_encode_rows(const float *W, int out, int in, int bits, const float *c
     p.status = device_status_ptr();
     const int L = levels_of(bits);
     for (int j = 0; j < kMaxLevels; ++j) p.cb[j] = j < L ? cb[j] : 0.0f;
-    const bool aligned = (in % kGroup == 0) && !(reinterpret_cast<uintptr_t>(W) & 15);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    switch (bits) {
-    case 2: aligned ? launch_encode_t<2, true>(p, st) : launch_encode_t<2, false>(p, st); break;
-    case 3: aligned ? launch_encode_t<3, true>(p, st) : launch_encode_t<3, false>(p, st); break;
-    case 4: aligned ? launch_encode_t<4, true>(p, st) : launch_encode_t<4, false>(p, st); break;
-    case 5: aligned ? launch_encode_t<5, true>(p, st) : launch_encode_t<5, false>(p, st); break;
+    if (group == kGroup64) {
+        switch (bits) {
+        case 1: launch_encode_warp<64, 1>(p, st); break;
+        case 2: launch_encode_warp<64, 2>(p, st); break;
+        case 3: launch_encode_warp<64, 3>(p, st); break;
+        case 4: launch_encode_warp<64, 4>(p, st); break;
+        case 5: launch_encode_warp<64, 5>(p, st); break;
+        }
+    } else if (bits == 1) {
+        launch_encode_warp<128, 1>(p, st);
+    } else {
+        const bool aligned = (in % kGroup == 0) && !(reinterpret_cast<uintptr_t>(W) & 15);
+        switch (bits) {
+        case 2: aligned ? launch_encode_t<2, true>(p, st) : launch_encode_t<2, false>(p, st); break;
+        case 3: aligned ? launch_encode_t<3, true>(p, st) : launch_encode_t<3, false>(p, st); break;
+        case 4: aligned ? launch_encode_t<4, true>(p, st) : launch_encode_t<4, false>(p, st); break;
+        case 5: aligned ? launch_encode_t<5, true>(p, st) : launch_encode_t<5, false>(p, st); break;
+        }
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "encode launch: %s", cudaGetErrorString(e));

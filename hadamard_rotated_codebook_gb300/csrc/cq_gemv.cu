@@ -39,6 +39,7 @@ struct GemvMat {
     const float *xs;
     float *y;
     int out, in, ng, bits, xdt, B, lut, kcg, nchunks, row_tiles, items_before;
+    int group;  // 128 or 64
 };
 
 struct GemvParams {
@@ -48,28 +49,32 @@ struct GemvParams {
 };
 
 // Rotates activation groups [gbeg, gend) of every batch row into zs:
-// zs[(b*kcg + (g-gbeg))*kZPad + k] = (H x_{b,g})[k].
+// zs[(b*kcg + (g-gbeg))*kZPad + k] = (H x_{b,g})[k]. A warp task covers 128
+// positions: one group of 128, or two groups of 64 (lanes 0-15 and 16-31,
+// whose transforms stop before the stage that would mix the two halves).
 __device__ void rotate_chunk(const GemvMat &M, int gbeg, int gend, int kcg, float *zs) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int ngc = gend - gbeg;
-    for (int task = warp; task < M.B * ngc; task += kGemvThreads / 32) {
-        const int b = task / ngc, gl = task % ngc, g = gbeg + gl;
+    const int ngc = gend - gbeg, per = kGroup / M.group, nspan = (ngc + per - 1) / per;
+    const int half = M.group == kGroup ? 32 : 16;  // lanes per group
+    for (int task = warp; task < M.B * nspan; task += kGemvThreads / 32) {
+        const int b = task / nspan, gl = (task % nspan) * per + lane / half, g = gbeg + gl;
+        const bool live = gl < ngc;
         float v[4];
-        float scale = kInvSqrt128;
+        float scale = M.group == kGroup ? kInvSqrt128 : 0.125f;
         if (M.xdt == CQ_X_I8) {
             const int8_t *xq = static_cast<const int8_t *>(M.x) + (size_t)b * M.in;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int col = g * kGroup + 4 * lane + i;
-                v[i] = col < M.in ? (float)xq[col] : 0.0f;
+                const int col = g * M.group + (4 * lane + i) % M.group;
+                v[i] = live && col < M.in ? (float)xq[col] : 0.0f;
             }
-            scale = __fmul_rn(M.xs[b], kInvSqrt128);
+            scale = __fmul_rn(M.xs[b], scale);
         } else {
             const float *xf = static_cast<const float *>(M.x) + (size_t)b * M.in;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int col = g * kGroup + 4 * lane + i;
-                v[i] = col < M.in ? xf[col] : 0.0f;
+                const int col = g * M.group + (4 * lane + i) % M.group;
+                v[i] = live && col < M.in ? xf[col] : 0.0f;
             }
         }
         // coordinate bits 0,1 in registers
@@ -78,22 +83,25 @@ __device__ void rotate_chunk(const GemvMat &M, int gbeg, int gend, int kcg, floa
         v[1] = a1 + a3;
         v[2] = a0 - a2;
         v[3] = a1 - a3;
-        // coordinate bits 2..6 across lanes
+        // coordinate bits 2..6 across lanes (bit 6 only within a group of 128)
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1)
+            if (m < half)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
-                v[i] = (lane & m) ? o - v[i] : v[i] + o;
-            }
-        float *dst = zs + (size_t)(b * kcg + gl) * kZPad + 4 * lane;
+                for (int i = 0; i < 4; ++i) {
+                    const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+                    v[i] = (lane & m) ? o - v[i] : v[i] + o;
+                }
+        if (live) {
+            float *dst = zs + (size_t)(b * kcg + gl) * kZPad + (4 * lane) % M.group;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = v[i] * scale;
+            for (int i = 0; i < 4; ++i) dst[i] = v[i] * scale;
+        }
     }
 }
 
 template <int W>
-__device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[4 * W], int k) {
+__device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[4 * W], int k) {  // code k of a group
     const int bit = k * W, word = bit >> 5, off = bit & 31;
     uint32_t v = w[word] >> off;
     if (off + W > 32) v |= w[word + 1] << (32 - off);
@@ -127,28 +135,41 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
         rotate_chunk(M, gbeg, gend, M.kcg, zs);
         __syncthreads();
 
-        const int ngc = gend - gbeg;
-        const size_t rowBytes = (size_t)M.ng * 16 * W;
+        const int ngc = gend - gbeg, G = M.group;
+        const size_t grpBytes = (size_t)G * W / 8, rowBytes = (size_t)M.ng * grpBytes;
         for (int pr = threadIdx.x; pr < kRowsPerItem * ngc; pr += kGemvThreads) {
             const int r = pr / ngc, gl = pr % ngc, o = row0 + r;
             if (o >= M.out) continue;
             const int g = gbeg + gl;
             uint32_t w[4 * W];
-            const uint4 *src = reinterpret_cast<const uint4 *>(M.codes + (size_t)o * rowBytes + (size_t)g * 16 * W);
+            const uint8_t *gp = M.codes + (size_t)o * rowBytes + (size_t)g * grpBytes;
+            if (G == kGroup) {  // 16 W bytes: W 16-byte loads
+                const uint4 *src = reinterpret_cast<const uint4 *>(gp);
 #pragma unroll
-            for (int i = 0; i < W; ++i) {
-                const uint4 t = __ldg(src + i);
-                w[4 * i] = t.x;
-                w[4 * i + 1] = t.y;
-                w[4 * i + 2] = t.z;
-                w[4 * i + 3] = t.w;
+                for (int i = 0; i < W; ++i) {
+                    const uint4 t = __ldg(src + i);
+                    w[4 * i] = t.x;
+                    w[4 * i + 1] = t.y;
+                    w[4 * i + 2] = t.z;
+                    w[4 * i + 3] = t.w;
+                }
+            } else {  // 8 W bytes: W 8-byte loads
+                const uint2 *src = reinterpret_cast<const uint2 *>(gp);
+#pragma unroll
+                for (int i = 0; i < W; ++i) {
+                    const uint2 t = __ldg(src + i);
+                    w[2 * i] = t.x;
+                    w[2 * i + 1] = t.y;
+                }
+#pragma unroll
+                for (int i = 2 * W; i < 4 * W; ++i) w[i] = 0u;
             }
             float acc[BMAX];
 #pragma unroll
             for (int b = 0; b < BMAX; ++b) acc[b] = 0.0f;
             const float *z = zs + (size_t)gl * kZPad;
 #pragma unroll 8
-            for (int k = 0; k < kGroup; ++k) {
+            for (int k = 0; k < G; ++k) {
                 const float lv = lut_s[code_at<W>(w, k)];
 #pragma unroll
                 for (int b = 0; b < BMAX; ++b)
@@ -208,7 +229,7 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
     }
     // One launch per code width present; each launch walks all descriptors of
     // its width (matrices of other widths contribute no items).
-    for (int W = 2; W <= 4; ++W) {
+    for (int W = 1; W <= 4; ++W) {
         static GemvParams p;  // large: keep off the stack
         p.n = 0;
         int bmax = 0, nlut = 0, items = 0, zfloats = 0;
@@ -219,7 +240,8 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
                 continue;
             }
             GemvMat &M = p.m[p.n];
-            const int ip = in_padded(d[i].in);
+            const int ip = in_padded(d[i].in, d[i].group);
+            M.group = d[i].group;
             M.codes = d[i].blob;
             M.norms = reinterpret_cast<const __half *>(d[i].blob + (size_t)d[i].out * ip * W / 8);
             M.x = d[i].x;
@@ -227,7 +249,7 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
             M.y = d[i].y;
             M.out = d[i].out;
             M.in = d[i].in;
-            M.ng = ip / kGroup;
+            M.ng = ip / d[i].group;
             M.bits = d[i].bits;
             M.xdt = d[i].x_dtype;
             M.B = d[i].B;
@@ -268,6 +290,7 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
         const size_t smem = sizeof(float) * (zfloats + kRowsPerItem * 16);
         const int grid = std::min(items, sm_count() * 8);
         switch (W) {
+        case 1: launch_b<1>(bmax, p, smem, grid, st); break;
         case 2: launch_b<2>(bmax, p, smem, grid, st); break;
         case 3: launch_b<3>(bmax, p, smem, grid, st); break;
         case 4: launch_b<4>(bmax, p, smem, grid, st); break;

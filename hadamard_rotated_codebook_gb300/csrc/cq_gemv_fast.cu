@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
 
 bool gemv_fast_eligible(const cq_gemv_desc &d) {
     const int ng = in_padded(d.in) / kGroup;
-    if (d.in <= 0 || d.out <= 0) return false;
+    if (d.in <= 0 || d.out <= 0 || d.group != kGroup) return false;
     const int W = width_of(d.bits);
     return (W == 2 || W == 4) && d.B <= kMaxFastB && ng <= kMaxFastNg;
 }

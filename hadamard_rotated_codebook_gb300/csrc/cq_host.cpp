@@ -107,7 +107,7 @@ int cq_code_width(int bits) { return width_of(bits); }
 int cq_codebook_init(int bits, int group, float *levels, size_t cap, size_t *n_levels) {
     clear_error();
     const int L = levels_of(bits);
-    if (L < 0) return set_error(CQ_ERR_ARG, "bits must be 2, 3, 4 or 5, got %d", bits);
+    if (L < 0) return set_error(CQ_ERR_ARG, "bits must be 1, 2, 3, 4 or 5, got %d", bits);
     if (group < 8 || !is_pow2((uint64_t)group))
         return set_error(CQ_ERR_ARG, "group must be a power of two >= 8, got %d", group);
     if (n_levels) *n_levels = (size_t)L;
@@ -140,12 +140,17 @@ uint64_t cq_packed_bytes(int out, int in, int group, int bits) {
 
 // ------------------------------------------------------------ device calls --
 
-static int check_matrix(int out, int in, int group, int bits) {
-    if (levels_of(bits) < 0) return set_error(CQ_ERR_ARG, "bits must be 2, 3, 4 or 5, got %d", bits);
-    if (group != kGroup)
-        return set_error(CQ_ERR_SHAPE, "the kernels support group = 128 only, got %d", group);
+// wide: the entry point also takes group 64 and binary codes (encode, GEMV,
+// row gather); the GEMM and the KV cache take group 128 and 2..5 bits.
+static int check_matrix(int out, int in, int group, int bits, bool wide = true) {
+    if (levels_of(bits) < 0) return set_error(CQ_ERR_ARG, "bits must be 1, 2, 3, 4 or 5, got %d", bits);
+    if (wide && group != kGroup && group != kGroup64)
+        return set_error(CQ_ERR_SHAPE, "this entry point supports group = 64 or 128, got %d", group);
+    if (!wide && group != kGroup)
+        return set_error(CQ_ERR_SHAPE, "this entry point supports group = 128 only, got %d", group);
+    if (!wide && bits == 1) return set_error(CQ_ERR_SHAPE, "this entry point does not take binary codes");
     if (out < 0 || in < 0) return set_error(CQ_ERR_SHAPE, "negative size out=%d in=%d", out, in);
-    if ((int64_t)out * in_padded(in) > ((int64_t)1 << 40))
+    if ((int64_t)out * in_padded(in, group) > ((int64_t)1 << 40))
         return set_error(CQ_ERR_SHAPE, "matrix too large");
     return CQ_OK;
 }
@@ -158,7 +163,7 @@ int cq_encode(const float *W, int out, int in, int group, int bits, const float 
     if ((st = check_codebook(codebook, bits))) return st;
     if (out == 0 || in == 0) return CQ_OK;  // empty matrix: nothing to write
     if (!W || !blob) return set_error(CQ_ERR_ARG, "W and blob must be non-null");
-    return launch_encode(W, out, in, bits, codebook, blob, stream);
+    return launch_encode(W, out, in, group, bits, codebook, blob, stream);
 }
 
 int cq_act_quant_int8(const float *X, int M, int in, int8_t *Xq, float *s, void *stream) {
@@ -252,13 +257,13 @@ int cq_gather_rows(const uint8_t *blob, int out, int in, int group, int bits, co
     if (reinterpret_cast<uintptr_t>(blob) & 15) return set_error(CQ_ERR_ARG, "blob must be 16-byte aligned");
     float lv[16];
     level_table(bits, codebook, lv);
-    return launch_gather_rows(blob, out, in, bits, lv, idx, n, dst, stream);
+    return launch_gather_rows(blob, out, in, group, bits, lv, idx, n, dst, stream);
 }
 
 int cq_kv_write(uint8_t *cache, int cap, int in, int bits, const float *codebook, const float *rows, int t0, int n,
                 void *stream) {
     clear_error();
-    int st = check_matrix(cap, in, kGroup, bits);
+    int st = check_matrix(cap, in, kGroup, bits, false);
     if (st) return st;
     if ((st = check_codebook(codebook, bits))) return st;
     if (n < 0 || t0 < 0 || (long long)t0 + n > cap)
@@ -269,7 +274,7 @@ int cq_kv_write(uint8_t *cache, int cap, int in, int bits, const float *codebook
     const size_t rb = (size_t)in_padded(in) * width_of(bits) / 8, ng = in_padded(in) / kGroup;
     uint8_t *codes = cache + (size_t)t0 * rb;
     uint8_t *norms = cache + (size_t)cap * rb + 2 * ng * (size_t)t0;
-    return launch_encode_rows(rows, n, in, bits, codebook, codes, norms, stream);
+    return launch_encode_rows(rows, n, in, kGroup, bits, codebook, codes, norms, stream);
 }
 
 int cq_kv_attend(const cq_kv_geom *g, const cq_kv_seq *seqs, int n_seqs, void *stream) {
@@ -283,7 +288,7 @@ int cq_kv_attend(const cq_kv_geom *g, const cq_kv_seq *seqs, int n_seqs, void *s
         (long long)g->n_kv_heads * g->head_dim_v > 512)
         return set_error(CQ_ERR_SHAPE, "cache rows of %d x %d (keys) and %d x %d (values) exceed 512 or are empty",
                          g->n_kv_heads, g->head_dim_k, g->n_kv_heads, g->head_dim_v);
-    if (width_of(g->k_bits) < 0 || width_of(g->v_bits) < 0)
+    if (width_of(g->k_bits) < 2 || width_of(g->v_bits) < 2)
         return set_error(CQ_ERR_ARG, "bits must be 2, 3, 4 or 5 (got %d, %d)", g->k_bits, g->v_bits);
     int st = check_codebook(g->k_codebook, g->k_bits);
     if (st) return st;
@@ -305,7 +310,7 @@ int cq_kv_attend(const cq_kv_geom *g, const cq_kv_seq *seqs, int n_seqs, void *s
 }
 
 static int check_gemm_desc(const cq_gemm_desc &d, int i) {
-    int st = check_matrix(d.out, d.in, d.group, d.bits);
+    int st = check_matrix(d.out, d.in, d.group, d.bits, false);
     if (st) return prefix_error(st, i);
     if ((st = check_codebook(d.codebook, d.bits))) return prefix_error(st, i);
     if (d.M < 0) return set_error(CQ_ERR_SHAPE, "descriptor %d: negative M", i);

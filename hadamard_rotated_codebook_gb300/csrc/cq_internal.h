@@ -14,12 +14,14 @@ namespace cq {
 int set_error(int code, const char *fmt, ...);
 void clear_error();
 
-constexpr int kGroup = 128;          // the group size the kernels support
+constexpr int kGroup = 128;          // the group size of the GEMM, the tensor-core GEMV and the KV cache
+constexpr int kGroup64 = 64;         // the other group the encoder, the fp32 GEMV and the row gather take
 constexpr int kMaxLevels = 16;
 constexpr int kMaxLuts = 8;          // distinct codebooks per grouped launch
 
 inline int levels_of(int bits) {
     switch (bits) {
+    case 1: return 2;
     case 2: return 4;
     case 3: return 8;
     case 4: return 16;
@@ -29,6 +31,7 @@ inline int levels_of(int bits) {
 }
 inline int width_of(int bits) {
     switch (bits) {
+    case 1: return 1;
     case 2: return 2;
     case 3: return 3;
     case 4: return 4;
@@ -36,17 +39,17 @@ inline int width_of(int bits) {
     default: return -1;
     }
 }
-inline int in_padded(int in) { return (in + kGroup - 1) / kGroup * kGroup; }
+inline int in_padded(int in, int group = kGroup) { return (in + group - 1) / group * group; }
 
 // Checks a host codebook: non-null, finite, strictly increasing.
 int check_codebook(const float *cb, int bits);
 
 // ------------------------------------------------------------- encode --
-int launch_encode(const float *W, int out, int in, int bits, const float *cb,
+int launch_encode(const float *W, int out, int in, int group, int bits, const float *cb,
                   uint8_t *blob, void *stream);
 // Encodes W[n][in] into explicit code and norm regions (rows of a larger
 // blob: codes at `codes`, fp16 norms at `norms`).
-int launch_encode_rows(const float *W, int n, int in, int bits, const float *cb, uint8_t *codes,
+int launch_encode_rows(const float *W, int n, int in, int group, int bits, const float *cb, uint8_t *codes,
                        uint8_t *norms, void *stream);
 int launch_act_quant(const float *X, int M, int in, int8_t *Xq, float *s,
                      void *stream);
@@ -83,7 +86,7 @@ constexpr unsigned int kStatusIndex = 0x80000000u;
 
 // ------------------------------------------------------------- gather --
 // `levels`: the 16-entry level table by code (ternary crumbs sign-extend).
-int launch_gather_rows(const uint8_t *blob, int out, int in, int bits, const float *levels,
+int launch_gather_rows(const uint8_t *blob, int out, int in, int group, int bits, const float *levels,
                        const int32_t *idx, int n, float *dst, void *stream);
 
 // Level by code, 16 entries (ternary crumbs read as signed 2-bit values).

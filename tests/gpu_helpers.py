@@ -25,21 +25,21 @@ def check_matmul(y, y_ref, bound, what=""):
     return worst
 
 
-def sub_blob(blob, out, n_in, bits, rows):
+def sub_blob(blob, out, n_in, bits, rows, group=128):
     """Blob of a subset of rows (codes of those rows, then their norms)."""
-    ip = O.in_padded(n_in)
+    ip = O.in_padded(n_in, group)
     rb = ip * O.width(bits) // 8
-    ng = ip // 128
+    ng = ip // group
     codes = blob[: out * rb].reshape(out, rb)[rows]
     norms = blob[out * rb:].reshape(out, ng * 2)[rows]
     return np.concatenate([codes.ravel(), norms.ravel()])
 
 
-def compare_encodings(blob_gpu, blob_ref, flags, out, n_in, bits):
+def compare_encodings(blob_gpu, blob_ref, flags, out, n_in, bits, group=128):
     """Codes must be equal except at flagged boundary coordinates; norms
     must be bit-exact. Returns (n_boundary, n_boundary_mismatch)."""
-    cg, ng_ = O.unpack(blob_gpu, out, n_in, bits)
-    cr, nr = O.unpack(blob_ref, out, n_in, bits)
+    cg, ng_ = O.unpack(blob_gpu, out, n_in, bits, group)
+    cr, nr = O.unpack(blob_ref, out, n_in, bits, group)
     assert np.array_equal(ng_, nr), f"{int((ng_ != nr).sum())} fp16 norms differ"
     diff = cg != cr
     bad = diff & (flags == 0)

@@ -45,7 +45,7 @@ def test_library_is_built_for_sm103a(C):
     assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4, 5])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 5])
 def test_codebook_init_matches_oracle(C, bits):
     np.testing.assert_array_equal(C.cq_codebook_init(bits, 128), O.analytic_codebook(bits, 128))
     np.testing.assert_array_equal(C.cq_codebook_init(bits, 64), O.analytic_codebook(bits, 64))
@@ -64,10 +64,10 @@ def test_codebook_init_query_and_errors(C):
 
 
 def test_levels_and_widths(C):
-    for bits in (2, 3, 4, 5):
+    for bits in (1, 2, 3, 4, 5):
         assert C.cq_levels(bits) == O.levels(bits)
         assert C.cq_code_width(bits) == O.width(bits)
-    assert C.cq_levels(1) == -1 and C.cq_code_width(7) == -1
+    assert C.cq_levels(0) == -1 and C.cq_code_width(7) == -1
 
 
 def test_packed_bytes_matches_oracle(C):
@@ -88,8 +88,14 @@ def test_device_entry_points_reject_bad_arguments_before_launch(C):
     lib = _capi.load()
     cb = (ctypes.c_float * 4)(-0.1, -0.03, 0.03, 0.1)
     bad = (ctypes.c_float * 4)(-0.1, 0.03, -0.03, 0.1)
-    assert lib.cq_encode(None, 4, 128, 64, 2, cb, None, None) == _capi.CQ_ERR_SHAPE
-    assert b"group = 128" in lib.cq_last_error()
+    assert lib.cq_encode(None, 4, 128, 32, 2, cb, None, None) == _capi.CQ_ERR_SHAPE
+    assert b"group = 64 or 128" in lib.cq_last_error()
+    assert lib.cq_encode(None, 4, 128, 64, 2, cb, None, None) == _capi.CQ_ERR_ARG  # group 64 taken; null W
+    g64 = _capi.GemmDesc(blob=1, Xq=1, x_scale=1, Y=1, codebook=cb, out=4, in_=128, group=64, bits=2, M=8)
+    assert lib.cq_gemm_grouped(ctypes.byref(g64), 1, None) == _capi.CQ_ERR_SHAPE  # the GEMM keeps group 128
+    b1 = (ctypes.c_float * 2)(-0.07, 0.07)
+    g1 = _capi.GemmDesc(blob=1, Xq=1, x_scale=1, Y=1, codebook=b1, out=4, in_=128, group=128, bits=1, M=8)
+    assert lib.cq_gemm_grouped(ctypes.byref(g1), 1, None) == _capi.CQ_ERR_SHAPE  # and no binary codes
     assert lib.cq_encode(None, 4, 128, 128, 2, bad, None, None) == _capi.CQ_ERR_ARG
     assert b"increasing" in lib.cq_last_error()
     assert lib.cq_encode(None, 4, 128, 128, 7, cb, None, None) == _capi.CQ_ERR_ARG
