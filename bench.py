@@ -246,7 +246,7 @@ def run_cq(args):
     peaks, peak_kind = measured_peaks()
     barrier, max_over_ranks = rank_ops(world, device)
 
-    if args.only in ("gemm", "encode", "gather", "kv"):
+    if args.only in ("gemm", "encode", "gather", "kv", "g64"):
         # one part alone, for profiling: only that part's buffers are held
         stream = torch.cuda.Stream(device)
         if args.only == "gemm":
@@ -256,6 +256,8 @@ def run_cq(args):
             res = bench_gather(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
         elif args.only == "kv":
             res = bench_kv(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
+        elif args.only == "g64":
+            res = bench_g64(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
         else:
             res = bench_encode(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world, args.encode_count)
         if rank == 0:
@@ -381,6 +383,7 @@ def run_cq(args):
                                         args.encode_count)
         result["gather"] = bench_gather(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
         result["kv"] = bench_kv(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
+        result["group64_binary"] = bench_g64(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
     if rank == 0 and world == 1 and not args.skip_cpu:
         result["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     if rank == 0:
@@ -596,6 +599,73 @@ def bench_kv(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world)
                          "algorithmic_bytes_per_launch": algo}}
 
 
+def bench_g64(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world):
+    """Group-64 CQ2 and binary (group 128) weights: one grouped GEMV launch
+    over 64 matrices of 4096 x 4096 (batch 1, fp32 activations), the set
+    larger than L2, plus the encoder on 4 x 8192^2 at group 64 CQ2."""
+    res = {}
+    for name, group, bits in (("cq2_group64", 64, 2), ("binary_group128", 128, 1)):
+        out = n_in = 4096
+        cb = C.cq_codebook_init(bits, group)
+        nb = C.cq_packed_bytes(out, n_in, group, bits)
+        ip = (n_in + group - 1) // group * group
+        items = []
+        for i in range(64):
+            blob = torch.from_numpy(S.random_blob(out * ip * (2 if bits == 5 else bits) // 8, out * ip // group,
+                                                  30000 + 100 * bits + i)).to(device)
+            x = S.normal((1, n_in), 31000 + i).to(device)
+            items.append(dict(blob=blob, out=out, **{"in": n_in}, bits=bits, codebook=cb, x=x, group=group,
+                              y=torch.empty((1, out), dtype=torch.float32, device=device)))
+        plan = C.GemvPlan(items)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                plan.run(stream)
+        stream.synchronize()
+        Kg = 20
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(Kg):
+                plan.run(stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1)) / Kg
+        algo = 64 * (nb + 4 * n_in + 4 * out)
+        gbs = algo / (ms * 1e-3) / 1e9
+        res[name] = {"metric": f"GEMV GB/s, 64 x 4096x4096, group {group}, {bits}-bit codes, batch 1",
+                     "value": round(world * gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4), "steps": Kg,
+                     "packed_bytes_per_step": 64 * nb,
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                                  "algorithmic_bytes_per_launch": algo}}
+    # encoder at group 64
+    cb = C.cq_codebook_init(2, 64)
+    Ws = [S.normal((8192, 8192), 32000 + i, S.W_STD, device=device) for i in range(4)]
+    blobs = [torch.empty(C.cq_packed_bytes(8192, 8192, 64, 2), dtype=torch.uint8, device=device) for _ in range(4)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            C.cq_encode(Ws[0], 2, cb, group=64, blob=blobs[0])
+    stream.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for W, bl in zip(Ws, blobs):
+            C.cq_encode(W, 2, cb, group=64, blob=bl)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1)) / 4
+    algo = 8192 * 8192 * 4 + blobs[0].numel()
+    gbs = algo / (ms * 1e-3) / 1e9
+    res["encode_cq2_group64"] = {"metric": "encode GB/s, 8192x8192 fp32 -> CQ2 at group 64",
+                                 "value": round(world * gbs, 1), "unit": "GB/s", "ms_per_matrix": round(ms, 4),
+                                 "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                                              "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                              "traffic": None, "algorithmic_bytes_per_launch": algo}}
+    return res
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def _oracle_step_sample(budget_s: float):
@@ -667,7 +737,7 @@ def main():
     ap.add_argument("--skip-extra", action="store_true", help="decode step only")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--encode-count", type=int, default=0, help="matrices in the encode part (default 16)")
-    ap.add_argument("--only", default="all", choices=["all", "gemm", "encode", "gather", "kv"],
+    ap.add_argument("--only", default="all", choices=["all", "gemm", "encode", "gather", "kv", "g64"],
                     help="time one secondary part alone and print its JSON object (profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
