@@ -234,6 +234,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     __shared__ FastMat sM;
     __shared__ __half s_lv[16];  // the codebook's levels (parameter reads with a
                                  // per-lane index would serialise)
+    // The next launch on the stream (the next decode step) may start its
+    // blocks as this grid's blocks retire: its weight copies and level table
+    // do not depend on this grid, and it waits for it before reading its
+    // activation (programmatic dependent launch).
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int mi = p.item_mat[blockIdx.x];
     if (threadIdx.x < (int)(sizeof(FastMat) / 4))
         reinterpret_cast<uint32_t *>(&sM)[threadIdx.x] = reinterpret_cast<const uint32_t *>(&p.m[mi])[threadIdx.x];
@@ -248,14 +253,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     const int nrows = 16 * tiles;
     const int rowBytes = ng * (kind == 0 ? 32 : 64);
     const int rs = M.row_stride;  // padded shared-memory row stride (bytes)
-
-    // ---- 0. the activation values of this warp's first group (every batch
-    // row), requested first: their latency overlaps the copies and the table ----
-    float xv[kMaxFastB][4];
-    if (warp < ng)
-#pragma unroll
-        for (int b = 0; b < kMaxFastB; ++b)
-            if (b < B) load_x_bg(M, b, warp, lane, xv[b]);
 
     uint8_t *sc = smem + p.smem_codes;                             // [nrows][rs]
     __half *sn = reinterpret_cast<__half *>(smem + p.smem_norms);  // [nrows][ng]
@@ -318,8 +315,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
         }
     }
 
-    // ---- 3. the activation: warp w rotates groups w, w+8, ... of every
-    // batch row into B fragments and 1/sigma ----
+    // ---- 3. the activation, once the grid before this one on the stream
+    // (which may have written it) is complete: warp w rotates groups w, w+8,
+    // ... of every batch row into B fragments and 1/sigma ----
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    float xv[kMaxFastB][4];
+    if (warp < ng)
+#pragma unroll
+        for (int b = 0; b < kMaxFastB; ++b)
+            if (b < B) load_x_bg(M, b, warp, lane, xv[b]);
     {
         uint32_t(*terms)[kGroup] = reinterpret_cast<uint32_t(*)[kGroup]>(smem + p.smem_terms) + warp * kMaxFastB;
         for (int g = warp; g < ng; g += kWarps) {
@@ -459,7 +463,17 @@ static int flush(FastParams &p, int &nm, int &nlut, Need &need, cudaStream_t st)
         attr = true;
     }
     if (smem > 200 * 1024) return set_error(CQ_ERR_SHAPE, "fast GEMV needs %zu bytes of shared memory", smem);
-    gemv_fast_kernel<<<p.n_items, kThreads, smem, st>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.n_items);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr_pdl[1];
+    attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr_pdl;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, gemv_fast_kernel, p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "fast gemv launch: %s", cudaGetErrorString(e));
     p.n_items = 0;
