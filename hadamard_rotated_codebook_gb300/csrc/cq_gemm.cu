@@ -835,6 +835,10 @@ __global__ void __launch_bounds__(tc3::kThreads, 1) gemm_x8_kernel(const __grid_
     __shared__ tc2::Mat s_mat[14];   // per warp: the current matrix
     __shared__ tc2::SchedTab s_tab;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // The next launch on the stream may start its blocks as this grid's
+    // blocks retire (its weight expansion does not depend on this grid; its
+    // producer waits for it before the first activation load).
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     tc2::load_sched(p, &s_tab);
 
     if (warp == 0) {  // two 128-column fp32 accumulators and two 128-column X slots
@@ -1378,7 +1382,10 @@ static int run_gemm_x8(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t 
 static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, cudaStream_t st) {
     bool any_wide = false, any_narrow = false;
     for (size_t j = 0; j < pl.ptr.size(); ++j) (pl.wide[j] ? any_wide : any_narrow) = true;
-    bool pdl = false;  // the kernel launched last triggers its dependents early
+    // The first kernel may overlap the kernel before it on the stream; that
+    // one's early trigger (if any) decides how much. Every read of data a
+    // previous grid may have written follows griddepcontrol.wait.
+    bool pdl = true;
     // every distinct activation of the wide matrices rotated in one launch
     if (any_wide) {
         static RotTable rt;
