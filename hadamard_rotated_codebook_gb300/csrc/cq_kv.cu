@@ -180,6 +180,111 @@ __device__ void finish_heads(const KvParams &p, const float *sr, const float *sl
     }
 }
 
+// The block's queries as key-side B fragments: for head b and key group g,
+// z = H0 x (x = q_b at its head's columns of the row) scaled by a power of
+// two sigma and split into fp16 hi + lo terms; word (g, nu, nt, lane) of
+// column n = 8 nt + lane/4 (head n/2, term n%2) holds positions
+// 32 (lane%4) + 4 nu + {0,1} and {2,3}. isig[b][g] = 1/sigma. Ends with a
+// block barrier (terms may be reused after it).
+__device__ void rotate_queries(const KvParams &p, const float *qv, uint32_t *terms, float *isig, uint2 *zf) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gq = lane >> 2, c = lane & 3;
+    const int Hq = p.Hq, ngk = p.ngk, ntk = p.ntk;
+    for (int task = warp; task < Hq * ngk; task += kWarps) {
+        const int b = task / ngk, g = task - b * ngk;
+        const int c0 = (b / p.per) * p.dk;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int col = g * kGroup + 4 * lane + i;
+            v[i] = (col >= c0 && col < c0 + p.dk) ? qv[(size_t)b * p.dk + col - c0] : 0.0f;
+        }
+        fwht128(v, lane);
+        float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+        for (int m = 16; m; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        const float sigma = pow2_scale(mx, 16384.0f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x = __fmul_rn(v[i], sigma);
+            const __half hh = __float2half_rn(x);
+            const __half ll = __float2half_rn(__fsub_rn(x, __half2float(hh)));
+            terms[(b * ngk + g) * kGroup + 4 * lane + i] =
+                (uint32_t)__half_as_ushort(hh) | ((uint32_t)__half_as_ushort(ll) << 16);
+        }
+        if (lane == 0) isig[b * ngk + g] = 1.0f / sigma;
+    }
+    __syncthreads();
+    for (int g = 0; g < ngk; ++g)
+        for (int nu = warp; nu < 8; nu += kWarps)
+            for (int nt = 0; nt < ntk; ++nt) {
+                const int n = 8 * nt + gq, b = n >> 1, tau = n & 1, k0 = 32 * c + 4 * nu;
+                uint2 f = make_uint2(0u, 0u);
+                if (b < Hq) {
+                    const uint32_t *tw = terms + (b * ngk + g) * kGroup + k0;
+                    f.x = ((tw[0] >> (16 * tau)) & 0xffffu) | (((tw[1] >> (16 * tau)) & 0xffffu) << 16);
+                    f.y = ((tw[2] >> (16 * tau)) & 0xffffu) | (((tw[3] >> (16 * tau)) & 0xffffu) << 16);
+                }
+                zf[((g * 8 + nu) * ntk + nt) * 32 + lane] = f;
+            }
+    __syncthreads();
+}
+
+// The end of a segment, once sr[b][k] holds the rotated value sums and
+// sM / sL the running max and sum per head: one part writes o directly;
+// otherwise the part goes to workspace slot `slot` and the last block of the
+// sequence to finish (atomic ticket) merges all parts into o. `scratch`
+// holds n_parts * Hq floats. All threads of the block call this; it ends
+// with a block barrier.
+__device__ void emit_segment(const KvParams &p, float *sr, float *sM, float *sL, float *scratch, float *ov, int si,
+                             int n_parts, int slot, int slot0, int *s_last) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, Hq = p.Hq, ipv = p.ngv * kGroup;
+    if (n_parts == 1) {
+        finish_heads(p, sr, sL, ov, warp, lane);
+        __syncthreads();
+        return;
+    }
+    float *pdst = p.part + (size_t)slot * Hq * ipv;
+    for (int i = tid; i < Hq * ipv; i += kThreads) __stcg(pdst + i, sr[i]);
+    if (tid < Hq) {
+        __stcg(p.ml + ((size_t)slot * Hq + tid) * 2, sM[tid]);
+        __stcg(p.ml + ((size_t)slot * Hq + tid) * 2 + 1, sL[tid]);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) *s_last = atomicAdd(p.ticket + si, 1u) == (unsigned)(n_parts - 1);
+    __syncthreads();
+    if (!*s_last) return;  // uniform; the caller's next segment starts after this barrier
+    // the last block of the sequence merges the partials
+    __threadfence();
+    const float *ml0 = p.ml + (size_t)slot0 * Hq * 2;
+    if (tid < Hq) {
+        float mx = -INFINITY;
+        for (int ch = 0; ch < n_parts; ++ch) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)ch * Hq + tid) * 2));
+        sM[tid] = mx;
+    }
+    __syncthreads();
+    for (int i = tid; i < n_parts * Hq; i += kThreads) scratch[i] = exp2f(__ldcg(ml0 + 2 * (size_t)i) - sM[i % Hq]);
+    __syncthreads();
+    if (tid < Hq) {
+        float l = 0.0f;
+        for (int ch = 0; ch < n_parts; ++ch)
+            l = fmaf(__ldcg(ml0 + ((size_t)ch * Hq + tid) * 2 + 1), scratch[ch * Hq + tid], l);
+        sL[tid] = l;
+    }
+    const float *part0 = p.part + (size_t)slot0 * Hq * ipv;
+    for (int i = tid; i < Hq * ipv; i += kThreads) {
+        const int b = i / ipv;
+        float r = 0.0f;
+        for (int ch = 0; ch < n_parts; ++ch)
+            r = fmaf(__ldcg(part0 + (size_t)ch * Hq * ipv + i), scratch[ch * Hq + b], r);
+        sr[i] = r;
+    }
+    if (tid == 0) p.ticket[si] = 0u;  // ready for the next launch
+    __syncthreads();
+    finish_heads(p, sr, sL, ov, warp, lane);
+    __syncthreads();
+}
+
 // Accumulator slot ms of a warp's value-side work: coordinate of its row
 // gq (hi = 0) or gq + 8 (hi = 1). With 2-bit codes a unit is a pair of
 // 16-coordinate slices fed by one byte lookup per token: slice A holds
@@ -269,45 +374,7 @@ __global__ void __launch_bounds__(kThreads, 3) kv_attend_kernel(const __grid_con
         sL[tid] = 0.0f;
         sF[tid] = 1.0f;  // heads past Hq keep 1 (their accumulators stay 0)
     }
-    for (int task = warp; task < Hq * ngk; task += kWarps) {
-        const int b = task / ngk, g = task - b * ngk;
-        const int c0 = (b / p.per) * p.dk;
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int col = g * kGroup + 4 * lane + i;
-            v[i] = (col >= c0 && col < c0 + p.dk) ? qv[(size_t)b * p.dk + col - c0] : 0.0f;
-        }
-        fwht128(v, lane);
-        float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-        for (int m = 16; m; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-        const float sigma = pow2_scale(mx, 16384.0f);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float x = __fmul_rn(v[i], sigma);
-            const __half hh = __float2half_rn(x);
-            const __half ll = __float2half_rn(__fsub_rn(x, __half2float(hh)));
-            terms[(b * ngk + g) * kGroup + 4 * lane + i] =
-                (uint32_t)__half_as_ushort(hh) | ((uint32_t)__half_as_ushort(ll) << 16);
-        }
-        if (lane == 0) isig[b * ngk + g] = 1.0f / sigma;
-    }
-    __syncthreads();
-    // B fragments: word (g, nu, nt, lane) of column n = 8 nt + lane/4 (head n/2,
-    // term n%2), positions 32 (lane%4) + 4 nu + {0,1} and {2,3}
-    for (int g = 0; g < ngk; ++g)
-        for (int nu = warp; nu < 8; nu += kWarps)
-            for (int nt = 0; nt < ntk; ++nt) {
-                const int n = 8 * nt + gq, b = n >> 1, tau = n & 1, k0 = 32 * c + 4 * nu;
-                uint2 f = make_uint2(0u, 0u);
-                if (b < Hq) {
-                    const uint32_t *tw = terms + (b * ngk + g) * kGroup + k0;
-                    f.x = ((tw[0] >> (16 * tau)) & 0xffffu) | (((tw[1] >> (16 * tau)) & 0xffffu) << 16);
-                    f.y = ((tw[2] >> (16 * tau)) & 0xffffu) | (((tw[3] >> (16 * tau)) & 0xffffu) << 16);
-                }
-                zf[((g * 8 + nu) * ntk + nt) * 32 + lane] = f;
-            }
+    rotate_queries(p, qv, terms, isig, zf);
     __syncthreads();  // terms (aliased by the value staging) are dead from here
 
     const int rbk = ngk * 16 * WK, rbv = ngv * 16 * WV, cprk = rbk >> 4, cprv = rbv >> 4;
@@ -583,51 +650,284 @@ __global__ void __launch_bounds__(kThreads, 3) kv_attend_kernel(const __grid_con
         }
     }
     __syncthreads();
-    if (n_parts == 1) {
-        finish_heads(p, sr, sL, ov, warp, lane);
+    emit_segment(p, sr, sM, sL, sp, ov, si, n_parts, slot0 + part, slot0, &s_last);
+    }  // segments
+}
+
+// ------------------------------------------- warp-autonomous variant --
+// For 2-bit keys and values whose cache rows fit one group (at most 128
+// values, e.g. two heads of 48 or 64): each warp owns every eighth 16-token
+// tile of the block's segment and takes it through its own cp.async stages,
+// the logits, an online softmax of its own (running max and sum per head in
+// registers) and the rotated value sums (all 128 coordinates of its heads,
+// 64 registers), without a block barrier in the loop. The warps' states
+// merge once per segment.
+constexpr int kWRows = 16;                        // tokens per warp tile
+constexpr int kWKRow = 32;                        // staged key row (one group of 2-bit codes)
+constexpr int kWVRow = 48;                        // staged value row: 32 bytes + 16 (the four rows a warp
+                                                  // reads per byte position fall in distinct banks)
+constexpr int kWOffV = kWRows * kWKRow;           // value rows
+constexpr int kWOffN = kWOffV + kWRows * kWVRow;  // key norms (16 fp16), then value norms
+constexpr int kWStage = kWOffN + 64;
+constexpr int kWStages = 4;
+constexpr int kWScr = 20;                         // scratch row stride (floats): conflict-free transposes
+
+// 2^x by the hardware approximation (relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// NTK: key-side n-tiles (hi and lo columns of 4 heads each), ceil(Hq / 4).
+template <int NTK>
+__global__ void __launch_bounds__(kThreads, 2) kv_attend_warp_kernel(const __grid_constant__ KvParams p) {
+    constexpr int ntk = NTK, ntv = (NTK + 1) / 2;  // value side: 8 heads per n-tile
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float sMw[kWarps][kMaxHeads], sLw[kWarps][kMaxHeads], sFw[kWarps][kMaxHeads];
+    __shared__ float sM[kMaxHeads], sL[kMaxHeads];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, c = lane & 3, r16 = lane & 15;
+    const int Hq = p.Hq;
+
+    const uint2 *tabk = reinterpret_cast<const uint2 *>(smem + p.sm_tabk) + r16;  // [256][16] levels of a byte
+    const uint2 *tabv = reinterpret_cast<const uint2 *>(smem + p.sm_tabv) + r16;
+    uint2 *zf = reinterpret_cast<uint2 *>(smem + p.sm_zf);
+    float *isig = reinterpret_cast<float *>(smem + p.sm_isig);
+    float *scr = reinterpret_cast<float *>(smem + p.sm_p) + warp * kWRows * kWScr;  // this warp's [16][kWScr]
+    uint8_t *wst = smem + p.sm_stage + warp * kWStages * kWStage;                  // this warp's stages
+    uint32_t *terms = reinterpret_cast<uint32_t *>(smem + p.sm_terms);  // setup only (aliases the stages)
+    float *sr = reinterpret_cast<float *>(smem + p.sm_r);               // end only: [Hq][128], then merge factors
+
+    for (int side = 0; side < 2; ++side) {  // byte -> four fp16 levels, 16 replicas
+        if (side == 1 && p.sm_tabv == p.sm_tabk) break;
+        const uint16_t *lv = side ? p.lvv : p.lvk;
+        uint32_t *t = reinterpret_cast<uint32_t *>(smem + (side ? p.sm_tabv : p.sm_tabk));
+        for (int i = tid; i < 256 * 16; i += kThreads) {
+            const int e = i >> 4;
+            t[2 * i] = (uint32_t)lv[e & 3] | ((uint32_t)lv[(e >> 2) & 3] << 16);
+            t[2 * i + 1] = (uint32_t)lv[(e >> 4) & 3] | ((uint32_t)lv[e >> 6] << 16);
+        }
+    }
+    for (int q = blockIdx.x; q < p.n_seqs; q += gridDim.x)  // empty softmax: o = 0
+        if (p.s[q].n == 0)
+            for (int i = tid; i < Hq * p.dv; i += kThreads) p.s[q].o[i] = 0.0f;
+
+    const int G = gridDim.x, T = p.total_sub, bid = blockIdx.x;
+    const int x_end = (int)(((long long)(bid + 1) * T) / G);
+    for (int x = (int)(((long long)bid * T) / G); x < x_end;) {
+        int lo = 0, hi = p.n_seqs - 1;  // the sequence holding sub-tile x
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.s[mid].sub0 <= x) lo = mid;
+            else hi = mid - 1;
+        }
+        const int si = lo;
+        const uint8_t *const kc = p.s[si].kc;
+        const uint8_t *const vc = p.s[si].vc;
+        float *const ov = p.s[si].o;
+        const int cap = p.s[si].cap, n_tok = p.s[si].n, n_parts = p.s[si].n_parts, slot0 = p.s[si].slot0;
+        const int sub0 = p.s[si].sub0, sub_end = sub0 + (n_tok + kTile - 1) / kTile;
+        const int seg_end = min(x_end, sub_end), part = bid - p.s[si].part_b0;
+        const int t_begin = (x - sub0) * kTile, t_end = min(n_tok, (seg_end - sub0) * kTile);
+        x = seg_end;
+        rotate_queries(p, p.s[si].q, terms, isig, zf);  // ends with a barrier: the stages are free
+
+        const uint8_t *const knorm_b = kc + (size_t)cap * kWKRow;
+        const uint8_t *const vnorm_b = vc + (size_t)cap * 32;
+        const int ntiles = (t_end - t_begin + kWRows - 1) / kWRows;
+        const int mine = warp < ntiles ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+        // Copies of this warp's k-th tile into stage k % kWStages (one commit
+        // group per tile, empty past the end): lane l copies half l & 1 of key
+        // and value row l >> 1; lanes 0-3 the two norm blocks.
+        auto issue = [&](int k) {
+            if (k < mine) {
+                uint8_t *st = wst + (k % kWStages) * kWStage;
+                const int t0 = t_begin + (warp + kWarps * k) * kWRows, nv = min(kWRows, t_end - t0);
+                const int r = lane >> 1, h = lane & 1;
+                const bool ok = r < nv;
+                const size_t row = (size_t)(t0 + (ok ? r : 0));
+                cp_async16(st + r * kWKRow + 16 * h, kc + row * kWKRow + 16 * h, ok ? 16 : 0);
+                cp_async16(st + kWOffV + r * kWVRow + 16 * h, vc + row * 32 + 16 * h, ok ? 16 : 0);
+                if (lane < 4) {
+                    const int which = lane >> 1, piece = lane & 1;
+                    const int bytes = min(16, max(0, 2 * nv - 16 * piece));
+                    const uint8_t *src = (which ? vnorm_b : knorm_b) + (size_t)t0 * 2 + 16 * piece;
+                    cp_async16(st + kWOffN + 32 * which + 16 * piece, bytes ? src : knorm_b, bytes);
+                }
+            }
+            cp_async_commit();
+        };
+
+        float m_h[4], l_h[4];  // running max (base 2) and sum of heads 4 nt + c
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            m_h[nt] = -INFINITY;
+            l_h[nt] = 0.0f;
+        }
+        float acc[8][2][4];  // slot 2u + m: coordinates 4(8u + gq) + 2m + {0 (row gq), 1 (row gq + 8)}
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[j][nt][i] = 0.0f;
+
+        for (int k = 0; k + 1 < kWStages; ++k) issue(k);
+        for (int k = 0; k < mine; ++k) {
+            issue(k + kWStages - 1);
+            cp_async_wait<kWStages - 1>();
+            __syncwarp();
+            const uint8_t *st = wst + (k % kWStages) * kWStage;
+            const int t0 = t_begin + (warp + kWarps * k) * kWRows, nv = min(kWRows, t_end - t0);
+            const __half *kn = reinterpret_cast<const __half *>(st + kWOffN);
+            const __half *vn = kn + kWRows;
+            // ---- logits of rows gq and gq + 8 for heads 4 nt + c ----
+            const bool va = gq < nv, vb = gq + 8 < nv;
+            float sa[4], sb[4];
+            {
+                const uint2 ca = *reinterpret_cast<const uint2 *>(st + gq * kWKRow + 8 * c);
+                const uint2 cb = *reinterpret_cast<const uint2 *>(st + (gq + 8) * kWKRow + 8 * c);
+                float d[4][4];
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) d[nt][i] = 0.0f;
+#pragma unroll
+                for (int nu = 0; nu < 8; ++nu) {
+                    const uint32_t wa = nu < 4 ? ca.x : ca.y, wb = nu < 4 ? cb.x : cb.y;
+                    const uint2 ea = tabk[((wa >> (8 * (nu & 3))) & 0xffu) * 16];
+                    const uint2 eb = tabk[((wb >> (8 * (nu & 3))) & 0xffu) * 16];
+                    const uint2 *zb = zf + (nu * ntk) * 32 + lane;
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt)
+                        if (nt < ntk) {
+                            const uint2 bf = zb[nt * 32];
+                            mma_f16(d[nt], ea.x, eb.x, ea.y, eb.y, bf.x, bf.y);
+                        }
+                }
+                const float na = __half2float(kn[gq]), nb = __half2float(kn[gq + 8]);
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int b = 4 * nt + c;
+                    const float is = nt < ntk && b < Hq ? isig[b] * p.logit_scale : 0.0f;
+                    sa[nt] = va && nt < ntk && b < Hq ? na * is * (d[nt][0] + d[nt][1]) : -INFINITY;
+                    sb[nt] = vb && nt < ntk && b < Hq ? nb * is * (d[nt][2] + d[nt][3]) : -INFINITY;
+                }
+            }
+            // ---- online softmax of the warp's heads; weights p * n_v to the scratch ----
+            const float nva = __half2float(vn[gq]), nvb = __half2float(vn[gq + 8]);  // 0 past the end
+            bool moved = false;  // some head's running max changed: the sums are rescaled
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int b = 4 * nt + c;
+                if (nt >= ntk) break;  // uniform
+                float mx = fmaxf(sa[nt], sb[nt]);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float mn = b < Hq ? fmaxf(m_h[nt], mx) : 0.0f;  // a tile has a live row: finite
+                const float pa = ex2(sa[nt] - mn), pb = ex2(sb[nt] - mn);
+                float sum = pa + pb;
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                const float f = b < Hq && mn != m_h[nt] ? ex2(m_h[nt] - mn) : 1.0f;  // 0 on the warp's first tile
+                moved |= f != 1.0f;
+                l_h[nt] = fmaf(l_h[nt], f, sum);
+                m_h[nt] = mn;
+                if (b < Hq) {
+                    scr[gq * kWScr + b] = pa * nva;
+                    scr[(gq + 8) * kWScr + b] = pb * nvb;
+                    if (gq == 0) sFw[warp][b] = f;
+                }
+            }
+            moved = __any_sync(0xffffffffu, moved);
+            __syncwarp();
+            // ---- rotated value sums: rescale, then A = coordinates x tokens ----
+            uint2 bw[2];  // B fragments: tokens 2c, 2c+1 | 2c+8, 2c+9 of column (head) 8 nt + gq
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int b = 8 * nt + gq;
+                bw[nt] = make_uint2(0u, 0u);
+                if (nt < ntv && b < Hq) {
+                    bw[nt].x = pack_h2(scr[2 * c * kWScr + b], scr[(2 * c + 1) * kWScr + b]);
+                    bw[nt].y = pack_h2(scr[(2 * c + 8) * kWScr + b], scr[(2 * c + 9) * kWScr + b]);
+                }
+                if (nt < ntv && moved) {
+                    const int h0 = 8 * nt + 2 * c;
+                    const float f0 = h0 < Hq ? sFw[warp][h0] : 1.0f, f1 = h0 + 1 < Hq ? sFw[warp][h0 + 1] : 1.0f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        acc[j][nt][0] *= f0;
+                        acc[j][nt][1] *= f1;
+                        acc[j][nt][2] *= f0;
+                        acc[j][nt][3] *= f1;
+                    }
+                }
+            }
+            const uint8_t *vrow = st + kWOffV + 2 * c * kWVRow + gq;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint8_t *q = vrow + 8 * u;
+                const uint2 h0 = tabv[(uint32_t)q[0] * 16], h1 = tabv[(uint32_t)q[kWVRow] * 16];
+                const uint2 h2 = tabv[(uint32_t)q[8 * kWVRow] * 16], h3 = tabv[(uint32_t)q[9 * kWVRow] * 16];
+                const uint32_t aA0 = __byte_perm(h0.x, h1.x, 0x5410), aA1 = __byte_perm(h0.x, h1.x, 0x7632);
+                const uint32_t aA2 = __byte_perm(h2.x, h3.x, 0x5410), aA3 = __byte_perm(h2.x, h3.x, 0x7632);
+                const uint32_t aB0 = __byte_perm(h0.y, h1.y, 0x5410), aB1 = __byte_perm(h0.y, h1.y, 0x7632);
+                const uint32_t aB2 = __byte_perm(h2.y, h3.y, 0x5410), aB3 = __byte_perm(h2.y, h3.y, 0x7632);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+                    if (nt < ntv) {
+                        mma_f16(acc[2 * u][nt], aA0, aA1, aA2, aA3, bw[nt].x, bw[nt].y);
+                        mma_f16(acc[2 * u + 1][nt], aB0, aB1, aB2, aB3, bw[nt].x, bw[nt].y);
+                    }
+            }
+            __syncwarp();  // the scratch and this stage are rewritten next
+        }
+        cp_async_wait<0>();  // only empty groups remain
+
+        // ---- merge the warps: per head M = max over warps, factors 2^(m_w - M) ----
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const int b = 4 * nt + c;
+            if (gq == 0 && nt < ntk && b < Hq) {
+                sMw[warp][b] = m_h[nt];
+                sLw[warp][b] = l_h[nt];
+            }
+        }
+        __syncthreads();  // every warp is out of its stages: sr may reuse them
+        if (tid < Hq) {
+            float mx = -INFINITY;
+            for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, sMw[w][tid]);
+            float l = 0.0f;
+            for (int w = 0; w < kWarps; ++w)
+                if (sMw[w][tid] != -INFINITY) l = fmaf(sLw[w][tid], exp2f(sMw[w][tid] - mx), l);
+            sM[tid] = mx;
+            sL[tid] = l;
+        }
+        for (int i = tid; i < Hq * kGroup; i += kThreads) sr[i] = 0.0f;
         __syncthreads();
-        continue;
-    }
-    const int slot = slot0 + part;
-    float *pdst = p.part + (size_t)slot * Hq * ipv;
-    for (int i = tid; i < Hq * ipv; i += kThreads) __stcg(pdst + i, sr[i]);
-    if (tid < Hq) {
-        __stcg(p.ml + ((size_t)slot * Hq + tid) * 2, sM[tid]);
-        __stcg(p.ml + ((size_t)slot * Hq + tid) * 2 + 1, sL[tid]);
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(p.ticket + si, 1u) == (unsigned)(n_parts - 1);
-    __syncthreads();
-    if (!s_last) continue;  // (s_last is uniform; the next segment starts after a barrier)
-    // ---- F. the last block of the sequence merges the partials ----
-    __threadfence();
-    const float *ml0 = p.ml + (size_t)slot0 * Hq * 2;
-    if (tid < Hq) {
-        float mx = -INFINITY;
-        for (int ch = 0; ch < n_parts; ++ch) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)ch * Hq + tid) * 2));
-        sM[tid] = mx;
-    }
-    __syncthreads();
-    // per (chunk, head) rescale factors (the logits' buffer holds 16 * kSpRow >= n_chunks * Hq floats)
-    for (int i = tid; i < n_parts * Hq; i += kThreads) sp[i] = exp2f(__ldcg(ml0 + 2 * (size_t)i) - sM[i % Hq]);
-    __syncthreads();
-    if (tid < Hq) {
-        float l = 0.0f;
-        for (int ch = 0; ch < n_parts; ++ch) l = fmaf(__ldcg(ml0 + ((size_t)ch * Hq + tid) * 2 + 1), sp[ch * Hq + tid], l);
-        sL[tid] = l;
-    }
-    const float *part0 = p.part + (size_t)slot0 * Hq * ipv;
-    for (int i = tid; i < Hq * ipv; i += kThreads) {
-        const int b = i / ipv;
-        float r = 0.0f;
-        for (int ch = 0; ch < n_parts; ++ch) r = fmaf(__ldcg(part0 + (size_t)ch * Hq * ipv + i), sp[ch * Hq + b], r);
-        sr[i] = r;
-    }
-    if (tid == 0) p.ticket[si] = 0u;  // ready for the next launch
-    __syncthreads();
-    finish_heads(p, sr, sL, ov, warp, lane);
-    __syncthreads();
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            if (nt >= ntv) break;
+            const int h0 = 8 * nt + 2 * c;
+            const float f0 = h0 < Hq && sMw[warp][h0] != -INFINITY ? exp2f(sMw[warp][h0] - sM[h0]) : 0.0f;
+            const float f1 = h0 + 1 < Hq && sMw[warp][h0 + 1] != -INFINITY ? exp2f(sMw[warp][h0 + 1] - sM[h0 + 1]) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int k0 = 4 * (8 * (j >> 1) + gq) + 2 * (j & 1);
+                if (h0 < Hq) {
+                    atomicAdd(sr + h0 * kGroup + k0, acc[j][nt][0] * f0);
+                    atomicAdd(sr + h0 * kGroup + k0 + 1, acc[j][nt][2] * f0);
+                }
+                if (h0 + 1 < Hq) {
+                    atomicAdd(sr + (h0 + 1) * kGroup + k0, acc[j][nt][1] * f1);
+                    atomicAdd(sr + (h0 + 1) * kGroup + k0 + 1, acc[j][nt][3] * f1);
+                }
+            }
+        }
+        __syncthreads();
+        emit_segment(p, sr, sM, sL, sr + Hq * kGroup, ov, si, n_parts, slot0 + part, slot0, &s_last);
     }  // segments
 }
 
@@ -657,6 +957,33 @@ template <int WK, int WV>
 int dispatch_t(bool occ, const KvParams &p, int grid, int smem, cudaStream_t st) {
     if (occ) return occupancy_t<WK, WV>(smem);
     launch_t<WK, WV>(p, grid, smem, st);
+    return CQ_OK;
+}
+
+// Resident blocks per SM of the warp-autonomous kernel at `smem` bytes.
+template <int NTK>
+int occupancy_warp_t(int smem) {
+    static int attr = 0;
+    if (smem > attr) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kv_attend_warp_kernel<NTK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention attribute: %s", cudaGetErrorString(e));
+        attr = smem;
+    }
+    int nb = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kv_attend_warp_kernel<NTK>, kThreads, smem);
+    if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention occupancy: %s", cudaGetErrorString(e));
+    return std::max(nb, 1);
+}
+
+// occ: the occupancy of the warp kernel for ntk key n-tiles; else launch it.
+int dispatch_warp(int ntk, bool occ, const KvParams &p, int grid, int smem, cudaStream_t st) {
+    switch (ntk) {
+    case 1: if (occ) return occupancy_warp_t<1>(smem); kv_attend_warp_kernel<1><<<grid, kThreads, smem, st>>>(p); break;
+    case 2: if (occ) return occupancy_warp_t<2>(smem); kv_attend_warp_kernel<2><<<grid, kThreads, smem, st>>>(p); break;
+    case 3: if (occ) return occupancy_warp_t<3>(smem); kv_attend_warp_kernel<3><<<grid, kThreads, smem, st>>>(p); break;
+    default: if (occ) return occupancy_warp_t<4>(smem); kv_attend_warp_kernel<4><<<grid, kThreads, smem, st>>>(p); break;
+    }
     return CQ_OK;
 }
 
@@ -756,9 +1083,24 @@ int launch_kv_attend(const cq_kv_geom &g, const cq_kv_seq *seqs, int n, const fl
     // (sub-tiles) and the rotated sums (end)
     p.sm_terms = p.sm_stage = p.sm_r = off;
     off += union_bytes(p.n_stages);
-    const int smem = off;
+    int smem = off;
 
-    const int per_sm = dispatch(WK, WV, true, p, 0, smem, st);
+    // 2-bit keys and values in rows of one group: the warp-autonomous kernel,
+    // with its own layout after the tables: query fragments, 1/sigma, the
+    // warps' scratch rows, then one region for the query terms (setup), the
+    // warps' stages (loop) and the rotated sums with the merge factors (end)
+    const bool warp_path = WK == 2 && WV == 2 && p.ngk == 1 && p.ngv == 1;
+    if (warp_path) {
+        off = p.sm_zf;
+        off += align16(8 * p.ntk * 32 * 8);
+        p.sm_isig = off;  off += align16(Hq * 4);
+        p.sm_p = off;     off += align16(kWarps * kWRows * kWScr * 4);
+        p.sm_terms = p.sm_stage = p.sm_r = off;
+        off += align16(std::max({kWarps * kWStages * kWStage, Hq * kGroup * 4, Hq * kGroup * 4 + kMaxParts * Hq * 4}));
+        smem = off;
+    }
+
+    const int per_sm = warp_path ? dispatch_warp(p.ntk, true, p, 0, smem, st) : dispatch(WK, WV, true, p, 0, smem, st);
     if (per_sm < 0) return per_sm;
     const long long slots_gpu = (long long)per_sm * sm_count();
     for (int base = 0; base < n; base += kMaxSeqs) {
@@ -815,7 +1157,8 @@ int launch_kv_attend(const cq_kv_geom &g, const cq_kv_seq *seqs, int n, const fl
             const cudaError_t e = cudaMemsetAsync(p.ticket, 0, (size_t)cnt * 4, st);
             if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention tickets: %s", cudaGetErrorString(e));
         }
-        dispatch(WK, WV, false, p, G, smem, st);
+        if (warp_path) dispatch_warp(p.ntk, false, p, G, smem, st);
+        else dispatch(WK, WV, false, p, G, smem, st);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention launch: %s", cudaGetErrorString(e));
     }
