@@ -60,7 +60,7 @@ struct FastMat {
     const float *xs;
     float *y;
     int out, in, ng, bits, xdt, B;
-    int kind;      // 0: 2-bit codes, 1: 4-bit codes
+    int kind;      // 0: 2-bit codes, 1: 4-bit codes, 2: 1-bit codes
     int lut;       // index into FastParams::lut
     int tiles;     // row tiles (16 rows) per CTA
     int kchunks;   // warps sharing one tile (split of the groups)
@@ -211,6 +211,20 @@ __device__ __forceinline__ void lut2_group(float (&acc)[4], uint2 cr, uint2 cs, 
     for (int i = 0; i < 4; ++i) acc[i] = fmaf(i >= 2 ? ns : nr, d[i], acc[i]);
 }
 
+// 1-bit codes: the lane's 4 code bytes of each row cover positions 32t ..
+// 32t+31; MMA nu takes positions 32t + 4nu .. +3, nibble nu of the word.
+__device__ __forceinline__ void lut1_group(float (&acc)[4], uint32_t cr, uint32_t cs, const uint2 *tab_lane,
+                                           const uint32_t (&fr)[kFragWords], float nr, float ns) {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int nu = 0; nu < 8; ++nu) {
+        const uint2 er = tab_lane[((cr >> (4 * nu)) & 15u) * 16], es = tab_lane[((cs >> (4 * nu)) & 15u) * 16];
+        mma_f16(d, er.x, es.x, er.y, es.y, fr[2 * nu], fr[2 * nu + 1]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = fmaf(i >= 2 ? ns : nr, d[i], acc[i]);
+}
+
 __device__ __forceinline__ void lut4_group(float (&acc)[4], uint4 cr, uint4 cs, const uint32_t *tab_lane,
                                            const uint32_t (&fr)[kFragWords], float nr, float ns) {
     float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -251,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     const int ng = M.ng, B = M.B, kind = M.kind, tiles = M.tiles;
     const int row0 = ((int)blockIdx.x - M.item0) * 16 * tiles;
     const int nrows = 16 * tiles;
-    const int rowBytes = ng * (kind == 0 ? 32 : 64);
+    const int rowBytes = ng * (kind == 0 ? 32 : kind == 1 ? 64 : 16);
     const int rs = M.row_stride;  // padded shared-memory row stride (bytes)
 
     uint8_t *sc = smem + p.smem_codes;                             // [nrows][rs]
@@ -295,7 +309,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     // ---- 2. while they land: the level table and the output scales ----
     {
         const __half *lv = s_lv;
-        if (kind == 0) {
+        if (kind == 2) {
+            // nibble -> four fp16 levels (codes LSB first), 16 copies
+            uint2 *tab = reinterpret_cast<uint2 *>(smem + p.smem_tab);
+            for (int e = threadIdx.x; e < 16 * 16; e += kThreads) {
+                const int v = e >> 4;
+                tab[e] = make_uint2(
+                    (uint32_t)__half_as_ushort(lv[v & 1]) | ((uint32_t)__half_as_ushort(lv[(v >> 1) & 1]) << 16),
+                    (uint32_t)__half_as_ushort(lv[(v >> 2) & 1]) | ((uint32_t)__half_as_ushort(lv[v >> 3]) << 16));
+            }
+        } else if (kind == 0) {
             // byte -> four fp16 levels (codes LSB first), 16 copies so that a
             // half-warp's 8-byte lookups hit distinct banks
             uint2 *tab = reinterpret_cast<uint2 *>(smem + p.smem_tab);
@@ -374,7 +397,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
             const float inv = t < B ? ginv[t * ng + g] : 0.0f;
             const float n0 = __half2float(sn[ra * ng + g]) * inv, n1 = __half2float(sn[(ra + 8) * ng + g]) * inv;
             const float n2 = __half2float(sn[rb * ng + g]) * inv, n3 = __half2float(sn[(rb + 8) * ng + g]) * inv;
-            if (kind == 0) {
+            if (kind == 2) {
+                const uint32_t c0 = *reinterpret_cast<const uint32_t *>(sc + (size_t)ra * rs + g * 16 + 4 * t);
+                const uint32_t c1 = *reinterpret_cast<const uint32_t *>(sc + (size_t)(ra + 8) * rs + g * 16 + 4 * t);
+                lut1_group(acc[0], c0, c1, tab2, fr, n0, n1);
+                if (has_b) {
+                    const uint32_t c2 = *reinterpret_cast<const uint32_t *>(sc + (size_t)rb * rs + g * 16 + 4 * t);
+                    const uint32_t c3 = *reinterpret_cast<const uint32_t *>(sc + (size_t)(rb + 8) * rs + g * 16 + 4 * t);
+                    lut1_group(acc[1], c2, c3, tab2, fr, n2, n3);
+                }
+            } else if (kind == 0) {
                 const uint2 c0 = *reinterpret_cast<const uint2 *>(sc + (size_t)ra * rs + g * 32 + 8 * t);
                 const uint2 c1 = *reinterpret_cast<const uint2 *>(sc + (size_t)(ra + 8) * rs + g * 32 + 8 * t);
                 lut2_group(acc[0], c0, c1, tab2, fr, n0, n1);
@@ -433,7 +465,7 @@ bool gemv_fast_eligible(const cq_gemv_desc &d) {
     const int ng = in_padded(d.in) / kGroup;
     if (d.in <= 0 || d.out <= 0 || d.group != kGroup) return false;
     const int W = width_of(d.bits);
-    return (W == 2 || W == 4) && d.B <= kMaxFastB && ng <= kMaxFastNg;
+    return (W == 1 || W == 2 || W == 4) && d.B <= kMaxFastB && ng <= kMaxFastNg;
 }
 
 // Shared-memory needs of one launch (maxima over its matrices).
@@ -493,9 +525,9 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
     for (int ii = 0; ii < n; ++ii) {
         const cq_gemv_desc &D = d[idx[ii]];
         const int ip = in_padded(D.in), W = width_of(D.bits), ng = ip / kGroup;
-        const int kind = W == 2 ? 0 : 1;
+        const int kind = W == 2 ? 0 : W == 4 ? 1 : 2;
         // rows per CTA: about 48 KB of codes, a power-of-two number of 16-row tiles
-        const int rowB = ng * (kind == 0 ? 32 : 64) + 2 * ng;
+        const int rowB = ng * (kind == 0 ? 32 : kind == 1 ? 64 : 16) + 2 * ng;
         const int tiles = std::max(1, (48 * 1024) / (rowB * 16));
         int tp = 1;
         while (tp * 2 <= tiles && tp * 2 <= 32) tp *= 2;
@@ -550,9 +582,10 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
         M.kchunks = tp >= kWarps ? 1 : std::min(kWarps / tp, M.ng);
         // row stride in shared memory: the 2-bit path reads 8 bytes per lane
         // (rows of a half-warp must start 8 banks apart), the 4-bit path 16
-        // bytes (rows of a quarter-warp 16 banks apart)
-        const int rowBytes = M.ng * (M.kind == 0 ? 32 : 64);
-        const int want = M.kind == 0 ? 32 : 64;
+        // bytes (rows of a quarter-warp 16 banks apart), the 1-bit path 4
+        // bytes (the warp's eight rows 4 banks apart)
+        const int rowBytes = M.ng * (M.kind == 0 ? 32 : M.kind == 1 ? 64 : 16);
+        const int want = M.kind == 0 ? 32 : M.kind == 1 ? 64 : 16;
         M.row_stride = rowBytes + (((want - rowBytes) % 128) + 128) % 128;
 
         M.item0 = p.n_items;
