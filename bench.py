@@ -42,9 +42,11 @@ WORKLOAD = ("Needle-shaped decode step, batch 1: 27 x {Q 512x512, K 256x512, V 2
 # hash of the sources it was built from: once a source changes the entry no
 # longer matches and traffic reads null.
 NCU_TRAFFIC = {
-    "gemv_fast": ("c3de10983de6e38f", 9774336),
-    "gemm_x8": ("0da92c438e16f398", 527862272),
-    "gather_cq4": ("6d3e28f53fe8a3fd", 75240192),
+    "gemv_fast": ("c6df894184183afa", 9777408),
+    "gemm_x8": ("0da92c438e16f398", 527802624),
+    "encode_cq2": ("7e3cefd173abbca5", 281678080),
+    "gather_cq4": ("6d3e28f53fe8a3fd", 75090944),
+    "kv_attend": ("35baf7ac93d888e3", 149307904),
 }
 KERNEL_SOURCES = {
     "gemv_fast": ("cq_gemv_fast.cu", "cq_internal.h"),
