@@ -605,7 +605,7 @@ def bench_g64(C, S, torch, device, stream, peaks, barrier, max_over_ranks, world
     over 64 matrices of 4096 x 4096 (batch 1, fp32 activations), the set
     larger than L2, plus the encoder on 4 x 8192^2 at group 64 CQ2."""
     res = {}
-    for name, group, bits in (("cq2_group64", 64, 2), ("binary_group128", 128, 1)):
+    for name, group, bits in (("cq2_group64", 64, 2), ("binary_group128", 128, 1), ("cq2_group128", 128, 2)):
         out = n_in = 4096
         cb = C.cq_codebook_init(bits, group)
         nb = C.cq_packed_bytes(out, n_in, group, bits)

@@ -526,9 +526,11 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
         const cq_gemv_desc &D = d[idx[ii]];
         const int ip = in_padded(D.in), W = width_of(D.bits), ng = ip / kGroup;
         const int kind = W == 2 ? 0 : W == 4 ? 1 : 2;
-        // rows per CTA: about 48 KB of codes, a power-of-two number of 16-row tiles
+        // rows per CTA: about 48 KB of codes (96 KB for inputs of 16 groups or
+        // more, whose rotation each CTA repeats), a power-of-two number of 16-row tiles
         const int rowB = ng * (kind == 0 ? 32 : kind == 1 ? 64 : 16) + 2 * ng;
-        const int tiles = std::max(1, (48 * 1024) / (rowB * 16));
+        const int budget = (ng >= 16 ? 96 : 48) * 1024;
+        const int tiles = std::max(1, budget / (rowB * 16));
         int tp = 1;
         while (tp * 2 <= tiles && tp * 2 <= 32) tp *= 2;
         const int need_tiles = (D.out + 15) / 16;
