@@ -215,16 +215,23 @@ void launch_b(int bmax, const GemvParams &p, size_t smem, int grid, cudaStream_t
 
 int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // Small batches go to the tensor-core kernel (one launch for all of
-    // them); the rest run here.
-    int fast_idx[CQ_MAX_GROUPED], nfast = 0;
+    // Small batches go to the tensor-core kernels (one launch for all of the
+    // matrices with inputs up to 15 groups, a streamed launch for wider
+    // ones); the rest run here.
+    int fast_idx[CQ_MAX_GROUPED], nfast = 0, stream_idx[CQ_MAX_GROUPED], nstream = 0;
     bool is_fast[CQ_MAX_GROUPED];
     for (int i = 0; i < n; ++i) {
-        is_fast[i] = gemv_fast_eligible(d[i]);
-        if (is_fast[i]) fast_idx[nfast++] = i;
+        const bool sf = gemv_stream_eligible(d[i]);
+        is_fast[i] = sf || gemv_fast_eligible(d[i]);
+        if (sf) stream_idx[nstream++] = i;
+        else if (is_fast[i]) fast_idx[nfast++] = i;
     }
     if (nfast) {
         int st2 = launch_gemv_fast(d, fast_idx, nfast, stream);
+        if (st2) return st2;
+    }
+    if (nstream) {
+        int st2 = launch_gemv_stream(d, stream_idx, nstream, stream);
         if (st2) return st2;
     }
     // One launch per code width present; each launch walks all descriptors of

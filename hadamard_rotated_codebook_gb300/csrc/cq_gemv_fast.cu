@@ -240,6 +240,61 @@ __device__ __forceinline__ void lut4_group(float (&acc)[4], uint4 cr, uint4 cs, 
     for (int i = 0; i < 4; ++i) acc[i] = fmaf(i >= 2 ? ns : nr, d[i], acc[i]);
 }
 
+// Level table of this matrix's codes in shared memory at `tab`: 2-bit codes
+// a byte -> four fp16 levels (16 copies, so that a half-warp's 8-byte lookups
+// hit distinct banks); 4-bit codes a byte -> two levels (32 copies); 1-bit
+// codes a nibble -> four levels (16 copies).
+__device__ void build_level_table(int kind, const __half *lv, uint8_t *tab) {
+    if (kind == 2) {
+        uint2 *t = reinterpret_cast<uint2 *>(tab);
+        for (int e = threadIdx.x; e < 16 * 16; e += blockDim.x) {
+            const int v = e >> 4;
+            t[e] = make_uint2(
+                (uint32_t)__half_as_ushort(lv[v & 1]) | ((uint32_t)__half_as_ushort(lv[(v >> 1) & 1]) << 16),
+                (uint32_t)__half_as_ushort(lv[(v >> 2) & 1]) | ((uint32_t)__half_as_ushort(lv[v >> 3]) << 16));
+        }
+    } else if (kind == 0) {
+        uint2 *t = reinterpret_cast<uint2 *>(tab);
+        for (int e = threadIdx.x; e < 256 * 16; e += blockDim.x) {
+            const int v = e >> 4;
+            t[e] = make_uint2(
+                (uint32_t)__half_as_ushort(lv[v & 3]) | ((uint32_t)__half_as_ushort(lv[(v >> 2) & 3]) << 16),
+                (uint32_t)__half_as_ushort(lv[(v >> 4) & 3]) | ((uint32_t)__half_as_ushort(lv[v >> 6]) << 16));
+        }
+    } else {
+        uint32_t *t = reinterpret_cast<uint32_t *>(tab);
+        for (int e = threadIdx.x; e < 256 * 32; e += blockDim.x) {
+            const int v = e >> 5;
+            t[e] = (uint32_t)__half_as_ushort(lv[v & 15]) | ((uint32_t)__half_as_ushort(lv[v >> 4]) << 16);
+        }
+    }
+}
+
+// The activation of M as B fragments: warp w rotates groups w, w+8, ... of
+// every batch row (scratch `terms`: kWarps x kMaxFastB x 128 words) into
+// frag[g] and 1/sigma into ginv[b][g]. No block barrier: the caller syncs.
+__device__ void rotate_activation(const FastMat &M, uint8_t *terms_base, uint32_t *frag, float *ginv) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, ng = M.ng, B = M.B;
+    float xv[kMaxFastB][4];
+    if (warp < ng)  // the first group's values, requested before anything else
+#pragma unroll
+        for (int b = 0; b < kMaxFastB; ++b)
+            if (b < B) load_x_bg(M, b, warp, lane, xv[b]);
+    uint32_t(*terms)[kGroup] = reinterpret_cast<uint32_t(*)[kGroup]>(terms_base) + warp * kMaxFastB;
+    for (int g = warp; g < ng; g += kWarps) {
+#pragma unroll
+        for (int b = 0; b < kMaxFastB; ++b) {
+            if (b >= B) break;
+            if (g != warp) load_x_bg(M, b, g, lane, xv[b]);
+            const float inv = rotate_bg(xv[b], lane, terms[b]);
+            if (lane == 0) ginv[b * ng + g] = inv;
+        }
+        __syncwarp();
+        frag_words(M, terms, lane, frag + (size_t)g * 32 * kFragWords);
+        __syncwarp();
+    }
+}
+
 // ------------------------------------------------------------ the kernel --
 __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_constant__ FastParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -306,62 +361,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
         asm volatile("cp.async.commit_group;\n" ::);
     }
 
-    // ---- 2. while they land: the level table and the output scales ----
-    {
-        const __half *lv = s_lv;
-        if (kind == 2) {
-            // nibble -> four fp16 levels (codes LSB first), 16 copies
-            uint2 *tab = reinterpret_cast<uint2 *>(smem + p.smem_tab);
-            for (int e = threadIdx.x; e < 16 * 16; e += kThreads) {
-                const int v = e >> 4;
-                tab[e] = make_uint2(
-                    (uint32_t)__half_as_ushort(lv[v & 1]) | ((uint32_t)__half_as_ushort(lv[(v >> 1) & 1]) << 16),
-                    (uint32_t)__half_as_ushort(lv[(v >> 2) & 1]) | ((uint32_t)__half_as_ushort(lv[v >> 3]) << 16));
-            }
-        } else if (kind == 0) {
-            // byte -> four fp16 levels (codes LSB first), 16 copies so that a
-            // half-warp's 8-byte lookups hit distinct banks
-            uint2 *tab = reinterpret_cast<uint2 *>(smem + p.smem_tab);
-            for (int e = threadIdx.x; e < 256 * 16; e += kThreads) {
-                const int v = e >> 4;
-                tab[e] = make_uint2(
-                    (uint32_t)__half_as_ushort(lv[v & 3]) | ((uint32_t)__half_as_ushort(lv[(v >> 2) & 3]) << 16),
-                    (uint32_t)__half_as_ushort(lv[(v >> 4) & 3]) | ((uint32_t)__half_as_ushort(lv[v >> 6]) << 16));
-            }
-        } else {
-            // byte -> two fp16 levels (low nibble first), 32 copies
-            uint32_t *tab = reinterpret_cast<uint32_t *>(smem + p.smem_tab);
-            for (int e = threadIdx.x; e < 256 * 32; e += kThreads) {
-                const int v = e >> 5;
-                tab[e] = (uint32_t)__half_as_ushort(lv[v & 15]) | ((uint32_t)__half_as_ushort(lv[v >> 4]) << 16);
-            }
-        }
-    }
+    // ---- 2. while they land: the level table ----
+    build_level_table(kind, s_lv, smem + p.smem_tab);
 
     // ---- 3. the activation, once the grid before this one on the stream
     // (which may have written it) is complete: warp w rotates groups w, w+8,
     // ... of every batch row into B fragments and 1/sigma ----
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    float xv[kMaxFastB][4];
-    if (warp < ng)
-#pragma unroll
-        for (int b = 0; b < kMaxFastB; ++b)
-            if (b < B) load_x_bg(M, b, warp, lane, xv[b]);
-    {
-        uint32_t(*terms)[kGroup] = reinterpret_cast<uint32_t(*)[kGroup]>(smem + p.smem_terms) + warp * kMaxFastB;
-        for (int g = warp; g < ng; g += kWarps) {
-#pragma unroll
-            for (int b = 0; b < kMaxFastB; ++b) {
-                if (b >= B) break;
-                if (g != warp) load_x_bg(M, b, g, lane, xv[b]);
-                const float inv = rotate_bg(xv[b], lane, terms[b]);
-                if (lane == 0) ginv[b * ng + g] = inv;
-            }
-            __syncwarp();
-            frag_words(M, terms, lane, frag + (size_t)g * 32 * kFragWords);
-            __syncwarp();
-        }
-    }
+    rotate_activation(M, smem + p.smem_terms, frag, ginv);
     asm volatile("cp.async.wait_all;\n" ::: "memory");
     __syncthreads();
 
@@ -459,13 +466,227 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     }
 }
 
+// ------------------------------------------------- wide inputs, streamed --
+// For inputs of 16 to 32 groups: one block per SM walks an equal run of the
+// call's 16-row tiles (runs cross matrix boundaries). Per matrix it meets, it
+// builds the level table (when the codebook changes) and rotates the
+// activation once; then the code rows of each tile stream through three
+// shared-memory stages (16-byte cp.async, two tiles ahead), every warp takes
+// every eighth group of the tile, and the partial sums meet in shared memory.
+constexpr int kStreamMats = 200;
+constexpr int kStreamStages = 3;
+
+struct StreamParams {
+    int n_mats, total_tiles;
+    int tiles_before[kStreamMats + 1];  // first tile of each matrix in the flat order
+    int smem_tab, smem_terms, smem_frag, smem_red, smem_stage, stage_bytes, n_stages;
+    __half lut[kStreamMats][16];
+    FastMat m[kStreamMats];
+};
+
+__global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_constant__ StreamParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ FastMat sM;
+    __shared__ __half s_lv[16];
+    __shared__ float ginv[kMaxFastB * kMaxFastNg];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gq = lane >> 2, t = lane & 3;
+    uint32_t *frag = reinterpret_cast<uint32_t *>(smem + p.smem_frag);
+    float *red = reinterpret_cast<float *>(smem + p.smem_red);  // [kWarps][16 rows][kMaxFastB]
+    const uint2 *tab2 = reinterpret_cast<const uint2 *>(smem + p.smem_tab) + (lane & 15);
+    const uint32_t *tab4 = reinterpret_cast<const uint32_t *>(smem + p.smem_tab) + lane;
+
+    const int T = p.total_tiles, G = gridDim.x, bid = blockIdx.x;
+    const int x_end = (int)(((long long)(bid + 1) * T) / G);
+    int cur_lut = -1;
+    for (int x = (int)(((long long)bid * T) / G); x < x_end;) {
+        int lo = 0, hi = p.n_mats - 1;  // the matrix holding tile x
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.tiles_before[mid] <= x) lo = mid;
+            else hi = mid - 1;
+        }
+        const int mi = lo, seg_end = min(x_end, p.tiles_before[mi + 1]);
+        __syncthreads();  // the previous segment is done with sM, the table, the fragments and the stages
+        if (threadIdx.x < (int)(sizeof(FastMat) / 4))
+            reinterpret_cast<uint32_t *>(&sM)[threadIdx.x] = reinterpret_cast<const uint32_t *>(&p.m[mi])[threadIdx.x];
+        else if (threadIdx.x >= 128 && threadIdx.x < 144)
+            s_lv[threadIdx.x - 128] = p.lut[mi][threadIdx.x - 128];
+        __syncthreads();
+        const FastMat &M = sM;
+        const int ng = M.ng, B = M.B, kind = M.kind, rs = M.row_stride;
+        const int rowBytes = ng * (kind == 0 ? 32 : kind == 1 ? 64 : 16), cpr = rowBytes / 16;
+        const int t0 = x - p.tiles_before[mi], ntile = seg_end - x;  // first tile of the matrix, tiles here
+        if (M.lut != cur_lut) {
+            build_level_table(kind, s_lv, smem + p.smem_tab);
+            cur_lut = M.lut;
+        }
+        rotate_activation(M, smem + p.smem_terms, frag, ginv);
+
+        // copies of the segment's i-th tile into stage i % NS: its code rows
+        // (rows past the matrix zero-filled), then its norms
+        const int NS = p.n_stages;
+        auto issue = [&](int i) {
+            if (i < ntile) {
+                uint8_t *st = smem + p.smem_stage + (i % NS) * p.stage_bytes;
+                const int row0 = 16 * (t0 + i), valid = min(16, M.out - row0);
+                for (int c = threadIdx.x; c < 16 * cpr; c += kThreads) {
+                    const int r = c / cpr, k = c - r * cpr;
+                    const bool ok = r < valid;
+                    cp_async16(st + r * rs + 16 * k, M.codes + (size_t)(ok ? row0 + r : 0) * rowBytes + 16 * k,
+                               ok ? 16 : 0);
+                }
+                const int nbytes = 16 * ng * 2, avail = valid * ng * 2;
+                const uint8_t *src = reinterpret_cast<const uint8_t *>(M.norms + (size_t)row0 * ng);
+                for (int c = threadIdx.x; 16 * c < nbytes; c += kThreads) {
+                    const int left = avail - 16 * c, n = left >= 16 ? 16 : (left > 0 ? left : 0);
+                    cp_async16(st + 16 * rs + 16 * c, n ? src + 16 * c : src, n);
+                }
+            }
+            asm volatile("cp.async.commit_group;\n" ::);
+        };
+        for (int k = 0; k + 1 < NS; ++k) issue(k);
+        const bool live = gq < 2 * B;  // this lane's B column belongs to a batch row
+        for (int i = 0; i < ntile; ++i) {
+            issue(i + NS - 1);
+            // tile i landed (NS - 1 younger groups may still fly); the fragments are complete
+            if (NS == 4) asm volatile("cp.async.wait_group 3;\n" ::: "memory");
+            else asm volatile("cp.async.wait_group 2;\n" ::: "memory");
+            __syncthreads();
+            const uint8_t *sc = smem + p.smem_stage + (i % NS) * p.stage_bytes;
+            const __half *sn = reinterpret_cast<const __half *>(sc + 16 * rs);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int g = warp; g < ng; g += kWarps) {
+                uint32_t fr[kFragWords];
+                const uint4 *fl = reinterpret_cast<const uint4 *>(frag + (size_t)g * 32 * kFragWords) + lane;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 v = live ? fl[32 * k] : make_uint4(0, 0, 0, 0);
+                    fr[4 * k] = v.x, fr[4 * k + 1] = v.y, fr[4 * k + 2] = v.z, fr[4 * k + 3] = v.w;
+                }
+                const float inv = t < B ? ginv[t * ng + g] : 0.0f;
+                const float n0 = __half2float(sn[gq * ng + g]) * inv, n1 = __half2float(sn[(gq + 8) * ng + g]) * inv;
+                if (kind == 2) {
+                    const uint32_t c0 = *reinterpret_cast<const uint32_t *>(sc + gq * rs + g * 16 + 4 * t);
+                    const uint32_t c1 = *reinterpret_cast<const uint32_t *>(sc + (gq + 8) * rs + g * 16 + 4 * t);
+                    lut1_group(acc, c0, c1, tab2, fr, n0, n1);
+                } else if (kind == 0) {
+                    const uint2 c0 = *reinterpret_cast<const uint2 *>(sc + gq * rs + g * 32 + 8 * t);
+                    const uint2 c1 = *reinterpret_cast<const uint2 *>(sc + (gq + 8) * rs + g * 32 + 8 * t);
+                    lut2_group(acc, c0, c1, tab2, fr, n0, n1);
+                } else {
+                    const uint4 c0 = *reinterpret_cast<const uint4 *>(sc + gq * rs + g * 64 + 16 * t);
+                    const uint4 c1 = *reinterpret_cast<const uint4 *>(sc + (gq + 8) * rs + g * 64 + 16 * t);
+                    lut4_group(acc, c0, c1, tab4, fr, n0, n1);
+                }
+            }
+            if (t < B) {  // columns 2t, 2t+1: hi and lo terms of batch row t
+                red[(warp * 16 + gq) * kMaxFastB + t] = acc[0] + acc[1];
+                red[(warp * 16 + gq + 8) * kMaxFastB + t] = acc[2] + acc[3];
+            }
+            __syncthreads();  // partial sums complete; the stage may be refilled
+            if (threadIdx.x < 16 * B) {
+                const int r = threadIdx.x / B, b = threadIdx.x - r * B, row = 16 * (t0 + i) + r;
+                float sum = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) sum += red[(w * 16 + r) * kMaxFastB + b];
+                if (row < M.out) {
+                    const float ab = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[b], kInvSqrt128) : kInvSqrt128;
+                    M.y[(size_t)b * M.out + row] = sum * ab;
+                }
+            }
+        }
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+        x = seg_end;
+    }
+}
+
 }  // namespace
+
+bool gemv_stream_eligible(const cq_gemv_desc &d) {
+    const int ng = in_padded(d.in) / kGroup, W = width_of(d.bits);
+    return d.group == kGroup && d.out > 0 && (W == 1 || W == 2 || W == 4) && d.B <= kMaxFastB && ng >= 16 &&
+           ng <= kMaxFastNg;
+}
+
+int launch_gemv_stream(const cq_gemv_desc *d, const int *idx, int n, void *stream) {
+    static StreamParams p;  // large: keep off the stack
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    for (int base = 0; base < n; base += kStreamMats) {
+        const int cnt = std::min(kStreamMats, n - base);
+        int tiles = 0, ng_max = 0, row_max = 0;
+        for (int j = 0; j < cnt; ++j) {
+            const cq_gemv_desc &D = d[idx[base + j]];
+            const int ip = in_padded(D.in), W = width_of(D.bits), ng = ip / kGroup;
+            FastMat &M = p.m[j];
+            M.codes = D.blob;
+            M.norms = reinterpret_cast<const __half *>(D.blob + (size_t)D.out * ip * W / 8);
+            M.x = D.x;
+            M.xs = D.x_scale;
+            M.y = D.y;
+            M.out = D.out;
+            M.in = D.in;
+            M.ng = ng;
+            M.bits = D.bits;
+            M.xdt = D.x_dtype;
+            M.B = D.B;
+            M.kind = W == 2 ? 0 : W == 4 ? 1 : 2;
+            M.lut = j;  // one table per matrix; rebuilt only when it changes along a block's run
+            M.tiles = M.kchunks = M.item0 = 0;
+            const int rowBytes = ng * (M.kind == 0 ? 32 : M.kind == 1 ? 64 : 16);
+            const int want = M.kind == 0 ? 32 : M.kind == 1 ? 64 : 16;  // see launch_gemv_fast
+            M.row_stride = rowBytes + (((want - rowBytes) % 128) + 128) % 128;
+            float lv[16];
+            level_table(D.bits, D.codebook, lv);
+            for (int k = 0; k < 16; ++k) p.lut[j][k] = __float2half_rn(lv[k]);
+            // the same levels as the previous matrix: keep its table
+            if (j > 0) {
+                bool same = p.m[j - 1].kind == M.kind;
+                for (int k = 0; k < 16; ++k) same &= __half_as_ushort(p.lut[j][k]) == __half_as_ushort(p.lut[j - 1][k]);
+                if (same) M.lut = p.m[j - 1].lut;
+            }
+            p.tiles_before[j] = tiles;
+            tiles += (D.out + 15) / 16;
+            ng_max = std::max(ng_max, ng);
+            row_max = std::max(row_max, M.row_stride);
+        }
+        p.tiles_before[cnt] = tiles;
+        p.n_mats = cnt;
+        p.total_tiles = tiles;
+        size_t off = 0;
+        auto place = [&](int &field, size_t bytes) {
+            field = (int)off;
+            off += (bytes + 15) / 16 * 16;
+        };
+        place(p.smem_tab, 256 * 32 * sizeof(uint32_t));
+        place(p.smem_terms, (size_t)kWarps * kMaxFastB * kGroup * sizeof(uint32_t));
+        place(p.smem_frag, (size_t)ng_max * 32 * kFragWords * sizeof(uint32_t));
+        place(p.smem_red, (size_t)kWarps * 16 * kMaxFastB * sizeof(float));
+        p.stage_bytes = (16 * row_max + 32 * ng_max + 15) / 16 * 16;
+        p.n_stages = kStreamStages;
+        place(p.smem_stage, (size_t)p.n_stages * p.stage_bytes);
+        const size_t smem = off;
+        static size_t attr = 0;  // the dynamic shared memory the kernel may use, raised as needed
+        if (smem > attr) {
+            const cudaError_t ea =
+                cudaFuncSetAttribute(gemv_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (ea != cudaSuccess)
+                return set_error(CQ_ERR_SHAPE, "streamed GEMV needs %zu bytes of shared memory: %s", smem,
+                                 cudaGetErrorString(ea));
+            attr = smem;
+        }
+        const int grid = std::min(tiles, sm_count());
+        gemv_stream_kernel<<<grid, kThreads, smem, st>>>(p);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "streamed gemv launch: %s", cudaGetErrorString(e));
+    }
+    return CQ_OK;
+}
 
 bool gemv_fast_eligible(const cq_gemv_desc &d) {
     const int ng = in_padded(d.in) / kGroup;
     if (d.in <= 0 || d.out <= 0 || d.group != kGroup) return false;
     const int W = width_of(d.bits);
-    return (W == 1 || W == 2 || W == 4) && d.B <= kMaxFastB && ng <= kMaxFastNg;
+    return (W == 1 || W == 2 || W == 4) && d.B <= kMaxFastB && ng <= kMaxFastNg && !gemv_stream_eligible(d);
 }
 
 // Shared-memory needs of one launch (maxima over its matrices).

@@ -60,6 +60,11 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream);
 // takes, and one launch over the descriptors d[idx[0..n)].
 bool gemv_fast_eligible(const cq_gemv_desc &d);
 int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream);
+// Streamed tensor-core GEMV for inputs of 16..32 groups (one block per SM,
+// one activation rotation per block and matrix): which descriptors, and the
+// launches over d[idx[0..n)].
+bool gemv_stream_eligible(const cq_gemv_desc &d);
+int launch_gemv_stream(const cq_gemv_desc *d, const int *idx, int n, void *stream);
 
 
 // --------------------------------------------------------------- gemm --
