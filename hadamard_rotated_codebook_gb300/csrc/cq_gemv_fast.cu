@@ -244,10 +244,10 @@ __device__ __forceinline__ void lut4_group(float (&acc)[4], uint4 cr, uint4 cs, 
 // a byte -> four fp16 levels (16 copies, so that a half-warp's 8-byte lookups
 // hit distinct banks); 4-bit codes a byte -> two levels (32 copies); 1-bit
 // codes a nibble -> four levels (16 copies).
-__device__ void build_level_table(int kind, const __half *lv, uint8_t *tab) {
+__device__ __forceinline__ void build_level_table(int kind, const __half *lv, uint8_t *tab) {
     if (kind == 2) {
         uint2 *t = reinterpret_cast<uint2 *>(tab);
-        for (int e = threadIdx.x; e < 16 * 16; e += blockDim.x) {
+        for (int e = threadIdx.x; e < 16 * 16; e += kThreads) {
             const int v = e >> 4;
             t[e] = make_uint2(
                 (uint32_t)__half_as_ushort(lv[v & 1]) | ((uint32_t)__half_as_ushort(lv[(v >> 1) & 1]) << 16),
@@ -255,7 +255,7 @@ __device__ void build_level_table(int kind, const __half *lv, uint8_t *tab) {
         }
     } else if (kind == 0) {
         uint2 *t = reinterpret_cast<uint2 *>(tab);
-        for (int e = threadIdx.x; e < 256 * 16; e += blockDim.x) {
+        for (int e = threadIdx.x; e < 256 * 16; e += kThreads) {
             const int v = e >> 4;
             t[e] = make_uint2(
                 (uint32_t)__half_as_ushort(lv[v & 3]) | ((uint32_t)__half_as_ushort(lv[(v >> 2) & 3]) << 16),
@@ -263,7 +263,7 @@ __device__ void build_level_table(int kind, const __half *lv, uint8_t *tab) {
         }
     } else {
         uint32_t *t = reinterpret_cast<uint32_t *>(tab);
-        for (int e = threadIdx.x; e < 256 * 32; e += blockDim.x) {
+        for (int e = threadIdx.x; e < 256 * 32; e += kThreads) {
             const int v = e >> 5;
             t[e] = (uint32_t)__half_as_ushort(lv[v & 15]) | ((uint32_t)__half_as_ushort(lv[v >> 4]) << 16);
         }
@@ -273,7 +273,7 @@ __device__ void build_level_table(int kind, const __half *lv, uint8_t *tab) {
 // The activation of M as B fragments: warp w rotates groups w, w+8, ... of
 // every batch row (scratch `terms`: kWarps x kMaxFastB x 128 words) into
 // frag[g] and 1/sigma into ginv[b][g]. No block barrier: the caller syncs.
-__device__ void rotate_activation(const FastMat &M, uint8_t *terms_base, uint32_t *frag, float *ginv) {
+__device__ __forceinline__ void rotate_activation(const FastMat &M, uint8_t *terms_base, uint32_t *frag, float *ginv) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, ng = M.ng, B = M.B;
     float xv[kMaxFastB][4];
     if (warp < ng)  // the first group's values, requested before anything else
