@@ -137,6 +137,7 @@ __device__ __forceinline__ void load_x_bg(const FastMat &A, int b, int g, int la
 // z = H0 x_{b,g} (without the 1/sqrt(128); exact integers for int8 x). Position k is written to terms[k] as fp16
 // hi | lo of sigma * z[k], sigma a power of two per (b, g) (|sigma z| <=
 // 2^14, so hi + lo carries z to ~2^-22 relative); returns 1/sigma.
+template <bool G64 = false>
 __device__ float rotate_bg(float (&v)[4], int lane, uint32_t *terms) {
     float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
     v[0] = a0 + a2;
@@ -144,7 +145,7 @@ __device__ float rotate_bg(float (&v)[4], int lane, uint32_t *terms) {
     v[2] = a0 - a2;
     v[3] = a1 - a3;
 #pragma unroll
-    for (int m = 1; m < 32; m <<= 1)
+    for (int m = 1; m < (G64 ? 16 : 32); m <<= 1)  // groups of 64: positions 0-63 and 64-127 apart
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
@@ -273,6 +274,7 @@ __device__ __forceinline__ void build_level_table(int kind, const __half *lv, ui
 // The activation of M as B fragments: warp w rotates groups w, w+8, ... of
 // every batch row (scratch `terms`: kWarps x kMaxFastB x 128 words) into
 // frag[g] and 1/sigma into ginv[b][g]. No block barrier: the caller syncs.
+template <bool G64 = false>
 __device__ __forceinline__ void rotate_activation(const FastMat &M, uint8_t *terms_base, uint32_t *frag, float *ginv) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, ng = M.ng, B = M.B;
     float xv[kMaxFastB][4];
@@ -286,12 +288,50 @@ __device__ __forceinline__ void rotate_activation(const FastMat &M, uint8_t *ter
         for (int b = 0; b < kMaxFastB; ++b) {
             if (b >= B) break;
             if (g != warp) load_x_bg(M, b, g, lane, xv[b]);
-            const float inv = rotate_bg(xv[b], lane, terms[b]);
+            const float inv = rotate_bg<G64>(xv[b], lane, terms[b]);
             if (lane == 0) ginv[b * ng + g] = inv;
         }
         __syncwarp();
         frag_words(M, terms, lane, frag + (size_t)g * 32 * kFragWords);
         __syncwarp();
+    }
+}
+
+// Groups of 64 (streamed kernel): a lane quarter owns 32 consecutive
+// positions of a 128-span and one MMA sums all four quarters, so the two
+// halves run as separate chains d (quarters 0-1) and e (2-3), each MMA
+// reading the B words of the other half as zero, and take their own norms.
+template <int KIND>
+__device__ __forceinline__ void lut_group64(float (&acc)[4], const uint8_t *rowr, const uint8_t *rows,
+                                            const void *tab, const uint32_t (&fr)[kFragWords], float nr, float ns,
+                                            float hr, float hs) {
+    const int lane = threadIdx.x & 31, t = lane & 3;
+    const bool lo = t < 2;
+    float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int nu = 0; nu < 8; ++nu) {
+        uint32_t a0, a1, a2, a3;
+        if (KIND == 0) {  // 2-bit: byte nu of the lane's 8 bytes
+            const uint2 *tb = static_cast<const uint2 *>(tab) + (lane & 15);
+            const uint2 er = tb[(uint32_t)rowr[8 * t + nu] * 16], es = tb[(uint32_t)rows[8 * t + nu] * 16];
+            a0 = er.x, a1 = es.x, a2 = er.y, a3 = es.y;
+        } else if (KIND == 2) {  // 1-bit: nibble nu of the lane's 4 bytes
+            const uint2 *tb = static_cast<const uint2 *>(tab) + (lane & 15);
+            const uint32_t wr = rowr[4 * t + (nu >> 1)] >> (4 * (nu & 1)), ws = rows[4 * t + (nu >> 1)] >> (4 * (nu & 1));
+            const uint2 er = tb[(wr & 15u) * 16], es = tb[(ws & 15u) * 16];
+            a0 = er.x, a1 = es.x, a2 = er.y, a3 = es.y;
+        } else {  // 4-bit: bytes 2nu, 2nu+1 of the lane's 16 bytes
+            const uint32_t *tb = static_cast<const uint32_t *>(tab) + lane;
+            a0 = tb[(uint32_t)rowr[16 * t + 2 * nu] * 32], a2 = tb[(uint32_t)rowr[16 * t + 2 * nu + 1] * 32];
+            a1 = tb[(uint32_t)rows[16 * t + 2 * nu] * 32], a3 = tb[(uint32_t)rows[16 * t + 2 * nu + 1] * 32];
+        }
+        mma_f16(d, a0, a1, a2, a3, lo ? fr[2 * nu] : 0u, lo ? fr[2 * nu + 1] : 0u);
+        mma_f16(e, a0, a1, a2, a3, lo ? 0u : fr[2 * nu], lo ? 0u : fr[2 * nu + 1]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[i] = fmaf(i >= 2 ? ns : nr, d[i], acc[i]);
+        acc[i] = fmaf(i >= 2 ? hs : hr, e[i], acc[i]);
     }
 }
 
@@ -484,6 +524,8 @@ struct StreamParams {
     FastMat m[kStreamMats];
 };
 
+// G64: groups of 64 (two norms per 128-span and two MMA chains).
+template <bool G64>
 __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_constant__ StreamParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ FastMat sM;
@@ -514,13 +556,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
         __syncthreads();
         const FastMat &M = sM;
         const int ng = M.ng, B = M.B, kind = M.kind, rs = M.row_stride;
+        const int nn = G64 ? 2 * ng : ng;  // norms per row
+        const float gscale = G64 ? 0.125f : kInvSqrt128;  // 1/sqrt(group)
         const int rowBytes = ng * (kind == 0 ? 32 : kind == 1 ? 64 : 16), cpr = rowBytes / 16;
         const int t0 = x - p.tiles_before[mi], ntile = seg_end - x;  // first tile of the matrix, tiles here
         if (M.lut != cur_lut) {
             build_level_table(kind, s_lv, smem + p.smem_tab);
             cur_lut = M.lut;
         }
-        rotate_activation(M, smem + p.smem_terms, frag, ginv);
+        rotate_activation<G64>(M, smem + p.smem_terms, frag, ginv);
 
         // copies of the segment's i-th tile into stage i % NS: its code rows
         // (rows past the matrix zero-filled), then its norms
@@ -535,8 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
                     cp_async16(st + r * rs + 16 * k, M.codes + (size_t)(ok ? row0 + r : 0) * rowBytes + 16 * k,
                                ok ? 16 : 0);
                 }
-                const int nbytes = 16 * ng * 2, avail = valid * ng * 2;
-                const uint8_t *src = reinterpret_cast<const uint8_t *>(M.norms + (size_t)row0 * ng);
+                const int nbytes = 16 * nn * 2, avail = valid * nn * 2;
+                const uint8_t *src = reinterpret_cast<const uint8_t *>(M.norms + (size_t)row0 * nn);
                 for (int c = threadIdx.x; 16 * c < nbytes; c += kThreads) {
                     const int left = avail - 16 * c, n = left >= 16 ? 16 : (left > 0 ? left : 0);
                     cp_async16(st + 16 * rs + 16 * c, n ? src + 16 * c : src, n);
@@ -564,6 +608,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
                     fr[4 * k] = v.x, fr[4 * k + 1] = v.y, fr[4 * k + 2] = v.z, fr[4 * k + 3] = v.w;
                 }
                 const float inv = t < B ? ginv[t * ng + g] : 0.0f;
+                if (G64) {
+                    const float n0 = __half2float(sn[gq * nn + 2 * g]) * inv;
+                    const float n1 = __half2float(sn[(gq + 8) * nn + 2 * g]) * inv;
+                    const float h0 = __half2float(sn[gq * nn + 2 * g + 1]) * inv;
+                    const float h1 = __half2float(sn[(gq + 8) * nn + 2 * g + 1]) * inv;
+                    const int gb = g * (kind == 0 ? 32 : kind == 1 ? 64 : 16);
+                    const uint8_t *r0 = sc + gq * rs + gb, *r1 = sc + (gq + 8) * rs + gb;
+                    const void *tab = smem + p.smem_tab;
+                    if (kind == 2) lut_group64<2>(acc, r0, r1, tab, fr, n0, n1, h0, h1);
+                    else if (kind == 0) lut_group64<0>(acc, r0, r1, tab, fr, n0, n1, h0, h1);
+                    else lut_group64<1>(acc, r0, r1, tab, fr, n0, n1, h0, h1);
+                    continue;
+                }
                 const float n0 = __half2float(sn[gq * ng + g]) * inv, n1 = __half2float(sn[(gq + 8) * ng + g]) * inv;
                 if (kind == 2) {
                     const uint32_t c0 = *reinterpret_cast<const uint32_t *>(sc + gq * rs + g * 16 + 4 * t);
@@ -590,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) sum += red[(w * 16 + r) * kMaxFastB + b];
                 if (row < M.out) {
-                    const float ab = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[b], kInvSqrt128) : kInvSqrt128;
+                    const float ab = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[b], gscale) : gscale;
                     M.y[(size_t)b * M.out + row] = sum * ab;
                 }
             }
@@ -604,11 +661,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
 
 bool gemv_stream_eligible(const cq_gemv_desc &d) {
     const int ng = in_padded(d.in) / kGroup, W = width_of(d.bits);
-    return d.group == kGroup && d.out > 0 && (W == 1 || W == 2 || W == 4) && d.B <= kMaxFastB && ng >= 16 &&
-           ng <= kMaxFastNg;
+    // groups of 64 in whole 128-spans only
+    const bool grp = d.group == kGroup || (d.group == kGroup64 && d.in % kGroup == 0);
+    return grp && d.out > 0 && (W == 1 || W == 2 || W == 4) && d.B <= kMaxFastB && ng >= 16 && ng <= kMaxFastNg;
 }
 
-int launch_gemv_stream(const cq_gemv_desc *d, const int *idx, int n, void *stream) {
+int launch_gemv_stream_g(const cq_gemv_desc *d, const int *idx, int n, bool g64, void *stream);
+
+int launch_gemv_stream(const cq_gemv_desc *d, const int *idx_all, int n_all, void *stream) {
+    // groups of 128 and of 64 go to separate instances
+    int i128[CQ_MAX_GROUPED], i64[CQ_MAX_GROUPED], n128 = 0, n64 = 0;
+    for (int i = 0; i < n_all; ++i) {
+        if (d[idx_all[i]].group == kGroup64) i64[n64++] = idx_all[i];
+        else i128[n128++] = idx_all[i];
+    }
+    for (int pass = 0; pass < 2; ++pass) {
+        const int rc = launch_gemv_stream_g(d, pass ? i64 : i128, pass ? n64 : n128, pass == 1, stream);
+        if (rc) return rc;
+    }
+    return CQ_OK;
+}
+
+int launch_gemv_stream_g(const cq_gemv_desc *d, const int *idx, int n, bool g64, void *stream) {
     static StreamParams p;  // large: keep off the stack
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     for (int base = 0; base < n; base += kStreamMats) {
@@ -661,21 +735,22 @@ int launch_gemv_stream(const cq_gemv_desc *d, const int *idx, int n, void *strea
         place(p.smem_terms, (size_t)kWarps * kMaxFastB * kGroup * sizeof(uint32_t));
         place(p.smem_frag, (size_t)ng_max * 32 * kFragWords * sizeof(uint32_t));
         place(p.smem_red, (size_t)kWarps * 16 * kMaxFastB * sizeof(float));
-        p.stage_bytes = (16 * row_max + 32 * ng_max + 15) / 16 * 16;
+        p.stage_bytes = (16 * row_max + 32 * ng_max * (g64 ? 2 : 1) + 15) / 16 * 16;
         p.n_stages = kStreamStages;
         place(p.smem_stage, (size_t)p.n_stages * p.stage_bytes);
         const size_t smem = off;
-        static size_t attr = 0;  // the dynamic shared memory the kernel may use, raised as needed
-        if (smem > attr) {
-            const cudaError_t ea =
-                cudaFuncSetAttribute(gemv_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        static size_t attr[2] = {0, 0};  // the dynamic shared memory each instance may use, raised as needed
+        if (smem > attr[g64]) {
+            const cudaError_t ea = cudaFuncSetAttribute(g64 ? gemv_stream_kernel<true> : gemv_stream_kernel<false>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (ea != cudaSuccess)
                 return set_error(CQ_ERR_SHAPE, "streamed GEMV needs %zu bytes of shared memory: %s", smem,
                                  cudaGetErrorString(ea));
-            attr = smem;
+            attr[g64] = smem;
         }
         const int grid = std::min(tiles, sm_count());
-        gemv_stream_kernel<<<grid, kThreads, smem, st>>>(p);
+        if (g64) gemv_stream_kernel<true><<<grid, kThreads, smem, st>>>(p);
+        else gemv_stream_kernel<false><<<grid, kThreads, smem, st>>>(p);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "streamed gemv launch: %s", cudaGetErrorString(e));
     }

@@ -144,3 +144,20 @@ def test_gather_out_of_range_group64(C):
     assert np.all(g[1:] == 0)
     ref = O.gather_rows(blob, out, n_in, 2, cb, [1], 64)
     assert np.all(np.abs(g[0] - ref[0]) <= _gather_bound(blob, out, n_in, 2, 64, cb, [1])[0])
+
+
+@pytest.mark.parametrize("group,bits", [(64, 1), (64, 2), (64, 4), (128, 1), (128, 4)])
+@pytest.mark.parametrize("B", [1, 3])
+@pytest.mark.parametrize("shape", [(200, 2048), (37, 4096)])
+def test_gemv_wide_inputs_streamed(C, group, bits, B, shape):
+    """Inputs of 16 to 32 spans of 128 take the streamed tensor-core kernel
+    (one rotation per block and matrix; groups of 64 as two chains per span),
+    ragged row counts included."""
+    out, n_in = shape
+    blob = _rand_blob(out, n_in, bits, group, 98 + out + bits + group + B)
+    cb = O.analytic_codebook(bits, group)
+    x = S.normal((B, n_in), 99 + B)
+    y = C.cq_gemv(torch.from_numpy(blob).cuda(), out, n_in, bits, cb, x.cuda(), group=group)
+    torch.cuda.synchronize()
+    y_ref, bound = O.matmul(O.dequant(blob, out, n_in, bits, cb, group), x.numpy())
+    check_matmul(y.cpu().numpy(), y_ref, bound, f"streamed g{group} cq{bits} B={B} {shape}")
