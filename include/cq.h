@@ -31,11 +31,16 @@
  *    otherwise. cudaMalloc and torch allocations satisfy this.
  *  - Matrices are row-major [out][in], stored pre-transposed as in [CF]
  *    "Five regions": an output row is contiguous along the reduction axis.
- *  - The kernels support group = 128 (the only group size the pages ship);
- *    other powers of two are valid in the format and container and are
- *    rejected by the device entry points with CQ_ERR_SHAPE.
- *  - bits: 2, 3, 4 (CQ2/CQ3/CQ4, 4/8/16 levels) or 5, the ternary marker of
- *    [NJ] "Shared codebooks" (3 levels {-c, 0, +c}, stored as 2-bit crumbs).
+ *  - Groups: cq_encode, cq_gemv* and cq_gather_rows take group 128 (what
+ *    the pages ship) or 64 (which the OpenNeedle engine also tests);
+ *    cq_gemm* and the KV cache take group 128. Other powers of two are valid
+ *    in the format and container and are rejected by the device entry points
+ *    with CQ_ERR_SHAPE.
+ *  - bits: 2, 3, 4 (CQ2/CQ3/CQ4, 4/8/16 levels), 5, the ternary marker of
+ *    [NJ] "Shared codebooks" (3 levels {-c, 0, +c}, stored as 2-bit crumbs),
+ *    or 1, binary codes ([CF] "Cactus Quants": eight per byte, two
+ *    closed-form levels +-sqrt(2/pi)/sqrt(group)). cq_gemm* and the KV cache
+ *    do not take binary codes.
  *  - A codebook is cq_levels(bits) floats, strictly increasing, already
  *    divided by sqrt(group) ([NJ] "Shared codebooks"). For bits = 5 it is
  *    {-c, 0, +c}.
@@ -111,7 +116,7 @@ uint64_t cq_packed_bytes(int out, int in, int group, int bits);
 /* Encode W[out][in] (fp32, device) into one CQ blob (device, exactly
  * cq_packed_bytes(out,in,group,bits) bytes): codes of all rows as an
  * LSB-first bitstream per row, then fp16 norms [out][in_pad/group].
- * Per group of 128 along the input axis ([CF] "Cactus Quants", [ON] CQ
+ * Per group (128 or 64) along the input axis ([CF] "Cactus Quants", [ON] CQ
  * quantisation): zero-pad, rotate by the normalised Walsh-Hadamard matrix
  * (natural Sylvester order), fp32 norm n, direction u = r / max(n, 1e-12),
  * nearest level per coordinate with ties to the smaller index (decided in
@@ -146,7 +151,7 @@ int cq_act_quant_int8(const float *X, int M, int in, int8_t *Xq, float *s,
  * addressing): the kernels then read the activation and write the result
  * across the host link themselves, with no separate copy (on Grace-Blackwell
  * over NVLink-C2C). blob is device memory.
- * Errors: CQ_ERR_ARG, CQ_ERR_SHAPE (group != 128, B out of range),
+ * Errors: CQ_ERR_ARG, CQ_ERR_SHAPE (group other than 64 or 128, B out of range),
  * CQ_ERR_CUDA. */
 int cq_gemv(const uint8_t *blob, int out, int in, int group, int bits,
             const float *codebook, const void *x, int x_dtype,
@@ -272,7 +277,7 @@ int cq_gemm_noalloc(const uint8_t *blob, int out, int in, int group, int bits,
  * device, fully overwritten. n may be 0.
  * An index outside [0, out) yields a row of zeros and marks the device
  * status word, which a following cq_device_status reports as CQ_ERR_INDEX.
- * Errors: CQ_ERR_ARG, CQ_ERR_SHAPE (group != 128), CQ_ERR_CUDA. */
+ * Errors: CQ_ERR_ARG, CQ_ERR_SHAPE (group other than 64 or 128), CQ_ERR_CUDA. */
 int cq_gather_rows(const uint8_t *blob, int out, int in, int group, int bits,
                    const float *codebook, const int32_t *idx, int n,
                    float *dst, void *stream);
