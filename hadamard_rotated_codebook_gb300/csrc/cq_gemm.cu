@@ -1298,7 +1298,7 @@ static void level_table(const cq_gemm_desc &d, float lut[16]) {
 // gemm_x8_kernel (more only when a parameter block fills up). `pdl`: the
 // first launch may overlap the kernel launched just before it.
 static int run_gemm_x8(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws, bool pdl, cudaStream_t st) {
-    static tc2::Params p;
+    static thread_local tc2::Params p;  // large: off the stack, one per host thread
     std::vector<int> map_of(pl.ptr.size(), -1);
     int nmaps = 0, nlut = 0, tiles = 0, runs = 0, ngmax = 0;
     p.n = 0;
@@ -1388,7 +1388,7 @@ static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws
     bool pdl = true;
     // every distinct activation of the wide matrices rotated in one launch
     if (any_wide) {
-        static RotTable rt;
+        static thread_local RotTable rt;  // large: off the stack, one per host thread
         rt.n = 0;
         rt.task_before[0] = 0;
         for (size_t j = 0; j < pl.ptr.size(); ++j) {
@@ -1426,7 +1426,7 @@ static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws
     if (!any_wide) return CQ_OK;
     cudaError_t e;
     for (int W = 2; W <= 4; ++W) {
-        static GemmParams p;
+        static thread_local GemmParams p;  // large: off the stack, one per host thread
         p.n = 0;
         int nlut = 0, tiles = 0;
         for (int i = 0; i < n; ++i) {

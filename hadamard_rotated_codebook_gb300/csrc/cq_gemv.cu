@@ -237,7 +237,7 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
     // One launch per code width present; each launch walks all descriptors of
     // its width (matrices of other widths contribute no items).
     for (int W = 1; W <= 4; ++W) {
-        static GemvParams p;  // large: keep off the stack
+        static thread_local GemvParams p;  // large: off the stack, one per host thread
         p.n = 0;
         int bmax = 0, nlut = 0, items = 0, zfloats = 0;
         for (int i = 0; i < n; ++i) {

@@ -683,7 +683,7 @@ int launch_gemv_stream(const cq_gemv_desc *d, const int *idx_all, int n_all, voi
 }
 
 int launch_gemv_stream_g(const cq_gemv_desc *d, const int *idx, int n, bool g64, void *stream) {
-    static StreamParams p;  // large: keep off the stack
+    static thread_local StreamParams p;  // large: off the stack, one per host thread
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     for (int base = 0; base < n; base += kStreamMats) {
         const int cnt = std::min(kStreamMats, n - base);
@@ -812,7 +812,7 @@ static int flush(FastParams &p, int &nm, int &nlut, Need &need, cudaStream_t st)
 }
 
 int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream) {
-    static FastParams p;
+    static thread_local FastParams p;  // large: off the stack, one per host thread
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     p.n_items = 0;
     int nlut = 0, nm = 0;
