@@ -182,3 +182,26 @@ def test_missing_file_is_io_error(C, tmp_path):
     with pytest.raises(CQError) as ei:
         C.cq_cact_open(str(tmp_path / "nope.cact"))
     assert "CQ_ERR_IO" in str(ei.value)
+
+
+def test_round_trip_binary_and_group64_records(C, tmp_path):
+    """Binary codes (bits 1, eight per byte) and 64-wide groups are valid
+    records ([CF] "Cactus Quants"): the reader checks their byte counts with
+    the same formula and hands back the blobs unchanged; a record whose
+    nbytes disagrees is refused."""
+    rng = np.random.RandomState(2)
+    W = (rng.randn(9, 256) * 0.02).astype(np.float32)
+    b1, _, _ = O.encode(W, 1, O.analytic_codebook(1, 128), 128)
+    b64, _, _ = O.encode(W, 2, O.analytic_codebook(2, 64), 64)
+    assert b1.size == 9 * 256 // 8 + 9 * 2 * 2 and b64.size == 9 * 256 // 4 + 9 * 4 * 2
+    ts = [dict(dtype=3, shape=(9, 256), data=b1.tobytes(), group=128, bits=1),
+          dict(dtype=3, shape=(9, 256), data=b64.tobytes(), group=64, bits=2)]
+    path = str(tmp_path / "g.cact")
+    C.cq_cact_write(path, ts, _codebook28(), 128)
+    with C.cq_cact_open(path) as r:
+        for i, t in enumerate(ts):
+            got = r.tensor(i)
+            assert got.data == t["data"] and got.group == t["group"] and got.bits == t["bits"]
+    bad = [dict(dtype=3, shape=(9, 256), data=b1.tobytes()[:-2], group=128, bits=1)]
+    with pytest.raises(C.CQError):
+        C.cq_cact_write(str(tmp_path / "bad.cact"), bad, _codebook28(), 128)

@@ -161,3 +161,24 @@ def test_gemv_wide_inputs_streamed(C, group, bits, B, shape):
     torch.cuda.synchronize()
     y_ref, bound = O.matmul(O.dequant(blob, out, n_in, bits, cb, group), x.numpy())
     check_matmul(y.cpu().numpy(), y_ref, bound, f"streamed g{group} cq{bits} B={B} {shape}")
+
+
+def test_gemv_more_streamed_matrices_than_one_launch_holds(C):
+    """210 wide matrices (16 rows each, in = 2048; CQ2 and binary at group
+    128 interleaved) in one grouped call: more than one streamed launch
+    holds, so the call is split."""
+    items, refs = [], []
+    x = S.normal((2, 2048), 120)
+    xd = x.cuda()
+    for j in range(210):
+        group, bits = ((128, 2), (128, 1))[j % 2]
+        blob = _rand_blob(16, 2048, bits, group, 2000 + j)
+        cb = O.analytic_codebook(bits, group)
+        items.append(dict(blob=torch.from_numpy(blob).cuda(), out=16, **{"in": 2048}, bits=bits, codebook=cb,
+                          x=xd, group=group))
+        if j % 23 == 0:  # the oracle checks a sample
+            refs.append((j, O.matmul(O.dequant(blob, 16, 2048, bits, cb, group), x.numpy())))
+    ys = C.cq_gemv_grouped(items)
+    torch.cuda.synchronize()
+    for j, (y_ref, bound) in refs:
+        check_matmul(ys[j].cpu().numpy(), y_ref, bound, f"matrix {j}")
