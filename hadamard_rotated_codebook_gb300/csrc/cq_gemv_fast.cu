@@ -60,7 +60,7 @@ struct FastMat {
     const float *xs;
     float *y;
     int out, in, ng, bits, xdt, B;
-    int kind;      // 0: 2-bit codes, 1: 4-bit codes, 2: 1-bit codes
+    int kind;      // 0: 2-bit codes, 1: 4-bit codes, 2: 1-bit codes, 3: 3-bit codes
     int lut;       // index into FastParams::lut
     int tiles;     // row tiles (16 rows) per CTA
     int kchunks;   // warps sharing one tile (split of the groups)
@@ -226,6 +226,38 @@ __device__ __forceinline__ void lut1_group(float (&acc)[4], uint32_t cr, uint32_
     for (int i = 0; i < 4; ++i) acc[i] = fmaf(i >= 2 ? ns : nr, d[i], acc[i]);
 }
 
+// The lane's three code words of a 3-bit row at `p` (12 bytes from 4-byte
+// aligned shared memory), with a zero word after them.
+__device__ __forceinline__ void load3(const uint8_t *p, uint32_t (&w)[4]) {
+    const uint32_t *q = reinterpret_cast<const uint32_t *>(p);
+    w[0] = q[0];
+    w[1] = q[1];
+    w[2] = q[2];
+    w[3] = 0u;
+}
+
+// 3-bit codes: the lane's 12 code bytes of each row (three words) cover
+// positions 32t .. 32t+31; MMA nu takes the 6-bit code pairs at bits 12 nu
+// and 12 nu + 6 of them (a pair may straddle two words), each a lookup of
+// two fp16 levels.
+__device__ __forceinline__ void lut3_group(float (&acc)[4], const uint32_t (&wr)[4], const uint32_t (&ws)[4],
+                                           const uint32_t *tab_lane, const uint32_t (&fr)[kFragWords], float nr,
+                                           float ns) {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int nu = 0; nu < 8; ++nu) {
+        const int b0 = 12 * nu, b1 = b0 + 6;
+        const uint32_t p0 = __funnelshift_r(wr[b0 >> 5], wr[(b0 >> 5) + 1], b0 & 31) & 63u;
+        const uint32_t p1 = __funnelshift_r(wr[b1 >> 5], wr[(b1 >> 5) + 1], b1 & 31) & 63u;
+        const uint32_t q0 = __funnelshift_r(ws[b0 >> 5], ws[(b0 >> 5) + 1], b0 & 31) & 63u;
+        const uint32_t q1 = __funnelshift_r(ws[b1 >> 5], ws[(b1 >> 5) + 1], b1 & 31) & 63u;
+        mma_f16(d, tab_lane[p0 * 32], tab_lane[q0 * 32], tab_lane[p1 * 32], tab_lane[q1 * 32], fr[2 * nu],
+                fr[2 * nu + 1]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = fmaf(i >= 2 ? ns : nr, d[i], acc[i]);
+}
+
 __device__ __forceinline__ void lut4_group(float (&acc)[4], uint4 cr, uint4 cs, const uint32_t *tab_lane,
                                            const uint32_t (&fr)[kFragWords], float nr, float ns) {
     float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -245,8 +277,15 @@ __device__ __forceinline__ void lut4_group(float (&acc)[4], uint4 cr, uint4 cs, 
 // a byte -> four fp16 levels (16 copies, so that a half-warp's 8-byte lookups
 // hit distinct banks); 4-bit codes a byte -> two levels (32 copies); 1-bit
 // codes a nibble -> four levels (16 copies).
+template <bool WITH3 = false>  // 3-bit tables only where the kernel takes 3-bit codes
 __device__ __forceinline__ void build_level_table(int kind, const __half *lv, uint8_t *tab) {
-    if (kind == 2) {
+    if (WITH3 && kind == 3) {  // a 6-bit code pair -> two fp16 levels, 32 copies
+        uint32_t *t = reinterpret_cast<uint32_t *>(tab);
+        for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
+            const int v = e >> 5;
+            t[e] = (uint32_t)__half_as_ushort(lv[v & 7]) | ((uint32_t)__half_as_ushort(lv[v >> 3]) << 16);
+        }
+    } else if (kind == 2) {
         uint2 *t = reinterpret_cast<uint2 *>(tab);
         for (int e = threadIdx.x; e < 16 * 16; e += kThreads) {
             const int v = e >> 4;
@@ -360,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     const int ng = M.ng, B = M.B, kind = M.kind, tiles = M.tiles;
     const int row0 = ((int)blockIdx.x - M.item0) * 16 * tiles;
     const int nrows = 16 * tiles;
-    const int rowBytes = ng * (kind == 0 ? 32 : kind == 1 ? 64 : 16);
+    const int rowBytes = ng * (kind == 0 ? 32 : kind == 1 ? 64 : kind == 3 ? 48 : 16);
     const int rs = M.row_stride;  // padded shared-memory row stride (bytes)
 
     uint8_t *sc = smem + p.smem_codes;                             // [nrows][rs]
@@ -558,10 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
         const int ng = M.ng, B = M.B, kind = M.kind, rs = M.row_stride;
         const int nn = G64 ? 2 * ng : ng;  // norms per row
         const float gscale = G64 ? 0.125f : kInvSqrt128;  // 1/sqrt(group)
-        const int rowBytes = ng * (kind == 0 ? 32 : kind == 1 ? 64 : 16), cpr = rowBytes / 16;
+        const int rowBytes = ng * (kind == 0 ? 32 : kind == 1 ? 64 : kind == 3 ? 48 : 16), cpr = rowBytes / 16;
         const int t0 = x - p.tiles_before[mi], ntile = seg_end - x;  // first tile of the matrix, tiles here
         if (M.lut != cur_lut) {
-            build_level_table(kind, s_lv, smem + p.smem_tab);
+            build_level_table<true>(kind, s_lv, smem + p.smem_tab);
             cur_lut = M.lut;
         }
         rotate_activation<G64>(M, smem + p.smem_terms, frag, ginv);
@@ -613,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
                     const float n1 = __half2float(sn[(gq + 8) * nn + 2 * g]) * inv;
                     const float h0 = __half2float(sn[gq * nn + 2 * g + 1]) * inv;
                     const float h1 = __half2float(sn[(gq + 8) * nn + 2 * g + 1]) * inv;
-                    const int gb = g * (kind == 0 ? 32 : kind == 1 ? 64 : 16);
+                    const int gb = g * (kind == 0 ? 32 : kind == 1 ? 64 : kind == 3 ? 48 : 16);
                     const uint8_t *r0 = sc + gq * rs + gb, *r1 = sc + (gq + 8) * rs + gb;
                     const void *tab = smem + p.smem_tab;
                     if (kind == 2) lut_group64<2>(acc, r0, r1, tab, fr, n0, n1, h0, h1);
@@ -622,7 +661,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
                     continue;
                 }
                 const float n0 = __half2float(sn[gq * ng + g]) * inv, n1 = __half2float(sn[(gq + 8) * ng + g]) * inv;
-                if (kind == 2) {
+                if (kind == 3) {
+                    uint32_t w0[4], w1[4];
+                    load3(sc + gq * rs + g * 48 + 12 * t, w0);
+                    load3(sc + (gq + 8) * rs + g * 48 + 12 * t, w1);
+                    lut3_group(acc, w0, w1, tab4, fr, n0, n1);
+                } else if (kind == 2) {
                     const uint32_t c0 = *reinterpret_cast<const uint32_t *>(sc + gq * rs + g * 16 + 4 * t);
                     const uint32_t c1 = *reinterpret_cast<const uint32_t *>(sc + (gq + 8) * rs + g * 16 + 4 * t);
                     lut1_group(acc, c0, c1, tab2, fr, n0, n1);
@@ -662,8 +706,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
 bool gemv_stream_eligible(const cq_gemv_desc &d) {
     const int ng = in_padded(d.in) / kGroup, W = width_of(d.bits);
     // groups of 64 in whole 128-spans only
-    const bool grp = d.group == kGroup || (d.group == kGroup64 && d.in % kGroup == 0);
-    return grp && d.out > 0 && (W == 1 || W == 2 || W == 4) && d.B <= kMaxFastB && ng >= 16 && ng <= kMaxFastNg;
+    const bool grp = d.group == kGroup || (d.group == kGroup64 && d.in % kGroup == 0 && W != 3);
+    return grp && d.out > 0 && (W >= 1 && W <= 4) && d.B <= kMaxFastB && ng >= 16 && ng <= kMaxFastNg;
 }
 
 int launch_gemv_stream_g(const cq_gemv_desc *d, const int *idx, int n, bool g64, void *stream);
@@ -703,11 +747,11 @@ int launch_gemv_stream_g(const cq_gemv_desc *d, const int *idx, int n, bool g64,
             M.bits = D.bits;
             M.xdt = D.x_dtype;
             M.B = D.B;
-            M.kind = W == 2 ? 0 : W == 4 ? 1 : 2;
+            M.kind = W == 2 ? 0 : W == 4 ? 1 : W == 3 ? 3 : 2;
             M.lut = j;  // one table per matrix; rebuilt only when it changes along a block's run
             M.tiles = M.kchunks = M.item0 = 0;
-            const int rowBytes = ng * (M.kind == 0 ? 32 : M.kind == 1 ? 64 : 16);
-            const int want = M.kind == 0 ? 32 : M.kind == 1 ? 64 : 16;  // see launch_gemv_fast
+            const int rowBytes = ng * (M.kind == 0 ? 32 : M.kind == 1 ? 64 : M.kind == 3 ? 48 : 16);
+            const int want = M.kind == 0 ? 32 : M.kind == 1 ? 64 : M.kind == 3 ? 48 : 16;  // see launch_gemv_fast
             M.row_stride = rowBytes + (((want - rowBytes) % 128) + 128) % 128;
             float lv[16];
             level_table(D.bits, D.codebook, lv);
@@ -761,7 +805,9 @@ bool gemv_fast_eligible(const cq_gemv_desc &d) {
     const int ng = in_padded(d.in) / kGroup;
     if (d.in <= 0 || d.out <= 0 || d.group != kGroup) return false;
     const int W = width_of(d.bits);
-    return (W == 1 || W == 2 || W == 4) && d.B <= kMaxFastB && ng <= kMaxFastNg && !gemv_stream_eligible(d);
+    // 3-bit codes only on the streamed kernel (wide inputs): their product
+    // branch would cost this kernel registers on the decode step
+    return W != 3 && (W >= 1 && W <= 4) && d.B <= kMaxFastB && ng <= kMaxFastNg && !gemv_stream_eligible(d);
 }
 
 // Shared-memory needs of one launch (maxima over its matrices).
@@ -821,10 +867,10 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
     for (int ii = 0; ii < n; ++ii) {
         const cq_gemv_desc &D = d[idx[ii]];
         const int ip = in_padded(D.in), W = width_of(D.bits), ng = ip / kGroup;
-        const int kind = W == 2 ? 0 : W == 4 ? 1 : 2;
+        const int kind = W == 2 ? 0 : W == 4 ? 1 : W == 3 ? 3 : 2;
         // rows per CTA: about 48 KB of codes (96 KB for inputs of 16 groups or
         // more, whose rotation each CTA repeats), a power-of-two number of 16-row tiles
-        const int rowB = ng * (kind == 0 ? 32 : kind == 1 ? 64 : 16) + 2 * ng;
+        const int rowB = ng * (kind == 0 ? 32 : kind == 1 ? 64 : kind == 3 ? 48 : 16) + 2 * ng;
         const int budget = (ng >= 16 ? 96 : 48) * 1024;
         const int tiles = std::max(1, budget / (rowB * 16));
         int tp = 1;
@@ -881,9 +927,11 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
         // row stride in shared memory: the 2-bit path reads 8 bytes per lane
         // (rows of a half-warp must start 8 banks apart), the 4-bit path 16
         // bytes (rows of a quarter-warp 16 banks apart), the 1-bit path 4
-        // bytes (the warp's eight rows 4 banks apart)
-        const int rowBytes = M.ng * (M.kind == 0 ? 32 : M.kind == 1 ? 64 : 16);
-        const int want = M.kind == 0 ? 32 : M.kind == 1 ? 64 : 16;
+        // bytes (the warp's eight rows 4 banks apart), the 3-bit path three
+        // words per lane (stride = 48 mod 128 bytes puts a warp's 32 reads
+        // on 32 banks)
+        const int rowBytes = M.ng * (M.kind == 0 ? 32 : M.kind == 1 ? 64 : M.kind == 3 ? 48 : 16);
+        const int want = M.kind == 0 ? 32 : M.kind == 1 ? 64 : M.kind == 3 ? 48 : 16;
         M.row_stride = rowBytes + (((want - rowBytes) % 128) + 128) % 128;
 
         M.item0 = p.n_items;
