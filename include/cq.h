@@ -138,11 +138,13 @@ int cq_act_quant_int8(const float *X, int M, int in, int8_t *Xq, float *s,
  * which equals W_hat x_b exactly in real arithmetic: the activation is
  * rotated once per group (in-register fast Walsh-Hadamard transform) and the
  * weights are never expanded to a dense matrix ([CF] "How the kernel reads
- * it"). On the tensor-core paths (1-, 2- and 4-bit codes at group 128,
- * B <= 4, in <= 4096; inputs of 2048 or more stream their code rows through
- * one persistent block per SM) the codebook levels are rounded to fp16 and
+ * it"). On the tensor-core paths (B <= 4: 1-, 2- and 4-bit codes at group
+ * 128 with in < 2048; for 2048 <= in <= 4096 every code width at group 128,
+ * and groups of 64 other than 3-bit, through one persistent block per SM
+ * that streams the code rows) the codebook levels are rounded to fp16 and
  * multiplied with z split into fp16 hi + lo terms, accumulating in fp32;
- * other shapes (group 64, 3-bit codes, B > 4) use fp32 arithmetic.
+ * other shapes (B > 4, and the rest of group 64 and 3-bit codes) use fp32
+ * arithmetic.
  * x: fp32 [B][in] (x_dtype = CQ_X_F32, x_scale ignored, may be NULL) or
  *    int8 [B][in] with x_scale fp32 [B] (x_dtype = CQ_X_I8).
  * y: fp32 [B][out], fully overwritten.
