@@ -38,8 +38,10 @@ namespace cq {
 namespace {
 
 constexpr int kEncThreads = 256;
-constexpr int kEncGroupsPerTile = kEncThreads / 2;             // 128 groups
-constexpr int kEncTileFloats = kEncGroupsPerTile * kGroup;     // 16384 floats = 64 KB
+constexpr int kEncWarps = kEncThreads / 32;                    // 8
+constexpr int kEncWarpGroups = 16;                             // groups per warp tile (a thread pair each)
+constexpr int kEncWarpFloats = kEncWarpGroups * kGroup;        // 2048 floats = 8 KB
+constexpr int kEncTileFloats = kEncWarps * kEncWarpFloats;     // 64 KB of staging per CTA
 constexpr float kInvSqrt128 = 0.08838834764831845f;            // 1/sqrt(128)
 
 struct EncodeParams {
@@ -92,19 +94,25 @@ __device__ __forceinline__ int level_index(float u, const float (&T)[16]) {
 
 // BITS: 2, 3, 4 or 5 (ternary). ALIGNED: in % 128 == 0 and W 16-byte aligned,
 // so the groups of the matrix form one contiguous fp32 array.
+//
+// Every warp works on its own: it owns an 8 KB staging buffer and an
+// mbarrier, takes tiles of 16 consecutive groups (one per thread pair) in a
+// grid-stride order, and issues the next tile's copy as soon as its own 32
+// threads hold the current one in registers. No barrier spans more than one
+// warp, so a slow warp delays nobody else's copy.
 template <int BITS, bool ALIGNED>
 __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_constant__ EncodeParams p) {
     constexpr int L = BITS == 5 ? 3 : (1 << BITS);
     constexpr int W = BITS == 5 ? 2 : BITS;  // code width
     extern __shared__ float4 smem4[];
-    float *tile = reinterpret_cast<float *>(smem4);
     __shared__ float s_thr[16];
-    __shared__ __align__(8) uint64_t s_bar;  // aligned rows: the tile's bulk copy
+    __shared__ __align__(8) uint64_t s_bar[kEncWarps];  // aligned rows: each warp's bulk copy
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid < L - 1) s_thr[tid] = decision_threshold(p.cb[tid], p.cb[tid + 1]);
-    if (ALIGNED && tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"((uint32_t)__cvta_generic_to_shared(&s_bar)));
+    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_bar[warp]);
+    if (ALIGNED && lane == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(bar));
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     __syncthreads();
@@ -112,34 +120,35 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
 #pragma unroll
     for (int j = 0; j < 16; ++j) T[j] = j < L - 1 ? s_thr[j] : 0.0f;
 
-    const int pair = tid >> 1, h = tid & 1, f = pair & 3;
-    const long long n_tiles = (p.n_groups + kEncGroupsPerTile - 1) / kEncGroupsPerTile;
+    const int pair = lane >> 1, h = lane & 1, f = pair & 3;
+    float4 *buf = smem4 + warp * (kEncWarpFloats / 4);
+    float *tile = reinterpret_cast<float *>(buf);
+    const long long n_tiles = (p.n_groups + kEncWarpGroups - 1) / kEncWarpGroups;
+    const long long first = (long long)blockIdx.x * kEncWarps + warp;
+    const long long stride = (long long)gridDim.x * kEncWarps;
 
     // Aligned rows: the tile's groups are one contiguous block of W, staged by
-    // one bulk copy (TMA engine) that completes on s_bar; the next tile's
-    // copy is issued as soon as every thread has moved the current tile to
-    // registers, so it streams while that tile is encoded. Groups past the
-    // end of the matrix are not copied (their codes are never stored).
+    // one bulk copy (TMA engine) that completes on the warp's mbarrier.
+    // Groups past the end of the matrix are not copied (their codes are
+    // never stored).
     auto stage = [&](long long tt) {
-        const long long gs = tt * kEncGroupsPerTile;
-        const long long ngrp = p.n_groups - gs < kEncGroupsPerTile ? p.n_groups - gs : kEncGroupsPerTile;
+        const long long gs = tt * kEncWarpGroups;
+        const long long ngrp = p.n_groups - gs < kEncWarpGroups ? p.n_groups - gs : kEncWarpGroups;
         const uint32_t bytes = (uint32_t)ngrp * kGroup * 4;
-        const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_bar);
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
         asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-                         (uint32_t)__cvta_generic_to_shared(smem4)),
+                         (uint32_t)__cvta_generic_to_shared(buf)),
                      "l"(p.W + gs * kGroup), "r"(bytes), "r"(bar)
                      : "memory");
     };
-    if (ALIGNED && tid == 0 && blockIdx.x < n_tiles) stage(blockIdx.x);
+    if (ALIGNED && lane == 0 && first < n_tiles) stage(first);
     uint32_t phase = 0;  // parity of the bulk copy being waited for
 
-    for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-        const long long g0 = t * kEncGroupsPerTile;
-        // ---- stage 128 groups into shared memory (coalesced) ----
+    for (long long t = first; t < n_tiles; t += stride) {
+        const long long g0 = t * kEncWarpGroups;
+        // ---- stage 16 groups into the warp's buffer ----
         if (ALIGNED) {
             // bounded wait for the tile's bulk copy (on expiry the status word records it)
-            const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_bar);
             bool done = false;
             for (unsigned i = 0; i < (1u << 24) && !done; ++i) {
                 uint32_t ok;
@@ -150,10 +159,10 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
                     : "memory");
                 done = ok != 0;
             }
-            if (!done && tid == 0 && p.status) atomicOr(p.status, 0x45430001u);
+            if (!done && lane == 0 && p.status) atomicOr(p.status, 0x45430001u);
             phase ^= 1u;
         } else {
-            for (int i = tid; i < kEncTileFloats; i += kEncThreads) {
+            for (int i = lane; i < kEncWarpFloats; i += 32) {
                 const long long G = g0 + i / kGroup;
                 float v = 0.0f;
                 if (G < p.n_groups) {
@@ -163,13 +172,13 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
                 }
                 tile[i] = v;
             }
-            __syncthreads();
+            __syncwarp();
         }
 
         const long long G = g0 + pair;
         // ---- load my 64 values: register 4j+e = coordinate 8(j^f)+4h+e ----
         float x[64];
-        const float4 *grp = smem4 + pair * (kGroup / 4);
+        const float4 *grp = buf + pair * (kGroup / 4);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             float4 v = grp[2 * (j ^ f) + h];
@@ -178,8 +187,8 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
             x[4 * j + 2] = v.z;
             x[4 * j + 3] = v.w;
         }
-        __syncthreads();  // the tile may be overwritten from here on
-        if (ALIGNED && tid == 0 && t + gridDim.x < n_tiles) stage(t + gridDim.x);
+        __syncwarp();  // the warp's buffer may be overwritten from here on
+        if (ALIGNED && lane == 0 && t + stride < n_tiles) stage(t + stride);
 
         // ---- sum of squares, pairwise in fp32 ----
         float sq[32];
@@ -437,8 +446,9 @@ int launch_encode_t(const EncodeParams &p, cudaStream_t st) {
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
-    const long long tiles = (p.n_groups + kEncGroupsPerTile - 1) / kEncGroupsPerTile;
-    const long long grid = std::min<long long>(tiles, (long long)sm_count() * 2);
+    const long long tiles = (p.n_groups + kEncWarpGroups - 1) / kEncWarpGroups;
+    const long long blocks = (tiles + kEncWarps - 1) / kEncWarps;
+    const long long grid = std::min<long long>(blocks, (long long)sm_count() * 2);
     k<<<(unsigned)grid, kEncThreads, smem, st>>>(p);
     return CQ_OK;
 }
