@@ -176,31 +176,37 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
         }
 
         const long long G = g0 + pair;
-        // ---- load my 64 values: register 4j+e = coordinate 8(j^f)+4h+e ----
+        // ---- load: register 4j+e = coordinate c = 8(j^f)+4h+e after the
+        // butterfly on coordinate bit 2, done here from both halves of the
+        // group (the partner's half a second read of shared memory). The
+        // transform's stages commute, so taking this one first leaves the
+        // result exact up to rounding order. Squares use the original values.
         float x[64];
+        float sq[32];
+        const float sg = h ? -1.0f : 1.0f;  // h = 0: a + b;  h = 1: b - a  (fma by +-1 is exact)
         const float4 *grp = buf + pair * (kGroup / 4);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            float4 v = grp[2 * (j ^ f) + h];
-            x[4 * j + 0] = v.x;
-            x[4 * j + 1] = v.y;
-            x[4 * j + 2] = v.z;
-            x[4 * j + 3] = v.w;
+            const float4 a = grp[2 * (j ^ f) + h];
+            const float4 b = grp[2 * (j ^ f) + (h ^ 1)];
+            sq[2 * j] = __fadd_rn(__fmul_rn(a.x, a.x), __fmul_rn(a.y, a.y));
+            sq[2 * j + 1] = __fadd_rn(__fmul_rn(a.z, a.z), __fmul_rn(a.w, a.w));
+            x[4 * j + 0] = __fmaf_rn(sg, a.x, b.x);
+            x[4 * j + 1] = __fmaf_rn(sg, a.y, b.y);
+            x[4 * j + 2] = __fmaf_rn(sg, a.z, b.z);
+            x[4 * j + 3] = __fmaf_rn(sg, a.w, b.w);
         }
         __syncwarp();  // the warp's buffer may be overwritten from here on
         if (ALIGNED && lane == 0 && t + stride < n_tiles) stage(t + stride);
 
         // ---- sum of squares, pairwise in fp32 ----
-        float sq[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sq[i] = __fadd_rn(__fmul_rn(x[2 * i], x[2 * i]), __fmul_rn(x[2 * i + 1], x[2 * i + 1]));
 #pragma unroll
         for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
             for (int i = 0; i < w; ++i) sq[i] = __fadd_rn(sq[i], sq[i + w]);
         const float s32 = __fadd_rn(sq[0], __shfl_xor_sync(0xffffffffu, sq[0], 1));
 
-        // ---- fast Walsh-Hadamard transform: 6 stages in registers ----
+        // ---- fast Walsh-Hadamard transform: the other 6 stages in registers ----
 #pragma unroll
         for (int bit = 1; bit < 64; bit <<= 1)
 #pragma unroll
@@ -210,12 +216,6 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
                     x[r] = __fadd_rn(a, b);
                     x[r | bit] = __fsub_rn(a, b);
                 }
-        // ... and one across the thread pair (coordinate bit 2)
-#pragma unroll
-        for (int r = 0; r < 64; ++r) {
-            float o = __shfl_xor_sync(0xffffffffu, x[r], 1);
-            x[r] = h ? __fsub_rn(o, x[r]) : __fadd_rn(x[r], o);
-        }
 
         // ---- fp32 group norm, exact fp16 storage ----
         float n32 = __fsqrt_rn(s32);
