@@ -44,7 +44,7 @@ WORKLOAD = ("Needle-shaped decode step, batch 1: 27 x {Q 512x512, K 256x512, V 2
 NCU_TRAFFIC = {
     "gemv_fast": ("75d08df624551252", 9777664),
     "gemm_x8": ("dd123d837be7b655", 527848448),
-    "encode_cq2": ("be9d210c91996f3a", 282315008),
+    "encode_cq2": ("d6aa9d34094c044f", 282315008),
     "gather_cq4": ("5fb8fc86d8fb3ba1", 75002880),
     "kv_attend": ("b470d32ba9762b74", 148856064),
 }

@@ -313,10 +313,181 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(const __grid_con
     }
 }
 
-// ------------------------------------------- group 64 and binary codes --
-// One warp per 128 positions: a group of 128, or two groups of 64 (lanes
-// 0-15 and 16-31, whose transforms stop before the stage that would mix
-// them). Lane l holds coordinates 4l..4l+3. Same steps as encode_kernel:
+// ---------------------------------------------- group 64, one thread each --
+// A group of 64 fits in one thread's registers, so each lane of a warp takes
+// one group of the warp's 32-group (8 KB) tile and keeps the transform, the
+// norm and the packing to itself: no shuffles. Staging as in encode_kernel:
+// a warp-private buffer, filled by one bulk copy on an mbarrier when the
+// rows are 64-aligned. Lane l reads its 16-byte chunks in the order
+// j ^ m, m = l & 7 (the 8 lanes of a quarter-warp then hit 8 different
+// bank groups), so register 4j+e holds coordinate 4(j^m)+e. The transform
+// over the register index then yields, in register s, the rotation's
+// coordinate s times (-1)^popc((s >> 2) & m), since the Sylvester matrix
+// satisfies H[s][c ^ d] = H[s][c] H[s][d].
+template <int BITS, bool ALIGNED>
+__global__ void __launch_bounds__(kEncThreads, 2) encode_g64_kernel(const __grid_constant__ EncodeParams p) {
+    constexpr int L = BITS == 5 ? 3 : (1 << BITS);
+    constexpr int W = BITS == 5 ? 2 : BITS;
+    constexpr int TG = 32;             // groups per warp tile
+    constexpr int TF = TG * kGroup64;  // 2048 floats = 8 KB
+    static_assert(TF == kEncWarpFloats, "warp tile size");
+    extern __shared__ float4 smem4[];
+    __shared__ float s_thr[16];
+    __shared__ __align__(8) uint64_t s_bar[kEncWarps];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < L - 1) s_thr[tid] = decision_threshold(p.cb[tid], p.cb[tid + 1]);
+    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_bar[warp]);
+    if (ALIGNED && lane == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(bar));
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+    float T[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) T[j] = j < L - 1 ? s_thr[j] : 0.0f;
+
+    const int m = lane & 7;
+    float4 *buf = smem4 + warp * (TF / 4);
+    float *tile = reinterpret_cast<float *>(buf);
+    const long long n_tiles = (p.n_groups + TG - 1) / TG;
+    const long long first = (long long)blockIdx.x * kEncWarps + warp;
+    const long long stride = (long long)gridDim.x * kEncWarps;
+
+    auto stage = [&](long long tt) {
+        const long long gs = tt * TG;
+        const long long ngrp = p.n_groups - gs < TG ? p.n_groups - gs : TG;
+        const uint32_t bytes = (uint32_t)ngrp * kGroup64 * 4;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(buf)),
+                     "l"(p.W + gs * kGroup64), "r"(bytes), "r"(bar)
+                     : "memory");
+    };
+    if (ALIGNED && lane == 0 && first < n_tiles) stage(first);
+    uint32_t phase = 0;
+
+    for (long long t = first; t < n_tiles; t += stride) {
+        const long long g0 = t * TG;
+        if (ALIGNED) {
+            bool done = false;
+            for (unsigned i = 0; i < (1u << 24) && !done; ++i) {
+                uint32_t ok;
+                asm volatile(
+                    "{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n selp.u32 %0, 1, 0, q;\n}\n"
+                    : "=r"(ok)
+                    : "r"(bar), "r"(phase)
+                    : "memory");
+                done = ok != 0;
+            }
+            if (!done && lane == 0 && p.status) atomicOr(p.status, 0x45430001u);
+            phase ^= 1u;
+        } else {
+            for (int i = lane; i < TF; i += 32) {
+                const long long Gx = g0 + i / kGroup64;
+                float v = 0.0f;
+                if (Gx < p.n_groups) {
+                    const long long o = Gx / p.ng;
+                    const int col = (int)(Gx - o * p.ng) * kGroup64 + (i % kGroup64);
+                    if (col < p.in) v = __ldcs(p.W + o * p.in + col);
+                }
+                tile[i] = v;
+            }
+            __syncwarp();
+        }
+
+        const long long Gi = g0 + lane;
+        float x[64];
+        float sq[32];
+        const float4 *grp = buf + lane * (kGroup64 / 4);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float4 v = grp[j ^ m];
+            sq[2 * j] = __fadd_rn(__fmul_rn(v.x, v.x), __fmul_rn(v.y, v.y));
+            sq[2 * j + 1] = __fadd_rn(__fmul_rn(v.z, v.z), __fmul_rn(v.w, v.w));
+            x[4 * j + 0] = v.x;
+            x[4 * j + 1] = v.y;
+            x[4 * j + 2] = v.z;
+            x[4 * j + 3] = v.w;
+        }
+        __syncwarp();  // the warp's buffer may be overwritten from here on
+        if (ALIGNED && lane == 0 && t + stride < n_tiles) stage(t + stride);
+
+        // sum of squares, a tree in fp32
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) sq[i] = __fadd_rn(sq[i], sq[i + w]);
+        const float s32 = sq[0];
+
+        // the 6-stage transform in registers
+#pragma unroll
+        for (int bit = 1; bit < 64; bit <<= 1)
+#pragma unroll
+            for (int r = 0; r < 64; ++r)
+                if (!(r & bit)) {
+                    const float a = x[r], b = x[r | bit];
+                    x[r] = __fadd_rn(a, b);
+                    x[r | bit] = __fsub_rn(a, b);
+                }
+
+        // fp32 norm; exact fp64 recount when its fp16 rounding is in doubt
+        float n32 = __fsqrt_rn(s32);
+        bool sure = s32 >= 1e-30f && s32 <= 1e30f;
+        if (sure) {
+            const __half lo = __float2half_rn(__fmul_rn(n32, 1.0f - 5e-7f));
+            const __half hi = __float2half_rn(__fmul_rn(n32, 1.0f + 5e-7f));
+            sure = __half_as_ushort(lo) == __half_as_ushort(hi);
+        }
+        if (!sure && Gi < p.n_groups) {
+            const long long o = Gi / p.ng;
+            const int gcol = (int)(Gi - o * p.ng) * kGroup64;
+            double d = 0.0;
+            for (int c = 0; c < kGroup64; ++c) {
+                const double w = gcol + c < p.in ? (double)p.W[o * p.in + gcol + c] : 0.0;
+                d = __fma_rn(w, w, d);
+            }
+            n32 = __double2float_rn(__dsqrt_rn(d));
+        }
+
+        // codes, LSB-first: coordinate s at bit W*s of the group's stream
+        const float sc = __fdiv_rn(0.125f, fmaxf(n32, 1e-12f));  // 1/sqrt(64) over the norm
+        float scale8[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) scale8[b] = (__popc(b & m) & 1) ? -sc : sc;
+        uint32_t outw[2 * W];
+#pragma unroll
+        for (int k = 0; k < 2 * W; ++k) outw[k] = 0;
+#pragma unroll
+        for (int s = 0; s < 64; ++s) {
+            const float u = __fmul_rn(x[s], scale8[(s >> 2) & 7]);
+            int q = level_index<L>(u, T);
+            if (BITS == 5) q = (q - 1) & 3;  // ternary crumb
+            const int bp = W * s;
+            outw[bp / 32] |= (uint32_t)q << (bp % 32);
+            if (bp % 32 + W > 32) outw[bp / 32 + 1] |= (uint32_t)q >> (32 - bp % 32);
+        }
+        if (Gi < p.n_groups) {
+            uint8_t *dst = p.codes + Gi * (8 * W);
+            if (W % 2 == 0) {
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                for (int k = 0; k < W / 2; ++k)
+                    __stcs(d4 + k, make_uint4(outw[4 * k], outw[4 * k + 1], outw[4 * k + 2], outw[4 * k + 3]));
+            } else {
+                uint2 *d2 = reinterpret_cast<uint2 *>(dst);
+#pragma unroll
+                for (int k = 0; k < W; ++k) __stcs(d2 + k, make_uint2(outw[2 * k], outw[2 * k + 1]));
+            }
+            p.norms[Gi] = __float2half_rn(n32);
+        }
+    }
+}
+
+// ------------------------------------------- binary codes at group 128 --
+// One warp per 128 positions: a group of 128 (binary codes), or two groups
+// of 64 (lanes 0-15 and 16-31, whose transforms stop before the stage that
+// would mix them; groups of 64 normally take encode_g64_kernel). Lane l holds coordinates 4l..4l+3. Same steps as encode_kernel:
 // fp32 sum of squares in a tree (fp64 recount near an fp16 rounding
 // boundary), FWHT, u = r / n, threshold search, LSB-first packing.
 template <int G, int BITS>
@@ -472,6 +643,21 @@ int launch_encode(const float *W, int out, int in, int group, int bits, const fl
     return launch_encode_rows(W, out, in, group, bits, cb, blob, blob + (size_t)out * rowBytes, stream);
 }
 
+template <int BITS, bool ALIGNED>
+void launch_encode_g64(const EncodeParams &p, cudaStream_t st) {
+    const size_t smem = kEncTileFloats * sizeof(float);
+    auto k = encode_g64_kernel<BITS, ALIGNED>;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attr = true;
+    }
+    const long long tiles = (p.n_groups + 31) / 32;  // 32 groups per warp tile
+    const long long blocks = (tiles + kEncWarps - 1) / kEncWarps;
+    const long long grid = std::min<long long>(blocks, (long long)sm_count() * 2);
+    k<<<(unsigned)grid, kEncThreads, smem, st>>>(p);
+}
+
 template <int G, int BITS>
 void launch_encode_warp(const EncodeParams &p, cudaStream_t st) {
     const long long tasks = (p.n_groups + 128 / G - 1) / (128 / G);
@@ -495,12 +681,13 @@ int launch_encode_rows(const float *W, int out, int in, int group, int bits, con
     for (int j = 0; j < kMaxLevels; ++j) p.cb[j] = j < L ? cb[j] : 0.0f;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (group == kGroup64) {
+        const bool aligned = (in % kGroup64 == 0) && !(reinterpret_cast<uintptr_t>(W) & 15);
         switch (bits) {
-        case 1: launch_encode_warp<64, 1>(p, st); break;
-        case 2: launch_encode_warp<64, 2>(p, st); break;
-        case 3: launch_encode_warp<64, 3>(p, st); break;
-        case 4: launch_encode_warp<64, 4>(p, st); break;
-        case 5: launch_encode_warp<64, 5>(p, st); break;
+        case 1: aligned ? launch_encode_g64<1, true>(p, st) : launch_encode_g64<1, false>(p, st); break;
+        case 2: aligned ? launch_encode_g64<2, true>(p, st) : launch_encode_g64<2, false>(p, st); break;
+        case 3: aligned ? launch_encode_g64<3, true>(p, st) : launch_encode_g64<3, false>(p, st); break;
+        case 4: aligned ? launch_encode_g64<4, true>(p, st) : launch_encode_g64<4, false>(p, st); break;
+        case 5: aligned ? launch_encode_g64<5, true>(p, st) : launch_encode_g64<5, false>(p, st); break;
         }
     } else if (bits == 1) {
         launch_encode_warp<128, 1>(p, st);
