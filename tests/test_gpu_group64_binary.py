@@ -29,7 +29,7 @@ def _rand_blob(out, n_in, bits, group, seed):
 
 
 @pytest.mark.parametrize("group,bits", GEOMS)
-@pytest.mark.parametrize("shape", [(512, 512), (3, 65), (33, 200), (1, 1), (130, 1000)])
+@pytest.mark.parametrize("shape", [(512, 512), (3, 65), (33, 200), (1, 1), (130, 1000), (3, 64), (7, 320)])
 def test_encode_parity(C, group, bits, shape):
     W = S.normal(shape, 70 + bits + group, S.W_STD)
     cb = O.analytic_codebook(bits, group)
