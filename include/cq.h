@@ -121,7 +121,10 @@ uint64_t cq_packed_bytes(int out, int in, int group, int bits);
  * (natural Sylvester order), fp32 norm n, direction u = r / max(n, 1e-12),
  * nearest level per coordinate with ties to the smaller index (decided in
  * fp32), fp16(n) stored. Ternary crumbs: 0 -> 00, +c -> 01, -c -> 11.
- * W and blob must not overlap. Errors: CQ_ERR_ARG, CQ_ERR_SHAPE,
+ * W and blob must not overlap. A W that is 16-byte aligned with `in` a
+ * multiple of the group is staged by bulk copies (the fast path; binary
+ * codes at group 128 are always read per thread); any other layout is read
+ * per thread, with the same results. Errors: CQ_ERR_ARG, CQ_ERR_SHAPE,
  * CQ_ERR_CUDA. */
 int cq_encode(const float *W, int out, int in, int group, int bits,
               const float *codebook, uint8_t *blob, void *stream);
