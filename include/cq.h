@@ -82,11 +82,11 @@ int cq_version(void);
 
 /* ------------------------------------------------------------- host -- */
 
-/* Number of codebook levels for `bits` (4, 8, 16; 3 for the ternary
- * marker 5), or -1. */
+/* Number of codebook levels for `bits` (2 for binary codes, bits = 1;
+ * 4, 8, 16 for bits 2-4; 3 for the ternary marker 5), or -1. */
 int cq_levels(int bits);
 
-/* Packed code width in bits per weight (2, 3, 4; 2 for ternary), or -1. */
+/* Packed code width in bits per weight (1, 2, 3, 4; 2 for ternary), or -1. */
 int cq_code_width(int bits);
 
 /* Analytic codebook for `bits` and `group`.
