@@ -69,6 +69,22 @@ def _io_ptr(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
     return t.data_ptr()
 
 
+def _on(device):
+    """Makes `device` current for a library call: the library keeps its
+    per-device state (SM count, status word, workspaces, the fixed scratch
+    array) for the device that is current when it is called."""
+    return torch.cuda.device(device)
+
+
+def _check_blob(blob: torch.Tensor, out: int, n_in: int, group: int, bits: int, name: str = "blob"):
+    """A blob shorter than its geometry would be read past its end on the
+    device, which the C ABI (a bare pointer) cannot see. Invalid geometries
+    (size 0) are left to the library, which reports them."""
+    need = cq_packed_bytes(out, n_in, group, bits)
+    if isinstance(blob, torch.Tensor) and blob.numel() < need:
+        raise ValueError(f"{name} holds {blob.numel()} bytes, the CQ matrix needs {need}")
+
+
 def _codebook_arg(codebook, bits: int):
     cb = np.ascontiguousarray(np.asarray(
         codebook.detach().cpu() if isinstance(codebook, torch.Tensor) else codebook,
@@ -117,8 +133,9 @@ def cq_encode(W: torch.Tensor, bits: int, codebook, group: int = GROUP,
     elif blob.numel() != nbytes:
         raise ValueError(f"blob must hold {nbytes} bytes")
     _, cbp = _codebook_arg(codebook, bits)
-    check(_lib().cq_encode(_dev_ptr(W, torch.float32, "W"), out, n_in, group, bits, cbp,
-                           _dev_ptr(blob, torch.uint8, "blob"), _stream(W.device)))
+    with _on(W.device):
+        check(_lib().cq_encode(_dev_ptr(W, torch.float32, "W"), out, n_in, group, bits, cbp,
+                               _dev_ptr(blob, torch.uint8, "blob"), _stream(W.device)))
     return blob
 
 
@@ -131,9 +148,12 @@ def cq_act_quant_int8(X: torch.Tensor, Xq: Optional[torch.Tensor] = None,
         Xq = torch.empty((M, n_in), dtype=torch.int8, device=X.device)
     if s is None:
         s = torch.empty(M, dtype=torch.float32, device=X.device)
-    check(_lib().cq_act_quant_int8(_dev_ptr(X2, torch.float32, "X"), M, n_in,
-                                   _dev_ptr(Xq, torch.int8, "Xq"), _dev_ptr(s, torch.float32, "s"),
-                                   _stream(X.device)))
+    if tuple(Xq.shape) != (M, n_in) or s.numel() != M:
+        raise ValueError("Xq must be [M, in] and s [M]")
+    with _on(X.device):
+        check(_lib().cq_act_quant_int8(_dev_ptr(X2, torch.float32, "X"), M, n_in,
+                                       _dev_ptr(Xq, torch.int8, "Xq"), _dev_ptr(s, torch.float32, "s"),
+                                       _stream(X.device)))
     return Xq, s
 
 
@@ -148,11 +168,16 @@ def _gemv_desc(blob, out, n_in, bits, codebook, x, x_scale, y, group, keep):
         xdt = CQ_X_I8
         if x_scale is None:
             raise ValueError("int8 activations need x_scale")
+        if x_scale.numel() < B:
+            raise ValueError(f"x_scale has {x_scale.numel()} entries, the batch has {B}")
         xs = _io_ptr(x_scale, torch.float32, "x_scale")
     else:
         raise TypeError("x must be float32 or int8")
     if y is None:
         y = torch.empty((B, out), dtype=torch.float32, device=blob.device)
+    elif y.numel() < B * out:
+        raise ValueError(f"y holds {y.numel()} values, the product has {B * out}")
+    _check_blob(blob, out, n_in, group, bits)
     cb, cbp = _codebook_arg(codebook, bits)
     keep.append(cb)
     d = GemvDesc(blob=_dev_ptr(blob, torch.uint8, "blob"), x=_io_ptr(x2, x2.dtype, "x"),
@@ -168,7 +193,8 @@ def cq_gemv(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook, x: tor
     per-token scales x_scale[B]."""
     keep = []
     d, y = _gemv_desc(blob, out, n_in, bits, codebook, x, x_scale, y, group, keep)
-    check(_lib().cq_gemv_grouped(ctypes.byref(d), 1, _stream(blob.device)))
+    with _on(blob.device):
+        check(_lib().cq_gemv_grouped(ctypes.byref(d), 1, _stream(blob.device)))
     return y
 
 
@@ -184,7 +210,8 @@ def cq_gemv_grouped(items: Sequence[dict]) -> list:
         ds.append(d)
         ys.append(y)
     arr = (GemvDesc * len(ds))(*ds)
-    check(_lib().cq_gemv_grouped(arr, len(ds), _stream(items[0]["blob"].device)))
+    with _on(items[0]["blob"].device):
+        check(_lib().cq_gemv_grouped(arr, len(ds), _stream(items[0]["blob"].device)))
     return ys
 
 
@@ -202,9 +229,12 @@ def cq_gemv_shared(blobs: Sequence[torch.Tensor], outs: Sequence[int], n_in: int
     bp = (ctypes.c_void_p * n)(*[_dev_ptr(b, torch.uint8, "blob") for b in blobs])
     op = (ctypes.c_int * n)(*outs)
     yp = (ctypes.c_void_p * n)(*[y.data_ptr() for y in ys])
+    for b, o in zip(blobs, outs):
+        _check_blob(b, o, n_in, group, bits)
     cb, cbp = _codebook_arg(codebook, bits)
-    check(_lib().cq_gemv_shared(bp, op, n, n_in, group, bits, cbp, d.x, d.x_dtype, d.x_scale, d.B, yp,
-                                _stream(blobs[0].device)))
+    with _on(blobs[0].device):
+        check(_lib().cq_gemv_shared(bp, op, n, n_in, group, bits, cbp, d.x, d.x_dtype, d.x_scale, d.B, yp,
+                                    _stream(blobs[0].device)))
     return ys
 
 
@@ -226,14 +256,27 @@ class GemvPlan:
 
     def run(self, stream: Optional[torch.cuda.Stream] = None):
         st = ctypes.c_void_p((stream or torch.cuda.current_stream(self._device)).cuda_stream)
-        check(_lib().cq_gemv_grouped(self._arr, self._n, st))
+        with _on(self._device):
+            check(_lib().cq_gemv_grouped(self._arr, self._n, st))
         return self.ys
 
 
-def _gemm_desc(blob, out, n_in, bits, codebook, Xq, x_scale, Y, group, keep):
+def _gemm_checks(blob, out, n_in, bits, Xq, x_scale, Y, group):
+    """Sizes the C ABI cannot see: a short blob or scale buffer would be
+    read past its end on the device."""
     if Xq.dim() != 2 or Xq.shape[1] != n_in:
         raise ValueError("Xq must be [M, in]")
     M = Xq.shape[0]
+    if x_scale.numel() != M:
+        raise ValueError(f"x_scale has {x_scale.numel()} entries, Xq has {M} rows")
+    if Y is not None and tuple(Y.shape) != (M, out):
+        raise ValueError(f"Y must be [{M}, {out}]")
+    _check_blob(blob, out, n_in, group, bits)
+    return M
+
+
+def _gemm_desc(blob, out, n_in, bits, codebook, Xq, x_scale, Y, group, keep):
+    M = _gemm_checks(blob, out, n_in, bits, Xq, x_scale, Y, group)
     if Y is None:
         Y = torch.empty((M, out), dtype=torch.float32, device=Xq.device)
     cb, cbp = _codebook_arg(codebook, bits)
@@ -249,7 +292,8 @@ def cq_gemm(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook, Xq: to
     """Y[M, out] = s[m] * W_hat Xq[m] on the tensor cores (int8 per-token activations)."""
     keep = []
     d, Y = _gemm_desc(blob, out, n_in, bits, codebook, Xq, x_scale, Y, group, keep)
-    check(_lib().cq_gemm_grouped(ctypes.byref(d), 1, _stream(Xq.device)))
+    with _on(Xq.device):
+        check(_lib().cq_gemm_grouped(ctypes.byref(d), 1, _stream(Xq.device)))
     return Y
 
 
@@ -260,11 +304,14 @@ def cq_gemm_noalloc(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook
     CQ_GEMM_NOALLOC_MAX_ELEMS = M * in_pad fp16 values). Y must be given.
     Calls share that array, so calls that overlap on the GPU race."""
     cb, cbp = _codebook_arg(codebook, bits)
-    if Xq.dim() != 2 or Xq.shape[1] != n_in or Y.shape != (Xq.shape[0], out):
-        raise ValueError("Xq must be [M, in] and Y [M, out]")
-    check(_lib().cq_gemm_noalloc(_dev_ptr(blob, torch.uint8, "blob"), out, n_in, group, bits, cbp,
-                                 _dev_ptr(Xq, torch.int8, "Xq"), _dev_ptr(x_scale, torch.float32, "x_scale"),
-                                 Xq.shape[0], _dev_ptr(Y, torch.float32, "Y"), _stream(Xq.device)))
+    if Y is None:
+        raise ValueError("cq_gemm_noalloc writes into a caller-owned Y [M, out]")
+    M = _gemm_checks(blob, out, n_in, bits, Xq, x_scale, Y, group)
+    # the library picks the scratch array of the current device
+    with _on(Xq.device):
+        check(_lib().cq_gemm_noalloc(_dev_ptr(blob, torch.uint8, "blob"), out, n_in, group, bits, cbp,
+                                     _dev_ptr(Xq, torch.int8, "Xq"), _dev_ptr(x_scale, torch.float32, "x_scale"),
+                                     M, _dev_ptr(Y, torch.float32, "Y"), _stream(Xq.device)))
     return Y
 
 
@@ -279,7 +326,8 @@ def cq_gemm_grouped(items: Sequence[dict]) -> list:
         ds.append(d)
         Ys.append(Y)
     arr = (GemmDesc * len(ds))(*ds)
-    check(_lib().cq_gemm_grouped(arr, len(ds), _stream(items[0]["Xq"].device)))
+    with _on(items[0]["Xq"].device):
+        check(_lib().cq_gemm_grouped(arr, len(ds), _stream(items[0]["Xq"].device)))
     return Ys
 
 
@@ -295,10 +343,12 @@ def cq_gather_rows(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook,
         dst = torch.empty((n, n_in), dtype=torch.float32, device=idx.device)
     if dst.shape != (n, n_in):
         raise ValueError("dst must be [n, in]")
+    _check_blob(blob, out, n_in, group, bits)
     cb, cbp = _codebook_arg(codebook, bits)
-    check(_lib().cq_gather_rows(_dev_ptr(blob, torch.uint8, "blob"), out, n_in, group, bits, cbp,
-                                _dev_ptr(idx, torch.int32, "idx"), n, _dev_ptr(dst, torch.float32, "dst"),
-                                _stream(idx.device)))
+    with _on(idx.device):
+        check(_lib().cq_gather_rows(_dev_ptr(blob, torch.uint8, "blob"), out, n_in, group, bits, cbp,
+                                    _dev_ptr(idx, torch.int32, "idx"), n, _dev_ptr(dst, torch.float32, "dst"),
+                                    _stream(idx.device)))
     return dst
 
 
@@ -310,10 +360,12 @@ def cq_kv_write(cache: torch.Tensor, cap: int, n_in: int, bits: int, codebook, r
     rows2 = rows if rows.dim() == 2 else rows.reshape(1, -1)
     if rows2.shape[1] != n_in:
         raise ValueError(f"rows have {rows2.shape[1]} columns, cache rows have {n_in}")
+    _check_blob(cache, cap, n_in, GROUP, bits, "cache")
     cb, cbp = _codebook_arg(codebook, bits)
-    check(_lib().cq_kv_write(_dev_ptr(cache, torch.uint8, "cache"), cap, n_in, bits, cbp,
-                             _dev_ptr(rows2, torch.float32, "rows"), t0, rows2.shape[0],
-                             _stream(cache.device)))
+    with _on(cache.device):
+        check(_lib().cq_kv_write(_dev_ptr(cache, torch.uint8, "cache"), cap, n_in, bits, cbp,
+                                 _dev_ptr(rows2, torch.float32, "rows"), t0, rows2.shape[0],
+                                 _stream(cache.device)))
 
 
 def cq_kv_attend(seqs: Sequence[dict], n_q_heads: int, n_kv_heads: int, head_dim_k: int,
@@ -343,14 +395,16 @@ def cq_kv_attend(seqs: Sequence[dict], n_q_heads: int, n_kv_heads: int, head_dim
                        v_cache=_dev_ptr(it["v_cache"], torch.uint8, "v_cache"),
                        q=_dev_ptr(q, torch.float32, "q"), o=_dev_ptr(o, torch.float32, "o"),
                        cap=it["cap"], n_tokens=it["n_tokens"])
-    check(_lib().cq_kv_attend(ctypes.byref(geom), arr, len(seqs), _stream(seqs[0]["q"].device)))
+    with _on(seqs[0]["q"].device):
+        check(_lib().cq_kv_attend(ctypes.byref(geom), arr, len(seqs), _stream(seqs[0]["q"].device)))
     return outs
 
 
 def cq_device_status(device: Optional[torch.device] = None) -> int:
     """Reads and clears the device status word of bounded waits (raises
     CQError(CQ_ERR_TIMEOUT) if one gave up)."""
-    return check(_lib().cq_device_status(_stream(device)))
+    with _on(device if device is not None else torch.cuda.current_device()):
+        return check(_lib().cq_device_status(_stream(device)))
 
 
 # -------------------------------------------------------------- container

@@ -32,6 +32,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "cq_internal.h"
 
 namespace cq {
@@ -612,11 +614,8 @@ template <int BITS, bool ALIGNED>
 int launch_encode_t(const EncodeParams &p, cudaStream_t st) {
     const size_t smem = kEncTileFloats * sizeof(float);
     auto k = encode_kernel<BITS, ALIGNED>;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attr = true;
-    }
+    const int rc = ensure_smem(reinterpret_cast<const void *>(k), smem);
+    if (rc) return rc;
     const long long tiles = (p.n_groups + kEncWarpGroups - 1) / kEncWarpGroups;
     const long long blocks = (tiles + kEncWarps - 1) / kEncWarps;
     const long long grid = std::min<long long>(blocks, (long long)sm_count() * 2);
@@ -627,12 +626,19 @@ int launch_encode_t(const EncodeParams &p, cudaStream_t st) {
 }  // namespace
 
 int sm_count() {
-    static int n = 0;
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 1;
+    }
+    int n = cache[dev].load(std::memory_order_relaxed);
     if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 1;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 1;
+        }
+        cache[dev].store(n, std::memory_order_relaxed);  // every writer stores the same value
     }
     return n;
 }
@@ -644,18 +650,16 @@ int launch_encode(const float *W, int out, int in, int group, int bits, const fl
 }
 
 template <int BITS, bool ALIGNED>
-void launch_encode_g64(const EncodeParams &p, cudaStream_t st) {
+int launch_encode_g64(const EncodeParams &p, cudaStream_t st) {
     const size_t smem = kEncTileFloats * sizeof(float);
     auto k = encode_g64_kernel<BITS, ALIGNED>;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attr = true;
-    }
+    const int rc = ensure_smem(reinterpret_cast<const void *>(k), smem);
+    if (rc) return rc;
     const long long tiles = (p.n_groups + 31) / 32;  // 32 groups per warp tile
     const long long blocks = (tiles + kEncWarps - 1) / kEncWarps;
     const long long grid = std::min<long long>(blocks, (long long)sm_count() * 2);
     k<<<(unsigned)grid, kEncThreads, smem, st>>>(p);
+    return CQ_OK;
 }
 
 template <int G, int BITS>
@@ -680,26 +684,28 @@ int launch_encode_rows(const float *W, int out, int in, int group, int bits, con
     const int L = levels_of(bits);
     for (int j = 0; j < kMaxLevels; ++j) p.cb[j] = j < L ? cb[j] : 0.0f;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int rc = CQ_OK;
     if (group == kGroup64) {
         const bool aligned = (in % kGroup64 == 0) && !(reinterpret_cast<uintptr_t>(W) & 15);
         switch (bits) {
-        case 1: aligned ? launch_encode_g64<1, true>(p, st) : launch_encode_g64<1, false>(p, st); break;
-        case 2: aligned ? launch_encode_g64<2, true>(p, st) : launch_encode_g64<2, false>(p, st); break;
-        case 3: aligned ? launch_encode_g64<3, true>(p, st) : launch_encode_g64<3, false>(p, st); break;
-        case 4: aligned ? launch_encode_g64<4, true>(p, st) : launch_encode_g64<4, false>(p, st); break;
-        case 5: aligned ? launch_encode_g64<5, true>(p, st) : launch_encode_g64<5, false>(p, st); break;
+        case 1: rc = aligned ? launch_encode_g64<1, true>(p, st) : launch_encode_g64<1, false>(p, st); break;
+        case 2: rc = aligned ? launch_encode_g64<2, true>(p, st) : launch_encode_g64<2, false>(p, st); break;
+        case 3: rc = aligned ? launch_encode_g64<3, true>(p, st) : launch_encode_g64<3, false>(p, st); break;
+        case 4: rc = aligned ? launch_encode_g64<4, true>(p, st) : launch_encode_g64<4, false>(p, st); break;
+        case 5: rc = aligned ? launch_encode_g64<5, true>(p, st) : launch_encode_g64<5, false>(p, st); break;
         }
     } else if (bits == 1) {
         launch_encode_warp<128, 1>(p, st);
     } else {
         const bool aligned = (in % kGroup == 0) && !(reinterpret_cast<uintptr_t>(W) & 15);
         switch (bits) {
-        case 2: aligned ? launch_encode_t<2, true>(p, st) : launch_encode_t<2, false>(p, st); break;
-        case 3: aligned ? launch_encode_t<3, true>(p, st) : launch_encode_t<3, false>(p, st); break;
-        case 4: aligned ? launch_encode_t<4, true>(p, st) : launch_encode_t<4, false>(p, st); break;
-        case 5: aligned ? launch_encode_t<5, true>(p, st) : launch_encode_t<5, false>(p, st); break;
+        case 2: rc = aligned ? launch_encode_t<2, true>(p, st) : launch_encode_t<2, false>(p, st); break;
+        case 3: rc = aligned ? launch_encode_t<3, true>(p, st) : launch_encode_t<3, false>(p, st); break;
+        case 4: rc = aligned ? launch_encode_t<4, true>(p, st) : launch_encode_t<4, false>(p, st); break;
+        case 5: rc = aligned ? launch_encode_t<5, true>(p, st) : launch_encode_t<5, false>(p, st); break;
         }
     }
+    if (rc) return rc;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "encode launch: %s", cudaGetErrorString(e));
     return CQ_OK;

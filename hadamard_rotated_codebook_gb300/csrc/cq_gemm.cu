@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <vector>
@@ -31,21 +32,46 @@ namespace cq {
 static __device__ unsigned int g_cq_device_status = 0;
 
 unsigned int *device_status_ptr() {
-    static unsigned int *ptr[64];
+    // one slot per device; threads that race on an empty slot all store the
+    // same address, and the slots are atomic so that the race is defined
+    static std::atomic<unsigned int *> ptr[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         cudaGetLastError();
         return nullptr;
     }
-    if (!ptr[dev]) {
+    unsigned int *q = ptr[dev].load(std::memory_order_acquire);
+    if (!q) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_cq_device_status) != cudaSuccess) {
             cudaGetLastError();
             return nullptr;
         }
-        ptr[dev] = static_cast<unsigned int *>(p);
+        q = static_cast<unsigned int *>(p);
+        ptr[dev].store(q, std::memory_order_release);
     }
-    return ptr[dev];
+    return q;
+}
+
+int ensure_smem(const void *func, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, size_t> raised;  // (kernel, device) -> bytes allowed
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(CQ_ERR_CUDA, "no current CUDA device: %s", cudaGetErrorString(e));
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    size_t &have = raised[{func, dev}];
+    if (have >= bytes) return CQ_OK;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(CQ_ERR_SHAPE, "kernel needs %zu bytes of shared memory: %s", bytes, cudaGetErrorString(e));
+    }
+    have = bytes;
+    return CQ_OK;
 }
 
 int read_and_clear_device_status(void *stream) {
@@ -456,13 +482,11 @@ __global__ void __launch_bounds__(tc::kThreads, 1) gemm_tc_kernel(const __grid_c
 }
 
 template <int W>
-void launch_tc(const GemmParams &p, int grid, size_t smem, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(gemm_tc_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attr = true;
-    }
+int launch_tc(const GemmParams &p, int grid, size_t smem, cudaStream_t st) {
+    const int rc = ensure_smem(reinterpret_cast<const void *>(gemm_tc_kernel<W>), smem);
+    if (rc) return rc;
     gemm_tc_kernel<W><<<grid, tc::kThreads, smem, st>>>(p);
+    return CQ_OK;
 }
 
 // ------------------------------- pipelined GEMM for inputs up to 512 wide --
@@ -1099,13 +1123,8 @@ __global__ void __launch_bounds__(tc3::kThreads, 1) gemm_x8_kernel(const __grid_
 // this library's that triggers early; only the TMA producer then waits for
 // it, so every other input must be complete when that kernel started).
 int launch_x8(const tc2::Params &p, int grid, bool pdl, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(gemm_x8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc3::kSmem);
-        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm smem attribute: %s", cudaGetErrorString(e));
-        attr = true;
-    }
+    const int rc = ensure_smem(reinterpret_cast<const void *>(gemm_x8_kernel), tc3::kSmem);
+    if (rc) return rc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(tc3::kThreads);
@@ -1471,11 +1490,13 @@ static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws
         p.total_tiles = tiles;
         const size_t smem = 2 * tc::kOpBytes + 1024;
         const int grid = std::min(tiles, sm_count() * 2);
+        int rc = CQ_OK;
         switch (W) {
-        case 2: launch_tc<2>(p, grid, smem, st); break;
-        case 3: launch_tc<3>(p, grid, smem, st); break;
-        case 4: launch_tc<4>(p, grid, smem, st); break;
+        case 2: rc = launch_tc<2>(p, grid, smem, st); break;
+        case 3: rc = launch_tc<3>(p, grid, smem, st); break;
+        case 4: rc = launch_tc<4>(p, grid, smem, st); break;
         }
+        if (rc) return rc;
         e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
     }
@@ -1495,8 +1516,10 @@ static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws
 static __device__ __align__(256) __half g_noalloc_scratch[CQ_GEMM_NOALLOC_MAX_ELEMS];
 
 // Device address of the array, looked up once per device (host code cannot
-// use the array's name as a device pointer).
-static void *g_noalloc_ptr[64];
+// use the array's name as a device pointer). Host threads that race on an
+// empty slot all store the same address; the slots are atomic so that the
+// race is a defined one.
+static std::atomic<void *> g_noalloc_ptr[64];
 
 }  // namespace cq
 
@@ -1551,19 +1574,19 @@ extern "C" int cq_gemm_noalloc(const uint8_t *blob, int out, int in, int group, 
         cudaGetLastError();
         return set_error(CQ_ERR_CUDA, "cq_gemm_noalloc: no current CUDA device");
     }
-    if (!g_noalloc_ptr[dev]) {
-        void *ptr = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess || !ptr) {
+    void *scratch = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (!scratch) {
+        const cudaError_t e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+        if (e != cudaSuccess || !scratch) {
             cudaGetLastError();
             return set_error(CQ_ERR_CUDA, "cq_gemm_noalloc: cannot resolve the scratch array: %s",
                              cudaGetErrorString(e));
         }
-        g_noalloc_ptr[dev] = ptr;
+        g_noalloc_ptr[dev].store(scratch, std::memory_order_release);
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     ActPlan pl;
     plan_activations(&d, 1, s, pl);
     if (pl.ptr.empty()) return CQ_OK;
-    return run_gemm(&d, 1, pl, static_cast<uint8_t *>(g_noalloc_ptr[dev]), s);
+    return run_gemm(&d, 1, pl, static_cast<uint8_t *>(scratch), s);
 }

@@ -193,22 +193,20 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const __grid_constan
 }
 
 template <int W, int BMAX>
-void launch_w(const GemvParams &p, size_t smem, int grid, cudaStream_t st) {
+int launch_w(const GemvParams &p, size_t smem, int grid, cudaStream_t st) {
     auto k = gemv_kernel<W, BMAX>;
-    static int attr_set = 0;  // raise the dynamic shared memory cap once
-    if (!attr_set) {
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024 + 4096);
-        attr_set = 1;
-    }
+    const int rc = ensure_smem(reinterpret_cast<const void *>(k), 64 * 1024 + 4096);
+    if (rc) return rc;
     k<<<grid, kGemvThreads, smem, st>>>(p);
+    return CQ_OK;
 }
 
 template <int W>
-void launch_b(int bmax, const GemvParams &p, size_t smem, int grid, cudaStream_t st) {
-    if (bmax <= 1) launch_w<W, 1>(p, smem, grid, st);
-    else if (bmax <= 4) launch_w<W, 4>(p, smem, grid, st);
-    else if (bmax <= 8) launch_w<W, 8>(p, smem, grid, st);
-    else launch_w<W, 16>(p, smem, grid, st);
+int launch_b(int bmax, const GemvParams &p, size_t smem, int grid, cudaStream_t st) {
+    if (bmax <= 1) return launch_w<W, 1>(p, smem, grid, st);
+    if (bmax <= 4) return launch_w<W, 4>(p, smem, grid, st);
+    if (bmax <= 8) return launch_w<W, 8>(p, smem, grid, st);
+    return launch_w<W, 16>(p, smem, grid, st);
 }
 
 }  // namespace
@@ -296,12 +294,14 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
         p.zfloats = zfloats;
         const size_t smem = sizeof(float) * (zfloats + kRowsPerItem * 16);
         const int grid = std::min(items, sm_count() * 8);
+        int rc = CQ_OK;
         switch (W) {
-        case 1: launch_b<1>(bmax, p, smem, grid, st); break;
-        case 2: launch_b<2>(bmax, p, smem, grid, st); break;
-        case 3: launch_b<3>(bmax, p, smem, grid, st); break;
-        case 4: launch_b<4>(bmax, p, smem, grid, st); break;
+        case 1: rc = launch_b<1>(bmax, p, smem, grid, st); break;
+        case 2: rc = launch_b<2>(bmax, p, smem, grid, st); break;
+        case 3: rc = launch_b<3>(bmax, p, smem, grid, st); break;
+        case 4: rc = launch_b<4>(bmax, p, smem, grid, st); break;
         }
+        if (rc) return rc;
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "gemv launch: %s", cudaGetErrorString(e));
     }

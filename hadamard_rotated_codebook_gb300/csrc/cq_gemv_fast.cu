@@ -783,14 +783,11 @@ int launch_gemv_stream_g(const cq_gemv_desc *d, const int *idx, int n, bool g64,
         p.n_stages = kStreamStages;
         place(p.smem_stage, (size_t)p.n_stages * p.stage_bytes);
         const size_t smem = off;
-        static size_t attr[2] = {0, 0};  // the dynamic shared memory each instance may use, raised as needed
-        if (smem > attr[g64]) {
-            const cudaError_t ea = cudaFuncSetAttribute(g64 ? gemv_stream_kernel<true> : gemv_stream_kernel<false>,
-                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (ea != cudaSuccess)
-                return set_error(CQ_ERR_SHAPE, "streamed GEMV needs %zu bytes of shared memory: %s", smem,
-                                 cudaGetErrorString(ea));
-            attr[g64] = smem;
+        {
+            const int rc = ensure_smem(g64 ? reinterpret_cast<const void *>(gemv_stream_kernel<true>)
+                                           : reinterpret_cast<const void *>(gemv_stream_kernel<false>),
+                                       smem);
+            if (rc) return rc;
         }
         const int grid = std::min(tiles, sm_count());
         if (g64) gemv_stream_kernel<true><<<grid, kThreads, smem, st>>>(p);
@@ -831,12 +828,11 @@ static int flush(FastParams &p, int &nm, int &nlut, Need &need, cudaStream_t st)
     place(p.smem_terms, (size_t)kWarps * kMaxFastB * kGroup * sizeof(uint32_t));  // rotation scratch: 16 KB
     const size_t smem = off;
     p.n_mats = nm;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(gemv_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        attr = true;
-    }
     if (smem > 200 * 1024) return set_error(CQ_ERR_SHAPE, "fast GEMV needs %zu bytes of shared memory", smem);
+    {
+        const int rc = ensure_smem(reinterpret_cast<const void *>(gemv_fast_kernel), 200 * 1024);
+        if (rc) return rc;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.n_items);
     cfg.blockDim = dim3(kThreads);

@@ -72,8 +72,13 @@ int launch_gemm_grouped(const cq_gemm_desc *d, int n, void *stream);
 // Argument checks of one GEMM descriptor (as cq_gemm does them).
 int check_gemm_args(const cq_gemm_desc &d);
 
-// Number of SMs of the current device (cached).
+// Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Raises the dynamic shared-memory limit of kernel `func` to at least
+// `bytes` on the current device. The attribute belongs to the device, so it
+// is tracked per (kernel, device) and set under a lock; CQ_OK or CQ_ERR_CUDA.
+int ensure_smem(const void *func, size_t bytes);
 
 // Device scratch of at least `bytes` for work queued on `stream`; `kind`
 // selects an independent buffer (0: GEMM rotated or padded activations).

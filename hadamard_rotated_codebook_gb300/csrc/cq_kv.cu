@@ -936,12 +936,8 @@ __global__ void __launch_bounds__(kThreads, 2) kv_attend_warp_kernel(const __gri
 template <int WK, int WV>
 int occupancy_t(int smem) {
     auto k = kv_attend_kernel<WK, WV>;
-    static int attr = 0;
-    if (smem > attr) {
-        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention attribute: %s", cudaGetErrorString(e));
-        attr = smem;
-    }
+    const int rc = ensure_smem(reinterpret_cast<const void *>(k), smem);
+    if (rc) return rc;
     int nb = 0;
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k, kThreads, smem);
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention occupancy: %s", cudaGetErrorString(e));
@@ -963,13 +959,8 @@ int dispatch_t(bool occ, const KvParams &p, int grid, int smem, cudaStream_t st)
 // Resident blocks per SM of the warp-autonomous kernel at `smem` bytes.
 template <int NTK>
 int occupancy_warp_t(int smem) {
-    static int attr = 0;
-    if (smem > attr) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(kv_attend_warp_kernel<NTK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention attribute: %s", cudaGetErrorString(e));
-        attr = smem;
-    }
+    const int rc = ensure_smem(reinterpret_cast<const void *>(kv_attend_warp_kernel<NTK>), smem);
+    if (rc) return rc;
     int nb = 0;
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kv_attend_warp_kernel<NTK>, kThreads, smem);
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "kv attention occupancy: %s", cudaGetErrorString(e));

@@ -104,8 +104,30 @@ def decode_activation(a: int, tokens: int = 1, n_in: int = 512, device="cpu") ->
 
 SWEEP_SHAPES = [(4096, 4096), (14336, 4096)]
 SWEEP_BITS = [2, 3, 4, 5]
+SWEEP_BATCHES = [1, 16]
 ENCODE_SHAPE = (8192, 8192)
 ENCODE_COUNT = 16
+
+
+def single_weights(device="cpu") -> torch.Tensor:
+    """The single 512x512 CQ2 matrix: N(0, 0.02^2), seed 0."""
+    return normal((512, 512), 0, W_STD, device)
+
+
+def single_activation(device="cpu") -> torch.Tensor:
+    """Its batch-1 activation: N(0, 1), seed 1."""
+    return normal((1, 512), 1, 1.0, device)
+
+
+def sweep_weights(shape, bits: int, device="cpu") -> torch.Tensor:
+    """Width-sweep weights: 0.02 * Student t (4 dof), one seed per shape and width."""
+    seed = 3000 + 10 * SWEEP_SHAPES.index(tuple(shape)) + SWEEP_BITS.index(bits)
+    return student_t4(tuple(shape), seed, W_STD, device)
+
+
+def sweep_activation(B: int, n_in: int, device="cpu") -> torch.Tensor:
+    """Width-sweep activations: fp32 N(0, 1), [B, n_in]."""
+    return normal((B, n_in), 3500 + B, 1.0, device)
 
 
 def encode_matrix(i: int, device="cpu", shape=ENCODE_SHAPE) -> torch.Tensor:

@@ -1,4 +1,7 @@
-"""Shared helpers of the GPU parity tests (comparison rules only)."""
+"""Shared helpers of the GPU parity tests (comparison rules only). The
+benchmark's oracle leg reuses the same rules for its parity statistics."""
+import math
+
 import numpy as np
 
 import oracle as O
@@ -53,11 +56,14 @@ def attention_bound(Kh, Vh, q, P, o_ref, n_kv_heads, scale):
     cache), so it may be off by d_t = scale * 2e-3 * sum_i |k_t,i||q_i|; with
     d = max_t d_t every softmax weight moves by a factor within e^(+-2d), so
     o moves by at most (e^(2d) - 1) * sum_t p_t |v_t - o|. The value sum is a
-    product over CQ weights taken in the rotated domain, which bounds its
-    error by 2e-3 * sum_t p_t ||v_t||_2 in every coordinate."""
+    product over CQ weights taken in the rotated domain, group by group,
+    which bounds its error in a coordinate of group g by
+    2e-3 * sum_t p_t ||v_t,g||_2 (the 2-norm of row t's group g)."""
     Hq, dk = q.shape
     per = Hq // n_kv_heads
     dv = Vh.shape[1] // n_kv_heads
+    ng = (Vh.shape[1] + 127) // 128
+    gnorm = [np.linalg.norm(Vh[:, 128 * g:128 * (g + 1)], axis=1) for g in range(ng)]  # [T] each
     bound = np.zeros_like(o_ref)
     for b in range(Hq):
         h = b // per
@@ -66,8 +72,9 @@ def attention_bound(Kh, Vh, q, P, o_ref, n_kv_heads, scale):
         kh, vh = Kh[:, h * dk:(h + 1) * dk], Vh[:, h * dv:(h + 1) * dv]
         d = scale * MATMUL_TOL * float((np.abs(kh) @ np.abs(q[b])).max())
         spread = P[b] @ np.abs(vh - o_ref[b])
-        vnorm = float(P[b] @ np.linalg.norm(Vh, axis=1))
-        bound[b] = np.expm1(2 * d) * spread + MATMUL_TOL * vnorm
+        gsum = np.array([float(P[b] @ gnorm[g]) for g in range(ng)])
+        cols = (h * dv + np.arange(dv)) // 128  # the group of each of the head's columns
+        bound[b] = np.expm1(2 * d) * spread + MATMUL_TOL * gsum[cols]
     return bound
 
 
@@ -84,3 +91,22 @@ def check_attention(o, o_ref, bound, what=""):
         cos = float(np.dot(o[b], o_ref[b]) / (no * nr))
         assert cos >= COS_MIN, f"{what}: cosine {cos:.8f} in head {b}"
     return worst
+
+
+def gather_bound(blob, out, n_in, bits, cb, rows):
+    """Per-element bound of the row gather's fp32 arithmetic: the 128-point
+    transform adds seven rounded stages over values bounded by sum|c[q]|,
+    then one rounded scaling by n/sqrt(128): |err| <= 1e-6 * n/sqrt(128) *
+    sum_k |c[q_k]| per group (a factor ~16 above 8 * 2^-24)."""
+    codes, norms = O.unpack(blob, out, n_in, bits)
+    lv = np.zeros(16)
+    if bits == 5:
+        c = float(cb[2])
+        lv[1], lv[2], lv[3] = c, -2.0 * c, -c
+    else:
+        lv[:len(cb)] = np.asarray(cb, dtype=np.float64)
+    n = O.f16_bits_to_f32(norms).astype(np.float64).reshape(norms.shape)
+    ng = codes.shape[1] // 128
+    s = np.abs(lv[codes]).reshape(out, ng, 128).sum(axis=2) * n / math.sqrt(128)  # [out][ng]
+    b = np.repeat(s, 128, axis=1)[:, :n_in]
+    return 1e-6 * b[rows] + 1e-30

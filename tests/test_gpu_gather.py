@@ -8,6 +8,7 @@ import torch
 
 import oracle as O
 import synthetic as S
+from tests.gpu_helpers import gather_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -24,22 +25,7 @@ def _rand_blob(out, n_in, bits, seed):
 
 
 def _bound(blob, out, n_in, bits, cb, rows):
-    """Per-element bound of fp32 arithmetic: the 128-point transform adds
-    seven rounded stages over values bounded by sum|c[q]|, then one rounded
-    scaling by n/sqrt(128): |err| <= 1e-6 * n/sqrt(128) * sum_k |c[q_k]| per
-    group (a factor ~16 above 8 * 2^-24)."""
-    codes, norms = O.unpack(blob, out, n_in, bits)
-    lv = np.zeros(16)
-    if bits == 5:
-        c = float(cb[2])
-        lv[1], lv[2], lv[3] = c, -2.0 * c, -c
-    else:
-        lv[:len(cb)] = np.asarray(cb, dtype=np.float64)
-    n = O.f16_bits_to_f32(norms).astype(np.float64).reshape(norms.shape)
-    ng = codes.shape[1] // 128
-    s = np.abs(lv[codes]).reshape(out, ng, 128).sum(axis=2) * n / math.sqrt(128)  # [out][ng]
-    b = np.repeat(s, 128, axis=1)[:, :n_in]
-    return 1e-6 * b[rows] + 1e-30
+    return gather_bound(blob, out, n_in, bits, cb, rows)
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 5])
