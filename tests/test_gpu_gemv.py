@@ -228,3 +228,38 @@ def test_gemv_host_resident_activations_and_outputs(C, B):
     C.cq_gemv(blob, out, n_in, bits, cb, xq_h, xs_h, y=y_h)
     torch.cuda.synchronize()
     assert torch.equal(y_h, y_d.cpu())
+
+
+def test_gemv_grouped_mixed_widths_activations_and_batches(C):
+    """One grouped call over many small matrices of every tensor-core width
+    (CQ2, ternary, CQ4, binary), inputs of 1 to 12 groups, batches 1 to 4,
+    fp32 and int8 activations, some shared between consecutive matrices:
+    the launch cuts these into runs that cross matrix, activation and width
+    boundaries. Every output is checked against the oracle."""
+    rng = np.random.RandomState(41)
+    items, refs = [], []
+    x_prev = None
+    for i in range(60):
+        bits = [2, 5, 4, 1][i % 4] if i < 40 else 2
+        n_in = int(rng.choice([128, 200, 384, 512, 1000, 1536]))
+        out = int(rng.choice([1, 16, 40, 129, 256, 300]))
+        B = int(rng.choice([1, 2, 3, 4]))
+        if x_prev is not None and x_prev[0].shape[1] == n_in and rng.rand() < 0.5:
+            x, xs, xt = x_prev  # shares the previous matrix's activation
+        elif rng.rand() < 0.5:
+            xf = S.normal((B, n_in), 600 + i)
+            x, xs, xt = xf.cuda(), None, xf.numpy().astype(np.float64)
+        else:
+            q, s = O.act_quant_int8(S.normal((B, n_in), 600 + i).numpy())
+            x, xs = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+            xt = q.astype(np.float64) * s.astype(np.float64)[:, None]
+        x_prev = (x, xs, xt)
+        cb = O.analytic_codebook(bits)
+        blob = _rand_blob(out, n_in, bits, 650 + i)
+        items.append(dict(blob=torch.from_numpy(blob).cuda(), out=out, **{"in": n_in}, bits=bits, codebook=cb, x=x,
+                          x_scale=xs))
+        refs.append(_oracle_y(blob, out, n_in, bits, cb, xt))
+    ys = C.cq_gemv_grouped(items)
+    torch.cuda.synchronize()
+    for i, (y, (y_ref, bound)) in enumerate(zip(ys, refs)):
+        check_matmul(y.cpu().numpy(), y_ref, bound, f"item {i}")
