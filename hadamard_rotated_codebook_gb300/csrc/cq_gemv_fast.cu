@@ -1,24 +1,38 @@
-// cq_gemv_fast.cu -- tensor-core GEMV over CQ-packed weights at small
-// batches: the tile kernel (inputs of up to 12 groups: the decode step) and
-// the streamed kernel (inputs of 16 to 32 groups).
+// cq_gemv_fast.cu -- tensor-core GEMV over CQ-packed weights for small
+// batches (the decode step): 2-bit codes (CQ2, ternary) and 4-bit codes
+// (CQ4), batch <= 4, inputs of at most 32 groups.
 //
 // Per group g of 128 inputs the product is the rotated-domain identity
 // (OpenNeedle docs/reference.md; "The .cact archive and Cactus Quants",
 // "Reconstructing one group"):
 //     y[o] += n[o][g] * sum_k c[q[o,g,k]] * z[g,k],   z = H x (per group).
-// The activation is rotated once per thread block and laid out as MMA
-// operand fragments in shared memory; the weights are never expanded
-// beyond the registers that feed one MMA ("How the kernel reads it").
+// Each CTA rotates the activation of its matrix itself (a few warp-tasks:
+// one per group and batch row) and lays z out as MMA operand fragments in
+// shared memory; the FWHT is shared by all the rows of the CTA ("How the
+// kernel reads it"). A separate prologue kernel would put a launch and a
+// round trip through global memory on the critical path of a decode step.
 //
-// GB300 mapping. The weights stay packed in HBM and in shared memory. Code
-// bytes become fp16 levels in registers -- through byte -> levels tables
-// replicated across the shared-memory banks (conflict-free lookups), or,
-// for 2-bit codes, partly by byte permutes over the levels' bytes held in
-// registers -- and feed mma.sync m16n8k16 (fp16 in, fp32 accumulate) as the
-// A operand. z enters as the B operand split into fp16 hi + lo terms (two
-// MMA columns per batch row), so the products are exact up to the fp16
-// rounding of the levels. Each norm and the activation's power-of-two scale
-// are applied in fp32 per row and group.
+// GB300 mapping. The weights stay packed in HBM and in shared memory; a
+// code byte is expanded to fp16 levels in registers through a 256-entry
+// table (four 2-bit codes -> four halves, or two 4-bit codes -> two halves),
+// replicated across the shared-memory banks so that every lane's lookup is
+// conflict-free, and the halves feed mma.sync m16n8k16 (fp16 in, fp32
+// accumulate) as the A operand. z enters as the B operand split into fp16
+// hi + lo terms (two MMA columns per batch row), so the products are exact
+// up to the fp16 rounding of the levels. At batch 1 a CQ2 weight costs a
+// quarter of a table lookup, a quarter of a byte extraction and 1/256 of an
+// MMA, which keeps every pipe below the rate at which HBM delivers codes.
+// (The e4m3 form of mma.sync is not a native instruction on this GPU: each
+// one executes as two fp16 MMAs plus operand conversions, so fp8 operands
+// would only add work.)
+//
+// Work: a CTA owns one matrix's row range (16*T rows) and its whole input.
+// At entry it issues 16-byte cp.async copies of its contiguous code rows and
+// norms into shared memory (rows padded so the operand reads are free of
+// bank conflicts; rows past the matrix are zero-filled), then, while they
+// land, builds the level table and rotates the activation. Its warps split
+// the row tiles and, when a CTA has fewer tiles than warps, the groups of the
+// input (partial sums meet in shared memory).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -33,6 +47,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kMaxFastMats = 200;
+constexpr int kMaxFastItems = 2048;
 constexpr int kMaxFastB = 4;
 constexpr int kMaxFastNg = 32;
 constexpr int kFragWords = 16;  // B-fragment words per lane and group
@@ -45,7 +61,7 @@ struct FastMat {
     float *y;
     int out, in, ng, bits, xdt, B;
     int kind;      // 0: 2-bit codes, 1: 4-bit codes, 2: 1-bit codes, 3: 3-bit codes
-    int lut;       // index into the launch's level tables
+    int lut;       // index into FastParams::lut
     int tiles;     // row tiles (16 rows) per CTA
     int kchunks;   // warps sharing one tile (split of the groups)
     int item0;     // first CTA of this matrix
@@ -53,6 +69,17 @@ struct FastMat {
 };
 
 static_assert(sizeof(FastMat) % 4 == 0 && sizeof(FastMat) / 4 <= 256, "descriptor copy");
+
+struct FastParams {
+    int n_items;
+    // byte offsets of the shared regions: code rows, norms, B fragments
+    // [ng][4][32 lanes][4] words, partial sums, level table, rotation scratch
+    int smem_codes, smem_norms, smem_frag, smem_red, smem_tab, smem_terms;
+    __half lut[kMaxLuts][16];  // levels by code (2-bit: entries 0..3)
+    FastMat m[kMaxFastMats];
+    int n_mats;
+    uint8_t item_mat[kMaxFastItems];  // CTA -> matrix
+};
 
 constexpr float kInvSqrt128 = 0.08838834764831845f;
 
@@ -347,353 +374,175 @@ __device__ __forceinline__ void lut_group64(float (&acc)[4], const uint8_t *rowr
     }
 }
 
-// --------------------------------------------------------- the tile kernel --
-// GEMV over inputs of at most 12 groups at batch <= 4 (the decode step). The
-// 16-row tiles of a launch, in the order of its matrices, are cut into runs
-// of about equal bytes, one run per CTA and two CTAs per SM. A CTA copies its
-// run's code rows and norms into shared memory and builds its level table
-// before it waits for the grid ahead of it on the stream (programmatic
-// dependent launch), so that those copies overlap the previous launch; then
-// it rotates each distinct activation its run reads once (an activation
-// "slot": the FWHT of a group in one warp, its fp16 hi + lo terms moved into
-// MMA B fragments by warp shuffles), and its warps take the run's tiles
-// round-robin, each tile with all of its groups, and write the outputs.
-//
-// 2-bit codes (CQ2, ternary crumbs) are expanded to fp16 levels two ways,
-// half of each lane's code bytes each way, so that neither the shared-memory
-// pipe nor the integer pipe carries all of the expansion: bytes 0-3 of a
-// lane's 8 code bytes per row and group go through the byte -> four levels
-// table (one 8-byte lookup per byte); bytes 4-7 are expanded in registers:
-// the four 2-bit fields at bit 2i of the word's bytes become byte selectors
-// (c -> c | (c | 4) << 4) of a byte permute over the four levels' low and
-// high bytes, which yields the fp16 pairs (field i of bytes 4,5) and (field i
-// of bytes 6,7). The MMA k order of those pairs differs from the table's;
-// the activation fragments are laid out to match ("hybrid" layout). 4-bit
-// and 1-bit codes use their tables only ("natural" layout).
-constexpr int kTileMaxMats = 144;
-constexpr int kTileMaxSegs = 448;
-constexpr int kTileMaxCtas = 320;
-constexpr int kTileRunSegs = 8;            // matrices per run
-constexpr int kTileSlots = 6;              // distinct activations per run (at most 12 / ng)
-constexpr int kTileFragGroups = 12;        // activation fragments per CTA: slots x groups
-constexpr int kTileMaxNg = 12;
-constexpr int kTileCodeBudget = 48 * 1024;  // shared-memory bytes of code rows per run (padded rows)
-
-struct TileSeg {
-    int mat;     // matrix (index into TileParams::m)
-    int tile0;   // first 16-row tile of the matrix in this run
-    int ntiles;  // tiles of the matrix in this run
-    int slot;    // activation slot of the run
-};
-
-struct TileParams {
-    int smem_tab, smem_codes, smem_norms, smem_frag;  // byte offsets of the shared regions
-    int cta_seg[kTileMaxCtas + 1];                    // segments of CTA c: cta_seg[c] .. cta_seg[c+1]-1
-    TileSeg seg[kTileMaxSegs];
-    __half lut[kMaxLuts][16];
-    FastMat m[kTileMaxMats];
-};
-
-static_assert(sizeof(TileParams) <= 32000, "kernel parameter block");
-
-// z of one batch row and group after rotate_bg, as this lane's four
-// positions 4 lane + i (fp16 hi | lo << 16); returns the B-fragment words
-// of batch row b into w (lanes whose MMA column is another batch row keep
-// their words). Word f of lane (gq, t): MMA j = f / 2, half h = f % 2.
-// Natural layout: positions 32t + 4j + 2h + {0, 1}; hybrid layout, MMAs
-// j >= 4: positions 32t + 16 + 8h + (j - 4) + {0, 4}. Column gq holds batch
-// row gq / 2, term gq % 2 (hi / lo).
-template <bool HYB>
-__device__ __forceinline__ void frag_from_lanes(const uint32_t (&e)[4], int b, int lane, uint32_t (&w)[kFragWords]) {
-    const int gq = lane >> 2, t = lane & 3, tau = 16 * (gq & 1);
-    const bool mine = (gq >> 1) == b;
-#pragma unroll
-    for (int f = 0; f < kFragWords; ++f) {
-        const int j = f >> 1, h = f & 1;
-        uint32_t a, c;
-        if (!HYB || j < 4) {
-            a = __shfl_sync(0xffffffffu, e[2 * h], 8 * t + j);
-            c = __shfl_sync(0xffffffffu, e[2 * h + 1], 8 * t + j);
-        } else {
-            a = __shfl_sync(0xffffffffu, e[j - 4], 8 * t + 4 + 2 * h);
-            c = __shfl_sync(0xffffffffu, e[j - 4], 8 * t + 5 + 2 * h);
-        }
-        if (mine) w[f] = ((a >> tau) & 0xffffu) | (((c >> tau) & 0xffffu) << 16);
-    }
-}
-
-// Rotation of (batch row b, group g) by one warp from this lane's values v
-// (load_x_bg): z = H0 x (exact integers for int8 x), scaled by a power of
-// two sigma (|sigma z| <= 2^14) and split into fp16 hi + lo terms, returned
-// per position 4 lane + i in e; returns 1/sigma.
-__device__ __forceinline__ float rotate_regs(float (&v)[4], int lane, uint32_t (&e)[4]) {
-    float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
-    v[0] = a0 + a2;
-    v[1] = a1 + a3;
-    v[2] = a0 - a2;
-    v[3] = a1 - a3;
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
-            v[i] = (lane & m) ? o - v[i] : v[i] + o;
-        }
-    float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-    for (int m = 16; m; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-    const float sigma = pow2_scale(mx, 16384.0f);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float x = __fmul_rn(v[i], sigma);
-        const __half hi = __float2half_rn(x);
-        const __half lo = __float2half_rn(__fsub_rn(x, __half2float(hi)));
-        e[i] = (uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16);
-    }
-    return 1.0f / sigma;
-}
-
-// Register expansion of 2-bit codes: the fields at bit 2i of the four bytes
-// of w, as fp16 level pairs (bytes 0, 1) in lo[i] and (bytes 2, 3) in hi[i].
-// llo / lhi hold the low / high bytes of the four levels.
-__device__ __forceinline__ void expand2_regs(uint32_t w, uint32_t llo, uint32_t lhi, uint32_t (&lo)[4],
-                                             uint32_t (&hi)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t x = (w >> (2 * i)) & 0x03030303u;
-        const uint32_t s = x * 0x11u + 0x40404040u;  // c -> selector nibbles c, c | 4
-        lo[i] = __byte_perm(llo, lhi, s);
-        hi[i] = __byte_perm(llo, lhi, s >> 16);
-    }
-}
-
-// One 16-row tile and one group: rows gq (codes cr) and gq + 8 (cs) of this
-// lane, products of the group's 8 MMAs into d.
-template <int KIND>
-__device__ __forceinline__ void tile_group(float (&d)[4], const uint8_t *r0, const uint8_t *r1, const uint8_t *tab,
-                                           uint32_t llo, uint32_t lhi, const uint32_t (&fr)[kFragWords], int lane) {
-    const int t = lane & 3;
-    if (KIND == 0) {  // 2-bit: bytes 8t .. 8t+7 of the group
-        const uint2 cr = *reinterpret_cast<const uint2 *>(r0 + 8 * t);
-        const uint2 cs = *reinterpret_cast<const uint2 *>(r1 + 8 * t);
-        const uint8_t *tb = tab + 8 * (lane & 15);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint2 er = *reinterpret_cast<const uint2 *>(tb + 128 * __byte_perm(cr.x, 0, 0x4440 + i));
-            const uint2 es = *reinterpret_cast<const uint2 *>(tb + 128 * __byte_perm(cs.x, 0, 0x4440 + i));
-            mma_f16(d, er.x, es.x, er.y, es.y, fr[2 * i], fr[2 * i + 1]);
-        }
-        uint32_t rl[4], rh[4], sl[4], sh[4];
-        expand2_regs(cr.y, llo, lhi, rl, rh);
-        expand2_regs(cs.y, llo, lhi, sl, sh);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mma_f16(d, rl[i], sl[i], rh[i], sh[i], fr[8 + 2 * i], fr[9 + 2 * i]);
-    } else if (KIND == 1) {  // 4-bit: bytes 16t .. 16t+15, MMA j takes bytes 2j, 2j+1
-        const uint4 cr = *reinterpret_cast<const uint4 *>(r0 + 16 * t);
-        const uint4 cs = *reinterpret_cast<const uint4 *>(r1 + 16 * t);
-        const uint32_t wr[4] = {cr.x, cr.y, cr.z, cr.w}, ws[4] = {cs.x, cs.y, cs.z, cs.w};
-        const uint8_t *tb = tab + 4 * lane;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t r = wr[j >> 1] >> (16 * (j & 1)), s = ws[j >> 1] >> (16 * (j & 1));
-            const uint32_t a0 = *reinterpret_cast<const uint32_t *>(tb + 128 * (r & 0xffu));
-            const uint32_t a2 = *reinterpret_cast<const uint32_t *>(tb + 128 * ((r >> 8) & 0xffu));
-            const uint32_t a1 = *reinterpret_cast<const uint32_t *>(tb + 128 * (s & 0xffu));
-            const uint32_t a3 = *reinterpret_cast<const uint32_t *>(tb + 128 * ((s >> 8) & 0xffu));
-            mma_f16(d, a0, a1, a2, a3, fr[2 * j], fr[2 * j + 1]);
-        }
-    } else {  // 1-bit: bytes 4t .. 4t+3, MMA j takes nibble j
-        const uint32_t cr = *reinterpret_cast<const uint32_t *>(r0 + 4 * t);
-        const uint32_t cs = *reinterpret_cast<const uint32_t *>(r1 + 4 * t);
-        const uint8_t *tb = tab + 8 * (lane & 15);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint2 er = *reinterpret_cast<const uint2 *>(tb + 128 * ((cr >> (4 * j)) & 15u));
-            const uint2 es = *reinterpret_cast<const uint2 *>(tb + 128 * ((cs >> (4 * j)) & 15u));
-            mma_f16(d, er.x, es.x, er.y, es.y, fr[2 * j], fr[2 * j + 1]);
-        }
-    }
-}
-
-template <int KIND>
-__device__ __forceinline__ void tile_run(const TileParams &p, const FastMat *sM, const TileSeg *sS, const int *s_tp,
-                                         const int *s_cb, const int *s_nb, const int *s_slot_g0,
-                                         const float (*s_ginv)[kMaxFastB][kTileMaxNg],
-                                         const float (*s_alpha)[kMaxFastB], uint8_t *smem, uint32_t llo, uint32_t lhi,
-                                         int nseg) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gq = lane >> 2, t = lane & 3;
-    const uint8_t *sc = smem + p.smem_codes, *sn = smem + p.smem_norms, *tab = smem + p.smem_tab;
-    const uint32_t *frag = reinterpret_cast<const uint32_t *>(smem + p.smem_frag);
-    const int total = s_tp[nseg];
-    int s = 0;
-#pragma unroll 1
-    for (int tt = warp; tt < total; tt += kWarps) {
-        while (tt >= s_tp[s + 1]) ++s;
-        const FastMat &M = sM[s];
-        const int ng = M.ng, B = M.B, rs = M.row_stride, sl = sS[s].slot;
-        const int lt = tt - s_tp[s];  // tile of this segment
-        const uint8_t *rowr = sc + s_cb[s] + (size_t)(16 * lt + gq) * rs;
-        const __half *nr = reinterpret_cast<const __half *>(sn + s_nb[s]) + (16 * lt + gq) * ng;
-        const bool live = gq < 2 * B;  // this lane's B column belongs to a batch row
-        const int gbytes = KIND == 0 ? 32 : KIND == 1 ? 64 : 16;
-        const uint32_t *fs = frag + (size_t)s_slot_g0[sl] * 32 * kFragWords;  // the slot's fragments
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-        for (int g = 0; g < ng; ++g) {
-            uint32_t fr[kFragWords];
-            const uint4 *fl = reinterpret_cast<const uint4 *>(fs + (size_t)g * 32 * kFragWords) + lane;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint4 v = live ? fl[32 * k] : make_uint4(0, 0, 0, 0);
-                fr[4 * k] = v.x, fr[4 * k + 1] = v.y, fr[4 * k + 2] = v.z, fr[4 * k + 3] = v.w;
-            }
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_group<KIND>(d, rowr + g * gbytes, rowr + 8 * rs + g * gbytes, tab, llo, lhi, fr, lane);
-            const float inv = t < B ? s_ginv[sl][t][g] : 0.0f;
-            const float n0 = __half2float(nr[g]) * inv, n1 = __half2float(nr[8 * ng + g]) * inv;
-            acc[0] = fmaf(n0, d[0], acc[0]);
-            acc[1] = fmaf(n0, d[1], acc[1]);
-            acc[2] = fmaf(n1, d[2], acc[2]);
-            acc[3] = fmaf(n1, d[3], acc[3]);
-        }
-        // columns 2t, 2t+1: hi and lo terms of batch row t
-        if (t < B) {
-            const int row = 16 * (sS[s].tile0 + lt) + gq;
-            const float a = s_alpha[sl][t];
-            if (row < M.out) M.y[(size_t)t * M.out + row] = (acc[0] + acc[1]) * a;
-            if (row + 8 < M.out) M.y[(size_t)t * M.out + row + 8] = (acc[2] + acc[3]) * a;
-        }
-    }
-}
-
-__global__ void __launch_bounds__(kThreads, 2) gemv_tile_kernel(const __grid_constant__ TileParams p) {
+// ------------------------------------------------------------ the kernel --
+__global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_constant__ FastParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ FastMat sM[kTileRunSegs];
-    __shared__ TileSeg sS[kTileRunSegs];
-    __shared__ int s_tp[kTileRunSegs + 1];  // first run tile of each segment
-    __shared__ int s_cb[kTileRunSegs];      // byte offset of each segment's code rows
-    __shared__ int s_nb[kTileRunSegs];      // byte offset of each segment's norms
-    __shared__ int s_slot_seg[kTileSlots];  // a segment of each slot
-    __shared__ int s_slot_g0[kTileSlots];   // first fragment group of each slot
-    __shared__ __half s_lv[16];
-    __shared__ float s_ginv[kTileSlots][kMaxFastB][kTileMaxNg];  // 1/sigma per slot, batch row, group
-    __shared__ float s_alpha[kTileSlots][kMaxFastB];             // output scale per slot and batch row
-    // The next launch on the stream may start its blocks as soon as this
-    // grid's blocks are resident: its copies and table do not depend on this
-    // grid, and it waits for this grid before it reads activations or writes
-    // outputs.
+    // one copy of this CTA's matrix descriptor in shared memory (parameter
+    // reads with a runtime index would otherwise repeat inside the loops)
+    __shared__ FastMat sM;
+    __shared__ __half s_lv[16];  // the codebook's levels (parameter reads with a
+                                 // per-lane index would serialise)
+    // The next launch on the stream (the next decode step) may start its
+    // blocks as this grid's blocks retire: its weight copies and level table
+    // do not depend on this grid, and it waits for it before reading its
+    // activation (programmatic dependent launch).
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    const int mi = p.item_mat[blockIdx.x];
+    if (threadIdx.x < (int)(sizeof(FastMat) / 4))
+        reinterpret_cast<uint32_t *>(&sM)[threadIdx.x] = reinterpret_cast<const uint32_t *>(&p.m[mi])[threadIdx.x];
+    else if (threadIdx.x >= 128 && threadIdx.x < 144)
+        s_lv[threadIdx.x - 128] = p.lut[p.m[mi].lut][threadIdx.x - 128];
+    __syncthreads();
+    const FastMat &M = sM;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int s0 = p.cta_seg[blockIdx.x], nseg = p.cta_seg[blockIdx.x + 1] - s0;
-    constexpr int kMatWords = sizeof(FastMat) / 4;
-    for (int e = threadIdx.x; e < nseg * kMatWords; e += kThreads) {
-        const int s = e / kMatWords, w = e - s * kMatWords;
-        reinterpret_cast<uint32_t *>(&sM[s])[w] = reinterpret_cast<const uint32_t *>(&p.m[p.seg[s0 + s].mat])[w];
-    }
-    if (threadIdx.x < nseg) sS[threadIdx.x] = p.seg[s0 + threadIdx.x];
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int tp = 0, cb = 0, nb = 0;
-        for (int s = 0; s < nseg; ++s) {
-            s_tp[s] = tp;
-            s_cb[s] = cb;
-            s_nb[s] = nb;
-            tp += sS[s].ntiles;
-            cb += 16 * sS[s].ntiles * sM[s].row_stride;
-            nb += (32 * sS[s].ntiles * sM[s].ng + 15) / 16 * 16;
-            s_slot_seg[sS[s].slot] = s;
-        }
-        s_tp[nseg] = tp;
-        // slots are numbered in run order: slot k+1 starts after slot k's groups
-        int g0 = 0;
-        for (int sl = 0; sl < kTileSlots; ++sl) {
-            s_slot_g0[sl] = g0;
-            for (int s = 0; s < nseg; ++s)
-                if (sS[s].slot == sl) {
-                    g0 += sM[s].ng;
-                    break;
-                }
-        }
-    }
-    if (threadIdx.x >= 32 && threadIdx.x < 48) s_lv[threadIdx.x - 32] = p.lut[p.m[p.seg[s0].mat].lut][threadIdx.x - 32];
-    __syncthreads();
-    const int kind = sM[0].kind;
+    const int gq = lane >> 2, t = lane & 3;
+    const int ng = M.ng, B = M.B, kind = M.kind, tiles = M.tiles;
+    const int row0 = ((int)blockIdx.x - M.item0) * 16 * tiles;
+    const int nrows = 16 * tiles;
+    const int rowBytes = ng * (kind == 0 ? 32 : kind == 1 ? 64 : kind == 3 ? 48 : 16);
+    const int rs = M.row_stride;  // padded shared-memory row stride (bytes)
 
-    // ---- 1. code rows and norms of the run -> shared memory (16-byte
-    // cp.async; rows past a matrix zero-filled), then the level table ----
-    for (int s = 0; s < nseg; ++s) {
-        const FastMat &M = sM[s];
-        const int rowBytes = M.ng * (kind == 0 ? 32 : kind == 1 ? 64 : 16), cpr = rowBytes / 16, rs = M.row_stride;
-        const int row0 = 16 * sS[s].tile0, nrows = 16 * sS[s].ntiles, valid = min(nrows, M.out - row0);
-        uint8_t *dst = smem + p.smem_codes + s_cb[s];
-        for (int c = threadIdx.x; c < nrows * cpr; c += kThreads) {
-            const int r = c / cpr, k = c - r * cpr;
-            const bool ok = r < valid;
-            cp_async16(dst + (size_t)r * rs + 16 * k, M.codes + (size_t)(ok ? row0 + r : 0) * rowBytes + 16 * k,
-                       ok ? 16 : 0);
-        }
-        const int nbytes = nrows * M.ng * 2, avail = valid * M.ng * 2;
-        const uint8_t *src = reinterpret_cast<const uint8_t *>(M.norms + (size_t)row0 * M.ng);
-        uint8_t *nd = smem + p.smem_norms + s_nb[s];
-        for (int c = threadIdx.x; 16 * c < nbytes; c += kThreads) {
-            const int left = avail - 16 * c, n = left >= 16 ? 16 : (left > 0 ? left : 0);
-            cp_async16(nd + 16 * c, n ? src + 16 * c : src, n);
-        }
-    }
-    asm volatile("cp.async.commit_group;\n" ::);
-    build_level_table(kind, s_lv, smem + p.smem_tab);
-    // the four 2-bit levels' low and high bytes, for the register expansion
-    uint32_t llo = 0, lhi = 0;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint32_t h = __half_as_ushort(s_lv[c]);
-        llo |= (h & 0xffu) << (8 * c);
-        lhi |= (h >> 8) << (8 * c);
-    }
+    uint8_t *sc = smem + p.smem_codes;                             // [nrows][rs]
+    __half *sn = reinterpret_cast<__half *>(smem + p.smem_norms);  // [nrows][ng]
+    uint32_t *frag = reinterpret_cast<uint32_t *>(smem + p.smem_frag);
+    float *red = reinterpret_cast<float *>(smem + p.smem_red);
+    __shared__ float ginv[kMaxFastB * kMaxFastNg];  // 1/sigma [B][ng]
 
-    // ---- 2. the activations, once the grid ahead of this one on the stream
-    // (which may have written them) is complete: warp w rotates the
-    // (slot, group) tasks w, w+8, ... for every batch row of the slot ----
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    int nslot = 0;
-    for (int s = 0; s < nseg; ++s) nslot = max(nslot, sS[s].slot + 1);
-    if (threadIdx.x < nslot * kMaxFastB) {
-        const int sl = threadIdx.x / kMaxFastB, b = threadIdx.x % kMaxFastB;
-        const FastMat &A = sM[s_slot_seg[sl]];
-        s_alpha[sl][b] = b < A.B && A.xdt == CQ_X_I8 ? __fmul_rn(A.xs[b], kInvSqrt128) : kInvSqrt128;
-    }
+    // ---- 1. code rows and norms -> shared memory (16-byte cp.async; rows
+    // past the matrix zero-filled) ----
     {
-        int task = 0;
-        uint32_t *frag = reinterpret_cast<uint32_t *>(smem + p.smem_frag);
-        for (int sl = 0; sl < nslot; ++sl) {
-            const FastMat &A = sM[s_slot_seg[sl]];
-            for (int g = 0; g < A.ng; ++g, ++task) {
-                if (task % kWarps != warp) continue;
-                uint32_t w[kFragWords];
-#pragma unroll
-                for (int f = 0; f < kFragWords; ++f) w[f] = 0u;
-                for (int b = 0; b < A.B; ++b) {
-                    float v[4];
-                    uint32_t e[4];
-                    load_x_bg(A, b, g, lane, v);
-                    const float inv = rotate_regs(v, lane, e);
-                    if (lane == 0) s_ginv[sl][b][g] = inv;
-                    if (kind == 0) frag_from_lanes<true>(e, b, lane, w);
-                    else frag_from_lanes<false>(e, b, lane, w);
+        const int cpr = rowBytes / 16;  // 16-byte chunks per code row
+        const int rows_valid = min(nrows, M.out - row0);
+        if (cpr <= 32) {
+            // a warp copies rpi rows per step, lane -> (row lr, chunk lc)
+            const int rpi = 32 / cpr, lr = lane / cpr, lc = lane - lr * cpr;
+            if (lr < rpi)
+                for (int r = warp * rpi + lr; r < nrows; r += kWarps * rpi) {
+                    const bool ok = r < rows_valid;
+                    cp_async16(sc + (size_t)r * rs + 16 * lc,
+                               M.codes + (size_t)(ok ? row0 + r : 0) * rowBytes + 16 * lc, ok ? 16 : 0);
                 }
-                uint4 *d4 = reinterpret_cast<uint4 *>(frag + (size_t)(s_slot_g0[sl] + g) * 32 * kFragWords);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) d4[i * 32 + lane] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        } else {
+            for (int r = warp; r < nrows; r += kWarps) {
+                const bool ok = r < rows_valid;
+                for (int c = lane; c < cpr; c += 32)
+                    cp_async16(sc + (size_t)r * rs + 16 * c, M.codes + (size_t)(ok ? row0 + r : 0) * rowBytes + 16 * c,
+                               ok ? 16 : 0);
             }
         }
+        const int nbytes = nrows * ng * 2, avail = rows_valid * ng * 2;
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(M.norms + (size_t)row0 * ng);
+        for (int c = threadIdx.x; 16 * c < nbytes; c += kThreads) {
+            const int left = avail - 16 * c;
+            const int n = left >= 16 ? 16 : (left > 0 ? left : 0);
+            cp_async16(reinterpret_cast<uint8_t *>(sn) + 16 * c, n ? src + 16 * c : src, n);
+        }
+        asm volatile("cp.async.commit_group;\n" ::);
     }
+
+    // ---- 2. while they land: the level table ----
+    build_level_table(kind, s_lv, smem + p.smem_tab);
+
+    // ---- 3. the activation, once the grid before this one on the stream
+    // (which may have written it) is complete: warp w rotates groups w, w+8,
+    // ... of every batch row into B fragments and 1/sigma ----
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    rotate_activation(M, smem + p.smem_terms, frag, ginv);
     asm volatile("cp.async.wait_all;\n" ::: "memory");
     __syncthreads();
 
-    // ---- 3. products: warp w takes the run's tiles w, w+8, ... ----
-    if (kind == 0) tile_run<0>(p, sM, sS, s_tp, s_cb, s_nb, s_slot_g0, s_ginv, s_alpha, smem, llo, lhi, nseg);
-    else if (kind == 1) tile_run<1>(p, sM, sS, s_tp, s_cb, s_nb, s_slot_g0, s_ginv, s_alpha, smem, llo, lhi, nseg);
-    else tile_run<2>(p, sM, sS, s_tp, s_cb, s_nb, s_slot_g0, s_ginv, s_alpha, smem, llo, lhi, nseg);
+    // ---- 4. products. Warp w takes tiles w, w+8, ... with every group
+    // (two tiles at a time share each group's B fragments), or, with fewer
+    // tiles than warps, one tile and every KC-th group ----
+    const int KC = M.kchunks;
+    const bool wide = tiles >= kWarps;
+    const int step = wide ? kWarps : tiles + 1;
+    const int kc = wide ? 0 : warp % KC;
+    const bool live = gq < 2 * B;  // this lane's B column belongs to a batch row
+    // output scale of this lane's batch row t
+    const float alpha = t < B && M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[t], kInvSqrt128) : kInvSqrt128;
+    const uint2 *tab2 = reinterpret_cast<const uint2 *>(smem + p.smem_tab) + (lane & 15);
+    const uint32_t *tab4 = reinterpret_cast<const uint32_t *>(smem + p.smem_tab) + lane;
+
+#pragma unroll 1
+    for (int ta = wide ? warp : warp / KC; ta < tiles; ta += 2 * step) {
+        const int tb = ta + step;
+        const bool has_b = tb < tiles;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const int ra = 16 * ta + gq, rb = 16 * (has_b ? tb : ta) + gq;  // local rows (and +8)
+#pragma unroll 1
+        for (int g = kc; g < ng; g += KC) {
+            // B columns 2B .. 7 are zero: only the lanes of the live columns load
+            uint32_t fr[kFragWords];
+            const uint4 *fl = reinterpret_cast<const uint4 *>(frag + (size_t)g * 32 * kFragWords) + lane;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = live ? fl[32 * i] : make_uint4(0, 0, 0, 0);
+                fr[4 * i] = v.x, fr[4 * i + 1] = v.y, fr[4 * i + 2] = v.z, fr[4 * i + 3] = v.w;
+            }
+            const float inv = t < B ? ginv[t * ng + g] : 0.0f;
+            const float n0 = __half2float(sn[ra * ng + g]) * inv, n1 = __half2float(sn[(ra + 8) * ng + g]) * inv;
+            const float n2 = __half2float(sn[rb * ng + g]) * inv, n3 = __half2float(sn[(rb + 8) * ng + g]) * inv;
+            if (kind == 2) {
+                const uint32_t c0 = *reinterpret_cast<const uint32_t *>(sc + (size_t)ra * rs + g * 16 + 4 * t);
+                const uint32_t c1 = *reinterpret_cast<const uint32_t *>(sc + (size_t)(ra + 8) * rs + g * 16 + 4 * t);
+                lut1_group(acc[0], c0, c1, tab2, fr, n0, n1);
+                if (has_b) {
+                    const uint32_t c2 = *reinterpret_cast<const uint32_t *>(sc + (size_t)rb * rs + g * 16 + 4 * t);
+                    const uint32_t c3 = *reinterpret_cast<const uint32_t *>(sc + (size_t)(rb + 8) * rs + g * 16 + 4 * t);
+                    lut1_group(acc[1], c2, c3, tab2, fr, n2, n3);
+                }
+            } else if (kind == 0) {
+                const uint2 c0 = *reinterpret_cast<const uint2 *>(sc + (size_t)ra * rs + g * 32 + 8 * t);
+                const uint2 c1 = *reinterpret_cast<const uint2 *>(sc + (size_t)(ra + 8) * rs + g * 32 + 8 * t);
+                lut2_group(acc[0], c0, c1, tab2, fr, n0, n1);
+                if (has_b) {
+                    const uint2 c2 = *reinterpret_cast<const uint2 *>(sc + (size_t)rb * rs + g * 32 + 8 * t);
+                    const uint2 c3 = *reinterpret_cast<const uint2 *>(sc + (size_t)(rb + 8) * rs + g * 32 + 8 * t);
+                    lut2_group(acc[1], c2, c3, tab2, fr, n2, n3);
+                }
+            } else {
+                const uint4 c0 = *reinterpret_cast<const uint4 *>(sc + (size_t)ra * rs + g * 64 + 16 * t);
+                const uint4 c1 = *reinterpret_cast<const uint4 *>(sc + (size_t)(ra + 8) * rs + g * 64 + 16 * t);
+                lut4_group(acc[0], c0, c1, tab4, fr, n0, n1);
+                if (has_b) {
+                    const uint4 c2 = *reinterpret_cast<const uint4 *>(sc + (size_t)rb * rs + g * 64 + 16 * t);
+                    const uint4 c3 = *reinterpret_cast<const uint4 *>(sc + (size_t)(rb + 8) * rs + g * 64 + 16 * t);
+                    lut4_group(acc[1], c2, c3, tab4, fr, n2, n3);
+                }
+            }
+        }
+        // per-row totals of batch t (columns 2t, 2t+1 hold its hi and lo terms)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (h == 1 && !has_b) break;
+            const int tl = h ? tb : ta;
+            const int row_r = row0 + 16 * tl + gq, row_s = row_r + 8;
+            const float yr = acc[h][0] + acc[h][1], ys = acc[h][2] + acc[h][3];
+            if (t < B) {
+                if (KC == 1) {
+                    if (row_r < M.out) M.y[(size_t)t * M.out + row_r] = yr * alpha;
+                    if (row_s < M.out) M.y[(size_t)t * M.out + row_s] = ys * alpha;
+                } else {
+                    float *rt = red + ((size_t)(tl * KC + kc) * 16) * kMaxFastB;
+                    rt[gq * kMaxFastB + t] = yr;
+                    rt[(gq + 8) * kMaxFastB + t] = ys;
+                }
+            }
+        }
+    }
+    if (KC > 1) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < tiles * 16 * B; e += kThreads) {
+            const int tl = e / (16 * B), rr = (e / B) % 16, b = e % B;
+            const int row = row0 + 16 * tl + rr;
+            if (row >= M.out) continue;
+            float sum = 0.0f;
+            for (int c = 0; c < KC; ++c) sum += red[((size_t)(tl * KC + c) * 16 + rr) * kMaxFastB + b];
+            const float ab = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[b], kInvSqrt128) : kInvSqrt128;
+            M.y[(size_t)b * M.out + row] = sum * ab;
+        }
+    }
 }
 
 // ------------------------------------------------- wide inputs, streamed --
@@ -953,215 +802,145 @@ bool gemv_fast_eligible(const cq_gemv_desc &d) {
     const int ng = in_padded(d.in) / kGroup;
     if (d.in <= 0 || d.out <= 0 || d.group != kGroup) return false;
     const int W = width_of(d.bits);
-    return (W == 1 || W == 2 || W == 4) && d.B <= kMaxFastB && ng <= kTileMaxNg && !gemv_stream_eligible(d);
+    // 3-bit codes only on the streamed kernel (wide inputs): their product
+    // branch would cost this kernel registers on the decode step
+    return W != 3 && (W >= 1 && W <= 4) && d.B <= kMaxFastB && ng <= kMaxFastNg && !gemv_stream_eligible(d);
 }
 
-namespace {
-
-int tile_kind(int W) { return W == 2 ? 0 : W == 4 ? 1 : 2; }
-int tile_gbytes(int kind) { return kind == 0 ? 32 : kind == 1 ? 64 : 16; }
-
-// Shared-memory row stride of a code row: the 2-bit path reads 8 bytes per
-// lane (the rows of a half-warp start 8 banks apart), the 4-bit path 16
-// bytes (the rows of a quarter-warp 16 banks apart), the 1-bit path 4 bytes
-// (the warp's eight rows 4 banks apart).
-int tile_row_stride(int kind, int ng) {
-    const int rowBytes = ng * tile_gbytes(kind), want = tile_gbytes(kind);
-    return rowBytes + (((want - rowBytes) % 128) + 128) % 128;
-}
-
-// The level table by code of a descriptor (ternary crumbs sign-extend).
-void tile_levels(const cq_gemv_desc &D, __half lut[16]) {
-    for (int j = 0; j < 16; ++j) lut[j] = __float2half_rn(0.0f);
-    if (D.bits == 5) {
-        const float c = D.codebook[2];
-        lut[1] = __float2half_rn(c);
-        lut[2] = __float2half_rn(-2.0f * c);
-        lut[3] = __float2half_rn(-c);
-    } else {
-        for (int j = 0; j < levels_of(D.bits); ++j) lut[j] = __float2half_rn(D.codebook[j]);
-    }
-}
-
-// One launch being assembled: matrices, runs (one per CTA) and their
-// segments, and the shared-memory maxima over its runs.
-struct TileBuild {
-    TileParams *p;
-    int nm = 0, nseg = 0, ncta = 0, nlut = 0;
-    size_t codes_max = 0, norms_max = 0;
-    bool table = false;  // some run needs a 32 KB level table
-    // the open run
-    int run_seg0 = 0, run_tiles = 0, run_kind = -1, run_lut = -1, run_nslot = 0, run_groups = 0;
-    size_t run_bytes = 0, run_codes = 0, run_norms = 0;
-    const cq_gemv_desc *run_key = nullptr;  // descriptor of the open slot's activation
+// Shared-memory needs of one launch (maxima over its matrices).
+struct Need {
+    size_t codes = 0, norms = 0, frag = 0, red = 0;
 };
 
-bool same_activation(const cq_gemv_desc *a, const cq_gemv_desc *b) {
-    return a && b && a->x == b->x && a->x_scale == b->x_scale && a->B == b->B && a->x_dtype == b->x_dtype &&
-           a->in == b->in;
-}
-
-void close_run(TileBuild &L) {
-    if (L.nseg == L.run_seg0) return;
-    L.p->cta_seg[++L.ncta] = L.nseg;
-    L.codes_max = std::max(L.codes_max, L.run_codes);
-    L.norms_max = std::max(L.norms_max, L.run_norms);
-    if (L.run_kind != 2) L.table = true;
-    L.run_seg0 = L.nseg;
-    L.run_tiles = 0;
-    L.run_kind = L.run_lut = -1;
-    L.run_nslot = L.run_groups = 0;
-    L.run_bytes = L.run_codes = L.run_norms = 0;
-    L.run_key = nullptr;
-}
-
-int tile_flush(TileBuild &L, cudaStream_t st) {
-    close_run(L);
-    if (L.ncta) {
-        TileParams &p = *L.p;
-        size_t off = 0;
-        auto place = [&](int &field, size_t bytes) {
-            field = (int)off;
-            off += (bytes + 15) / 16 * 16;
-        };
-        place(p.smem_tab, L.table ? 256 * 32 * sizeof(uint32_t) : 16 * 16 * sizeof(uint2));
-        place(p.smem_codes, L.codes_max);
-        place(p.smem_norms, L.norms_max);
-        place(p.smem_frag, (size_t)kTileFragGroups * 32 * kFragWords * sizeof(uint32_t));
-        const size_t smem = off;
-        const int rc = ensure_smem(reinterpret_cast<const void *>(gemv_tile_kernel), smem);
+// Launches the GEMV over the CTAs gathered in p; resets p.
+static int flush(FastParams &p, int &nm, int &nlut, Need &need, cudaStream_t st) {
+    if (!p.n_items) return CQ_OK;
+    size_t off = 0;
+    auto place = [&](int &field, size_t bytes) {
+        field = (int)off;
+        off += (bytes + 15) / 16 * 16;
+    };
+    place(p.smem_codes, need.codes);
+    place(p.smem_norms, need.norms);
+    place(p.smem_frag, need.frag);
+    place(p.smem_red, need.red);
+    place(p.smem_tab, 256 * 32 * sizeof(uint32_t));  // either table: 32 KB
+    place(p.smem_terms, (size_t)kWarps * kMaxFastB * kGroup * sizeof(uint32_t));  // rotation scratch: 16 KB
+    const size_t smem = off;
+    p.n_mats = nm;
+    if (smem > 200 * 1024) return set_error(CQ_ERR_SHAPE, "fast GEMV needs %zu bytes of shared memory", smem);
+    {
+        const int rc = ensure_smem(reinterpret_cast<const void *>(gemv_fast_kernel), 200 * 1024);
         if (rc) return rc;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)L.ncta);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = st;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        at[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        cudaLaunchKernelEx(&cfg, gemv_tile_kernel, p);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "tile gemv launch: %s", cudaGetErrorString(e));
     }
-    L.nm = L.nseg = L.ncta = L.nlut = 0;
-    L.run_seg0 = 0;
-    L.codes_max = L.norms_max = 0;
-    L.table = false;
-    L.p->cta_seg[0] = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.n_items);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr_pdl[1];
+    attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr_pdl;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, gemv_fast_kernel, p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "fast gemv launch: %s", cudaGetErrorString(e));
+    p.n_items = 0;
+    nm = 0;
+    nlut = 0;
+    need = Need();
     return CQ_OK;
 }
 
-}  // namespace
-
 int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream) {
-    static thread_local TileParams p;  // large: off the stack, one per host thread
+    static thread_local FastParams p;  // large: off the stack, one per host thread
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    TileBuild L;
-    L.p = &p;
-    p.cta_seg[0] = 0;
-    // the byte target of a run: the launch's bytes (padded code rows and
-    // norms) spread over two CTAs per SM, at least kMinTiles tiles
-    constexpr int kMinTiles = 4;
-    size_t total = 0;
+    p.n_items = 0;
+    int nlut = 0, nm = 0;
+    Need need;
+    auto do_flush = [&]() -> int { return flush(p, nm, nlut, need, st); };
     for (int ii = 0; ii < n; ++ii) {
         const cq_gemv_desc &D = d[idx[ii]];
-        const int ng = in_padded(D.in) / kGroup, kind = tile_kind(width_of(D.bits));
-        total += (size_t)((D.out + 15) / 16) * (16 * tile_row_stride(kind, ng) + 32 * ng);
-    }
-    const size_t target = std::max<size_t>(1, total / (2 * (size_t)sm_count()) * 100 / 94);
-    for (int ii = 0; ii < n; ++ii) {
-        const cq_gemv_desc &D = d[idx[ii]];
-        const int ng = in_padded(D.in) / kGroup, W = width_of(D.bits), kind = tile_kind(W);
-        const int rs = tile_row_stride(kind, ng), tiles = (D.out + 15) / 16;
-        const size_t tile_codes = 16 * (size_t)rs, tile_norms = 32 * (size_t)ng;
-        __half lut[16];
-        tile_levels(D, lut);
-        int mi = -1, li = -1;
-        for (int tl = 0; tl < tiles; ++tl) {
-            // the matrix and its level table in the current launch (again
-            // after a flush)
-            if (mi < 0) {
-                if (L.nm == kTileMaxMats) {
-                    const int rc = tile_flush(L, st);
-                    if (rc) return rc;
-                }
-                li = -1;
-                for (int j = 0; j < L.nlut; ++j) {
-                    bool same = true;
-                    for (int k = 0; k < 16; ++k) same &= __half_as_ushort(p.lut[j][k]) == __half_as_ushort(lut[k]);
-                    if (same) li = j;
-                }
-                if (li < 0) {
-                    if (L.nlut == kMaxLuts) {
-                        const int rc = tile_flush(L, st);
-                        if (rc) return rc;
-                    }
-                    for (int k = 0; k < 16; ++k) p.lut[L.nlut][k] = lut[k];
-                    li = L.nlut++;
-                }
-                FastMat &M = p.m[L.nm];
-                M.codes = D.blob;
-                M.norms = reinterpret_cast<const __half *>(D.blob + (size_t)D.out * in_padded(D.in) * W / 8);
-                M.x = D.x;
-                M.xs = D.x_scale;
-                M.y = D.y;
-                M.out = D.out;
-                M.in = D.in;
-                M.ng = ng;
-                M.bits = D.bits;
-                M.xdt = D.x_dtype;
-                M.B = D.B;
-                M.kind = kind;
-                M.lut = li;
-                M.tiles = M.kchunks = M.item0 = 0;
-                M.row_stride = rs;
-                mi = L.nm++;
-            }
-            // does this tile start a new run?
-            const bool new_slot = !same_activation(L.run_key, &D);
-            bool cut = L.run_tiles > 0 &&
-                       (kind != L.run_kind || li != L.run_lut || L.run_codes + tile_codes > (size_t)kTileCodeBudget ||
-                        (L.run_bytes + tile_codes + tile_norms > target && L.run_tiles >= kMinTiles) ||
-                        (new_slot && (L.run_nslot == kTileSlots || L.run_groups + ng > kTileFragGroups)));
-            const bool new_seg = cut || L.nseg == L.run_seg0 || p.seg[L.nseg - 1].mat != mi;
-            if (!cut && new_seg && L.nseg - L.run_seg0 == kTileRunSegs) cut = true;
-            if (cut) {
-                close_run(L);
-                if (L.ncta == kTileMaxCtas || L.nseg + kTileRunSegs > kTileMaxSegs) {
-                    const int rc = tile_flush(L, st);
-                    if (rc) return rc;
-                    mi = -1;
-                    --tl;  // add this tile again, to the new launch
-                    continue;
-                }
-            }
-            if (L.run_tiles == 0) {
-                L.run_kind = kind;
-                L.run_lut = li;
-            }
-            if (!same_activation(L.run_key, &D)) {
-                L.run_key = &D;
-                ++L.run_nslot;
-                L.run_groups += ng;
-            }
-            if (cut || new_seg) {
-                TileSeg &S = p.seg[L.nseg++];
-                S.mat = mi;
-                S.tile0 = tl;
-                S.ntiles = 0;
-                S.slot = L.run_nslot - 1;
-                L.run_norms = (L.run_norms + 15) / 16 * 16;  // each segment's norms start 16-byte aligned
-            }
-            ++p.seg[L.nseg - 1].ntiles;
-            ++L.run_tiles;
-            L.run_bytes += tile_codes + tile_norms;
-            L.run_codes += tile_codes;
-            L.run_norms += tile_norms;
+        const int ip = in_padded(D.in), W = width_of(D.bits), ng = ip / kGroup;
+        const int kind = W == 2 ? 0 : W == 4 ? 1 : W == 3 ? 3 : 2;
+        // rows per CTA: about 48 KB of codes (96 KB for inputs of 16 groups or
+        // more, whose rotation each CTA repeats), a power-of-two number of 16-row tiles
+        const int rowB = ng * (kind == 0 ? 32 : kind == 1 ? 64 : kind == 3 ? 48 : 16) + 2 * ng;
+        const int budget = (ng >= 16 ? 96 : 48) * 1024;
+        const int tiles = std::max(1, budget / (rowB * 16));
+        int tp = 1;
+        while (tp * 2 <= tiles && tp * 2 <= 32) tp *= 2;
+        const int need_tiles = (D.out + 15) / 16;
+        while (tp > 1 && tp / 2 >= need_tiles) tp /= 2;
+        const int items = (D.out + 16 * tp - 1) / (16 * tp);
+        if (items > kMaxFastItems) return set_error(CQ_ERR_SHAPE, "matrix too tall for one fast GEMV launch");
+        if (nm == kMaxFastMats || p.n_items + items > kMaxFastItems) {
+            const int e = do_flush();
+            if (e) return e;
         }
+        // the level table of this codebook (ternary crumbs sign-extend)
+        __half lut[16];
+        for (int j = 0; j < 16; ++j) lut[j] = __float2half_rn(0.0f);
+        if (D.bits == 5) {
+            const float c = D.codebook[2];
+            lut[1] = __float2half_rn(c);
+            lut[2] = __float2half_rn(-2.0f * c);
+            lut[3] = __float2half_rn(-c);
+        } else {
+            for (int j = 0; j < levels_of(D.bits); ++j) lut[j] = __float2half_rn(D.codebook[j]);
+        }
+        int li = -1;
+        for (int j = 0; j < nlut; ++j) {
+            bool same = true;
+            for (int k = 0; k < 16; ++k) same &= __half_as_ushort(p.lut[j][k]) == __half_as_ushort(lut[k]);
+            if (same) li = j;
+        }
+        if (li < 0) {
+            if (nlut == kMaxLuts) {
+                const int e = do_flush();
+                if (e) return e;
+            }
+            for (int k = 0; k < 16; ++k) p.lut[nlut][k] = lut[k];
+            li = nlut++;
+        }
+        FastMat &M = p.m[nm];
+        M.codes = D.blob;
+        M.norms = reinterpret_cast<const __half *>(D.blob + (size_t)D.out * ip * W / 8);
+        M.x = D.x;
+        M.xs = D.x_scale;
+        M.y = D.y;
+        M.out = D.out;
+        M.in = D.in;
+        M.ng = ng;
+        M.bits = D.bits;
+        M.xdt = D.x_dtype;
+        M.B = D.B;
+        M.kind = kind;
+        M.lut = li;
+        M.tiles = tp;
+        M.kchunks = tp >= kWarps ? 1 : std::min(kWarps / tp, M.ng);
+        // row stride in shared memory: the 2-bit path reads 8 bytes per lane
+        // (rows of a half-warp must start 8 banks apart), the 4-bit path 16
+        // bytes (rows of a quarter-warp 16 banks apart), the 1-bit path 4
+        // bytes (the warp's eight rows 4 banks apart), the 3-bit path three
+        // words per lane (stride = 48 mod 128 bytes puts a warp's 32 reads
+        // on 32 banks)
+        const int rowBytes = M.ng * (M.kind == 0 ? 32 : M.kind == 1 ? 64 : M.kind == 3 ? 48 : 16);
+        const int want = M.kind == 0 ? 32 : M.kind == 1 ? 64 : M.kind == 3 ? 48 : 16;
+        M.row_stride = rowBytes + (((want - rowBytes) % 128) + 128) % 128;
+
+        M.item0 = p.n_items;
+        for (int k = 0; k < items; ++k) p.item_mat[p.n_items + k] = (uint8_t)nm;
+        p.n_items += items;
+        const size_t nrows = 16 * (size_t)tp;
+        need.codes = std::max(need.codes, nrows * M.row_stride);
+        need.norms = std::max(need.norms, nrows * M.ng * 2);
+        need.frag = std::max(need.frag, (size_t)M.ng * 32 * kFragWords * sizeof(uint32_t));
+        if (M.kchunks > 1) need.red = std::max(need.red, (size_t)M.tiles * M.kchunks * 16 * kMaxFastB * sizeof(float));
+        ++nm;
     }
-    return tile_flush(L, st);
+    return do_flush();
 }
 
 }  // namespace cq

@@ -85,20 +85,20 @@ def test_noalloc_python_wrapper_and_no_new_device_memory():
     shapes = [(c[0], c[1], c[3]) for c in CASES] + [(64, 1024, 2)]
     Ys = [torch.empty((Xq.shape[0], out), device="cuda") for (blob, cb, Xq, xs, _, _), (out, _, _) in
           zip(cases, shapes)]
-    for (blob, cb, Xq, xs, _, _), (out, n_in, bits), Y in zip(cases, shapes):
+    for (blob, cb, Xq, xs, _, _), (out, n_in, bits), Y in zip(cases, shapes, Ys):
         C.cq_gemm_noalloc(blob, out, n_in, bits, cb, Xq, xs, Y)  # set-up and kernel loading
     torch.cuda.synchronize()
     fresh = torch.cuda.Stream()
     free0, _ = torch.cuda.mem_get_info()
     with torch.cuda.stream(fresh):
-        for _ in range(2):
-            for (blob, cb, Xq, xs, _, _), (out, n_in, bits), Y in zip(cases, shapes):
+        for _rep in range(2):
+            for (blob, cb, Xq, xs, _, _), (out, n_in, bits), Y in zip(cases, shapes, Ys):
                 Y.fill_(float("nan"))
                 C.cq_gemm_noalloc(blob, out, n_in, bits, cb, Xq, xs, Y)
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
-    for (blob, cb, Xq, xs, y_ref, bound), (out, n_in, bits), Y in zip(cases, shapes):
+    for (blob, cb, Xq, xs, y_ref, bound), (out, n_in, bits), Y in zip(cases, shapes, Ys):
         check_matmul(Y.cpu().numpy(), y_ref, bound, f"wrapper {out}x{n_in} bits={bits}")
 
 
