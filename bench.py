@@ -608,6 +608,9 @@ def gemv_kernel_name(out, n_in, bits, B, group=128):
         return "gemv_stream_kernel"
     if B <= 4 and group == 128 and w != 3 and ng <= 32:
         return "gemv_fast_kernel"
+    cols = 2 * B if B <= 4 else 8 * ((B + 7) // 8)
+    if group == 128 and ng <= 128 and ng * cols * 256 + B * ng * 4 <= 136 * 1024:
+        return "act_frag_kernel + gemv_wide_kernel"
     return "gemv_kernel (fp32)"
 
 

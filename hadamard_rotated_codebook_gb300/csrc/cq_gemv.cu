@@ -217,12 +217,16 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
     // matrices with inputs up to 15 groups, a streamed launch for wider
     // ones); the rest run here.
     int fast_idx[CQ_MAX_GROUPED], nfast = 0, stream_idx[CQ_MAX_GROUPED], nstream = 0;
+    int wide_idx[CQ_MAX_GROUPED], nwide = 0;
     bool is_fast[CQ_MAX_GROUPED];
     for (int i = 0; i < n; ++i) {
         const bool sf = gemv_stream_eligible(d[i]);
-        is_fast[i] = sf || gemv_fast_eligible(d[i]);
+        const bool ff = !sf && gemv_fast_eligible(d[i]);
+        const bool wf = !sf && !ff && gemv_wide_eligible(d[i]);
+        is_fast[i] = sf || ff || wf;
         if (sf) stream_idx[nstream++] = i;
-        else if (is_fast[i]) fast_idx[nfast++] = i;
+        else if (ff) fast_idx[nfast++] = i;
+        else if (wf) wide_idx[nwide++] = i;
     }
     if (nfast) {
         int st2 = launch_gemv_fast(d, fast_idx, nfast, stream);
@@ -230,6 +234,10 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
     }
     if (nstream) {
         int st2 = launch_gemv_stream(d, stream_idx, nstream, stream);
+        if (st2) return st2;
+    }
+    if (nwide) {
+        int st2 = launch_gemv_wide(d, wide_idx, nwide, stream);
         if (st2) return st2;
     }
     // One launch per code width present; each launch walks all descriptors of

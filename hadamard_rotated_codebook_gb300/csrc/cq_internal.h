@@ -65,6 +65,11 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
 // launches over d[idx[0..n)].
 bool gemv_stream_eligible(const cq_gemv_desc &d);
 int launch_gemv_stream(const cq_gemv_desc *d, const int *idx, int n, void *stream);
+// Tensor-core GEMV for the other shapes at group 128 (wide inputs, 3-bit
+// codes, batches up to 16; cq_gemv_wide.cu): a rotation launch into a
+// workspace, then the products; which descriptors, and the launches.
+bool gemv_wide_eligible(const cq_gemv_desc &d);
+int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream);
 
 
 // --------------------------------------------------------------- gemm --

@@ -141,13 +141,19 @@ int cq_act_quant_int8(const float *X, int M, int in, int8_t *Xq, float *s,
  * which equals W_hat x_b exactly in real arithmetic: the activation is
  * rotated once per group (in-register fast Walsh-Hadamard transform) and the
  * weights are never expanded to a dense matrix ([CF] "How the kernel reads
- * it"). On the tensor-core paths (B <= 4: 1-, 2- and 4-bit codes at group
- * 128 with in < 2048; for 2048 <= in <= 4096 every code width at group 128,
- * and groups of 64 other than 3-bit, through one persistent block per SM
- * that streams the code rows) the codebook levels are rounded to fp16 and
- * multiplied with z split into fp16 hi + lo terms, accumulating in fp32;
- * other shapes (B > 4, and the rest of group 64 and 3-bit codes) use fp32
- * arithmetic.
+ * it"). Every shape at group 128 runs on the tensor cores (mma.sync, fp32
+ * accumulation) with the codebook levels rounded to fp16: B <= 4 with 1-, 2-
+ * and 4-bit codes and in < 2048 in one launch whose blocks rotate their own
+ * activation; B <= 4 with 2048 <= in <= 4096 (every width, and groups of 64
+ * other than 3-bit) through one persistent block per SM that streams the
+ * code rows; the other group-128 shapes (3-bit codes, other input widths up
+ * to 128 groups, batches 5 to 16) as a rotation launch, which writes each
+ * distinct activation's MMA fragments once into a library-owned device
+ * workspace (grown on demand: make one untimed call before capturing a CUDA
+ * graph), followed by the products. z enters as fp16 hi + lo terms for
+ * B <= 4 and as one fp16 term for B >= 5. The remaining shapes (the rest of
+ * group 64, batches of 5 to 16 with too many groups for the workspace's
+ * shared-memory stage) use fp32 arithmetic.
  * x: fp32 [B][in] (x_dtype = CQ_X_F32, x_scale ignored, may be NULL) or
  *    int8 [B][in] with x_scale fp32 [B] (x_dtype = CQ_X_I8).
  * y: fp32 [B][out], fully overwritten.
