@@ -85,7 +85,7 @@ constexpr float kInvSqrt128 = 0.08838834764831845f;
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -138,7 +138,7 @@ __device__ __forceinline__ void load_x_bg(const FastMat &A, int b, int g, int la
 // hi | lo of sigma * z[k], sigma a power of two per (b, g) (|sigma z| <=
 // 2^14, so hi + lo carries z to ~2^-22 relative); returns 1/sigma.
 template <bool G64 = false>
-__device__ float rotate_bg(float (&v)[4], int lane, uint32_t *terms) {
+__device__ float rotate_bg(float (&v)[4], int lane, uint32_t *terms, bool ints) {
     float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
     v[0] = a0 + a2;
     v[1] = a1 + a3;
@@ -151,10 +151,15 @@ __device__ float rotate_bg(float (&v)[4], int lane, uint32_t *terms) {
             const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
             v[i] = (lane & m) ? o - v[i] : v[i] + o;
         }
-    float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    // int8 activations give integers |z| <= 128 * 128, which hi + lo carry
+    // exactly unscaled; otherwise scale by a power of two to |sigma z| <= 2^14
+    float sigma = 1.0f;
+    if (!ints) {
+        float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
-    for (int m = 16; m; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-    const float sigma = pow2_scale(mx, 16384.0f);
+        for (int m = 16; m; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        sigma = pow2_scale(mx, 16384.0f);
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float x = __fmul_rn(v[i], sigma);
@@ -277,6 +282,7 @@ __device__ __forceinline__ void lut4_group(float (&acc)[4], uint4 cr, uint4 cs, 
 // a byte -> four fp16 levels (16 copies, so that a half-warp's 8-byte lookups
 // hit distinct banks); 4-bit codes a byte -> two levels (32 copies); 1-bit
 // codes a nibble -> four levels (16 copies).
+static_assert(kThreads == 256, "one table entry per thread");
 template <bool WITH3 = false>  // 3-bit tables only where the kernel takes 3-bit codes
 __device__ __forceinline__ void build_level_table(int kind, const __half *lv, uint8_t *tab) {
     if (WITH3 && kind == 3) {  // a 6-bit code pair -> two fp16 levels, 32 copies
@@ -294,19 +300,21 @@ __device__ __forceinline__ void build_level_table(int kind, const __half *lv, ui
                 (uint32_t)__half_as_ushort(lv[(v >> 2) & 1]) | ((uint32_t)__half_as_ushort(lv[v >> 3]) << 16));
         }
     } else if (kind == 0) {
-        uint2 *t = reinterpret_cast<uint2 *>(tab);
-        for (int e = threadIdx.x; e < 256 * 16; e += kThreads) {
-            const int v = e >> 4;
-            t[e] = make_uint2(
-                (uint32_t)__half_as_ushort(lv[v & 3]) | ((uint32_t)__half_as_ushort(lv[(v >> 2) & 3]) << 16),
-                (uint32_t)__half_as_ushort(lv[(v >> 4) & 3]) | ((uint32_t)__half_as_ushort(lv[v >> 6]) << 16));
-        }
+        // one entry per thread, written to its 16 replica slots in an order
+        // rotated by the entry (a half-warp's stores fall in distinct banks)
+        const int v = threadIdx.x;
+        const uint2 e = make_uint2(
+            (uint32_t)__half_as_ushort(lv[v & 3]) | ((uint32_t)__half_as_ushort(lv[(v >> 2) & 3]) << 16),
+            (uint32_t)__half_as_ushort(lv[(v >> 4) & 3]) | ((uint32_t)__half_as_ushort(lv[v >> 6]) << 16));
+        uint2 *t = reinterpret_cast<uint2 *>(tab) + 16 * v;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) t[(r + v) & 15] = e;
     } else {
-        uint32_t *t = reinterpret_cast<uint32_t *>(tab);
-        for (int e = threadIdx.x; e < 256 * 32; e += kThreads) {
-            const int v = e >> 5;
-            t[e] = (uint32_t)__half_as_ushort(lv[v & 15]) | ((uint32_t)__half_as_ushort(lv[v >> 4]) << 16);
-        }
+        const int v = threadIdx.x;  // one entry per thread, 32 replica slots
+        const uint32_t e = (uint32_t)__half_as_ushort(lv[v & 15]) | ((uint32_t)__half_as_ushort(lv[v >> 4]) << 16);
+        uint32_t *t = reinterpret_cast<uint32_t *>(tab) + 32 * v;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) t[(r + v) & 31] = e;
     }
 }
 
@@ -327,7 +335,7 @@ __device__ __forceinline__ void rotate_activation(const FastMat &M, uint8_t *ter
         for (int b = 0; b < kMaxFastB; ++b) {
             if (b >= B) break;
             if (g != warp) load_x_bg(M, b, g, lane, xv[b]);
-            const float inv = rotate_bg<G64>(xv[b], lane, terms[b]);
+            const float inv = rotate_bg<G64>(xv[b], lane, terms[b], M.xdt == CQ_X_I8);
             if (lane == 0) ginv[b * ng + g] = inv;
         }
         __syncwarp();
