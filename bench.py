@@ -898,6 +898,61 @@ def bench_kv(cx):
                                      kernel="kv_attend_warp_kernel<3>", algorithmic_bytes_per_launch=algo)}
 
 
+def bench_g64_gemm(cx, M=2048):
+    """The GEMM at M=2048 int8 tokens over group-64 CQ2 and binary weights
+    beside group-128 CQ2: 16 matrices of 4096 x 512 (weights rotated back on
+    chip) and 4 of 4096 x 4096 (rotated activations), one grouped call per
+    step; the fp32 outputs (512 MB and 128 MB) exceed L2."""
+    import numpy as np
+    C, S, torch, stream = cx.C, cx.S, cx.torch, cx.stream
+    res = {}
+    cases = (("gemm_cq2_group64_in512", 64, 2, 16, 512), ("gemm_binary_in512", 128, 1, 16, 512),
+             ("gemm_cq2_group128_in512", 128, 2, 16, 512), ("gemm_binary_in4096", 128, 1, 4, 4096),
+             ("gemm_cq2_group128_in4096", 128, 2, 4, 4096))
+    for name, group, bits, nmat, n_in in cases:
+        out = 4096
+        cb = C.cq_codebook_init(bits, group)
+        nb = C.cq_packed_bytes(out, n_in, group, bits)
+        Xq, xs = C.cq_act_quant_int8(S.normal((M, n_in), 33000 + n_in, device=cx.device))
+        items = []
+        for i in range(nmat):
+            blob = torch.from_numpy(S.random_blob(out * n_in * bits // 8, out * n_in // group,
+                                                  34000 + 100 * bits + group + i)).to(cx.device)
+            items.append(dict(blob=blob, out=out, **{"in": n_in}, bits=bits, codebook=cb, Xq=Xq, x_scale=xs,
+                              group=group, Y=torch.empty((M, out), dtype=torch.float32, device=cx.device)))
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                C.cq_gemm_grouped(items)
+        stream.synchronize()
+
+        def steps():
+            for _ in range(5):
+                C.cq_gemm_grouped(items)
+
+        g = graph_of(torch, stream, steps)
+        reps = 20
+        ms = cx.timed(g.replay, reps) / (5 * reps)
+        C.cq_device_status(cx.device)
+        flops = 2.0 * M * out * n_in * nmat
+        tflops = flops / (ms * 1e-3) / 1e12
+        toks, rows = sample_rows(M, 4), sample_rows(out, 8)
+        td, rd = torch.from_numpy(toks).to(cx.device), torch.from_numpy(rows).to(cx.device)
+        x = Xq[td].cpu().numpy().astype(np.float64) * xs[td].cpu().numpy().astype(np.float64)[:, None]
+        per = [dict(blob=host_sub_blob(it["blob"].cpu().numpy(), out, n_in, bits, rows, group), rows=rows,
+                    n_in=n_in, bits=bits, group=group, cb=np.asarray(cb), x=x,
+                    y=it["Y"][td][:, rd].cpu().numpy()) for it in items[:2]]
+        cx.samples.add(("group64_binary", name), "gemm", per=per)
+        res[name] = {"metric": f"CQ GEMM TFLOP/s at M={M}, {nmat} x {out}x{n_in}, group {group}, {bits}-bit codes",
+                     "value": round(cx.world * tflops, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
+                     "steps": 5 * reps, "packed_bytes_per_step": nmat * nb,
+                     "l2": f"outputs larger than L2 (fp32 Y, {4 * M * out * nmat / 1e6:.0f} MB per step)",
+                     "tensor_view": {"achieved": round(tflops, 2), "peak": cx.peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                     "frac": round(tflops / cx.peaks["bf16_tflops"], 4),
+                                     "peak_source": cx.peak_kind + " (bf16 dense; fp16 operands run at the same rate)"}}
+        del items, g
+    return res
+
+
 def bench_g64(cx):
     """Group-64 CQ2 and binary (group 128) weights: one grouped GEMV launch
     over 64 matrices of 4096 x 4096 (batch 1, fp32 activations), the set
@@ -944,6 +999,7 @@ def bench_g64(cx):
                      "roofline": hbm_roofline(gbs, cx.peaks, cx.peak_kind, None,
                                               kernel="gemv_stream_kernel", algorithmic_bytes_per_launch=algo)}
         del items, plan, g
+    res.update(bench_g64_gemm(cx))
     # encoder at group 64
     cb = C.cq_codebook_init(2, 64)
     ne = 8
@@ -1171,7 +1227,7 @@ def oracle_leg(result, samples, budget_s=10.0):
             stats, n = [], 0
             for s in ss:
                 for p in s["per"]:
-                    What = O.dequant(p["blob"], len(p["rows"]), p["n_in"], p["bits"], p["cb"])
+                    What = O.dequant(p["blob"], len(p["rows"]), p["n_in"], p["bits"], p["cb"], p.get("group", 128))
                     y_ref, bd = O.matmul(What, p["x"])
                     stats.append(_product_stats(p["y"], y_ref, bd))
                     n += p["y"].size

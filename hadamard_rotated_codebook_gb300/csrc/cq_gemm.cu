@@ -508,8 +508,9 @@ struct Mat {
     const float *xs;
     float *Y;
     int out, ng, M, lut, act, n_tiles, m_tiles, tiles_before, runs_before;
-    int w;  // code width in bits (2: CQ2 and ternary, 3, 4)
+    int w;  // code width in bits (1: binary, 2: CQ2 and ternary, 3, 4) | kG64 for groups of 64
 };
+constexpr int kG64 = 0x100;  // Mat::w flag: groups of 64 (two norms per 128-wide span)
 
 struct Params {
     CUtensorMap tmap[kMaxActs];  // one per distinct rotated activation
@@ -747,13 +748,18 @@ __device__ __forceinline__ void fwht64(float (&a)[64]) {
 // inputs k and k+64 that the first step of H_128 combines are read at once,
 // tab[v] = c[v & 3] + c[v >> 2] and tab[16 + v] = c[v & 3] - c[v >> 2] for
 // the nibble v = q[k] | q[k+64] << 2; other widths: tab[q] = c[q].
-template <int W>
+//
+// Groups of 64 (G64): each 64-wide half of a span is a group of its own,
+// with its own norm, so segment s holds H_64 c[q] of inputs 64 s .. 64 s + 63
+// scaled by n[o][2g + s] / sqrt(64) ("Cactus Quants": the group is the unit
+// of the rotation and of the norm).
+template <int W, bool G64>
 __device__ __forceinline__ bool expand_row(const tc2::Mat &G, const float *levels, float *tab, int o, int e,
                                            uint8_t *sW, uint64_t *w_empty, uint64_t *w_full, uint32_t &pe,
                                            volatile int *abort) {
     const int lane = threadIdx.x & 31;
     __syncwarp();  // the previous run's reads of the table are done
-    if (W == 2) {
+    if (W == 2 && !G64) {
         const int v = lane & 15;
         tab[lane] = lane < 16 ? levels[v & 3] + levels[v >> 2] : levels[v & 3] - levels[v >> 2];
     } else if (lane < 16) {
@@ -763,25 +769,32 @@ __device__ __forceinline__ bool expand_row(const tc2::Mat &G, const float *level
     const bool orow = o < G.out;
     const int ng = G.ng;
     const uint4 *src = reinterpret_cast<const uint4 *>(G.codes + (size_t)o * ng * 16 * W);
-    const __half *nsrc = G.norms + (size_t)o * ng;
+    const int nper = G64 ? 2 : 1;  // norms per 128-wide span
+    const __half *nsrc = G.norms + (size_t)o * ng * nper;
     uint32_t w[4 * W];
-    float nrm = 0.0f;
+    float nrm = 0.0f, nrm1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < W; ++i) {
         const uint4 v = orow ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
         w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
     }
-    if (orow) nrm = __half2float(nsrc[0]);
+    if (orow) {
+        nrm = __half2float(nsrc[0]);
+        if (G64) nrm1 = __half2float(nsrc[1]);
+    }
     for (int g = 0; g < ng; ++g) {
         uint32_t wn[4 * W];
-        float nn = 0.0f;
+        float nn = 0.0f, nn1 = 0.0f;
         const bool more = orow && g + 1 < ng;
 #pragma unroll
         for (int i = 0; i < W; ++i) {
             const uint4 v = more ? __ldg(src + (g + 1) * W + i) : make_uint4(0, 0, 0, 0);
             wn[4 * i] = v.x, wn[4 * i + 1] = v.y, wn[4 * i + 2] = v.z, wn[4 * i + 3] = v.w;
         }
-        if (more) nn = __half2float(nsrc[g + 1]);
+        if (more) {
+            nn = __half2float(nsrc[(g + 1) * nper]);
+            if (G64) nn1 = __half2float(nsrc[(g + 1) * nper + 1]);
+        }
         if (!tc2::wait(&w_empty[g], (pe >> g) & 1u, abort, 0x47480016u)) return false;
         pe ^= 1u << g;
         const float sc = nrm * kInvSqrt128;
@@ -792,9 +805,13 @@ __device__ __forceinline__ bool expand_row(const tc2::Mat &G, const float *level
             // from being computed once and held across the passes)
 #pragma unroll
             for (int i = 0; i < 4 * W; ++i) asm volatile("" : "+r"(w[i]));
-            // a = v_lo + v_hi (pass 0) or v_lo - v_hi (pass 1)
+            // a = v_lo + v_hi (pass 0) or v_lo - v_hi (pass 1); groups of
+            // 64: a = v_lo (pass 0) or v_hi (pass 1)
             float a[64];
-            if (W == 2) {
+            if (G64) {
+#pragma unroll
+                for (int k = 0; k < 64; ++k) a[k] = tab[code_at<W>(w, 64 * pass + k)];
+            } else if (W == 2) {
                 const float *t = tab + 16 * pass;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {  // word m: codes 16m .. 16m+15; word m+4: the same + 64
@@ -812,13 +829,14 @@ __device__ __forceinline__ bool expand_row(const tc2::Mat &G, const float *level
                 for (int k = 0; k < 64; ++k) a[k] = fmaf(sgn, tab[code_at<W>(w, k + 64)], tab[code_at<W>(w, k)]);
             }
             fwht64(a);
+            const float scp = G64 ? (pass ? nrm1 : nrm) * 0.125f : sc;  // n / sqrt(64) per half
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 uint4 c;
-                c.x = tc::h2_bits(__floats2half2_rn(a[8 * j] * sc, a[8 * j + 1] * sc));
-                c.y = tc::h2_bits(__floats2half2_rn(a[8 * j + 2] * sc, a[8 * j + 3] * sc));
-                c.z = tc::h2_bits(__floats2half2_rn(a[8 * j + 4] * sc, a[8 * j + 5] * sc));
-                c.w = tc::h2_bits(__floats2half2_rn(a[8 * j + 6] * sc, a[8 * j + 7] * sc));
+                c.x = tc::h2_bits(__floats2half2_rn(a[8 * j] * scp, a[8 * j + 1] * scp));
+                c.y = tc::h2_bits(__floats2half2_rn(a[8 * j + 2] * scp, a[8 * j + 3] * scp));
+                c.z = tc::h2_bits(__floats2half2_rn(a[8 * j + 4] * scp, a[8 * j + 5] * scp));
+                c.w = tc::h2_bits(__floats2half2_rn(a[8 * j + 6] * scp, a[8 * j + 7] * scp));
                 sts128(row + pass * tc::kSegBytes + ((j ^ (e & 7)) << 4), c);
             }
         }
@@ -829,6 +847,7 @@ __device__ __forceinline__ bool expand_row(const tc2::Mat &G, const float *level
 #pragma unroll
         for (int i = 0; i < 4 * W; ++i) w[i] = wn[i];
         nrm = nn;
+        nrm1 = nn1;
     }
     return true;
 }
@@ -1104,9 +1123,17 @@ __global__ void __launch_bounds__(tc3::kThreads, 1) gemm_x8_kernel(const __grid_
             const tc2::Mat &G = tc2::warp_mat(p, c.mat, &s_mat[warp]);
             const float *levels = p.lut[G.lut];
             const int o = c.o0() + e;
-            const bool ok = G.w == 2   ? tc3::expand_row<2>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort)
-                            : G.w == 3 ? tc3::expand_row<3>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort)
-                                       : tc3::expand_row<4>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort);
+            bool ok;
+            switch (G.w) {
+            case 1: ok = tc3::expand_row<1, false>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort); break;
+            case 2: ok = tc3::expand_row<2, false>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort); break;
+            case 3: ok = tc3::expand_row<3, false>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort); break;
+            case 4: ok = tc3::expand_row<4, false>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort); break;
+            case 1 | tc2::kG64: ok = tc3::expand_row<1, true>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort); break;
+            case 2 | tc2::kG64: ok = tc3::expand_row<2, true>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort); break;
+            case 3 | tc2::kG64: ok = tc3::expand_row<3, true>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort); break;
+            default: ok = tc3::expand_row<4, true>(G, levels, lv, o, e, sW, w_empty, w_full, pe, &s_abort); break;
+            }
             if (!ok) break;
         }
     }
@@ -1385,7 +1412,7 @@ static int run_gemm_x8(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t 
         G.M = d[i].M;
         G.lut = li;
         G.act = map_of[a];
-        G.w = W;
+        G.w = W | (d[i].group == kGroup64 ? tc2::kG64 : 0);
         G.n_tiles = (G.out + tc::kTileRows - 1) / tc::kTileRows;
         G.m_tiles = (G.M + tc2::kTok - 1) / tc2::kTok;
         G.tiles_before = tiles;
@@ -1444,7 +1471,7 @@ static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws
     }
     if (!any_wide) return CQ_OK;
     cudaError_t e;
-    for (int W = 2; W <= 4; ++W) {
+    for (int W = 1; W <= 4; ++W) {
         static thread_local GemmParams p;  // large: off the stack, one per host thread
         p.n = 0;
         int nlut = 0, tiles = 0;
@@ -1492,6 +1519,7 @@ static int run_gemm(const cq_gemm_desc *d, int n, const ActPlan &pl, uint8_t *ws
         const int grid = std::min(tiles, sm_count() * 2);
         int rc = CQ_OK;
         switch (W) {
+        case 1: rc = launch_tc<1>(p, grid, smem, st); break;
         case 2: rc = launch_tc<2>(p, grid, smem, st); break;
         case 3: rc = launch_tc<3>(p, grid, smem, st); break;
         case 4: rc = launch_tc<4>(p, grid, smem, st); break;

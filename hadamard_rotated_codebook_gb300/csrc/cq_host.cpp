@@ -310,8 +310,12 @@ int cq_kv_attend(const cq_kv_geom *g, const cq_kv_seq *seqs, int n_seqs, void *s
 }
 
 static int check_gemm_desc(const cq_gemm_desc &d, int i) {
-    int st = check_matrix(d.out, d.in, d.group, d.bits, false);
+    // binary codes at any width; groups of 64 on inputs of whole 128-wide
+    // spans up to 512 (the product that rotates the weight rows)
+    int st = check_matrix(d.out, d.in, d.group, d.bits, true);
     if (st) return prefix_error(st, i);
+    if (d.group == kGroup64 && (d.in % kGroup != 0 || d.in > 4 * kGroup))
+        return prefix_error(set_error(CQ_ERR_SHAPE, "groups of 64 need in a multiple of 128 and at most 512, got %d", d.in), i);
     if ((st = check_codebook(d.codebook, d.bits))) return prefix_error(st, i);
     if (d.M < 0) return set_error(CQ_ERR_SHAPE, "descriptor %d: negative M", i);
     if (d.M > 0 && d.out > 0 && !d.Y) return set_error(CQ_ERR_ARG, "descriptor %d: null Y", i);

@@ -33,14 +33,15 @@
  *    "Five regions": an output row is contiguous along the reduction axis.
  *  - Groups: cq_encode, cq_gemv* and cq_gather_rows take group 128 (what
  *    the pages ship) or 64 (which the OpenNeedle engine also tests);
- *    cq_gemm* and the KV cache take group 128. Other powers of two are valid
+ *    cq_gemm* take group 64 only on inputs that are a multiple of 128 and
+ *    at most 512; the KV cache takes group 128. Other powers of two are valid
  *    in the format and container and are rejected by the device entry points
  *    with CQ_ERR_SHAPE.
  *  - bits: 2, 3, 4 (CQ2/CQ3/CQ4, 4/8/16 levels), 5, the ternary marker of
  *    [NJ] "Shared codebooks" (3 levels {-c, 0, +c}, stored as 2-bit crumbs),
  *    or 1, binary codes ([CF] "Cactus Quants": eight per byte, two
- *    closed-form levels +-sqrt(2/pi)/sqrt(group)). cq_gemm* and the KV cache
- *    do not take binary codes.
+ *    closed-form levels +-sqrt(2/pi)/sqrt(group)). The KV cache does not
+ *    take binary codes.
  *  - A codebook is cq_levels(bits) floats, strictly increasing, already
  *    divided by sqrt(group) ([NJ] "Shared codebooks"). For bits = 5 it is
  *    {-c, 0, +c}.
@@ -214,7 +215,8 @@ int cq_gemv_shared(const uint8_t *const *blobs, const int *outs, int n_mats,
  * is cheaper ("Reconstructing one group": n <c[q], H x> = <n H c[q], x>):
  *  - in <= 512: per run of token tiles, the 128 weight rows of a tile are
  *    expanded and rotated back once, W''[o][k] = fp16(n[o][g] (H c[q])[k]),
- *    and meet the int8 activations directly (exact in fp16);
+ *    and meet the int8 activations directly (exact in fp16); groups of 64
+ *    are rotated back half-span by half-span with H_64 and their own norms;
  *  - in > 512: the activations are rotated exactly in integers per group
  *    (H0 Xq, |v| <= 16384), stored in fp16, and meet W'[o][k] =
  *    fp16(c[q] n[o][g]).

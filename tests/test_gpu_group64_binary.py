@@ -182,3 +182,66 @@ def test_gemv_more_streamed_matrices_than_one_launch_holds(C):
     torch.cuda.synchronize()
     for j, (y_ref, bound) in refs:
         check_matmul(ys[j].cpu().numpy(), y_ref, bound, f"matrix {j}")
+
+
+def _gemm_check(C, group, bits, out, n_in, M, seed, toks=None):
+    blob = _rand_blob(out, n_in, bits, group, seed)
+    cb = O.analytic_codebook(bits, group)
+    q, s = O.act_quant_int8(S.normal((M, n_in), seed + 1).numpy())
+    Y = C.cq_gemm(torch.from_numpy(blob).cuda(), out, n_in, bits, cb, torch.from_numpy(q).cuda(),
+                  torch.from_numpy(s).cuda(), group=group)
+    torch.cuda.synchronize()
+    toks = np.arange(M) if toks is None else np.asarray(toks)
+    xt = q[toks].astype(np.float64) * s[toks].astype(np.float64)[:, None]
+    y_ref, bound = O.matmul(O.dequant(blob, out, n_in, bits, cb, group), xt)
+    check_matmul(Y.cpu().numpy()[toks], y_ref, bound, f"gemm g{group} cq{bits} M={M} {out}x{n_in}")
+
+
+@pytest.mark.parametrize("group,bits", [(64, 1), (64, 2), (64, 3), (64, 4), (64, 5), (128, 1)])
+@pytest.mark.parametrize("shape", [(200, 384), (3, 128), (512, 512)])
+@pytest.mark.parametrize("M", [64, 2048])
+def test_gemm_parity(C, group, bits, shape, M):
+    """Tensor-core product over int8 tokens: groups of 64 (each half of a
+    128-wide span rotated by H_64 with its own norm) and binary codes."""
+    out, n_in = shape
+    toks = None if M <= 64 else [0, 1, 130, 1023, 1500, 2047]
+    _gemm_check(C, group, bits, out, n_in, M, 300 + bits + group + out, toks)
+
+
+@pytest.mark.parametrize("shape", [(130, 1000), (64, 4096)])
+@pytest.mark.parametrize("M", [64, 2048])
+def test_gemm_binary_rotated_activations(C, shape, M):
+    """Binary codes on inputs wider than 512 (the product over rotated
+    activations), ragged input width included."""
+    out, n_in = shape
+    toks = None if M <= 64 else [0, 5, 999, 2047]
+    _gemm_check(C, 128, 1, out, n_in, M, 400 + out, toks)
+
+
+def test_gemm_grouped_mixes_group64_binary_and_cq2(C):
+    n_in = 256
+    q, s = O.act_quant_int8(S.normal((70, n_in), 410).numpy())
+    xq, xs = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+    xt = q.astype(np.float64) * s.astype(np.float64)[:, None]
+    items, refs = [], []
+    for j, (g, b) in enumerate([(64, 2), (128, 1), (128, 2), (64, 1), (64, 4)]):
+        out = 90 + 40 * j
+        blob = _rand_blob(out, n_in, b, g, 411 + j)
+        cb = O.analytic_codebook(b, g)
+        items.append(dict(blob=torch.from_numpy(blob).cuda(), out=out, **{"in": n_in}, bits=b, codebook=cb,
+                          Xq=xq, x_scale=xs, group=g))
+        refs.append(O.matmul(O.dequant(blob, out, n_in, b, cb, g), xt))
+    Ys = C.cq_gemm_grouped(items)
+    torch.cuda.synchronize()
+    for j, (Y, (y_ref, bound)) in enumerate(zip(Ys, refs)):
+        check_matmul(Y.cpu().numpy(), y_ref, bound, f"grouped item {j}")
+
+
+@pytest.mark.parametrize("n_in", [200, 640])
+def test_gemm_group64_rejects_unsupported_widths(C, n_in):
+    """Groups of 64 in the product: whole 128-wide spans, at most 512 inputs."""
+    blob = _rand_blob(8, n_in, 2, 64, 420)
+    q = torch.zeros((4, n_in), dtype=torch.int8, device="cuda")
+    s = torch.ones(4, dtype=torch.float32, device="cuda")
+    with pytest.raises(C.CQError):
+        C.cq_gemm(torch.from_numpy(blob).cuda(), 8, n_in, 2, O.analytic_codebook(2, 64), q, s, group=64)

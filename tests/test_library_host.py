@@ -91,11 +91,17 @@ def test_device_entry_points_reject_bad_arguments_before_launch(C):
     assert lib.cq_encode(None, 4, 128, 32, 2, cb, None, None) == _capi.CQ_ERR_SHAPE
     assert b"group = 64 or 128" in lib.cq_last_error()
     assert lib.cq_encode(None, 4, 128, 64, 2, cb, None, None) == _capi.CQ_ERR_ARG  # group 64 taken; null W
+    # the GEMM takes groups of 64 on whole 128-wide spans up to 512 inputs;
+    # the sizes pass and the unaligned pointers are the error
     g64 = _capi.GemmDesc(blob=1, Xq=1, x_scale=1, Y=1, codebook=cb, out=4, in_=128, group=64, bits=2, M=8)
-    assert lib.cq_gemm_grouped(ctypes.byref(g64), 1, None) == _capi.CQ_ERR_SHAPE  # the GEMM keeps group 128
+    assert lib.cq_gemm_grouped(ctypes.byref(g64), 1, None) == _capi.CQ_ERR_ARG
+    for n_in in (192, 640):
+        g64.in_ = n_in
+        assert lib.cq_gemm_grouped(ctypes.byref(g64), 1, None) == _capi.CQ_ERR_SHAPE
+        assert b"groups of 64" in lib.cq_last_error()
     b1 = (ctypes.c_float * 2)(-0.07, 0.07)
-    g1 = _capi.GemmDesc(blob=1, Xq=1, x_scale=1, Y=1, codebook=b1, out=4, in_=128, group=128, bits=1, M=8)
-    assert lib.cq_gemm_grouped(ctypes.byref(g1), 1, None) == _capi.CQ_ERR_SHAPE  # and no binary codes
+    g1 = _capi.GemmDesc(blob=1, Xq=1, x_scale=1, Y=1, codebook=b1, out=4, in_=1000, group=128, bits=1, M=8)
+    assert lib.cq_gemm_grouped(ctypes.byref(g1), 1, None) == _capi.CQ_ERR_ARG  # binary codes taken
     assert lib.cq_encode(None, 4, 128, 128, 2, bad, None, None) == _capi.CQ_ERR_ARG
     assert b"increasing" in lib.cq_last_error()
     assert lib.cq_encode(None, 4, 128, 128, 7, cb, None, None) == _capi.CQ_ERR_ARG
