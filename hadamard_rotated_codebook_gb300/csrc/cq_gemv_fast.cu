@@ -202,16 +202,26 @@ __device__ void frag_words(const FastMat &A, const uint32_t (*terms)[kGroup], in
 // 32t + 4nu .. +3, i.e. byte nu (2-bit) or bytes 2nu, 2nu+1 (4-bit).
 // d[0], d[1]: row r, columns 2t, 2t+1 (hi, lo terms of batch t); d[2], d[3]:
 // row s.
+//
+// One lookup serves both rows: its index holds row r's codes of a position
+// pair in the low nibble and row s's codes of the same pair in the high
+// nibble, so the entry's two words are the fragment registers as they stand
+// (the table maps a byte to the levels of its four 2-bit fields).
 __device__ __forceinline__ void lut2_group(float (&acc)[4], uint2 cr, uint2 cs, const uint2 *tab_lane,
                                            const uint32_t (&fr)[kFragWords], float nr, float ns) {
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t wr[2] = {cr.x, cr.y}, ws[2] = {cs.x, cs.y};
+    uint32_t lo[2], hi[2];  // bytes: positions 4nu, 4nu+1 (lo) and 4nu+2, 4nu+3 (hi) of both rows
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        lo[i] = (wr[i] & 0x0f0f0f0fu) | ((ws[i] << 4) & 0xf0f0f0f0u);
+        hi[i] = ((wr[i] >> 4) & 0x0f0f0f0fu) | (ws[i] & 0xf0f0f0f0u);
+    }
 #pragma unroll
     for (int nu = 0; nu < 8; ++nu) {
-        const uint32_t br = __byte_perm(wr[nu >> 2], 0, 0x4440 + (nu & 3));
-        const uint32_t bs = __byte_perm(ws[nu >> 2], 0, 0x4440 + (nu & 3));
-        const uint2 er = tab_lane[br * 16], es = tab_lane[bs * 16];
-        mma_f16(d, er.x, es.x, er.y, es.y, fr[2 * nu], fr[2 * nu + 1]);
+        const uint2 e0 = tab_lane[__byte_perm(lo[nu >> 2], 0, 0x4440 + (nu & 3)) * 16];
+        const uint2 e1 = tab_lane[__byte_perm(hi[nu >> 2], 0, 0x4440 + (nu & 3)) * 16];
+        mma_f16(d, e0.x, e0.y, e1.x, e1.y, fr[2 * nu], fr[2 * nu + 1]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = fmaf(i >= 2 ? ns : nr, d[i], acc[i]);
@@ -219,13 +229,17 @@ __device__ __forceinline__ void lut2_group(float (&acc)[4], uint2 cr, uint2 cs, 
 
 // 1-bit codes: the lane's 4 code bytes of each row cover positions 32t ..
 // 32t+31; MMA nu takes positions 32t + 4nu .. +3, nibble nu of the word.
+// One lookup serves both rows, as for 2-bit codes: bit pairs of row r in
+// bits 0-1 and of row s in bits 2-3 of the nibble.
 __device__ __forceinline__ void lut1_group(float (&acc)[4], uint32_t cr, uint32_t cs, const uint2 *tab_lane,
                                            const uint32_t (&fr)[kFragWords], float nr, float ns) {
     float d[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t lo = (cr & 0x33333333u) | ((cs << 2) & 0xccccccccu);
+    const uint32_t hi = ((cr >> 2) & 0x33333333u) | (cs & 0xccccccccu);
 #pragma unroll
     for (int nu = 0; nu < 8; ++nu) {
-        const uint2 er = tab_lane[((cr >> (4 * nu)) & 15u) * 16], es = tab_lane[((cs >> (4 * nu)) & 15u) * 16];
-        mma_f16(d, er.x, es.x, er.y, es.y, fr[2 * nu], fr[2 * nu + 1]);
+        const uint2 e0 = tab_lane[((lo >> (4 * nu)) & 15u) * 16], e1 = tab_lane[((hi >> (4 * nu)) & 15u) * 16];
+        mma_f16(d, e0.x, e0.y, e1.x, e1.y, fr[2 * nu], fr[2 * nu + 1]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = fmaf(i >= 2 ? ns : nr, d[i], acc[i]);
@@ -713,8 +727,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
 
 bool gemv_stream_eligible(const cq_gemv_desc &d) {
     const int ng = in_padded(d.in) / kGroup, W = width_of(d.bits);
-    // groups of 64 in whole 128-spans only
-    const bool grp = d.group == kGroup || (d.group == kGroup64 && d.in % kGroup == 0 && W != 3);
+    // groups of 64 in whole 128-spans, and 3- and 4-bit codes at group 128
+    // (2-bit and 1-bit codes this wide take the split products of
+    // cq_gemv_wide.cu)
+    const bool grp = (d.group == kGroup64 && d.in % kGroup == 0 && W != 3) || (d.group == kGroup && W >= 3);
     return grp && d.out > 0 && (W >= 1 && W <= 4) && d.B <= kMaxFastB && ng >= 16 && ng <= kMaxFastNg;
 }
 
@@ -812,7 +828,7 @@ bool gemv_fast_eligible(const cq_gemv_desc &d) {
     const int W = width_of(d.bits);
     // 3-bit codes only on the streamed kernel (wide inputs): their product
     // branch would cost this kernel registers on the decode step
-    return W != 3 && (W >= 1 && W <= 4) && d.B <= kMaxFastB && ng <= kMaxFastNg && !gemv_stream_eligible(d);
+    return W != 3 && (W >= 1 && W <= 4) && d.B <= kMaxFastB && ng < 16 && !gemv_stream_eligible(d);
 }
 
 // Shared-memory needs of one launch (maxima over its matrices).

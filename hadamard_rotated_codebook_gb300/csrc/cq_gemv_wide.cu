@@ -1,6 +1,5 @@
-// cq_gemv_wide.cu -- tensor-core GEMV over CQ-packed weights for wide inputs
-// (16 groups and more) and for batches of 5 to 16: every code width at
-// group 128.
+// cq_gemv_wide.cu -- tensor-core GEMV over CQ-packed weights at group 128
+// for wide inputs (16 groups and more) and for batches of 5 to 16.
 //
 // Per group g of 128 inputs the product is the rotated-domain identity
 // (OpenNeedle docs/reference.md; "The .cact archive and Cactus Quants",
@@ -14,8 +13,10 @@
 //     fragment layout in a workspace (a lane's four positions are exactly
 //     two fragment words, so no shuffles are needed), with 1/sigma per
 //     (batch row, group).
-//  2. gemv_wide_kernel, launched as a programmatic dependent of the first:
-//     one block per SM walks an equal run of the call's 16-row tiles.
+//  2. the products, launched as programmatic dependents of the first:
+//     gemv_split_kernel (further below) for batches of 1 to 4 with 2-bit and
+//     1-bit codes, gemv_wide_kernel for the rest. In gemv_wide_kernel one
+//     block per SM walks an equal run of the call's 16-row tiles.
 //     Before it waits for the rotation it builds its level table and starts
 //     its code copies; then it copies the fragments of its matrix's
 //     activation into shared memory once, and streams the tiles through four
@@ -35,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <vector>
 
 #include "cq_internal.h"
 
@@ -68,6 +70,8 @@ struct WActParams {
     int task0[kWMaxActs + 1];  // first warp task of each activation
     uint32_t *frag;
     float *ginv;
+    unsigned int *zero;  // tile counters of the split products, cleared here
+    int n_zero;
     WAct a[kWMaxActs];
 };
 
@@ -90,6 +94,7 @@ __device__ __forceinline__ float w_pow2_scale(float amax, float lim) {
 __global__ void __launch_bounds__(kWThreads) act_frag_kernel(const __grid_constant__ WActParams p) {
     // the GEMV launched after this one may start its prologue at once
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    for (int i = blockIdx.x * kWThreads + threadIdx.x; i < p.n_zero; i += gridDim.x * kWThreads) p.zero[i] = 0u;
     const int lane = threadIdx.x & 31;
     const int task = blockIdx.x * kWWarps + (threadIdx.x >> 5);
     if (task >= p.task0[p.n]) return;
@@ -202,10 +207,10 @@ __device__ __forceinline__ void w_cp16(void *dst, const void *src, int src_bytes
 }
 
 // Level tables in shared memory at `tab`, replicated so that each lane reads
-// its own copy (conflict-free whatever the codes): 2-bit codes a byte -> four
-// fp16 levels (16 copies of 8 bytes), 4-bit codes a byte -> two levels (32
-// copies of 4 bytes), 1-bit codes a nibble -> four levels (16 copies), 3-bit
-// codes a 6-bit pair -> two levels (32 copies).
+// its own copy (conflict-free whatever the codes): 2-bit codes a byte -> the
+// fp16 levels of its four 2-bit fields (16 copies of 8 bytes), 4-bit codes a
+// byte -> two levels (32 copies of 4 bytes), 1-bit codes a nibble -> four
+// levels (16 copies), 3-bit codes a 6-bit pair -> two levels (32 copies).
 __device__ void w_build_table(int kind, const __half *lv, uint8_t *tab) {
     auto h = [&](int c) { return (uint32_t)__half_as_ushort(lv[c]); };
     if (kind == 0) {
@@ -261,23 +266,32 @@ __device__ __forceinline__ void w_load(const uint8_t *r0, const uint8_t *r1, int
 
 // The A fragment of MMA nu (positions 32t + 4nu .. +3 of the group):
 // {row gq positions 0-1, row gq+8 positions 0-1, row gq positions 2-3,
-// row gq+8 positions 2-3}, through the replicated level tables.
+// row gq+8 positions 2-3}, through the replicated level tables. For 2-bit
+// and 1-bit codes one lookup serves both rows: the index is made of row gq's
+// codes of a position pair (low bits) and row gq+8's codes of the same pair
+// (high bits), and the entry's two words are then fragment registers a0, a1
+// (or a2, a3) as they stand.
 template <int KIND>
 __device__ __forceinline__ void w_decode(const WCodes &c, int nu, const uint8_t *tab, int lane, uint32_t (&a)[4]) {
-    if (KIND == 0) {  // byte nu of the lane's 8 -> four levels
+    if (KIND == 0) {  // byte nu of the lane's 8: low nibbles (positions 0-1), high nibbles (2-3)
         const uint2 *tb = reinterpret_cast<const uint2 *>(tab) + (lane & 15);
-        const uint2 er = tb[__byte_perm(c.r[nu >> 2], 0, 0x4440 + (nu & 3)) * 16];
-        const uint2 es = tb[__byte_perm(c.s[nu >> 2], 0, 0x4440 + (nu & 3)) * 16];
-        a[0] = er.x, a[1] = es.x, a[2] = er.y, a[3] = es.y;
+        const uint32_t wr = c.r[nu >> 2], ws = c.s[nu >> 2];
+        const uint32_t lo = (wr & 0x0f0f0f0fu) | ((ws << 4) & 0xf0f0f0f0u);
+        const uint32_t hi = ((wr >> 4) & 0x0f0f0f0fu) | (ws & 0xf0f0f0f0u);
+        const uint2 e0 = tb[__byte_perm(lo, 0, 0x4440 + (nu & 3)) * 16];
+        const uint2 e1 = tb[__byte_perm(hi, 0, 0x4440 + (nu & 3)) * 16];
+        a[0] = e0.x, a[1] = e0.y, a[2] = e1.x, a[3] = e1.y;
     } else if (KIND == 1) {  // bytes 2nu, 2nu+1 of the lane's 16 -> two levels each
         const uint32_t *tb = reinterpret_cast<const uint32_t *>(tab) + lane;
         const uint32_t r = c.r[nu >> 1] >> (16 * (nu & 1)), s = c.s[nu >> 1] >> (16 * (nu & 1));
         a[0] = tb[(r & 0xffu) * 32], a[2] = tb[((r >> 8) & 0xffu) * 32];
         a[1] = tb[(s & 0xffu) * 32], a[3] = tb[((s >> 8) & 0xffu) * 32];
-    } else if (KIND == 2) {  // nibble nu of the lane's 4 bytes -> four levels
+    } else if (KIND == 2) {  // nibble nu of the lane's 4 bytes: bit pairs 0-1 (positions 0-1) and 2-3 (2-3)
         const uint2 *tb = reinterpret_cast<const uint2 *>(tab) + (lane & 15);
-        const uint2 er = tb[((c.r[0] >> (4 * nu)) & 15u) * 16], es = tb[((c.s[0] >> (4 * nu)) & 15u) * 16];
-        a[0] = er.x, a[1] = es.x, a[2] = er.y, a[3] = es.y;
+        const uint32_t lo = (c.r[0] & 0x33333333u) | ((c.s[0] << 2) & 0xccccccccu);
+        const uint32_t hi = ((c.r[0] >> 2) & 0x33333333u) | (c.s[0] & 0xccccccccu);
+        const uint2 e0 = tb[((lo >> (4 * nu)) & 15u) * 16], e1 = tb[((hi >> (4 * nu)) & 15u) * 16];
+        a[0] = e0.x, a[1] = e0.y, a[2] = e1.x, a[3] = e1.y;
     } else {  // the 6-bit code pairs at bits 12 nu and 12 nu + 6 of the lane's 12 bytes
         const uint32_t *tb = reinterpret_cast<const uint32_t *>(tab) + lane;
         const int b0 = 12 * nu, b1 = b0 + 6;
@@ -506,6 +520,481 @@ __global__ void __launch_bounds__(kWGThreads, 1) gemv_wide_kernel(const __grid_c
     if (!waited) asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
+
+// ----------------------------------------------------- split products --
+// gemv_split_kernel: the product step behind the same rotation launch, with
+// the work cut finer than a block's run of tiles and every warp on its own
+// pipeline. The host sends it batches of 1 to 4 with 2-bit and 1-bit codes
+// (the kernel itself takes every width and batches up to 16). A
+// unit is (matrix, k-slice of its groups, 16-row tile); units are numbered
+// matrix by matrix, k-slice by k-slice, tile fastest, and each block takes an
+// equal contiguous range of them, split evenly over its 16 warps. A matrix
+// is cut into k-slices only when its tiles alone would leave more than three
+// quarters of the warps idle (one 4096-row matrix has 256 tiles for 2432
+// warps); the k-slices of a tile then
+// leave their partial sums in a workspace and the last one to finish (a
+// counter per tile) adds them in k-slice order, so the result does not
+// depend on the order in which they finish.
+//
+// Every warp streams its own units through three shared-memory stages of
+// one chunk each (16 rows x 128 code bytes: four CQ2 groups, two CQ4 or CQ3
+// groups, eight binary groups): one lane per row issues a 1-D TMA bulk copy
+// of the row's chunk (completion on the stage's mbarrier) and a 4-byte
+// cp.async of its norms. No block barrier runs inside the loop. A block
+// copies the fragments of the (matrix, k-slice) pairs of its range into
+// shared memory once, after the rotation launch is complete.
+constexpr int kSWarps = 16;
+constexpr int kSThreads = 32 * kSWarps;
+constexpr int kSStages = 3;
+constexpr int kSMaxMats = 128;
+constexpr int kSMaxPairs = 24;  // (matrix, k-slice) pairs of one block's range
+constexpr int kSNormRow = 16;   // bytes of norms per row and stage (up to eight groups)
+
+struct SMat {
+    const uint8_t *codes;
+    const __half *norms;
+    float *y;
+    const float *xs;
+    long long unit0;  // first unit of the matrix
+    long long frag;   // word offset of its activation's fragments
+    long long ginv;   // float offset of its activation's 1/sigma
+    int out, ng, B, xdt, cols;
+    int tiles, nks, gk;  // 16-row tiles, k-slices, groups per k-slice
+    int cnt0;            // first tile counter (k-sliced matrices)
+    long long part0;     // first partial-sum slot [unit][16][B] (k-sliced matrices)
+};
+
+struct SParams {
+    int n_mats;
+    long long total_units;
+    long long units_before[kSMaxMats + 1];
+    const uint32_t *frag;
+    const float *ginv;
+    float *part;
+    unsigned int *cnt;
+    unsigned int *status;
+    int smem_frag, frag_budget, smem_stage;
+    __half lut[16];
+    SMat m[kSMaxMats];
+};
+
+static_assert(sizeof(SParams) <= 32000, "kernel parameter block");
+
+// Code bytes per group and groups per chunk of each kind.
+__host__ __device__ constexpr int s_gbytes(int kind) { return kind == 0 ? 32 : kind == 1 ? 64 : kind == 2 ? 16 : 48; }
+__host__ __device__ constexpr int s_gc(int kind) { return kind == 0 ? 4 : kind == 1 ? 2 : kind == 2 ? 8 : 2; }
+// Row stride of a stage: the chunk plus padding that spreads a warp's reads
+// of its rows over the banks (as for the sliced kernel's stages).
+__host__ __device__ constexpr int s_rs(int kind) {
+    return kind == 0 ? 160 : kind == 1 ? 192 : kind == 2 ? 144 : 176;
+}
+__host__ __device__ constexpr int s_stage_bytes(int kind) { return 16 * s_rs(kind) + 16 * kSNormRow; }
+
+// One (matrix, k-slice) pair of a block's range and where its fragments and
+// 1/sigma sit in shared memory.
+struct SPair {
+    long long u_end;  // units of the pair in the range end here
+    int m, s, g_lo, g_n, frag_off, ginv_off;  // frag_off in 16-byte units, ginv_off in floats
+};
+
+__device__ __forceinline__ uint32_t s_smem(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Bounded wait on an mbarrier phase: false after about a second.
+__device__ __forceinline__ bool s_wait(uint32_t bar, uint32_t parity) {
+    for (unsigned it = 0; it < (1u << 20); ++it) {
+        uint32_t r;
+        asm volatile(
+            "{\n .reg .pred pp;\n mbarrier.try_wait.parity.shared::cta.b64 pp, [%1], %2, %3;\n selp.u32 %0, 1, 0, pp;\n}\n"
+            : "=r"(r)
+            : "r"(bar), "r"(parity), "r"(1000u)
+            : "memory");
+        if (r) return true;
+    }
+    return false;
+}
+
+// Two groups of a chunk (g, g + 1) as two independent MMA chains, for one
+// column block; the second group's codes, fragments and norms are zero when
+// `two` is false (its chain then adds nothing).
+template <int KIND, bool HILO>
+__device__ __forceinline__ void s_group2(const uint8_t *r0, int rs, const uint8_t *tab, const uint32_t *frag, int g,
+                                         int cols, int B, int ngs, float n0a, float n1a, float n0b, float n1b, bool two,
+                                         const float *ginv, const uint4 *zero, float (&acc)[4]) {
+    const int lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
+    constexpr int GB = s_gbytes(KIND);
+    WCodes ca, cb;
+    w_load<KIND>(r0, r0 + 8 * rs, t, ca);
+    if (two) {
+        w_load<KIND>(r0 + GB, r0 + GB + 8 * rs, t, cb);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cb.r[i] = cb.s[i] = 0u;
+    }
+    // this lane's fragment column gq; lanes of columns past the batch read
+    // the zero block (one address, no selects on the loaded words)
+    const bool live = HILO ? gq < 2 * B : gq < B;
+    const uint4 *f4 = reinterpret_cast<const uint4 *>(frag);
+    const uint4 *pa = live ? f4 + (((size_t)g * 4) * cols + gq) * 4 + t : zero;
+    const uint4 *pb = live && two ? f4 + (((size_t)(g + 1) * 4) * cols + gq) * 4 + t : zero;
+    const int sa = live ? cols * 4 : 0, sb = live && two ? cols * 4 : 0;
+    uint32_t fa[16], fb[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint4 va = pa[k * sa], vb = pb[k * sb];
+        fa[4 * k] = va.x, fa[4 * k + 1] = va.y, fa[4 * k + 2] = va.z, fa[4 * k + 3] = va.w;
+        fb[4 * k] = vb.x, fb[4 * k + 1] = vb.y, fb[4 * k + 2] = vb.z, fb[4 * k + 3] = vb.w;
+    }
+    float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int nu = 0; nu < 8; ++nu) {
+        uint32_t a[4], b[4];
+        w_decode<KIND>(ca, nu, tab, lane, a);
+        w_decode<KIND>(cb, nu, tab, lane, b);
+        w_mma(da, a, fa[2 * nu], fa[2 * nu + 1]);
+        w_mma(db, b, fb[2 * nu], fb[2 * nu + 1]);
+    }
+    if (HILO) {  // columns 2t, 2t+1: hi and lo terms of batch row t
+        const float ia = t < B ? ginv[t * ngs + g] : 0.0f, ib = t < B && two ? ginv[t * ngs + g + 1] : 0.0f;
+        acc[0] = fmaf(n0b * ib, db[0], fmaf(n0a * ia, da[0], acc[0]));
+        acc[1] = fmaf(n0b * ib, db[1], fmaf(n0a * ia, da[1], acc[1]));
+        acc[2] = fmaf(n1b * ib, db[2], fmaf(n1a * ia, da[2], acc[2]));
+        acc[3] = fmaf(n1b * ib, db[3], fmaf(n1a * ia, da[3], acc[3]));
+    } else {  // columns 2t, 2t+1: batch rows 2t, 2t+1
+        const int b0 = 2 * t;
+        const float i0a = b0 < B ? ginv[b0 * ngs + g] : 0.0f, i1a = b0 + 1 < B ? ginv[(b0 + 1) * ngs + g] : 0.0f;
+        const float i0b = b0 < B && two ? ginv[b0 * ngs + g + 1] : 0.0f;
+        const float i1b = b0 + 1 < B && two ? ginv[(b0 + 1) * ngs + g + 1] : 0.0f;
+        acc[0] = fmaf(n0b * i0b, db[0], fmaf(n0a * i0a, da[0], acc[0]));
+        acc[1] = fmaf(n0b * i1b, db[1], fmaf(n0a * i1a, da[1], acc[1]));
+        acc[2] = fmaf(n1b * i0b, db[2], fmaf(n1a * i0a, da[2], acc[2]));
+        acc[3] = fmaf(n1b * i1b, db[3], fmaf(n1a * i1a, da[3], acc[3]));
+    }
+}
+
+template <int KIND, int NB, bool HILO>
+__global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_constant__ SParams p) {
+    constexpr int GC = s_gc(KIND), GB = s_gbytes(KIND), RS = s_rs(KIND), SB = s_stage_bytes(KIND);
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ __align__(8) uint64_t s_bar[kSWarps * kSStages];
+    __shared__ SPair s_pair[kSMaxPairs + 1];
+    __shared__ SMat s_mat[kSMaxPairs];
+    __shared__ __half s_lv[16];
+    __shared__ int s_npair, s_bad;
+    __shared__ uint4 s_zero;  // what fragment loads of columns past the batch read
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gq = lane >> 2, t = lane & 3;
+    const long long U = p.total_units;
+    const long long cu0 = U * blockIdx.x / gridDim.x, cu1 = U * (blockIdx.x + 1) / gridDim.x;
+    const long long wu0 = cu0 + (cu1 - cu0) * warp / kSWarps, wu1 = cu0 + (cu1 - cu0) * (warp + 1) / kSWarps;
+
+    if (threadIdx.x == 0) {
+        s_zero = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < kSWarps * kSStages; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(s_smem(&s_bar[i])));
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        // the (matrix, k-slice) pairs of the range, and where their fragments go
+        int n = 0, foff = 0, goff = 0;
+        long long u = cu0;
+        int m = 0;
+        while (u < cu1 && n < kSMaxPairs) {
+            while (p.units_before[m + 1] <= u) ++m;
+            const SMat &M = p.m[m];
+            const int s = (int)((u - M.unit0) / M.tiles);
+            const long long end = min(cu1, M.unit0 + (long long)(s + 1) * M.tiles);
+            SPair &P = s_pair[n];
+            P.u_end = end;
+            P.m = m;
+            P.s = s;
+            P.g_lo = s * M.gk;
+            P.g_n = min(M.gk, M.ng - P.g_lo);
+            // a pair that reads the same fragments as the one before shares them
+            const bool same = n > 0 && s_mat[n - 1].frag == M.frag && s_mat[n - 1].cols == M.cols &&
+                              s_pair[n - 1].g_lo == P.g_lo && s_pair[n - 1].g_n == P.g_n && s_mat[n - 1].B == M.B;
+            if (same) {
+                P.frag_off = s_pair[n - 1].frag_off;
+                P.ginv_off = s_pair[n - 1].ginv_off;
+            } else {
+                P.frag_off = foff;
+                P.ginv_off = goff;
+                foff += P.g_n * M.cols * 16;
+                goff += M.B * P.g_n;
+            }
+            s_mat[n] = M;
+            ++n;
+            u = end;
+        }
+        s_pair[n].u_end = 0x7fffffffffffffffLL;  // sentinel
+        s_npair = n;
+        // the host planned every range to fit; a block whose range does not
+        // is reported and does nothing
+        s_bad = u < cu1 || (size_t)foff * 16 + (size_t)goff * 4 > (size_t)p.frag_budget;
+        if (s_bad && p.status) atomicOr(p.status, 0x47570010u);
+    }
+    if (threadIdx.x < 16) s_lv[threadIdx.x] = p.lut[threadIdx.x];
+    __syncthreads();
+    w_build_table(KIND, s_lv, smem);
+    const bool ok_range = !s_bad && s_npair > 0;
+
+    uint8_t *stage0 = smem + p.smem_stage + (size_t)warp * kSStages * SB;
+    const uint32_t bar0 = s_smem(&s_bar[warp * kSStages]);
+    bool abort = !ok_range;
+
+    // ---- the warp's chunk stream: the issue side runs kSStages - 1 chunks
+    // ahead of the products. Each side keeps its unit's numbers in registers
+    // (read from shared memory once per unit). ----
+    long long iu = wu0;                   // issue side: unit, pair, chunk, chunks
+    int ipair = 0, ic = 0, inch = 0, iga0 = 0, igend = 0, ivalid = 0;
+    const uint8_t *irow = nullptr;        // this lane's code row (lanes < 16)
+    const __half *inrow = nullptr;        // and its norms
+    auto iload = [&]() {
+        while (iu >= s_pair[ipair].u_end) ++ipair;
+        const SPair &P = s_pair[ipair];
+        const SMat &M = s_mat[ipair];
+        const int row0 = 16 * (int)(iu - M.unit0 - (long long)P.s * M.tiles);
+        iga0 = P.g_lo;
+        igend = P.g_lo + P.g_n;
+        inch = (P.g_n + GC - 1) / GC;
+        ic = 0;
+        ivalid = min(16, M.out - row0);
+        const int r = row0 + min(lane & 15, ivalid - 1);  // rows past the matrix repeat the last one
+        irow = M.codes + (size_t)r * M.ng * GB;
+        inrow = M.norms + (size_t)r * M.ng;
+    };
+    int iq = 0, copied = 0;  // next stage to fill; chunks with copies so far
+    auto issue = [&]() {
+        if (iu < wu1 && !abort) {
+            uint8_t *st = stage0 + iq * SB;
+            const int ga = iga0 + ic * GC, gcnt = min(GC, igend - ga), bytes = gcnt * GB;
+            const uint32_t bar = bar0 + 8 * iq;
+            // earlier generic reads of the stage come before the copy rewrites it
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            __syncwarp();
+            if (lane == 0)
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(ivalid * bytes)
+                             : "memory");
+            __syncwarp();
+            if (lane < ivalid)
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                        s_smem(st + lane * RS)),
+                    "l"(irow + (size_t)ga * GB), "r"(bytes), "r"(bar)
+                    : "memory");
+            if (lane < 16) {  // this row's norms of the chunk
+                const __half *src = inrow + ga;
+                __half *dst = reinterpret_cast<__half *>(st + 16 * RS + lane * kSNormRow);
+                if (((reinterpret_cast<uintptr_t>(src) & 3) == 0) && (gcnt & 1) == 0) {
+#pragma unroll
+                    for (int i = 0; i < GC; i += 2)
+                        if (i < gcnt)
+                            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s_smem(dst + i)), "l"(src + i)
+                                         : "memory");
+                } else {
+                    for (int i = 0; i < gcnt; ++i) dst[i] = src[i];
+                }
+            }
+            if (++ic == inch && ++iu < wu1) iload();
+            ++copied;
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+        iq = iq + 1 == kSStages ? 0 : iq + 1;
+    };
+    if (wu0 < wu1 && !abort) iload();
+    // the code copies do not depend on the launch before this one
+    for (int i = 0; i + 1 < kSStages; ++i) issue();
+
+    // ---- fragments and 1/sigma of the range's pairs, once the rotation is complete ----
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    uint4 *sfrag = reinterpret_cast<uint4 *>(smem + p.smem_frag);
+    float *sginv = reinterpret_cast<float *>(smem + p.smem_frag);
+    int ginv_base = 0;  // after every pair's fragments
+    for (int i = 0; i < (ok_range ? s_npair : 0); ++i)
+        ginv_base = max(ginv_base, s_pair[i].frag_off + s_pair[i].g_n * s_mat[i].cols * 16);
+    sginv += 4 * ginv_base;
+    for (int i = 0; i < (ok_range ? s_npair : 0); ++i) {
+        if (i > 0 && s_pair[i].frag_off == s_pair[i - 1].frag_off) continue;
+        const SPair &P = s_pair[i];
+        const SMat &M = s_mat[i];
+        const int n16 = P.g_n * M.cols * 16;
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.frag + M.frag) + (size_t)P.g_lo * M.cols * 16;
+        for (int e = threadIdx.x; e < n16; e += kSThreads) sfrag[P.frag_off + e] = src[e];
+        for (int e = threadIdx.x; e < M.B * P.g_n; e += kSThreads) {
+            const int b = e / P.g_n, g = e - b * P.g_n;
+            sginv[P.ginv_off + e] = p.ginv[M.ginv + (size_t)b * M.ng + P.g_lo + g];
+        }
+    }
+    __syncthreads();
+
+    // ---- the products ----
+    long long cu = wu0;  // product side: unit, pair, chunk, chunks
+    int cpair = 0, cc = 0, cnch = 0, cglo = 0, cgend = 0, ccols = 0, cB = 0, cgn = 0, ct = 0;
+    const uint32_t *cfrag = nullptr;
+    const float *cginv = nullptr;
+    auto cload = [&]() {
+        while (cu >= s_pair[cpair].u_end) ++cpair;
+        const SPair &P = s_pair[cpair];
+        const SMat &M = s_mat[cpair];
+        ct = (int)(cu - M.unit0 - (long long)P.s * M.tiles);
+        cglo = P.g_lo;
+        cgn = P.g_n;
+        cgend = P.g_lo + P.g_n;
+        cnch = (P.g_n + GC - 1) / GC;
+        cc = 0;
+        ccols = M.cols;
+        cB = M.B;
+        cfrag = reinterpret_cast<const uint32_t *>(sfrag + P.frag_off);
+        cginv = sginv + P.ginv_off;
+    };
+    if (wu0 < wu1 && !abort) cload();
+    int cq = 0, done = 0;
+    uint32_t phase = 0;  // bit q: parity of stage q's next completion
+    float acc[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
+    const uint8_t *tab = smem;
+    while (cu < wu1 && !abort) {
+        issue();
+        if (!s_wait(bar0 + 8 * cq, (phase >> cq) & 1u)) {
+            if (lane == 0 && p.status) atomicOr(p.status, 0x47570011u);
+            abort = true;
+            break;
+        }
+        phase ^= 1u << cq;
+        asm volatile("cp.async.wait_group %0;\n" ::"n"(kSStages - 1) : "memory");
+        __syncwarp();
+        const uint8_t *st = stage0 + cq * SB;
+        const __half *sn = reinterpret_cast<const __half *>(st + 16 * RS);
+        const int gl0 = cc * GC, gcnt = min(GC, cgn - gl0);  // the chunk's groups, local to the k-slice
+        if (NB == 1) {
+#pragma unroll
+            for (int gl = 0; gl < GC; gl += 2) {
+                if (gl < gcnt) {
+                    const bool two = gl + 1 < gcnt;
+                    const float n0a = __half2float(sn[gq * (kSNormRow / 2) + gl]);
+                    const float n1a = __half2float(sn[(gq + 8) * (kSNormRow / 2) + gl]);
+                    const float n0b = two ? __half2float(sn[gq * (kSNormRow / 2) + gl + 1]) : 0.0f;
+                    const float n1b = two ? __half2float(sn[(gq + 8) * (kSNormRow / 2) + gl + 1]) : 0.0f;
+                    s_group2<KIND, HILO>(st + gq * RS + gl * GB, RS, tab, cfrag, gl0 + gl, ccols, cB, cgn, n0a, n1a,
+                                         n0b, n1b, two, cginv, &s_zero, reinterpret_cast<float(&)[4]>(acc[0]));
+                }
+            }
+        } else {
+            for (int gl = 0; gl < gcnt; ++gl) {
+                const float n0 = __half2float(sn[gq * (kSNormRow / 2) + gl]);
+                const float n1 = __half2float(sn[(gq + 8) * (kSNormRow / 2) + gl]);
+                w_group<KIND, NB, HILO>(st + gq * RS + gl * GB, RS, tab, cfrag, gl0 + gl, ccols, cB, cgn, n0, n1,
+                                        cginv, acc);
+            }
+        }
+        cq = cq + 1 == kSStages ? 0 : cq + 1;
+        ++done;
+        if (++cc == cnch) {  // the unit is complete
+            const SMat &M = s_mat[cpair];
+            const int B = cB;
+            const int row_r = 16 * ct + gq, row_s = row_r + 8;
+            // this lane's values: (batch row, row) pairs
+            float v[NB][4];
+            int bb[NB][4];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                if (HILO) {
+                    v[nb][0] = acc[nb][0] + acc[nb][1];
+                    v[nb][1] = acc[nb][2] + acc[nb][3];
+                    bb[nb][0] = bb[nb][1] = t;
+                    bb[nb][2] = bb[nb][3] = kWMaxB;  // unused
+                    v[nb][2] = v[nb][3] = 0.0f;
+                } else {
+                    v[nb][0] = acc[nb][0];
+                    v[nb][1] = acc[nb][2];
+                    v[nb][2] = acc[nb][1];
+                    v[nb][3] = acc[nb][3];
+                    bb[nb][0] = bb[nb][1] = 8 * nb + 2 * t;
+                    bb[nb][2] = bb[nb][3] = 8 * nb + 2 * t + 1;
+                }
+                acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
+            }
+            if (M.nks == 1) {
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int b = bb[nb][j], row = (j & 1) ? row_s : row_r;
+                        if (b < B && row < M.out) {
+                            const float a = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[b], kWInvSqrt128) : kWInvSqrt128;
+                            M.y[(size_t)b * M.out + row] = v[nb][j] * a;
+                        }
+                    }
+            } else {
+                // partial sums of this k-slice, then the tile's counter
+                const int s = cglo / M.gk;
+                float *part = p.part + (M.part0 + (long long)s * M.tiles + ct) * 16 * B;
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int b = bb[nb][j];
+                        if (b < B) part[((j & 1) ? gq + 8 : gq) * B + b] = v[nb][j];
+                    }
+                __threadfence();
+                __syncwarp();
+                unsigned old = 0;
+                if (lane == 0) old = atomicAdd(p.cnt + M.cnt0 + ct, 1u);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old == (unsigned)M.nks - 1) {  // the last k-slice of the tile: add them in order
+                    __threadfence();
+                    const float *base = p.part + (M.part0 + ct) * 16 * B;
+                    // lane l adds elements l, l + 32, ...; its loads (element i,
+                    // k-slice s2 in the order q = i * nks + s2) go out 16 at a
+                    // time (the host keeps them to one batch), then the sums run
+                    // in k-slice order
+                    const int E = 16 * B, ne = (E + 31) / 32, tot = ne * M.nks;
+                    const size_t sstride = (size_t)M.tiles * 16 * B;
+                    float sum = 0.0f;
+                    int cur = -1;
+                    auto put = [&](int i, float v2) {
+                        const int e2 = lane + 32 * i;
+                        if (e2 >= E) return;
+                        const int r = e2 / B, b = e2 - r * B, row = 16 * ct + r;
+                        if (row < M.out) {
+                            const float a = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[b], kWInvSqrt128) : kWInvSqrt128;
+                            M.y[(size_t)b * M.out + row] = v2 * a;
+                        }
+                    };
+                    for (int q0 = 0; q0 < tot; q0 += 16) {
+                        float vv[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int q = q0 + j, i = q / M.nks, s2 = q - i * M.nks, e2 = lane + 32 * i;
+                            vv[j] = (q < tot && e2 < E) ? __ldcg(base + (size_t)s2 * sstride + e2) : 0.0f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int q = q0 + j;
+                            if (q >= tot) break;
+                            const int i = q / M.nks;
+                            if (i != cur) {
+                                if (cur >= 0) put(cur, sum);
+                                sum = 0.0f;
+                                cur = i;
+                            }
+                            sum += vv[j];
+                        }
+                    }
+                    if (cur >= 0) put(cur, sum);
+                    if (lane == 0) p.cnt[M.cnt0 + ct] = 0u;  // ready for the next launch
+                }
+            }
+            if (++cu < wu1) cload();
+        }
+    }
+    // copies still in flight land before the block exits (bounded)
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    for (int i = done; i < copied; ++i) {
+        s_wait(bar0 + 8 * cq, (phase >> cq) & 1u);
+        phase ^= 1u << cq;
+        cq = cq + 1 == kSStages ? 0 : cq + 1;
+    }
+}
+
 }  // namespace
 
 namespace {
@@ -530,6 +1019,160 @@ int w_row_stride(int kind, int ng) {
 }
 
 size_t w_frag_bytes(int ng, int B) { return (size_t)ng * w_cols(B) * 256 + (size_t)B * ng * 4; }
+
+// ---- split products: host planning ----
+// Groups per k-slice and k-slice count of a matrix of ng groups for split
+// factor S (k-slices of whole chunks, except a matrix narrower than one).
+void s_slices(int ng, int S, int kind, int &gk, int &nks) {
+    const int gc = s_gc(kind);
+    gk = (ng + S - 1) / S;
+    gk = (gk + gc - 1) / gc * gc;
+    if (gk > ng) gk = ng;
+    nks = (ng + gk - 1) / gk;
+}
+
+size_t s_table_bytes(int kind) { return kind == 0 || kind == 1 ? 32768 : kind == 2 ? 2048 : 8192; }
+
+// Fills p for the matrices sel[0..cnt) (one code width, one codebook, one
+// batch class): picks the smallest split factor that gives a quarter of the
+// grid's warps a unit (or splits as far as chunks allow) and whose every
+// block range fits its fragments in shared memory. Returns the dynamic
+// shared memory, or 0 if no split fits (the caller uses the sliced kernel).
+size_t plan_split(SParams &p, const cq_gemv_desc *d, const int *idx, const int *sel, int cnt, const int *act_of,
+                  const WAct *acts, int kind, int grid, long long &part_floats, int &counters) {
+    if (cnt > kSMaxMats) return 0;
+    const size_t stages = (size_t)kSWarps * kSStages * s_stage_bytes(kind);
+    const size_t limit = 227 * 1024 - 6 * 1024;  // dynamic shared memory next to the static arrays
+    if (s_table_bytes(kind) + stages >= limit) return 0;
+    const size_t budget = limit - s_table_bytes(kind) - stages;
+    const long long W = (long long)grid * kSWarps;
+    static thread_local std::vector<int> gk, nks, tiles;
+    static thread_local std::vector<long long> unit0;
+    gk.resize(cnt);
+    nks.resize(cnt);
+    tiles.resize(cnt);
+    unit0.resize(cnt + 1);
+    for (int S = 1; S <= 1024; S *= 2) {
+        long long U = 0;
+        bool more = false;  // a larger S would split some matrix further
+        for (int j = 0; j < cnt; ++j) {
+            const cq_gemv_desc &D = d[idx[sel[j]]];
+            const int ng = in_padded(D.in) / kGroup;
+            // at most 16 partial sums per lane for the tile's last k-slice to add
+            const int cap = std::max(1, 16 / ((16 * D.B + 31) / 32));
+            const int Sj = std::min(S, cap);
+            s_slices(ng, Sj, kind, gk[j], nks[j]);
+            int g2, n2;
+            s_slices(ng, std::min(2 * S, cap), kind, g2, n2);
+            more |= n2 > nks[j];
+            tiles[j] = (D.out + 15) / 16;
+            unit0[j] = U;
+            U += (long long)tiles[j] * nks[j];
+        }
+        unit0[cnt] = U;
+        // a unit ends in a fence and an atomic when its matrix is k-sliced,
+        // so slices stop once a quarter of the warps have a unit
+        if (4 * U < W && more) continue;
+        // every block's range: its (matrix, k-slice) pairs and their fragments
+        bool fits = true;
+        for (int b = 0; b < grid && fits; ++b) {
+            const long long c0 = U * b / grid, c1 = U * (b + 1) / grid;
+            long long u = c0;
+            int m = 0, pairs = 0, pm = -1, ps = -1;
+            size_t bytes = 0;
+            while (u < c1) {
+                while (unit0[m + 1] <= u) ++m;
+                const int s = (int)((u - unit0[m]) / tiles[m]);
+                const cq_gemv_desc &D = d[idx[sel[m]]];
+                const int ng = in_padded(D.in) / kGroup, gn = std::min(gk[m], ng - s * gk[m]);
+                const WAct &A = acts[act_of[sel[m]]];
+                const bool same = pm >= 0 && act_of[sel[pm]] == act_of[sel[m]] && ps == s && gk[pm] == gk[m];
+                if (!same) bytes += (size_t)gn * A.cols * 256 + (size_t)A.B * gn * 4;
+                pm = m;
+                ps = s;
+                ++pairs;
+                u = std::min(c1, unit0[m] + (long long)(s + 1) * tiles[m]);
+            }
+            fits = pairs <= kSMaxPairs && bytes <= budget;
+        }
+        if (!fits) {
+            if (!more) return 0;
+            continue;
+        }
+        // accepted: the parameter block
+        p.n_mats = cnt;
+        p.total_units = U;
+        for (int j = 0; j < cnt; ++j) {
+            const int ii = sel[j];
+            const cq_gemv_desc &D = d[idx[ii]];
+            const WAct &A = acts[act_of[ii]];
+            const int W_ = width_of(D.bits), ng = in_padded(D.in) / kGroup;
+            SMat &M = p.m[j];
+            M.codes = D.blob;
+            M.norms = reinterpret_cast<const __half *>(D.blob + (size_t)D.out * in_padded(D.in) * W_ / 8);
+            M.y = D.y;
+            M.xs = D.x_scale;
+            M.unit0 = unit0[j];
+            M.frag = A.frag;
+            M.ginv = A.ginv;
+            M.out = D.out;
+            M.ng = ng;
+            M.B = D.B;
+            M.xdt = D.x_dtype;
+            M.cols = A.cols;
+            M.tiles = tiles[j];
+            M.nks = nks[j];
+            M.gk = gk[j];
+            M.cnt0 = 0;
+            M.part0 = 0;
+            if (nks[j] > 1) {
+                M.cnt0 = counters;
+                counters += tiles[j];
+                M.part0 = part_floats / (16 * D.B);  // slots of 16 * B floats
+                if (part_floats % (16 * D.B)) {      // align the matrix's first slot
+                    M.part0 += 1;
+                    part_floats = M.part0 * 16 * D.B;
+                }
+                part_floats += (long long)tiles[j] * nks[j] * 16 * D.B;
+            }
+            p.units_before[j] = unit0[j];
+        }
+        p.units_before[cnt] = U;
+        p.smem_frag = (int)s_table_bytes(kind);
+        p.frag_budget = (int)budget;
+        p.smem_stage = (int)(s_table_bytes(kind) + budget);
+        return (size_t)p.smem_stage + stages;
+    }
+    return 0;
+}
+
+template <int KIND, int NB, bool HILO>
+int s_launch(const SParams &p, int grid, size_t smem, cudaStream_t st) {
+    auto k = gemv_split_kernel<KIND, NB, HILO>;
+    const int rc = ensure_smem(reinterpret_cast<const void *>(k), smem);
+    if (rc) return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kSThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, k, p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "split gemv launch: %s", cudaGetErrorString(e));
+    return CQ_OK;
+}
+
+template <int KIND>
+int s_launch_cls(int cls, const SParams &p, int grid, size_t smem, cudaStream_t st) {
+    if (cls == 0) return s_launch<KIND, 1, true>(p, grid, smem, st);
+    if (cls == 1) return s_launch<KIND, 1, false>(p, grid, smem, st);
+    return s_launch<KIND, 2, false>(p, grid, smem, st);
+}
 
 template <int NB, bool HILO>
 int w_launch(WParams &p, int grid, size_t smem, cudaStream_t st) {
@@ -566,8 +1209,8 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream)
     static thread_local WActParams ap;  // large: off the stack, one per host thread
     static thread_local WParams wp;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // ---- the distinct activations of the call (consecutive descriptors
-    // reading the same activation share one rotation) ----
+    // ---- the distinct activations of the call (descriptors reading the
+    // same activation share one rotation) ----
     int act_of[CQ_MAX_GROUPED];
     int n_act = 0;
     long long words = 0, floats = 0;
@@ -596,35 +1239,113 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream)
         }
         act_of[ii] = a;
     }
+    // ---- the split launches: one per (batch class, code width, codebook);
+    // what does not fit them goes to the sliced kernel ----
+    struct Plan {
+        int kind, cls;
+        size_t smem;
+    };
+    static thread_local std::vector<SParams> plans;
+    std::vector<Plan> meta;
+    bool sliced[CQ_MAX_GROUPED] = {};
+    const int grid = sm_count();
+    long long part_floats = 0;
+    int counters = 0;
+    {
+        bool taken[CQ_MAX_GROUPED] = {};
+        for (int ii = 0; ii < n; ++ii) {
+            if (taken[ii]) continue;
+            const cq_gemv_desc &D0 = d[idx[ii]];
+            const int cls = D0.B <= 4 ? 0 : D0.B <= 8 ? 1 : 2, kind = w_kind(D0.bits);
+            float lv0[16];
+            level_table(D0.bits, D0.codebook, lv0);
+            int sel[CQ_MAX_GROUPED], cnt = 0;
+            for (int jj = ii; jj < n; ++jj) {
+                if (taken[jj]) continue;
+                const cq_gemv_desc &D = d[idx[jj]];
+                const int c2 = D.B <= 4 ? 0 : D.B <= 8 ? 1 : 2;
+                if (c2 != cls || w_kind(D.bits) != kind) continue;
+                float lv[16];
+                level_table(D.bits, D.codebook, lv);
+                bool same = true;
+                for (int k = 0; k < 16; ++k)
+                    same &= __half_as_ushort(__float2half_rn(lv[k])) == __half_as_ushort(__float2half_rn(lv0[k]));
+                if (!same) continue;
+                taken[jj] = true;
+                sel[cnt++] = jj;
+            }
+            // the split products serve batches of up to 4 with 2-bit and 1-bit
+            // codes; wider codes (fewer groups per chunk) and larger batches
+            // run faster on the sliced kernel
+            if (cls != 0 || (kind != 0 && kind != 2)) {
+                for (int j = 0; j < cnt; ++j) sliced[sel[j]] = true;
+                continue;
+            }
+            for (int b0 = 0; b0 < cnt; b0 += kSMaxMats) {
+                const int c = std::min(kSMaxMats, cnt - b0);
+                if (plans.size() <= meta.size()) plans.resize(meta.size() + 1);
+                SParams &P = plans[meta.size()];
+                const size_t smem = plan_split(P, d, idx, sel + b0, c, act_of, acts, kind, grid, part_floats, counters);
+                if (!smem) {
+                    for (int j = 0; j < c; ++j) sliced[sel[b0 + j]] = true;
+                    continue;
+                }
+                for (int k = 0; k < 16; ++k) P.lut[k] = __float2half_rn(lv0[k]);
+                meta.push_back({kind, cls, smem});
+            }
+        }
+    }
     int err = 0;
-    const size_t ws_bytes = (size_t)words * 4 + (size_t)floats * 4 + 16;
+    const size_t ws_bytes = (size_t)words * 4 + (size_t)floats * 4 + (size_t)part_floats * 4 + (size_t)counters * 4 + 64;
     uint8_t *ws = static_cast<uint8_t *>(stream_workspace(stream, 2, ws_bytes, &err));
     if (!ws) return err;
     uint32_t *frag = reinterpret_cast<uint32_t *>(ws);
     float *ginv = reinterpret_cast<float *>(ws + (size_t)words * 4);
-    // ---- 1. one rotation launch per kWMaxActs activations ----
+    float *part = ginv + floats;
+    unsigned int *cnt = reinterpret_cast<unsigned int *>(part + part_floats);
+    // ---- 1. one rotation launch per kWMaxActs activations (the first also
+    // clears the split launches' tile counters) ----
     for (int a0 = 0; a0 < n_act; a0 += kWMaxActs) {
-        const int cnt = std::min(kWMaxActs, n_act - a0);
-        ap.n = cnt;
+        const int c = std::min(kWMaxActs, n_act - a0);
+        ap.n = c;
         ap.frag = frag;
         ap.ginv = ginv;
+        ap.zero = cnt;
+        ap.n_zero = a0 == 0 ? counters : 0;
         int tasks = 0;
-        for (int j = 0; j < cnt; ++j) {
+        for (int j = 0; j < c; ++j) {
             ap.a[j] = acts[a0 + j];
             ap.task0[j] = tasks;
             tasks += acts[a0 + j].ng * acts[a0 + j].B;
         }
-        ap.task0[cnt] = tasks;
+        ap.task0[c] = tasks;
         act_frag_kernel<<<(tasks + kWWarps - 1) / kWWarps, kWThreads, 0, st>>>(ap);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "activation rotation launch: %s", cudaGetErrorString(e));
     }
-    // ---- 2. the products: one launch per batch class, kWMaxMats matrices each ----
+    // ---- 2. the split products ----
+    for (size_t k = 0; k < meta.size(); ++k) {
+        SParams &P = plans[k];
+        P.frag = frag;
+        P.ginv = ginv;
+        P.part = part;
+        P.cnt = cnt;
+        P.status = device_status_ptr();
+        int rc = CQ_OK;
+        switch (meta[k].kind) {
+        case 0: rc = s_launch_cls<0>(meta[k].cls, P, grid, meta[k].smem, st); break;
+        case 1: rc = s_launch_cls<1>(meta[k].cls, P, grid, meta[k].smem, st); break;
+        case 2: rc = s_launch_cls<2>(meta[k].cls, P, grid, meta[k].smem, st); break;
+        default: rc = s_launch_cls<3>(meta[k].cls, P, grid, meta[k].smem, st); break;
+        }
+        if (rc) return rc;
+    }
+    // ---- 3. the rest: the sliced products, one launch per batch class ----
     for (int cls = 0; cls < 3; ++cls) {
         int sel[CQ_MAX_GROUPED], ns = 0;
         for (int ii = 0; ii < n; ++ii) {
             const int B = d[idx[ii]].B, c = B <= 4 ? 0 : B <= 8 ? 1 : 2;
-            if (c == cls) sel[ns++] = ii;
+            if (c == cls && sliced[ii]) sel[ns++] = ii;
         }
         for (int base = 0; base < ns; base += kWMaxMats) {
             const int cnt = std::min(kWMaxMats, ns - base);
