@@ -14,8 +14,8 @@
 //     two fragment words, so no shuffles are needed), with 1/sigma per
 //     (batch row, group).
 //  2. the products, launched as programmatic dependents of the first:
-//     gemv_split_kernel (further below) for batches of 1 to 4 with 2-bit and
-//     1-bit codes, gemv_wide_kernel for the rest. In gemv_wide_kernel one
+//     gemv_split_kernel (further below) for batches of 1 to 4 with 1-, 2-
+//     and 4-bit codes, gemv_wide_kernel for the rest. In gemv_wide_kernel one
 //     block per SM walks an equal run of the call's 16-row tiles.
 //     Before it waits for the rotation it builds its level table and starts
 //     its code copies; then it copies the fragments of its matrix's
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kWGThreads, 1) gemv_wide_kernel(const __grid_c
 // ----------------------------------------------------- split products --
 // gemv_split_kernel: the product step behind the same rotation launch, with
 // the work cut finer than a block's run of tiles and every warp on its own
-// pipeline. The host sends it batches of 1 to 4 with 2-bit and 1-bit codes
+// pipeline. The host sends it batches of 1 to 4 with 1-, 2- and 4-bit codes
 // (the kernel itself takes every width and batches up to 16). A
 // unit is (matrix, k-slice of its groups, 16-row tile); units are numbered
 // matrix by matrix, k-slice by k-slice, tile fastest, and each block takes an
@@ -536,11 +536,11 @@ __global__ void __launch_bounds__(kWGThreads, 1) gemv_wide_kernel(const __grid_c
 // counter per tile) adds them in k-slice order, so the result does not
 // depend on the order in which they finish.
 //
-// Every warp streams its own units through three shared-memory stages of
-// one chunk each (16 rows x 128 code bytes: four CQ2 groups, two CQ4 or CQ3
-// groups, eight binary groups): one lane per row issues a 1-D TMA bulk copy
-// of the row's chunk (completion on the stage's mbarrier) and a 4-byte
-// cp.async of its norms. No block barrier runs inside the loop. A block
+// Every warp streams its own units through shared-memory stages of one
+// chunk each: two stages of 16 rows x 256 code bytes (eight CQ2 groups, four
+// CQ4 groups, sixteen binary groups), or three of 16 x 96 (two CQ3 groups).
+// One lane per row issues a 1-D TMA bulk copy of the row's chunk (completion
+// on the stage's mbarrier) and a cp.async of its norms. No block barrier runs inside the loop. A block
 // copies the fragments of the (matrix, k-slice) pairs of its range into
 // shared memory once, after the rotation launch is complete.
 constexpr int kSWarps = 16;
@@ -548,7 +548,6 @@ constexpr int kSThreads = 32 * kSWarps;
 constexpr int kSStages = 3;
 constexpr int kSMaxMats = 128;
 constexpr int kSMaxPairs = 24;  // (matrix, k-slice) pairs of one block's range
-constexpr int kSNormRow = 16;   // bytes of norms per row and stage (up to eight groups)
 
 struct SMat {
     const uint8_t *codes;
@@ -582,13 +581,18 @@ static_assert(sizeof(SParams) <= 32000, "kernel parameter block");
 
 // Code bytes per group and groups per chunk of each kind.
 __host__ __device__ constexpr int s_gbytes(int kind) { return kind == 0 ? 32 : kind == 1 ? 64 : kind == 2 ? 16 : 48; }
-__host__ __device__ constexpr int s_gc(int kind) { return kind == 0 ? 4 : kind == 1 ? 2 : kind == 2 ? 8 : 2; }
+__host__ __device__ constexpr int s_gc(int kind) { return kind == 0 ? 8 : kind == 1 ? 4 : kind == 2 ? 16 : 2; }
+// Stages per warp: two of 256 code bytes per row for 1-, 2- and 4-bit codes,
+// three of 96 for 3-bit codes.
+__host__ __device__ constexpr int s_ns(int kind) { return kind == 3 ? 3 : 2; }
 // Row stride of a stage: the chunk plus padding that spreads a warp's reads
 // of its rows over the banks (as for the sliced kernel's stages).
 __host__ __device__ constexpr int s_rs(int kind) {
-    return kind == 0 ? 160 : kind == 1 ? 192 : kind == 2 ? 144 : 176;
+    return kind == 0 ? 288 : kind == 1 ? 320 : kind == 2 ? 272 : 176;
 }
-__host__ __device__ constexpr int s_stage_bytes(int kind) { return 16 * s_rs(kind) + 16 * kSNormRow; }
+// Bytes of norms per row of a stage (a multiple of 16).
+__host__ __device__ constexpr int s_nr(int kind) { return (2 * s_gc(kind) + 15) / 16 * 16; }
+__host__ __device__ constexpr int s_stage_bytes(int kind) { return 16 * s_rs(kind) + 16 * s_nr(kind); }
 
 // One (matrix, k-slice) pair of a block's range and where its fragments and
 // 1/sigma sit in shared memory.
@@ -673,7 +677,8 @@ __device__ __forceinline__ void s_group2(const uint8_t *r0, int rs, const uint8_
 
 template <int KIND, int NB, bool HILO>
 __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_constant__ SParams p) {
-    constexpr int GC = s_gc(KIND), GB = s_gbytes(KIND), RS = s_rs(KIND), SB = s_stage_bytes(KIND);
+    constexpr int GC = s_gc(KIND), GB = s_gbytes(KIND), RS = s_rs(KIND), SB = s_stage_bytes(KIND), NS = s_ns(KIND);
+    constexpr int NR = s_nr(KIND) / 2;  // norms per row of a stage
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[kSWarps * kSStages];
     __shared__ SPair s_pair[kSMaxPairs + 1];
@@ -689,7 +694,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
 
     if (threadIdx.x == 0) {
         s_zero = make_uint4(0, 0, 0, 0);
-        for (int i = 0; i < kSWarps * kSStages; ++i)
+        for (int i = 0; i < kSWarps * NS; ++i)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(s_smem(&s_bar[i])));
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         // the (matrix, k-slice) pairs of the range, and where their fragments go
@@ -735,12 +740,12 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
     w_build_table(KIND, s_lv, smem);
     const bool ok_range = !s_bad && s_npair > 0;
 
-    uint8_t *stage0 = smem + p.smem_stage + (size_t)warp * kSStages * SB;
-    const uint32_t bar0 = s_smem(&s_bar[warp * kSStages]);
+    uint8_t *stage0 = smem + p.smem_stage + (size_t)warp * NS * SB;
+    const uint32_t bar0 = s_smem(&s_bar[warp * NS]);
     bool abort = !ok_range;
 
-    // ---- the warp's chunk stream: the issue side runs kSStages - 1 chunks
-    // ahead of the products. Each side keeps its unit's numbers in registers
+    // ---- the warp's chunk stream: the issue side runs NS - 1 chunks ahead
+    // of the products. Each side keeps its unit's numbers in registers
     // (read from shared memory once per unit). ----
     long long iu = wu0;                   // issue side: unit, pair, chunk, chunks
     int ipair = 0, ic = 0, inch = 0, iga0 = 0, igend = 0, ivalid = 0;
@@ -781,8 +786,15 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
                     : "memory");
             if (lane < 16) {  // this row's norms of the chunk
                 const __half *src = inrow + ga;
-                __half *dst = reinterpret_cast<__half *>(st + 16 * RS + lane * kSNormRow);
-                if (((reinterpret_cast<uintptr_t>(src) & 3) == 0) && (gcnt & 1) == 0) {
+                __half *dst = reinterpret_cast<__half *>(st + 16 * RS + lane * 2 * NR);
+                if ((gcnt & 7) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+#pragma unroll
+                    for (int i = 0; i < GC; i += 8)
+                        if (i < gcnt)
+                            asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(s_smem(dst + i)),
+                                         "l"(src + i)
+                                         : "memory");
+                } else if (((reinterpret_cast<uintptr_t>(src) & 3) == 0) && (gcnt & 1) == 0) {
 #pragma unroll
                     for (int i = 0; i < GC; i += 2)
                         if (i < gcnt)
@@ -796,11 +808,11 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
             ++copied;
         }
         asm volatile("cp.async.commit_group;\n" ::: "memory");
-        iq = iq + 1 == kSStages ? 0 : iq + 1;
+        iq = iq + 1 == NS ? 0 : iq + 1;
     };
     if (wu0 < wu1 && !abort) iload();
     // the code copies do not depend on the launch before this one
-    for (int i = 0; i + 1 < kSStages; ++i) issue();
+    for (int i = 0; i + 1 < NS; ++i) issue();
 
     // ---- fragments and 1/sigma of the range's pairs, once the rotation is complete ----
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -859,7 +871,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
             break;
         }
         phase ^= 1u << cq;
-        asm volatile("cp.async.wait_group %0;\n" ::"n"(kSStages - 1) : "memory");
+        asm volatile("cp.async.wait_group %0;\n" ::"n"(NS - 1) : "memory");
         __syncwarp();
         const uint8_t *st = stage0 + cq * SB;
         const __half *sn = reinterpret_cast<const __half *>(st + 16 * RS);
@@ -869,23 +881,23 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
             for (int gl = 0; gl < GC; gl += 2) {
                 if (gl < gcnt) {
                     const bool two = gl + 1 < gcnt;
-                    const float n0a = __half2float(sn[gq * (kSNormRow / 2) + gl]);
-                    const float n1a = __half2float(sn[(gq + 8) * (kSNormRow / 2) + gl]);
-                    const float n0b = two ? __half2float(sn[gq * (kSNormRow / 2) + gl + 1]) : 0.0f;
-                    const float n1b = two ? __half2float(sn[(gq + 8) * (kSNormRow / 2) + gl + 1]) : 0.0f;
+                    const float n0a = __half2float(sn[gq * NR + gl]);
+                    const float n1a = __half2float(sn[(gq + 8) * NR + gl]);
+                    const float n0b = two ? __half2float(sn[gq * NR + gl + 1]) : 0.0f;
+                    const float n1b = two ? __half2float(sn[(gq + 8) * NR + gl + 1]) : 0.0f;
                     s_group2<KIND, HILO>(st + gq * RS + gl * GB, RS, tab, cfrag, gl0 + gl, ccols, cB, cgn, n0a, n1a,
                                          n0b, n1b, two, cginv, &s_zero, reinterpret_cast<float(&)[4]>(acc[0]));
                 }
             }
         } else {
             for (int gl = 0; gl < gcnt; ++gl) {
-                const float n0 = __half2float(sn[gq * (kSNormRow / 2) + gl]);
-                const float n1 = __half2float(sn[(gq + 8) * (kSNormRow / 2) + gl]);
+                const float n0 = __half2float(sn[gq * NR + gl]);
+                const float n1 = __half2float(sn[(gq + 8) * NR + gl]);
                 w_group<KIND, NB, HILO>(st + gq * RS + gl * GB, RS, tab, cfrag, gl0 + gl, ccols, cB, cgn, n0, n1,
                                         cginv, acc);
             }
         }
-        cq = cq + 1 == kSStages ? 0 : cq + 1;
+        cq = cq + 1 == NS ? 0 : cq + 1;
         ++done;
         if (++cc == cnch) {  // the unit is complete
             const SMat &M = s_mat[cpair];
@@ -991,7 +1003,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
     for (int i = done; i < copied; ++i) {
         s_wait(bar0 + 8 * cq, (phase >> cq) & 1u);
         phase ^= 1u << cq;
-        cq = cq + 1 == kSStages ? 0 : cq + 1;
+        cq = cq + 1 == NS ? 0 : cq + 1;
     }
 }
 
@@ -1041,7 +1053,7 @@ size_t s_table_bytes(int kind) { return kind == 0 || kind == 1 ? 32768 : kind ==
 size_t plan_split(SParams &p, const cq_gemv_desc *d, const int *idx, const int *sel, int cnt, const int *act_of,
                   const WAct *acts, int kind, int grid, long long &part_floats, int &counters) {
     if (cnt > kSMaxMats) return 0;
-    const size_t stages = (size_t)kSWarps * kSStages * s_stage_bytes(kind);
+    const size_t stages = (size_t)kSWarps * s_ns(kind) * s_stage_bytes(kind);
     const size_t limit = 227 * 1024 - 6 * 1024;  // dynamic shared memory next to the static arrays
     if (s_table_bytes(kind) + stages >= limit) return 0;
     const size_t budget = limit - s_table_bytes(kind) - stages;
@@ -1274,10 +1286,10 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream)
                 taken[jj] = true;
                 sel[cnt++] = jj;
             }
-            // the split products serve batches of up to 4 with 2-bit and 1-bit
-            // codes; wider codes (fewer groups per chunk) and larger batches
-            // run faster on the sliced kernel
-            if (cls != 0 || (kind != 0 && kind != 2)) {
+            // the split products serve batches of up to 4 with 1-, 2- and 4-bit
+            // codes; 3-bit codes (two groups per chunk) and larger batches run
+            // faster on the sliced kernel
+            if (cls != 0 || kind == 3) {
                 for (int j = 0; j < cnt; ++j) sliced[sel[j]] = true;
                 continue;
             }
