@@ -57,11 +57,12 @@ WORKLOAD = ("Needle-shaped decode step, batch 1: 27 x {Q 512x512, K 256x512, V 2
 # hash of the sources it was built from: once a source changes the entry no
 # longer matches and traffic reads null.
 NCU_TRAFFIC = {
-    "gemv_fast": ("75d08df624551252", 9777664),
-    "gemm_x8": ("dd123d837be7b655", 527848448),
-    "encode_cq2": ("d6aa9d34094c044f", 282315008),
-    "gather_cq4": ("5fb8fc86d8fb3ba1", 75002880),
-    "kv_attend": ("b470d32ba9762b74", 148856064),
+    "gemv_fast": ("066ddb5104d761ba", 9777920),
+    "gemm_x8": ("eafec9c3c7051437", 527629824),
+    "encode_cq2": ("9b9931b39a97b3a4", 282200320),
+    "gather_cq4": ("418b3cc16e02bd42", 74119680),
+    "kv_attend": ("fcabe59d60877ca7", 148691456),
+    "gemv_split": ("c4de1e7786b5230c", 289867264),
 }
 KERNEL_SOURCES = {
     "gemv_fast": ("cq_gemv_fast.cu", "cq_internal.h"),
@@ -69,6 +70,7 @@ KERNEL_SOURCES = {
     "encode_cq2": ("cq_encode.cu", "cq_internal.h"),
     "gather_cq4": ("cq_gather.cu", "cq_internal.h"),
     "kv_attend": ("cq_kv.cu", "cq_internal.h"),
+    "gemv_split": ("cq_gemv_wide.cu", "cq_internal.h"),
 }
 
 
@@ -998,7 +1000,8 @@ def bench_g64(cx):
                      "value": round(cx.world * gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
                      "steps": 10 * reps, "packed_bytes_per_step": 64 * nb,
                      "l2": f"one set of 64 matrices ({64 * nb / 1e6:.0f} MB > L2)",
-                     "roofline": hbm_roofline(gbs, cx.peaks, cx.peak_kind, None,
+                     "roofline": hbm_roofline(gbs, cx.peaks, cx.peak_kind,
+                                              ncu_traffic("gemv_split") if name == "cq2_group128" else None,
                                               kernel=gemv_kernel_name(out, n_in, bits, 1, group),
                                               algorithmic_bytes_per_launch=algo)}
         del items, plan, g
