@@ -692,48 +692,70 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
     const long long cu0 = U * blockIdx.x / gridDim.x, cu1 = U * (blockIdx.x + 1) / gridDim.x;
     const long long wu0 = cu0 + (cu1 - cu0) * warp / kSWarps, wu1 = cu0 + (cu1 - cu0) * (warp + 1) / kSWarps;
 
-    if (threadIdx.x == 0) {
-        s_zero = make_uint4(0, 0, 0, 0);
-        for (int i = 0; i < kSWarps * NS; ++i)
+    if (warp == 1) {  // the stage barriers
+        for (int i = lane; i < kSWarps * NS; i += 32)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(s_smem(&s_bar[i])));
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-        // the (matrix, k-slice) pairs of the range, and where their fragments go
-        int n = 0, foff = 0, goff = 0;
-        long long u = cu0;
-        int m = 0;
-        while (u < cu1 && n < kSMaxPairs) {
-            while (p.units_before[m + 1] <= u) ++m;
-            const SMat &M = p.m[m];
-            const int s = (int)((u - M.unit0) / M.tiles);
-            const long long end = min(cu1, M.unit0 + (long long)(s + 1) * M.tiles);
-            SPair &P = s_pair[n];
-            P.u_end = end;
-            P.m = m;
-            P.s = s;
-            P.g_lo = s * M.gk;
-            P.g_n = min(M.gk, M.ng - P.g_lo);
-            // a pair that reads the same fragments as the one before shares them
-            const bool same = n > 0 && s_mat[n - 1].frag == M.frag && s_mat[n - 1].cols == M.cols &&
-                              s_pair[n - 1].g_lo == P.g_lo && s_pair[n - 1].g_n == P.g_n && s_mat[n - 1].B == M.B;
-            if (same) {
-                P.frag_off = s_pair[n - 1].frag_off;
-                P.ginv_off = s_pair[n - 1].ginv_off;
-            } else {
-                P.frag_off = foff;
-                P.ginv_off = goff;
-                foff += P.g_n * M.cols * 16;
-                goff += M.B * P.g_n;
-            }
-            s_mat[n] = M;
-            ++n;
-            u = end;
+        __syncwarp();
+        if (lane == 0) {
+            asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+            s_zero = make_uint4(0, 0, 0, 0);
         }
-        s_pair[n].u_end = 0x7fffffffffffffffLL;  // sentinel
-        s_npair = n;
-        // the host planned every range to fit; a block whose range does not
-        // is reported and does nothing
-        s_bad = u < cu1 || (size_t)foff * 16 + (size_t)goff * 4 > (size_t)p.frag_budget;
-        if (s_bad && p.status) atomicOr(p.status, 0x47570010u);
+    } else if (warp == 0) {
+        // the matrix of the range's first unit: the last m with units_before[m] <= cu0
+        // (the lanes compare 32 entries at a time; the table is ascending)
+        int m0 = -1;
+        for (int base = 0; base <= p.n_mats; base += 32) {
+            const int i = base + lane;
+            m0 += __popc(__ballot_sync(0xffffffffu, i <= p.n_mats && p.units_before[i] <= cu0));
+        }
+        if (lane == 0) {
+            // the (matrix, k-slice) pairs of the range, and where their fragments go
+            int n = 0, foff = 0, goff = 0, pm = -1;
+            long long u = cu0;
+            int m = max(m0, 0);
+            while (u < cu1 && n < kSMaxPairs) {
+                while (p.units_before[m + 1] <= u) ++m;
+                const SMat &M = p.m[m];
+                const long long unit0 = M.unit0;
+                const int tiles = M.tiles, gk = M.gk, ng = M.ng, cols = M.cols, B = M.B;
+                const long long frag = M.frag;
+                const int s = (int)((u - unit0) / tiles);
+                const long long end = min(cu1, unit0 + (long long)(s + 1) * tiles);
+                SPair &P = s_pair[n];
+                P.u_end = end;
+                P.m = m;
+                P.s = s;
+                P.g_lo = s * gk;
+                P.g_n = min(gk, ng - P.g_lo);
+                // a pair that reads the same fragments as the one before shares them
+                const bool same = n > 0 && p.m[pm].frag == frag && p.m[pm].cols == cols && s_pair[n - 1].g_lo == P.g_lo &&
+                                  s_pair[n - 1].g_n == P.g_n && p.m[pm].B == B;
+                if (same) {
+                    P.frag_off = s_pair[n - 1].frag_off;
+                    P.ginv_off = s_pair[n - 1].ginv_off;
+                } else {
+                    P.frag_off = foff;
+                    P.ginv_off = goff;
+                    foff += P.g_n * cols * 16;
+                    goff += B * P.g_n;
+                }
+                pm = m;
+                ++n;
+                u = end;
+            }
+            s_pair[n].u_end = 0x7fffffffffffffffLL;  // sentinel
+            s_npair = n;
+            // the host planned every range to fit; a block whose range does not
+            // is reported and does nothing
+            s_bad = u < cu1 || (size_t)foff * 16 + (size_t)goff * 4 > (size_t)p.frag_budget;
+            if (s_bad && p.status) atomicOr(p.status, 0x47570010u);
+        }
+        __syncwarp();
+        // the pairs' matrix descriptors, word by word across the lanes
+        for (int n = 0; n < s_npair; ++n) {
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(&p.m[s_pair[n].m]);
+            for (int w = lane; w < (int)(sizeof(SMat) / 4); w += 32) reinterpret_cast<uint32_t *>(&s_mat[n])[w] = src[w];
+        }
     }
     if (threadIdx.x < 16) s_lv[threadIdx.x] = p.lut[threadIdx.x];
     __syncthreads();
