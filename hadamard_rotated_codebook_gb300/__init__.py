@@ -13,6 +13,7 @@ Page citations use the page title and section:
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 from dataclasses import dataclass
 from typing import Iterable, Optional, Sequence
@@ -72,8 +73,12 @@ def _io_ptr(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
 def _on(device):
     """Makes `device` current for a library call: the library keeps its
     per-device state (SM count, status word, workspaces, the fixed scratch
-    array) for the device that is current when it is called."""
-    return torch.cuda.device(device)
+    array) for the device that is current when it is called. When it is
+    current already, nothing is switched (the common case costs one query)."""
+    dev = torch.device(device) if not isinstance(device, torch.device) else device
+    if dev.index is None or dev.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(dev)
 
 
 def _check_blob(blob: torch.Tensor, out: int, n_in: int, group: int, bits: int, name: str = "blob"):

@@ -38,6 +38,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
+#include <vector>
 
 #include "cq_internal.h"
 
@@ -836,8 +838,8 @@ struct Need {
 };
 
 // Launches the GEMV over the CTAs gathered in p; resets p.
-static int flush(FastParams &p, int &nm, int &nlut, Need &need, cudaStream_t st) {
-    if (!p.n_items) return CQ_OK;
+// Shared-memory layout of a launch from its needs; the dynamic bytes.
+static size_t fast_layout(FastParams &p, const Need &need) {
     size_t off = 0;
     auto place = [&](int &field, size_t bytes) {
         field = (int)off;
@@ -849,8 +851,10 @@ static int flush(FastParams &p, int &nm, int &nlut, Need &need, cudaStream_t st)
     place(p.smem_red, need.red);
     place(p.smem_tab, 256 * 32 * sizeof(uint32_t));  // either table: 32 KB
     place(p.smem_terms, (size_t)kWarps * kMaxFastB * kGroup * sizeof(uint32_t));  // rotation scratch: 16 KB
-    const size_t smem = off;
-    p.n_mats = nm;
+    return off;
+}
+
+static int fast_launch(const FastParams &p, size_t smem, cudaStream_t st) {
     if (smem > 200 * 1024) return set_error(CQ_ERR_SHAPE, "fast GEMV needs %zu bytes of shared memory", smem);
     {
         const int rc = ensure_smem(reinterpret_cast<const void *>(gemv_fast_kernel), 200 * 1024);
@@ -869,6 +873,46 @@ static int flush(FastParams &p, int &nm, int &nlut, Need &need, cudaStream_t st)
     cudaLaunchKernelEx(&cfg, gemv_fast_kernel, p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "fast gemv launch: %s", cudaGetErrorString(e));
+    return CQ_OK;
+}
+
+// Recent single-launch calls of this host thread: their descriptors, their
+// levels and the parameter blocks built from them. A call with the same
+// descriptors and levels as one of them (a decode loop calls the same grouped
+// GEMVs, one per layer group, every token) is launched from its block without
+// rebuilding it. Entries are found by a key mixed from the buffer addresses
+// and confirmed by comparing every descriptor byte and level.
+struct FastMemo {
+    uint64_t key = 0;
+    std::vector<cq_gemv_desc> d;
+    std::vector<float> levels;
+    FastParams p;
+    size_t smem = 0;
+};
+constexpr int kFastMemos = 64;
+
+static uint64_t memo_key(const cq_gemv_desc *d, const int *idx, int n) {
+    uint64_t h = 0x9e3779b97f4a7c15ull ^ (uint64_t)n;
+    for (int ii = 0; ii < n; ++ii) {
+        const cq_gemv_desc &D = d[idx[ii]];
+        h = (h ^ reinterpret_cast<uintptr_t>(D.blob)) * 0x100000001b3ull;
+        h = (h ^ reinterpret_cast<uintptr_t>(D.y)) * 0x100000001b3ull;
+    }
+    return h;
+}
+
+static void memo_levels(const cq_gemv_desc &D, std::vector<float> &out) {
+    const int L = levels_of(D.bits);
+    for (int j = 0; j < L; ++j) out.push_back(D.codebook[j]);
+}
+
+static int flush(FastParams &p, int &nm, int &nlut, Need &need, cudaStream_t st, int *launches = nullptr) {
+    if (!p.n_items) return CQ_OK;
+    p.n_mats = nm;
+    const size_t smem = fast_layout(p, need);
+    const int rc = fast_launch(p, smem, st);
+    if (rc) return rc;
+    if (launches) ++*launches;
     p.n_items = 0;
     nm = 0;
     nlut = 0;
@@ -878,11 +922,24 @@ static int flush(FastParams &p, int &nm, int &nlut, Need &need, cudaStream_t st)
 
 int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream) {
     static thread_local FastParams p;  // large: off the stack, one per host thread
+    static thread_local std::vector<FastMemo> memos;
+    static thread_local int memo_next = 0;
+    static thread_local std::vector<float> lv_now;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the same descriptors and levels as a recent single-launch call: launch its block
+    const uint64_t key = memo_key(d, idx, n);
+    lv_now.clear();
+    for (int ii = 0; ii < n; ++ii) memo_levels(d[idx[ii]], lv_now);
+    for (const FastMemo &m : memos) {
+        if (m.key != key || (int)m.d.size() != n || m.levels != lv_now) continue;
+        bool same = true;
+        for (int ii = 0; ii < n && same; ++ii) same = std::memcmp(&d[idx[ii]], &m.d[ii], sizeof(cq_gemv_desc)) == 0;
+        if (same) return fast_launch(m.p, m.smem, st);
+    }
     p.n_items = 0;
-    int nlut = 0, nm = 0;
+    int nlut = 0, nm = 0, launches = 0;
     Need need;
-    auto do_flush = [&]() -> int { return flush(p, nm, nlut, need, st); };
+    auto do_flush = [&]() -> int { return flush(p, nm, nlut, need, st, &launches); };
     for (int ii = 0; ii < n; ++ii) {
         const cq_gemv_desc &D = d[idx[ii]];
         const int ip = in_padded(D.in), W = width_of(D.bits), ng = ip / kGroup;
@@ -962,6 +1019,23 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
         need.frag = std::max(need.frag, (size_t)M.ng * 32 * kFragWords * sizeof(uint32_t));
         if (M.kchunks > 1) need.red = std::max(need.red, (size_t)M.tiles * M.kchunks * 16 * kMaxFastB * sizeof(float));
         ++nm;
+    }
+    if (launches == 0 && p.n_items > 0) {  // one launch holds the call: remember its block
+        p.n_mats = nm;
+        const size_t smem = fast_layout(p, need);
+        const int rc = fast_launch(p, smem, st);
+        if (rc) return rc;
+        if ((int)memos.size() < kFastMemos) memos.emplace_back();
+        FastMemo &memo = memos[memo_next];
+        memo_next = (memo_next + 1) % kFastMemos;
+        memo.key = key;
+        memo.d.clear();
+        for (int ii = 0; ii < n; ++ii) memo.d.push_back(d[idx[ii]]);
+        memo.levels = lv_now;
+        memo.p = p;
+        memo.smem = smem;
+        p.n_items = 0;
+        return CQ_OK;
     }
     return do_flush();
 }
