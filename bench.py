@@ -616,7 +616,9 @@ def gemv_kernel_name(out, n_in, bits, B, group=128):
     ng = (n_in + group - 1) // group
     ng128 = (n_in + 127) // 128
     w = 2 if bits == 5 else bits
-    if B <= 4 and 16 <= ng128 <= 32 and ((group == 64 and n_in % 128 == 0 and w != 3) or (group == 128 and w == 3)):
+    if group == 64 and B <= 4 and n_in % 128 == 0 and w != 3 and ng128 <= 128:
+        return "act_frag_kernel + gemv_split_kernel"
+    if B <= 4 and 16 <= ng128 <= 32 and group == 128 and w == 3:
         return "gemv_stream_kernel"
     if B <= 4 and group == 128 and w != 3 and ng < 16:
         return "gemv_fast_kernel"

@@ -213,16 +213,19 @@ int launch_b(int bmax, const GemvParams &p, size_t smem, int grid, cudaStream_t 
 
 int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // Small batches go to the tensor-core kernels (one launch for all of the
-    // matrices with inputs up to 15 groups, a streamed launch for wider
-    // ones); the rest run here.
+    // The tensor-core kernels take what they can: one launch for all of the
+    // matrices with inputs up to 15 groups, a streamed launch for 3-bit codes
+    // of 16 to 32 groups, a rotation launch and split or sliced products for
+    // the rest (groups of 64 go there first, and to the streamed kernel only
+    // if no split launch takes them); what is left runs here.
     int fast_idx[CQ_MAX_GROUPED], nfast = 0, stream_idx[CQ_MAX_GROUPED], nstream = 0;
-    int wide_idx[CQ_MAX_GROUPED], nwide = 0;
+    int wide_idx[CQ_MAX_GROUPED], nwide = 0, rejected[CQ_MAX_GROUPED], nrej = 0;
     bool is_fast[CQ_MAX_GROUPED];
     for (int i = 0; i < n; ++i) {
-        const bool sf = gemv_stream_eligible(d[i]);
-        const bool ff = !sf && gemv_fast_eligible(d[i]);
-        const bool wf = !sf && !ff && gemv_wide_eligible(d[i]);
+        const bool g64w = d[i].group == kGroup64 && gemv_wide_eligible(d[i]);
+        const bool sf = !g64w && gemv_stream_eligible(d[i]);
+        const bool ff = !g64w && !sf && gemv_fast_eligible(d[i]);
+        const bool wf = g64w || (!sf && !ff && gemv_wide_eligible(d[i]));
         is_fast[i] = sf || ff || wf;
         if (sf) stream_idx[nstream++] = i;
         else if (ff) fast_idx[nfast++] = i;
@@ -232,12 +235,17 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
         int st2 = launch_gemv_fast(d, fast_idx, nfast, stream);
         if (st2) return st2;
     }
+    if (nwide) {
+        int st2 = launch_gemv_wide(d, wide_idx, nwide, stream, rejected, &nrej);
+        if (st2) return st2;
+        for (int r = 0; r < nrej; ++r) {
+            const int i = rejected[r];
+            if (gemv_stream_eligible(d[i])) stream_idx[nstream++] = i;
+            else is_fast[i] = false;
+        }
+    }
     if (nstream) {
         int st2 = launch_gemv_stream(d, stream_idx, nstream, stream);
-        if (st2) return st2;
-    }
-    if (nwide) {
-        int st2 = launch_gemv_wide(d, wide_idx, nwide, stream);
         if (st2) return st2;
     }
     // One launch per code width present; each launch walks all descriptors of

@@ -60,6 +60,7 @@ struct WAct {
     const void *x;     // [B][in], fp32 or int8
     const float *xs;   // [B] for int8
     int xdt, in, ng, B;
+    int g64;           // groups of 64: two 64-point transforms per 128-span, half-major fragments
     int cols;          // fragment columns: 2B (hi, lo) for B <= 4, else 8 * ceil(B / 8) (hi)
     long long frag;    // word offset of the fragments in the workspace: [g][4 k][cols][4 t][4 words]
     long long ginv;    // float offset of 1/sigma [B][ng] in the workspace
@@ -91,6 +92,11 @@ __device__ __forceinline__ float w_pow2_scale(float amax, float lim) {
 // 2j and 2j + 1 of lane t. Words are stored 4 to a 16-byte unit, the units of
 // one k = f / 4 consecutive over (column, t), so that a warp's 16-byte loads
 // of them are free of bank conflicts.
+// Groups of 64 (a 128-span holds two): the butterfly stops before the stage
+// that mixes the halves, and the words are half-major: word 2j + h of lane t
+// holds positions 64 (j / 4) + 16t + 4 (j % 4) + 2h + {0, 1}, so MMAs 0-3 of
+// a span read only its first half and MMAs 4-7 only its second; lane
+// l = 16 (j / 4) + 4t + j % 4 owns them.
 __global__ void __launch_bounds__(kWThreads) act_frag_kernel(const __grid_constant__ WActParams p) {
     // the GEMV launched after this one may start its prologue at once
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -124,12 +130,15 @@ __global__ void __launch_bounds__(kWThreads) act_frag_kernel(const __grid_consta
         v[2] = a0 - a2;
         v[3] = a1 - a3;
     }
+    const int mlim = A.g64 ? 16 : 32;  // lane bit 4 is position bit 6: the halves of a span
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1)
+        if (m < mlim) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
-            v[i] = (lane & m) ? o - v[i] : v[i] + o;
+            for (int i = 0; i < 4; ++i) {
+                const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+                v[i] = (lane & m) ? o - v[i] : v[i] + o;
+            }
         }
     // int8 activations give integers |z| <= 128 * 128, which hi + lo carry
     // exactly unscaled; otherwise scale by a power of two to |sigma z| <= 2^14
@@ -149,7 +158,7 @@ __global__ void __launch_bounds__(kWThreads) act_frag_kernel(const __grid_consta
         hi16[i] = __half_as_ushort(h);
         lo16[i] = __half_as_ushort(l);
     }
-    const int t = lane >> 3, j = lane & 7;
+    const int t = A.g64 ? (lane >> 2) & 3 : lane >> 3, j = A.g64 ? ((lane >> 4) << 2) | (lane & 3) : lane & 7;
     const bool hilo = A.B <= 4;
     uint32_t *base = p.frag + A.frag;
     const int k = j >> 1, w2 = 2 * (j & 1);  // words 2j, 2j+1: unit k, offset w2
@@ -524,8 +533,9 @@ __global__ void __launch_bounds__(kWGThreads, 1) gemv_wide_kernel(const __grid_c
 // ----------------------------------------------------- split products --
 // gemv_split_kernel: the product step behind the same rotation launch, with
 // the work cut finer than a block's run of tiles and every warp on its own
-// pipeline. The host sends it batches of 1 to 4 with 1-, 2- and 4-bit codes
-// (the kernel itself takes every width and batches up to 16). A
+// pipeline. It takes batches of 1 to 4 with 1-, 2- and 4-bit codes, at
+// groups of 128 and of 64 (3-bit codes, two groups per 96-byte chunk, and
+// larger batches run faster on the sliced kernel above). A
 // unit is (matrix, k-slice of its groups, 16-row tile); units are numbered
 // matrix by matrix, k-slice by k-slice, tile fastest, and each block takes an
 // equal contiguous range of them, split evenly over its 16 warps. A matrix
@@ -537,15 +547,14 @@ __global__ void __launch_bounds__(kWGThreads, 1) gemv_wide_kernel(const __grid_c
 // depend on the order in which they finish.
 //
 // Every warp streams its own units through shared-memory stages of one
-// chunk each: two stages of 16 rows x 256 code bytes (eight CQ2 groups, four
-// CQ4 groups, sixteen binary groups), or three of 16 x 96 (two CQ3 groups).
-// One lane per row issues a 1-D TMA bulk copy of the row's chunk (completion
+// chunk each: two stages of 16 rows x 256 code bytes (eight CQ2 128-spans,
+// four CQ4 spans, sixteen binary spans). One lane per row issues a 1-D TMA bulk copy of the row's chunk (completion
 // on the stage's mbarrier) and a cp.async of its norms. No block barrier runs inside the loop. A block
 // copies the fragments of the (matrix, k-slice) pairs of its range into
 // shared memory once, after the rotation launch is complete.
 constexpr int kSWarps = 16;
 constexpr int kSThreads = 32 * kSWarps;
-constexpr int kSStages = 3;
+constexpr int kSStages = 2;
 constexpr int kSMaxMats = 128;
 constexpr int kSMaxPairs = 24;  // (matrix, k-slice) pairs of one block's range
 
@@ -582,17 +591,21 @@ static_assert(sizeof(SParams) <= 32000, "kernel parameter block");
 // Code bytes per group and groups per chunk of each kind.
 __host__ __device__ constexpr int s_gbytes(int kind) { return kind == 0 ? 32 : kind == 1 ? 64 : kind == 2 ? 16 : 48; }
 __host__ __device__ constexpr int s_gc(int kind) { return kind == 0 ? 8 : kind == 1 ? 4 : kind == 2 ? 16 : 2; }
-// Stages per warp: two of 256 code bytes per row for 1-, 2- and 4-bit codes,
-// three of 96 for 3-bit codes.
-__host__ __device__ constexpr int s_ns(int kind) { return kind == 3 ? 3 : 2; }
 // Row stride of a stage: the chunk plus padding that spreads a warp's reads
-// of its rows over the banks (as for the sliced kernel's stages).
-__host__ __device__ constexpr int s_rs(int kind) {
-    return kind == 0 ? 288 : kind == 1 ? 320 : kind == 2 ? 272 : 176;
+// of its rows over the banks (as for the sliced kernel's stages). Groups of
+// 64 read 4-byte words (2-bit codes) or 8-byte words (4-bit) of each half,
+// rows 4 and 8 banks apart; 1-bit codes 2-byte halves, rows 4 banks apart.
+__host__ __device__ constexpr int s_rs(int kind, bool g64 = false) {
+    return g64 ? (kind == 1 ? 288 : 272) : kind == 0 ? 288 : kind == 1 ? 320 : kind == 2 ? 272 : 176;
 }
-// Bytes of norms per row of a stage (a multiple of 16).
-__host__ __device__ constexpr int s_nr(int kind) { return (2 * s_gc(kind) + 15) / 16 * 16; }
-__host__ __device__ constexpr int s_stage_bytes(int kind) { return 16 * s_rs(kind) + 16 * s_nr(kind); }
+// Bytes of norms per row of a stage (a multiple of 16): one fp16 norm per
+// group, two per 128-span for groups of 64.
+__host__ __device__ constexpr int s_nr(int kind, bool g64 = false) {
+    return (2 * s_gc(kind) * (g64 ? 2 : 1) + 15) / 16 * 16;
+}
+__host__ __device__ constexpr int s_stage_bytes(int kind, bool g64 = false) {
+    return 16 * s_rs(kind, g64) + 16 * s_nr(kind, g64);
+}
 
 // One (matrix, k-slice) pair of a block's range and where its fragments and
 // 1/sigma sit in shared memory.
@@ -617,26 +630,54 @@ __device__ __forceinline__ bool s_wait(uint32_t bar, uint32_t parity) {
     return false;
 }
 
-// Two groups of a chunk (g, g + 1) as two independent MMA chains, for one
-// column block; the second group's codes, fragments and norms are zero when
-// `two` is false (its chain then adds nothing).
-template <int KIND, bool HILO>
+// The code words of one 128-span of groups of 64 for this lane, in the
+// half-major order of the fragments: MMA nu reads positions
+// 64 (nu / 4) + 16t + 4 (nu % 4) .. +3, so the words of each half are loaded
+// apart and w_decode then indexes them as it does for groups of 128.
+template <int KIND>
+__device__ __forceinline__ void s_load64(const uint8_t *r0, const uint8_t *r1, int t, WCodes &c) {
+    if (KIND == 0) {  // bytes 4t .. 4t+3 of each 16-byte half
+        c.r[0] = *reinterpret_cast<const uint32_t *>(r0 + 4 * t), c.r[1] = *reinterpret_cast<const uint32_t *>(r0 + 16 + 4 * t);
+        c.s[0] = *reinterpret_cast<const uint32_t *>(r1 + 4 * t), c.s[1] = *reinterpret_cast<const uint32_t *>(r1 + 16 + 4 * t);
+    } else if (KIND == 1) {  // bytes 8t .. 8t+7 of each 32-byte half
+        const uint2 a = *reinterpret_cast<const uint2 *>(r0 + 8 * t), b = *reinterpret_cast<const uint2 *>(r0 + 32 + 8 * t);
+        const uint2 e = *reinterpret_cast<const uint2 *>(r1 + 8 * t), f = *reinterpret_cast<const uint2 *>(r1 + 32 + 8 * t);
+        c.r[0] = a.x, c.r[1] = a.y, c.r[2] = b.x, c.r[3] = b.y, c.s[0] = e.x, c.s[1] = e.y, c.s[2] = f.x, c.s[3] = f.y;
+    } else {  // 1-bit codes: bytes 2t, 2t+1 of each 8-byte half, as one word
+        const uint16_t *q0 = reinterpret_cast<const uint16_t *>(r0), *q1 = reinterpret_cast<const uint16_t *>(r1);
+        c.r[0] = (uint32_t)q0[t] | ((uint32_t)q0[4 + t] << 16);
+        c.s[0] = (uint32_t)q1[t] | ((uint32_t)q1[4 + t] << 16);
+    }
+}
+
+// Two groups of a chunk (g, g + 1) as two independent MMA chains (fragment
+// columns 2b and 2b + 1: the hi and lo terms of batch row b); the second
+// group's codes, fragments and norms are zero when `two` is false (its chain
+// then adds nothing). G64: g and g + 1 are
+// 128-spans of two groups of 64 each; MMAs 0-3 and 4-7 of a span then run as
+// separate chains, scaled by the norms of the first half (n..) and of the
+// second (m..).
+template <int KIND, bool G64>
 __device__ __forceinline__ void s_group2(const uint8_t *r0, int rs, const uint8_t *tab, const uint32_t *frag, int g,
-                                         int cols, int B, int ngs, float n0a, float n1a, float n0b, float n1b, bool two,
-                                         const float *ginv, const uint4 *zero, float (&acc)[4]) {
+                                         int cols, int B, int ngs, float n0a, float n1a, float n0b, float n1b,
+                                         float m0a, float m1a, float m0b, float m1b, bool two, const float *ginv,
+                                         const uint4 *zero, float (&acc)[4]) {
+    static_assert(!G64 || KIND != 3, "groups of 64: 1-, 2- and 4-bit codes");
     const int lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
     constexpr int GB = s_gbytes(KIND);
     WCodes ca, cb;
-    w_load<KIND>(r0, r0 + 8 * rs, t, ca);
+    if (G64) s_load64<KIND>(r0, r0 + 8 * rs, t, ca);
+    else w_load<KIND>(r0, r0 + 8 * rs, t, ca);
     if (two) {
-        w_load<KIND>(r0 + GB, r0 + GB + 8 * rs, t, cb);
+        if (G64) s_load64<KIND>(r0 + GB, r0 + GB + 8 * rs, t, cb);
+        else w_load<KIND>(r0 + GB, r0 + GB + 8 * rs, t, cb);
     } else {
 #pragma unroll
         for (int i = 0; i < 4; ++i) cb.r[i] = cb.s[i] = 0u;
     }
     // this lane's fragment column gq; lanes of columns past the batch read
     // the zero block (one address, no selects on the loaded words)
-    const bool live = HILO ? gq < 2 * B : gq < B;
+    const bool live = gq < 2 * B;
     const uint4 *f4 = reinterpret_cast<const uint4 *>(frag);
     const uint4 *pa = live ? f4 + (((size_t)g * 4) * cols + gq) * 4 + t : zero;
     const uint4 *pb = live && two ? f4 + (((size_t)(g + 1) * 4) * cols + gq) * 4 + t : zero;
@@ -649,36 +690,41 @@ __device__ __forceinline__ void s_group2(const uint8_t *r0, int rs, const uint8_
         fb[4 * k] = vb.x, fb[4 * k + 1] = vb.y, fb[4 * k + 2] = vb.z, fb[4 * k + 3] = vb.w;
     }
     float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+    float ea[4] = {0.f, 0.f, 0.f, 0.f}, eb[4] = {0.f, 0.f, 0.f, 0.f};  // second halves (G64)
 #pragma unroll
     for (int nu = 0; nu < 8; ++nu) {
         uint32_t a[4], b[4];
         w_decode<KIND>(ca, nu, tab, lane, a);
         w_decode<KIND>(cb, nu, tab, lane, b);
-        w_mma(da, a, fa[2 * nu], fa[2 * nu + 1]);
-        w_mma(db, b, fb[2 * nu], fb[2 * nu + 1]);
+        if (G64 && nu >= 4) {
+            w_mma(ea, a, fa[2 * nu], fa[2 * nu + 1]);
+            w_mma(eb, b, fb[2 * nu], fb[2 * nu + 1]);
+        } else {
+            w_mma(da, a, fa[2 * nu], fa[2 * nu + 1]);
+            w_mma(db, b, fb[2 * nu], fb[2 * nu + 1]);
+        }
     }
-    if (HILO) {  // columns 2t, 2t+1: hi and lo terms of batch row t
-        const float ia = t < B ? ginv[t * ngs + g] : 0.0f, ib = t < B && two ? ginv[t * ngs + g + 1] : 0.0f;
-        acc[0] = fmaf(n0b * ib, db[0], fmaf(n0a * ia, da[0], acc[0]));
-        acc[1] = fmaf(n0b * ib, db[1], fmaf(n0a * ia, da[1], acc[1]));
-        acc[2] = fmaf(n1b * ib, db[2], fmaf(n1a * ia, da[2], acc[2]));
-        acc[3] = fmaf(n1b * ib, db[3], fmaf(n1a * ia, da[3], acc[3]));
-    } else {  // columns 2t, 2t+1: batch rows 2t, 2t+1
-        const int b0 = 2 * t;
-        const float i0a = b0 < B ? ginv[b0 * ngs + g] : 0.0f, i1a = b0 + 1 < B ? ginv[(b0 + 1) * ngs + g] : 0.0f;
-        const float i0b = b0 < B && two ? ginv[b0 * ngs + g + 1] : 0.0f;
-        const float i1b = b0 + 1 < B && two ? ginv[(b0 + 1) * ngs + g + 1] : 0.0f;
-        acc[0] = fmaf(n0b * i0b, db[0], fmaf(n0a * i0a, da[0], acc[0]));
-        acc[1] = fmaf(n0b * i1b, db[1], fmaf(n0a * i1a, da[1], acc[1]));
-        acc[2] = fmaf(n1b * i0b, db[2], fmaf(n1a * i0a, da[2], acc[2]));
-        acc[3] = fmaf(n1b * i1b, db[3], fmaf(n1a * i1a, da[3], acc[3]));
+    // this lane's outputs: columns 2t, 2t+1 (hi and lo terms of batch row t)
+    const float ia = t < B ? ginv[t * ngs + g] : 0.0f, ib = t < B && two ? ginv[t * ngs + g + 1] : 0.0f;
+    acc[0] = fmaf(n0b * ib, db[0], fmaf(n0a * ia, da[0], acc[0]));
+    acc[1] = fmaf(n0b * ib, db[1], fmaf(n0a * ia, da[1], acc[1]));
+    acc[2] = fmaf(n1b * ib, db[2], fmaf(n1a * ia, da[2], acc[2]));
+    acc[3] = fmaf(n1b * ib, db[3], fmaf(n1a * ia, da[3], acc[3]));
+    if (G64) {
+        acc[0] = fmaf(m0b * ib, eb[0], fmaf(m0a * ia, ea[0], acc[0]));
+        acc[1] = fmaf(m0b * ib, eb[1], fmaf(m0a * ia, ea[1], acc[1]));
+        acc[2] = fmaf(m1b * ib, eb[2], fmaf(m1a * ia, ea[2], acc[2]));
+        acc[3] = fmaf(m1b * ib, eb[3], fmaf(m1a * ia, ea[3], acc[3]));
     }
 }
 
-template <int KIND, int NB, bool HILO>
+template <int KIND, bool G64>
 __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_constant__ SParams p) {
-    constexpr int GC = s_gc(KIND), GB = s_gbytes(KIND), RS = s_rs(KIND), SB = s_stage_bytes(KIND), NS = s_ns(KIND);
-    constexpr int NR = s_nr(KIND) / 2;  // norms per row of a stage
+    constexpr int GC = s_gc(KIND), GB = s_gbytes(KIND), RS = s_rs(KIND, G64), SB = s_stage_bytes(KIND, G64);
+    constexpr int NS = kSStages;
+    constexpr int NR = s_nr(KIND, G64) / 2;  // norms per row of a stage
+    constexpr int NPS = G64 ? 2 : 1;         // norms per 128-span
+    constexpr float kScale = G64 ? 0.125f : kWInvSqrt128;  // 1 / sqrt(group)
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ __align__(8) uint64_t s_bar[kSWarps * kSStages];
     __shared__ SPair s_pair[kSMaxPairs + 1];
@@ -785,7 +831,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
         ivalid = min(16, M.out - row0);
         const int r = row0 + min(lane & 15, ivalid - 1);  // rows past the matrix repeat the last one
         irow = M.codes + (size_t)r * M.ng * GB;
-        inrow = M.norms + (size_t)r * M.ng;
+        inrow = M.norms + (size_t)r * M.ng * NPS;
     };
     int iq = 0, copied = 0;  // next stage to fill; chunks with copies so far
     auto issue = [&]() {
@@ -807,23 +853,24 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
                     "l"(irow + (size_t)ga * GB), "r"(bytes), "r"(bar)
                     : "memory");
             if (lane < 16) {  // this row's norms of the chunk
-                const __half *src = inrow + ga;
+                const __half *src = inrow + ga * NPS;
+                const int nn = gcnt * NPS;
                 __half *dst = reinterpret_cast<__half *>(st + 16 * RS + lane * 2 * NR);
-                if ((gcnt & 7) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+                if ((nn & 7) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
 #pragma unroll
-                    for (int i = 0; i < GC; i += 8)
-                        if (i < gcnt)
+                    for (int i = 0; i < GC * NPS; i += 8)
+                        if (i < nn)
                             asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(s_smem(dst + i)),
                                          "l"(src + i)
                                          : "memory");
-                } else if (((reinterpret_cast<uintptr_t>(src) & 3) == 0) && (gcnt & 1) == 0) {
+                } else if (((reinterpret_cast<uintptr_t>(src) & 3) == 0) && (nn & 1) == 0) {
 #pragma unroll
-                    for (int i = 0; i < GC; i += 2)
-                        if (i < gcnt)
+                    for (int i = 0; i < GC * NPS; i += 2)
+                        if (i < nn)
                             asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s_smem(dst + i)), "l"(src + i)
                                          : "memory");
                 } else {
-                    for (int i = 0; i < gcnt; ++i) dst[i] = src[i];
+                    for (int i = 0; i < nn; ++i) dst[i] = src[i];
                 }
             }
             if (++ic == inch && ++iu < wu1) iload();
@@ -881,9 +928,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
     if (wu0 < wu1 && !abort) cload();
     int cq = 0, done = 0;
     uint32_t phase = 0;  // bit q: parity of stage q's next completion
-    float acc[NB][4];
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // rows gq, gq + 8 x columns 2t, 2t + 1 (hi, lo of batch row t)
     const uint8_t *tab = smem;
     while (cu < wu1 && !abort) {
         issue();
@@ -898,25 +943,24 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
         const uint8_t *st = stage0 + cq * SB;
         const __half *sn = reinterpret_cast<const __half *>(st + 16 * RS);
         const int gl0 = cc * GC, gcnt = min(GC, cgn - gl0);  // the chunk's groups, local to the k-slice
-        if (NB == 1) {
 #pragma unroll
-            for (int gl = 0; gl < GC; gl += 2) {
-                if (gl < gcnt) {
-                    const bool two = gl + 1 < gcnt;
-                    const float n0a = __half2float(sn[gq * NR + gl]);
-                    const float n1a = __half2float(sn[(gq + 8) * NR + gl]);
-                    const float n0b = two ? __half2float(sn[gq * NR + gl + 1]) : 0.0f;
-                    const float n1b = two ? __half2float(sn[(gq + 8) * NR + gl + 1]) : 0.0f;
-                    s_group2<KIND, HILO>(st + gq * RS + gl * GB, RS, tab, cfrag, gl0 + gl, ccols, cB, cgn, n0a, n1a,
-                                         n0b, n1b, two, cginv, &s_zero, reinterpret_cast<float(&)[4]>(acc[0]));
+        for (int gl = 0; gl < GC; gl += 2) {
+            if (gl < gcnt) {
+                const bool two = gl + 1 < gcnt;
+                // norms of rows gq and gq + 8: span gl (a) and gl + 1 (b);
+                // for groups of 64 the first halves' (n) and second halves' (m)
+                const __half *s0 = sn + gq * NR + gl * NPS, *s1 = sn + (gq + 8) * NR + gl * NPS;
+                const float n0a = __half2float(s0[0]), n1a = __half2float(s1[0]);
+                const float n0b = two ? __half2float(s0[NPS]) : 0.0f, n1b = two ? __half2float(s1[NPS]) : 0.0f;
+                float m0a = n0a, m1a = n1a, m0b = n0b, m1b = n1b;
+                if (G64) {
+                    m0a = __half2float(s0[1]);
+                    m1a = __half2float(s1[1]);
+                    m0b = two ? __half2float(s0[3]) : 0.0f;
+                    m1b = two ? __half2float(s1[3]) : 0.0f;
                 }
-            }
-        } else {
-            for (int gl = 0; gl < gcnt; ++gl) {
-                const float n0 = __half2float(sn[gq * NR + gl]);
-                const float n1 = __half2float(sn[(gq + 8) * NR + gl]);
-                w_group<KIND, NB, HILO>(st + gq * RS + gl * GB, RS, tab, cfrag, gl0 + gl, ccols, cB, cgn, n0, n1,
-                                        cginv, acc);
+                s_group2<KIND, G64>(st + gq * RS + gl * GB, RS, tab, cfrag, gl0 + gl, ccols, cB, cgn, n0a, n1a, n0b,
+                                    n1b, m0a, m1a, m0b, m1b, two, cginv, &s_zero, acc);
             }
         }
         cq = cq + 1 == NS ? 0 : cq + 1;
@@ -925,49 +969,23 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
             const SMat &M = s_mat[cpair];
             const int B = cB;
             const int row_r = 16 * ct + gq, row_s = row_r + 8;
-            // this lane's values: (batch row, row) pairs
-            float v[NB][4];
-            int bb[NB][4];
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-                if (HILO) {
-                    v[nb][0] = acc[nb][0] + acc[nb][1];
-                    v[nb][1] = acc[nb][2] + acc[nb][3];
-                    bb[nb][0] = bb[nb][1] = t;
-                    bb[nb][2] = bb[nb][3] = kWMaxB;  // unused
-                    v[nb][2] = v[nb][3] = 0.0f;
-                } else {
-                    v[nb][0] = acc[nb][0];
-                    v[nb][1] = acc[nb][2];
-                    v[nb][2] = acc[nb][1];
-                    v[nb][3] = acc[nb][3];
-                    bb[nb][0] = bb[nb][1] = 8 * nb + 2 * t;
-                    bb[nb][2] = bb[nb][3] = 8 * nb + 2 * t + 1;
-                }
-                acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
-            }
+            // this lane's values: batch row t, rows gq and gq + 8 (hi + lo terms)
+            const float vr = acc[0] + acc[1], vs = acc[2] + acc[3];
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
             if (M.nks == 1) {
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int b = bb[nb][j], row = (j & 1) ? row_s : row_r;
-                        if (b < B && row < M.out) {
-                            const float a = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[b], kWInvSqrt128) : kWInvSqrt128;
-                            M.y[(size_t)b * M.out + row] = v[nb][j] * a;
-                        }
-                    }
+                if (t < B) {
+                    const float a = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[t], kScale) : kScale;
+                    if (row_r < M.out) M.y[(size_t)t * M.out + row_r] = vr * a;
+                    if (row_s < M.out) M.y[(size_t)t * M.out + row_s] = vs * a;
+                }
             } else {
                 // partial sums of this k-slice, then the tile's counter
                 const int s = cglo / M.gk;
                 float *part = p.part + (M.part0 + (long long)s * M.tiles + ct) * 16 * B;
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int b = bb[nb][j];
-                        if (b < B) part[((j & 1) ? gq + 8 : gq) * B + b] = v[nb][j];
-                    }
+                if (t < B) {
+                    part[gq * B + t] = vr;
+                    part[(gq + 8) * B + t] = vs;
+                }
                 __threadfence();
                 __syncwarp();
                 unsigned old = 0;
@@ -989,7 +1007,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
                         if (e2 >= E) return;
                         const int r = e2 / B, b = e2 - r * B, row = 16 * ct + r;
                         if (row < M.out) {
-                            const float a = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[b], kWInvSqrt128) : kWInvSqrt128;
+                            const float a = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[b], kScale) : kScale;
                             M.y[(size_t)b * M.out + row] = v2 * a;
                         }
                     };
@@ -1073,9 +1091,9 @@ size_t s_table_bytes(int kind) { return kind == 0 || kind == 1 ? 32768 : kind ==
 // block range fits its fragments in shared memory. Returns the dynamic
 // shared memory, or 0 if no split fits (the caller uses the sliced kernel).
 size_t plan_split(SParams &p, const cq_gemv_desc *d, const int *idx, const int *sel, int cnt, const int *act_of,
-                  const WAct *acts, int kind, int grid, long long &part_floats, int &counters) {
+                  const WAct *acts, int kind, bool g64, int grid, long long &part_floats, int &counters) {
     if (cnt > kSMaxMats) return 0;
-    const size_t stages = (size_t)kSWarps * s_ns(kind) * s_stage_bytes(kind);
+    const size_t stages = (size_t)kSWarps * kSStages * s_stage_bytes(kind, g64);
     const size_t limit = 227 * 1024 - 6 * 1024;  // dynamic shared memory next to the static arrays
     if (s_table_bytes(kind) + stages >= limit) return 0;
     const size_t budget = limit - s_table_bytes(kind) - stages;
@@ -1180,9 +1198,9 @@ size_t plan_split(SParams &p, const cq_gemv_desc *d, const int *idx, const int *
     return 0;
 }
 
-template <int KIND, int NB, bool HILO>
+template <int KIND, bool G64>
 int s_launch(const SParams &p, int grid, size_t smem, cudaStream_t st) {
-    auto k = gemv_split_kernel<KIND, NB, HILO>;
+    auto k = gemv_split_kernel<KIND, G64>;
     const int rc = ensure_smem(reinterpret_cast<const void *>(k), smem);
     if (rc) return rc;
     cudaLaunchConfig_t cfg = {};
@@ -1199,13 +1217,6 @@ int s_launch(const SParams &p, int grid, size_t smem, cudaStream_t st) {
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "split gemv launch: %s", cudaGetErrorString(e));
     return CQ_OK;
-}
-
-template <int KIND>
-int s_launch_cls(int cls, const SParams &p, int grid, size_t smem, cudaStream_t st) {
-    if (cls == 0) return s_launch<KIND, 1, true>(p, grid, smem, st);
-    if (cls == 1) return s_launch<KIND, 1, false>(p, grid, smem, st);
-    return s_launch<KIND, 2, false>(p, grid, smem, st);
 }
 
 template <int NB, bool HILO>
@@ -1232,13 +1243,17 @@ int w_launch(WParams &p, int grid, size_t smem, cudaStream_t st) {
 }  // namespace
 
 bool gemv_wide_eligible(const cq_gemv_desc &d) {
-    if (d.group != kGroup || d.in <= 0 || d.out <= 0 || d.B < 1 || d.B > kWMaxB) return false;
+    if (d.in <= 0 || d.out <= 0 || d.B < 1 || d.B > kWMaxB) return false;
     const int W = width_of(d.bits), ng = in_padded(d.in) / kGroup;
     if (W < 1 || W > 4 || ng > 128) return false;
-    return w_frag_bytes(ng, d.B) <= (size_t)kWFragBudget;
+    // groups of 64 in whole 128-spans: the split products only (batches up
+    // to 4, 1-, 2- and 4-bit codes)
+    if (d.group == kGroup64) return d.in % kGroup == 0 && d.B <= 4 && W != 3;
+    return d.group == kGroup && w_frag_bytes(ng, d.B) <= (size_t)kWFragBudget;
 }
 
-int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream) {
+int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream, int *rejected, int *n_rejected) {
+    *n_rejected = 0;
     if (n <= 0) return CQ_OK;
     static thread_local WActParams ap;  // large: off the stack, one per host thread
     static thread_local WParams wp;
@@ -1254,7 +1269,7 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream)
         int a = -1;
         for (int j = 0; j < n_act; ++j)
             if (acts[j].x == D.x && acts[j].xs == D.x_scale && acts[j].xdt == D.x_dtype && acts[j].in == D.in &&
-                acts[j].B == D.B)
+                acts[j].B == D.B && acts[j].g64 == (D.group == kGroup64))
                 a = j;
         if (a < 0) {
             WAct &A = acts[n_act];
@@ -1264,6 +1279,7 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream)
             A.in = D.in;
             A.ng = in_padded(D.in) / kGroup;
             A.B = D.B;
+            A.g64 = D.group == kGroup64;
             A.cols = w_cols(D.B);
             A.frag = words;
             A.ginv = floats;
@@ -1273,10 +1289,12 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream)
         }
         act_of[ii] = a;
     }
-    // ---- the split launches: one per (batch class, code width, codebook);
-    // what does not fit them goes to the sliced kernel ----
+    // ---- the split launches: one per (batch class, code width, group,
+    // codebook); what does not fit them goes to the sliced kernel (groups of
+    // 128) or back to the caller (groups of 64) ----
     struct Plan {
-        int kind, cls;
+        int kind;
+        bool g64;
         size_t smem;
     };
     static thread_local std::vector<SParams> plans;
@@ -1291,6 +1309,7 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream)
             if (taken[ii]) continue;
             const cq_gemv_desc &D0 = d[idx[ii]];
             const int cls = D0.B <= 4 ? 0 : D0.B <= 8 ? 1 : 2, kind = w_kind(D0.bits);
+            const bool g64 = D0.group == kGroup64;
             float lv0[16];
             level_table(D0.bits, D0.codebook, lv0);
             int sel[CQ_MAX_GROUPED], cnt = 0;
@@ -1298,7 +1317,7 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream)
                 if (taken[jj]) continue;
                 const cq_gemv_desc &D = d[idx[jj]];
                 const int c2 = D.B <= 4 ? 0 : D.B <= 8 ? 1 : 2;
-                if (c2 != cls || w_kind(D.bits) != kind) continue;
+                if (c2 != cls || w_kind(D.bits) != kind || (D.group == kGroup64) != g64) continue;
                 float lv[16];
                 level_table(D.bits, D.codebook, lv);
                 bool same = true;
@@ -1311,7 +1330,7 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream)
             // the split products serve batches of up to 4 with 1-, 2- and 4-bit
             // codes; 3-bit codes (two groups per chunk) and larger batches run
             // faster on the sliced kernel
-            if (cls != 0 || kind == 3) {
+            if (cls != 0 || kind == 3) {  // never groups of 64 (see gemv_wide_eligible)
                 for (int j = 0; j < cnt; ++j) sliced[sel[j]] = true;
                 continue;
             }
@@ -1319,13 +1338,17 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream)
                 const int c = std::min(kSMaxMats, cnt - b0);
                 if (plans.size() <= meta.size()) plans.resize(meta.size() + 1);
                 SParams &P = plans[meta.size()];
-                const size_t smem = plan_split(P, d, idx, sel + b0, c, act_of, acts, kind, grid, part_floats, counters);
+                const size_t smem =
+                    plan_split(P, d, idx, sel + b0, c, act_of, acts, kind, g64, grid, part_floats, counters);
                 if (!smem) {
-                    for (int j = 0; j < c; ++j) sliced[sel[b0 + j]] = true;
+                    for (int j = 0; j < c; ++j) {
+                        if (g64) rejected[(*n_rejected)++] = idx[sel[b0 + j]];
+                        else sliced[sel[b0 + j]] = true;
+                    }
                     continue;
                 }
                 for (int k = 0; k < 16; ++k) P.lut[k] = __float2half_rn(lv0[k]);
-                meta.push_back({kind, cls, smem});
+                meta.push_back({kind, g64, smem});
             }
         }
     }
@@ -1365,12 +1388,13 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream)
         P.part = part;
         P.cnt = cnt;
         P.status = device_status_ptr();
+        const bool g64 = meta[k].g64;
+        const size_t smem = meta[k].smem;
         int rc = CQ_OK;
         switch (meta[k].kind) {
-        case 0: rc = s_launch_cls<0>(meta[k].cls, P, grid, meta[k].smem, st); break;
-        case 1: rc = s_launch_cls<1>(meta[k].cls, P, grid, meta[k].smem, st); break;
-        case 2: rc = s_launch_cls<2>(meta[k].cls, P, grid, meta[k].smem, st); break;
-        default: rc = s_launch_cls<3>(meta[k].cls, P, grid, meta[k].smem, st); break;
+        case 0: rc = g64 ? s_launch<0, true>(P, grid, smem, st) : s_launch<0, false>(P, grid, smem, st); break;
+        case 1: rc = g64 ? s_launch<1, true>(P, grid, smem, st) : s_launch<1, false>(P, grid, smem, st); break;
+        default: rc = g64 ? s_launch<2, true>(P, grid, smem, st) : s_launch<2, false>(P, grid, smem, st); break;
         }
         if (rc) return rc;
     }

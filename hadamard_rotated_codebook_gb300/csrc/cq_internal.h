@@ -65,11 +65,14 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
 // launches over d[idx[0..n)].
 bool gemv_stream_eligible(const cq_gemv_desc &d);
 int launch_gemv_stream(const cq_gemv_desc *d, const int *idx, int n, void *stream);
-// Tensor-core GEMV for the other shapes at group 128 (wide inputs, 3-bit
-// codes, batches up to 16; cq_gemv_wide.cu): a rotation launch into a
-// workspace, then the products; which descriptors, and the launches.
+// Tensor-core GEMV for the other shapes (cq_gemv_wide.cu): wide inputs,
+// 3-bit codes and batches up to 16 at group 128, and groups of 64 in whole
+// 128-spans at batches up to 4. A rotation launch into a workspace, then the
+// products; which descriptors, and the launches. Groups of 64 that no split
+// launch can take are returned in rejected[0..*n_rejected) (descriptor
+// indices; room for n) for the streamed or the fp32 kernel.
 bool gemv_wide_eligible(const cq_gemv_desc &d);
-int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream);
+int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream, int *rejected, int *n_rejected);
 
 
 // --------------------------------------------------------------- gemm --

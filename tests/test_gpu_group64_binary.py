@@ -149,10 +149,10 @@ def test_gather_out_of_range_group64(C):
 @pytest.mark.parametrize("group,bits", [(64, 1), (64, 2), (64, 4), (128, 1), (128, 4)])
 @pytest.mark.parametrize("B", [1, 3])
 @pytest.mark.parametrize("shape", [(200, 2048), (37, 4096)])
-def test_gemv_wide_inputs_streamed(C, group, bits, B, shape):
-    """Inputs of 16 to 32 spans of 128 take the streamed tensor-core kernel
-    (one rotation per block and matrix; groups of 64 as two chains per span),
-    ragged row counts included."""
+def test_gemv_wide_inputs(C, group, bits, B, shape):
+    """Inputs of 16 to 32 spans of 128 take the split tensor-core products
+    (a rotation launch, then per-warp units; groups of 64 as two chains per
+    span with their own norms), ragged row counts included."""
     out, n_in = shape
     blob = _rand_blob(out, n_in, bits, group, 98 + out + bits + group + B)
     cb = O.analytic_codebook(bits, group)
@@ -160,13 +160,13 @@ def test_gemv_wide_inputs_streamed(C, group, bits, B, shape):
     y = C.cq_gemv(torch.from_numpy(blob).cuda(), out, n_in, bits, cb, x.cuda(), group=group)
     torch.cuda.synchronize()
     y_ref, bound = O.matmul(O.dequant(blob, out, n_in, bits, cb, group), x.numpy())
-    check_matmul(y.cpu().numpy(), y_ref, bound, f"streamed g{group} cq{bits} B={B} {shape}")
+    check_matmul(y.cpu().numpy(), y_ref, bound, f"wide g{group} cq{bits} B={B} {shape}")
 
 
-def test_gemv_more_streamed_matrices_than_one_launch_holds(C):
+def test_gemv_more_wide_matrices_than_one_launch_holds(C):
     """210 wide matrices (16 rows each, in = 2048; CQ2 and binary at group
-    128 interleaved) in one grouped call: more than one streamed launch
-    holds, so the call is split."""
+    128 interleaved) in one grouped call: more than one split launch holds
+    (128 matrices), so each code width's set is cut in two launches."""
     items, refs = [], []
     x = S.normal((2, 2048), 120)
     xd = x.cuda()
