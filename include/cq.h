@@ -145,16 +145,18 @@ int cq_act_quant_int8(const float *X, int M, int in, int8_t *Xq, float *s,
  * it"). Every shape at group 128 runs on the tensor cores (mma.sync, fp32
  * accumulation) with the codebook levels rounded to fp16: B <= 4 with 1-, 2-
  * and 4-bit codes and in < 2048 in one launch whose blocks rotate their own
- * activation; 3-bit codes at B <= 4 with 2048 <= in <= 4096, and groups of
- * 64 on such inputs (other than 3-bit), through one persistent block per SM
- * that streams the code rows; the other group-128 shapes (inputs of 2048
- * up to 128 groups, batches 5 to 16) as a rotation launch, which writes
- * each distinct activation's MMA fragments once into a library-owned device
- * workspace (grown on demand: make one untimed call before capturing a CUDA
- * graph), followed by the products: per-warp pipelines over (matrix,
- * k-slice, 16-row tile) units for B <= 4 with 1-, 2- and 4-bit codes, whose
- * k-slices of a tile are summed in slice order (the results do not depend
- * on scheduling), and block-wide slices otherwise. z enters as fp16 hi + lo
+ * activation; 3-bit codes at B <= 4 with 2048 <= in <= 4096 through one
+ * persistent block per SM that streams the code rows; the other group-128
+ * shapes (inputs of 2048 up to 128 groups, batches 5 to 16), and groups of
+ * 64 whose input is a multiple of 128 (up to 16384) at B <= 4 with 1-, 2-
+ * and 4-bit codes, as a rotation launch, which writes each distinct
+ * activation's MMA fragments once into a library-owned device workspace
+ * (grown on demand: make one untimed call before capturing a CUDA graph),
+ * followed by the products: per-warp pipelines over (matrix, k-slice,
+ * 16-row tile) units for B <= 4 with 1-, 2- and 4-bit codes, whose k-slices
+ * of a tile are summed in slice order (the results do not depend on
+ * scheduling), and block-wide slices otherwise. Groups of 64 that no
+ * per-warp plan fits take the streaming kernel. z enters as fp16 hi + lo
  * terms for B <= 4 and as one fp16 term for B >= 5. The remaining shapes
  * (the rest of group 64, batches of 5 to 16 with too many groups for the
  * workspace's shared-memory stage) use fp32 arithmetic.
