@@ -74,6 +74,8 @@ int ensure_smem(const void *func, size_t bytes) {
     return CQ_OK;
 }
 
+static void reset_counters();
+
 int read_and_clear_device_status(void *stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     unsigned int v = 0;
@@ -84,7 +86,10 @@ int read_and_clear_device_status(void *stream) {
     const unsigned int zero = 0;
     e = cudaMemcpyToSymbol(g_cq_device_status, &zero, sizeof(zero));
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
-    if (v & ~kStatusIndex) return set_error(CQ_ERR_TIMEOUT, "a bounded device wait gave up (code 0x%08x)", v);
+    if (v & ~kStatusIndex) {
+        reset_counters();
+        return set_error(CQ_ERR_TIMEOUT, "a bounded device wait gave up (code 0x%08x)", v);
+    }
     if (v) return set_error(CQ_ERR_INDEX, "a gathered row index was out of range");
     return CQ_OK;
 }
@@ -1260,6 +1265,47 @@ void *stream_workspace(void *stream, int kind, size_t bytes, int *err) {
     w.ptr = p;
     w.bytes = want;
     return w.ptr;
+}
+
+constexpr int kCounterKind = 3;  // stream_workspace kind of the zeroed counters
+
+unsigned int *stream_counters(void *stream, size_t n, int *err) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    WsBuf &w = g_ws[WsKey{dev, st, kCounterKind}];
+    const size_t bytes = n * sizeof(unsigned int);
+    if (w.bytes >= bytes) return static_cast<unsigned int *>(w.ptr);
+    const size_t want = std::max(bytes, (size_t)4096);
+    void *p = nullptr;
+    if (cudaMalloc(&p, want) != cudaSuccess) {
+        cudaGetLastError();
+        *err = set_error(CQ_ERR_NOMEM, "cannot allocate %zu bytes of counters", want);
+        return nullptr;
+    }
+    if (cudaMemsetAsync(p, 0, want, st) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p);
+        *err = set_error(CQ_ERR_CUDA, "cannot clear the counters");
+        return nullptr;
+    }
+    if (w.ptr) g_ws_retired.push_back(w.ptr);
+    w.ptr = p;
+    w.bytes = want;
+    return static_cast<unsigned int *>(w.ptr);
+}
+
+// After a device wait gave up: every counter buffer of this device back to zero.
+static void reset_counters() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    cudaDeviceSynchronize();
+    for (auto &kv : g_ws)
+        if (kv.first.dev == dev && kv.first.kind == kCounterKind && kv.second.ptr)
+            cudaMemset(kv.second.ptr, 0, kv.second.bytes);
+    cudaDeviceSynchronize();
 }
 
 // Distinct activations of a call and their workspace (256-byte aligned

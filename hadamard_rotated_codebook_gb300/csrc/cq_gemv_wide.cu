@@ -60,7 +60,7 @@ struct WAct {
     const void *x;     // [B][in], fp32 or int8
     const float *xs;   // [B] for int8
     int xdt, in, ng, B;
-    int g64;           // groups of 64: two 64-point transforms per 128-span, half-major fragments
+    int g64;           // groups of 64 (told apart from the same x read at group 128)
     int cols;          // fragment columns: 2B (hi, lo) for B <= 4, else 8 * ceil(B / 8) (hi)
     long long frag;    // word offset of the fragments in the workspace: [g][4 k][cols][4 t][4 words]
     long long ginv;    // float offset of 1/sigma [B][ng] in the workspace
@@ -71,8 +71,6 @@ struct WActParams {
     int task0[kWMaxActs + 1];  // first warp task of each activation
     uint32_t *frag;
     float *ginv;
-    unsigned int *zero;  // tile counters of the split products, cleared here
-    int n_zero;
     WAct a[kWMaxActs];
 };
 
@@ -91,16 +89,11 @@ __device__ __forceinline__ float w_pow2_scale(float amax, float lim) {
 // 32t + 4j + 2h + {0, 1}: lane l = 8t + j owns exactly the positions of words
 // 2j and 2j + 1 of lane t. Words are stored 4 to a 16-byte unit, the units of
 // one k = f / 4 consecutive over (column, t), so that a warp's 16-byte loads
-// of them are free of bank conflicts.
-// Groups of 64 (a 128-span holds two): the butterfly stops before the stage
-// that mixes the halves, and the words are half-major: word 2j + h of lane t
-// holds positions 64 (j / 4) + 16t + 4 (j % 4) + 2h + {0, 1}, so MMAs 0-3 of
-// a span read only its first half and MMAs 4-7 only its second; lane
-// l = 16 (j / 4) + 4t + j % 4 owns them.
+// of them are free of bank conflicts. (This launch serves the sliced
+// kernel; the split products rotate their activations themselves.)
 __global__ void __launch_bounds__(kWThreads) act_frag_kernel(const __grid_constant__ WActParams p) {
     // the GEMV launched after this one may start its prologue at once
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-    for (int i = blockIdx.x * kWThreads + threadIdx.x; i < p.n_zero; i += gridDim.x * kWThreads) p.zero[i] = 0u;
     const int lane = threadIdx.x & 31;
     const int task = blockIdx.x * kWWarps + (threadIdx.x >> 5);
     if (task >= p.task0[p.n]) return;
@@ -130,15 +123,12 @@ __global__ void __launch_bounds__(kWThreads) act_frag_kernel(const __grid_consta
         v[2] = a0 - a2;
         v[3] = a1 - a3;
     }
-    const int mlim = A.g64 ? 16 : 32;  // lane bit 4 is position bit 6: the halves of a span
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1)
-        if (m < mlim) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
-                v[i] = (lane & m) ? o - v[i] : v[i] + o;
-            }
+        for (int i = 0; i < 4; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+            v[i] = (lane & m) ? o - v[i] : v[i] + o;
         }
     // int8 activations give integers |z| <= 128 * 128, which hi + lo carry
     // exactly unscaled; otherwise scale by a power of two to |sigma z| <= 2^14
@@ -158,7 +148,7 @@ __global__ void __launch_bounds__(kWThreads) act_frag_kernel(const __grid_consta
         hi16[i] = __half_as_ushort(h);
         lo16[i] = __half_as_ushort(l);
     }
-    const int t = A.g64 ? (lane >> 2) & 3 : lane >> 3, j = A.g64 ? ((lane >> 4) << 2) | (lane & 3) : lane & 7;
+    const int t = lane >> 3, j = lane & 7;
     const bool hilo = A.B <= 4;
     uint32_t *base = p.frag + A.frag;
     const int k = j >> 1, w2 = 2 * (j & 1);  // words 2j, 2j+1: unit k, offset w2
@@ -550,8 +540,9 @@ __global__ void __launch_bounds__(kWGThreads, 1) gemv_wide_kernel(const __grid_c
 // chunk each: two stages of 16 rows x 256 code bytes (eight CQ2 128-spans,
 // four CQ4 spans, sixteen binary spans). One lane per row issues a 1-D TMA bulk copy of the row's chunk (completion
 // on the stage's mbarrier) and a cp.async of its norms. No block barrier runs inside the loop. A block
-// copies the fragments of the (matrix, k-slice) pairs of its range into
-// shared memory once, after the rotation launch is complete.
+// rotates the activation groups of the (matrix, k-slice) pairs of its range
+// into shared memory once, after the launch before it is complete (one
+// launch per call: no rotation launch on the critical path).
 constexpr int kSWarps = 16;
 constexpr int kSThreads = 32 * kSWarps;
 constexpr int kSStages = 2;
@@ -564,8 +555,9 @@ struct SMat {
     float *y;
     const float *xs;
     long long unit0;  // first unit of the matrix
-    long long frag;   // word offset of its activation's fragments
-    long long ginv;   // float offset of its activation's 1/sigma
+    const void *x;    // the activation [B][in], fp32 or int8
+    int act;          // which distinct activation of the launch x is
+    int in;
     int out, ng, B, xdt, cols;
     int tiles, nks, gk;  // 16-row tiles, k-slices, groups per k-slice
     int cnt0;            // first tile counter (k-sliced matrices)
@@ -576,8 +568,6 @@ struct SParams {
     int n_mats;
     long long total_units;
     long long units_before[kSMaxMats + 1];
-    const uint32_t *frag;
-    const float *ginv;
     float *part;
     unsigned int *cnt;
     unsigned int *status;
@@ -764,7 +754,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
                 const SMat &M = p.m[m];
                 const long long unit0 = M.unit0;
                 const int tiles = M.tiles, gk = M.gk, ng = M.ng, cols = M.cols, B = M.B;
-                const long long frag = M.frag;
+                const int act = M.act;
                 const int s = (int)((u - unit0) / tiles);
                 const long long end = min(cu1, unit0 + (long long)(s + 1) * tiles);
                 SPair &P = s_pair[n];
@@ -774,7 +764,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
                 P.g_lo = s * gk;
                 P.g_n = min(gk, ng - P.g_lo);
                 // a pair that reads the same fragments as the one before shares them
-                const bool same = n > 0 && p.m[pm].frag == frag && p.m[pm].cols == cols && s_pair[n - 1].g_lo == P.g_lo &&
+                const bool same = n > 0 && p.m[pm].act == act && p.m[pm].cols == cols && s_pair[n - 1].g_lo == P.g_lo &&
                                   s_pair[n - 1].g_n == P.g_n && p.m[pm].B == B;
                 if (same) {
                     P.frag_off = s_pair[n - 1].frag_off;
@@ -883,25 +873,91 @@ __global__ void __launch_bounds__(kSThreads, 1) gemv_split_kernel(const __grid_c
     // the code copies do not depend on the launch before this one
     for (int i = 0; i + 1 < NS; ++i) issue();
 
-    // ---- fragments and 1/sigma of the range's pairs, once the rotation is complete ----
+    // ---- fragments and 1/sigma of the range's pairs: this block rotates the
+    // k-slice groups of each distinct (activation, k-slice) it meets, once
+    // the launch before this one (which may write the activation) is
+    // complete. A task is (pair, group of the slice, batch row): one warp
+    // runs the FWHT of the group in registers (lane l holds positions
+    // 4l .. 4l+3) and writes the fp16 hi and lo terms of sigma z straight
+    // into the MMA B-fragment layout, as the rotation launch does for the
+    // sliced kernel. Groups of 64 stop before the butterfly stage that mixes
+    // a span's halves (lane bit 4 is position bit 6) and take a half-major
+    // word order: word 2j + h of MMA lane t holds positions
+    // 64 (j / 4) + 16t + 4 (j % 4) + 2h + {0, 1}, so MMAs 0-3 of a span read
+    // only its first half and MMAs 4-7 only its second (lane
+    // l = 16 (j / 4) + 4t + j % 4 owns them). ----
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     uint4 *sfrag = reinterpret_cast<uint4 *>(smem + p.smem_frag);
     float *sginv = reinterpret_cast<float *>(smem + p.smem_frag);
-    int ginv_base = 0;  // after every pair's fragments
-    for (int i = 0; i < (ok_range ? s_npair : 0); ++i)
-        ginv_base = max(ginv_base, s_pair[i].frag_off + s_pair[i].g_n * s_mat[i].cols * 16);
-    sginv += 4 * ginv_base;
+    int ginv_base = 0, ntask = 0;  // after every pair's fragments; rotation tasks of the range
     for (int i = 0; i < (ok_range ? s_npair : 0); ++i) {
-        if (i > 0 && s_pair[i].frag_off == s_pair[i - 1].frag_off) continue;
+        ginv_base = max(ginv_base, s_pair[i].frag_off + s_pair[i].g_n * s_mat[i].cols * 16);
+        if (i == 0 || s_pair[i].frag_off != s_pair[i - 1].frag_off) ntask += s_pair[i].g_n * s_mat[i].B;
+    }
+    sginv += 4 * ginv_base;
+    for (int task = warp; task < ntask; task += kSWarps) {
+        int i = 0, base = 0;  // the pair of the task
+        for (;; ++i) {
+            if (i > 0 && s_pair[i].frag_off == s_pair[i - 1].frag_off) continue;
+            const int nt = s_pair[i].g_n * s_mat[i].B;
+            if (task < base + nt) break;
+            base += nt;
+        }
         const SPair &P = s_pair[i];
         const SMat &M = s_mat[i];
-        const int n16 = P.g_n * M.cols * 16;
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.frag + M.frag) + (size_t)P.g_lo * M.cols * 16;
-        for (int e = threadIdx.x; e < n16; e += kSThreads) sfrag[P.frag_off + e] = src[e];
-        for (int e = threadIdx.x; e < M.B * P.g_n; e += kSThreads) {
-            const int b = e / P.g_n, g = e - b * P.g_n;
-            sginv[P.ginv_off + e] = p.ginv[M.ginv + (size_t)b * M.ng + P.g_lo + g];
+        const int local = task - base, gl = local / M.B, b = local - gl * M.B;
+        const int col0 = (P.g_lo + gl) * kGroup + 4 * lane;
+        float v[4];
+        if (M.xdt == CQ_X_I8) {
+            const int8_t *xq = static_cast<const int8_t *>(M.x) + (size_t)b * M.in;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = col0 + k < M.in ? (float)xq[col0 + k] : 0.0f;
+        } else {
+            const float *xf = static_cast<const float *>(M.x) + (size_t)b * M.in;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = col0 + k < M.in ? xf[col0 + k] : 0.0f;
         }
+        {
+            const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+            v[0] = a0 + a2;
+            v[1] = a1 + a3;
+            v[2] = a0 - a2;
+            v[3] = a1 - a3;
+        }
+#pragma unroll
+        for (int m = 1; m < (G64 ? 16 : 32); m <<= 1)  // lane bit 4 is position bit 6: the halves of a span
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float o = __shfl_xor_sync(0xffffffffu, v[k], m);
+                v[k] = (lane & m) ? o - v[k] : v[k] + o;
+            }
+        // int8 activations give integers |z| <= 128 * 128, which hi + lo carry
+        // exactly unscaled; otherwise scale by a power of two to |sigma z| <= 2^14
+        float sigma = 1.0f;
+        if (M.xdt != CQ_X_I8) {
+            float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+            for (int m = 16; m; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+            sigma = w_pow2_scale(mx, 16384.0f);
+        }
+        uint32_t hi16[4], lo16[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float xs = __fmul_rn(v[k], sigma);
+            const __half h = __float2half_rn(xs);
+            const __half l = __float2half_rn(__fsub_rn(xs, __half2float(h)));
+            hi16[k] = __half_as_ushort(h);
+            lo16[k] = __half_as_ushort(l);
+        }
+        // this lane's positions are words 2j, 2j+1 of MMA lane t (unit k = j / 2, offset 2 (j % 2))
+        const int tt = G64 ? (lane >> 2) & 3 : lane >> 3, j = G64 ? ((lane >> 4) << 2) | (lane & 3) : lane & 7;
+        uint32_t *fw = reinterpret_cast<uint32_t *>(sfrag + P.frag_off);
+        const int k = j >> 1, w2 = 2 * (j & 1);
+        *reinterpret_cast<uint2 *>(fw + ((((size_t)gl * 4 + k) * M.cols + 2 * b) * 4 + tt) * 4 + w2) =
+            make_uint2(hi16[0] | (hi16[1] << 16), hi16[2] | (hi16[3] << 16));
+        *reinterpret_cast<uint2 *>(fw + ((((size_t)gl * 4 + k) * M.cols + 2 * b + 1) * 4 + tt) * 4 + w2) =
+            make_uint2(lo16[0] | (lo16[1] << 16), lo16[2] | (lo16[3] << 16));
+        if (lane == 0) sginv[P.ginv_off + b * P.g_n + gl] = 1.0f / sigma;
     }
     __syncthreads();
 
@@ -1165,8 +1221,9 @@ size_t plan_split(SParams &p, const cq_gemv_desc *d, const int *idx, const int *
             M.y = D.y;
             M.xs = D.x_scale;
             M.unit0 = unit0[j];
-            M.frag = A.frag;
-            M.ginv = A.ginv;
+            M.x = D.x;
+            M.act = act_of[ii];
+            M.in = D.in;
             M.out = D.out;
             M.ng = ng;
             M.B = D.B;
@@ -1262,7 +1319,6 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream,
     // same activation share one rotation) ----
     int act_of[CQ_MAX_GROUPED];
     int n_act = 0;
-    long long words = 0, floats = 0;
     static thread_local WAct acts[CQ_MAX_GROUPED];
     for (int ii = 0; ii < n; ++ii) {
         const cq_gemv_desc &D = d[idx[ii]];
@@ -1281,10 +1337,7 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream,
             A.B = D.B;
             A.g64 = D.group == kGroup64;
             A.cols = w_cols(D.B);
-            A.frag = words;
-            A.ginv = floats;
-            words += (long long)A.ng * A.cols * 64;
-            floats += (long long)A.B * A.ng;
+            A.frag = A.ginv = 0;
             a = n_act++;
         }
         act_of[ii] = a;
@@ -1352,39 +1405,58 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream,
             }
         }
     }
+    // ---- workspace: the fragments of the activations that the sliced
+    // kernel reads (the split products rotate their own), then 1/sigma and
+    // the split products' partial sums; the tile counters live apart,
+    // zeroed when allocated and left zero by every launch ----
+    bool need[CQ_MAX_GROUPED] = {};
+    for (int ii = 0; ii < n; ++ii)
+        if (sliced[ii]) need[act_of[ii]] = true;
+    long long words = 0, floats = 0;
+    for (int a = 0; a < n_act; ++a) {
+        if (!need[a]) continue;
+        acts[a].frag = words;
+        acts[a].ginv = floats;
+        words += (long long)acts[a].ng * acts[a].cols * 64;
+        floats += (long long)acts[a].B * acts[a].ng;
+    }
     int err = 0;
-    const size_t ws_bytes = (size_t)words * 4 + (size_t)floats * 4 + (size_t)part_floats * 4 + (size_t)counters * 4 + 64;
+    const size_t ws_bytes = (size_t)words * 4 + (size_t)floats * 4 + (size_t)part_floats * 4 + 64;
     uint8_t *ws = static_cast<uint8_t *>(stream_workspace(stream, 2, ws_bytes, &err));
     if (!ws) return err;
     uint32_t *frag = reinterpret_cast<uint32_t *>(ws);
     float *ginv = reinterpret_cast<float *>(ws + (size_t)words * 4);
     float *part = ginv + floats;
-    unsigned int *cnt = reinterpret_cast<unsigned int *>(part + part_floats);
-    // ---- 1. one rotation launch per kWMaxActs activations (the first also
-    // clears the split launches' tile counters) ----
-    for (int a0 = 0; a0 < n_act; a0 += kWMaxActs) {
-        const int c = std::min(kWMaxActs, n_act - a0);
-        ap.n = c;
-        ap.frag = frag;
-        ap.ginv = ginv;
-        ap.zero = cnt;
-        ap.n_zero = a0 == 0 ? counters : 0;
-        int tasks = 0;
-        for (int j = 0; j < c; ++j) {
-            ap.a[j] = acts[a0 + j];
-            ap.task0[j] = tasks;
-            tasks += acts[a0 + j].ng * acts[a0 + j].B;
+    unsigned int *cnt = nullptr;
+    if (counters) {
+        cnt = stream_counters(stream, (size_t)counters, &err);
+        if (!cnt) return err;
+    }
+    // ---- 1. one rotation launch per kWMaxActs activations of the sliced kernel ----
+    {
+        int sel_act[CQ_MAX_GROUPED], na = 0;
+        for (int a = 0; a < n_act; ++a)
+            if (need[a]) sel_act[na++] = a;
+        for (int a0 = 0; a0 < na; a0 += kWMaxActs) {
+            const int c = std::min(kWMaxActs, na - a0);
+            ap.n = c;
+            ap.frag = frag;
+            ap.ginv = ginv;
+            int tasks = 0;
+            for (int j = 0; j < c; ++j) {
+                ap.a[j] = acts[sel_act[a0 + j]];
+                ap.task0[j] = tasks;
+                tasks += ap.a[j].ng * ap.a[j].B;
+            }
+            ap.task0[c] = tasks;
+            act_frag_kernel<<<(tasks + kWWarps - 1) / kWWarps, kWThreads, 0, st>>>(ap);
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "activation rotation launch: %s", cudaGetErrorString(e));
         }
-        ap.task0[c] = tasks;
-        act_frag_kernel<<<(tasks + kWWarps - 1) / kWWarps, kWThreads, 0, st>>>(ap);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "activation rotation launch: %s", cudaGetErrorString(e));
     }
     // ---- 2. the split products ----
     for (size_t k = 0; k < meta.size(); ++k) {
         SParams &P = plans[k];
-        P.frag = frag;
-        P.ginv = ginv;
         P.part = part;
         P.cnt = cnt;
         P.status = device_status_ptr();

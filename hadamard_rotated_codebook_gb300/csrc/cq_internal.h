@@ -92,6 +92,12 @@ int ensure_smem(const void *func, size_t bytes);
 // selects an independent buffer (0: GEMM rotated or padded activations).
 // Grow-only; null with *err set if allocation fails.
 void *stream_workspace(void *stream, int kind, size_t bytes, int *err);
+// Zero-initialised device counters (at least n) for work queued on `stream`:
+// grow-only, zeroed on the stream when (re)allocated. The kernels that use
+// them leave them zero; read_and_clear_device_status zeroes them again
+// after a device wait gave up (an aborted launch may leave some nonzero).
+// Null with *err set if allocation fails.
+unsigned int *stream_counters(void *stream, size_t n, int *err);
 
 // Device status word shared by kernels with bounded waits (defined in
 // cq_gemm.cu; kernels OR a nonzero code into it when a wait gives up).
