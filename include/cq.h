@@ -149,13 +149,13 @@ int cq_act_quant_int8(const float *X, int M, int in, int8_t *Xq, float *s,
  * persistent block per SM that streams the code rows; the other group-128
  * shapes (inputs of 2048 up to 128 groups, batches 5 to 16), and groups of
  * 64 whose input is a multiple of 128 (up to 16384) at B <= 4 with 1-, 2-
- * and 4-bit codes, as a rotation launch, which writes each distinct
- * activation's MMA fragments once into a library-owned device workspace
- * (grown on demand: make one untimed call before capturing a CUDA graph),
- * followed by the products: per-warp pipelines over (matrix, k-slice,
- * 16-row tile) units for B <= 4 with 1-, 2- and 4-bit codes, whose k-slices
- * of a tile are summed in slice order (the results do not depend on
- * scheduling), and block-wide slices otherwise. Groups of 64 that no
+ * and 4-bit codes: for B <= 4 with 1-, 2- and 4-bit codes one launch of
+ * per-warp pipelines over (matrix, k-slice, 16-row tile) units whose blocks
+ * rotate the activation groups they need, the k-slices of a tile summed in
+ * slice order (the results do not depend on scheduling); otherwise a
+ * rotation launch, which writes each distinct activation's MMA fragments
+ * once, and block-wide slices. Both use library-owned device buffers
+ * (grown on demand: make one untimed call before capturing a CUDA graph). Groups of 64 that no
  * per-warp plan fits take the streaming kernel. z enters as fp16 hi + lo
  * terms for B <= 4 and as one fp16 term for B >= 5. The remaining shapes
  * (the rest of group 64, batches of 5 to 16 with too many groups for the
