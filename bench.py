@@ -287,14 +287,16 @@ def decode_workload(C, S, device, copies_min_bytes, samples=None):
 
 def make_plans(C, wl, Xq, xs, ybuf):
     """One grouped-GEMV plan per weight copy, reading the activations Xq/xs
-    and writing ybuf (device tensors, or pinned host tensors)."""
+    and writing ybuf (device tensors, or pinned host tensors). With xs None,
+    Xq holds fp32 activations that the call quantises per token itself."""
     plans = []
     for cp in wl["copies"]:
         items = []
         for m, o, sz, yo in zip(wl["mats"], wl["offs"], wl["sizes"], wl["yoffs"]):
+            act = (dict(x=Xq[m.act:m.act + 1], quantize=True) if xs is None else
+                   dict(x=Xq[m.act:m.act + 1], x_scale=xs[m.act:m.act + 1]))
             items.append(dict(blob=cp[o:o + sz], out=m.out, **{"in": m.n_in}, bits=m.bits, codebook=wl["cbs"][m.bits],
-                              x=Xq[m.act:m.act + 1], x_scale=xs[m.act:m.act + 1],
-                              y=ybuf[yo:yo + m.out].view(1, m.out)))
+                              y=ybuf[yo:yo + m.out].view(1, m.out), **act))
         plans.append(C.GemvPlan(items))
     return plans
 
@@ -482,23 +484,23 @@ def bench_decode(cx, wl, K, Wm):
 
 def bench_e2e(cx, wl, K):
     """The decode step end to end through the public API: every step copies
-    its fp32 activations from pinned host memory to the device, quantises
-    them per token (cq_act_quant_int8), runs the grouped GEMV, whose kernel
-    writes the outputs into pinned host memory in place (the host link,
-    NVLink-C2C on Grace-Blackwell), and the host waits for the step before
-    the next one. `e2e` makes the calls eagerly (the ctypes calls, argument
+    its fp32 activations from pinned host memory to the device and runs the
+    grouped GEMV on them with per-token int8 quantisation inside the call
+    (CQ_X_F32Q: bit-identical to cq_act_quant_int8 followed by the int8
+    call); its kernel writes the outputs into pinned host memory in place
+    (the host link, NVLink-C2C on Grace-Blackwell), and the host waits for
+    the step before the next one. `e2e` makes the calls eagerly (the ctypes calls, argument
     checks and launches are inside the region); `e2e_graph` replays the same
     calls captured once as a CUDA graph."""
     torch, C, stream, R = cx.torch, cx.C, cx.stream, wl["R"]
     X_h = wl["X"].cpu().pin_memory()
     X_d = torch.empty_like(wl["X"])
     y_h = torch.zeros(wl["out_total"], dtype=torch.float32).pin_memory()
-    plans_h = make_plans(C, wl, wl["Xq"], wl["xs"], y_h)
+    plans_h = make_plans(C, wl, X_d, None, y_h)
     h2d, d2h = X_h.numel() * 4, 4 * wl["out_total"]
 
     def one(i):
         X_d.copy_(X_h, non_blocking=True)
-        C.cq_act_quant_int8(X_d, wl["Xq"], wl["xs"])
         plans_h[i % R].run(stream)
 
     Ke = min(K, 2000)
@@ -537,8 +539,8 @@ def bench_e2e(cx, wl, K):
            "batch_ms_per_step": [round(b / per, 6) for b in batch_ms],
            "timing": f"host wall clock over eager steps, each ending in a stream synchronize; median of {nb} "
                      f"batches of {per} steps",
-           "path": "fp32 activations pinned host -> device copy -> cq_act_quant_int8 -> cq_gemv_grouped "
-                   "(outputs written to pinned host memory in place)"}
+           "path": "fp32 activations pinned host -> device copy -> cq_gemv_grouped with per-token int8 "
+                   "quantisation in the call (outputs written to pinned host memory in place)"}
 
     Kg = min(K, 20000)
     ce = min(Kg, 4 * R * max(1, 1000 // (4 * R)))
@@ -556,7 +558,8 @@ def bench_e2e(cx, wl, K):
         raise RuntimeError("graph end-to-end outputs differ from the device-resident run")
     eg = {"value": round(aggregate_gbs(wl["packed"], Kg, cx.world, ms), 1), "unit": "GB/s",
           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Kg, "ms_per_step": round(ms / Kg, 6),
-          "gpu_launches_per_step": 2, "timing": "CUDA events around graph replays of the same steps"}
+          "gpu_launches_per_step": 1, "copies_per_step": 1,
+          "timing": "CUDA events around graph replays of the same steps"}
     return e2e, eg
 
 

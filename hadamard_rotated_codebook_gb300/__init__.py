@@ -23,7 +23,7 @@ import torch
 
 from . import _capi
 from ._capi import (CQ_DTYPE_CQ, CQ_DTYPE_FP16, CQ_DTYPE_FP32, CQ_DTYPE_RAW, CQ_X_F32,
-                    CQ_X_I8, CQError, GemmDesc, GemvDesc, KvGeom, KvSeq, TensorDesc, check)
+                    CQ_X_F32Q, CQ_X_I8, CQError, GemmDesc, GemvDesc, KvGeom, KvSeq, TensorDesc, check)
 
 GROUP = 128
 
@@ -162,13 +162,15 @@ def cq_act_quant_int8(X: torch.Tensor, Xq: Optional[torch.Tensor] = None,
     return Xq, s
 
 
-def _gemv_desc(blob, out, n_in, bits, codebook, x, x_scale, y, group, keep):
+def _gemv_desc(blob, out, n_in, bits, codebook, x, x_scale, y, group, keep, quantize=False):
     x2 = x if x.dim() == 2 else x.reshape(1, -1)
     B = x2.shape[0]
     if x2.shape[1] != n_in:
         raise ValueError(f"x has {x2.shape[1]} columns, matrix has in={n_in}")
+    if quantize and x2.dtype != torch.float32:
+        raise TypeError("quantize=True needs fp32 activations")
     if x2.dtype == torch.float32:
-        xdt, xs = CQ_X_F32, None
+        xdt, xs = (CQ_X_F32Q if quantize else CQ_X_F32), None
     elif x2.dtype == torch.int8:
         xdt = CQ_X_I8
         if x_scale is None:
@@ -193,11 +195,12 @@ def _gemv_desc(blob, out, n_in, bits, codebook, x, x_scale, y, group, keep):
 
 def cq_gemv(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook, x: torch.Tensor,
             x_scale: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
-            group: int = GROUP) -> torch.Tensor:
+            group: int = GROUP, quantize: bool = False) -> torch.Tensor:
     """y[B, out] = W_hat x over one CQ blob; x fp32 [B, in] or int8 with
-    per-token scales x_scale[B]."""
+    per-token scales x_scale[B]. quantize=True: fp32 x is quantised per token
+    to int8 inside the call (as cq_act_quant_int8 does) before the product."""
     keep = []
-    d, y = _gemv_desc(blob, out, n_in, bits, codebook, x, x_scale, y, group, keep)
+    d, y = _gemv_desc(blob, out, n_in, bits, codebook, x, x_scale, y, group, keep, quantize)
     with _on(blob.device):
         check(_lib().cq_gemv_grouped(ctypes.byref(d), 1, _stream(blob.device)))
     return y
@@ -205,13 +208,14 @@ def cq_gemv(blob: torch.Tensor, out: int, n_in: int, bits: int, codebook, x: tor
 
 def cq_gemv_grouped(items: Sequence[dict]) -> list:
     """Runs many GEMVs in one launch. Each item is a dict with keys blob,
-    out, in, bits, codebook, x and optionally x_scale, y. Returns the ys."""
+    out, in, bits, codebook, x and optionally x_scale, y, group, quantize.
+    Returns the ys."""
     if not items:
         return []
     keep, ds, ys = [], [], []
     for it in items:
         d, y = _gemv_desc(it["blob"], it["out"], it["in"], it["bits"], it["codebook"], it["x"],
-                          it.get("x_scale"), it.get("y"), it.get("group", GROUP), keep)
+                          it.get("x_scale"), it.get("y"), it.get("group", GROUP), keep, it.get("quantize", False))
         ds.append(d)
         ys.append(y)
     arr = (GemvDesc * len(ds))(*ds)
@@ -251,7 +255,8 @@ class GemvPlan:
         self._keep, ds, self.ys = [], [], []
         for it in items:
             d, y = _gemv_desc(it["blob"], it["out"], it["in"], it["bits"], it["codebook"], it["x"],
-                              it.get("x_scale"), it.get("y"), it.get("group", GROUP), self._keep)
+                              it.get("x_scale"), it.get("y"), it.get("group", GROUP), self._keep,
+                              it.get("quantize", False))
             ds.append(d)
             self.ys.append(y)
         self._items = list(items)  # keep tensors alive

@@ -19,7 +19,7 @@ P = ctypes.POINTER
 CQ_OK = 0
 CQ_ERR_ARG, CQ_ERR_SHAPE, CQ_ERR_FORMAT, CQ_ERR_IO = -1, -2, -3, -4
 CQ_ERR_CUDA, CQ_ERR_TIMEOUT, CQ_ERR_NOMEM, CQ_ERR_INDEX = -5, -6, -7, -8
-CQ_X_F32, CQ_X_I8 = 0, 1
+CQ_X_F32, CQ_X_I8, CQ_X_F32Q = 0, 1, 2
 CQ_GEMV_MAX_BATCH = 16
 CQ_MAX_GROUPED = 256
 CQ_GEMM_NOALLOC_MAX_ELEMS = 2 * 1024 * 1024

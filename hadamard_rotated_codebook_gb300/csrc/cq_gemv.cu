@@ -211,8 +211,65 @@ int launch_b(int bmax, const GemvParams &p, size_t smem, int grid, cudaStream_t 
 
 }  // namespace
 
-int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream) {
+namespace {
+
+// Whether the descriptor takes the decode kernel (the routing below).
+bool takes_fast(const cq_gemv_desc &d) {
+    const bool g64w = d.group == kGroup64 && gemv_wide_eligible(d);
+    return !g64w && !gemv_stream_eligible(d) && gemv_fast_eligible(d);
+}
+
+// CQ_X_F32Q activations of descriptors that the decode kernel does not take
+// are quantised first (one quantiser launch per distinct activation, into a
+// library workspace); their descriptors then read int8 and the scales. The
+// decode kernel quantises its own. Returns the descriptors to route (d
+// itself when nothing was quantised), or null with *err set.
+const cq_gemv_desc *prequantize(const cq_gemv_desc *d, int n, void *stream, int *err) {
+    bool any = false;
+    for (int i = 0; i < n && !any; ++i) any = d[i].x_dtype == CQ_X_F32Q && d[i].out > 0 && d[i].in > 0 && !takes_fast(d[i]);
+    if (!any) return d;
+    static thread_local cq_gemv_desc dq[CQ_MAX_GROUPED];
+    int src[CQ_MAX_GROUPED];  // descriptor whose activation another one shares (or itself)
+    size_t off[CQ_MAX_GROUPED], bytes = 0;
+    for (int i = 0; i < n; ++i) {
+        dq[i] = d[i];
+        src[i] = -1;
+        if (d[i].x_dtype != CQ_X_F32Q || d[i].out <= 0 || d[i].in <= 0 || takes_fast(d[i])) continue;
+        for (int j = 0; j < i && src[i] < 0; ++j)
+            if (src[j] == j && d[j].x == d[i].x && d[j].in == d[i].in && d[j].B == d[i].B) src[i] = j;
+        if (src[i] >= 0) continue;
+        src[i] = i;
+        off[i] = bytes;  // int8 [B][in], then fp32 scales [B], 256-byte aligned pieces
+        bytes += ((size_t)d[i].B * d[i].in + 255) / 256 * 256 + ((size_t)d[i].B * 4 + 255) / 256 * 256;
+    }
+    uint8_t *ws = static_cast<uint8_t *>(stream_workspace(stream, 4, bytes, err));
+    if (!ws) return nullptr;
+    for (int i = 0; i < n; ++i) {
+        if (src[i] < 0) continue;
+        const int j = src[i];
+        int8_t *q = reinterpret_cast<int8_t *>(ws + off[j]);
+        float *sc = reinterpret_cast<float *>(ws + off[j] + ((size_t)d[j].B * d[j].in + 255) / 256 * 256);
+        if (j == i) {
+            const int rc = launch_act_quant(static_cast<const float *>(d[i].x), d[i].B, d[i].in, q, sc, stream);
+            if (rc) {
+                *err = rc;
+                return nullptr;
+            }
+        }
+        dq[i].x = q;
+        dq[i].x_scale = sc;
+        dq[i].x_dtype = CQ_X_I8;
+    }
+    return dq;
+}
+
+}  // namespace
+
+int launch_gemv_grouped(const cq_gemv_desc *d_in, int n, void *stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int qerr = CQ_OK;
+    const cq_gemv_desc *d = prequantize(d_in, n, stream, &qerr);
+    if (!d) return qerr;
     // The tensor-core kernels take what they can: one launch for all of the
     // matrices with inputs up to 15 groups, a streamed launch for 3-bit codes
     // of 16 to 32 groups, a rotation launch and split or sliced products for

@@ -337,9 +337,45 @@ __device__ __forceinline__ void build_level_table(int kind, const __half *lv, ui
 // The activation of M as B fragments: warp w rotates groups w, w+8, ... of
 // every batch row (scratch `terms`: kWarps x kMaxFastB x 128 words) into
 // frag[g] and 1/sigma into ginv[b][g]. No block barrier: the caller syncs.
-template <bool G64 = false>
-__device__ __forceinline__ void rotate_activation(const FastMat &M, uint8_t *terms_base, uint32_t *frag, float *ginv) {
+// Per-token scales of CQ_X_F32Q activations, by the rule of the activation
+// quantiser (s = absmax/127 with IEEE division, 1 for an all-zero row): the
+// block's threads scan each batch row of x. Every thread of the block calls
+// this (two block barriers).
+__device__ void token_scales(const FastMat &M, float *sq) {
+    __shared__ float red[kMaxFastB][kWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float *x = static_cast<const float *>(M.x);
+    for (int b = 0; b < M.B; ++b) {
+        float amax = 0.0f;
+        for (int k = threadIdx.x; k < M.in; k += kThreads) amax = fmaxf(amax, fabsf(x[(size_t)b * M.in + k]));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) red[b][warp] = amax;
+    }
+    __syncthreads();
+    if (threadIdx.x < M.B) {
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v = fmaxf(v, red[threadIdx.x][w]);
+        sq[threadIdx.x] = v > 0.0f ? __fdiv_rn(v, 127.0f) : 1.0f;
+    }
+    __syncthreads();
+}
+
+// int8 quantisation of four activation values with the token's scale s:
+// clamp(rint(x / s), -128, 127), as the activation quantiser computes it.
+__device__ __forceinline__ void quantize4(float (&v)[4], float s) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = fminf(fmaxf(rintf(__fdiv_rn(v[i], s)), -128.0f), 127.0f);
+}
+
+// QUANT: the launch may hold CQ_X_F32Q activations, quantised here before
+// the rotation with the per-token scales sq.
+template <bool G64 = false, bool QUANT = false>
+__device__ __forceinline__ void rotate_activation(const FastMat &M, uint8_t *terms_base, uint32_t *frag, float *ginv,
+                                                  const float *sq = nullptr) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, ng = M.ng, B = M.B;
+    const bool quant = QUANT && M.xdt == CQ_X_F32Q;
     float xv[kMaxFastB][4];
     if (warp < ng)  // the first group's values, requested before anything else
 #pragma unroll
@@ -351,7 +387,8 @@ __device__ __forceinline__ void rotate_activation(const FastMat &M, uint8_t *ter
         for (int b = 0; b < kMaxFastB; ++b) {
             if (b >= B) break;
             if (g != warp) load_x_bg(M, b, g, lane, xv[b]);
-            const float inv = rotate_bg<G64>(xv[b], lane, terms[b], M.xdt == CQ_X_I8);
+            if (quant) quantize4(xv[b], sq[b]);
+            const float inv = rotate_bg<G64>(xv[b], lane, terms[b], M.xdt == CQ_X_I8 || quant);
             if (lane == 0) ginv[b * ng + g] = inv;
         }
         __syncwarp();
@@ -399,6 +436,9 @@ __device__ __forceinline__ void lut_group64(float (&acc)[4], const uint8_t *rowr
 }
 
 // ------------------------------------------------------------ the kernel --
+// QUANT: the instance for launches with CQ_X_F32Q activations (the others
+// run the instance without the quantisation steps).
+template <bool QUANT>
 __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_constant__ FastParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     // one copy of this CTA's matrix descriptor in shared memory (parameter
@@ -471,7 +511,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     // (which may have written it) is complete: warp w rotates groups w, w+8,
     // ... of every batch row into B fragments and 1/sigma ----
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    rotate_activation(M, smem + p.smem_terms, frag, ginv);
+    __shared__ float s_q[kMaxFastB];  // per-token scales of CQ_X_F32Q activations
+    if (QUANT && M.xdt == CQ_X_F32Q) token_scales(M, s_q);  // uniform across the block
+    rotate_activation<false, QUANT>(M, smem + p.smem_terms, frag, ginv, s_q);
     asm volatile("cp.async.wait_all;\n" ::: "memory");
     __syncthreads();
 
@@ -484,7 +526,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
     const int kc = wide ? 0 : warp % KC;
     const bool live = gq < 2 * B;  // this lane's B column belongs to a batch row
     // output scale of this lane's batch row t
-    const float alpha = t < B && M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[t], kInvSqrt128) : kInvSqrt128;
+    const float alpha = QUANT && t < B && M.xdt == CQ_X_F32Q ? __fmul_rn(s_q[t], kInvSqrt128)
+                        : t < B && M.xdt == CQ_X_I8         ? __fmul_rn(M.xs[t], kInvSqrt128)
+                                                            : kInvSqrt128;
     const uint2 *tab2 = reinterpret_cast<const uint2 *>(smem + p.smem_tab) + (lane & 15);
     const uint32_t *tab4 = reinterpret_cast<const uint32_t *>(smem + p.smem_tab) + lane;
 
@@ -563,7 +607,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fast_kernel(const __grid_con
             if (row >= M.out) continue;
             float sum = 0.0f;
             for (int c = 0; c < KC; ++c) sum += red[((size_t)(tl * KC + c) * 16 + rr) * kMaxFastB + b];
-            const float ab = M.xdt == CQ_X_I8 ? __fmul_rn(M.xs[b], kInvSqrt128) : kInvSqrt128;
+            const float ab = QUANT && M.xdt == CQ_X_F32Q ? __fmul_rn(s_q[b], kInvSqrt128)
+                             : M.xdt == CQ_X_I8          ? __fmul_rn(M.xs[b], kInvSqrt128)
+                                                         : kInvSqrt128;
             M.y[(size_t)b * M.out + row] = sum * ab;
         }
     }
@@ -858,8 +904,11 @@ static size_t fast_layout(FastParams &p, const Need &need) {
 
 static int fast_launch(const FastParams &p, size_t smem, cudaStream_t st) {
     if (smem > 200 * 1024) return set_error(CQ_ERR_SHAPE, "fast GEMV needs %zu bytes of shared memory", smem);
+    bool quant = false;  // CQ_X_F32Q activations in the launch
+    for (int i = 0; i < p.n_mats && !quant; ++i) quant = p.m[i].xdt == CQ_X_F32Q;
+    auto kern = quant ? gemv_fast_kernel<true> : gemv_fast_kernel<false>;
     {
-        const int rc = ensure_smem(reinterpret_cast<const void *>(gemv_fast_kernel), 200 * 1024);
+        const int rc = ensure_smem(reinterpret_cast<const void *>(kern), 200 * 1024);
         if (rc) return rc;
     }
     cudaLaunchConfig_t cfg = {};
@@ -872,7 +921,7 @@ static int fast_launch(const FastParams &p, size_t smem, cudaStream_t st) {
     attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr_pdl;
     cfg.numAttrs = 1;
-    cudaLaunchKernelEx(&cfg, gemv_fast_kernel, p);
+    cudaLaunchKernelEx(&cfg, kern, p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(CQ_ERR_CUDA, "fast gemv launch: %s", cudaGetErrorString(e));
     return CQ_OK;

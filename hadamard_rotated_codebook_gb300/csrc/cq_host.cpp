@@ -180,7 +180,7 @@ static int check_gemv_desc(const cq_gemv_desc &d, int i) {
     if ((st = check_codebook(d.codebook, d.bits))) return prefix_error(st, i);
     if (d.B < 1 || d.B > CQ_GEMV_MAX_BATCH)
         return set_error(CQ_ERR_SHAPE, "descriptor %d: batch must be 1..%d, got %d", i, CQ_GEMV_MAX_BATCH, d.B);
-    if (d.x_dtype != CQ_X_F32 && d.x_dtype != CQ_X_I8)
+    if (d.x_dtype != CQ_X_F32 && d.x_dtype != CQ_X_I8 && d.x_dtype != CQ_X_F32Q)
         return set_error(CQ_ERR_ARG, "descriptor %d: unknown x_dtype %d", i, d.x_dtype);
     if (d.out > 0 && !d.y) return set_error(CQ_ERR_ARG, "descriptor %d: null y", i);
     if (d.out > 0 && d.in > 0 && !d.blob) return set_error(CQ_ERR_ARG, "descriptor %d: null blob", i);

@@ -69,6 +69,11 @@ extern "C" {
 /* Activation element types for cq_gemv. */
 #define CQ_X_F32 0 /* fp32 activations x[B][in] */
 #define CQ_X_I8 1  /* int8 activations q[B][in] with fp32 per-token scales s[B]: x = s*q */
+/* fp32 activations x[B][in], quantised per token inside the call exactly as
+ * cq_act_quant_int8 does (s = absmax/127, q = clamp(rint(x/s))) and then
+ * multiplied as CQ_X_I8 with those scales: the same results, bit for bit, as
+ * cq_act_quant_int8 followed by a CQ_X_I8 call. x_scale is ignored. */
+#define CQ_X_F32Q 2
 
 /* Largest batch accepted by cq_gemv / cq_gemv_grouped. */
 #define CQ_GEMV_MAX_BATCH 16
@@ -160,8 +165,11 @@ int cq_act_quant_int8(const float *X, int M, int in, int8_t *Xq, float *s,
  * terms for B <= 4 and as one fp16 term for B >= 5. The remaining shapes
  * (the rest of group 64, batches of 5 to 16 with too many groups for the
  * workspace's shared-memory stage) use fp32 arithmetic.
- * x: fp32 [B][in] (x_dtype = CQ_X_F32, x_scale ignored, may be NULL) or
- *    int8 [B][in] with x_scale fp32 [B] (x_dtype = CQ_X_I8).
+ * x: fp32 [B][in] (x_dtype = CQ_X_F32, x_scale ignored, may be NULL),
+ *    int8 [B][in] with x_scale fp32 [B] (x_dtype = CQ_X_I8), or fp32 [B][in]
+ *    quantised per token inside the call (x_dtype = CQ_X_F32Q: the decode
+ *    kernel quantises as it rotates, in the same launch; other shapes first
+ *    quantise into a library workspace with one more launch).
  * y: fp32 [B][out], fully overwritten.
  * x, x_scale and y are device memory or page-locked host memory that the
  * device can address (cudaHostAlloc / cudaHostRegister with unified
@@ -181,7 +189,7 @@ int cq_gemv(const uint8_t *blob, int out, int in, int group, int bits,
 typedef struct cq_gemv_desc {
     const uint8_t *blob;
     const void *x;        /* [B][in], fp32 or int8 per x_dtype */
-    const float *x_scale; /* [B] for CQ_X_I8, else NULL */
+    const float *x_scale; /* [B] for CQ_X_I8, else ignored (may be NULL) */
     float *y;             /* [B][out] */
     const float *codebook;/* host pointer */
     int out, in, group, bits, x_dtype, B;

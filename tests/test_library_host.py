@@ -113,6 +113,13 @@ def test_device_entry_points_reject_bad_arguments_before_launch(C):
     assert b"descriptor 0" in lib.cq_last_error()
     d.B, d.x_dtype = 1, _capi.CQ_X_I8
     assert lib.cq_gemv_grouped(ctypes.byref(d), 1, None) == _capi.CQ_ERR_ARG  # no scales
+    d.x_dtype = 3
+    assert lib.cq_gemv_grouped(ctypes.byref(d), 1, None) == _capi.CQ_ERR_ARG  # unknown activation type
+    assert b"x_dtype" in lib.cq_last_error()
+    d.x_dtype, d.blob = _capi.CQ_X_F32Q, 8  # quantised in the call: no scales needed; a misaligned blob
+    assert lib.cq_gemv_grouped(ctypes.byref(d), 1, None) == _capi.CQ_ERR_ARG  # is the next check to fail
+    assert b"16-byte aligned" in lib.cq_last_error()
+    d.blob = 1
     assert lib.cq_gemv_grouped(ctypes.byref(d), 0, None) == _capi.CQ_ERR_ARG
     g = _capi.GemmDesc(blob=1, Xq=1, x_scale=None, Y=1, codebook=cb, out=4, in_=128, group=128,
                        bits=2, M=8)
