@@ -33,6 +33,12 @@
 // land, builds the level table and rotates the activation. Its warps split
 // the row tiles and, when a CTA has fewer tiles than warps, the groups of the
 // input (partial sums meet in shared memory).
+//
+// Activations arrive as fp32, as int8 with per-token scales, or as fp32 to
+// be quantised per token inside the call (CQ_X_F32Q): the kernel's QUANT
+// instance scans the token's absmax first and quantises each value as it
+// loads it, with the activation quantiser's rule, so a decode step needs no
+// separate quantiser launch.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 

@@ -1,31 +1,33 @@
-// cq_gemv_wide.cu -- tensor-core GEMV over CQ-packed weights at group 128
-// for wide inputs (16 groups and more) and for batches of 5 to 16.
+// cq_gemv_wide.cu -- tensor-core GEMV over CQ-packed weights for wide
+// inputs (16 groups and more at group 128, groups of 64 in whole 128-spans)
+// and for batches of 5 to 16.
 //
 // Per group g of 128 inputs the product is the rotated-domain identity
 // (OpenNeedle docs/reference.md; "The .cact archive and Cactus Quants",
 // "Reconstructing one group"):
 //     y[b][o] = sum_g n[o][g] * sum_k c[q[o,g,k]] * z[b,g,k],   z = H x (per group).
 //
-// Two launches per call.
-//  1. act_frag_kernel rotates every distinct activation of the call once:
-//     one warp per (activation, group, batch row) computes z = H0 x with the
-//     FWHT in registers and writes its fp16 terms straight into the MMA B
-//     fragment layout in a workspace (a lane's four positions are exactly
-//     two fragment words, so no shuffles are needed), with 1/sigma per
-//     (batch row, group).
-//  2. the products, launched as programmatic dependents of the first:
-//     gemv_split_kernel (further below) for batches of 1 to 4 with 1-, 2-
-//     and 4-bit codes, gemv_wide_kernel for the rest. In gemv_wide_kernel one
-//     block per SM walks an equal run of the call's 16-row tiles.
-//     Before it waits for the rotation it builds its level table and starts
-//     its code copies; then it copies the fragments of its matrix's
-//     activation into shared memory once, and streams the tiles through four
-//     shared-memory stages in slices of about 512 code bytes per row. The
-//     eight warps split a slice's groups: each expands its groups' code bytes
-//     to fp16 levels through the replicated byte -> levels table (the A
-//     operand of mma.sync m16n8k16, fp32 accumulation) and multiplies them
-//     with the fragments of every batch row; a tile's partial sums meet in
-//     shared memory.
+// Two kinds of products:
+//  - gemv_split_kernel (further below), batches of 1 to 4 with 1-, 2- and
+//    4-bit codes at group 128 or 64: one launch per call. Each block
+//    rotates the activation groups of its (matrix, k-slice) pairs itself
+//    (one warp per group and batch row, the FWHT in registers, fp16 terms
+//    written straight into the MMA B-fragment layout in shared memory) and
+//    its warps stream (matrix, k-slice, 16-row tile) units through private
+//    TMA pipelines.
+//  - gemv_wide_kernel, the rest (batches of 5 to 16, 3-bit codes): behind a
+//    rotation launch, act_frag_kernel, which rotates every distinct
+//    activation of the call once into a workspace in the same fragment
+//    layout, with 1/sigma per (batch row, group). One block per SM walks an
+//    equal run of the call's 16-row tiles. Before it waits for the rotation
+//    it builds its level table and starts its code copies; then it copies
+//    the fragments of its matrix's activation into shared memory once, and
+//    streams the tiles through shared-memory stages in slices of about 512
+//    code bytes per row. The warps split a slice's groups: each expands its
+//    groups' code bytes to fp16 levels through the replicated byte -> levels
+//    table (the A operand of mma.sync m16n8k16, fp32 accumulation) and
+//    multiplies them with the fragments of every batch row; a tile's partial
+//    sums meet in shared memory.
 //
 // Precision. Batches of 1 to 4 carry z as fp16 hi + lo terms (two MMA
 // columns per batch row, z to ~2^-22 relative). Batches of 5 to 16 carry z as
