@@ -57,12 +57,13 @@ WORKLOAD = ("Needle-shaped decode step, batch 1: 27 x {Q 512x512, K 256x512, V 2
 # hash of the sources it was built from: once a source changes the entry no
 # longer matches and traffic reads null.
 NCU_TRAFFIC = {
-    "gemv_fast": ("066ddb5104d761ba", 9777920),
-    "gemm_x8": ("eafec9c3c7051437", 527629824),
-    "encode_cq2": ("9b9931b39a97b3a4", 282200320),
-    "gather_cq4": ("418b3cc16e02bd42", 74119680),
-    "kv_attend": ("fcabe59d60877ca7", 148691456),
-    "gemv_split": ("c4de1e7786b5230c", 289867264),
+    "gemv_fast": ("59756e27d4314701", 9777664),
+    "gemm_x8": ("36923f44dd95004a", 527435776),
+    "encode_cq2": ("212df32af66eea0a", 282170624),
+    "gather_cq4": ("2f0463b08520137e", 74082304),
+    "kv_attend": ("49623d5f08a98bb6", 148752896),
+    "gemv_split": ("b57afce6f235c235", 289797888),
+    "gemv_split_g64": ("b57afce6f235c235", 306636800),
 }
 KERNEL_SOURCES = {
     "gemv_fast": ("cq_gemv_fast.cu", "cq_internal.h"),
@@ -71,6 +72,7 @@ KERNEL_SOURCES = {
     "gather_cq4": ("cq_gather.cu", "cq_internal.h"),
     "kv_attend": ("cq_kv.cu", "cq_internal.h"),
     "gemv_split": ("cq_gemv_wide.cu", "cq_internal.h"),
+    "gemv_split_g64": ("cq_gemv_wide.cu", "cq_internal.h"),
 }
 
 
@@ -1016,7 +1018,8 @@ def bench_g64(cx):
                      "steps": 10 * reps, "packed_bytes_per_step": 64 * nb,
                      "l2": f"one set of 64 matrices ({64 * nb / 1e6:.0f} MB > L2)",
                      "roofline": hbm_roofline(gbs, cx.peaks, cx.peak_kind,
-                                              ncu_traffic("gemv_split") if name == "cq2_group128" else None,
+                                              ncu_traffic("gemv_split") if name == "cq2_group128" else
+                                              ncu_traffic("gemv_split_g64") if name == "cq2_group64" else None,
                                               kernel=gemv_kernel_name(out, n_in, bits, 1, group),
                                               algorithmic_bytes_per_launch=algo)}
         del items, plan, g
