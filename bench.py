@@ -623,13 +623,11 @@ def gemv_kernel_name(out, n_in, bits, B, group=128):
     w = 2 if bits == 5 else bits
     if group == 64 and B <= 4 and n_in % 128 == 0 and w != 3 and ng128 <= 128:
         return "gemv_split_kernel"
-    if B <= 4 and 16 <= ng128 <= 32 and group == 128 and w == 3:
-        return "gemv_stream_kernel"
     if B <= 4 and group == 128 and w != 3 and ng < 16:
         return "gemv_fast_kernel"
     cols = 2 * B if B <= 4 else 8 * ((B + 7) // 8)
     if group == 128 and ng <= 128 and ng * cols * 256 + B * ng * 4 <= 136 * 1024:
-        if B <= 4 and w != 3:
+        if B <= 4:
             return "gemv_split_kernel"
         return "act_frag_kernel + gemv_wide_kernel"
     return "gemv_kernel (fp32)"

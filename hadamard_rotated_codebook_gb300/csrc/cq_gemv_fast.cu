@@ -781,11 +781,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
 
 bool gemv_stream_eligible(const cq_gemv_desc &d) {
     const int ng = in_padded(d.in) / kGroup, W = width_of(d.bits);
-    // 3-bit codes at group 128 (1-, 2- and 4-bit codes this wide take the
-    // split products of cq_gemv_wide.cu), and groups of 64 in whole 128-spans
-    // (those take the split products first: this kernel gets the ones no
-    // split launch could take)
-    const bool grp = (d.group == kGroup64 && d.in % kGroup == 0 && W != 3) || (d.group == kGroup && W == 3);
+    // groups of 64 in whole 128-spans; they take the split products of
+    // cq_gemv_wide.cu first, and this kernel gets the ones no split launch
+    // could take (every group-128 shape this wide takes the split products)
+    const bool grp = d.group == kGroup64 && d.in % kGroup == 0 && W != 3;
     return grp && d.out > 0 && (W >= 1 && W <= 4) && d.B <= kMaxFastB && ng >= 16 && ng <= kMaxFastNg;
 }
 

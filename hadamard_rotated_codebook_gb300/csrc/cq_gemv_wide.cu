@@ -8,14 +8,15 @@
 //     y[b][o] = sum_g n[o][g] * sum_k c[q[o,g,k]] * z[b,g,k],   z = H x (per group).
 //
 // Two kinds of products:
-//  - gemv_split_kernel (further below), batches of 1 to 4 with 1-, 2- and
-//    4-bit codes at group 128 or 64: one launch per call. Each block
+//  - gemv_split_kernel (further below), batches of 1 to 4 with 1- to 4-bit
+//    codes at group 128 and 1-, 2- and 4-bit codes at group 64: one launch
+//    per call. Each block
 //    rotates the activation groups of its (matrix, k-slice) pairs itself
 //    (one warp per group and batch row, the FWHT in registers, fp16 terms
 //    written straight into the MMA B-fragment layout in shared memory) and
 //    its warps stream (matrix, k-slice, 16-row tile) units through private
 //    TMA pipelines.
-//  - gemv_wide_kernel, the rest (batches of 5 to 16, 3-bit codes): behind a
+//  - gemv_wide_kernel, the rest (batches of 5 to 16): behind a
 //    rotation launch, act_frag_kernel, which rotates every distinct
 //    activation of the call once into a workspace in the same fragment
 //    layout, with 1/sigma per (batch row, group). One block per SM walks an
@@ -523,11 +524,10 @@ __global__ void __launch_bounds__(kWGThreads, 1) gemv_wide_kernel(const __grid_c
 
 
 // ----------------------------------------------------- split products --
-// gemv_split_kernel: the product step behind the same rotation launch, with
-// the work cut finer than a block's run of tiles and every warp on its own
-// pipeline. It takes batches of 1 to 4 with 1-, 2- and 4-bit codes, at
-// groups of 128 and of 64 (3-bit codes, two groups per 96-byte chunk, and
-// larger batches run faster on the sliced kernel above). A
+// gemv_split_kernel: the products with the work cut finer than a block's
+// run of tiles and every warp on its own pipeline. It takes batches of 1 to
+// 4 with 1-, 2-, 3- and 4-bit codes at group 128, and 1-, 2- and 4-bit codes
+// at group 64 (larger batches run faster on the sliced kernel above). A
 // unit is (matrix, k-slice of its groups, 16-row tile); units are numbered
 // matrix by matrix, k-slice by k-slice, tile fastest, and each block takes an
 // equal contiguous range of them, split evenly over its 16 warps. A matrix
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kWGThreads, 1) gemv_wide_kernel(const __grid_c
 //
 // Every warp streams its own units through shared-memory stages of one
 // chunk each: two stages of 16 rows x 256 code bytes (eight CQ2 128-spans,
-// four CQ4 spans, sixteen binary spans). One lane per row issues a 1-D TMA bulk copy of the row's chunk (completion
+// four CQ4 spans, sixteen binary spans) or x 192 (four CQ3 spans). One lane per row issues a 1-D TMA bulk copy of the row's chunk (completion
 // on the stage's mbarrier) and a cp.async of its norms. No block barrier runs inside the loop. A block
 // rotates the activation groups of the (matrix, k-slice) pairs of its range
 // into shared memory once, after the launch before it is complete (one
@@ -582,13 +582,15 @@ static_assert(sizeof(SParams) <= 32000, "kernel parameter block");
 
 // Code bytes per group and groups per chunk of each kind.
 __host__ __device__ constexpr int s_gbytes(int kind) { return kind == 0 ? 32 : kind == 1 ? 64 : kind == 2 ? 16 : 48; }
-__host__ __device__ constexpr int s_gc(int kind) { return kind == 0 ? 8 : kind == 1 ? 4 : kind == 2 ? 16 : 2; }
+__host__ __device__ constexpr int s_gc(int kind) { return kind == 0 ? 8 : kind == 1 ? 4 : kind == 2 ? 16 : 4; }
 // Row stride of a stage: the chunk plus padding that spreads a warp's reads
-// of its rows over the banks (as for the sliced kernel's stages). Groups of
-// 64 read 4-byte words (2-bit codes) or 8-byte words (4-bit) of each half,
+// of its rows over the banks (as for the sliced kernel's stages). 3-bit
+// codes: each lane reads three words at 12t, rows 240 bytes (28 banks) apart,
+// so a warp's 32 reads of one word index fall in 32 distinct banks. Groups
+// of 64 read 4-byte words (2-bit codes) or 8-byte words (4-bit) of each half,
 // rows 4 and 8 banks apart; 1-bit codes 2-byte halves, rows 4 banks apart.
 __host__ __device__ constexpr int s_rs(int kind, bool g64 = false) {
-    return g64 ? (kind == 1 ? 288 : 272) : kind == 0 ? 288 : kind == 1 ? 320 : kind == 2 ? 272 : 176;
+    return g64 ? (kind == 1 ? 288 : 272) : kind == 0 ? 288 : kind == 1 ? 320 : kind == 2 ? 272 : 240;
 }
 // Bytes of norms per row of a stage (a multiple of 16): one fp16 norm per
 // group, two per 128-span for groups of 64.
@@ -1382,10 +1384,9 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream,
                 taken[jj] = true;
                 sel[cnt++] = jj;
             }
-            // the split products serve batches of up to 4 with 1-, 2- and 4-bit
-            // codes; 3-bit codes (two groups per chunk) and larger batches run
+            // the split products serve batches of up to 4; larger batches run
             // faster on the sliced kernel
-            if (cls != 0 || kind == 3) {  // never groups of 64 (see gemv_wide_eligible)
+            if (cls != 0) {  // never groups of 64 (see gemv_wide_eligible)
                 for (int j = 0; j < cnt; ++j) sliced[sel[j]] = true;
                 continue;
             }
@@ -1468,7 +1469,8 @@ int launch_gemv_wide(const cq_gemv_desc *d, const int *idx, int n, void *stream,
         switch (meta[k].kind) {
         case 0: rc = g64 ? s_launch<0, true>(P, grid, smem, st) : s_launch<0, false>(P, grid, smem, st); break;
         case 1: rc = g64 ? s_launch<1, true>(P, grid, smem, st) : s_launch<1, false>(P, grid, smem, st); break;
-        default: rc = g64 ? s_launch<2, true>(P, grid, smem, st) : s_launch<2, false>(P, grid, smem, st); break;
+        case 2: rc = g64 ? s_launch<2, true>(P, grid, smem, st) : s_launch<2, false>(P, grid, smem, st); break;
+        default: rc = s_launch<3, false>(P, grid, smem, st); break;  // 3-bit codes: group 128 only
         }
         if (rc) return rc;
     }

@@ -60,14 +60,16 @@ int launch_gemv_grouped(const cq_gemv_desc *d, int n, void *stream);
 // takes, and one launch over the descriptors d[idx[0..n)].
 bool gemv_fast_eligible(const cq_gemv_desc &d);
 int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream);
-// Streamed tensor-core GEMV for inputs of 16..32 groups (one block per SM,
-// one activation rotation per block and matrix): which descriptors, and the
+// Streamed tensor-core GEMV for inputs of 16..32 spans at group 64 (one
+// block per SM, one activation rotation per block and matrix): the fallback
+// for groups of 64 that no split launch takes. Which descriptors, and the
 // launches over d[idx[0..n)].
 bool gemv_stream_eligible(const cq_gemv_desc &d);
 int launch_gemv_stream(const cq_gemv_desc *d, const int *idx, int n, void *stream);
 // Tensor-core GEMV for the other shapes (cq_gemv_wide.cu): wide inputs,
 // 3-bit codes and batches up to 16 at group 128, and groups of 64 in whole
-// 128-spans at batches up to 4. A rotation launch into a workspace, then the
+// 128-spans at batches up to 4 (split products for batches up to 4, sliced
+// products for 5 to 16). A rotation launch into a workspace, then the
 // products; which descriptors, and the launches. Groups of 64 that no split
 // launch can take are returned in rejected[0..*n_rejected) (descriptor
 // indices; room for n) for the streamed or the fp32 kernel.

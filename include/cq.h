@@ -148,20 +148,20 @@ int cq_act_quant_int8(const float *X, int M, int in, int8_t *Xq, float *s,
  * rotated once per group (in-register fast Walsh-Hadamard transform) and the
  * weights are never expanded to a dense matrix ([CF] "How the kernel reads
  * it"). Every shape at group 128 runs on the tensor cores (mma.sync, fp32
- * accumulation) with the codebook levels rounded to fp16: B <= 4 with 1-, 2-
- * and 4-bit codes and in < 2048 in one launch whose blocks rotate their own
- * activation; 3-bit codes at B <= 4 with 2048 <= in <= 4096 through one
- * persistent block per SM that streams the code rows; the other group-128
- * shapes (inputs of 2048 up to 128 groups, batches 5 to 16), and groups of
- * 64 whose input is a multiple of 128 (up to 16384) at B <= 4 with 1-, 2-
- * and 4-bit codes: for B <= 4 with 1-, 2- and 4-bit codes one launch of
- * per-warp pipelines over (matrix, k-slice, 16-row tile) units whose blocks
- * rotate the activation groups they need, the k-slices of a tile summed in
- * slice order (the results do not depend on scheduling); otherwise a
- * rotation launch, which writes each distinct activation's MMA fragments
- * once, and block-wide slices. Both use library-owned device buffers
- * (grown on demand: make one untimed call before capturing a CUDA graph). Groups of 64 that no
- * per-warp plan fits take the streaming kernel. z enters as fp16 hi + lo
+ * accumulation) with the codebook levels rounded to fp16:
+ *  - B <= 4 with 1-, 2- and 4-bit codes and in < 2048: one launch whose
+ *    blocks rotate their own activation (the decode step);
+ *  - the other B <= 4 shapes (3-bit codes, inputs of 2048 up to 128
+ *    groups), and groups of 64 whose input is a multiple of 128 (up to 16384)
+ *    with 1-, 2- and 4-bit codes: one launch of per-warp pipelines over
+ *    (matrix, k-slice, 16-row tile) units whose blocks rotate the activation
+ *    groups they need, the k-slices of a tile summed in slice order (the
+ *    results do not depend on scheduling); groups of 64 that no such plan
+ *    fits take a streaming kernel;
+ *  - batches of 5 to 16: a rotation launch, which writes each distinct
+ *    activation's MMA fragments once, and block-wide slices.
+ * The last two use library-owned device buffers (grown on demand: make one
+ * untimed call before capturing a CUDA graph). z enters as fp16 hi + lo
  * terms for B <= 4 and as one fp16 term for B >= 5. The remaining shapes
  * (the rest of group 64, batches of 5 to 16 with too many groups for the
  * workspace's shared-memory stage) use fp32 arithmetic.

@@ -1,5 +1,5 @@
 """GPU parity of the split GEMV products (inputs of 16 groups and more at
-group 128, batches of 1 to 4, 1-, 2- and 4-bit codes and ternary): units of
+group 128, batches of 1 to 4, 1-, 2-, 3- and 4-bit codes and ternary): units of
 (matrix, k-slice, 16-row tile), k-slices of a tile summed in slice order by
 the last one to finish. Checked against the oracle's dense product on the
 same seeded inputs; repeated calls must give the same bits."""
@@ -30,9 +30,9 @@ def _rows(out):
     return np.array(sorted({min(max(v, 0), out - 1) for v in r}))
 
 
-@pytest.mark.parametrize("bits", [1, 2, 4, 5])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("B", [1, 2, 4])
-@pytest.mark.parametrize("shape", [(4096, 4096), (4100, 3000), (129, 16384), (40, 2048)])
+@pytest.mark.parametrize("shape", [(4096, 4096), (4100, 3000), (129, 16384), (40, 2048), (33, 640)])
 def test_split_single_matrices(C, bits, B, shape):
     """One matrix per call: 4096 rows (k-sliced in four), a ragged last tile
     and an input that is not a multiple of 128, a 16384-wide input over nine
@@ -96,10 +96,9 @@ def test_split_repeat_calls_bit_identical(C):
 
 
 def test_split_grouped_with_every_other_route(C):
-    """One grouped call whose matrices go to the split products (CQ2, CQ4,
-    binary at batch <= 4 on wide inputs), the streamed kernel (CQ3 and group
-    64), the sliced products (batch 8) and the per-matrix kernel (short
-    inputs): every output against the oracle."""
+    """One grouped call whose matrices go to the split products (CQ2, CQ3,
+    CQ4, binary at batch <= 4, group 64), the sliced products (batch 8) and
+    the decode kernel (short inputs): every output against the oracle."""
     specs = [(300, 4096, 2, 128, 1), (200, 2048, 4, 128, 2), (64, 3000, 1, 128, 1), (150, 2048, 3, 128, 1),
              (96, 2048, 2, 64, 1), (130, 2048, 2, 128, 8), (256, 512, 2, 128, 1), (333, 4096, 5, 128, 4)]
     items, refs = [], []
