@@ -992,6 +992,34 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
         for (int ii = 0; ii < n && same; ++ii) same = std::memcmp(&d[idx[ii]], &m.d[ii], sizeof(cq_gemv_desc)) == 0;
         if (same) return fast_launch(m.p, m.smem, st);
     }
+    // rows per CTA: about 48 KB of codes (96 KB for inputs of 16 groups or
+    // more, whose rotation each CTA repeats), a power-of-two number of
+    // 16-row tiles, halved `shrink` times
+    auto tiles_per_cta = [&](const cq_gemv_desc &D, int shrink) {
+        const int ip = in_padded(D.in), W = width_of(D.bits), ng = ip / kGroup;
+        const int kind = W == 2 ? 0 : W == 4 ? 1 : W == 3 ? 3 : 2;
+        const int rowB = ng * (kind == 0 ? 32 : kind == 1 ? 64 : kind == 3 ? 48 : 16) + 2 * ng;
+        const int budget = (ng >= 16 ? 96 : 48) * 1024;
+        const int tiles = std::max(1, budget / (rowB * 16));
+        int tp = 1;
+        while (tp * 2 <= tiles && tp * 2 <= 32) tp *= 2;
+        const int need_tiles = (D.out + 15) / 16;
+        while (tp > 1 && tp / 2 >= need_tiles) tp /= 2;
+        return std::max(1, tp >> shrink);
+    };
+    // a call too small to give every SM a CTA (a single matrix) takes fewer
+    // rows per CTA, so that its products spread over more SMs
+    int shrink = 0;
+    for (;; ++shrink) {
+        long long items = 0;
+        bool more = false;
+        for (int ii = 0; ii < n; ++ii) {
+            const int tp = tiles_per_cta(d[idx[ii]], shrink);
+            items += (d[idx[ii]].out + 16 * tp - 1) / (16 * tp);
+            more |= tp > 1;
+        }
+        if (items >= sm_count() || !more || shrink == 5) break;
+    }
     p.n_items = 0;
     int nlut = 0, nm = 0, launches = 0;
     Need need;
@@ -1000,15 +1028,7 @@ int launch_gemv_fast(const cq_gemv_desc *d, const int *idx, int n, void *stream)
         const cq_gemv_desc &D = d[idx[ii]];
         const int ip = in_padded(D.in), W = width_of(D.bits), ng = ip / kGroup;
         const int kind = W == 2 ? 0 : W == 4 ? 1 : W == 3 ? 3 : 2;
-        // rows per CTA: about 48 KB of codes (96 KB for inputs of 16 groups or
-        // more, whose rotation each CTA repeats), a power-of-two number of 16-row tiles
-        const int rowB = ng * (kind == 0 ? 32 : kind == 1 ? 64 : kind == 3 ? 48 : 16) + 2 * ng;
-        const int budget = (ng >= 16 ? 96 : 48) * 1024;
-        const int tiles = std::max(1, budget / (rowB * 16));
-        int tp = 1;
-        while (tp * 2 <= tiles && tp * 2 <= 32) tp *= 2;
-        const int need_tiles = (D.out + 15) / 16;
-        while (tp > 1 && tp / 2 >= need_tiles) tp /= 2;
+        const int tp = tiles_per_cta(D, shrink);
         const int items = (D.out + 16 * tp - 1) / (16 * tp);
         if (items > kMaxFastItems) return set_error(CQ_ERR_SHAPE, "matrix too tall for one fast GEMV launch");
         if (nm == kMaxFastMats || p.n_items + items > kMaxFastItems) {
