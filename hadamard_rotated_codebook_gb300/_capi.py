@@ -97,6 +97,7 @@ SIGNATURES = {
     "cq_kv_attend": (c_int, [P(KvGeom), P(KvSeq), c_int, c_void_p]),
     "cq_device_status": (c_int, [c_void_p]),
     "cq_selftest_wait_timeout": (c_int, [c_void_p]),
+    "cq_selftest_dirty_counters": (c_int, [c_void_p]),
     "cq_cact_write": (c_int, [c_char_p, P(TensorDesc), c_int, P(c_float), c_uint32]),
     "cq_cact_open": (c_int, [c_char_p, P(c_void_p)]),
     "cq_cact_open_memory": (c_int, [c_void_p, c_uint64, P(c_void_p)]),

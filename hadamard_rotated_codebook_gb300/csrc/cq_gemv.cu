@@ -382,3 +382,16 @@ int launch_gemv_grouped(const cq_gemv_desc *d_in, int n, void *stream) {
 }
 
 }  // namespace cq
+
+// Diagnostic (include/cq.h): the split products' tile counters of `stream`
+// set to a nonzero pattern.
+extern "C" int cq_selftest_dirty_counters(void *stream) {
+    using namespace cq;
+    clear_error();
+    int err = CQ_OK;
+    unsigned int *c = stream_counters(stream, 1024, &err);
+    if (!c) return err;
+    if (cudaMemsetAsync(c, 0x01, 1024 * sizeof(unsigned int), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return set_error(CQ_ERR_CUDA, "counter fill: %s", cudaGetErrorString(cudaGetLastError()));
+    return CQ_OK;
+}

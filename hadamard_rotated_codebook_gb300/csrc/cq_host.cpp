@@ -366,6 +366,7 @@ int cq_device_status(void *stream) {
     return read_and_clear_device_status(stream);
 }
 
+
 // --------------------------------------------------------------- container --
 
 struct cq_cact {

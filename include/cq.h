@@ -391,6 +391,14 @@ int cq_device_status(void *stream);
  * usable. Errors: CQ_ERR_CUDA if the launch fails. */
 int cq_selftest_wait_timeout(void *stream);
 
+/* Diagnostic without a counterpart on the pages: sets the split GEMV's tile
+ * counters of `stream` (allocated if needed; at least 1024 of them) to a
+ * nonzero pattern, as a launch whose waits gave up midway could leave them.
+ * While they are dirty, k-sliced products of that stream do not write their
+ * sums; the cq_device_status call that reports a give-up zeroes the counters
+ * again. Errors: CQ_ERR_NOMEM, CQ_ERR_CUDA. */
+int cq_selftest_dirty_counters(void *stream);
+
 /* -------------------------------------------------------- container -- */
 /*
  * Own .cact-shaped container (the pages disagree on the header: 196 bytes

@@ -35,3 +35,30 @@ def test_bounded_wait_gives_up_and_host_sees_timeout():
     What = O.dequant(blob, out, n_in, bits, cb)
     ref, bound = O.matmul(What, q.astype(np.float64) * s.astype(np.float64)[:, None])
     assert np.all(np.abs(Y.cpu().numpy() - ref) <= 2e-3 * bound)
+
+
+def test_status_read_after_give_up_zeroes_split_counters():
+    """The split GEMV's per-tile counters are left zero by every launch and
+    zeroed when allocated; a launch that gave up midway could leave some
+    set. With them set (a diagnostic fills them), the k-sliced sums of a
+    4096 x 4096 matrix are not written; the status read that reports a
+    give-up zeroes them, and the next call has the bits of a clean one."""
+    import hadamard_rotated_codebook_gb300 as C
+    from hadamard_rotated_codebook_gb300 import _capi
+    lib = _capi.load()
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.cq_device_status(st) == _capi.CQ_OK
+    out = n_in = 4096  # 256 row tiles, too few for the SMs' warps: k-sliced
+    blob = torch.from_numpy(S.random_blob(out * n_in * 2 // 8, out * n_in // 128, 73)).cuda()
+    cb = O.analytic_codebook(2)
+    x = S.normal((1, n_in), 74).cuda()
+    y0 = C.cq_gemv(blob, out, n_in, 2, cb, x).clone()
+    assert lib.cq_selftest_dirty_counters(st) == _capi.CQ_OK
+    y_bad = C.cq_gemv(blob, out, n_in, 2, cb, x, y=torch.zeros_like(y0))
+    torch.cuda.synchronize()
+    assert not torch.equal(y_bad, y0)  # no k-slice saw itself last
+    assert lib.cq_selftest_wait_timeout(st) == _capi.CQ_OK
+    assert lib.cq_device_status(st) == _capi.CQ_ERR_TIMEOUT  # ... and the counters are zero again
+    y1 = C.cq_gemv(blob, out, n_in, 2, cb, x, y=torch.zeros_like(y0))
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y0)
